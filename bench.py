@@ -1,0 +1,559 @@
+#!/usr/bin/env python3
+"""Benchmark of the implicit-GEMM convolution path on GB300.
+
+One step = one pass of the workload's hot path over one batch of synthetic
+input.  The default workload is the ResNet-style bf16 block: the 3x3 stride-1
+conv 32x56x56x64 -> 64 with fused residual (beta = 1) followed by the 3x3
+stride-2 downsample 32x56x56x64 -> 32x28x28x128.  Filters are packed once
+before timing (the pack is timed separately and reported as pack_us).
+
+Timing: W warm-up steps, then K steps, each preceded by an L2 flush (a write
+of max(2 x L2, 256 MiB), outside the events); every launch is bracketed by
+CUDA events on the stream it runs on; the barrier + synchronize bracket the
+region; the step time is the max over ranks.  One JSON line on rank 0.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                  [--workload resnet_block|<one of synthetic.WORKLOADS>]
+
+--impl reference times the CPU oracle (single-threaded fp64 direct loops) on
+a bounded sample of the same workload per step, on the host cores.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "conv TFLOP/s per dtype/shape and % of GB300 dense tensor peak (GB/s if mem-bound)"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+KERNEL_SOURCES = ["transposed_conv_implicit_gb300/csrc/conv_kernel.cuh",
+                  "transposed_conv_implicit_gb300/csrc/ptx.cuh",
+                  "transposed_conv_implicit_gb300/csrc/conv_params.h",
+                  "transposed_conv_implicit_gb300/csrc/conv_api.cu",
+                  "transposed_conv_implicit_gb300/csrc/conv_kernels.cu"]
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for rel in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        try:
+            with open(path) as f:
+                data = json.load(f)
+            out = {}
+            for key in ("hbm_gbs", "bf16_tflops", "bf16_tflops_sustained"):
+                v = data.get(key)
+                if isinstance(v, dict):
+                    v = v.get("value")
+                if isinstance(v, (int, float)):
+                    out[key] = float(v)
+            if "hbm_gbs" in out and "bf16_tflops" in out:
+                out.setdefault("bf16_tflops_sustained", out["bf16_tflops"])
+                return out, "measured"
+        except (OSError, ValueError):
+            pass
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def workload_cases(name):
+    from transposed_conv_implicit_gb300 import synthetic
+    if name == "resnet_block":
+        return [synthetic.WORKLOADS[n] for n in synthetic.RESNET_BLOCK]
+    return [synthetic.WORKLOADS[name]]
+
+
+def describe(cases):
+    parts = []
+    for c in cases:
+        kind = "convT" if c.kind == "transposed" else "conv"
+        s = "%s %s %dx%dx%dx%d -> %dx%dx%dx%d %dx%d s%d p%d" % (
+            c.dtype, kind, c.N, c.H, c.W, c.C_in, c.N, c.Ho, c.Wo, c.C_out, c.R, c.S, c.stride, c.pad)
+        if c.has_residual:
+            s += " +%.2g*src" % c.beta
+        if c.epilogue != "none":
+            s += " " + c.epilogue
+        parts.append(s)
+    return "; ".join(parts)
+
+
+# ----------------------------------------------------------------------------- clocks
+class ClockSampler:
+    """nvidia-smi clocks/throttle reasons sampled during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int, period_ms: int = 50):
+        self.gpu_index = gpu_index
+        self.period_ms = period_ms
+        self.proc = None
+        self.lines = []
+        self._reader = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu_index), "--query-gpu=" + self.FIELDS,
+                 "--format=csv,noheader,nounits", "-lms", str(self.period_ms)],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self._reader = threading.Thread(target=self._read, daemon=True)
+        self._reader.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self._reader.join(timeout=5)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax.append(float(f[2]))
+            except ValueError:
+                continue
+            for name, val in zip(names, f[5:9]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ----------------------------------------------------------------------------- CPU oracle timing
+def oracle_sample_seconds(cases, inputs, budget_s, min_s=0.0):
+    """Run the oracle (as it stands) over whole images of each case, image by
+    image, until `budget_s` is spent or the batch is done.  Returns
+    (flops, seconds, images)."""
+    import numpy as np
+    import oracle
+    dec = []
+    for case, inp in zip(cases, inputs):
+        x = oracle.decode(_bits(inp["x"]), case.dtype)
+        w = oracle.decode(_bits(inp["w"]), case.dtype)
+        src = oracle.decode(_bits(inp["src"]), case.out_dtype) if inp["src"] is not None else None
+        dec.append((x, w, src))
+    flops = 0
+    images = 0
+    t0 = time.perf_counter()
+    N = min(c.N for c in cases)
+    for i in range(N):
+        for case, (x, w, src) in zip(cases, dec):
+            _oracle_one(case, x[i:i + 1], w, None if src is None else src[i:i + 1])
+            flops += case.flops // case.N
+        images += 1
+        if time.perf_counter() - t0 >= budget_s:
+            break
+    return flops, time.perf_counter() - t0, images
+
+
+def oracle_points_step(cases, dec, npix, rng):
+    """One reference-arm step: the oracle evaluates `npix` output pixels (all
+    channels) of each case, at seeded random positions."""
+    import numpy as np
+    import oracle
+    flops = 0
+    for case, (x, w, src) in zip(cases, dec):
+        total_pix = case.N * case.Ho * case.Wo
+        pix = rng.integers(0, total_pix, size=npix)
+        pts = (pix[:, None] * case.C_out + np.arange(case.C_out)[None, :]).reshape(-1)
+        _oracle_points(case, x, w, src, pts)
+        flops += 2 * npix * case.C_out * case.R * case.S * case.C_in
+    return flops
+
+
+def _bits(t):
+    from transposed_conv_implicit_gb300 import synthetic
+    return synthetic.raw_bits(t)
+
+
+def _oracle_one(case, x, w, src):
+    import oracle
+    st, pd = (case.stride,) * 2, (case.pad,) * 2
+    if case.kind == "transposed":
+        return oracle.conv_transposed(x, w, out_hw=(case.Ho, case.Wo), stride=st, padding=pd,
+                                      source=src, beta=case.beta, act=case.epilogue)
+    return oracle.conv2d_fwd(x, w, filter_is_fcrs=case.filter_layout == "FCRS", stride=st,
+                             padding=pd, source=src, beta=case.beta, act=case.epilogue)
+
+
+def _oracle_points(case, x, w, src, pts):
+    import oracle
+    st, pd = (case.stride,) * 2, (case.pad,) * 2
+    if case.kind == "transposed":
+        return oracle.conv_transposed_points(x, w, pts, out_hw=(case.Ho, case.Wo), stride=st,
+                                             padding=pd, source=src, beta=case.beta,
+                                             act=case.epilogue)
+    return oracle.conv2d_fwd_points(x, w, pts, filter_is_fcrs=case.filter_layout == "FCRS",
+                                    stride=st, padding=pd, source=src, beta=case.beta,
+                                    act=case.epilogue)
+
+
+# ----------------------------------------------------------------------------- distributed
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        backend = os.environ.get("BENCH_DIST_BACKEND", "nccl")
+        dist.init_process_group(backend=backend)
+    return world, rank, local
+
+
+def dist_max(value: float, world: int, device) -> float:
+    """Max of a host float over all ranks (host-side timing reduction only)."""
+    if world <= 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    dev = device if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([value], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def dist_barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+# ----------------------------------------------------------------------------- reference arm
+def run_reference(args, world, rank):
+    if rank != 0:
+        return 0
+    import numpy as np
+    import oracle
+    from transposed_conv_implicit_gb300 import synthetic
+    cases = workload_cases(args.workload)
+    inputs = [synthetic.make_inputs(c) for c in cases]
+    dec = []
+    for case, inp in zip(cases, inputs):
+        dec.append((oracle.decode(_bits(inp["x"]), case.dtype), oracle.decode(_bits(inp["w"]), case.dtype),
+                    oracle.decode(_bits(inp["src"]), case.out_dtype) if inp["src"] is not None else None))
+    rng = np.random.default_rng(1234)
+    # Size the per-step sample so the whole run stays within about two minutes.
+    t0 = time.perf_counter()
+    oracle_points_step(cases, dec, 8, rng)
+    per_pix = (time.perf_counter() - t0) / 8
+    budget = min(1.0, 120.0 / max(1, args.steps + args.warmup))
+    npix = max(1, int(budget / max(per_pix, 1e-9)))
+    for _ in range(args.warmup):
+        oracle_points_step(cases, dec, npix, rng)
+    flops = 0
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        flops += oracle_points_step(cases, dec, npix, rng)
+    secs = time.perf_counter() - t0
+    value = flops / secs / 1e12
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": secs / args.steps * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": cases[0].dtype,
+        "data": "synthetic",
+        "config": {"workload": args.workload + ": " + describe(cases),
+                   "sample": "%d output pixels x all channels per conv per step" % npix},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": 1, "kind": "oracle",
+                         "sample": "%d seeded output pixels (all channels) of each conv per step, "
+                                   "fp64 single-threaded direct loops" % npix},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line))
+    return 0
+
+
+# ----------------------------------------------------------------------------- our arm
+def run_ours(args, world, rank, local):
+    import torch
+    import transposed_conv_implicit_gb300 as cg
+    from transposed_conv_implicit_gb300 import synthetic
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    cases = workload_cases(args.workload)
+    inputs = [synthetic.make_inputs(c) for c in cases]
+    stream = torch.cuda.current_stream(dev)
+
+    # Device-resident tensors, packed filters, bound launches.
+    calls, outs, packed = [], [], []
+    pack_ev = (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+    dev_inputs = []
+    for case, inp in zip(cases, inputs):
+        x = inp["x"].to(dev)
+        w = inp["w"].to(dev)
+        src = inp["src"].to(dev) if inp["src"] is not None else None
+        dev_inputs.append((x, w, src))
+    pack_ev[0].record(stream)
+    for case, (x, w, src) in zip(cases, dev_inputs):
+        st, pd = (case.stride,) * 2, (case.pad,) * 2
+        if case.kind == "transposed":
+            packed.append(cg.conv_transposed_pack_filter(w, stride=st, padding=pd))
+        else:
+            packed.append(cg.conv2d_pack_filter(w, filter_is_fcrs=case.filter_layout == "FCRS"))
+    pack_ev[1].record(stream)
+    workspace = cg.new_workspace(cg.CONV_STATUS_BYTES, dev)
+    for case, (x, w, src), pk in zip(cases, dev_inputs, packed):
+        out = torch.empty(case.out_shape, dtype=synthetic.TORCH_DTYPES[case.out_dtype], device=dev)
+        outs.append(out)
+        st, pd = (case.stride,) * 2, (case.pad,) * 2
+        kw = dict(r=case.R, s=case.S, stride=st, has_residual=case.has_residual, source=src,
+                  beta=case.beta, epilogue=case.epilogue, workspace=workspace, stream=stream)
+        if case.kind == "transposed":
+            calls.append(cg.bind_conv_transposed_packed(x, pk, out, padding=pd, **kw))
+        else:
+            calls.append(cg.bind_conv2d_fwd_packed(x, pk, out, symmetric_padding=pd, **kw))
+    torch.cuda.synchronize(dev)
+    pack_us = pack_ev[0].elapsed_time(pack_ev[1]) * 1e3
+
+    props = torch.cuda.get_device_properties(dev)
+    l2 = int(getattr(props, "L2_cache_size", 128 << 20))
+    flush = torch.empty(max(2 * l2, 256 << 20), dtype=torch.uint8, device=dev)
+
+    def step(evs=None):
+        for i, call in enumerate(calls):
+            if evs is not None:
+                evs[i].record(stream)
+            call()
+        if evs is not None:
+            evs[len(calls)].record(stream)
+
+    for _ in range(args.warmup):
+        flush.fill_(1)
+        step()
+    torch.cuda.synchronize(dev)
+    status, bits = cg.conv_check_device_status(workspace)
+    if status != 0:
+        raise RuntimeError("device status after warm-up: %s (bits %d)" % (cg.conv_status_string(status), bits))
+
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(calls) + 1)] for _ in range(args.steps)]
+    sampler = ClockSampler(local) if rank == 0 or world > 1 else None
+    if sampler:
+        sampler.start()
+        time.sleep(0.3)
+    dist_barrier(world)
+    torch.cuda.synchronize(dev)
+    wall0 = time.perf_counter()
+    for k in range(args.steps):
+        flush.fill_(1)
+        step(ev[k])
+    torch.cuda.synchronize(dev)
+    wall = time.perf_counter() - wall0
+    dist_barrier(world)
+    clocks = sampler.stop() if sampler else None
+    status, bits = cg.conv_check_device_status(workspace)
+    if status != 0:
+        raise RuntimeError("device status after timing: %s (bits %d)" % (cg.conv_status_string(status), bits))
+
+    per_kernel_ms = [[ev[k][i].elapsed_time(ev[k][i + 1]) for k in range(args.steps)]
+                     for i in range(len(calls))]
+    step_ms = [ev[k][0].elapsed_time(ev[k][len(calls)]) for k in range(args.steps)]
+    total_ms = dist_max(sum(step_ms), world, dev)
+    ms_per_step = total_ms / args.steps
+    flops_step = sum(c.flops for c in cases)
+    value = flops_step * world * args.steps / (total_ms * 1e-3) / 1e12
+
+    # Roofline of the dominant kernel (largest share of the step).
+    mean_k = [statistics.fmean(v) for v in per_kernel_ms]
+    dom = max(range(len(cases)), key=lambda i: mean_k[i])
+    dcase = cases[dom]
+    peaks, peak_src = load_peaks()
+    ridge_flop_per_byte = peaks["bf16_tflops"] * 1e12 / (peaks["hbm_gbs"] * 1e9)
+    dt_mult = 2.0 if dcase.dtype == "f8e4m3" else 1.0
+    if dcase.flops / dcase.bytes < ridge_flop_per_byte * dt_mult:
+        achieved = dcase.bytes / (mean_k[dom] * 1e-3) / 1e9
+        roof = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s"}
+    else:
+        achieved = dcase.flops / (mean_k[dom] * 1e-3) / 1e12
+        roof = {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"] * dt_mult,
+                "unit": "TFLOP/s"}
+    roof["frac"] = roof["achieved"] / roof["peak"]
+    roof["peak_source"] = peak_src
+    roof["kernel"] = dcase.name
+    roof["traffic"] = lookup_traffic(dcase.name)
+
+    per_kernel = {}
+    for i, c in enumerate(cases):
+        us = mean_k[i] * 1e3
+        per_kernel[c.name] = {"us": round(us, 3), "tflops": round(c.flops / (us * 1e-6) / 1e12, 2),
+                              "gbs": round(c.bytes / (us * 1e-6) / 1e9, 1),
+                              "p10_us": round(_pct(per_kernel_ms[i], 10) * 1e3, 3),
+                              "p90_us": round(_pct(per_kernel_ms[i], 90) * 1e3, 3)}
+
+    e2e = run_e2e(args, cases, inputs, dev, stream) if not args.no_e2e else None
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        flops, secs, images = oracle_sample_seconds(cases, inputs, args.cpu_budget)
+        cpu = {"value": flops / secs / 1e12, "unit": "TFLOP/s", "cores": 1, "kind": "oracle",
+               "sample": "first %d of %d images of every conv in the workload, full images, fp64 "
+                         "single-threaded direct loops (%.1f s)" % (images, min(c.N for c in cases), secs)}
+
+    if rank != 0:
+        return 0
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": cases[0].dtype, "data": "synthetic",
+        "config": {"workload": args.workload + ": " + describe(cases),
+                   "l2": "flushed before every step (write of %d MiB), flush outside the events"
+                         % (flush.numel() >> 20),
+                   "filters": "packed once before timing",
+                   "parallelism": "replicas" if world > 1 else "single GPU",
+                   "gpu": props.name, "sms": props.multi_processor_count},
+        "roofline": roof,
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "gpu_launches": len(calls) * args.steps,
+        "clocks": clocks,
+        "pack_us": round(pack_us, 2),
+        "per_kernel": per_kernel,
+        "wall_s": round(wall, 3),
+        "kernel_hash": kernel_source_hash(),
+    }
+    print(json.dumps(line))
+    return 0
+
+
+def _pct(vals, p):
+    s = sorted(vals)
+    return s[min(len(s) - 1, max(0, int(round(p / 100.0 * (len(s) - 1)))))]
+
+
+def lookup_traffic(kernel_name):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on
+    the current kernel sources; else None."""
+    path = os.path.join(ROOT, "profiles", "dram_traffic.json")
+    if not os.path.exists(path):
+        return None
+    try:
+        with open(path) as f:
+            data = json.load(f)
+    except (OSError, ValueError):
+        return None
+    if data.get("kernel_hash") != kernel_source_hash():
+        return None
+    entry = data.get("kernels", {}).get(kernel_name)
+    return entry.get("dram_bytes_per_launch") if entry else None
+
+
+def run_e2e(args, cases, inputs, dev, stream):
+    """End to end through the public API: pinned host input -> device, the
+    convolutions, device -> pinned host output, every step."""
+    import torch
+    import transposed_conv_implicit_gb300 as cg
+    from transposed_conv_implicit_gb300 import synthetic
+    host_in, dev_in, host_out, dev_out, packed = [], [], [], [], []
+    h2d = d2h = 0
+    for case, inp in zip(cases, inputs):
+        hx = inp["x"].pin_memory()
+        hs = inp["src"].pin_memory() if inp["src"] is not None else None
+        host_in.append((hx, hs))
+        dev_in.append((torch.empty_like(hx, device=dev), torch.empty_like(hs, device=dev) if hs is not None else None))
+        h2d += hx.numel() * hx.element_size() + (hs.numel() * hs.element_size() if hs is not None else 0)
+        o = torch.empty(case.out_shape, dtype=synthetic.TORCH_DTYPES[case.out_dtype], device=dev)
+        dev_out.append(o)
+        host_out.append(torch.empty(o.shape, dtype=o.dtype, pin_memory=True))
+        d2h += o.numel() * o.element_size()
+        w = inp["w"].to(dev)
+        st, pd = (case.stride,) * 2, (case.pad,) * 2
+        if case.kind == "transposed":
+            packed.append(cg.conv_transposed_pack_filter(w, stride=st, padding=pd))
+        else:
+            packed.append(cg.conv2d_pack_filter(w, filter_is_fcrs=case.filter_layout == "FCRS"))
+    ws = cg.new_workspace(cg.CONV_STATUS_BYTES, dev)
+
+    def one_step():
+        for case, (hx, hs), (dx, ds), pk, o, ho in zip(cases, host_in, dev_in, packed, dev_out, host_out):
+            dx.copy_(hx, non_blocking=True)
+            if hs is not None:
+                ds.copy_(hs, non_blocking=True)
+            st, pd = (case.stride,) * 2, (case.pad,) * 2
+            kw = dict(r=case.R, s=case.S, stride=st, has_residual=case.has_residual, source=ds,
+                      beta=case.beta, epilogue=case.epilogue, workspace=ws)
+            if case.kind == "transposed":
+                cg.conv_transposed_packed(dx, pk, o, padding=pd, **kw)
+            else:
+                cg.conv2d_fwd_packed(dx, pk, o, symmetric_padding=pd, **kw)
+            ho.copy_(o, non_blocking=True)
+
+    for _ in range(max(1, args.warmup)):
+        one_step()
+    torch.cuda.synchronize(dev)
+    steps = max(1, min(args.steps, 200))
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        one_step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    ms = e0.elapsed_time(e1) / steps
+    status, bits = cg.conv_check_device_status(ws)
+    if status != 0:
+        raise RuntimeError("device status after e2e: %s" % cg.conv_status_string(status))
+    flops = sum(c.flops for c in cases)
+    return {"value": flops / (ms * 1e-3) / 1e12, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "ms_per_step": ms, "steps": steps}
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--workload", default="resnet_block")
+    ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle CPU baseline")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    world, rank, local = dist_setup()
+    try:
+        if args.impl == "reference":
+            return run_reference(args, world, rank)
+        return run_ours(args, world, rank, local)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,181 @@
+"""The C ABI without a GPU: the library builds, loads and exports every symbol
+the headers declare, and host-side validation returns the documented status
+codes before any CUDA call (the pointers here are never dereferenced).
+
+Gates from "dispatch_amd_4wave_conv2d" (Parameters, Args) and the transposed
+conv's shape rule; see include/conv_gb300.h.
+"""
+import ctypes
+import os
+import re
+
+import pytest
+
+import transposed_conv_implicit_gb300 as cg
+from transposed_conv_implicit_gb300 import _lib, build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+OK, INVALID, NOTSUP, MISALIGNED, WS_SMALL = 0, 1, 2, 3, 4
+BF16, F16, F8 = 0, 1, 2
+
+# Fake, 16-byte-aligned device addresses: validation never dereferences them.
+A, B, C, D, WS = (ctypes.c_void_p(0x10000 * k) for k in (1, 2, 3, 4, 5))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return _lib.lib()
+
+
+def _declared_functions():
+    names = []
+    for fn in sorted(os.listdir(os.path.join(ROOT, "include"))):
+        text = open(os.path.join(ROOT, "include", fn)).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        names += re.findall(r"^[A-Za-z_][\w\s\*]*?\b(\w+)\s*\(", text, flags=re.M)
+    return sorted(set(n for n in names if n not in ("defined",)))
+
+
+def test_every_declared_symbol_is_exported(lib):
+    declared = _declared_functions()
+    assert "conv2d_fwd" in declared and "conv_transposed" in declared
+    for name in declared:
+        assert hasattr(lib, name), name
+    assert sorted(_lib.EXPORTS) == declared
+
+
+def test_status_strings(lib):
+    for code, name in [(0, "CONV_OK"), (1, "CONV_ERR_INVALID_VALUE"), (2, "CONV_ERR_NOT_SUPPORTED"),
+                       (3, "CONV_ERR_MISALIGNED"), (4, "CONV_ERR_WORKSPACE_TOO_SMALL"),
+                       (5, "CONV_ERR_CUDA"), (6, "CONV_ERR_DEVICE_TIMEOUT")]:
+        assert lib.conv_status_string(code).decode() == name
+
+
+def test_sizes(lib):
+    assert lib.conv2d_packed_filter_bytes(3, 3, 64, 64, BF16) == 3 * 3 * 64 * 64 * 2
+    assert lib.conv2d_packed_filter_bytes(3, 3, 320, 320, F8) == 3 * 3 * 320 * 320
+    assert lib.conv2d_workspace_size(3, 3, 64, 64, BF16) == 256 + 73728
+    assert lib.conv2d_packed_filter_bytes(0, 3, 64, 64, BF16) == 0
+    # 4x4 filter, stride 2: four phases of 2x2 taps -> K = 4*C_in per phase.
+    assert lib.conv_transposed_packed_filter_bytes(4, 4, 256, 128, _lib.pair((2, 2)),
+                                                   _lib.pair((1, 1)), F16) == 4 * 128 * 1024 * 2
+    # 3x3 filter, stride 2, pad 1: phase taps 1x1,1x2,2x1,2x2 -> K_max = 4*C_in.
+    assert lib.conv_transposed_packed_filter_bytes(3, 3, 64, 32, _lib.pair((2, 2)),
+                                                   _lib.pair((1, 1)), BF16) == 4 * 32 * 256 * 2
+    assert lib.conv_transposed_packed_filter_bytes(3, 3, 64, 32, _lib.pair((1, 1)),
+                                                   _lib.pair((1, 1)), BF16) == 32 * 576 * 2
+
+
+def fwd(lib, *, inp=A, n=2, h=8, w=8, c=64, dt=BF16, flt=B, r=3, s=3, f=64, fcrs=0, out=C,
+        ho=None, wo=None, odt=None, stride=(1, 1), dil=(1, 1), pad=(1, 1), groups=1, res=0,
+        src=None, beta=0.0, epi=0, ws=WS, ws_bytes=1 << 20, packed=False):
+    odt = (BF16 if dt == F8 else dt) if odt is None else odt
+    if ho is None:
+        ho = (h + 2 * pad[0] - r) // stride[0] + 1 if stride[0] > 0 else 1
+    if wo is None:
+        wo = (w + 2 * pad[1] - s) // stride[1] + 1 if stride[1] > 0 else 1
+    src = ctypes.c_void_p(0) if src is None else src
+    tail = (_lib.pair(stride), _lib.pair(dil), _lib.pair(pad), groups, res, src, beta, epi, ws,
+            ws_bytes, None)
+    if packed:
+        return lib.conv2d_fwd_packed(inp, n, h, w, c, dt, flt, r, s, f, out, ho, wo, odt, *tail)
+    return lib.conv2d_fwd(inp, n, h, w, c, dt, flt, r, s, f, fcrs, out, ho, wo, odt, *tail)
+
+
+@pytest.mark.parametrize("kw,want", [
+    (dict(inp=ctypes.c_void_p(0)), INVALID),
+    (dict(out=ctypes.c_void_p(0)), INVALID),
+    (dict(ws=ctypes.c_void_p(0)), INVALID),
+    (dict(res=1), INVALID),                                   # residual without a source
+    (dict(inp=ctypes.c_void_p(0x10008)), MISALIGNED),
+    (dict(res=1, src=ctypes.c_void_p(0x20004)), MISALIGNED),
+    (dict(n=0), INVALID),
+    (dict(c=-64), INVALID),
+    (dict(ho=7), INVALID),                                    # inconsistent output size
+    (dict(epi=3), INVALID),
+    (dict(stride=(3, 3)), NOTSUP),
+    (dict(stride=(1, 2)), NOTSUP),
+    (dict(dil=(2, 2)), NOTSUP),
+    (dict(pad=(1, 2)), NOTSUP),
+    (dict(pad=(3, 3)), NOTSUP),
+    (dict(groups=2), NOTSUP),
+    (dict(dt=F8, odt=F8), NOTSUP),                            # fp8 must write bf16
+    (dict(dt=BF16, odt=F16), NOTSUP),
+    (dict(dt=7), NOTSUP),
+    (dict(c=8), NOTSUP),                                      # 16 B channel rows: no TMA block
+    (dict(c=24), NOTSUP),
+    (dict(r=33, s=33, h=40, w=40), NOTSUP),
+    (dict(ws_bytes=1000), WS_SMALL),                          # cannot hold the packed filter
+    (dict(ws_bytes=100, packed=True), WS_SMALL),
+])
+def test_forward_validation(lib, kw, want):
+    assert fwd(lib, **kw) == want
+
+
+def tr(lib, *, n=2, h=8, w=8, c=64, dt=F16, r=4, s=4, f=32, ho=None, wo=None, stride=(2, 2),
+       dil=(1, 1), pad=(1, 1), res=0, src=None, epi=0, ws_bytes=1 << 22, odt=None):
+    odt = (BF16 if dt == F8 else dt) if odt is None else odt
+    if ho is None:
+        ho = (h - 1) * stride[0] - 2 * pad[0] + r
+    if wo is None:
+        wo = (w - 1) * stride[1] - 2 * pad[1] + s
+    src = ctypes.c_void_p(0) if src is None else src
+    return lib.conv_transposed(A, n, h, w, c, dt, B, r, s, f, C, ho, wo, odt, _lib.pair(stride),
+                               _lib.pair(dil), _lib.pair(pad), res, src, 0.0, epi, WS, ws_bytes,
+                               None)
+
+
+@pytest.mark.parametrize("kw,want", [
+    (dict(ho=13), INVALID),                   # below (h-1)s - 2p + r
+    (dict(ho=18), INVALID),                   # output padding must be < stride
+    (dict(dil=(2, 2)), NOTSUP),
+    (dict(pad=(4, 4)), NOTSUP),               # pad >= r
+    (dict(stride=(2, 1)), NOTSUP),
+    (dict(stride=(3, 3)), NOTSUP),
+    (dict(c=8), NOTSUP),
+    (dict(dt=F8, odt=F16), NOTSUP),
+    (dict(res=1), INVALID),
+    (dict(ws_bytes=512), WS_SMALL),
+])
+def test_transposed_validation(lib, kw, want):
+    assert tr(lib, **kw) == want
+
+
+def test_pack_validation(lib):
+    assert lib.conv2d_pack_filter(B, 3, 3, 64, 64, 0, BF16, D, 100, None) == WS_SMALL
+    assert lib.conv2d_pack_filter(None, 3, 3, 64, 64, 0, BF16, D, 1 << 20, None) == INVALID
+    assert lib.conv2d_pack_filter(ctypes.c_void_p(0x20002), 3, 3, 64, 64, 0, BF16, D, 1 << 20,
+                                  None) == MISALIGNED
+    assert lib.conv_transposed_pack_filter(B, 4, 4, 64, 32, _lib.pair((2, 2)), _lib.pair((1, 1)),
+                                           F16, D, 64, None) == WS_SMALL
+    assert lib.conv_transposed_pack_filter(B, 4, 4, 64, 32, _lib.pair((3, 3)), _lib.pair((1, 1)),
+                                           F16, D, 1 << 20, None) == NOTSUP
+
+
+def _plan(lib, n, h, w, c, dt, r, f, st, pd, sms=148):
+    out = (ctypes.c_int * 7)()
+    assert lib.conv_testing_fwd_plan(n, h, w, c, dt, r, r, f, _lib.pair((st, st)), _lib.pair((pd, pd)),
+                                     sms, out) == OK
+    return dict(zip(("bn", "bk", "stages", "smem", "tiles", "grid", "tmem"), list(out)))
+
+
+def test_tile_plans_for_the_workloads(lib):
+    p = _plan(lib, 32, 56, 56, 64, BF16, 3, 64, 1, 1)            # ResNet 3x3
+    assert (p["bn"], p["bk"], p["tiles"], p["tmem"]) == (64, 64, 784, 128)
+    assert p["smem"] <= 227 * 1024 and p["stages"] >= 4
+    p = _plan(lib, 16, 64, 64, 320, F8, 3, 320, 1, 1)            # fp8: 2 x 160 columns, 64-ch blocks
+    assert (p["bn"], p["bk"], p["tiles"], p["tmem"]) == (160, 64, 1024, 512)
+    p = _plan(lib, 1, 512, 512, 128, BF16, 3, 3, 1, 1)           # C_out = 3: one 16-wide masked tile
+    assert (p["bn"], p["bk"], p["tiles"]) == (16, 64, 2048)
+    p = _plan(lib, 1, 256, 256, 512, BF16, 3, 512, 1, 1)
+    assert (p["bn"], p["tiles"], p["tmem"]) == (256, 1024, 512)
+    p = _plan(lib, 1, 16, 16, 16, BF16, 3, 16, 1, 1)             # 32-byte channel rows
+    assert (p["bn"], p["bk"], p["tiles"], p["grid"]) == (16, 16, 2, 2)
+
+
+def test_binding_raises_without_library(monkeypatch, tmp_path):
+    monkeypatch.setattr(_lib, "_lib", None)
+    monkeypatch.setattr(_lib, "LIB_PATH", str(tmp_path / "missing.so"))
+    with pytest.raises(_lib.ExtensionMissing):
+        cg.conv_status_string(0)

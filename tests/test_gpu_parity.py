@@ -1,0 +1,203 @@
+"""GPU parity: the CUDA path (through the C ABI) against the fp64 CPU oracle.
+
+Small cases are compared on every output element; the full-size workloads,
+run in the launch configuration the benchmark times, are compared on sampled
+outputs that the oracle evaluates one by one.  Integer-valued cases must
+match bit for bit.  The bound is the one in tests/_harness.py.
+"""
+import itertools
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from tests import _harness as H
+from transposed_conv_implicit_gb300 import synthetic
+from transposed_conv_implicit_gb300.synthetic import ConvCase, Dist, WORKLOADS
+
+pytestmark = pytest.mark.gpu
+
+
+def _fwd(name, dt, N, Hh, W, C, F, R, st, pd, *, layout="RSCF", res=False, beta=0.0, epi="none",
+         seed=1, xd=None, wd=None, S=None):
+    S = R if S is None else S
+    return ConvCase(name, "fwd", dt, N, Hh, W, C, F, R, S, st, pd, layout,
+                    xd or Dist("normal", 1.0), wd or Dist("normal", 1.0 / (R * S * C)), seed=seed,
+                    has_residual=res, beta=beta, src_dist=Dist("normal", 1.0) if res else None,
+                    epilogue=epi)
+
+
+def _tr(name, dt, N, Hh, W, C, F, R, st, pd, extra=0, *, res=False, beta=0.0, epi="none", seed=1,
+        xd=None, wd=None):
+    Ho = (Hh - 1) * st - 2 * pd + R + extra
+    Wo = (W - 1) * st - 2 * pd + R + extra
+    return ConvCase(name, "transposed", dt, N, Hh, W, C, F, R, R, st, pd, "RSFC",
+                    xd or Dist("normal", 1.0), wd or Dist("normal", 1.0 / (R * R * C)), seed=seed,
+                    has_residual=res, beta=beta, src_dist=Dist("normal", 1.0) if res else None,
+                    epilogue=epi, out_hw=(Ho, Wo))
+
+
+# Several M tiles with a ragged tail (N*Ho*Wo not a multiple of 128), edge
+# tiles along C_out (1, 3, 17, 272 = 2 x 144 with a ragged second tile), each
+# stride/padding/filter-size gate value, both forward layouts, all dtypes,
+# residual with several betas and every epilogue.
+SMALL_FWD = [
+    _fwd("b_3x3_s1p1", "bf16", 2, 13, 13, 64, 64, 3, 1, 1),
+    _fwd("b_3x3_s2p1", "bf16", 2, 13, 11, 64, 128, 3, 2, 1, layout="FCRS"),
+    _fwd("b_5x5_s2p2", "bf16", 2, 11, 12, 32, 48, 5, 2, 2),
+    _fwd("b_5x5_s1p2_res", "bf16", 1, 12, 14, 32, 32, 5, 1, 2, res=True, beta=-2.0),
+    _fwd("b_3x3_s1p0", "bf16", 2, 12, 9, 48, 24, 3, 1, 0),
+    _fwd("b_3x3_s2p2", "bf16", 1, 15, 15, 64, 80, 3, 2, 2, epi="relu"),
+    _fwd("b_1x1_s1p0", "bf16", 2, 9, 15, 128, 96, 1, 1, 0, layout="FCRS"),
+    _fwd("b_1x1_s2p0", "bf16", 2, 10, 10, 64, 64, 1, 2, 0),
+    _fwd("b_cout1", "bf16", 2, 11, 11, 64, 1, 3, 1, 1),
+    _fwd("b_cout3_head", "bf16", 1, 20, 20, 128, 3, 3, 1, 1),
+    _fwd("b_cout17_res", "bf16", 2, 10, 10, 32, 17, 3, 1, 1, res=True, beta=0.5),
+    _fwd("b_cout272", "bf16", 1, 12, 12, 64, 272, 3, 1, 1, layout="FCRS"),
+    _fwd("b_cout512_silu", "bf16", 1, 12, 12, 64, 512, 3, 1, 1, epi="silu"),
+    _fwd("b_cin16", "bf16", 1, 16, 16, 16, 16, 3, 1, 1),
+    _fwd("b_cin48_64B", "bf16", 2, 9, 9, 48, 32, 3, 2, 1),
+    _fwd("b_res_relu", "bf16", 2, 13, 13, 64, 64, 3, 1, 1, res=True, beta=1.0, epi="relu"),
+    _fwd("b_rect_3x5", "bf16", 1, 13, 17, 64, 64, 3, 1, 1, S=5),
+    _fwd("h_3x3_s1p1", "f16", 2, 13, 13, 64, 64, 3, 1, 1),
+    _fwd("h_5x5_s2p2", "f16", 2, 17, 17, 128, 128, 5, 2, 2),
+    _fwd("h_res_silu", "f16", 1, 14, 14, 64, 40, 3, 1, 1, res=True, beta=0.75, epi="silu"),
+    _fwd("h_cout3", "f16", 1, 15, 15, 32, 3, 3, 2, 1, layout="FCRS"),
+    _fwd("h_cin16", "f16", 2, 9, 9, 16, 32, 3, 1, 1),
+    _fwd("e_3x3_s1p1_res", "f8e4m3", 2, 11, 11, 320, 320, 3, 1, 1, layout="FCRS", res=True,
+         beta=0.5, wd=Dist("normal", 1.0 / math.sqrt(2880))),
+    _fwd("e_3x3_s2p1", "f8e4m3", 2, 13, 13, 64, 64, 3, 2, 1),
+    _fwd("e_1x1", "f8e4m3", 1, 12, 12, 128, 48, 1, 1, 0),
+    _fwd("e_5x5_p2_relu", "f8e4m3", 1, 12, 12, 32, 16, 5, 1, 2, epi="relu"),
+    _fwd("e_cout3", "f8e4m3", 1, 16, 16, 128, 3, 3, 1, 1),
+    _fwd("e_cin32_32B", "f8e4m3", 2, 10, 10, 32, 64, 3, 1, 1, layout="FCRS"),
+    _fwd("b_single_partial_tile", "bf16", 1, 5, 7, 64, 64, 3, 1, 1),
+    _fwd("b_exact_one_tile", "bf16", 2, 8, 8, 64, 64, 3, 1, 1),
+    _fwd("b_tiny_image", "bf16", 3, 2, 3, 32, 16, 3, 2, 2),
+]
+
+SMALL_TR = [
+    _tr("t_h_4x4_s2p1_relu", "f16", 2, 9, 8, 64, 64, 4, 2, 1, epi="relu"),
+    _tr("t_b_3x3_s2p1_op1", "bf16", 2, 7, 7, 64, 32, 3, 2, 1, extra=1),
+    _tr("t_b_3x3_s2p1_op0", "bf16", 1, 9, 9, 32, 48, 3, 2, 1),
+    _tr("t_b_3x3_s1p1", "bf16", 2, 9, 10, 64, 64, 3, 1, 1),
+    _tr("t_h_5x5_s2p2_res", "f16", 1, 8, 8, 128, 40, 5, 2, 2, res=True, beta=0.5),
+    _tr("t_b_2x2_s2p0", "bf16", 2, 8, 8, 64, 16, 2, 2, 0),
+    _tr("t_b_1x1_s2_zero_tap_phase", "bf16", 1, 9, 9, 32, 16, 1, 2, 0, extra=1, epi="relu"),
+    _tr("t_e_4x4_s2p1", "f8e4m3", 2, 8, 8, 64, 64, 4, 2, 1),
+    _tr("t_h_cout3", "f16", 1, 10, 10, 64, 3, 4, 2, 1),
+    _tr("t_h_cout256_silu", "f16", 1, 6, 6, 64, 256, 4, 2, 1, epi="silu"),
+]
+
+
+@pytest.mark.parametrize("case", SMALL_FWD + SMALL_TR, ids=lambda c: c.name)
+def test_small_case_every_element(case):
+    inp = synthetic.make_inputs(case)
+    out = H.run_gpu(case, inp)
+    torch.cuda.synchronize()
+    got = H.decode(out.cpu(), case.out_dtype)
+    ref = H.oracle_full(case, inp)
+    H.assert_parity(case, inp, got, ref)
+
+
+@pytest.mark.parametrize("case", [c for c in SMALL_FWD + SMALL_TR if c.name in (
+    "b_3x3_s2p1", "b_cout17_res", "e_3x3_s1p1_res", "t_h_4x4_s2p1_relu", "t_b_3x3_s2p1_op1")],
+    ids=lambda c: c.name)
+def test_unpacked_entry_point_equals_packed(case):
+    """conv2d_fwd / conv_transposed pack in the workspace; the result must be
+    bit-identical to the prepacked entry points."""
+    inp = synthetic.make_inputs(case)
+    a = H.run_gpu(case, inp, packed=True).cpu()
+    b = H.run_gpu(case, inp, packed=False).cpu()
+    assert torch.equal(a.view(torch.uint8), b.view(torch.uint8))
+
+
+def _int_case(name, kind, dt, N, Hh, W, C, F, R, st, pd, **kw):
+    xd = Dist("int", 2 if dt != "bf16" else 1)
+    wd = Dist("int", 1)
+    if kind == "fwd":
+        return _fwd(name, dt, N, Hh, W, C, F, R, st, pd, xd=xd, wd=wd, **kw)
+    return _tr(name, dt, N, Hh, W, C, F, R, st, pd, xd=xd, wd=wd, **kw)
+
+
+INT_CASES = [
+    _int_case("int_b_3x3", "fwd", "bf16", 2, 13, 13, 16, 16, 3, 1, 1),
+    _int_case("int_b_s2_res", "fwd", "bf16", 2, 11, 11, 16, 24, 3, 2, 1, res=False),
+    _int_case("int_h_5x5", "fwd", "f16", 1, 12, 12, 64, 32, 5, 2, 2, layout="FCRS"),
+    _int_case("int_e_3x3", "fwd", "f8e4m3", 2, 10, 10, 32, 64, 3, 1, 1),
+    _int_case("int_h_tr", "transposed", "f16", 2, 8, 8, 64, 32, 4, 2, 1),
+    _int_case("int_e_tr", "transposed", "f8e4m3", 1, 7, 7, 32, 16, 3, 2, 1, extra=1),
+]
+
+
+@pytest.mark.parametrize("case", INT_CASES, ids=lambda c: c.name)
+def test_integer_inputs_bit_exact(case):
+    """Integer inputs: every product and partial sum is exact in fp32 and the
+    result is exactly representable in the output dtype, so the GPU must equal
+    the oracle exactly."""
+    inp = synthetic.make_inputs(case)
+    ref = H.oracle_full(case, inp)
+    limit = 256 if case.out_dtype == "bf16" else 2048
+    assert np.abs(ref).max() <= limit
+    out = H.run_gpu(case, inp)
+    got = H.decode(out.cpu(), case.out_dtype)
+    mism = np.argwhere(got != ref)
+    assert mism.size == 0, mism[:5].tolist()
+
+
+@pytest.mark.parametrize("name", list(WORKLOADS), ids=str)
+def test_full_size_workload_sampled(name):
+    """Full-size workloads, sampled outputs checked against the oracle point by
+    point; every output must be finite."""
+    case = WORKLOADS[name]
+    inp = synthetic.make_inputs(case)
+    out = H.run_gpu(case, inp).cpu()
+    flat = H.decode(out, case.out_dtype).reshape(-1)
+    assert np.isfinite(flat).all()
+    pts = H.sample_points(case, 3000, seed=11)
+    ref = H.oracle_points(case, inp, pts)
+    H.assert_parity(case, inp, flat[pts], ref, "sampled")
+
+
+def test_tiny_workload_every_element():
+    case = WORKLOADS["tiny_bf16"]
+    inp = synthetic.make_inputs(case)
+    out = H.run_gpu(case, inp).cpu()
+    H.assert_parity(case, inp, H.decode(out, case.out_dtype), H.oracle_full(case, inp))
+
+
+def test_output_canaries_untouched():
+    """Writes stay inside the output: guard bands around it keep their NaN
+    pattern and no NaN is left inside."""
+    case = _fwd("canary", "bf16", 2, 11, 9, 64, 17, 3, 2, 1, res=True, beta=1.0)
+    inp = synthetic.make_inputs(case)
+    n = int(np.prod(case.out_shape))
+    guard = 4096
+    buf = torch.full((n + 2 * guard,), float("nan"), dtype=torch.bfloat16, device="cuda")
+    out = buf[guard:guard + n].view(case.out_shape)
+    H.run_gpu(case, inp, out=out)
+    torch.cuda.synchronize()
+    host = buf.cpu()
+    assert torch.isnan(host[:guard]).all() and torch.isnan(host[guard + n:]).all()
+    assert not torch.isnan(host[guard:guard + n]).any()
+    H.assert_parity(case, inp, H.decode(out.cpu(), "bf16"), H.oracle_full(case, inp))
+
+
+def test_repeated_calls_are_deterministic():
+    case = SMALL_FWD[0]
+    inp = synthetic.make_inputs(case)
+    a = H.run_gpu(case, inp).cpu()
+    b = H.run_gpu(case, inp).cpu()
+    assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+
+
+def test_status_clean_after_runs():
+    import transposed_conv_implicit_gb300 as cg
+    case = SMALL_FWD[0]
+    inp = synthetic.make_inputs(case)
+    ws = cg.new_workspace(cg.CONV_STATUS_BYTES, "cuda")
+    H.run_gpu(case, inp, workspace=ws)
+    status, bits = cg.conv_check_device_status(ws)
+    assert status == 0 and bits == 0

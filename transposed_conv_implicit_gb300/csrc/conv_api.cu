@@ -1,0 +1,873 @@
+// Host side of libconvgb300: argument validation (the acceptance gates), tile
+// planning, TMA tensor-map encoding, the filter-packing kernels and the C ABI
+// declared in include/conv_gb300.h.
+//
+// Gates follow "dispatch_amd_4wave_conv2d" (Parameters and Args): input dtype
+// fp8-e4m3 / bf16 / fp16, filter dtype = input dtype, output bf16 for fp8
+// inputs else the input dtype, stride (1,1) or (2,2), dilation (1,1),
+// symmetric padding (0,0)/(1,1)/(2,2), one group.  A failed gate returns
+// CONV_ERR_NOT_SUPPORTED: there is no fallback path.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <atomic>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "../../include/conv_gb300.h"
+#include "../../include/conv_gb300_testing.h"
+#include "conv_internal.h"
+
+using namespace convgb300;
+
+namespace {
+
+constexpr unsigned long long kDefaultTimeoutNs = 1000000000ull;  // one second per wait
+constexpr int kMaxFilterExtent = 32;
+constexpr size_t kSmemLimit = 227 * 1024;
+
+std::atomic<int> g_fault_mode{0};
+std::atomic<unsigned long long> g_timeout_ns{0};
+
+int elt_bytes(conv_dtype_t d) { return d == CONV_DTYPE_F8E4M3 ? 1 : 2; }
+
+bool known_dtype(conv_dtype_t d) {
+  return d == CONV_DTYPE_BF16 || d == CONV_DTYPE_F16 || d == CONV_DTYPE_F8E4M3;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// ------------------------------------------------------------------ driver
+struct DriverFns {
+  PFN_cuTensorMapEncodeIm2col_v12000 im2col = nullptr;
+  PFN_cuTensorMapEncodeTiled_v12000 tiled = nullptr;
+};
+
+const DriverFns* driver_fns() {
+  static DriverFns fns;
+  static bool ok = false;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    cudaDriverEntryPointQueryResult q1{}, q2{};
+    void* p1 = nullptr;
+    void* p2 = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeIm2col", &p1, 12000, cudaEnableDefault,
+                                         &q1) != cudaSuccess ||
+        cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p2, 12000, cudaEnableDefault,
+                                         &q2) != cudaSuccess ||
+        q1 != cudaDriverEntryPointSuccess || q2 != cudaDriverEntryPointSuccess || !p1 || !p2) {
+      return;
+    }
+    fns.im2col = reinterpret_cast<PFN_cuTensorMapEncodeIm2col_v12000>(p1);
+    fns.tiled = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p2);
+    ok = true;
+  });
+  return ok ? &fns : nullptr;
+}
+
+int device_sm_count() {
+  static std::atomic<int> cache[64];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return -1;
+  int v = cache[dev].load(std::memory_order_relaxed);
+  if (v > 0) return v;
+  if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return -1;
+  cache[dev].store(v, std::memory_order_relaxed);
+  return v;
+}
+
+CUtensorMapDataType tmap_dtype(conv_dtype_t d) {
+  if (d == CONV_DTYPE_BF16) return CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  if (d == CONV_DTYPE_F16) return CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+  return CU_TENSOR_MAP_DATA_TYPE_UINT8;  // fp8 moves as raw bytes
+}
+
+CUtensorMapSwizzle tmap_swizzle(uint32_t row_bytes) {
+  if (row_bytes == 128) return CU_TENSOR_MAP_SWIZZLE_128B;
+  if (row_bytes == 64) return CU_TENSOR_MAP_SWIZZLE_64B;
+  return CU_TENSOR_MAP_SWIZZLE_32B;
+}
+
+// ------------------------------------------------------------------ planning
+struct Plan {
+  ConvKernelParams kp;
+  conv_dtype_t in_dtype;
+  bool out_bf16;
+  int kind;
+  int phases_packed;   // phase slots in the packed filter
+  int kmax;            // packed K per phase slot
+  size_t packed_bytes;
+  int grid;
+  size_t smem_bytes;
+  // packing description of the transposed filter, per phase slot
+  int r0h[kMaxPhases], r0w[kMaxPhases], th[kMaxPhases], tw[kMaxPhases];
+  int sh, sw;
+};
+
+// Channels per k-block: the largest of 128/64/32 bytes that divides C_in.
+conv_status_t channel_block(int c_in, int elt, int* bk, uint32_t* row_bytes) {
+  const long long cb = static_cast<long long>(c_in) * elt;
+  for (uint32_t rb : {128u, 64u, 32u}) {
+    if (cb % rb == 0) {
+      *row_bytes = rb;
+      *bk = static_cast<int>(rb) / elt;
+      return CONV_OK;
+    }
+  }
+  return CONV_ERR_NOT_SUPPORTED;
+}
+
+// Tile width along C_out: one tile up to 256 channels (masked edge tile for
+// C_out not a multiple of 16), else equal tiles of at most 256.
+void choose_bn(int c_out, int* bn, int* n_tiles) {
+  int nt = (c_out + 255) / 256;
+  int per = (c_out + nt - 1) / nt;
+  *bn = ((per + 15) / 16) * 16;
+  *n_tiles = (c_out + *bn - 1) / *bn;
+}
+
+uint32_t make_idesc(conv_dtype_t in, int bn) {
+  // kind::f16: A/B format 0 = fp16, 1 = bf16; kind::f8f6f4: 0 = e4m3.
+  // D format (bits 4-5) 1 = fp32; both operands K-major (bits 15, 16 = 0);
+  // N >> 3 in bits 17-22; M >> 4 in bits 24-28.
+  uint32_t fmt = in == CONV_DTYPE_BF16 ? 1u : 0u;
+  uint32_t d = 0;
+  d |= 1u << 4;
+  d |= fmt << 7;
+  d |= fmt << 10;
+  d |= (static_cast<uint32_t>(bn) >> 3) << 17;
+  d |= (static_cast<uint32_t>(kBM) >> 4) << 24;
+  return d;
+}
+
+uint32_t next_pow2_cols(int cols) {
+  uint32_t c = 32;
+  while (c < static_cast<uint32_t>(cols)) c <<= 1;
+  return c;
+}
+
+conv_status_t encode_input_map(CUtensorMap* map, const void* input, int n, int h, int w, int c,
+                               conv_dtype_t dt, int bk, uint32_t row_bytes, int lower_w,
+                               int lower_h, int upper_w, int upper_h, int step_w, int step_h) {
+  const DriverFns* fns = driver_fns();
+  if (!fns) return CONV_ERR_CUDA;
+  if (lower_w < -128 || lower_w > 127 || lower_h < -128 || lower_h > 127 || upper_w < -128 ||
+      upper_w > 127 || upper_h < -128 || upper_h > 127)
+    return CONV_ERR_NOT_SUPPORTED;
+  const cuuint64_t e = static_cast<cuuint64_t>(elt_bytes(dt));
+  cuuint64_t dims[4] = {static_cast<cuuint64_t>(c), static_cast<cuuint64_t>(w),
+                        static_cast<cuuint64_t>(h), static_cast<cuuint64_t>(n)};
+  cuuint64_t strides[3] = {dims[0] * e, dims[0] * dims[1] * e, dims[0] * dims[1] * dims[2] * e};
+  int lower[2] = {lower_w, lower_h};
+  int upper[2] = {upper_w, upper_h};
+  cuuint32_t estr[4] = {1, static_cast<cuuint32_t>(step_w), static_cast<cuuint32_t>(step_h), 1};
+  CUresult r = fns->im2col(map, tmap_dtype(dt), 4, const_cast<void*>(input), dims, strides, lower,
+                           upper, static_cast<cuuint32_t>(bk), static_cast<cuuint32_t>(kBM), estr,
+                           CU_TENSOR_MAP_INTERLEAVE_NONE, tmap_swizzle(row_bytes),
+                           CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? CONV_OK : CONV_ERR_CUDA;
+}
+
+conv_status_t encode_filter_map(CUtensorMap* map, const void* packed, int kmax, int c_out,
+                                int phases, conv_dtype_t dt, int bk, int bn, uint32_t row_bytes) {
+  const DriverFns* fns = driver_fns();
+  if (!fns) return CONV_ERR_CUDA;
+  const cuuint64_t e = static_cast<cuuint64_t>(elt_bytes(dt));
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(kmax), static_cast<cuuint64_t>(c_out),
+                        static_cast<cuuint64_t>(phases)};
+  cuuint64_t strides[2] = {dims[0] * e, dims[0] * dims[1] * e};
+  cuuint32_t box[3] = {static_cast<cuuint32_t>(bk), static_cast<cuuint32_t>(bn), 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = fns->tiled(map, tmap_dtype(dt), 3, const_cast<void*>(packed), dims, strides, box,
+                          estr, CU_TENSOR_MAP_INTERLEAVE_NONE, tmap_swizzle(row_bytes),
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? CONV_OK : CONV_ERR_CUDA;
+}
+
+bool dtype_pair_ok(conv_dtype_t in, conv_dtype_t out) {
+  if (!known_dtype(in) || !known_dtype(out)) return false;
+  return in == CONV_DTYPE_F8E4M3 ? out == CONV_DTYPE_BF16 : out == in;
+}
+
+// Fills the tile configuration shared by forward and transposed plans.
+conv_status_t plan_tiles(Plan* pl, conv_dtype_t in, int c_in, int c_out) {
+  int bk = 0;
+  uint32_t row_bytes = 0;
+  conv_status_t st = channel_block(c_in, elt_bytes(in), &bk, &row_bytes);
+  if (st != CONV_OK) return st;
+  int bn = 0, n_tiles = 0;
+  choose_bn(c_out, &bn, &n_tiles);
+  ConvKernelParams& kp = pl->kp;
+  kp.bn = bn;
+  kp.n_tiles = n_tiles;
+  kp.bk = bk;
+  kp.c_blocks = c_in / bk;
+  kp.sw_bytes = row_bytes;
+  kp.idesc = make_idesc(in, bn);
+  kp.tmem_cols = next_pow2_cols(2 * bn);
+  const size_t stage_bytes = static_cast<size_t>(kBM + bn) * row_bytes;
+  const size_t fixed = 1024 + 256;
+  int stages = static_cast<int>((kSmemLimit - fixed) / stage_bytes);
+  stages = std::min(stages, kMaxStages);
+  if (stages < 2) return CONV_ERR_NOT_SUPPORTED;
+  kp.stages = stages;
+  pl->smem_bytes = fixed + stages * stage_bytes;
+  pl->in_dtype = in;
+  pl->out_bf16 = (in != CONV_DTYPE_F16);
+  pl->kind = in == CONV_DTYPE_F8E4M3 ? kKindF8 : kKindF16;
+  return CONV_OK;
+}
+
+struct FwdShape {
+  int n, h, w, c_in, r, s, c_out, ho, wo;
+  int stride_h, stride_w, pad_h, pad_w, dil_h, dil_w;
+  conv_dtype_t in_dtype, out_dtype;
+};
+
+conv_status_t check_fwd_shape(const FwdShape& f, int num_groups) {
+  if (f.n <= 0 || f.h <= 0 || f.w <= 0 || f.c_in <= 0 || f.r <= 0 || f.s <= 0 || f.c_out <= 0)
+    return CONV_ERR_INVALID_VALUE;
+  if (!known_dtype(f.in_dtype) || !known_dtype(f.out_dtype)) return CONV_ERR_NOT_SUPPORTED;
+  if (!dtype_pair_ok(f.in_dtype, f.out_dtype)) return CONV_ERR_NOT_SUPPORTED;
+  if (!((f.stride_h == 1 && f.stride_w == 1) || (f.stride_h == 2 && f.stride_w == 2)))
+    return CONV_ERR_NOT_SUPPORTED;
+  if (f.dil_h != 1 || f.dil_w != 1) return CONV_ERR_NOT_SUPPORTED;
+  if (f.pad_h != f.pad_w || f.pad_h < 0 || f.pad_h > 2) return CONV_ERR_NOT_SUPPORTED;
+  if (num_groups != 1) return CONV_ERR_NOT_SUPPORTED;
+  if (f.r > kMaxFilterExtent || f.s > kMaxFilterExtent) return CONV_ERR_NOT_SUPPORTED;
+  const long long ho = (static_cast<long long>(f.h) + 2 * f.pad_h - f.dil_h * (f.r - 1) - 1) /
+                           f.stride_h + 1;
+  const long long wo = (static_cast<long long>(f.w) + 2 * f.pad_w - f.dil_w * (f.s - 1) - 1) /
+                           f.stride_w + 1;
+  if (f.h + 2 * f.pad_h < f.dil_h * (f.r - 1) + 1 || f.w + 2 * f.pad_w < f.dil_w * (f.s - 1) + 1)
+    return CONV_ERR_INVALID_VALUE;
+  if (ho != f.ho || wo != f.wo) return CONV_ERR_INVALID_VALUE;
+  const long long rows = static_cast<long long>(f.n) * f.ho * f.wo;
+  if (rows > (1ll << 30)) return CONV_ERR_NOT_SUPPORTED;
+  return CONV_OK;
+}
+
+conv_status_t plan_fwd(const FwdShape& f, Plan* pl) {
+  std::memset(pl, 0, sizeof(*pl));
+  conv_status_t st = plan_tiles(pl, f.in_dtype, f.c_in, f.c_out);
+  if (st != CONV_OK) return st;
+  ConvKernelParams& kp = pl->kp;
+  kp.num_phases = 1;
+  kp.grid_h[0] = f.ho;
+  kp.grid_w[0] = f.wo;
+  kp.rows[0] = f.n * f.ho * f.wo;
+  kp.taps_h[0] = f.r;
+  kp.taps_w[0] = f.s;
+  kp.base_h[0] = -f.pad_h;
+  kp.base_w[0] = -f.pad_w;
+  kp.out_off_h[0] = 0;
+  kp.out_off_w[0] = 0;
+  kp.b_index[0] = 0;
+  kp.step_h = f.stride_h;
+  kp.step_w = f.stride_w;
+  kp.out_step_h = 1;
+  kp.out_step_w = 1;
+  kp.dil_h = f.dil_h;
+  kp.dil_w = f.dil_w;
+  const int m_tiles = (kp.rows[0] + kBM - 1) / kBM;
+  kp.tile_start[0] = 0;
+  kp.tile_start[1] = m_tiles * kp.n_tiles;
+  kp.total_tiles = kp.tile_start[1];
+  kp.Ho = f.ho;
+  kp.Wo = f.wo;
+  kp.Cout = f.c_out;
+  kp.vec_ok = (f.c_out * 2) % 16 == 0;
+  pl->phases_packed = 1;
+  pl->kmax = f.r * f.s * f.c_in;
+  pl->packed_bytes = static_cast<size_t>(f.c_out) * pl->kmax * elt_bytes(f.in_dtype);
+  return CONV_OK;
+}
+
+// Encodes the forward conv's input map (lower corner -pad, upper corner
+// pad - (S-1)*dil, element strides = conv stride).
+conv_status_t encode_fwd_input(const FwdShape& f, const void* input, Plan* pl) {
+  return encode_input_map(&pl->kp.map_a[0], input, f.n, f.h, f.w, f.c_in, f.in_dtype, pl->kp.bk,
+                          pl->kp.sw_bytes, -f.pad_w, -f.pad_h, f.pad_w - (f.s - 1) * f.dil_w,
+                          f.pad_h - (f.r - 1) * f.dil_h, f.stride_w, f.stride_h);
+}
+
+// Stride-phase decomposition of the transposed conv along one axis.
+// Output index o = st*j + a receives input i = j + L + u through filter tap
+// r(u) = r0 + st*(T-1-u), u in [0, T), where r0 = (a + pad) mod st,
+// T = #{r in [0,R) : r = r0 mod st}, q = (a + pad - r0)/st, L = q - T + 1.
+struct AxisPhase {
+  int r0, taps, lower, grid;
+};
+
+AxisPhase axis_phase(int a, int st, int pad, int R, int out_extent) {
+  AxisPhase ph;
+  ph.r0 = (a + pad) % st;
+  ph.taps = R > ph.r0 ? (R - ph.r0 + st - 1) / st : 0;
+  const int q = (a + pad - ph.r0) / st;
+  ph.lower = q - ph.taps + 1;
+  ph.grid = out_extent > a ? (out_extent - a + st - 1) / st : 0;
+  return ph;
+}
+
+struct TrShape {
+  int n, h, w, c_in, r, s, c_out, ho, wo;
+  int stride_h, stride_w, pad_h, pad_w, dil_h, dil_w;
+  conv_dtype_t in_dtype, out_dtype;
+};
+
+conv_status_t check_tr_shape(const TrShape& t) {
+  if (t.n <= 0 || t.h <= 0 || t.w <= 0 || t.c_in <= 0 || t.r <= 0 || t.s <= 0 || t.c_out <= 0 ||
+      t.ho <= 0 || t.wo <= 0)
+    return CONV_ERR_INVALID_VALUE;
+  if (!known_dtype(t.in_dtype) || !known_dtype(t.out_dtype)) return CONV_ERR_NOT_SUPPORTED;
+  if (!dtype_pair_ok(t.in_dtype, t.out_dtype)) return CONV_ERR_NOT_SUPPORTED;
+  if (!((t.stride_h == 1 && t.stride_w == 1) || (t.stride_h == 2 && t.stride_w == 2)))
+    return CONV_ERR_NOT_SUPPORTED;
+  if (t.dil_h != 1 || t.dil_w != 1) return CONV_ERR_NOT_SUPPORTED;
+  if (t.r > kMaxFilterExtent || t.s > kMaxFilterExtent) return CONV_ERR_NOT_SUPPORTED;
+  if (t.pad_h < 0 || t.pad_w < 0 || t.pad_h >= t.r || t.pad_w >= t.s) return CONV_ERR_NOT_SUPPORTED;
+  const long long base_h = static_cast<long long>(t.h - 1) * t.stride_h - 2 * t.pad_h + (t.r - 1) + 1;
+  const long long base_w = static_cast<long long>(t.w - 1) * t.stride_w - 2 * t.pad_w + (t.s - 1) + 1;
+  if (t.ho - base_h < 0 || t.ho - base_h >= t.stride_h) return CONV_ERR_INVALID_VALUE;
+  if (t.wo - base_w < 0 || t.wo - base_w >= t.stride_w) return CONV_ERR_INVALID_VALUE;
+  const long long rows = static_cast<long long>(t.n) * t.ho * t.wo;
+  if (rows > (1ll << 30)) return CONV_ERR_NOT_SUPPORTED;
+  return CONV_OK;
+}
+
+conv_status_t plan_transposed(const TrShape& t, Plan* pl) {
+  std::memset(pl, 0, sizeof(*pl));
+  conv_status_t st = plan_tiles(pl, t.in_dtype, t.c_in, t.c_out);
+  if (st != CONV_OK) return st;
+  ConvKernelParams& kp = pl->kp;
+  pl->sh = t.stride_h;
+  pl->sw = t.stride_w;
+  pl->phases_packed = t.stride_h * t.stride_w;
+  int kmax = 0;
+  int active = 0;
+  int tile = 0;
+  for (int a = 0; a < t.stride_h; ++a) {
+    const AxisPhase ya = axis_phase(a, t.stride_h, t.pad_h, t.r, t.ho);
+    for (int b = 0; b < t.stride_w; ++b) {
+      const AxisPhase xb = axis_phase(b, t.stride_w, t.pad_w, t.s, t.wo);
+      const int slot = a * t.stride_w + b;
+      pl->r0h[slot] = ya.r0;
+      pl->r0w[slot] = xb.r0;
+      pl->th[slot] = ya.taps;
+      pl->tw[slot] = xb.taps;
+      kmax = std::max(kmax, ya.taps * xb.taps * t.c_in);
+      if (ya.grid == 0 || xb.grid == 0) continue;
+      kp.grid_h[active] = ya.grid;
+      kp.grid_w[active] = xb.grid;
+      kp.rows[active] = t.n * ya.grid * xb.grid;
+      // A phase without taps still runs (kblocks = 0): it writes act(0 + beta*source).
+      kp.taps_h[active] = ya.taps;
+      kp.taps_w[active] = xb.taps;
+      kp.base_h[active] = ya.lower;
+      kp.base_w[active] = xb.lower;
+      kp.out_off_h[active] = a;
+      kp.out_off_w[active] = b;
+      kp.b_index[active] = slot;
+      kp.tile_start[active] = tile;
+      tile += ((kp.rows[active] + kBM - 1) / kBM) * kp.n_tiles;
+      ++active;
+    }
+  }
+  if (kmax == 0) kmax = t.c_in;  // keep the filter map well-formed
+  kp.num_phases = active;
+  kp.tile_start[active] = tile;
+  kp.total_tiles = tile;
+  kp.step_h = 1;
+  kp.step_w = 1;
+  kp.out_step_h = t.stride_h;
+  kp.out_step_w = t.stride_w;
+  kp.dil_h = 1;
+  kp.dil_w = 1;
+  kp.Ho = t.ho;
+  kp.Wo = t.wo;
+  kp.Cout = t.c_out;
+  kp.vec_ok = (t.c_out * 2) % 16 == 0;
+  pl->kmax = kmax;
+  pl->packed_bytes = static_cast<size_t>(pl->phases_packed) * t.c_out * kmax * elt_bytes(t.in_dtype);
+  return CONV_OK;
+}
+
+conv_status_t encode_tr_inputs(const TrShape& t, const void* input, Plan* pl) {
+  ConvKernelParams& kp = pl->kp;
+  for (int ph = 0; ph < kp.num_phases; ++ph) {
+    // Base pixels walk grid_w x grid_h positions at step 1: upper corner so the
+    // bounding box [lower, W-1+upper] holds exactly that many.
+    const int upper_w = kp.grid_w[ph] - t.w + kp.base_w[ph];
+    const int upper_h = kp.grid_h[ph] - t.h + kp.base_h[ph];
+    conv_status_t st = encode_input_map(&kp.map_a[ph], input, t.n, t.h, t.w, t.c_in, t.in_dtype,
+                                        kp.bk, kp.sw_bytes, kp.base_w[ph], kp.base_h[ph], upper_w,
+                                        upper_h, 1, 1);
+    if (st != CONV_OK) return st;
+  }
+  return CONV_OK;
+}
+
+// ------------------------------------------------------------------ packing kernels
+template <typename T>
+__global__ void pack_fwd_kernel(const T* __restrict__ w, T* __restrict__ out, int R, int S, int C,
+                                int F, int fcrs) {
+  const long long K = static_cast<long long>(R) * S * C;
+  const long long total = K * F;
+  for (long long idx = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; idx < total;
+       idx += static_cast<long long>(gridDim.x) * blockDim.x) {
+    const long long f = idx / K;
+    const long long k = idx - f * K;
+    const long long c = k % C;
+    const long long rs = k / C;
+    const long long s = rs % S;
+    const long long r = rs / S;
+    out[idx] = fcrs ? w[((f * C + c) * R + r) * S + s] : w[((r * S + s) * C + c) * F + f];
+  }
+}
+
+struct TrPackDesc {
+  int slots, kmax, sh, sw;
+  int r0h[kMaxPhases], r0w[kMaxPhases], th[kMaxPhases], tw[kMaxPhases];
+};
+
+template <typename T>
+__global__ void pack_transposed_kernel(const T* __restrict__ w, T* __restrict__ out, int R, int S,
+                                       int C, int F, TrPackDesc d) {
+  const long long per_slot = static_cast<long long>(F) * d.kmax;
+  const long long total = per_slot * d.slots;
+  for (long long idx = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; idx < total;
+       idx += static_cast<long long>(gridDim.x) * blockDim.x) {
+    const int slot = static_cast<int>(idx / per_slot);
+    const long long rem = idx - slot * per_slot;
+    const long long f = rem / d.kmax;
+    const long long k = rem - f * d.kmax;
+    const long long tap = k / C;
+    const long long c = k - tap * C;
+    const int th = d.th[slot], tw = d.tw[slot];
+    T v = T(0);
+    if (tap < static_cast<long long>(th) * tw) {
+      const int uh = static_cast<int>(tap / tw);
+      const int uw = static_cast<int>(tap - static_cast<long long>(uh) * tw);
+      const long long r = d.r0h[slot] + static_cast<long long>(d.sh) * (th - 1 - uh);
+      const long long s = d.r0w[slot] + static_cast<long long>(d.sw) * (tw - 1 - uw);
+      v = w[((r * S + s) * F + f) * C + c];  // RSFC [R][S][F][C]
+    }
+    out[idx] = v;
+  }
+}
+
+int pack_grid(long long total) {
+  long long blocks = (total + 255) / 256;
+  return static_cast<int>(std::min<long long>(std::max<long long>(blocks, 1), 4096));
+}
+
+conv_status_t launch_pack_fwd(const void* filter, int r, int s, int c_in, int c_out, int fcrs,
+                              conv_dtype_t dt, void* packed, cudaStream_t stream) {
+  const long long total = static_cast<long long>(r) * s * c_in * c_out;
+  if (elt_bytes(dt) == 2)
+    pack_fwd_kernel<uint16_t><<<pack_grid(total), 256, 0, stream>>>(
+        static_cast<const uint16_t*>(filter), static_cast<uint16_t*>(packed), r, s, c_in, c_out,
+        fcrs);
+  else
+    pack_fwd_kernel<uint8_t><<<pack_grid(total), 256, 0, stream>>>(
+        static_cast<const uint8_t*>(filter), static_cast<uint8_t*>(packed), r, s, c_in, c_out,
+        fcrs);
+  return cudaGetLastError() == cudaSuccess ? CONV_OK : CONV_ERR_CUDA;
+}
+
+conv_status_t launch_pack_tr(const Plan& pl, const void* filter, int r, int s, int c_in,
+                             int c_out, conv_dtype_t dt, void* packed, cudaStream_t stream) {
+  TrPackDesc d{};
+  d.slots = pl.phases_packed;
+  d.kmax = pl.kmax;
+  d.sh = pl.sh;
+  d.sw = pl.sw;
+  for (int i = 0; i < kMaxPhases; ++i) {
+    d.r0h[i] = pl.r0h[i];
+    d.r0w[i] = pl.r0w[i];
+    d.th[i] = pl.th[i];
+    d.tw[i] = pl.tw[i];
+  }
+  const long long total = static_cast<long long>(d.slots) * c_out * d.kmax;
+  if (elt_bytes(dt) == 2)
+    pack_transposed_kernel<uint16_t><<<pack_grid(total), 256, 0, stream>>>(
+        static_cast<const uint16_t*>(filter), static_cast<uint16_t*>(packed), r, s, c_in, c_out, d);
+  else
+    pack_transposed_kernel<uint8_t><<<pack_grid(total), 256, 0, stream>>>(
+        static_cast<const uint8_t*>(filter), static_cast<uint8_t*>(packed), r, s, c_in, c_out, d);
+  return cudaGetLastError() == cudaSuccess ? CONV_OK : CONV_ERR_CUDA;
+}
+
+// ------------------------------------------------------------------ launch
+conv_status_t finish_and_launch(Plan* pl, const void* packed, void* output, int has_residual,
+                                const void* source, float beta, conv_epilogue_t epilogue,
+                                void* workspace, cudaStream_t stream) {
+  ConvKernelParams& kp = pl->kp;
+  conv_status_t st = encode_filter_map(&kp.map_b, packed, pl->kmax, kp.Cout, pl->phases_packed,
+                                       pl->in_dtype, kp.bk, kp.bn, kp.sw_bytes);
+  if (st != CONV_OK) return st;
+  kp.has_residual = has_residual ? 1 : 0;
+  kp.src = has_residual ? source : nullptr;
+  kp.beta = has_residual ? beta : 0.0f;
+  kp.epilogue = static_cast<int>(epilogue);
+  kp.out = output;
+  kp.status = static_cast<unsigned int*>(workspace);
+  const unsigned long long tmo = g_timeout_ns.load(std::memory_order_relaxed);
+  kp.timeout_ns = tmo ? tmo : kDefaultTimeoutNs;
+  kp.fault_mode = g_fault_mode.load(std::memory_order_relaxed);
+  if (kp.total_tiles == 0) return CONV_OK;
+  const int sms = device_sm_count();
+  if (sms <= 0) return CONV_ERR_CUDA;
+  pl->grid = std::min(kp.total_tiles, sms);
+  cudaError_t e = launch_conv_igemm(pl->kind, pl->out_bf16, kp, pl->grid, pl->smem_bytes, stream);
+  return e == cudaSuccess ? CONV_OK : CONV_ERR_CUDA;
+}
+
+bool epilogue_ok(conv_epilogue_t e) {
+  return e == CONV_EPI_NONE || e == CONV_EPI_RELU || e == CONV_EPI_SILU;
+}
+
+conv_status_t check_common_ptrs(const void* input, const void* filter, void* output,
+                                int has_residual, const void* source, void* workspace) {
+  if (!input || !filter || !output || !workspace) return CONV_ERR_INVALID_VALUE;
+  if (has_residual && !source) return CONV_ERR_INVALID_VALUE;
+  if (!aligned16(input) || !aligned16(filter) || !aligned16(output) || !aligned16(workspace))
+    return CONV_ERR_MISALIGNED;
+  if (has_residual && !aligned16(source)) return CONV_ERR_MISALIGNED;
+  return CONV_OK;
+}
+
+size_t round_up_256(size_t v) { return (v + 255) & ~static_cast<size_t>(255); }
+
+FwdShape make_fwd_shape(int n, int h, int w, int c_in, conv_dtype_t in_dtype, int r, int s,
+                        int c_out, int ho, int wo, conv_dtype_t out_dtype, const int stride[2],
+                        const int dilation[2], const int pad[2]) {
+  FwdShape f{};
+  f.n = n; f.h = h; f.w = w; f.c_in = c_in; f.r = r; f.s = s; f.c_out = c_out; f.ho = ho; f.wo = wo;
+  f.stride_h = stride[0]; f.stride_w = stride[1];
+  f.pad_h = pad[0]; f.pad_w = pad[1];
+  f.dil_h = dilation[0]; f.dil_w = dilation[1];
+  f.in_dtype = in_dtype; f.out_dtype = out_dtype;
+  return f;
+}
+
+TrShape make_tr_shape(int n, int h, int w, int c_in, conv_dtype_t in_dtype, int r, int s,
+                      int c_out, int ho, int wo, conv_dtype_t out_dtype, const int stride[2],
+                      const int dilation[2], const int pad[2]) {
+  TrShape t{};
+  t.n = n; t.h = h; t.w = w; t.c_in = c_in; t.r = r; t.s = s; t.c_out = c_out; t.ho = ho; t.wo = wo;
+  t.stride_h = stride[0]; t.stride_w = stride[1];
+  t.pad_h = pad[0]; t.pad_w = pad[1];
+  t.dil_h = dilation[0]; t.dil_w = dilation[1];
+  t.in_dtype = in_dtype; t.out_dtype = out_dtype;
+  return t;
+}
+
+// Common body of conv2d_fwd / conv2d_fwd_packed.  `filter` is raw (packed
+// into the workspace first) unless `prepacked`.
+conv_status_t fwd_impl(const void* input, const FwdShape& f, const void* filter, int fcrs,
+                       bool prepacked, void* output, int num_groups, int has_residual,
+                       const void* source, float beta, conv_epilogue_t epilogue, void* workspace,
+                       size_t workspace_bytes, cudaStream_t stream) {
+  conv_status_t st = check_common_ptrs(input, filter, output, has_residual, source, workspace);
+  if (st != CONV_OK) return st;
+  if (!epilogue_ok(epilogue)) return CONV_ERR_INVALID_VALUE;
+  st = check_fwd_shape(f, num_groups);
+  if (st != CONV_OK) return st;
+  Plan pl;
+  st = plan_fwd(f, &pl);
+  if (st != CONV_OK) return st;
+  const size_t need = CONV_STATUS_BYTES + (prepacked ? 0 : round_up_256(pl.packed_bytes));
+  if (workspace_bytes < need) return CONV_ERR_WORKSPACE_TOO_SMALL;
+  st = encode_fwd_input(f, input, &pl);
+  if (st != CONV_OK) return st;
+  const void* packed = filter;
+  if (!prepacked) {
+    void* dst = static_cast<uint8_t*>(workspace) + CONV_STATUS_BYTES;
+    st = launch_pack_fwd(filter, f.r, f.s, f.c_in, f.c_out, fcrs, f.in_dtype, dst, stream);
+    if (st != CONV_OK) return st;
+    packed = dst;
+  }
+  return finish_and_launch(&pl, packed, output, has_residual, source, beta, epilogue, workspace,
+                           stream);
+}
+
+conv_status_t tr_impl(const void* input, const TrShape& t, const void* filter, bool prepacked,
+                      void* output, int has_residual, const void* source, float beta,
+                      conv_epilogue_t epilogue, void* workspace, size_t workspace_bytes,
+                      cudaStream_t stream) {
+  conv_status_t st = check_common_ptrs(input, filter, output, has_residual, source, workspace);
+  if (st != CONV_OK) return st;
+  if (!epilogue_ok(epilogue)) return CONV_ERR_INVALID_VALUE;
+  st = check_tr_shape(t);
+  if (st != CONV_OK) return st;
+  Plan pl;
+  st = plan_transposed(t, &pl);
+  if (st != CONV_OK) return st;
+  const size_t need = CONV_STATUS_BYTES + (prepacked ? 0 : round_up_256(pl.packed_bytes));
+  if (workspace_bytes < need) return CONV_ERR_WORKSPACE_TOO_SMALL;
+  st = encode_tr_inputs(t, input, &pl);
+  if (st != CONV_OK) return st;
+  const void* packed = filter;
+  if (!prepacked) {
+    void* dst = static_cast<uint8_t*>(workspace) + CONV_STATUS_BYTES;
+    st = launch_pack_tr(pl, filter, t.r, t.s, t.c_in, t.c_out, t.in_dtype, dst, stream);
+    if (st != CONV_OK) return st;
+    packed = dst;
+  }
+  return finish_and_launch(&pl, packed, output, has_residual, source, beta, epilogue, workspace,
+                           stream);
+}
+
+}  // namespace
+
+// =================================================================== C ABI
+extern "C" {
+
+const char* conv_status_string(conv_status_t status) {
+  switch (status) {
+    case CONV_OK: return "CONV_OK";
+    case CONV_ERR_INVALID_VALUE: return "CONV_ERR_INVALID_VALUE";
+    case CONV_ERR_NOT_SUPPORTED: return "CONV_ERR_NOT_SUPPORTED";
+    case CONV_ERR_MISALIGNED: return "CONV_ERR_MISALIGNED";
+    case CONV_ERR_WORKSPACE_TOO_SMALL: return "CONV_ERR_WORKSPACE_TOO_SMALL";
+    case CONV_ERR_CUDA: return "CONV_ERR_CUDA";
+    case CONV_ERR_DEVICE_TIMEOUT: return "CONV_ERR_DEVICE_TIMEOUT";
+  }
+  return "CONV_ERR_UNKNOWN";
+}
+
+size_t conv2d_packed_filter_bytes(int r, int s, int c_in, int c_out, conv_dtype_t dtype) {
+  if (r <= 0 || s <= 0 || c_in <= 0 || c_out <= 0 || !known_dtype(dtype)) return 0;
+  return static_cast<size_t>(r) * s * c_in * c_out * elt_bytes(dtype);
+}
+
+size_t conv2d_workspace_size(int r, int s, int c_in, int c_out, conv_dtype_t dtype) {
+  return CONV_STATUS_BYTES + round_up_256(conv2d_packed_filter_bytes(r, s, c_in, c_out, dtype));
+}
+
+conv_status_t conv2d_pack_filter(const void* filter, int r, int s, int c_in, int c_out,
+                                 int filter_is_fcrs, conv_dtype_t dtype, void* packed,
+                                 size_t packed_bytes, void* stream) {
+  if (!filter || !packed) return CONV_ERR_INVALID_VALUE;
+  if (r <= 0 || s <= 0 || c_in <= 0 || c_out <= 0) return CONV_ERR_INVALID_VALUE;
+  if (!known_dtype(dtype)) return CONV_ERR_NOT_SUPPORTED;
+  if (!aligned16(filter) || !aligned16(packed)) return CONV_ERR_MISALIGNED;
+  if (packed_bytes < conv2d_packed_filter_bytes(r, s, c_in, c_out, dtype))
+    return CONV_ERR_WORKSPACE_TOO_SMALL;
+  return launch_pack_fwd(filter, r, s, c_in, c_out, filter_is_fcrs ? 1 : 0, dtype, packed,
+                         static_cast<cudaStream_t>(stream));
+}
+
+conv_status_t conv2d_fwd(const void* input, int n, int h, int w, int c_in, conv_dtype_t in_dtype,
+                         const void* filter, int r, int s, int c_out, int filter_is_fcrs,
+                         void* output, int ho, int wo, conv_dtype_t out_dtype,
+                         const int stride[2], const int dilation[2],
+                         const int symmetric_padding[2], int num_groups, int has_residual,
+                         const void* source, float beta, conv_epilogue_t epilogue,
+                         void* workspace, size_t workspace_bytes, void* stream) {
+  if (!stride || !dilation || !symmetric_padding) return CONV_ERR_INVALID_VALUE;
+  const FwdShape f = make_fwd_shape(n, h, w, c_in, in_dtype, r, s, c_out, ho, wo, out_dtype,
+                                    stride, dilation, symmetric_padding);
+  return fwd_impl(input, f, filter, filter_is_fcrs ? 1 : 0, false, output, num_groups,
+                  has_residual, source, beta, epilogue, workspace, workspace_bytes,
+                  static_cast<cudaStream_t>(stream));
+}
+
+conv_status_t conv2d_fwd_packed(const void* input, int n, int h, int w, int c_in,
+                                conv_dtype_t in_dtype, const void* packed_filter, int r, int s,
+                                int c_out, void* output, int ho, int wo, conv_dtype_t out_dtype,
+                                const int stride[2], const int dilation[2],
+                                const int symmetric_padding[2], int num_groups, int has_residual,
+                                const void* source, float beta, conv_epilogue_t epilogue,
+                                void* workspace, size_t workspace_bytes, void* stream) {
+  if (!stride || !dilation || !symmetric_padding) return CONV_ERR_INVALID_VALUE;
+  const FwdShape f = make_fwd_shape(n, h, w, c_in, in_dtype, r, s, c_out, ho, wo, out_dtype,
+                                    stride, dilation, symmetric_padding);
+  return fwd_impl(input, f, packed_filter, 0, true, output, num_groups, has_residual, source, beta,
+                  epilogue, workspace, workspace_bytes, static_cast<cudaStream_t>(stream));
+}
+
+size_t conv_transposed_packed_filter_bytes(int r, int s, int c_in, int c_out, const int stride[2],
+                                           const int padding[2], conv_dtype_t dtype) {
+  if (!stride || !padding || r <= 0 || s <= 0 || c_in <= 0 || c_out <= 0 || !known_dtype(dtype))
+    return 0;
+  if (stride[0] <= 0 || stride[1] <= 0 || stride[0] > 2 || stride[1] > 2) return 0;
+  if (padding[0] < 0 || padding[1] < 0) return 0;
+  int kmax = 0;
+  for (int a = 0; a < stride[0]; ++a) {
+    const int ta = axis_phase(a, stride[0], padding[0], r, stride[0]).taps;
+    for (int b = 0; b < stride[1]; ++b) {
+      const int tb = axis_phase(b, stride[1], padding[1], s, stride[1]).taps;
+      kmax = std::max(kmax, ta * tb * c_in);
+    }
+  }
+  if (kmax == 0) kmax = c_in;
+  return static_cast<size_t>(stride[0]) * stride[1] * c_out * kmax * elt_bytes(dtype);
+}
+
+size_t conv_transposed_workspace_size(int r, int s, int c_in, int c_out, const int stride[2],
+                                      const int padding[2], conv_dtype_t dtype) {
+  return CONV_STATUS_BYTES +
+         round_up_256(conv_transposed_packed_filter_bytes(r, s, c_in, c_out, stride, padding, dtype));
+}
+
+conv_status_t conv_transposed_pack_filter(const void* filter_rsfc, int r, int s, int c_in,
+                                          int c_out, const int stride[2], const int padding[2],
+                                          conv_dtype_t dtype, void* packed, size_t packed_bytes,
+                                          void* stream) {
+  if (!filter_rsfc || !packed || !stride || !padding) return CONV_ERR_INVALID_VALUE;
+  if (r <= 0 || s <= 0 || c_in <= 0 || c_out <= 0) return CONV_ERR_INVALID_VALUE;
+  if (!known_dtype(dtype)) return CONV_ERR_NOT_SUPPORTED;
+  if (!((stride[0] == 1 && stride[1] == 1) || (stride[0] == 2 && stride[1] == 2)))
+    return CONV_ERR_NOT_SUPPORTED;
+  if (padding[0] < 0 || padding[1] < 0 || padding[0] >= r || padding[1] >= s)
+    return CONV_ERR_NOT_SUPPORTED;
+  if (!aligned16(filter_rsfc) || !aligned16(packed)) return CONV_ERR_MISALIGNED;
+  const size_t need = conv_transposed_packed_filter_bytes(r, s, c_in, c_out, stride, padding, dtype);
+  if (packed_bytes < need) return CONV_ERR_WORKSPACE_TOO_SMALL;
+  // The phase taps depend only on stride, padding and filter extent.
+  Plan pl;
+  std::memset(&pl, 0, sizeof(pl));
+  pl.sh = stride[0];
+  pl.sw = stride[1];
+  pl.phases_packed = stride[0] * stride[1];
+  int kmax = 0;
+  for (int a = 0; a < stride[0]; ++a) {
+    const AxisPhase ya = axis_phase(a, stride[0], padding[0], r, stride[0]);
+    for (int b = 0; b < stride[1]; ++b) {
+      const AxisPhase xb = axis_phase(b, stride[1], padding[1], s, stride[1]);
+      const int slot = a * stride[1] + b;
+      pl.r0h[slot] = ya.r0;
+      pl.r0w[slot] = xb.r0;
+      pl.th[slot] = ya.taps;
+      pl.tw[slot] = xb.taps;
+      kmax = std::max(kmax, ya.taps * xb.taps * c_in);
+    }
+  }
+  pl.kmax = kmax ? kmax : c_in;
+  return launch_pack_tr(pl, filter_rsfc, r, s, c_in, c_out, dtype, packed,
+                        static_cast<cudaStream_t>(stream));
+}
+
+conv_status_t conv_transposed(const void* input, int n, int h, int w, int c_in,
+                              conv_dtype_t in_dtype, const void* filter_rsfc, int r, int s,
+                              int c_out, void* output, int ho, int wo, conv_dtype_t out_dtype,
+                              const int stride[2], const int dilation[2], const int padding[2],
+                              int has_residual, const void* source, float beta,
+                              conv_epilogue_t epilogue, void* workspace, size_t workspace_bytes,
+                              void* stream) {
+  if (!stride || !dilation || !padding) return CONV_ERR_INVALID_VALUE;
+  const TrShape t = make_tr_shape(n, h, w, c_in, in_dtype, r, s, c_out, ho, wo, out_dtype, stride,
+                                  dilation, padding);
+  return tr_impl(input, t, filter_rsfc, false, output, has_residual, source, beta, epilogue,
+                 workspace, workspace_bytes, static_cast<cudaStream_t>(stream));
+}
+
+conv_status_t conv_transposed_packed(const void* input, int n, int h, int w, int c_in,
+                                     conv_dtype_t in_dtype, const void* packed_filter, int r,
+                                     int s, int c_out, void* output, int ho, int wo,
+                                     conv_dtype_t out_dtype, const int stride[2],
+                                     const int dilation[2], const int padding[2], int has_residual,
+                                     const void* source, float beta, conv_epilogue_t epilogue,
+                                     void* workspace, size_t workspace_bytes, void* stream) {
+  if (!stride || !dilation || !padding) return CONV_ERR_INVALID_VALUE;
+  const TrShape t = make_tr_shape(n, h, w, c_in, in_dtype, r, s, c_out, ho, wo, out_dtype, stride,
+                                  dilation, padding);
+  return tr_impl(input, t, packed_filter, true, output, has_residual, source, beta, epilogue,
+                 workspace, workspace_bytes, static_cast<cudaStream_t>(stream));
+}
+
+conv_status_t conv_check_device_status(void* workspace, void* stream, unsigned int* detail) {
+  if (detail) *detail = 0;
+  if (!workspace) return CONV_ERR_INVALID_VALUE;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (cudaStreamSynchronize(st) != cudaSuccess) return CONV_ERR_CUDA;
+  unsigned int bits = 0;
+  if (cudaMemcpy(&bits, workspace, sizeof(bits), cudaMemcpyDeviceToHost) != cudaSuccess)
+    return CONV_ERR_CUDA;
+  if (detail) *detail = bits;
+  if (bits == 0) return CONV_OK;
+  if (cudaMemset(workspace, 0, sizeof(bits)) != cudaSuccess) return CONV_ERR_CUDA;
+  return CONV_ERR_DEVICE_TIMEOUT;
+}
+
+// ------------------------------------------------------------------- testing hooks
+void conv_testing_set_wait_fault(int mode, unsigned long long timeout_ns) {
+  g_fault_mode.store(mode, std::memory_order_relaxed);
+  g_timeout_ns.store(timeout_ns, std::memory_order_relaxed);
+}
+
+conv_status_t conv_testing_fwd_plan(int n, int h, int w, int c_in, conv_dtype_t dtype, int r,
+                                    int s, int c_out, const int stride[2],
+                                    const int symmetric_padding[2], int num_sms, int out[7]) {
+  if (!stride || !symmetric_padding || !out) return CONV_ERR_INVALID_VALUE;
+  const int dil[2] = {1, 1};
+  const conv_dtype_t out_dt = dtype == CONV_DTYPE_F8E4M3 ? CONV_DTYPE_BF16 : dtype;
+  if (stride[0] <= 0 || stride[1] <= 0) return CONV_ERR_INVALID_VALUE;
+  const int ho = (h + 2 * symmetric_padding[0] - (r - 1) - 1) / stride[0] + 1;
+  const int wo = (w + 2 * symmetric_padding[1] - (s - 1) - 1) / stride[1] + 1;
+  const FwdShape f = make_fwd_shape(n, h, w, c_in, dtype, r, s, c_out, ho, wo, out_dt, stride, dil,
+                                    symmetric_padding);
+  conv_status_t st = check_fwd_shape(f, 1);
+  if (st != CONV_OK) return st;
+  Plan pl;
+  st = plan_fwd(f, &pl);
+  if (st != CONV_OK) return st;
+  out[0] = pl.kp.bn;
+  out[1] = pl.kp.bk;
+  out[2] = pl.kp.stages;
+  out[3] = static_cast<int>(pl.smem_bytes);
+  out[4] = pl.kp.total_tiles;
+  out[5] = std::min(pl.kp.total_tiles, num_sms);
+  out[6] = static_cast<int>(pl.kp.tmem_cols);
+  return CONV_OK;
+}
+
+conv_status_t conv_testing_im2col_tile(const void* input, int n, int h, int w, int c_in,
+                                       conv_dtype_t dtype, int r, int s, const int stride[2],
+                                       const int symmetric_padding[2], int m0, int tap_r,
+                                       int tap_s, int c0, void* out_tile, int* bk_out,
+                                       void* status_workspace, void* stream) {
+  if (!input || !out_tile || !status_workspace || !stride || !symmetric_padding)
+    return CONV_ERR_INVALID_VALUE;
+  if (!aligned16(input) || !aligned16(out_tile)) return CONV_ERR_MISALIGNED;
+  const int dil[2] = {1, 1};
+  const conv_dtype_t out_dt = dtype == CONV_DTYPE_F8E4M3 ? CONV_DTYPE_BF16 : dtype;
+  if (stride[0] <= 0 || stride[1] <= 0) return CONV_ERR_INVALID_VALUE;
+  const int ho = (h + 2 * symmetric_padding[0] - (r - 1) - 1) / stride[0] + 1;
+  const int wo = (w + 2 * symmetric_padding[1] - (s - 1) - 1) / stride[1] + 1;
+  const FwdShape f = make_fwd_shape(n, h, w, c_in, dtype, r, s, 16, ho, wo, out_dt, stride, dil,
+                                    symmetric_padding);
+  conv_status_t st = check_fwd_shape(f, 1);
+  if (st != CONV_OK) return st;
+  Plan pl;
+  st = plan_fwd(f, &pl);
+  if (st != CONV_OK) return st;
+  if (m0 < 0 || m0 >= pl.kp.rows[0] || tap_r < 0 || tap_r >= r || tap_s < 0 || tap_s >= s ||
+      c0 < 0 || c0 >= c_in || c0 % pl.kp.bk != 0)
+    return CONV_ERR_INVALID_VALUE;
+  st = encode_fwd_input(f, input, &pl);
+  if (st != CONV_OK) return st;
+  const int hw = ho * wo;
+  const int n_img = m0 / hw;
+  const int rem = m0 - n_img * hw;
+  const int j = rem / wo;
+  const int i = rem - j * wo;
+  const int h0 = -f.pad_h + j * f.stride_h;
+  const int w0 = -f.pad_w + i * f.stride_w;
+  if (bk_out) *bk_out = pl.kp.bk;
+  cudaStream_t cs = static_cast<cudaStream_t>(stream);
+  const unsigned long long tmo = g_timeout_ns.load(std::memory_order_relaxed);
+  cudaError_t e = launch_im2col_probe(pl.kp.map_a[0], c0, w0, h0, n_img, tap_s, tap_r,
+                                      pl.kp.sw_bytes, out_tile,
+                                      static_cast<unsigned int*>(status_workspace),
+                                      tmo ? tmo : kDefaultTimeoutNs, cs);
+  if (e != cudaSuccess) return CONV_ERR_CUDA;
+  return cudaStreamSynchronize(cs) == cudaSuccess ? CONV_OK : CONV_ERR_CUDA;
+}
+
+}  // extern "C"

@@ -1,0 +1,88 @@
+// Instances of the implicit-GEMM kernel and the im2col probe, with their launchers.
+#include <atomic>
+
+#include "conv_internal.h"
+#include "conv_kernel.cuh"
+
+namespace convgb300 {
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+
+template <int kKind, typename OutT>
+cudaError_t launch_instance(const ConvKernelParams& p, int grid, size_t smem_bytes,
+                            cudaStream_t stream) {
+  // The dynamic shared-memory limit is a per-device function attribute: raise
+  // it once per device to the largest size requested so far.
+  static std::atomic<size_t> configured[kMaxDevices];
+  int dev = 0;
+  cudaError_t err = cudaGetDevice(&dev);
+  if (err != cudaSuccess) return err;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  if (configured[dev].load(std::memory_order_relaxed) < smem_bytes) {
+    err = cudaFuncSetAttribute(conv_igemm_kernel<kKind, OutT>,
+                               cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               static_cast<int>(smem_bytes));
+    if (err != cudaSuccess) return err;
+    configured[dev].store(smem_bytes, std::memory_order_relaxed);
+  }
+  conv_igemm_kernel<kKind, OutT><<<grid, kThreads, smem_bytes, stream>>>(p);
+  return cudaGetLastError();
+}
+
+__global__ void im2col_probe_kernel(const __grid_constant__ CUtensorMap map, int c, int w, int h,
+                                    int n, int off_w, int off_h, uint32_t row_bytes,
+                                    uint8_t* __restrict__ out, unsigned int* status,
+                                    unsigned long long limit_ns) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* tile = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  __shared__ uint64_t bar;
+  __shared__ int abort_flag;
+  const uint32_t bytes = kBM * row_bytes;
+  if (threadIdx.x == 0) {
+    mbar_init(smem_u32(&bar), 1);
+    abort_flag = 0;
+    fence_barrier_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    mbar_arrive_expect_tx(smem_u32(&bar), bytes);
+    tma_load_im2col_4d(smem_u32(tile), &map, smem_u32(&bar), c, w, h, n,
+                       static_cast<uint16_t>(off_w), static_cast<uint16_t>(off_h));
+  }
+  const bool ok = mbar_wait_bounded(smem_u32(&bar), 0, &abort_flag, status, 1u, limit_ns);
+  if (!__syncthreads_and(ok)) {
+    if (threadIdx.x == 0) mbar_wait_drain(smem_u32(&bar), 0, limit_ns);
+    __syncthreads();
+    return;
+  }
+  // The TMA swizzle XORs the 16-byte chunk index with address bits 7 and up.
+  const uint32_t mask = row_bytes / 16 - 1;
+  for (uint32_t q = threadIdx.x; q < bytes / 16; q += blockDim.x) {
+    const uint32_t logical = q * 16;
+    const uint32_t phys = logical ^ (((logical >> 7) & mask) << 4);
+    reinterpret_cast<uint4*>(out)[q] = *reinterpret_cast<const uint4*>(tile + phys);
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_conv_igemm(int kind, bool out_bf16, const ConvKernelParams& p, int grid,
+                              size_t smem_bytes, cudaStream_t stream) {
+  if (kind == kKindF8) return launch_instance<kKindF8, __nv_bfloat16>(p, grid, smem_bytes, stream);
+  if (out_bf16) return launch_instance<kKindF16, __nv_bfloat16>(p, grid, smem_bytes, stream);
+  return launch_instance<kKindF16, __half>(p, grid, smem_bytes, stream);
+}
+
+cudaError_t launch_im2col_probe(const CUtensorMap& map, int c, int w, int h, int n, int off_w,
+                                int off_h, uint32_t row_bytes, void* out, unsigned int* status,
+                                unsigned long long limit_ns, cudaStream_t stream) {
+  const size_t smem = 1024 + static_cast<size_t>(kBM) * row_bytes;
+  im2col_probe_kernel<<<1, 128, smem, stream>>>(map, c, w, h, n, off_w, off_h, row_bytes,
+                                                static_cast<uint8_t*>(out), status, limit_ns);
+  return cudaGetLastError();
+}
+
+}  // namespace convgb300

@@ -1,0 +1,72 @@
+// Launch parameters shared by the host dispatcher and the implicit-GEMM
+// kernel.  Passed by value as a __grid_constant__ kernel argument, so the
+// tensor maps live in parameter space where TMA can read them.
+#pragma once
+
+#include <cstdint>
+#include <cuda.h>
+
+namespace convgb300 {
+
+constexpr int kBM = 128;             // rows (output pixels) per tile = MMA M
+constexpr int kThreads = 192;        // producer warp + MMA warp + 4 epilogue warps
+constexpr int kEpilogueWarps = 4;
+constexpr int kMaxPhases = 4;        // stride-phase GEMMs of a stride-2 transposed conv
+constexpr int kMaxStages = 12;
+
+constexpr int kKindF16 = 0;          // tcgen05.mma kind::f16 (bf16 or fp16 operands)
+constexpr int kKindF8 = 1;           // tcgen05.mma kind::f8f6f4 (fp8 e4m3 operands)
+
+constexpr int kEpiNone = 0;
+constexpr int kEpiRelu = 1;
+constexpr int kEpiSilu = 2;
+
+// Device status bits (OR-ed into the workspace status word).
+constexpr unsigned int kStatusProducerTimeout = 1u;
+constexpr unsigned int kStatusMmaTimeout = 2u;
+constexpr unsigned int kStatusEpilogueTimeout = 4u;
+
+struct ConvKernelParams {  // aligned like CUtensorMap (64 B or more)
+  CUtensorMap map_a[kMaxPhases];  // im2col maps over the NHWC input, one per phase
+  CUtensorMap map_b;              // tiled map over the packed filter [phase][C_out][K]
+
+  int num_phases;
+  int total_tiles;
+  int n_tiles;          // tiles along C_out
+  int bn;               // tile width along C_out (multiple of 16, <= 256)
+  int bk;               // input channels per k-block
+  int c_blocks;         // C_in / bk
+  int stages;           // depth of the shared-memory ring
+  uint32_t sw_bytes;    // bytes per operand row in a k-block (32, 64 or 128) = swizzle span
+  uint32_t idesc;       // tcgen05 instruction descriptor
+  uint32_t tmem_cols;   // allocated TMEM columns (two accumulators)
+
+  // Per phase: the output-pixel grid the GEMM rows walk, and where it reads.
+  int tile_start[kMaxPhases + 1];  // first tile index of each phase (prefix sums)
+  int rows[kMaxPhases];            // GEMM rows = N * grid_h * grid_w
+  int grid_h[kMaxPhases];
+  int grid_w[kMaxPhases];
+  int taps_h[kMaxPhases];          // filter taps along H contributing to this phase
+  int taps_w[kMaxPhases];
+  int base_h[kMaxPhases];          // input row of grid row 0 at tap 0
+  int base_w[kMaxPhases];
+  int out_off_h[kMaxPhases];       // output row = out_step_h * grid row + out_off_h
+  int out_off_w[kMaxPhases];
+  int step_h, step_w;              // input rows/cols advanced per grid row/col
+  int out_step_h, out_step_w;
+  int dil_h, dil_w;                // input offset per filter tap
+  int b_index[kMaxPhases];         // phase slot of the packed filter read by each phase
+
+  int Ho, Wo, Cout;
+  int vec_ok;                      // C_out * 2 bytes is a multiple of 16: 16-B stores
+  int has_residual;
+  int epilogue;
+  float beta;
+  const void* src;
+  void* out;
+  unsigned int* status;
+  unsigned long long timeout_ns;   // limit of every bounded wait
+  int fault_mode;                  // test hook: 1 = CTA 0 skips its first arrive
+};
+
+}  // namespace convgb300
