@@ -41,13 +41,17 @@ conv_status_t conv_testing_im2col_tile(const void* input, int n, int h, int w, i
                                        int tap_s, int c0, void* out_tile, int* bk_out,
                                        void* status_workspace, void* stream);
 
-/* The tile configuration the dispatcher picks for a forward convolution:
- * out[0] = bn (tile width along C_out), out[1] = bk (channels per k-block),
- * out[2] = pipeline stages, out[3] = dynamic shared memory bytes,
- * out[4] = total tiles, out[5] = grid size (CTAs), out[6] = TMEM columns. */
+/* The tile and shared-memory configuration the dispatcher picks for a
+ * forward convolution: out[0] = bn (tile width along C_out), out[1] = bk
+ * (channels per k-block), out[2] = pipeline stages, out[3] = dynamic shared
+ * memory bytes, out[4] = total tiles, out[5] = grid size (CTAs), out[6] =
+ * TMEM columns, out[7] = epilogue mode (0 direct stores, 1 TMA 2-D, 2 TMA
+ * phase grid), out[8] = filter resident in shared memory, out[9] = residual
+ * source buffers, out[10] = output staging buffers.  Host-only. */
 conv_status_t conv_testing_fwd_plan(int n, int h, int w, int c_in, conv_dtype_t dtype, int r,
                                     int s, int c_out, const int stride[2],
-                                    const int symmetric_padding[2], int num_sms, int out[7]);
+                                    const int symmetric_padding[2], int has_residual, int num_sms,
+                                    int out[11]);
 
 #ifdef __cplusplus
 }

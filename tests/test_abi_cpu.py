@@ -153,25 +153,31 @@ def test_pack_validation(lib):
                                            F16, D, 1 << 20, None) == NOTSUP
 
 
-def _plan(lib, n, h, w, c, dt, r, f, st, pd, sms=148):
-    out = (ctypes.c_int * 7)()
+def _plan(lib, n, h, w, c, dt, r, f, st, pd, res=0, sms=148):
+    out = (ctypes.c_int * 11)()
     assert lib.conv_testing_fwd_plan(n, h, w, c, dt, r, r, f, _lib.pair((st, st)), _lib.pair((pd, pd)),
-                                     sms, out) == OK
-    return dict(zip(("bn", "bk", "stages", "smem", "tiles", "grid", "tmem"), list(out)))
+                                     res, sms, out) == OK
+    keys = ("bn", "bk", "stages", "smem", "tiles", "grid", "tmem", "epi", "bres", "srcb", "stgb")
+    return dict(zip(keys, list(out)))
 
 
 def test_tile_plans_for_the_workloads(lib):
-    p = _plan(lib, 32, 56, 56, 64, BF16, 3, 64, 1, 1)            # ResNet 3x3
-    assert (p["bn"], p["bk"], p["tiles"], p["tmem"]) == (64, 64, 784, 128)
-    assert p["smem"] <= 227 * 1024 and p["stages"] >= 4
-    p = _plan(lib, 16, 64, 64, 320, F8, 3, 320, 1, 1)            # fp8: 2 x 160 columns, 64-ch blocks
-    assert (p["bn"], p["bk"], p["tiles"], p["tmem"]) == (160, 64, 1024, 512)
-    p = _plan(lib, 1, 512, 512, 128, BF16, 3, 3, 1, 1)           # C_out = 3: one 16-wide masked tile
-    assert (p["bn"], p["bk"], p["tiles"]) == (16, 64, 2048)
-    p = _plan(lib, 1, 256, 256, 512, BF16, 3, 512, 1, 1)
-    assert (p["bn"], p["tiles"], p["tmem"]) == (256, 1024, 512)
-    p = _plan(lib, 1, 16, 16, 16, BF16, 3, 16, 1, 1)             # 32-byte channel rows
-    assert (p["bn"], p["bk"], p["tiles"], p["grid"]) == (16, 16, 2, 2)
+    """The dispatcher's tile choices for the benchmark shapes (152 SMs)."""
+    p = _plan(lib, 32, 56, 56, 64, BF16, 3, 64, 1, 1, res=1, sms=152)   # ResNet 3x3 + residual
+    assert (p["bn"], p["bk"], p["tiles"], p["tmem"]) == (64, 64, 392, 256)   # 256-row tiles
+    assert (p["epi"], p["bres"]) == (1, 1)                 # TMA epilogue, filter resident
+    assert p["smem"] <= 227 * 1024 and p["stages"] >= 3
+    p = _plan(lib, 32, 56, 56, 64, BF16, 3, 128, 2, 1, sms=152)          # downsample: 147 KB filter
+    assert (p["bn"], p["tiles"], p["epi"], p["bres"]) == (128, 98, 1, 0) and p["stages"] >= 4
+    p = _plan(lib, 16, 64, 64, 320, F8, 3, 320, 1, 1, res=1, sms=152)    # fp8: 3 x 112 columns
+    assert (p["bn"], p["bk"], p["tiles"], p["tmem"], p["epi"]) == (112, 64, 768, 512, 1)
+    p = _plan(lib, 1, 512, 512, 128, BF16, 3, 3, 1, 1, sms=152)          # C_out = 3: masked 16-wide tile
+    assert (p["bn"], p["bk"], p["tiles"], p["epi"], p["bres"]) == (16, 64, 1024, 0, 1)
+    p = _plan(lib, 1, 16, 16, 16, BF16, 3, 16, 1, 1, sms=152)            # 32-byte channel rows
+    assert (p["bn"], p["bk"], p["grid"]) == (16, 16, p["tiles"])
+    for args in [(1, 256, 256, 512, BF16, 3, 512, 1, 1), (8, 128, 128, 128, F16, 5, 128, 2, 2)]:
+        q = _plan(lib, *args, sms=152)
+        assert q["smem"] <= 227 * 1024 and q["stages"] >= 3 and q["tmem"] <= 512
 
 
 def test_binding_raises_without_library(monkeypatch, tmp_path):

@@ -77,7 +77,7 @@ def _declare(lib):
     lib.conv_testing_set_wait_fault.restype = None
     lib.conv_testing_im2col_tile.argtypes = [P, I, I, I, I, I, I, I, IP, IP, I, I, I, I, P, IP, P, P]
     lib.conv_testing_im2col_tile.restype = I
-    lib.conv_testing_fwd_plan.argtypes = [I, I, I, I, I, I, I, I, IP, IP, I, IP]
+    lib.conv_testing_fwd_plan.argtypes = [I, I, I, I, I, I, I, I, IP, IP, I, I, IP]
     lib.conv_testing_fwd_plan.restype = I
     return lib
 

@@ -68,6 +68,21 @@ const DriverFns* driver_fns() {
   return ok ? &fns : nullptr;
 }
 
+// Cycles of the SM clock in `ns` nanoseconds (at the device's rated clock;
+// a throttled clock only makes the bounded waits last longer).
+long long ns_to_cycles(unsigned long long ns) {
+  static std::atomic<int> khz_cache[64];
+  int dev = 0;
+  int khz = 2100000;
+  if (cudaGetDevice(&dev) == cudaSuccess && dev >= 0 && dev < 64) {
+    int v = khz_cache[dev].load(std::memory_order_relaxed);
+    if (v <= 0 && cudaDeviceGetAttribute(&v, cudaDevAttrClockRate, dev) == cudaSuccess && v > 0)
+      khz_cache[dev].store(v, std::memory_order_relaxed);
+    if (v > 0) khz = v;
+  }
+  return static_cast<long long>(ns / 1000ull) * khz / 1000ll + 1;
+}
+
 int device_sm_count() {
   static std::atomic<int> cache[64];
   int dev = 0;
@@ -120,15 +135,6 @@ conv_status_t channel_block(int c_in, int elt, int* bk, uint32_t* row_bytes) {
   return CONV_ERR_NOT_SUPPORTED;
 }
 
-// Tile width along C_out: one tile up to 256 channels (masked edge tile for
-// C_out not a multiple of 16), else equal tiles of at most 256.
-void choose_bn(int c_out, int* bn, int* n_tiles) {
-  int nt = (c_out + 255) / 256;
-  int per = (c_out + nt - 1) / nt;
-  *bn = ((per + 15) / 16) * 16;
-  *n_tiles = (c_out + *bn - 1) / *bn;
-}
-
 uint32_t make_idesc(conv_dtype_t in, int bn) {
   // kind::f16: A/B format 0 = fp16, 1 = bf16; kind::f8f6f4: 0 = e4m3.
   // D format (bits 4-5) 1 = fp32; both operands K-major (bits 15, 16 = 0);
@@ -150,7 +156,7 @@ uint32_t next_pow2_cols(int cols) {
 }
 
 conv_status_t encode_input_map(CUtensorMap* map, const void* input, int n, int h, int w, int c,
-                               conv_dtype_t dt, int bk, uint32_t row_bytes, int lower_w,
+                               conv_dtype_t dt, int bk, uint32_t row_bytes, int pixels, int lower_w,
                                int lower_h, int upper_w, int upper_h, int step_w, int step_h) {
   const DriverFns* fns = driver_fns();
   if (!fns) return CONV_ERR_CUDA;
@@ -165,7 +171,7 @@ conv_status_t encode_input_map(CUtensorMap* map, const void* input, int n, int h
   int upper[2] = {upper_w, upper_h};
   cuuint32_t estr[4] = {1, static_cast<cuuint32_t>(step_w), static_cast<cuuint32_t>(step_h), 1};
   CUresult r = fns->im2col(map, tmap_dtype(dt), 4, const_cast<void*>(input), dims, strides, lower,
-                           upper, static_cast<cuuint32_t>(bk), static_cast<cuuint32_t>(kBM), estr,
+                           upper, static_cast<cuuint32_t>(bk), static_cast<cuuint32_t>(pixels), estr,
                            CU_TENSOR_MAP_INTERLEAVE_NONE, tmap_swizzle(row_bytes),
                            CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? CONV_OK : CONV_ERR_CUDA;
@@ -192,33 +198,67 @@ bool dtype_pair_ok(conv_dtype_t in, conv_dtype_t out) {
   return in == CONV_DTYPE_F8E4M3 ? out == CONV_DTYPE_BF16 : out == in;
 }
 
-// Fills the tile configuration shared by forward and transposed plans.
-conv_status_t plan_tiles(Plan* pl, conv_dtype_t in, int c_in, int c_out) {
+// Channel block, dtype and instruction kind (shared by forward and transposed plans).
+conv_status_t plan_channels(Plan* pl, conv_dtype_t in, int c_in) {
   int bk = 0;
   uint32_t row_bytes = 0;
   conv_status_t st = channel_block(c_in, elt_bytes(in), &bk, &row_bytes);
   if (st != CONV_OK) return st;
-  int bn = 0, n_tiles = 0;
-  choose_bn(c_out, &bn, &n_tiles);
   ConvKernelParams& kp = pl->kp;
-  kp.bn = bn;
-  kp.n_tiles = n_tiles;
   kp.bk = bk;
   kp.c_blocks = c_in / bk;
   kp.sw_bytes = row_bytes;
-  kp.idesc = make_idesc(in, bn);
-  kp.tmem_cols = next_pow2_cols(2 * bn);
-  const size_t stage_bytes = static_cast<size_t>(kBM + bn) * row_bytes;
-  const size_t fixed = 1024 + 256;
-  int stages = static_cast<int>((kSmemLimit - fixed) / stage_bytes);
-  stages = std::min(stages, kMaxStages);
-  if (stages < 2) return CONV_ERR_NOT_SUPPORTED;
-  kp.stages = stages;
-  pl->smem_bytes = fixed + stages * stage_bytes;
   pl->in_dtype = in;
   pl->out_bf16 = (in != CONV_DTYPE_F16);
   pl->kind = in == CONV_DTYPE_F8E4M3 ? kKindF8 : kKindF16;
   return CONV_OK;
+}
+
+// Tile shape: the C_out tile width bn (a multiple of 16, <= 256) and the tile
+// height (128 rows, or 256 rows as two 128-row MMAs sharing each filter
+// k-block when bn <= 128).  A small cost model from measured TMA behaviour on
+// this part (each load costs about 360 cycles plus bytes / 95 per SM, two
+// producers in flight) and the tensor-core rate picks the shape with the
+// shortest makespan over the persistent grid.
+void choose_tiling(Plan* pl, const long long rows[], int num_phases, int max_kblocks, int c_out,
+                   int num_sms) {
+  ConvKernelParams& kp = pl->kp;
+  const double flop_per_clk = pl->kind == kKindF8 ? 14300.0 : 7150.0;
+  double best = 1e300;
+  int best_bn = 16, best_nt = 1, best_mh = 1;
+  const int nt_min = (c_out + 255) / 256;
+  const int nt_max = std::max(nt_min, std::min((c_out + 15) / 16, nt_min + 8));
+  for (int mh = 2; mh >= 1; --mh) {
+    for (int nt = nt_min; nt <= nt_max; ++nt) {
+      const int per = (c_out + nt - 1) / nt;
+      const int bn = ((per + 15) / 16) * 16;
+      if (bn > 256 || (mh == 2 && bn > 128)) continue;
+      const int nte = (c_out + bn - 1) / bn;
+      long long tiles = 0;
+      for (int ph = 0; ph < num_phases; ++ph) tiles += ((rows[ph] + kBM * mh - 1) / (kBM * mh)) * nte;
+      const long long waves = (tiles + num_sms - 1) / std::max(num_sms, 1);
+      const double a = static_cast<double>(kBM) * mh * kp.sw_bytes;
+      const double b = static_cast<double>(bn) * kp.sw_bytes;
+      const bool res = num_phases == 1 && nte == 1 && max_kblocks * b <= 96.0 * 1024;
+      const double load = (360.0 + a / 95.0) + (res ? 0.0 : 360.0 + b / 95.0);
+      const double mma = 2.0 * kBM * mh * bn * kp.bk / flop_per_clk;
+      const double epi = static_cast<double>(kBM) * mh * bn * 2 / 64.0;
+      const double tile = max_kblocks * std::max(load, mma) + epi;
+      const double cost = waves * tile;
+      if (cost < best * 0.999) {
+        best = cost;
+        best_bn = bn;
+        best_nt = nte;
+        best_mh = mh;
+      }
+    }
+  }
+  kp.bn = best_bn;
+  kp.n_tiles = best_nt;
+  kp.m_halves = best_mh;
+  kp.acc_stride = static_cast<uint32_t>(best_mh * best_bn);
+  kp.tmem_cols = next_pow2_cols(2 * best_mh * best_bn);
+  kp.idesc = make_idesc(pl->in_dtype, best_bn);
 }
 
 struct FwdShape {
@@ -250,9 +290,9 @@ conv_status_t check_fwd_shape(const FwdShape& f, int num_groups) {
   return CONV_OK;
 }
 
-conv_status_t plan_fwd(const FwdShape& f, Plan* pl) {
+conv_status_t plan_fwd(const FwdShape& f, Plan* pl, int num_sms) {
   std::memset(pl, 0, sizeof(*pl));
-  conv_status_t st = plan_tiles(pl, f.in_dtype, f.c_in, f.c_out);
+  conv_status_t st = plan_channels(pl, f.in_dtype, f.c_in);
   if (st != CONV_OK) return st;
   ConvKernelParams& kp = pl->kp;
   kp.num_phases = 1;
@@ -272,7 +312,10 @@ conv_status_t plan_fwd(const FwdShape& f, Plan* pl) {
   kp.out_step_w = 1;
   kp.dil_h = f.dil_h;
   kp.dil_w = f.dil_w;
-  const int m_tiles = (kp.rows[0] + kBM - 1) / kBM;
+  const long long rows[1] = {kp.rows[0]};
+  choose_tiling(pl, rows, 1, f.r * f.s * kp.c_blocks, f.c_out, num_sms);
+  const int tile_m = kBM * kp.m_halves;
+  const int m_tiles = (kp.rows[0] + tile_m - 1) / tile_m;
   kp.tile_start[0] = 0;
   kp.tile_start[1] = m_tiles * kp.n_tiles;
   kp.total_tiles = kp.tile_start[1];
@@ -290,7 +333,7 @@ conv_status_t plan_fwd(const FwdShape& f, Plan* pl) {
 // pad - (S-1)*dil, element strides = conv stride).
 conv_status_t encode_fwd_input(const FwdShape& f, const void* input, Plan* pl) {
   return encode_input_map(&pl->kp.map_a[0], input, f.n, f.h, f.w, f.c_in, f.in_dtype, pl->kp.bk,
-                          pl->kp.sw_bytes, -f.pad_w, -f.pad_h, f.pad_w - (f.s - 1) * f.dil_w,
+                          pl->kp.sw_bytes, kBM * pl->kp.m_halves, -f.pad_w, -f.pad_h, f.pad_w - (f.s - 1) * f.dil_w,
                           f.pad_h - (f.r - 1) * f.dil_h, f.stride_w, f.stride_h);
 }
 
@@ -338,9 +381,9 @@ conv_status_t check_tr_shape(const TrShape& t) {
   return CONV_OK;
 }
 
-conv_status_t plan_transposed(const TrShape& t, Plan* pl) {
+conv_status_t plan_transposed(const TrShape& t, Plan* pl, int num_sms) {
   std::memset(pl, 0, sizeof(*pl));
-  conv_status_t st = plan_tiles(pl, t.in_dtype, t.c_in, t.c_out);
+  conv_status_t st = plan_channels(pl, t.in_dtype, t.c_in);
   if (st != CONV_OK) return st;
   ConvKernelParams& kp = pl->kp;
   pl->sh = t.stride_h;
@@ -348,7 +391,6 @@ conv_status_t plan_transposed(const TrShape& t, Plan* pl) {
   pl->phases_packed = t.stride_h * t.stride_w;
   int kmax = 0;
   int active = 0;
-  int tile = 0;
   for (int a = 0; a < t.stride_h; ++a) {
     const AxisPhase ya = axis_phase(a, t.stride_h, t.pad_h, t.r, t.ho);
     for (int b = 0; b < t.stride_w; ++b) {
@@ -371,13 +413,24 @@ conv_status_t plan_transposed(const TrShape& t, Plan* pl) {
       kp.out_off_h[active] = a;
       kp.out_off_w[active] = b;
       kp.b_index[active] = slot;
-      kp.tile_start[active] = tile;
-      tile += ((kp.rows[active] + kBM - 1) / kBM) * kp.n_tiles;
       ++active;
     }
   }
-  if (kmax == 0) kmax = t.c_in;  // keep the filter map well-formed
+  long long rows[kMaxPhases];
+  int max_kb = 0;
+  for (int ph = 0; ph < active; ++ph) {
+    rows[ph] = kp.rows[ph];
+    max_kb = std::max(max_kb, kp.taps_h[ph] * kp.taps_w[ph] * kp.c_blocks);
+  }
   kp.num_phases = active;
+  choose_tiling(pl, rows, active, max_kb, t.c_out, num_sms);
+  const int tile_m = kBM * kp.m_halves;
+  int tile = 0;
+  for (int ph = 0; ph < active; ++ph) {
+    kp.tile_start[ph] = tile;
+    tile += ((kp.rows[ph] + tile_m - 1) / tile_m) * kp.n_tiles;
+  }
+  if (kmax == 0) kmax = t.c_in;  // keep the filter map well-formed
   kp.tile_start[active] = tile;
   kp.total_tiles = tile;
   kp.step_h = 1;
@@ -403,7 +456,8 @@ conv_status_t encode_tr_inputs(const TrShape& t, const void* input, Plan* pl) {
     const int upper_w = kp.grid_w[ph] - t.w + kp.base_w[ph];
     const int upper_h = kp.grid_h[ph] - t.h + kp.base_h[ph];
     conv_status_t st = encode_input_map(&kp.map_a[ph], input, t.n, t.h, t.w, t.c_in, t.in_dtype,
-                                        kp.bk, kp.sw_bytes, kp.base_w[ph], kp.base_h[ph], upper_w,
+                                        kp.bk, kp.sw_bytes, kBM * kp.m_halves, kp.base_w[ph],
+                                        kp.base_h[ph], upper_w,
                                         upper_h, 1, 1);
     if (st != CONV_OK) return st;
   }
@@ -501,13 +555,220 @@ conv_status_t launch_pack_tr(const Plan& pl, const void* filter, int r, int s, i
   return cudaGetLastError() == cudaSuccess ? CONV_OK : CONV_ERR_CUDA;
 }
 
+// ------------------------------------------------------------------ epilogue + shared memory
+conv_status_t plan_memory_direct(Plan* pl);
+
+conv_status_t encode_out_map_2d(CUtensorMap* map, const void* base, int c_out, long long rows,
+                                conv_dtype_t out_dt, int cw) {
+  const DriverFns* fns = driver_fns();
+  if (!fns) return CONV_ERR_CUDA;
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(c_out), static_cast<cuuint64_t>(rows)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(c_out) * 2};
+  cuuint32_t box[2] = {static_cast<cuuint32_t>(cw), static_cast<cuuint32_t>(kBM)};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = fns->tiled(map, tmap_dtype(out_dt), 2, const_cast<void*>(base), dims, strides, box,
+                          estr, CU_TENSOR_MAP_INTERLEAVE_NONE, tmap_swizzle(cw * 2),
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? CONV_OK : CONV_ERR_CUDA;
+}
+
+// The pixels of one stride phase of the output, as a 4-D tensor
+// [N][grid_h][grid_w][C_out] with strides that skip the other phases.
+conv_status_t encode_out_map_phase(CUtensorMap* map, const void* out, const ConvKernelParams& kp,
+                                   int ph, int n, conv_dtype_t out_dt, int cw) {
+  const DriverFns* fns = driver_fns();
+  if (!fns) return CONV_ERR_CUDA;
+  const cuuint64_t e = 2, C = static_cast<cuuint64_t>(kp.Cout);
+  const uint8_t* base = static_cast<const uint8_t*>(out) +
+                        (static_cast<size_t>(kp.out_off_h[ph]) * kp.Wo + kp.out_off_w[ph]) * C * e;
+  cuuint64_t dims[4] = {C, static_cast<cuuint64_t>(kp.grid_w[ph]),
+                        static_cast<cuuint64_t>(kp.grid_h[ph]), static_cast<cuuint64_t>(n)};
+  cuuint64_t strides[3] = {static_cast<cuuint64_t>(kp.out_step_w) * C * e,
+                           static_cast<cuuint64_t>(kp.out_step_h) * kp.Wo * C * e,
+                           static_cast<cuuint64_t>(kp.Ho) * kp.Wo * C * e};
+  const int bw = kp.grid_w[ph] < kBM ? kp.grid_w[ph] : kBM;
+  cuuint32_t box[4] = {static_cast<cuuint32_t>(cw), static_cast<cuuint32_t>(bw),
+                       static_cast<cuuint32_t>(kBM / bw), 1};
+  cuuint32_t estr[4] = {1, 1, 1, 1};
+  CUresult r = fns->tiled(map, tmap_dtype(out_dt), 4, const_cast<uint8_t*>(base), dims, strides,
+                          box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, tmap_swizzle(cw * 2),
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? CONV_OK : CONV_ERR_CUDA;
+}
+
+uint32_t align1k(size_t v) { return static_cast<uint32_t>((v + 1023) & ~static_cast<size_t>(1023)); }
+
+// Picks the epilogue mode, the filter residency and the ring depth so that
+// everything fits in shared memory, and lays the buffers out.  No driver
+// calls: the TMA maps of the epilogue are encoded afterwards.
+conv_status_t layout_memory(Plan* pl, int has_residual) {
+  ConvKernelParams& kp = pl->kp;
+  // Epilogue mode: TMA tiles need 16-byte output rows; the transposed phase
+  // grids additionally need every 128-row tile to be a rectangle of one image.
+  int mode = 0;
+  if (kp.vec_ok) {
+    if (kp.num_phases == 1 && kp.out_step_h == 1 && kp.out_step_w == 1) {
+      mode = 1;
+    } else {
+      mode = 2;
+      for (int ph = 0; ph < kp.num_phases; ++ph) {
+        const int gw = kp.grid_w[ph], gh = kp.grid_h[ph];
+        const bool rect = (gw % kBM == 0) || (kBM % gw == 0 && gh % (kBM / gw) == 0);
+        if (!rect) mode = 0;
+      }
+    }
+  }
+  if (mode == 0) return plan_memory_direct(pl);
+  int cw = 16;
+  for (int c : {64, 32, 16})
+    if (kp.bn % c == 0) {
+      cw = c;
+      break;
+    }
+  // Two epilogue warpgroups split a tile's (half, chunk) items: make at least two.
+  if (kp.m_halves * (kp.bn / cw) < kEpilogueGroups && cw > 16) cw /= 2;
+  const uint32_t a_bytes = kBM * kp.m_halves * kp.sw_bytes;
+  const uint32_t b_bytes = static_cast<uint32_t>(kp.bn) * kp.sw_bytes;
+  const bool can_res = kp.num_phases == 1 && kp.n_tiles == 1;
+  const size_t bres = can_res ? static_cast<size_t>(kp.taps_h[0]) * kp.taps_w[0] * kp.c_blocks * b_bytes : 0;
+  const size_t src_tile = static_cast<size_t>(kBM) * kp.m_halves * kp.bn * 2;
+  const size_t chunk = static_cast<size_t>(kBM) * cw * 2;
+  const size_t bar_bytes = 1024;
+  struct Opt { bool res; int srcb, stgb; };
+  Opt opts[12];
+  int nopt = 0;
+  const int srcb_max = has_residual ? 2 : 0;
+  // With a residual the outputs are written in place into the source tile
+  // buffer and stored from there: no staging buffers.
+  const int stg_max = has_residual ? 0 : 2;
+  const int stg_min = has_residual ? 0 : 1;
+  for (int res = can_res ? 1 : 0; res >= 0; --res)
+    for (int srcb = srcb_max; srcb >= (srcb_max ? 1 : 0); --srcb)
+      for (int stgb = stg_max; stgb >= stg_min; --stgb) opts[nopt++] = Opt{res != 0, srcb, stgb};
+  // Rank the options: at least 3 ring stages; then the cheapest k-block
+  // (a resident filter saves one TMA load per k-block); then a prefetched
+  // residual source; then deeper rings.
+  int best = -1, best_stages = 0;
+  double best_key = 1e300;
+  for (int i = 0; i < nopt; ++i) {
+    const size_t used = 1024 + bar_bytes + (opts[i].res ? align1k(bres) : 0) +
+                        opts[i].srcb * align1k(src_tile) +
+                        kEpilogueGroups * opts[i].stgb * align1k(chunk);
+    const size_t stage = a_bytes + (opts[i].res ? 0 : b_bytes);
+    if (used + 2 * stage > kSmemLimit) continue;
+    const int st = static_cast<int>(std::min<size_t>(kMaxStages, (kSmemLimit - used) / stage));
+    const double load = (360.0 + a_bytes / 95.0) + (opts[i].res ? 0.0 : 360.0 + b_bytes / 95.0);
+    double key = load;
+    if (st < 3) key += 1e6;
+    if (opts[i].srcb < srcb_max) key += 50.0;
+    key -= 0.01 * st;
+    if (key < best_key) {
+      best_key = key;
+      best = i;
+      best_stages = st;
+    }
+  }
+  if (best < 0) return plan_memory_direct(pl);
+  const Opt o = opts[best];
+  kp.epi_mode = mode;
+  kp.cw = cw;
+  kp.b_resident = o.res ? 1 : 0;
+  kp.src_bufs = o.srcb;
+  kp.stg_bufs = o.stgb;
+  kp.stages = best_stages;
+  uint32_t off = 0;
+  kp.off_a = off;
+  off += align1k(static_cast<size_t>(best_stages) * a_bytes);
+  kp.off_b = off;
+  if (!o.res) off += align1k(static_cast<size_t>(best_stages) * b_bytes);
+  kp.off_bres = off;
+  if (o.res) off += align1k(bres);
+  kp.off_src = off;
+  off += o.srcb * align1k(src_tile);
+  kp.off_stg = off;
+  off += kEpilogueGroups * o.stgb * align1k(chunk);
+  kp.off_bar = off;
+  off += bar_bytes;
+  pl->smem_bytes = off + 1024;
+  return CONV_OK;
+}
+
+// Encodes the epilogue's output / source maps; falls back to the direct
+// epilogue if the driver rejects one of them.
+conv_status_t plan_memory(Plan* pl, int n_images, const void* output, const void* source,
+                          int has_residual) {
+  conv_status_t st = layout_memory(pl, has_residual);
+  if (st != CONV_OK) return st;
+  ConvKernelParams& kp = pl->kp;
+  const conv_dtype_t out_dt = pl->out_bf16 ? CONV_DTYPE_BF16 : CONV_DTYPE_F16;
+  if (kp.epi_mode == 1) {
+    const long long rows = kp.rows[0];
+    if (encode_out_map_2d(&kp.map_out[0], output, kp.Cout, rows, out_dt, kp.cw) != CONV_OK ||
+        (has_residual &&
+         encode_out_map_2d(&kp.map_src[0], source, kp.Cout, rows, out_dt, kp.cw) != CONV_OK))
+      return plan_memory_direct(pl);
+  } else if (kp.epi_mode == 2) {
+    for (int ph = 0; ph < kp.num_phases; ++ph)
+      if (encode_out_map_phase(&kp.map_out[ph], output, kp, ph, n_images, out_dt, kp.cw) != CONV_OK ||
+          (has_residual &&
+           encode_out_map_phase(&kp.map_src[ph], source, kp, ph, n_images, out_dt, kp.cw) != CONV_OK))
+        return plan_memory_direct(pl);
+  }
+  return CONV_OK;
+}
+
+// Direct-store epilogue: only the operand ring (and possibly the resident filter).
+conv_status_t plan_memory_direct(Plan* pl) {
+  ConvKernelParams& kp = pl->kp;
+  const uint32_t a_bytes = kBM * kp.m_halves * kp.sw_bytes;
+  const uint32_t b_bytes = static_cast<uint32_t>(kp.bn) * kp.sw_bytes;
+  const size_t bar_bytes = 1024;
+  kp.epi_mode = 0;
+  kp.cw = 16;
+  kp.src_bufs = 0;
+  kp.stg_bufs = 0;
+  const bool can_res = kp.num_phases == 1 && kp.n_tiles == 1;
+  const size_t bres = can_res ? static_cast<size_t>(kp.taps_h[0]) * kp.taps_w[0] * kp.c_blocks * b_bytes : 0;
+  bool res = false;
+  int stages = 0;
+  if (can_res) {
+    const size_t used = 1024 + bar_bytes + align1k(bres);
+    if (used + 4 * static_cast<size_t>(a_bytes) <= kSmemLimit) {
+      res = true;
+      stages = static_cast<int>(std::min<size_t>(kMaxStages, (kSmemLimit - used) / a_bytes));
+    }
+  }
+  if (!res) {
+    const size_t used = 1024 + bar_bytes;
+    stages = static_cast<int>(std::min<size_t>(kMaxStages, (kSmemLimit - used) / (a_bytes + b_bytes)));
+    if (stages < 2) return CONV_ERR_NOT_SUPPORTED;
+  }
+  kp.b_resident = res ? 1 : 0;
+  kp.stages = stages;
+  uint32_t off = 0;
+  kp.off_a = 0;
+  off += align1k(static_cast<size_t>(stages) * a_bytes);
+  kp.off_b = off;
+  if (!res) off += align1k(static_cast<size_t>(stages) * b_bytes);
+  kp.off_bres = off;
+  if (res) off += align1k(bres);
+  kp.off_src = off;
+  kp.off_stg = off;
+  kp.off_bar = off;
+  off += bar_bytes;
+  pl->smem_bytes = off + 1024;
+  return CONV_OK;
+}
+
 // ------------------------------------------------------------------ launch
-conv_status_t finish_and_launch(Plan* pl, const void* packed, void* output, int has_residual,
-                                const void* source, float beta, conv_epilogue_t epilogue,
-                                void* workspace, cudaStream_t stream) {
+conv_status_t finish_and_launch(Plan* pl, int n_images, const void* packed, void* output,
+                                int has_residual, const void* source, float beta,
+                                conv_epilogue_t epilogue, void* workspace, cudaStream_t stream) {
   ConvKernelParams& kp = pl->kp;
   conv_status_t st = encode_filter_map(&kp.map_b, packed, pl->kmax, kp.Cout, pl->phases_packed,
                                        pl->in_dtype, kp.bk, kp.bn, kp.sw_bytes);
+  if (st != CONV_OK) return st;
+  st = plan_memory(pl, n_images, output, has_residual ? source : nullptr, has_residual);
   if (st != CONV_OK) return st;
   kp.has_residual = has_residual ? 1 : 0;
   kp.src = has_residual ? source : nullptr;
@@ -516,7 +777,7 @@ conv_status_t finish_and_launch(Plan* pl, const void* packed, void* output, int 
   kp.out = output;
   kp.status = static_cast<unsigned int*>(workspace);
   const unsigned long long tmo = g_timeout_ns.load(std::memory_order_relaxed);
-  kp.timeout_ns = tmo ? tmo : kDefaultTimeoutNs;
+  kp.timeout_cycles = ns_to_cycles(tmo ? tmo : kDefaultTimeoutNs);
   kp.fault_mode = g_fault_mode.load(std::memory_order_relaxed);
   if (kp.total_tiles == 0) return CONV_OK;
   const int sms = device_sm_count();
@@ -577,11 +838,18 @@ conv_status_t fwd_impl(const void* input, const FwdShape& f, const void* filter,
   if (!epilogue_ok(epilogue)) return CONV_ERR_INVALID_VALUE;
   st = check_fwd_shape(f, num_groups);
   if (st != CONV_OK) return st;
-  Plan pl;
-  st = plan_fwd(f, &pl);
+  int bk = 0;
+  uint32_t row_bytes = 0;
+  st = channel_block(f.c_in, elt_bytes(f.in_dtype), &bk, &row_bytes);
   if (st != CONV_OK) return st;
-  const size_t need = CONV_STATUS_BYTES + (prepacked ? 0 : round_up_256(pl.packed_bytes));
+  const size_t packed_bytes = conv2d_packed_filter_bytes(f.r, f.s, f.c_in, f.c_out, f.in_dtype);
+  const size_t need = CONV_STATUS_BYTES + (prepacked ? 0 : round_up_256(packed_bytes));
   if (workspace_bytes < need) return CONV_ERR_WORKSPACE_TOO_SMALL;
+  const int sms = device_sm_count();
+  if (sms <= 0) return CONV_ERR_CUDA;
+  Plan pl;
+  st = plan_fwd(f, &pl, sms);
+  if (st != CONV_OK) return st;
   st = encode_fwd_input(f, input, &pl);
   if (st != CONV_OK) return st;
   const void* packed = filter;
@@ -591,8 +859,8 @@ conv_status_t fwd_impl(const void* input, const FwdShape& f, const void* filter,
     if (st != CONV_OK) return st;
     packed = dst;
   }
-  return finish_and_launch(&pl, packed, output, has_residual, source, beta, epilogue, workspace,
-                           stream);
+  return finish_and_launch(&pl, f.n, packed, output, has_residual, source, beta, epilogue,
+                           workspace, stream);
 }
 
 conv_status_t tr_impl(const void* input, const TrShape& t, const void* filter, bool prepacked,
@@ -604,11 +872,21 @@ conv_status_t tr_impl(const void* input, const TrShape& t, const void* filter, b
   if (!epilogue_ok(epilogue)) return CONV_ERR_INVALID_VALUE;
   st = check_tr_shape(t);
   if (st != CONV_OK) return st;
-  Plan pl;
-  st = plan_transposed(t, &pl);
+  int bk = 0;
+  uint32_t row_bytes = 0;
+  st = channel_block(t.c_in, elt_bytes(t.in_dtype), &bk, &row_bytes);
   if (st != CONV_OK) return st;
-  const size_t need = CONV_STATUS_BYTES + (prepacked ? 0 : round_up_256(pl.packed_bytes));
+  const int st_hw[2] = {t.stride_h, t.stride_w};
+  const int pad_hw[2] = {t.pad_h, t.pad_w};
+  const size_t packed_bytes =
+      conv_transposed_packed_filter_bytes(t.r, t.s, t.c_in, t.c_out, st_hw, pad_hw, t.in_dtype);
+  const size_t need = CONV_STATUS_BYTES + (prepacked ? 0 : round_up_256(packed_bytes));
   if (workspace_bytes < need) return CONV_ERR_WORKSPACE_TOO_SMALL;
+  const int sms = device_sm_count();
+  if (sms <= 0) return CONV_ERR_CUDA;
+  Plan pl;
+  st = plan_transposed(t, &pl, sms);
+  if (st != CONV_OK) return st;
   st = encode_tr_inputs(t, input, &pl);
   if (st != CONV_OK) return st;
   const void* packed = filter;
@@ -618,8 +896,8 @@ conv_status_t tr_impl(const void* input, const TrShape& t, const void* filter, b
     if (st != CONV_OK) return st;
     packed = dst;
   }
-  return finish_and_launch(&pl, packed, output, has_residual, source, beta, epilogue, workspace,
-                           stream);
+  return finish_and_launch(&pl, t.n, packed, output, has_residual, source, beta, epilogue,
+                           workspace, stream);
 }
 
 }  // namespace
@@ -803,7 +1081,8 @@ void conv_testing_set_wait_fault(int mode, unsigned long long timeout_ns) {
 
 conv_status_t conv_testing_fwd_plan(int n, int h, int w, int c_in, conv_dtype_t dtype, int r,
                                     int s, int c_out, const int stride[2],
-                                    const int symmetric_padding[2], int num_sms, int out[7]) {
+                                    const int symmetric_padding[2], int has_residual, int num_sms,
+                                    int out[11]) {
   if (!stride || !symmetric_padding || !out) return CONV_ERR_INVALID_VALUE;
   const int dil[2] = {1, 1};
   const conv_dtype_t out_dt = dtype == CONV_DTYPE_F8E4M3 ? CONV_DTYPE_BF16 : dtype;
@@ -815,7 +1094,9 @@ conv_status_t conv_testing_fwd_plan(int n, int h, int w, int c_in, conv_dtype_t 
   conv_status_t st = check_fwd_shape(f, 1);
   if (st != CONV_OK) return st;
   Plan pl;
-  st = plan_fwd(f, &pl);
+  st = plan_fwd(f, &pl, num_sms);
+  if (st != CONV_OK) return st;
+  st = layout_memory(&pl, has_residual);
   if (st != CONV_OK) return st;
   out[0] = pl.kp.bn;
   out[1] = pl.kp.bk;
@@ -824,6 +1105,10 @@ conv_status_t conv_testing_fwd_plan(int n, int h, int w, int c_in, conv_dtype_t 
   out[4] = pl.kp.total_tiles;
   out[5] = std::min(pl.kp.total_tiles, num_sms);
   out[6] = static_cast<int>(pl.kp.tmem_cols);
+  out[7] = pl.kp.epi_mode;
+  out[8] = pl.kp.b_resident;
+  out[9] = pl.kp.src_bufs;
+  out[10] = pl.kp.stg_bufs;
   return CONV_OK;
 }
 
@@ -845,8 +1130,9 @@ conv_status_t conv_testing_im2col_tile(const void* input, int n, int h, int w, i
   conv_status_t st = check_fwd_shape(f, 1);
   if (st != CONV_OK) return st;
   Plan pl;
-  st = plan_fwd(f, &pl);
+  st = plan_fwd(f, &pl, 1);
   if (st != CONV_OK) return st;
+  pl.kp.m_halves = 1;  // the probe copies out one 128-row column
   if (m0 < 0 || m0 >= pl.kp.rows[0] || tap_r < 0 || tap_r >= r || tap_s < 0 || tap_s >= s ||
       c0 < 0 || c0 >= c_in || c0 % pl.kp.bk != 0)
     return CONV_ERR_INVALID_VALUE;
@@ -865,7 +1151,7 @@ conv_status_t conv_testing_im2col_tile(const void* input, int n, int h, int w, i
   cudaError_t e = launch_im2col_probe(pl.kp.map_a[0], c0, w0, h0, n_img, tap_s, tap_r,
                                       pl.kp.sw_bytes, out_tile,
                                       static_cast<unsigned int*>(status_workspace),
-                                      tmo ? tmo : kDefaultTimeoutNs, cs);
+                                      ns_to_cycles(tmo ? tmo : kDefaultTimeoutNs), cs);
   if (e != cudaSuccess) return CONV_ERR_CUDA;
   return cudaStreamSynchronize(cs) == cudaSuccess ? CONV_OK : CONV_ERR_CUDA;
 }

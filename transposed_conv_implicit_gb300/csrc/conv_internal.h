@@ -14,6 +14,6 @@ cudaError_t launch_conv_igemm(int kind, bool out_bf16, const ConvKernelParams& p
 // One TMA im2col load into shared memory, copied out un-swizzled (test hook).
 cudaError_t launch_im2col_probe(const CUtensorMap& map, int c, int w, int h, int n, int off_w,
                                 int off_h, uint32_t row_bytes, void* out, unsigned int* status,
-                                unsigned long long limit_ns, cudaStream_t stream);
+                                long long limit_cycles, cudaStream_t stream);
 
 }  // namespace convgb300

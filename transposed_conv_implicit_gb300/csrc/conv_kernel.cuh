@@ -7,15 +7,21 @@
 // (the im2col matrix) is never materialised: each 128-pixel x (one filter tap,
 // bk channels) block is fetched straight from the NHWC input by a TMA im2col
 // load, with the hardware zero-filling pixels that fall in the padding.  The B
-// operand is the filter pre-packed once into a K-major [C_out][K] matrix.
+// operand is the filter pre-packed once into a K-major [C_out][K] matrix; when
+// it fits, it is loaded into shared memory once per CTA and kept there.
 //
 // Warp roles (192 threads, one persistent CTA per SM):
-//   warp 0      TMA producer: one elected lane streams (A, B) k-blocks into an
-//               S-stage shared-memory ring guarded by full/empty mbarriers;
+//   warp 0      TMA producer: one elected lane streams A (and B unless it is
+//               resident) k-blocks into an S-stage shared-memory ring guarded
+//               by full/empty mbarriers;
 //   warp 1      TMEM owner and MMA issuer: one lane issues tcgen05.mma
 //               (M=128, N=bn) into a double-buffered fp32 TMEM accumulator;
 //   warps 2-5   epilogue: tcgen05.ld the accumulator, add beta*source, apply
 //               the activation, round once to the output dtype and store.
+//               With a TMA epilogue the residual source tile is prefetched by
+//               TMA one tile ahead into swizzled shared memory, and results are
+//               staged in swizzled shared memory and written by TMA stores
+//               (which also clip the ragged M tail and the C_out edge tile).
 // Every wait is bounded in time; on expiry the CTA records a status bit,
 // stops, lets in-flight copies and MMAs land, frees TMEM and returns.
 #pragma once
@@ -42,9 +48,19 @@ __device__ __forceinline__ TileInfo decode_tile(const ConvKernelParams& p, int t
   TileInfo ti;
   ti.phase = ph;
   ti.n0 = (local % p.n_tiles) * p.bn;
-  ti.m0 = (local / p.n_tiles) * kBM;
+  ti.m0 = (local / p.n_tiles) * (kBM * p.m_halves);
   ti.kblocks = p.taps_h[ph] * p.taps_w[ph] * p.c_blocks;
   return ti;
+}
+
+// (image, grid row, grid column) of GEMM row m in phase ph.
+__device__ __forceinline__ void grid_pos(const ConvKernelParams& p, int ph, int m, int& n_img,
+                                         int& j, int& i) {
+  const int hw = p.grid_h[ph] * p.grid_w[ph];
+  n_img = m / hw;
+  const int rem = m - n_img * hw;
+  j = rem / p.grid_w[ph];
+  i = rem - j * p.grid_w[ph];
 }
 
 template <typename T>
@@ -69,11 +85,24 @@ __device__ __forceinline__ __half from_f32<__half>(float v) {
   return __float2half_rn(v);
 }
 
-// v = acc (+ beta*source); v = act(v); one round-to-nearest-even to OutT.
-// `nvalid` < 16 masks the columns beyond C_out (the edge tile).
+__device__ __forceinline__ float activation(float v, int epilogue) {
+  if (epilogue == kEpiRelu) return fmaxf(v, 0.0f);
+  if (epilogue == kEpiSilu) return v / (1.0f + __expf(-v));
+  return v;
+}
+
+// Byte offset of 16-byte piece q of row r in a [rows][row_bytes] tile stored
+// with the TMA swizzle whose span equals row_bytes (32, 64 or 128): the
+// piece index is XOR-ed with address bits 7 and up.
+__device__ __forceinline__ uint32_t swizzled_offset(uint32_t r, uint32_t q, uint32_t row_bytes) {
+  const uint32_t lin = r * row_bytes + q * 16;
+  return lin ^ (((lin >> 7) & (row_bytes / 16 - 1)) << 4);
+}
+
+// Direct-store epilogue for 16 columns (used when no TMA store map applies).
 template <typename OutT>
-__device__ __forceinline__ void epilogue_16(const ConvKernelParams& p, long long off,
-                                            const uint32_t (&acc)[16], int nvalid) {
+__device__ __forceinline__ void epilogue_16_direct(const ConvKernelParams& p, long long off,
+                                                   const uint32_t (&acc)[16], int nvalid) {
   float f[16];
 #pragma unroll
   for (int j = 0; j < 16; ++j) f[j] = __uint_as_float(acc[j]);
@@ -93,13 +122,8 @@ __device__ __forceinline__ void epilogue_16(const ConvKernelParams& p, long long
         if (j < nvalid) f[j] += p.beta * to_f32<OutT>(src[j]);
     }
   }
-  if (p.epilogue == kEpiRelu) {
 #pragma unroll
-    for (int j = 0; j < 16; ++j) f[j] = fmaxf(f[j], 0.0f);
-  } else if (p.epilogue == kEpiSilu) {
-#pragma unroll
-    for (int j = 0; j < 16; ++j) f[j] = f[j] / (1.0f + __expf(-f[j]));
-  }
+  for (int j = 0; j < 16; ++j) f[j] = activation(f[j], p.epilogue);
   OutT* dst = static_cast<OutT*>(p.out) + off;
   if (full_vec) {
     uint4 raw[2];
@@ -115,6 +139,128 @@ __device__ __forceinline__ void epilogue_16(const ConvKernelParams& p, long long
   }
 }
 
+// Issues the TMA loads of the residual-source chunks that epilogue group
+// `grp` owns in one tile: work item q = h * nchunks + c (128-row half h,
+// column chunk c) belongs to group q % 2.  The buffer is laid out
+// [half][chunk][128][cw]; completion is tracked by `bar`.
+__device__ __forceinline__ void issue_source_items(const ConvKernelParams& p, const TileInfo& ti,
+                                                   uint8_t* buf, uint32_t bar, int grp) {
+  const uint32_t chunk_bytes = kBM * p.cw * 2;
+  const int nchunks = p.bn / p.cw;
+  const int nitems = nchunks * p.m_halves;
+  const int mine = (nitems - grp + kEpilogueGroups - 1) / kEpilogueGroups;
+  if (mine <= 0) return;
+  mbar_arrive_expect_tx(bar, chunk_bytes * mine);
+  for (int q = grp; q < nitems; q += kEpilogueGroups) {
+    const int h = q / nchunks;
+    const int c = q - h * nchunks;
+    const int mh = ti.m0 + h * kBM;
+    const uint32_t dst = smem_u32(buf + q * chunk_bytes);
+    if (p.epi_mode == 1) {
+      tma_load_2d(dst, &p.map_src[ti.phase], bar, ti.n0 + c * p.cw, mh);
+    } else {
+      int n_img, j, i;
+      grid_pos(p, ti.phase, mh, n_img, j, i);
+      tma_load_4d(dst, &p.map_src[ti.phase], bar, ti.n0 + c * p.cw, i, j, n_img);
+    }
+  }
+}
+
+// Issues the MMAs of one k-block: kSteps K-steps of 32 bytes per operand row,
+// kHalves 128-row halves of A sharing the B operand.  Descriptors are built
+// from precomputed high bits plus an address field advanced by adds only: the
+// issuing thread is latency-bound, so nothing here divides or branches.
+template <int kKind, int kSteps, int kHalves>
+__device__ __forceinline__ void issue_kblock(uint32_t d_tmem, uint64_t desc_hi, uint32_t a_lo,
+                                             uint32_t b_lo, uint32_t half_lo, uint32_t bn_cols,
+                                             uint32_t idesc, uint32_t first_accumulate) {
+#pragma unroll
+  for (int kk = 0; kk < kSteps; ++kk) {
+    const uint64_t bdesc = desc_hi | static_cast<uint64_t>(b_lo + 2u * kk);
+    const uint32_t accumulate = kk == 0 ? first_accumulate : 1u;
+#pragma unroll
+    for (int h = 0; h < kHalves; ++h) {
+      const uint64_t adesc = desc_hi | static_cast<uint64_t>(a_lo + h * half_lo + 2u * kk);
+      if (kKind == kKindF16)
+        mma_f16(d_tmem + h * bn_cols, adesc, bdesc, idesc, accumulate);
+      else
+        mma_f8(d_tmem + h * bn_cols, adesc, bdesc, idesc, accumulate);
+    }
+  }
+}
+
+// The MMA role for one (kSteps, kHalves) specialisation.
+template <int kKind, int kSteps, int kHalves>
+__device__ __forceinline__ bool mma_role(const ConvKernelParams& p, uint32_t tmem_base,
+                                         uint8_t* a_ring, uint8_t* b_ring, uint8_t* b_res,
+                                         uint64_t* full, uint64_t* empty, uint64_t* tfull,
+                                         uint64_t* tempty, uint64_t* bres_full,
+                                         volatile int* abort_flag, unsigned int* status,
+                                         long long limit) {
+  const int stages = p.stages;
+  const uint32_t sw = p.sw_bytes;
+  const uint32_t a_bytes = kBM * kHalves * sw;
+  const uint32_t b_bytes = static_cast<uint32_t>(p.bn) * sw;
+  const uint64_t desc_hi = smem_desc_kmajor(0, sw);  // address field zero
+  const uint32_t a_lo0 = smem_u32(a_ring) >> 4;
+  const uint32_t b_lo0 = smem_u32(p.b_resident ? b_res : b_ring) >> 4;
+  const uint32_t a_step = a_bytes >> 4;
+  const uint32_t b_step = b_bytes >> 4;
+  const uint32_t half_lo = (kBM * sw) >> 4;
+  const uint32_t bn_cols = static_cast<uint32_t>(p.bn);
+  const uint32_t idesc = p.idesc;
+  const uint32_t full0 = smem_u32(full), empty0 = smem_u32(empty);
+  int stage = 0;
+  uint32_t phase = 0;
+  uint32_t a_lo = a_lo0;
+  uint32_t bs_lo = b_lo0;  // streamed B: advances with the ring
+  bool ok = true;
+  int it = 0;
+  if (p.b_resident && p.total_tiles > static_cast<int>(blockIdx.x)) {
+    ok = mbar_wait_bounded(smem_u32(bres_full), 0, abort_flag, status, kStatusMmaTimeout, limit);
+    tc_fence_after();
+  }
+  for (int t = blockIdx.x; ok && t < p.total_tiles; t += gridDim.x, ++it) {
+    const TileInfo ti = decode_tile(p, t);
+    const int acc = it & 1;
+    if (!mbar_wait_bounded(smem_u32(&tempty[acc]), static_cast<uint32_t>(((it >> 1) & 1) ^ 1),
+                           abort_flag, status, kStatusMmaTimeout, limit)) {
+      ok = false;
+      break;
+    }
+    tc_fence_after();
+    if (ti.kblocks == 0) {  // a phase with no filter taps: the epilogue writes act(0)
+      mbar_arrive(smem_u32(&tfull[acc]));
+      continue;
+    }
+    const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc) * p.acc_stride;
+    uint32_t br_lo = b_lo0;  // resident B: restarts every tile
+    for (int kb = 0; kb < ti.kblocks; ++kb) {
+      if (!mbar_wait_bounded(full0 + 8u * stage, phase, abort_flag, status, kStatusMmaTimeout,
+                             limit)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      issue_kblock<kKind, kSteps, kHalves>(d_tmem, desc_hi, a_lo, p.b_resident ? br_lo : bs_lo,
+                                           half_lo, bn_cols, idesc, kb != 0 ? 1u : 0u);
+      mma_commit(empty0 + 8u * stage);
+      br_lo += b_step;
+      a_lo += a_step;
+      bs_lo += b_step;
+      if (++stage == stages) {
+        stage = 0;
+        phase ^= 1u;
+        a_lo = a_lo0;
+        bs_lo = b_lo0;
+      }
+    }
+    if (!ok) break;
+    mma_commit(smem_u32(&tfull[acc]));
+  }
+  return ok;
+}
+
 template <int kKind, typename OutT>
 __global__ void __launch_bounds__(kThreads, 1)
     conv_igemm_kernel(const __grid_constant__ ConvKernelParams p) {
@@ -125,21 +271,26 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int lane = threadIdx.x & 31;
   const int stages = p.stages;
   const uint32_t sw = p.sw_bytes;
-  const uint32_t a_bytes = kBM * sw;
+  const uint32_t a_bytes = kBM * p.m_halves * sw;
   const uint32_t b_bytes = static_cast<uint32_t>(p.bn) * sw;
 
-  uint8_t* a_base = smem;
-  uint8_t* b_base = smem + stages * a_bytes;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(b_base + stages * b_bytes);
+  uint8_t* a_ring = smem + p.off_a;
+  uint8_t* b_ring = smem + p.off_b;
+  uint8_t* b_res = smem + p.off_bres;
+  uint8_t* src_base = smem + p.off_src;
+  uint8_t* stg_base = smem + p.off_stg;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + p.off_bar);
   uint64_t* full = bars;
   uint64_t* empty = bars + stages;
   uint64_t* tfull = bars + 2 * stages;
   uint64_t* tempty = tfull + 2;
   uint64_t* drain = tempty + 2;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  uint64_t* bres_full = drain + 1;
+  uint64_t* src_full = bres_full + 1;  // [buffer][group]
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(src_full + 4);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   unsigned int* status = p.status;
-  const uint64_t limit = p.timeout_ns;
+  const long long limit = p.timeout_cycles;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < stages; ++s) {
@@ -149,8 +300,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int a = 0; a < 2; ++a) {
       mbar_init(smem_u32(&tfull[a]), 1);
       mbar_init(smem_u32(&tempty[a]), kEpilogueWarps);
+      mbar_init(smem_u32(&src_full[2 * a]), 1);
+      mbar_init(smem_u32(&src_full[2 * a + 1]), 1);
     }
     mbar_init(smem_u32(drain), 1);
+    mbar_init(smem_u32(bres_full), 1);
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -166,116 +320,93 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
-  const uint32_t acc_cols = p.tmem_cols / 2;
 
-  if (warp == 0) {
-    // ------------------------------------------------------------ producer
+  if (warp == 0 || warp == kThreads / 32 - 1) {
+    // ------------------------------------------------------------ producers
+    // Two producer warps walk the same k-block sequence; k-block `seq` is
+    // issued by producer (seq & 1), so two TMA issue streams overlap.
     if (lane == 0) {
+      const int role = warp == 0 ? 0 : 1;
       int stage = 0;
       uint32_t phase = 0;
-      long long issued = 0;
+      long long seq = 0;
+      long long last_issued = -1;
       bool ok = true;
+      if (p.b_resident && role == 0) {
+        // The whole packed filter of the single phase / n-tile, once.
+        const int kbs = p.taps_h[0] * p.taps_w[0] * p.c_blocks;
+        const uint32_t bb = smem_u32(bres_full);
+        mbar_arrive_expect_tx(bb, b_bytes * kbs);
+        for (int kb = 0; kb < kbs; ++kb)
+          tma_load_3d(smem_u32(b_res + kb * b_bytes), &p.map_b, bb, kb * p.bk, 0, p.b_index[0]);
+      }
+      const uint32_t stage_tx = a_bytes + (p.b_resident ? 0u : b_bytes);
       for (int t = blockIdx.x; t < p.total_tiles && ok; t += gridDim.x) {
         const TileInfo ti = decode_tile(p, t);
         const int ph = ti.phase;
-        const int hw = p.grid_h[ph] * p.grid_w[ph];
-        const int n_img = ti.m0 / hw;
-        const int rem = ti.m0 - n_img * hw;
-        const int j = rem / p.grid_w[ph];
-        const int i = rem - j * p.grid_w[ph];
+        int n_img, j, i;
+        grid_pos(p, ph, ti.m0, n_img, j, i);
         const int h0 = p.base_h[ph] + j * p.step_h;
         const int w0 = p.base_w[ph] + i * p.step_w;
         const int tw = p.taps_w[ph];
-        for (int kb = 0; kb < ti.kblocks; ++kb) {
-          const int tap = kb / p.c_blocks;
-          const int cb = kb - tap * p.c_blocks;
-          const int uh = tap / tw;
-          const int uw = tap - uh * tw;
-          if (!mbar_wait_bounded(smem_u32(&empty[stage]), phase ^ 1u, abort_flag, status,
-                                 kStatusProducerTimeout, limit)) {
-            ok = false;
-            break;
-          }
-          if (p.fault_mode == 1 && blockIdx.x == 0 && issued == 0) {
-            // Test hook: leave this stage un-armed; its consumer can only time out.
-            ++issued;
-            if (++stage == stages) {
-              stage = 0;
-              phase ^= 1u;
+        const CUtensorMap* amap = &p.map_a[ph];
+        const int bz = p.b_index[ph];
+        int cb = 0, uw = 0, uh = 0;
+        for (int kb = 0; kb < ti.kblocks; ++kb, ++seq) {
+          if ((seq & 1) == role) {
+            if (!mbar_wait_bounded(smem_u32(&empty[stage]), phase ^ 1u, abort_flag, status,
+                                   kStatusProducerTimeout, limit)) {
+              ok = false;
+              break;
             }
-            continue;
+            last_issued = seq;
+            if (!(p.fault_mode == 1 && blockIdx.x == 0 && seq == 0)) {
+              // (fault_mode 1, a test hook: CTA 0 leaves its first stage un-armed.)
+              const uint32_t fb = smem_u32(&full[stage]);
+              mbar_arrive_expect_tx(fb, stage_tx);
+              tma_load_im2col_4d(smem_u32(a_ring + stage * a_bytes), amap, fb, cb * p.bk, w0, h0,
+                                 n_img, static_cast<uint16_t>(uw * p.dil_w),
+                                 static_cast<uint16_t>(uh * p.dil_h));
+              if (!p.b_resident)
+                tma_load_3d(smem_u32(b_ring + stage * b_bytes), &p.map_b, fb, kb * p.bk, ti.n0, bz);
+            }
           }
-          const uint32_t fb = smem_u32(&full[stage]);
-          mbar_arrive_expect_tx(fb, a_bytes + b_bytes);
-          tma_load_im2col_4d(smem_u32(a_base + stage * a_bytes), &p.map_a[ph], fb, cb * p.bk, w0,
-                             h0, n_img, static_cast<uint16_t>(uw * p.dil_w),
-                             static_cast<uint16_t>(uh * p.dil_h));
-          tma_load_3d(smem_u32(b_base + stage * b_bytes), &p.map_b, fb, kb * p.bk, ti.n0,
-                      p.b_index[ph]);
-          ++issued;
           if (++stage == stages) {
             stage = 0;
             phase ^= 1u;
           }
+          if (++cb == p.c_blocks) {
+            cb = 0;
+            if (++uw == tw) {
+              uw = 0;
+              ++uh;
+            }
+          }
         }
       }
       if (!ok) {
-        // Let every copy still in flight land before the CTA exits.
-        const long long first = issued > stages ? issued - stages : 0;
-        for (long long q = first; q < issued; ++q)
-          mbar_wait_drain(smem_u32(&full[q % stages]), static_cast<uint32_t>((q / stages) & 1),
-                          limit / 8 + 1);
+        // Let every copy this producer still has in flight land before exiting.
+        for (long long q = last_issued - stages + 1; q <= last_issued; ++q)
+          if (q >= 0 && (q & 1) == role)
+            mbar_wait_drain(smem_u32(&full[q % stages]), static_cast<uint32_t>((q / stages) & 1),
+                            limit / 8 + 1);
+        if (p.b_resident && role == 0) mbar_wait_drain(smem_u32(bres_full), 0, limit / 8 + 1);
       }
     }
     __syncwarp();
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      int stage = 0;
-      uint32_t phase = 0;
-      bool ok = true;
-      int it = 0;
-      for (int t = blockIdx.x; t < p.total_tiles; t += gridDim.x, ++it) {
-        const TileInfo ti = decode_tile(p, t);
-        const int acc = it & 1;
-        if (!mbar_wait_bounded(smem_u32(&tempty[acc]), static_cast<uint32_t>(((it >> 1) & 1) ^ 1),
-                               abort_flag, status, kStatusMmaTimeout, limit)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        if (ti.kblocks == 0) {  // a phase with no filter taps: the epilogue writes act(0)
-          mbar_arrive(smem_u32(&tfull[acc]));
-          continue;
-        }
-        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc) * acc_cols;
-        for (int kb = 0; kb < ti.kblocks; ++kb) {
-          if (!mbar_wait_bounded(smem_u32(&full[stage]), phase, abort_flag, status,
-                                 kStatusMmaTimeout, limit)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          const uint32_t a_addr = smem_u32(a_base + stage * a_bytes);
-          const uint32_t b_addr = smem_u32(b_base + stage * b_bytes);
-          for (uint32_t kk = 0; kk < sw / 32; ++kk) {
-            const uint64_t adesc = smem_desc_kmajor(a_addr + kk * 32, sw);
-            const uint64_t bdesc = smem_desc_kmajor(b_addr + kk * 32, sw);
-            const uint32_t accumulate = (kb | static_cast<int>(kk)) != 0;
-            if (kKind == kKindF16)
-              mma_f16(d_tmem, adesc, bdesc, p.idesc, accumulate);
-            else
-              mma_f8(d_tmem, adesc, bdesc, p.idesc, accumulate);
-          }
-          mma_commit(smem_u32(&empty[stage]));
-          if (++stage == stages) {
-            stage = 0;
-            phase ^= 1u;
-          }
-        }
-        if (!ok) break;
-        mma_commit(smem_u32(&tfull[acc]));
-      }
+      bool ok;
+      const int ks = static_cast<int>(sw / 32);
+#define CONV_MMA_ROLE(KS, MH)                                                                   \
+  mma_role<kKind, KS, MH>(p, tmem_base, a_ring, b_ring, b_res, full, empty, tfull, tempty, bres_full, \
+                          abort_flag, status, limit)
+      if (p.m_halves == 2)
+        ok = ks == 4 ? CONV_MMA_ROLE(4, 2) : (ks == 2 ? CONV_MMA_ROLE(2, 2) : CONV_MMA_ROLE(1, 2));
+      else
+        ok = ks == 4 ? CONV_MMA_ROLE(4, 1) : (ks == 2 ? CONV_MMA_ROLE(2, 1) : CONV_MMA_ROLE(1, 1));
+#undef CONV_MMA_ROLE
       if (!ok) {
         // Every MMA already issued must finish before TMEM is released.
         mma_commit(smem_u32(drain));
@@ -285,50 +416,196 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
   } else {
     // ------------------------------------------------------------ epilogue
+    // Two warpgroups (warps 2-5 and 6-9).  Each warp reads the TMEM lane
+    // quarter its warp index allows; group g takes the work items q % 2 == g
+    // of every tile (item = one 128-row half x one chunk of cw columns).
+    const int grp = (warp - 2) / 4;
     const int quarter = warp & 3;  // TMEM lanes this warp may read: [32*quarter, 32*quarter+32)
     const int row = quarter * 32 + lane;
     const uint32_t lane_field = static_cast<uint32_t>(quarter * 32) << 16;
+    const bool leader = (warp == 2 + 4 * grp) && lane == 0;
+    const uint32_t bar_id = 1 + grp;
     int it = 0;
-    for (int t = blockIdx.x; t < p.total_tiles; t += gridDim.x, ++it) {
-      const TileInfo ti = decode_tile(p, t);
-      const int acc = it & 1;
-      bool ok = mbar_wait_bounded(smem_u32(&tfull[acc]), static_cast<uint32_t>((it >> 1) & 1),
-                                  abort_flag, status, kStatusEpilogueTimeout, limit);
-      if (!__all_sync(0xFFFFFFFFu, ok)) break;
-      tc_fence_after();
-      const int ph = ti.phase;
-      const int m = ti.m0 + row;
-      const bool valid = m < p.rows[ph];
-      long long out_off = 0;
-      if (valid) {
-        const int hw = p.grid_h[ph] * p.grid_w[ph];
-        const int n_img = m / hw;
-        const int rem = m - n_img * hw;
-        const int j = rem / p.grid_w[ph];
-        const int i = rem - j * p.grid_w[ph];
-        const long long oy = static_cast<long long>(p.out_step_h) * j + p.out_off_h[ph];
-        const long long ox = static_cast<long long>(p.out_step_w) * i + p.out_off_w[ph];
-        out_off = ((static_cast<long long>(n_img) * p.Ho + oy) * p.Wo + ox) * p.Cout;
+    if (p.epi_mode != 0) {
+      const uint32_t row_bytes = static_cast<uint32_t>(p.cw) * 2;
+      const uint32_t chunk_bytes = kBM * row_bytes;
+      const int nchunks = p.bn / p.cw;
+      const int nitems = nchunks * p.m_halves;
+      const uint32_t src_tile_bytes = chunk_bytes * nitems;
+      const bool in_place = p.has_residual != 0;  // outputs overwrite the source chunk, stored from there
+      uint8_t* stg_grp = stg_base + grp * (p.stg_bufs * chunk_bytes);
+      int store_seq = 0;
+      int src_issued[2] = {0, 0};  // source loads issued per buffer (leader only)
+      if (p.has_residual && leader && static_cast<int>(blockIdx.x) < p.total_tiles) {
+        issue_source_items(p, decode_tile(p, blockIdx.x), src_base, smem_u32(&src_full[grp]), grp);
+        ++src_issued[0];
       }
-      const uint32_t taddr = tmem_base + lane_field + static_cast<uint32_t>(acc) * acc_cols;
-      for (int c0 = 0; c0 < p.bn; c0 += 16) {
-        uint32_t v[16];
-        if (ti.kblocks > 0) {
-          tmem_ld_32x32b_x16(taddr + static_cast<uint32_t>(c0), v);
-          tmem_wait_ld();
-        } else {
+      for (int t = blockIdx.x; t < p.total_tiles; t += gridDim.x, ++it) {
+        const TileInfo ti = decode_tile(p, t);
+        const int acc = it & 1;
+        const int sbuf = p.src_bufs == 2 ? acc : 0;
+        if (p.has_residual && leader && p.src_bufs == 2) {
+          const int tn = t + gridDim.x;
+          if (tn < p.total_tiles) {
+            // The other buffer last held tile it-1, whose stores must have read it.
+            bulk_wait_read_all();
+            issue_source_items(p, decode_tile(p, tn), src_base + (acc ^ 1) * src_tile_bytes,
+                               smem_u32(&src_full[2 * (acc ^ 1) + grp]), grp);
+            ++src_issued[acc ^ 1];
+          }
+        }
+        bool ok = mbar_wait_bounded(smem_u32(&tfull[acc]), static_cast<uint32_t>((it >> 1) & 1),
+                                    abort_flag, status, kStatusEpilogueTimeout, limit);
+        if (ok && p.has_residual && grp < nitems) {
+          const uint32_t par = static_cast<uint32_t>(p.src_bufs == 2 ? (it >> 1) & 1 : it & 1);
+          ok = mbar_wait_bounded(smem_u32(&src_full[2 * sbuf + grp]), par, abort_flag, status,
+                                 kStatusEpilogueTimeout, limit);
+        }
+        if (!__all_sync(0xFFFFFFFFu, ok)) break;
+        tc_fence_after();
+        uint8_t* src_tile = src_base + sbuf * src_tile_bytes;
+        const uint32_t tacc = tmem_base + lane_field + static_cast<uint32_t>(acc) * p.acc_stride;
+        if (grp >= nitems) {  // nothing for this group in this tile
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(smem_u32(&tempty[acc]));
+        }
+        for (int q = grp; q < nitems; q += kEpilogueGroups) {
+          const int h = q / nchunks;
+          const int c = q - h * nchunks;
+          const int mh = ti.m0 + h * kBM;
+          uint32_t v[64];
+          if (ti.kblocks > 0) {
+            const uint32_t taddr = tacc + static_cast<uint32_t>(h * p.bn + c * p.cw);
 #pragma unroll
-          for (int j = 0; j < 16; ++j) v[j] = 0u;
+            for (int k = 0; k < 4; ++k)
+              if (k < p.cw / 16)
+                tmem_ld_32x32b_x16(taddr + static_cast<uint32_t>(k * 16),
+                                   *reinterpret_cast<uint32_t(*)[16]>(&v[k * 16]));
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+              if (k < p.cw / 16)
+                tmem_wait_ld_regs(*reinterpret_cast<uint32_t(*)[16]>(&v[k * 16]));
+          } else {
+#pragma unroll
+            for (int k = 0; k < 64; ++k) v[k] = 0u;
+          }
+          if (q + kEpilogueGroups >= nitems) {
+            // This group's last TMEM read of the tile: hand the buffer back early.
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_u32(&tempty[acc]));
+          }
+          uint8_t* buf;
+          if (in_place) {
+            buf = src_tile + q * chunk_bytes;
+          } else {
+            buf = stg_grp + (p.stg_bufs == 2 ? (store_seq & 1) : 0) * chunk_bytes;
+            if (leader) {
+              if (p.stg_bufs == 2)
+                bulk_wait_read_le1();
+              else
+                bulk_wait_read_all();
+            }
+            named_barrier(bar_id, 128);
+          }
+          const int pieces = p.cw / 8;
+#pragma unroll
+          for (int k = 0; k < 8; ++k) {
+            if (k >= pieces) break;
+            float f[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) f[e] = __uint_as_float(v[k * 8 + e]);
+            const uint32_t off = swizzled_offset(static_cast<uint32_t>(row), k, row_bytes);
+            if (in_place) {
+              const uint4 raw = *reinterpret_cast<const uint4*>(buf + off);
+              const OutT* sv = reinterpret_cast<const OutT*>(&raw);
+#pragma unroll
+              for (int e = 0; e < 8; ++e) f[e] += p.beta * to_f32<OutT>(sv[e]);
+            }
+            uint4 packed;
+            OutT* o = reinterpret_cast<OutT*>(&packed);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) o[e] = from_f32<OutT>(activation(f[e], p.epilogue));
+            *reinterpret_cast<uint4*>(buf + off) = packed;
+          }
+          fence_proxy_async_shared();
+          named_barrier(bar_id, 128);
+          if (leader) {
+            if (p.epi_mode == 1) {
+              tma_store_2d(&p.map_out[ti.phase], smem_u32(buf), ti.n0 + c * p.cw, mh);
+            } else {
+              int n_img, gj, gi;
+              grid_pos(p, ti.phase, mh, n_img, gj, gi);
+              tma_store_4d(&p.map_out[ti.phase], smem_u32(buf), ti.n0 + c * p.cw, gi, gj, n_img);
+            }
+            bulk_commit_group();
+          }
+          ++store_seq;
         }
-        const int ch = ti.n0 + c0;
-        if (valid && ch < p.Cout) {
-          const int nvalid = p.Cout - ch < 16 ? p.Cout - ch : 16;
-          epilogue_16<OutT>(p, out_off + ch, v, nvalid);
+        if (p.has_residual && leader && p.src_bufs == 1) {
+          // Single source buffer: fetch the next tile's source once this
+          // tile's stores (which read it) are done reading.
+          const int tn = t + gridDim.x;
+          if (tn < p.total_tiles) {
+            bulk_wait_read_all();
+            issue_source_items(p, decode_tile(p, tn), src_base, smem_u32(&src_full[grp]), grp);
+            ++src_issued[0];
+          }
         }
       }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(&tempty[acc]));
+      if (leader) bulk_wait_all();
+      // On abort, source loads issued for tiles never processed must land
+      // before the CTA exits: wait for the latest phase of each buffer.
+      if (leader && p.has_residual && *abort_flag && grp < nitems) {
+        for (int b = 0; b < 2; ++b)
+          if (src_issued[b] > 0)
+            mbar_wait_drain(smem_u32(&src_full[2 * b + grp]),
+                            static_cast<uint32_t>((src_issued[b] - 1) & 1), limit / 8 + 1);
+      }
+    } else {
+      for (int t = blockIdx.x; t < p.total_tiles; t += gridDim.x, ++it) {
+        const TileInfo ti = decode_tile(p, t);
+        const int acc = it & 1;
+        bool ok = mbar_wait_bounded(smem_u32(&tfull[acc]), static_cast<uint32_t>((it >> 1) & 1),
+                                    abort_flag, status, kStatusEpilogueTimeout, limit);
+        if (!__all_sync(0xFFFFFFFFu, ok)) break;
+        tc_fence_after();
+        const int ph = ti.phase;
+        // Group g takes the 16-column chunks j with j % 2 == g of every half.
+        for (int h = 0; h < p.m_halves; ++h) {
+          const int m = ti.m0 + h * kBM + row;
+          const bool valid = m < p.rows[ph];
+          long long out_off = 0;
+          if (valid) {
+            int n_img, j, i;
+            grid_pos(p, ph, m, n_img, j, i);
+            const long long oy = static_cast<long long>(p.out_step_h) * j + p.out_off_h[ph];
+            const long long ox = static_cast<long long>(p.out_step_w) * i + p.out_off_w[ph];
+            out_off = ((static_cast<long long>(n_img) * p.Ho + oy) * p.Wo + ox) * p.Cout;
+          }
+          const uint32_t taddr = tmem_base + lane_field + static_cast<uint32_t>(acc) * p.acc_stride +
+                                 static_cast<uint32_t>(h * p.bn);
+          for (int c0 = grp * 16; c0 < p.bn; c0 += 16 * kEpilogueGroups) {
+            uint32_t v[16];
+            if (ti.kblocks > 0) {
+              tmem_ld_32x32b_x16(taddr + static_cast<uint32_t>(c0), v);
+              tmem_wait_ld_regs(v);
+            } else {
+#pragma unroll
+              for (int j = 0; j < 16; ++j) v[j] = 0u;
+            }
+            const int ch = ti.n0 + c0;
+            if (valid && ch < p.Cout) {
+              const int nvalid = p.Cout - ch < 16 ? p.Cout - ch : 16;
+              epilogue_16_direct<OutT>(p, out_off + ch, v, nvalid);
+            }
+          }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&tempty[acc]));
+      }
     }
   }
 

@@ -34,7 +34,7 @@ cudaError_t launch_instance(const ConvKernelParams& p, int grid, size_t smem_byt
 __global__ void im2col_probe_kernel(const __grid_constant__ CUtensorMap map, int c, int w, int h,
                                     int n, int off_w, int off_h, uint32_t row_bytes,
                                     uint8_t* __restrict__ out, unsigned int* status,
-                                    unsigned long long limit_ns) {
+                                    long long limit_cycles) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* tile = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -52,9 +52,9 @@ __global__ void im2col_probe_kernel(const __grid_constant__ CUtensorMap map, int
     tma_load_im2col_4d(smem_u32(tile), &map, smem_u32(&bar), c, w, h, n,
                        static_cast<uint16_t>(off_w), static_cast<uint16_t>(off_h));
   }
-  const bool ok = mbar_wait_bounded(smem_u32(&bar), 0, &abort_flag, status, 1u, limit_ns);
+  const bool ok = mbar_wait_bounded(smem_u32(&bar), 0, &abort_flag, status, 1u, limit_cycles);
   if (!__syncthreads_and(ok)) {
-    if (threadIdx.x == 0) mbar_wait_drain(smem_u32(&bar), 0, limit_ns);
+    if (threadIdx.x == 0) mbar_wait_drain(smem_u32(&bar), 0, limit_cycles);
     __syncthreads();
     return;
   }
@@ -78,10 +78,10 @@ cudaError_t launch_conv_igemm(int kind, bool out_bf16, const ConvKernelParams& p
 
 cudaError_t launch_im2col_probe(const CUtensorMap& map, int c, int w, int h, int n, int off_w,
                                 int off_h, uint32_t row_bytes, void* out, unsigned int* status,
-                                unsigned long long limit_ns, cudaStream_t stream) {
+                                long long limit_cycles, cudaStream_t stream) {
   const size_t smem = 1024 + static_cast<size_t>(kBM) * row_bytes;
   im2col_probe_kernel<<<1, 128, smem, stream>>>(map, c, w, h, n, off_w, off_h, row_bytes,
-                                                static_cast<uint8_t*>(out), status, limit_ns);
+                                                static_cast<uint8_t*>(out), status, limit_cycles);
   return cudaGetLastError();
 }
 

@@ -8,9 +8,10 @@
 
 namespace convgb300 {
 
-constexpr int kBM = 128;             // rows (output pixels) per tile = MMA M
-constexpr int kThreads = 192;        // producer warp + MMA warp + 4 epilogue warps
-constexpr int kEpilogueWarps = 4;
+constexpr int kBM = 128;             // rows (output pixels) per MMA = TMEM lanes
+constexpr int kThreads = 352;        // 2 producer warps + MMA warp + 8 epilogue warps
+constexpr int kEpilogueWarps = 8;    // two warpgroups; each covers the 128 TMEM lanes once
+constexpr int kEpilogueGroups = 2;
 constexpr int kMaxPhases = 4;        // stride-phase GEMMs of a stride-2 transposed conv
 constexpr int kMaxStages = 12;
 
@@ -29,9 +30,12 @@ constexpr unsigned int kStatusEpilogueTimeout = 4u;
 struct ConvKernelParams {  // aligned like CUtensorMap (64 B or more)
   CUtensorMap map_a[kMaxPhases];  // im2col maps over the NHWC input, one per phase
   CUtensorMap map_b;              // tiled map over the packed filter [phase][C_out][K]
+  CUtensorMap map_out[kMaxPhases];  // TMA-store maps over the output (epilogue modes 1, 2)
+  CUtensorMap map_src[kMaxPhases];  // TMA-load maps over the residual source (same boxes)
 
   int num_phases;
   int total_tiles;
+  int m_halves;         // 128-row halves per tile (1 or 2): tile_m = 128 * m_halves
   int n_tiles;          // tiles along C_out
   int bn;               // tile width along C_out (multiple of 16, <= 256)
   int bk;               // input channels per k-block
@@ -40,6 +44,7 @@ struct ConvKernelParams {  // aligned like CUtensorMap (64 B or more)
   uint32_t sw_bytes;    // bytes per operand row in a k-block (32, 64 or 128) = swizzle span
   uint32_t idesc;       // tcgen05 instruction descriptor
   uint32_t tmem_cols;   // allocated TMEM columns (two accumulators)
+  uint32_t acc_stride;  // TMEM columns per accumulator buffer = m_halves * bn
 
   // Per phase: the output-pixel grid the GEMM rows walk, and where it reads.
   int tile_start[kMaxPhases + 1];  // first tile index of each phase (prefix sums)
@@ -57,6 +62,14 @@ struct ConvKernelParams {  // aligned like CUtensorMap (64 B or more)
   int dil_h, dil_w;                // input offset per filter tap
   int b_index[kMaxPhases];         // phase slot of the packed filter read by each phase
 
+  // Shared-memory carve-up (byte offsets from the 1024-B aligned base).
+  uint32_t off_a, off_b, off_bres, off_src, off_stg, off_bar;
+  int b_resident;                  // whole packed filter kept in shared memory (one phase, one n-tile)
+  int epi_mode;                    // 0 direct stores, 1 TMA store [M][C_out], 2 TMA store 4-D phase grid
+  int cw;                          // epilogue chunk width in columns (16, 32 or 64)
+  int src_bufs;                    // residual-source tile buffers (0, 1 or 2)
+  int stg_bufs;                    // output staging buffers per epilogue group (0: in place)
+
   int Ho, Wo, Cout;
   int vec_ok;                      // C_out * 2 bytes is a multiple of 16: 16-B stores
   int has_residual;
@@ -65,7 +78,7 @@ struct ConvKernelParams {  // aligned like CUtensorMap (64 B or more)
   const void* src;
   void* out;
   unsigned int* status;
-  unsigned long long timeout_ns;   // limit of every bounded wait
+  long long timeout_cycles;        // limit of every bounded wait, in SM cycles
   int fault_mode;                  // test hook: 1 = CTA 0 skips its first arrive
 };
 
