@@ -99,6 +99,91 @@ __device__ __forceinline__ uint32_t swizzled_offset(uint32_t r, uint32_t q, uint
   return lin ^ (((lin >> 7) & (row_bytes / 16 - 1)) << 4);
 }
 
+// Two floats -> two packed 16-bit outputs (one conversion instruction).
+template <typename OutT>
+__device__ __forceinline__ uint32_t pack2(float a, float b);
+template <>
+__device__ __forceinline__ uint32_t pack2<__nv_bfloat16>(float a, float b) {
+  const __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
+  return *reinterpret_cast<const uint32_t*>(&v);
+}
+template <>
+__device__ __forceinline__ uint32_t pack2<__half>(float a, float b) {
+  const __half2 v = __floats2half2_rn(a, b);
+  return *reinterpret_cast<const uint32_t*>(&v);
+}
+
+// Two packed 16-bit values -> two floats.
+template <typename OutT>
+__device__ __forceinline__ float2 unpack2(uint32_t w);
+template <>
+__device__ __forceinline__ float2 unpack2<__nv_bfloat16>(uint32_t w) {
+  return __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w));
+}
+template <>
+__device__ __forceinline__ float2 unpack2<__half>(uint32_t w) {
+  return __half22float2(*reinterpret_cast<const __half2*>(&w));
+}
+
+template <int kAct>
+__device__ __forceinline__ float act_fixed(float v) {
+  if (kAct == kEpiRelu) return fmaxf(v, 0.0f);
+  if (kAct == kEpiSilu) return v / (1.0f + __expf(-v));
+  return v;
+}
+
+// One epilogue work item for this thread's row: kCw accumulator columns in
+// v, plus beta * source read from `buf` when kRes, activation kAct, one
+// rounding, written to `buf` at the same swizzled positions.
+template <typename OutT, int kCw, int kAct, bool kRes>
+__device__ __forceinline__ void process_row(const uint32_t (&v)[64], uint8_t* buf, uint32_t row,
+                                            float beta) {
+  constexpr uint32_t kRowBytes = kCw * 2;
+  constexpr int kPieces = kCw / 8;
+  uint4 src[kPieces];
+  uint32_t off[kPieces];
+#pragma unroll
+  for (int k = 0; k < kPieces; ++k) {
+    off[k] = swizzled_offset(row, k, kRowBytes);
+    if (kRes) src[k] = *reinterpret_cast<const uint4*>(buf + off[k]);
+  }
+#pragma unroll
+  for (int k = 0; k < kPieces; ++k) {
+    float f[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) f[e] = __uint_as_float(v[k * 8 + e]);
+    if (kRes) {
+      const uint32_t w[4] = {src[k].x, src[k].y, src[k].z, src[k].w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float2 sv = unpack2<OutT>(w[e]);
+        f[2 * e] = fmaf(beta, sv.x, f[2 * e]);
+        f[2 * e + 1] = fmaf(beta, sv.y, f[2 * e + 1]);
+      }
+    }
+    uint4 out;
+    out.x = pack2<OutT>(act_fixed<kAct>(f[0]), act_fixed<kAct>(f[1]));
+    out.y = pack2<OutT>(act_fixed<kAct>(f[2]), act_fixed<kAct>(f[3]));
+    out.z = pack2<OutT>(act_fixed<kAct>(f[4]), act_fixed<kAct>(f[5]));
+    out.w = pack2<OutT>(act_fixed<kAct>(f[6]), act_fixed<kAct>(f[7]));
+    *reinterpret_cast<uint4*>(buf + off[k]) = out;
+  }
+}
+
+template <typename OutT, int kCw>
+__device__ __forceinline__ void process_row_act(const uint32_t (&v)[64], uint8_t* buf,
+                                                uint32_t row, float beta, int act, bool res) {
+  if (res) {
+    if (act == kEpiRelu) process_row<OutT, kCw, kEpiRelu, true>(v, buf, row, beta);
+    else if (act == kEpiSilu) process_row<OutT, kCw, kEpiSilu, true>(v, buf, row, beta);
+    else process_row<OutT, kCw, kEpiNone, true>(v, buf, row, beta);
+  } else {
+    if (act == kEpiRelu) process_row<OutT, kCw, kEpiRelu, false>(v, buf, row, beta);
+    else if (act == kEpiSilu) process_row<OutT, kCw, kEpiSilu, false>(v, buf, row, beta);
+    else process_row<OutT, kCw, kEpiNone, false>(v, buf, row, beta);
+  }
+}
+
 // Direct-store epilogue for 16 columns (used when no TMA store map applies).
 template <typename OutT>
 __device__ __forceinline__ void epilogue_16_direct(const ConvKernelParams& p, long long off,
@@ -287,7 +372,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* drain = tempty + 2;
   uint64_t* bres_full = drain + 1;
   uint64_t* src_full = bres_full + 1;  // [buffer][group]
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(src_full + 4);
+  uint64_t* epi_done = src_full + 4;   // every epilogue warp has finished with TMEM
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(epi_done + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   unsigned int* status = p.status;
   const long long limit = p.timeout_cycles;
@@ -305,6 +391,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     mbar_init(smem_u32(drain), 1);
     mbar_init(smem_u32(bres_full), 1);
+    mbar_init(smem_u32(epi_done), kEpilogueWarps);
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -509,26 +596,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             named_barrier(bar_id, 128);
           }
-          const int pieces = p.cw / 8;
-#pragma unroll
-          for (int k = 0; k < 8; ++k) {
-            if (k >= pieces) break;
-            float f[8];
-#pragma unroll
-            for (int e = 0; e < 8; ++e) f[e] = __uint_as_float(v[k * 8 + e]);
-            const uint32_t off = swizzled_offset(static_cast<uint32_t>(row), k, row_bytes);
-            if (in_place) {
-              const uint4 raw = *reinterpret_cast<const uint4*>(buf + off);
-              const OutT* sv = reinterpret_cast<const OutT*>(&raw);
-#pragma unroll
-              for (int e = 0; e < 8; ++e) f[e] += p.beta * to_f32<OutT>(sv[e]);
-            }
-            uint4 packed;
-            OutT* o = reinterpret_cast<OutT*>(&packed);
-#pragma unroll
-            for (int e = 0; e < 8; ++e) o[e] = from_f32<OutT>(activation(f[e], p.epilogue));
-            *reinterpret_cast<uint4*>(buf + off) = packed;
-          }
+          if (p.cw == 64)
+            process_row_act<OutT, 64>(v, buf, static_cast<uint32_t>(row), p.beta, p.epilogue, in_place);
+          else if (p.cw == 32)
+            process_row_act<OutT, 32>(v, buf, static_cast<uint32_t>(row), p.beta, p.epilogue, in_place);
+          else
+            process_row_act<OutT, 16>(v, buf, static_cast<uint32_t>(row), p.beta, p.epilogue, in_place);
           fence_proxy_async_shared();
           named_barrier(bar_id, 128);
           if (leader) {
@@ -609,9 +682,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   }
 
-  tc_fence_before();
+  if (warp >= 2 && warp < 2 + kEpilogueWarps) {
+    tc_fence_before();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(smem_u32(epi_done));
+  }
   __syncthreads();
   if (warp == 1) {
+    // TMEM is released only once every epilogue warp has signalled that its
+    // last tcgen05.ld is complete.
+    if (lane == 0) mbar_wait_drain(smem_u32(epi_done), 0, limit);
+    __syncwarp();
     tc_fence_after();
     tmem_dealloc(tmem_base, p.tmem_cols);
   }
