@@ -22,8 +22,9 @@
  *  - Tensors are NHWC, dense, row-major, channels fastest.  All tensor
  *    pointers are DEVICE pointers, 16-byte aligned.
  *  - The caller owns all memory (input, filter, packed filter, output,
- *    source, workspace).  The library never allocates device memory; it keeps
- *    only host-side state (driver entry points, per-device attributes).
+ *    source, workspace).  The library never allocates device memory at run
+ *    time; it keeps host-side state (driver entry points, per-device
+ *    attributes) and one static device array used only by conv2d_fwd_noalloc.
  *  - Calls are asynchronous on `stream` (a cudaStream_t; NULL = the legacy
  *    default stream).  Outputs are valid once the stream has been synchronised.
  *  - Validation failures return before any launch and write nothing.
@@ -176,6 +177,38 @@ conv_status_t conv_transposed_packed(const void* input, int n, int h, int w, int
                                      const int dilation[2], const int padding[2], int has_residual,
                                      const void* source, float beta, conv_epilogue_t epilogue,
                                      void* workspace, size_t workspace_bytes, void* stream);
+
+/* ------------------------------------------------------------------------
+ * conv2d_fwd without any device allocation.  The pages have no counterpart:
+ * this entry point exists for callers that cannot allocate device memory --
+ * for example code running under a host framework that owns every device
+ * allocation, or a real-time loop whose policy forbids cudaMalloc after
+ * start-up -- and so cannot provide conv2d_fwd's workspace.
+ *
+ * Arguments, gates and results are those of conv2d_fwd (raw FCRS/RSCF filter;
+ * the caller still passes input, filter, output and source).  The packed
+ * filter and the status word go to a library-owned scratch array of 8 MiB
+ * (CONV_NOALLOC_SCRATCH_BYTES) that lives in device memory of every GPU that
+ * loads the library until the process exits.  Filters whose packed size plus
+ * CONV_STATUS_BYTES exceeds it return CONV_ERR_WORKSPACE_TOO_SMALL before
+ * any CUDA call.  The first call on a device resolves the scratch address
+ * for that device; make that first call before any stream capture.  Every
+ * call shares the one array: calls that overlap on the GPU (different
+ * streams, or devices sharing nothing but the library) race, so serialise
+ * them.  The status word is cleared at the start of each call; a bounded
+ * wait that runs out inside the kernel leaves the output incomplete and is
+ * not reported by this entry point (use conv2d_fwd with a workspace and
+ * conv_check_device_status when that report is needed).
+ * ------------------------------------------------------------------------ */
+#define CONV_NOALLOC_SCRATCH_BYTES (8u << 20)
+
+conv_status_t conv2d_fwd_noalloc(const void* input, int n, int h, int w, int c_in,
+                                 conv_dtype_t in_dtype, const void* filter, int r, int s, int c_out,
+                                 int filter_is_fcrs, void* output, int ho, int wo,
+                                 conv_dtype_t out_dtype, const int stride[2], const int dilation[2],
+                                 const int symmetric_padding[2], int num_groups, int has_residual,
+                                 const void* source, float beta, conv_epilogue_t epilogue,
+                                 void* stream);
 
 /* ------------------------------------------------------------------------
  * Device-side failure report.  Synchronises `stream`, reads the status

@@ -185,3 +185,12 @@ def test_binding_raises_without_library(monkeypatch, tmp_path):
     monkeypatch.setattr(_lib, "LIB_PATH", str(tmp_path / "missing.so"))
     with pytest.raises(_lib.ExtensionMissing):
         cg.conv_status_string(0)
+
+
+def test_noalloc_rejects_filters_beyond_its_scratch(lib):
+    # 5x5x2048x2048 bf16 packs to 210 MB, far beyond the 8 MiB scratch: rejected before any CUDA call.
+    status = lib.conv2d_fwd_noalloc(A, 1, 8, 8, 2048, BF16, B, 5, 5, 2048, 0, C, 8, 8, BF16,
+                                    _lib.pair((1, 1)), _lib.pair((1, 1)), _lib.pair((2, 2)), 1, 0,
+                                    None, 0.0, 0, None)
+    assert status == WS_SMALL
+    assert _lib.CONV_NOALLOC_SCRATCH_BYTES == 8 << 20

@@ -24,6 +24,7 @@ CONV_ERR_WORKSPACE_TOO_SMALL = 4
 CONV_ERR_CUDA = 5
 CONV_ERR_DEVICE_TIMEOUT = 6
 CONV_STATUS_BYTES = 256
+CONV_NOALLOC_SCRATCH_BYTES = 8 << 20
 
 # conv_dtype_t / conv_epilogue_t
 DTYPE_CODES = {"bf16": 0, "f16": 1, "f8e4m3": 2}
@@ -36,7 +37,7 @@ EXPORTS = (
     "conv_transposed_packed_filter_bytes", "conv_transposed_workspace_size",
     "conv_transposed_pack_filter", "conv_transposed", "conv_transposed_packed",
     "conv_check_device_status", "conv_testing_set_wait_fault", "conv_testing_im2col_tile",
-    "conv_testing_fwd_plan",
+    "conv_testing_fwd_plan", "conv2d_fwd_noalloc",
 )
 
 
@@ -71,6 +72,9 @@ def _declare(lib):
     lib.conv_transposed.restype = I
     lib.conv_transposed_packed.argtypes = [P, I, I, I, I, I, P, I, I, I, P, I, I, I] + tr_tail
     lib.conv_transposed_packed.restype = I
+    lib.conv2d_fwd_noalloc.argtypes = [P, I, I, I, I, I, P, I, I, I, I, P, I, I, I,
+                                       IP, IP, IP, I, I, P, F, I, P]
+    lib.conv2d_fwd_noalloc.restype = I
     lib.conv_check_device_status.argtypes = [P, P, ctypes.POINTER(ctypes.c_uint)]
     lib.conv_check_device_status.restype = I
     lib.conv_testing_set_wait_fault.argtypes = [I, U64]

@@ -902,6 +902,41 @@ conv_status_t tr_impl(const void* input, const TrShape& t, const void* filter, b
 
 }  // namespace
 
+namespace {
+
+// ------------------------------------------------------------------ no-allocation variant
+// Scratch for conv2d_fwd_noalloc: the status word and the packed filter live
+// in this file-scope device array instead of a caller-provided workspace.
+// Every GPU that loads the library holds it until the process exits.
+constexpr size_t kNoAllocScratchBytes = size_t(8) << 20;  // 8 MiB
+__device__ __align__(256) uint8_t g_noalloc_scratch[kNoAllocScratchBytes];
+
+// Device address of g_noalloc_scratch per device (host code must not use the
+// symbol itself as a pointer).  Resolved once per device by the first call
+// made with that device current.
+void* noalloc_scratch_ptr(conv_status_t* st) {
+  static std::mutex mu;
+  static void* ptrs[64] = {nullptr};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
+    *st = CONV_ERR_CUDA;
+    return nullptr;
+  }
+  std::lock_guard<std::mutex> lock(mu);
+  if (!ptrs[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) {
+      *st = CONV_ERR_CUDA;
+      return nullptr;
+    }
+    ptrs[dev] = p;
+  }
+  *st = CONV_OK;
+  return ptrs[dev];
+}
+
+}  // namespace
+
 // =================================================================== C ABI
 extern "C" {
 
@@ -1071,6 +1106,32 @@ conv_status_t conv_check_device_status(void* workspace, void* stream, unsigned i
   if (bits == 0) return CONV_OK;
   if (cudaMemset(workspace, 0, sizeof(bits)) != cudaSuccess) return CONV_ERR_CUDA;
   return CONV_ERR_DEVICE_TIMEOUT;
+}
+
+// See include/conv_gb300.h.  Validates the size against the scratch first
+// (no CUDA call on rejection), resolves the scratch address (first call per
+// device), clears the status word, then runs the ordinary conv2d_fwd path with
+// the scratch standing in for the workspace.
+conv_status_t conv2d_fwd_noalloc(const void* input, int n, int h, int w, int c_in,
+                                 conv_dtype_t in_dtype, const void* filter, int r, int s, int c_out,
+                                 int filter_is_fcrs, void* output, int ho, int wo,
+                                 conv_dtype_t out_dtype, const int stride[2], const int dilation[2],
+                                 const int symmetric_padding[2], int num_groups, int has_residual,
+                                 const void* source, float beta, conv_epilogue_t epilogue,
+                                 void* stream) {
+  if (r <= 0 || s <= 0 || c_in <= 0 || c_out <= 0 || !known_dtype(in_dtype))
+    return CONV_ERR_INVALID_VALUE;
+  const size_t need = conv2d_workspace_size(r, s, c_in, c_out, in_dtype);
+  if (need > kNoAllocScratchBytes) return CONV_ERR_WORKSPACE_TOO_SMALL;
+  conv_status_t st = CONV_OK;
+  void* scratch = noalloc_scratch_ptr(&st);
+  if (st != CONV_OK) return st;
+  if (cudaMemsetAsync(scratch, 0, CONV_STATUS_BYTES, static_cast<cudaStream_t>(stream)) !=
+      cudaSuccess)
+    return CONV_ERR_CUDA;
+  return conv2d_fwd(input, n, h, w, c_in, in_dtype, filter, r, s, c_out, filter_is_fcrs, output,
+                    ho, wo, out_dtype, stride, dilation, symmetric_padding, num_groups,
+                    has_residual, source, beta, epilogue, scratch, kNoAllocScratchBytes, stream);
 }
 
 // ------------------------------------------------------------------- testing hooks
