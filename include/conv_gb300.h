@@ -105,8 +105,8 @@ size_t conv2d_workspace_size(int r, int s, int c_in, int c_out, conv_dtype_t dty
  *
  * Gates (CONV_ERR_NOT_SUPPORTED otherwise): in_dtype in {BF16, F16, F8E4M3};
  * out_dtype as above; stride (1,1) or (2,2); dilation (1,1); padding (0,0),
- * (1,1) or (2,2); num_groups == 1; c_in * sizeof(in_dtype) a multiple of 32
- * bytes (the TMA im2col loader's channel block); r, s <= 32.
+ * (1,1) or (2,2); num_groups == 1; c_in * sizeof(in_dtype) a multiple of 16
+ * bytes and at least 32 bytes (the TMA im2col loader's channel rows); r, s <= 32.
  * CONV_ERR_INVALID_VALUE: null pointers, non-positive sizes, ho/wo not equal
  * to floor((h + 2p - (r-1) - 1)/stride) + 1, has_residual with NULL source,
  * unknown epilogue.
@@ -143,8 +143,8 @@ conv_status_t conv2d_fwd_packed(const void* input, int n, int h, int w, int c_in
  *  ho - ((h-1)*stride - 2*pad + (r-1) + 1) must lie in [0, stride) (the
  *  extra rows play the role of an output padding), likewise wo.
  * Gates: dtypes as conv2d_fwd; stride (1,1) or (2,2); dilation (1,1);
- * 0 <= pad < r (and < s); c_in * sizeof(in_dtype) a multiple of 32 bytes;
- * r, s <= 32.
+ * 0 <= pad < r (and < s); c_in * sizeof(in_dtype) a multiple of 16 bytes and
+ * at least 32 bytes; r, s <= 32.
  * conv_transposed packs the filter into the workspace on every call;
  * conv_transposed_packed takes the result of conv_transposed_pack_filter.
  * Packed layout: [stride_h*stride_w phases][c_out][K_max], phase (a, b) at

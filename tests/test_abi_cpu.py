@@ -103,8 +103,9 @@ def fwd(lib, *, inp=A, n=2, h=8, w=8, c=64, dt=BF16, flt=B, r=3, s=3, f=64, fcrs
     (dict(dt=F8, odt=F8), NOTSUP),                            # fp8 must write bf16
     (dict(dt=BF16, odt=F16), NOTSUP),
     (dict(dt=7), NOTSUP),
-    (dict(c=8), NOTSUP),                                      # 16 B channel rows: no TMA block
-    (dict(c=24), NOTSUP),
+    (dict(c=8), NOTSUP),                                      # 16 B channel rows: below one MMA K-step
+    (dict(c=20), NOTSUP),                                     # 40 B rows: not a multiple of 16 B
+    (dict(dt=F8, c=16), NOTSUP),                              # 16 B of fp8
     (dict(r=33, s=33, h=40, w=40), NOTSUP),
     (dict(ws_bytes=1000), WS_SMALL),                          # cannot hold the packed filter
     (dict(ws_bytes=100, packed=True), WS_SMALL),
@@ -169,8 +170,8 @@ def test_tile_plans_for_the_workloads(lib):
     assert p["smem"] <= 227 * 1024 and p["stages"] >= 3
     p = _plan(lib, 32, 56, 56, 64, BF16, 3, 128, 2, 1, sms=152)          # downsample: 147 KB filter
     assert (p["bn"], p["tiles"], p["epi"], p["bres"]) == (128, 98, 1, 0) and p["stages"] >= 4
-    p = _plan(lib, 16, 64, 64, 320, F8, 3, 320, 1, 1, res=1, sms=152)    # fp8: 3 x 112 columns
-    assert (p["bn"], p["bk"], p["tiles"], p["tmem"], p["epi"]) == (112, 64, 768, 512, 1)
+    p = _plan(lib, 16, 64, 64, 320, F8, 3, 320, 1, 1, res=1, sms=152)    # fp8: 2 x 160 columns,
+    assert (p["bn"], p["bk"], p["tiles"], p["tmem"], p["epi"]) == (160, 128, 1024, 512, 1)  # 128-ch blocks
     p = _plan(lib, 1, 512, 512, 128, BF16, 3, 3, 1, 1, sms=152)          # C_out = 3: masked 16-wide tile
     assert (p["bn"], p["bk"], p["tiles"], p["epi"], p["bres"]) == (16, 64, 1024, 0, 1)
     p = _plan(lib, 1, 16, 16, 16, BF16, 3, 16, 1, 1, sms=152)            # 32-byte channel rows

@@ -28,7 +28,8 @@ CASES = [
     ("bf16", 2, 9, 9, 64, 3, 1, 0, 48, 1, 1, 0),
     ("bf16", 1, 16, 16, 16, 3, 1, 1, 128, 2, 0, 0),
     ("f16", 2, 10, 10, 128, 5, 1, 2, 100, 0, 4, 64),
-    ("f8e4m3", 2, 9, 9, 320, 3, 1, 1, 70, 1, 2, 192),
+    ("f8e4m3", 2, 9, 9, 320, 3, 1, 1, 70, 1, 2, 256),   # last block reaches past C_in: zero tail
+    ("bf16", 1, 9, 9, 80, 3, 1, 1, 3, 2, 1, 64),           # 64-B rows, partial last block
     ("f8e4m3", 1, 11, 11, 128, 3, 2, 1, 0, 2, 0, 0),
 ]
 
@@ -45,7 +46,8 @@ def _expected(xbits, m0, tap_r, tap_s, c0, bk, stride, pad, R):
         iy = oy * stride - pad + tap_r
         ix = ox * stride - pad + tap_s
         if n < N and 0 <= iy < H and 0 <= ix < W:
-            out[i] = xbits[n, iy, ix, c0:c0 + bk]
+            hi = min(c0 + bk, C)
+            out[i, :hi - c0] = xbits[n, iy, ix, c0:hi]      # channels past C_in read as zero
     return out
 
 

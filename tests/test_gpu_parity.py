@@ -73,6 +73,9 @@ SMALL_FWD = [
     _fwd("e_5x5_p2_relu", "f8e4m3", 1, 12, 12, 32, 16, 5, 1, 2, epi="relu"),
     _fwd("e_cout3", "f8e4m3", 1, 16, 16, 128, 3, 3, 1, 1),
     _fwd("e_cin32_32B", "f8e4m3", 2, 10, 10, 32, 64, 3, 1, 1, layout="FCRS"),
+    _fwd("b_cin24_partial_block", "bf16", 2, 9, 10, 24, 32, 3, 1, 1),
+    _fwd("b_cin80_partial_block", "bf16", 1, 11, 11, 80, 48, 3, 2, 1, res=True, beta=1.0),
+    _fwd("e_cin160_partial_block", "f8e4m3", 1, 10, 10, 160, 64, 3, 1, 1, layout="FCRS"),
     _fwd("b_single_partial_tile", "bf16", 1, 5, 7, 64, 64, 3, 1, 1),
     _fwd("b_exact_one_tile", "bf16", 2, 8, 8, 64, 64, 3, 1, 1),
     _fwd("b_tiny_image", "bf16", 3, 2, 3, 32, 16, 3, 2, 2),
@@ -89,6 +92,7 @@ SMALL_TR = [
     _tr("t_e_4x4_s2p1", "f8e4m3", 2, 8, 8, 64, 64, 4, 2, 1),
     _tr("t_h_cout3", "f16", 1, 10, 10, 64, 3, 4, 2, 1),
     _tr("t_h_cout256_silu", "f16", 1, 6, 6, 64, 256, 4, 2, 1, epi="silu"),
+    _tr("t_h_cin80_partial_block", "f16", 1, 7, 7, 80, 32, 4, 2, 1),
 ]
 
 

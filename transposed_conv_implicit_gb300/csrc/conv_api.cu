@@ -122,17 +122,24 @@ struct Plan {
   int sh, sw;
 };
 
-// Channels per k-block: the largest of 128/64/32 bytes that divides C_in.
+// Channels per k-block: rows of 128, 64 or 32 bytes (the swizzle span).  The
+// last block of a filter tap may reach past C_in: the TMA zero-fills those
+// channels of A, so the filter values they meet (the next tap's, or zero
+// fill past K) contribute nothing.  Prefer 128-byte rows unless that wastes
+// more than a quarter of the MMA work; C_in * elt must be a multiple of 16
+// bytes (TMA strides and coordinates) and at least 32 bytes (one MMA K-step).
 conv_status_t channel_block(int c_in, int elt, int* bk, uint32_t* row_bytes) {
   const long long cb = static_cast<long long>(c_in) * elt;
-  for (uint32_t rb : {128u, 64u, 32u}) {
-    if (cb % rb == 0) {
-      *row_bytes = rb;
-      *bk = static_cast<int>(rb) / elt;
-      return CONV_OK;
-    }
+  if (cb % 16 != 0 || cb < 32) return CONV_ERR_NOT_SUPPORTED;
+  uint32_t rb = 32;
+  if (cb % 128 == 0 || (cb > 128 && ((cb + 127) / 128) * 128 * 4 <= cb * 5)) {
+    rb = 128;
+  } else if (cb % 64 == 0 || (cb > 64 && ((cb + 63) / 64) * 64 * 4 <= cb * 5)) {
+    rb = 64;
   }
-  return CONV_ERR_NOT_SUPPORTED;
+  *row_bytes = rb;
+  *bk = static_cast<int>(rb) / elt;
+  return CONV_OK;
 }
 
 uint32_t make_idesc(conv_dtype_t in, int bn) {
@@ -206,7 +213,8 @@ conv_status_t plan_channels(Plan* pl, conv_dtype_t in, int c_in) {
   if (st != CONV_OK) return st;
   ConvKernelParams& kp = pl->kp;
   kp.bk = bk;
-  kp.c_blocks = c_in / bk;
+  kp.c_blocks = (c_in + bk - 1) / bk;
+  kp.c_tail = c_in - kp.c_blocks * bk;
   kp.sw_bytes = row_bytes;
   pl->in_dtype = in;
   pl->out_bf16 = (in != CONV_DTYPE_F16);
@@ -216,18 +224,21 @@ conv_status_t plan_channels(Plan* pl, conv_dtype_t in, int c_in) {
 
 // Tile shape: the C_out tile width bn (a multiple of 16, <= 256) and the tile
 // height (128 rows, or 256 rows as two 128-row MMAs sharing each filter
-// k-block when bn <= 128).  A small cost model from measured TMA behaviour on
-// this part (each load costs about 360 cycles plus bytes / 95 per SM, two
-// producers in flight) and the tensor-core rate picks the shape with the
-// shortest makespan over the persistent grid.
+// k-block when bn <= 128).  A cost model from measurements on this part picks
+// the shape with the shortest makespan over the persistent grid:
+//  - one tcgen05.mma (M=128) occupies the tensor pipe ~63 cycles for N <= 128
+//    and proportionally longer above (127 cycles at N=256);
+//  - operand loads stream at ~70 bytes per cycle per SM, plus ~40 cycles of
+//    issue per TMA instruction;
+//  - a k-block costs the larger of the two; a tile adds its epilogue.
 void choose_tiling(Plan* pl, const long long rows[], int num_phases, int max_kblocks, int c_out,
                    int num_sms) {
   ConvKernelParams& kp = pl->kp;
-  const double flop_per_clk = pl->kind == kKindF8 ? 14300.0 : 7150.0;
   double best = 1e300;
   int best_bn = 16, best_nt = 1, best_mh = 1;
   const int nt_min = (c_out + 255) / 256;
   const int nt_max = std::max(nt_min, std::min((c_out + 15) / 16, nt_min + 8));
+  const int ksteps = static_cast<int>(kp.sw_bytes / 32);
   for (int mh = 2; mh >= 1; --mh) {
     for (int nt = nt_min; nt <= nt_max; ++nt) {
       const int per = (c_out + nt - 1) / nt;
@@ -240,8 +251,8 @@ void choose_tiling(Plan* pl, const long long rows[], int num_phases, int max_kbl
       const double a = static_cast<double>(kBM) * mh * kp.sw_bytes;
       const double b = static_cast<double>(bn) * kp.sw_bytes;
       const bool res = num_phases == 1 && nte == 1 && max_kblocks * b <= 96.0 * 1024;
-      const double load = (360.0 + a / 95.0) + (res ? 0.0 : 360.0 + b / 95.0);
-      const double mma = 2.0 * kBM * mh * bn * kp.bk / flop_per_clk;
+      const double load = (a + (res ? 0.0 : b)) / 70.0 + 40.0 * (res ? 1 : 2);
+      const double mma = static_cast<double>(mh) * ksteps * 63.0 * std::max(1.0, bn / 128.0);
       const double epi = static_cast<double>(kBM) * mh * bn * 2 / 64.0;
       const double tile = max_kblocks * std::max(load, mma) + epi;
       const double cost = waves * tile;
@@ -657,7 +668,7 @@ conv_status_t layout_memory(Plan* pl, int has_residual) {
     const size_t stage = a_bytes + (opts[i].res ? 0 : b_bytes);
     if (used + 2 * stage > kSmemLimit) continue;
     const int st = static_cast<int>(std::min<size_t>(kMaxStages, (kSmemLimit - used) / stage));
-    const double load = (360.0 + a_bytes / 95.0) + (opts[i].res ? 0.0 : 360.0 + b_bytes / 95.0);
+    const double load = (a_bytes + (opts[i].res ? 0.0 : b_bytes)) / 70.0 + 40.0 * (opts[i].res ? 1 : 2);
     double key = load;
     if (st < 3) key += 1e6;
     if (opts[i].srcb < srcb_max) key += 50.0;

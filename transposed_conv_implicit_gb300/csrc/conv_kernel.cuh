@@ -301,10 +301,6 @@ __device__ __forceinline__ bool mma_role(const ConvKernelParams& p, uint32_t tme
   uint32_t bs_lo = b_lo0;  // streamed B: advances with the ring
   bool ok = true;
   int it = 0;
-  if (p.b_resident && p.total_tiles > static_cast<int>(blockIdx.x)) {
-    ok = mbar_wait_bounded(smem_u32(bres_full), 0, abort_flag, status, kStatusMmaTimeout, limit);
-    tc_fence_after();
-  }
   for (int t = blockIdx.x; ok && t < p.total_tiles; t += gridDim.x, ++it) {
     const TileInfo ti = decode_tile(p, t);
     const int acc = it & 1;
@@ -419,15 +415,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       long long seq = 0;
       long long last_issued = -1;
       bool ok = true;
-      if (p.b_resident && role == 0) {
-        // The whole packed filter of the single phase / n-tile, once.
-        const int kbs = p.taps_h[0] * p.taps_w[0] * p.c_blocks;
-        const uint32_t bb = smem_u32(bres_full);
-        mbar_arrive_expect_tx(bb, b_bytes * kbs);
-        for (int kb = 0; kb < kbs; ++kb)
-          tma_load_3d(smem_u32(b_res + kb * b_bytes), &p.map_b, bb, kb * p.bk, 0, p.b_index[0]);
-      }
       const uint32_t stage_tx = a_bytes + (p.b_resident ? 0u : b_bytes);
+      bool first_tile = true;  // a resident filter is loaded k-block by k-block with it
       for (int t = blockIdx.x; t < p.total_tiles && ok; t += gridDim.x) {
         const TileInfo ti = decode_tile(p, t);
         const int ph = ti.phase;
@@ -439,6 +428,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         const CUtensorMap* amap = &p.map_a[ph];
         const int bz = p.b_index[ph];
         int cb = 0, uw = 0, uh = 0;
+        int bk_k = 0;  // k coordinate of this k-block in the packed filter: tap*C_in + cb*bk
+        const bool load_res = p.b_resident && first_tile;
+        first_tile = false;
         for (int kb = 0; kb < ti.kblocks; ++kb, ++seq) {
           if ((seq & 1) == role) {
             if (!mbar_wait_bounded(smem_u32(&empty[stage]), phase ^ 1u, abort_flag, status,
@@ -450,20 +442,24 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!(p.fault_mode == 1 && blockIdx.x == 0 && seq == 0)) {
               // (fault_mode 1, a test hook: CTA 0 leaves its first stage un-armed.)
               const uint32_t fb = smem_u32(&full[stage]);
-              mbar_arrive_expect_tx(fb, stage_tx);
+              mbar_arrive_expect_tx(fb, stage_tx + (load_res ? b_bytes : 0u));
               tma_load_im2col_4d(smem_u32(a_ring + stage * a_bytes), amap, fb, cb * p.bk, w0, h0,
                                  n_img, static_cast<uint16_t>(uw * p.dil_w),
                                  static_cast<uint16_t>(uh * p.dil_h));
               if (!p.b_resident)
-                tma_load_3d(smem_u32(b_ring + stage * b_bytes), &p.map_b, fb, kb * p.bk, ti.n0, bz);
+                tma_load_3d(smem_u32(b_ring + stage * b_bytes), &p.map_b, fb, bk_k, ti.n0, bz);
+              else if (load_res)
+                tma_load_3d(smem_u32(b_res + kb * b_bytes), &p.map_b, fb, bk_k, 0, bz);
             }
           }
           if (++stage == stages) {
             stage = 0;
             phase ^= 1u;
           }
+          bk_k += p.bk;
           if (++cb == p.c_blocks) {
             cb = 0;
+            bk_k += p.c_tail;  // the last block of a tap may reach past C_in: realign
             if (++uw == tw) {
               uw = 0;
               ++uh;
@@ -477,7 +473,6 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (q >= 0 && (q & 1) == role)
             mbar_wait_drain(smem_u32(&full[q % stages]), static_cast<uint32_t>((q / stages) & 1),
                             limit / 8 + 1);
-        if (p.b_resident && role == 0) mbar_wait_drain(smem_u32(bres_full), 0, limit / 8 + 1);
       }
     }
     __syncwarp();

@@ -39,7 +39,8 @@ struct ConvKernelParams {  // aligned like CUtensorMap (64 B or more)
   int n_tiles;          // tiles along C_out
   int bn;               // tile width along C_out (multiple of 16, <= 256)
   int bk;               // input channels per k-block
-  int c_blocks;         // C_in / bk
+  int c_blocks;         // ceil(C_in / bk): channel blocks per filter tap
+  int c_tail;           // C_in - c_blocks * bk (<= 0): k adjustment after a tap's last block
   int stages;           // depth of the shared-memory ring
   uint32_t sw_bytes;    // bytes per operand row in a k-block (32, 64 or 128) = swizzle span
   uint32_t idesc;       // tcgen05 instruction descriptor
