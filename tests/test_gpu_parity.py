@@ -76,6 +76,11 @@ SMALL_FWD = [
     _fwd("b_cin24_partial_block", "bf16", 2, 9, 10, 24, 32, 3, 1, 1),
     _fwd("b_cin80_partial_block", "bf16", 1, 11, 11, 80, 48, 3, 2, 1, res=True, beta=1.0),
     _fwd("e_cin160_partial_block", "f8e4m3", 1, 10, 10, 160, 64, 3, 1, 1, layout="FCRS"),
+    _fwd("b_window_cin160_partial", "bf16", 2, 10, 9, 160, 48, 3, 1, 1),
+    _fwd("b_window_rowblocks_res", "bf16", 2, 21, 20, 64, 64, 3, 1, 1, res=True, beta=1.0),
+    _fwd("b_window_5x5_p2", "bf16", 1, 17, 19, 64, 96, 5, 1, 2, res=True, beta=-0.5, epi="silu"),
+    _fwd("h_window_cout128", "f16", 2, 14, 12, 64, 128, 3, 1, 1, epi="relu"),
+    _fwd("b_window_cout256", "bf16", 1, 9, 11, 128, 256, 3, 1, 1, layout="FCRS"),
     _fwd("b_single_partial_tile", "bf16", 1, 5, 7, 64, 64, 3, 1, 1),
     _fwd("b_exact_one_tile", "bf16", 2, 8, 8, 64, 64, 3, 1, 1),
     _fwd("b_tiny_image", "bf16", 3, 2, 3, 32, 16, 3, 2, 2),

@@ -14,6 +14,7 @@
 #include <algorithm>
 #include <atomic>
 #include <cstdint>
+#include <cstdlib>
 #include <cstring>
 #include <mutex>
 
@@ -33,6 +34,15 @@ std::atomic<int> g_fault_mode{0};
 std::atomic<unsigned long long> g_timeout_ns{0};
 
 int elt_bytes(conv_dtype_t d) { return d == CONV_DTYPE_F8E4M3 ? 1 : 2; }
+
+// Tuning overrides read from the environment (0 or unset = let the planner
+// choose): CONV_TILE_M (128 or 256), CONV_TILE_N (a multiple of 16, <= 256),
+// CONV_FILTER_RESIDENT (0 forbids keeping the filter in shared memory),
+// CONV_MAX_STAGES (caps the operand ring).  Read on every call.
+int env_int(const char* name) {
+  const char* v = std::getenv(name);
+  return v ? std::atoi(v) : 0;
+}
 
 bool known_dtype(conv_dtype_t d) {
   return d == CONV_DTYPE_BF16 || d == CONV_DTYPE_F16 || d == CONV_DTYPE_F8E4M3;
@@ -215,6 +225,7 @@ conv_status_t plan_channels(Plan* pl, conv_dtype_t in, int c_in) {
   kp.bk = bk;
   kp.c_blocks = (c_in + bk - 1) / bk;
   kp.c_tail = c_in - kp.c_blocks * bk;
+  kp.c_in = c_in;
   kp.sw_bytes = row_bytes;
   pl->in_dtype = in;
   pl->out_bf16 = (in != CONV_DTYPE_F16);
@@ -252,9 +263,11 @@ void choose_tiling(Plan* pl, const long long rows[], int num_phases, int max_kbl
       const double b = static_cast<double>(bn) * kp.sw_bytes;
       const bool res = num_phases == 1 && nte == 1 && max_kblocks * b <= 96.0 * 1024;
       const double load = (a + (res ? 0.0 : b)) / 70.0 + 40.0 * (res ? 1 : 2);
-      const double mma = static_cast<double>(mh) * ksteps * 63.0 * std::max(1.0, bn / 128.0);
+      const double mma = static_cast<double>(mh) * ksteps * (63.0 * std::max(1.0, bn / 128.0) + 8.0);
       const double epi = static_cast<double>(kBM) * mh * bn * 2 / 64.0;
-      const double tile = max_kblocks * std::max(load, mma) + epi;
+      // The smaller term still costs a little (issue slots, barriers): it breaks
+      // ties in favour of fewer, wider MMAs.
+      const double tile = max_kblocks * (std::max(load, mma) + 0.1 * std::min(load, mma)) + epi;
       const double cost = waves * tile;
       if (cost < best * 0.999) {
         best = cost;
@@ -264,6 +277,15 @@ void choose_tiling(Plan* pl, const long long rows[], int num_phases, int max_kbl
       }
     }
   }
+  const int force_m = env_int("CONV_TILE_M");
+  const int force_n = env_int("CONV_TILE_N");
+  if (force_n >= 16 && force_n <= 256 && force_n % 16 == 0) {
+    best_bn = force_n;
+    best_nt = (c_out + force_n - 1) / force_n;
+    if (best_bn > 128) best_mh = 1;
+  }
+  if (force_m == 128) best_mh = 1;
+  if (force_m == 256 && best_bn <= 128) best_mh = 2;
   kp.bn = best_bn;
   kp.n_tiles = best_nt;
   kp.m_halves = best_mh;
@@ -301,7 +323,64 @@ conv_status_t check_fwd_shape(const FwdShape& f, int num_groups) {
   return CONV_OK;
 }
 
-conv_status_t plan_fwd(const FwdShape& f, Plan* pl, int num_sms) {
+uint32_t align1k(size_t v) { return static_cast<uint32_t>((v + 1023) & ~static_cast<size_t>(1023)); }
+
+// Row-window A loader for stride-1 forward convs: when a padded output row
+// (Wo + S - 1 pixels) fits in one 128-row MMA half, the tile's input rows are
+// loaded once per channel block and every filter tap reads them at a row
+// offset, instead of one im2col box per tap.  Needs 128-byte channel rows,
+// 16-byte output rows and one resident C_out tile.  CONV_WINDOW=-1 disables.
+conv_status_t layout_memory_window(Plan* pl, int has_residual);
+
+void plan_window(const FwdShape& f, Plan* pl, int num_sms, int has_residual) {
+  ConvKernelParams& kp = pl->kp;
+  kp.window = 0;
+  if (env_int("CONV_WINDOW") == -1) return;
+  if (f.stride_h != 1 || f.stride_w != 1 || f.dil_h != 1 || f.dil_w != 1) return;
+  if (kp.sw_bytes != 128 || !kp.vec_ok) return;
+  const int pitch = f.wo + f.s - 1;
+  if (pitch > kBM || f.c_out > 256) return;
+  const int bn = ((f.c_out + 15) / 16) * 16;
+  const size_t bres = static_cast<size_t>(f.r) * f.s * kp.c_blocks * bn * kp.sw_bytes;
+  if (bres > 120 * 1024) return;
+  const int mh = bn <= 128 ? 2 : 1;
+  const int rows = kBM / pitch;
+  const int rows_tile = mh * rows;
+  const int row_blocks = (f.ho + rows_tile - 1) / rows_tile;
+  (void)num_sms;
+  kp.window = 1;
+  kp.bn = bn;
+  kp.n_tiles = 1;
+  kp.m_halves = mh;
+  kp.acc_stride = static_cast<uint32_t>(mh * bn);
+  kp.tmem_cols = next_pow2_cols(2 * mh * bn);
+  kp.idesc = make_idesc(pl->in_dtype, bn);
+  kp.win_pitch = pitch;
+  kp.win_rows = rows;
+  kp.win_half_rows = rows * pitch;
+  kp.win_box_rows = rows_tile + f.r - 1;
+  kp.win_row_blocks = row_blocks;
+  kp.win_R = f.r;
+  kp.win_S = f.s;
+  kp.win_pad_h = f.pad_h;
+  kp.win_pad_w = f.pad_w;
+  // The last junk rows of the last half read past the box: cover them.
+  const int last_row = (mh - 1) * kp.win_half_rows + (f.r - 1) * pitch + (f.s - 1) + kBM;
+  const size_t rows_needed = std::max<size_t>(static_cast<size_t>(pitch) * kp.win_box_rows, last_row);
+  kp.win_stage_bytes = align1k(rows_needed * kp.sw_bytes);
+  kp.total_tiles = f.n * row_blocks;
+  kp.tile_start[0] = 0;
+  kp.tile_start[1] = kp.total_tiles;
+}
+
+// Tries the row-window plan; keeps the im2col plan if it does not fit.
+void plan_window_or_keep(const FwdShape& f, Plan* pl, int num_sms, int has_residual) {
+  const Plan saved = *pl;
+  plan_window(f, pl, num_sms, has_residual);
+  if (pl->kp.window && layout_memory_window(pl, has_residual) != CONV_OK) *pl = saved;
+}
+
+conv_status_t plan_fwd(const FwdShape& f, Plan* pl, int num_sms, int has_residual) {
   std::memset(pl, 0, sizeof(*pl));
   conv_status_t st = plan_channels(pl, f.in_dtype, f.c_in);
   if (st != CONV_OK) return st;
@@ -337,12 +416,32 @@ conv_status_t plan_fwd(const FwdShape& f, Plan* pl, int num_sms) {
   pl->phases_packed = 1;
   pl->kmax = f.r * f.s * f.c_in;
   pl->packed_bytes = static_cast<size_t>(f.c_out) * pl->kmax * elt_bytes(f.in_dtype);
+  plan_window_or_keep(f, pl, num_sms, has_residual);
   return CONV_OK;
 }
 
 // Encodes the forward conv's input map (lower corner -pad, upper corner
 // pad - (S-1)*dil, element strides = conv stride).
+conv_status_t encode_window_input(const FwdShape& f, const void* input, Plan* pl) {
+  const DriverFns* fns = driver_fns();
+  if (!fns) return CONV_ERR_CUDA;
+  const ConvKernelParams& kp = pl->kp;
+  const cuuint64_t e = static_cast<cuuint64_t>(elt_bytes(f.in_dtype));
+  cuuint64_t dims[4] = {static_cast<cuuint64_t>(f.c_in), static_cast<cuuint64_t>(f.w),
+                        static_cast<cuuint64_t>(f.h), static_cast<cuuint64_t>(f.n)};
+  cuuint64_t strides[3] = {dims[0] * e, dims[0] * dims[1] * e, dims[0] * dims[1] * dims[2] * e};
+  cuuint32_t box[4] = {static_cast<cuuint32_t>(kp.bk), static_cast<cuuint32_t>(kp.win_pitch),
+                       static_cast<cuuint32_t>(kp.win_box_rows), 1};
+  cuuint32_t estr[4] = {1, 1, 1, 1};
+  CUresult r = fns->tiled(&pl->kp.map_a[0], tmap_dtype(f.in_dtype), 4, const_cast<void*>(input),
+                          dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                          tmap_swizzle(kp.sw_bytes), CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? CONV_OK : CONV_ERR_CUDA;
+}
+
 conv_status_t encode_fwd_input(const FwdShape& f, const void* input, Plan* pl) {
+  if (pl->kp.window) return encode_window_input(f, input, pl);
   return encode_input_map(&pl->kp.map_a[0], input, f.n, f.h, f.w, f.c_in, f.in_dtype, pl->kp.bk,
                           pl->kp.sw_bytes, kBM * pl->kp.m_halves, -f.pad_w, -f.pad_h, f.pad_w - (f.s - 1) * f.dil_w,
                           f.pad_h - (f.r - 1) * f.dil_h, f.stride_w, f.stride_h);
@@ -607,13 +706,15 @@ conv_status_t encode_out_map_phase(CUtensorMap* map, const void* out, const Conv
   return r == CUDA_SUCCESS ? CONV_OK : CONV_ERR_CUDA;
 }
 
-uint32_t align1k(size_t v) { return static_cast<uint32_t>((v + 1023) & ~static_cast<size_t>(1023)); }
 
 // Picks the epilogue mode, the filter residency and the ring depth so that
 // everything fits in shared memory, and lays the buffers out.  No driver
 // calls: the TMA maps of the epilogue are encoded afterwards.
+conv_status_t layout_memory_window(Plan* pl, int has_residual);
+
 conv_status_t layout_memory(Plan* pl, int has_residual) {
   ConvKernelParams& kp = pl->kp;
+  if (kp.window) return layout_memory_window(pl, has_residual);
   // Epilogue mode: TMA tiles need 16-byte output rows; the transposed phase
   // grids additionally need every 128-row tile to be a rectangle of one image.
   int mode = 0;
@@ -640,7 +741,7 @@ conv_status_t layout_memory(Plan* pl, int has_residual) {
   if (kp.m_halves * (kp.bn / cw) < kEpilogueGroups && cw > 16) cw /= 2;
   const uint32_t a_bytes = kBM * kp.m_halves * kp.sw_bytes;
   const uint32_t b_bytes = static_cast<uint32_t>(kp.bn) * kp.sw_bytes;
-  const bool can_res = kp.num_phases == 1 && kp.n_tiles == 1;
+  const bool can_res = kp.num_phases == 1 && kp.n_tiles == 1 && !(std::getenv("CONV_FILTER_RESIDENT") && env_int("CONV_FILTER_RESIDENT") == 0);
   const size_t bres = can_res ? static_cast<size_t>(kp.taps_h[0]) * kp.taps_w[0] * kp.c_blocks * b_bytes : 0;
   const size_t src_tile = static_cast<size_t>(kBM) * kp.m_halves * kp.bn * 2;
   const size_t chunk = static_cast<size_t>(kBM) * cw * 2;
@@ -667,7 +768,8 @@ conv_status_t layout_memory(Plan* pl, int has_residual) {
                         kEpilogueGroups * opts[i].stgb * align1k(chunk);
     const size_t stage = a_bytes + (opts[i].res ? 0 : b_bytes);
     if (used + 2 * stage > kSmemLimit) continue;
-    const int st = static_cast<int>(std::min<size_t>(kMaxStages, (kSmemLimit - used) / stage));
+    int st = static_cast<int>(std::min<size_t>(kMaxStages, (kSmemLimit - used) / stage));
+    if (env_int("CONV_MAX_STAGES") >= 2) st = std::min(st, env_int("CONV_MAX_STAGES"));
     const double load = (a_bytes + (opts[i].res ? 0.0 : b_bytes)) / 70.0 + 40.0 * (opts[i].res ? 1 : 2);
     double key = load;
     if (st < 3) key += 1e6;
@@ -704,6 +806,80 @@ conv_status_t layout_memory(Plan* pl, int has_residual) {
   return CONV_OK;
 }
 
+// Row-window mode: the resident filter, an A ring of whole-tile boxes (at
+// least two), the residual-source tiles or output staging.
+conv_status_t layout_memory_window(Plan* pl, int has_residual) {
+  ConvKernelParams& kp = pl->kp;
+  int cw = 16;
+  for (int c : {64, 32, 16})
+    if (kp.bn % c == 0) {
+      cw = c;
+      break;
+    }
+  if (kp.m_halves * (kp.bn / cw) < kEpilogueGroups && cw > 16) cw /= 2;
+  const uint32_t b_bytes = static_cast<uint32_t>(kp.bn) * kp.sw_bytes;
+  const size_t bres = static_cast<size_t>(kp.win_R) * kp.win_S * kp.c_blocks * b_bytes;
+  const size_t src_tile = static_cast<size_t>(kBM) * kp.m_halves * kp.bn * 2;
+  const size_t chunk = static_cast<size_t>(kBM) * cw * 2;
+  const size_t bar_bytes = 1024;
+  const size_t stage = kp.win_stage_bytes;
+  int best_srcb = -1, best_stgb = -1, best_st = 0;
+  for (int srcb = has_residual ? 2 : 0; srcb >= (has_residual ? 1 : 0); --srcb)
+    for (int stgb = has_residual ? 0 : 2; stgb >= (has_residual ? 0 : 1); --stgb) {
+      const size_t used = 1024 + bar_bytes + align1k(bres) + srcb * align1k(src_tile) +
+                          kEpilogueGroups * stgb * align1k(chunk);
+      if (used + 2 * stage > kSmemLimit) continue;
+      int st = static_cast<int>(std::min<size_t>(kMaxStages, (kSmemLimit - used) / stage));
+      if (env_int("CONV_MAX_STAGES") >= 2) st = std::min(st, env_int("CONV_MAX_STAGES"));
+      if (st > best_st) {
+        best_st = st;
+        best_srcb = srcb;
+        best_stgb = stgb;
+      }
+    }
+  if (best_st < 2) {  // does not fit: plain im2col tiles
+    kp.window = 0;
+    return CONV_ERR_NOT_SUPPORTED;
+  }
+  kp.epi_mode = 3;
+  kp.cw = cw;
+  kp.b_resident = 1;
+  kp.src_bufs = best_srcb;
+  kp.stg_bufs = best_stgb;
+  kp.stages = best_st;
+  uint32_t off = 0;
+  kp.off_a = off;
+  off += align1k(static_cast<size_t>(best_st) * stage);
+  kp.off_b = off;
+  kp.off_bres = off;
+  off += align1k(bres);
+  kp.off_src = off;
+  off += best_srcb * align1k(src_tile);
+  kp.off_stg = off;
+  off += kEpilogueGroups * best_stgb * align1k(chunk);
+  kp.off_bar = off;
+  off += bar_bytes;
+  pl->smem_bytes = off + 1024;
+  return CONV_OK;
+}
+
+conv_status_t encode_out_map_window(CUtensorMap* map, const void* base, const ConvKernelParams& kp,
+                                    int n, conv_dtype_t out_dt) {
+  const DriverFns* fns = driver_fns();
+  if (!fns) return CONV_ERR_CUDA;
+  const cuuint64_t e = 2, C = static_cast<cuuint64_t>(kp.Cout);
+  cuuint64_t dims[4] = {C, static_cast<cuuint64_t>(kp.Wo), static_cast<cuuint64_t>(kp.Ho),
+                        static_cast<cuuint64_t>(n)};
+  cuuint64_t strides[3] = {C * e, C * e * kp.Wo, C * e * kp.Wo * kp.Ho};
+  cuuint32_t box[4] = {static_cast<cuuint32_t>(kp.cw), static_cast<cuuint32_t>(kp.win_pitch),
+                       static_cast<cuuint32_t>(kp.win_rows), 1};
+  cuuint32_t estr[4] = {1, 1, 1, 1};
+  CUresult r = fns->tiled(map, tmap_dtype(out_dt), 4, const_cast<void*>(base), dims, strides, box,
+                          estr, CU_TENSOR_MAP_INTERLEAVE_NONE, tmap_swizzle(kp.cw * 2),
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? CONV_OK : CONV_ERR_CUDA;
+}
+
 // Encodes the epilogue's output / source maps; falls back to the direct
 // epilogue if the driver rejects one of them.
 conv_status_t plan_memory(Plan* pl, int n_images, const void* output, const void* source,
@@ -712,7 +888,12 @@ conv_status_t plan_memory(Plan* pl, int n_images, const void* output, const void
   if (st != CONV_OK) return st;
   ConvKernelParams& kp = pl->kp;
   const conv_dtype_t out_dt = pl->out_bf16 ? CONV_DTYPE_BF16 : CONV_DTYPE_F16;
-  if (kp.epi_mode == 1) {
+  if (kp.epi_mode == 3) {
+    if (encode_out_map_window(&kp.map_out[0], output, kp, n_images, out_dt) != CONV_OK ||
+        (has_residual &&
+         encode_out_map_window(&kp.map_src[0], source, kp, n_images, out_dt) != CONV_OK))
+      return CONV_ERR_CUDA;
+  } else if (kp.epi_mode == 1) {
     const long long rows = kp.rows[0];
     if (encode_out_map_2d(&kp.map_out[0], output, kp.Cout, rows, out_dt, kp.cw) != CONV_OK ||
         (has_residual &&
@@ -790,6 +971,9 @@ conv_status_t finish_and_launch(Plan* pl, int n_images, const void* packed, void
   const unsigned long long tmo = g_timeout_ns.load(std::memory_order_relaxed);
   kp.timeout_cycles = ns_to_cycles(tmo ? tmo : kDefaultTimeoutNs);
   kp.fault_mode = g_fault_mode.load(std::memory_order_relaxed);
+  // Prefetching the next tile's input only pays when CTAs walk several tiles
+  // that all start at the first C_out tile (one n-tile).
+  kp.l2_prefetch = (kp.n_tiles == 1 && env_int("CONV_L2_PREFETCH") != -1) ? 1 : 0;
   if (kp.total_tiles == 0) return CONV_OK;
   const int sms = device_sm_count();
   if (sms <= 0) return CONV_ERR_CUDA;
@@ -859,7 +1043,7 @@ conv_status_t fwd_impl(const void* input, const FwdShape& f, const void* filter,
   const int sms = device_sm_count();
   if (sms <= 0) return CONV_ERR_CUDA;
   Plan pl;
-  st = plan_fwd(f, &pl, sms);
+  st = plan_fwd(f, &pl, sms, has_residual);
   if (st != CONV_OK) return st;
   st = encode_fwd_input(f, input, &pl);
   if (st != CONV_OK) return st;
@@ -1166,7 +1350,7 @@ conv_status_t conv_testing_fwd_plan(int n, int h, int w, int c_in, conv_dtype_t 
   conv_status_t st = check_fwd_shape(f, 1);
   if (st != CONV_OK) return st;
   Plan pl;
-  st = plan_fwd(f, &pl, num_sms);
+  st = plan_fwd(f, &pl, num_sms, has_residual);
   if (st != CONV_OK) return st;
   st = layout_memory(&pl, has_residual);
   if (st != CONV_OK) return st;
@@ -1202,9 +1386,10 @@ conv_status_t conv_testing_im2col_tile(const void* input, int n, int h, int w, i
   conv_status_t st = check_fwd_shape(f, 1);
   if (st != CONV_OK) return st;
   Plan pl;
-  st = plan_fwd(f, &pl, 1);
+  st = plan_fwd(f, &pl, 1, 0);
   if (st != CONV_OK) return st;
-  pl.kp.m_halves = 1;  // the probe copies out one 128-row column
+  pl.kp.m_halves = 1;  // the probe copies out one 128-row column of an im2col load
+  pl.kp.window = 0;
   if (m0 < 0 || m0 >= pl.kp.rows[0] || tap_r < 0 || tap_r >= r || tap_s < 0 || tap_s >= s ||
       c0 < 0 || c0 >= c_in || c0 % pl.kp.bk != 0)
     return CONV_ERR_INVALID_VALUE;

@@ -42,6 +42,14 @@ struct TileInfo {
 };
 
 __device__ __forceinline__ TileInfo decode_tile(const ConvKernelParams& p, int t) {
+  if (p.window) {  // one C_out tile; m0 carries the tile index
+    TileInfo ti;
+    ti.phase = 0;
+    ti.n0 = 0;
+    ti.m0 = t;
+    ti.kblocks = p.c_blocks;
+    return ti;
+  }
   int ph = 0;
   while (ph + 1 < p.num_phases && t >= p.tile_start[ph + 1]) ++ph;
   const int local = t - p.tile_start[ph];
@@ -51,6 +59,13 @@ __device__ __forceinline__ TileInfo decode_tile(const ConvKernelParams& p, int t
   ti.m0 = (local / p.n_tiles) * (kBM * p.m_halves);
   ti.kblocks = p.taps_h[ph] * p.taps_w[ph] * p.c_blocks;
   return ti;
+}
+
+// Image and first output row of row-window tile t.
+__device__ __forceinline__ void window_origin(const ConvKernelParams& p, int t, int& n_img,
+                                              int& oy0) {
+  n_img = t / p.win_row_blocks;
+  oy0 = (t - n_img * p.win_row_blocks) * (p.win_rows * p.m_halves);
 }
 
 // (image, grid row, grid column) of GEMM row m in phase ph.
@@ -235,7 +250,10 @@ __device__ __forceinline__ void issue_source_items(const ConvKernelParams& p, co
   const int nitems = nchunks * p.m_halves;
   const int mine = (nitems - grp + kEpilogueGroups - 1) / kEpilogueGroups;
   if (mine <= 0) return;
-  mbar_arrive_expect_tx(bar, chunk_bytes * mine);
+  // A row-window half fills only its win_half_rows rows of the chunk buffer.
+  const uint32_t box_bytes =
+      p.epi_mode == 3 ? static_cast<uint32_t>(p.win_half_rows) * p.cw * 2 : chunk_bytes;
+  mbar_arrive_expect_tx(bar, box_bytes * mine);
   for (int q = grp; q < nitems; q += kEpilogueGroups) {
     const int h = q / nchunks;
     const int c = q - h * nchunks;
@@ -243,6 +261,10 @@ __device__ __forceinline__ void issue_source_items(const ConvKernelParams& p, co
     const uint32_t dst = smem_u32(buf + q * chunk_bytes);
     if (p.epi_mode == 1) {
       tma_load_2d(dst, &p.map_src[ti.phase], bar, ti.n0 + c * p.cw, mh);
+    } else if (p.epi_mode == 3) {
+      int n_img, oy0;
+      window_origin(p, ti.m0, n_img, oy0);
+      tma_load_4d(dst, &p.map_src[0], bar, ti.n0 + c * p.cw, 0, oy0 + h * p.win_rows, n_img);
     } else {
       int n_img, j, i;
       grid_pos(p, ti.phase, mh, n_img, j, i);
@@ -342,6 +364,77 @@ __device__ __forceinline__ bool mma_role(const ConvKernelParams& p, uint32_t tme
   return ok;
 }
 
+// The MMA role of the row-window loader: one A box per channel block holds
+// the tile's input rows with halo; tap (r, s) of half h starts at box row
+// h*win_half_rows + r*win_pitch + s.  The filter is resident: block
+// (tap, cb) of the packed filter sits at index tap*c_blocks + cb.
+template <int kKind, int kSteps, int kHalves>
+__device__ __forceinline__ bool mma_role_window(const ConvKernelParams& p, uint32_t tmem_base,
+                                                uint8_t* a_ring, uint8_t* b_res, uint64_t* full,
+                                                uint64_t* empty, uint64_t* tfull, uint64_t* tempty,
+                                                volatile int* abort_flag, unsigned int* status,
+                                                long long limit) {
+  const int stages = p.stages;
+  const uint32_t sw = p.sw_bytes;  // 128 in this mode
+  const uint32_t b_bytes = static_cast<uint32_t>(p.bn) * sw;
+  const uint64_t desc_hi = smem_desc_kmajor(0, sw);
+  const uint32_t a_lo0 = smem_u32(a_ring) >> 4;
+  const uint32_t b_lo0 = smem_u32(b_res) >> 4;
+  const uint32_t a_step = p.win_stage_bytes >> 4;
+  const uint32_t b_step = b_bytes >> 4;
+  const uint32_t row_lo = sw >> 4;  // one box row in descriptor address units
+  const uint32_t half_lo = static_cast<uint32_t>(p.win_half_rows) * row_lo;
+  const uint32_t bn_cols = static_cast<uint32_t>(p.bn);
+  const uint32_t idesc = p.idesc;
+  const uint32_t full0 = smem_u32(full), empty0 = smem_u32(empty);
+  const int taps_s = p.win_S;
+  const int taps = p.win_R * p.win_S;
+  int stage = 0;
+  uint32_t phase = 0;
+  uint32_t a_lo = a_lo0;
+  bool ok = true;
+  int it = 0;
+  for (int t = blockIdx.x; ok && t < p.total_tiles; t += gridDim.x, ++it) {
+    const int acc = it & 1;
+    if (!mbar_wait_bounded(smem_u32(&tempty[acc]), static_cast<uint32_t>(((it >> 1) & 1) ^ 1),
+                           abort_flag, status, kStatusMmaTimeout, limit)) {
+      ok = false;
+      break;
+    }
+    tc_fence_after();
+    const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc) * p.acc_stride;
+    for (int cb = 0; cb < p.c_blocks; ++cb) {
+      if (!mbar_wait_bounded(full0 + 8u * stage, phase, abort_flag, status, kStatusMmaTimeout,
+                             limit)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      int r = 0, s = 0;
+      for (int tap = 0; tap < taps; ++tap) {
+        const uint32_t tap_lo = a_lo + static_cast<uint32_t>(r * p.win_pitch + s) * row_lo;
+        const uint32_t b_lo = b_lo0 + static_cast<uint32_t>(tap * p.c_blocks + cb) * b_step;
+        issue_kblock<kKind, kSteps, kHalves>(d_tmem, desc_hi, tap_lo, b_lo, half_lo, bn_cols,
+                                             idesc, (cb | tap) != 0 ? 1u : 0u);
+        if (++s == taps_s) {
+          s = 0;
+          ++r;
+        }
+      }
+      mma_commit(empty0 + 8u * stage);
+      a_lo += a_step;
+      if (++stage == stages) {
+        stage = 0;
+        phase ^= 1u;
+        a_lo = a_lo0;
+      }
+    }
+    if (!ok) break;
+    mma_commit(smem_u32(&tfull[acc]));
+  }
+  return ok;
+}
+
 template <int kKind, typename OutT>
 __global__ void __launch_bounds__(kThreads, 1)
     conv_igemm_kernel(const __grid_constant__ ConvKernelParams p) {
@@ -417,7 +510,42 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = true;
       const uint32_t stage_tx = a_bytes + (p.b_resident ? 0u : b_bytes);
       bool first_tile = true;  // a resident filter is loaded k-block by k-block with it
-      for (int t = blockIdx.x; t < p.total_tiles && ok; t += gridDim.x) {
+      if (p.window) {
+        // One tiled box of input rows (with halo) per channel block; the
+        // first tile also brings every tap's filter block of that channel block.
+        const uint32_t box_bytes = static_cast<uint32_t>(p.win_pitch * p.win_box_rows) * sw;
+        const int taps = p.win_R * p.win_S;
+        for (int t = blockIdx.x; t < p.total_tiles && ok; t += gridDim.x) {
+          int n_img, oy0;
+          window_origin(p, t, n_img, oy0);
+          for (int cb = 0; cb < p.c_blocks; ++cb, ++seq) {
+            if ((seq & 1) == role) {
+              if (!mbar_wait_bounded(smem_u32(&empty[stage]), phase ^ 1u, abort_flag, status,
+                                     kStatusProducerTimeout, limit)) {
+                ok = false;
+                break;
+              }
+              last_issued = seq;
+              if (!(p.fault_mode == 1 && blockIdx.x == 0 && seq == 0)) {
+                const uint32_t fb = smem_u32(&full[stage]);
+                mbar_arrive_expect_tx(fb, box_bytes + (first_tile ? b_bytes * taps : 0u));
+                tma_load_4d(smem_u32(a_ring + stage * p.win_stage_bytes), &p.map_a[0], fb,
+                            cb * p.bk, -p.win_pad_w, oy0 - p.win_pad_h, n_img);
+                if (first_tile)
+                  for (int tap = 0; tap < taps; ++tap)
+                    tma_load_3d(smem_u32(b_res + (tap * p.c_blocks + cb) * b_bytes), &p.map_b, fb,
+                                tap * p.c_in + cb * p.bk, 0, 0);
+              }
+            }
+            if (++stage == stages) {
+              stage = 0;
+              phase ^= 1u;
+            }
+          }
+          first_tile = false;
+        }
+      }
+      for (int t = blockIdx.x; !p.window && t < p.total_tiles && ok; t += gridDim.x) {
         const TileInfo ti = decode_tile(p, t);
         const int ph = ti.phase;
         int n_img, j, i;
@@ -431,6 +559,21 @@ __global__ void __launch_bounds__(kThreads, 1)
         int bk_k = 0;  // k coordinate of this k-block in the packed filter: tap*C_in + cb*bk
         const bool load_res = p.b_resident && first_tile;
         first_tile = false;
+        // This CTA's next tile: its A boxes are prefetched into L2 alongside
+        // this tile's loads, so they come from L2 rather than HBM later.
+        const int tn = t + static_cast<int>(gridDim.x);
+        const bool pf = p.l2_prefetch && tn < p.total_tiles;
+        int pf_n = 0, pf_h0 = 0, pf_w0 = 0;
+        const CUtensorMap* pf_map = amap;
+        if (pf) {
+          const TileInfo tin = decode_tile(p, tn);
+          int pj, pi;
+          grid_pos(p, tin.phase, tin.m0, pf_n, pj, pi);
+          pf_h0 = p.base_h[tin.phase] + pj * p.step_h;
+          pf_w0 = p.base_w[tin.phase] + pi * p.step_w;
+          pf_map = &p.map_a[tin.phase];
+          if (tin.kblocks != ti.kblocks || tin.n0 != 0 || tin.m0 == ti.m0) pf_n = -1;  // skip
+        }
         for (int kb = 0; kb < ti.kblocks; ++kb, ++seq) {
           if ((seq & 1) == role) {
             if (!mbar_wait_bounded(smem_u32(&empty[stage]), phase ^ 1u, abort_flag, status,
@@ -451,6 +594,10 @@ __global__ void __launch_bounds__(kThreads, 1)
               else if (load_res)
                 tma_load_3d(smem_u32(b_res + kb * b_bytes), &p.map_b, fb, bk_k, 0, bz);
             }
+            if (pf && pf_n >= 0)
+              tma_prefetch_im2col_4d(pf_map, cb * p.bk, pf_w0, pf_h0, pf_n,
+                                     static_cast<uint16_t>(uw * p.dil_w),
+                                     static_cast<uint16_t>(uh * p.dil_h));
           }
           if (++stage == stages) {
             stage = 0;
@@ -481,6 +628,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       bool ok;
       const int ks = static_cast<int>(sw / 32);
+      if (p.window) {
+        ok = p.m_halves == 2
+                 ? mma_role_window<kKind, 4, 2>(p, tmem_base, a_ring, b_res, full, empty, tfull,
+                                                tempty, abort_flag, status, limit)
+                 : mma_role_window<kKind, 4, 1>(p, tmem_base, a_ring, b_res, full, empty, tfull,
+                                                tempty, abort_flag, status, limit);
+        if (!ok) {
+          mma_commit(smem_u32(drain));
+          mbar_wait_drain(smem_u32(drain), 0, limit / 8 + 1);
+        }
+      } else {
 #define CONV_MMA_ROLE(KS, MH)                                                                   \
   mma_role<kKind, KS, MH>(p, tmem_base, a_ring, b_ring, b_res, full, empty, tfull, tempty, bres_full, \
                           abort_flag, status, limit)
@@ -493,6 +651,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // Every MMA already issued must finish before TMEM is released.
         mma_commit(smem_u32(drain));
         mbar_wait_drain(smem_u32(drain), 0, limit / 8 + 1);
+      }
       }
     }
     __syncwarp();
@@ -602,6 +761,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (leader) {
             if (p.epi_mode == 1) {
               tma_store_2d(&p.map_out[ti.phase], smem_u32(buf), ti.n0 + c * p.cw, mh);
+            } else if (p.epi_mode == 3) {
+              int n_img, oy0;
+              window_origin(p, ti.m0, n_img, oy0);
+              tma_store_4d(&p.map_out[0], smem_u32(buf), ti.n0 + c * p.cw, 0,
+                           oy0 + h * p.win_rows, n_img);
             } else {
               int n_img, gj, gi;
               grid_pos(p, ti.phase, mh, n_img, gj, gi);

@@ -41,6 +41,7 @@ struct ConvKernelParams {  // aligned like CUtensorMap (64 B or more)
   int bk;               // input channels per k-block
   int c_blocks;         // ceil(C_in / bk): channel blocks per filter tap
   int c_tail;           // C_in - c_blocks * bk (<= 0): k adjustment after a tap's last block
+  int c_in;
   int stages;           // depth of the shared-memory ring
   uint32_t sw_bytes;    // bytes per operand row in a k-block (32, 64 or 128) = swizzle span
   uint32_t idesc;       // tcgen05 instruction descriptor
@@ -66,6 +67,21 @@ struct ConvKernelParams {  // aligned like CUtensorMap (64 B or more)
   // Shared-memory carve-up (byte offsets from the 1024-B aligned base).
   uint32_t off_a, off_b, off_bres, off_src, off_stg, off_bar;
   int b_resident;                  // whole packed filter kept in shared memory (one phase, one n-tile)
+  int l2_prefetch;                 // prefetch the next tile's A boxes into L2
+
+  // Row-window A loader (stride-1 forward convs): a tile is win_rows output
+  // rows per 128-row half; its input rows (with halo) arrive as one tiled box
+  // [win_box_rows][win_pitch][bk] per channel block, and filter tap (r, s)
+  // reads it from row r*win_pitch + s on.  win_pitch = Wo + S - 1 <= 128.
+  int window;
+  int win_pitch;
+  int win_rows;                    // output rows per 128-row half
+  int win_half_rows;               // shared-memory rows per half = win_rows * win_pitch
+  int win_box_rows;                // input rows per box = m_halves * win_rows + R - 1
+  int win_row_blocks;              // tiles per image = ceil(Ho / (m_halves * win_rows))
+  int win_R, win_S;                // filter extent
+  int win_pad_h, win_pad_w;
+  uint32_t win_stage_bytes;        // A stage size (box plus the rows junk MMA rows may read)
   int epi_mode;                    // 0 direct stores, 1 TMA store [M][C_out], 2 TMA store 4-D phase grid
   int cw;                          // epilogue chunk width in columns (16, 32 or 64)
   int src_bufs;                    // residual-source tile buffers (0, 1 or 2)

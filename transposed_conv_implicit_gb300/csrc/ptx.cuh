@@ -167,6 +167,16 @@ __device__ __forceinline__ void tma_load_im2col_4d(uint32_t dst, const CUtensorM
       : "memory");
 }
 
+// L2 prefetch of the same im2col box (no shared memory, no barrier).
+__device__ __forceinline__ void tma_prefetch_im2col_4d(const CUtensorMap* map, int c, int w, int h,
+                                                       int n, uint16_t w_off, uint16_t h_off) {
+  asm volatile(
+      "cp.async.bulk.prefetch.tensor.4d.L2.global.im2col [%0, {%1, %2, %3, %4}], {%5, %6};" ::"l"(
+          reinterpret_cast<uint64_t>(map)),
+      "r"(c), "r"(w), "r"(h), "r"(n), "h"(w_off), "h"(h_off)
+      : "memory");
+}
+
 // ---------------------------------------------------------------- tcgen05
 __device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols) {
   asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem),
