@@ -8,9 +8,12 @@ stride-2 downsample 32x56x56x64 -> 32x28x28x128.  Filters are packed once
 before timing (the pack is timed separately and reported as pack_us).
 
 Timing: W warm-up steps, then K steps, each preceded by an L2 flush (a write
-of max(2 x L2, 256 MiB), outside the events); every launch is bracketed by
-CUDA events on the stream it runs on; the barrier + synchronize bracket the
-region; the step time is the max over ranks.  One JSON line on rank 0.
+of max(2 x L2, 256 MiB), outside the events).  Each step is bracketed by CUDA
+events on the launch stream; its launches follow each other directly (a conv
+may set up while the previous one drains: programmatic dependent launch).  A
+barrier + synchronize bracket the region; the step time is the max over
+ranks.  Per-kernel durations for the roofline come from a second loop in
+which every launch has its own events.  One JSON line on rank 0.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                   [--workload resnet_block|<one of synthetic.WORKLOADS>]
@@ -345,13 +348,9 @@ def run_ours(args, world, rank, local):
     l2 = int(getattr(props, "L2_cache_size", 128 << 20))
     flush = torch.empty(max(2 * l2, 256 << 20), dtype=torch.uint8, device=dev)
 
-    def step(evs=None):
-        for i, call in enumerate(calls):
-            if evs is not None:
-                evs[i].record(stream)
+    def step():
+        for call in calls:
             call()
-        if evs is not None:
-            evs[len(calls)].record(stream)
 
     for _ in range(args.warmup):
         flush.fill_(1)
@@ -361,7 +360,11 @@ def run_ours(args, world, rank, local):
     if status != 0:
         raise RuntimeError("device status after warm-up: %s (bits %d)" % (cg.conv_status_string(status), bits))
 
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(calls) + 1)] for _ in range(args.steps)]
+    # Timed region: K steps, each after an L2 flush (outside the events); the
+    # step's launches are back to back, so a conv may start its set-up while
+    # the previous one drains (programmatic dependent launch).
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
     sampler = ClockSampler(local) if rank == 0 or world > 1 else None
     if sampler:
         sampler.start()
@@ -371,7 +374,9 @@ def run_ours(args, world, rank, local):
     wall0 = time.perf_counter()
     for k in range(args.steps):
         flush.fill_(1)
-        step(ev[k])
+        ev[k][0].record(stream)
+        step()
+        ev[k][1].record(stream)
     torch.cuda.synchronize(dev)
     wall = time.perf_counter() - wall0
     dist_barrier(world)
@@ -379,10 +384,21 @@ def run_ours(args, world, rank, local):
     status, bits = cg.conv_check_device_status(workspace)
     if status != 0:
         raise RuntimeError("device status after timing: %s (bits %d)" % (cg.conv_status_string(status), bits))
+    step_ms = [a.elapsed_time(b) for a, b in ev]
 
-    per_kernel_ms = [[ev[k][i].elapsed_time(ev[k][i + 1]) for k in range(args.steps)]
+    # Per-kernel durations (for the roofline): every launch bracketed by its
+    # own events on the launch stream, each step after an L2 flush.
+    kreps = max(10, min(args.steps, 100))
+    kev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(calls) + 1)] for _ in range(kreps)]
+    for k in range(kreps):
+        flush.fill_(1)
+        for i, call in enumerate(calls):
+            kev[k][i].record(stream)
+            call()
+        kev[k][len(calls)].record(stream)
+    torch.cuda.synchronize(dev)
+    per_kernel_ms = [[kev[k][i].elapsed_time(kev[k][i + 1]) for k in range(kreps)]
                      for i in range(len(calls))]
-    step_ms = [ev[k][0].elapsed_time(ev[k][len(calls)]) for k in range(args.steps)]
     total_ms = dist_max(sum(step_ms), world, dev)
     ms_per_step = total_ms / args.steps
     flops_step = sum(c.flops for c in cases)
@@ -434,12 +450,14 @@ def run_ours(args, world, rank, local):
                    "l2": "flushed before every step (write of %d MiB), flush outside the events"
                          % (flush.numel() >> 20),
                    "filters": "packed once before timing",
+                   "per_kernel_timing": "separate loop, each launch bracketed by events",
                    "parallelism": "replicas" if world > 1 else "single GPU",
                    "gpu": props.name, "sms": props.multi_processor_count},
         "roofline": roof,
         "cpu_baseline": cpu,
         "e2e": e2e,
         "gpu_launches": len(calls) * args.steps,
+        "step_us_p10_p90": [round(_pct(step_ms, 10) * 1e3, 2), round(_pct(step_ms, 90) * 1e3, 2)],
         "clocks": clocks,
         "pack_us": round(pack_us, 2),
         "per_kernel": per_kernel,
@@ -534,7 +552,7 @@ def run_e2e(args, cases, inputs, dev, stream):
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--steps", type=int, default=1000)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--workload", default="resnet_block")

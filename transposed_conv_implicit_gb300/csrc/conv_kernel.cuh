@@ -496,6 +496,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  // Set-up above may overlap the previous kernel in the stream; every global
+  // memory access below comes after that kernel has completed.
+  grid_dependency_wait();
+  grid_launch_dependents();
 
   if (warp == 0 || warp == kThreads / 32 - 1) {
     // ------------------------------------------------------------ producers

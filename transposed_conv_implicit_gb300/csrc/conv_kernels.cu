@@ -27,7 +27,21 @@ cudaError_t launch_instance(const ConvKernelParams& p, int grid, size_t smem_byt
     if (err != cudaSuccess) return err;
     configured[dev].store(smem_bytes, std::memory_order_relaxed);
   }
-  conv_igemm_kernel<kKind, OutT><<<grid, kThreads, smem_bytes, stream>>>(p);
+  // Programmatic stream serialization: the kernel may be scheduled while the
+  // previous kernel of the stream drains; it waits (griddepcontrol.wait)
+  // before touching global memory, so stream order is preserved.
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(grid));
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem_bytes;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  err = cudaLaunchKernelEx(&cfg, conv_igemm_kernel<kKind, OutT>, p);
+  if (err != cudaSuccess) return err;
   return cudaGetLastError();
 }
 

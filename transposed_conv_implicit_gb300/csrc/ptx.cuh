@@ -16,6 +16,17 @@ __device__ __forceinline__ uint32_t smem_u32(const void* p) {
 // (the global nanosecond timer costs hundreds of cycles per read).
 __device__ __forceinline__ long long cycle_count() { return clock64(); }
 
+// Programmatic dependent launch: wait until the grids this one depends on
+// have completed and their memory is visible (a no-op when the launch had no
+// programmatic dependency), and allow dependent grids to start launching.
+__device__ __forceinline__ void grid_dependency_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+__device__ __forceinline__ void grid_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ---------------------------------------------------------------- mbarrier
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
