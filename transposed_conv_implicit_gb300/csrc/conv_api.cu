@@ -787,6 +787,8 @@ conv_status_t layout_memory(Plan* pl, int has_residual) {
   kp.cw = cw;
   kp.b_resident = o.res ? 1 : 0;
   kp.src_bufs = o.srcb;
+  kp.src_chunk_bytes = static_cast<uint32_t>(chunk);
+  kp.valid_rows = kBM;
   kp.stg_bufs = o.stgb;
   kp.stages = best_stages;
   uint32_t off = 0;
@@ -819,7 +821,9 @@ conv_status_t layout_memory_window(Plan* pl, int has_residual) {
   if (kp.m_halves * (kp.bn / cw) < kEpilogueGroups && cw > 16) cw /= 2;
   const uint32_t b_bytes = static_cast<uint32_t>(kp.bn) * kp.sw_bytes;
   const size_t bres = static_cast<size_t>(kp.win_R) * kp.win_S * kp.c_blocks * b_bytes;
-  const size_t src_tile = static_cast<size_t>(kBM) * kp.m_halves * kp.bn * 2;
+  // A source chunk holds only the half's stored rows (win_half_rows of 128).
+  const size_t src_chunk = align1k(static_cast<size_t>(kp.win_half_rows) * cw * 2);
+  const size_t src_tile = src_chunk * kp.m_halves * (kp.bn / cw);
   const size_t chunk = static_cast<size_t>(kBM) * cw * 2;
   const size_t bar_bytes = 1024;
   const size_t stage = kp.win_stage_bytes;
@@ -845,6 +849,8 @@ conv_status_t layout_memory_window(Plan* pl, int has_residual) {
   kp.cw = cw;
   kp.b_resident = 1;
   kp.src_bufs = best_srcb;
+  kp.src_chunk_bytes = static_cast<uint32_t>(src_chunk);
+  kp.valid_rows = kp.win_half_rows;
   kp.stg_bufs = best_stgb;
   kp.stages = best_st;
   uint32_t off = 0;
@@ -919,6 +925,8 @@ conv_status_t plan_memory_direct(Plan* pl) {
   kp.cw = 16;
   kp.src_bufs = 0;
   kp.stg_bufs = 0;
+  kp.src_chunk_bytes = 0;
+  kp.valid_rows = kBM;
   const bool can_res = kp.num_phases == 1 && kp.n_tiles == 1;
   const size_t bres = can_res ? static_cast<size_t>(kp.taps_h[0]) * kp.taps_w[0] * kp.c_blocks * b_bytes : 0;
   bool res = false;
@@ -970,6 +978,10 @@ conv_status_t finish_and_launch(Plan* pl, int n_images, const void* packed, void
   kp.status = static_cast<unsigned int*>(workspace);
   const unsigned long long tmo = g_timeout_ns.load(std::memory_order_relaxed);
   kp.timeout_cycles = ns_to_cycles(tmo ? tmo : kDefaultTimeoutNs);
+  {
+    const char* h = std::getenv("CONV_WAIT_HINT_NS");
+    kp.wait_hint_ns = h ? static_cast<uint32_t>(std::atoi(h)) : 0u;
+  }
   kp.fault_mode = g_fault_mode.load(std::memory_order_relaxed);
   // Prefetching the next tile's input only pays when CTAs walk several tiles
   // that all start at the first C_out tile (one n-tile).

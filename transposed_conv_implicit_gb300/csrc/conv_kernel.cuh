@@ -258,7 +258,7 @@ __device__ __forceinline__ void issue_source_items(const ConvKernelParams& p, co
     const int h = q / nchunks;
     const int c = q - h * nchunks;
     const int mh = ti.m0 + h * kBM;
-    const uint32_t dst = smem_u32(buf + q * chunk_bytes);
+    const uint32_t dst = smem_u32(buf + q * p.src_chunk_bytes);
     if (p.epi_mode == 1) {
       tma_load_2d(dst, &p.map_src[ti.phase], bar, ti.n0 + c * p.cw, mh);
     } else if (p.epi_mode == 3) {
@@ -525,7 +525,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int cb = 0; cb < p.c_blocks; ++cb, ++seq) {
             if ((seq & 1) == role) {
               if (!mbar_wait_bounded(smem_u32(&empty[stage]), phase ^ 1u, abort_flag, status,
-                                     kStatusProducerTimeout, limit)) {
+                                     kStatusProducerTimeout, limit, p.wait_hint_ns)) {
                 ok = false;
                 break;
               }
@@ -581,7 +581,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int kb = 0; kb < ti.kblocks; ++kb, ++seq) {
           if ((seq & 1) == role) {
             if (!mbar_wait_bounded(smem_u32(&empty[stage]), phase ^ 1u, abort_flag, status,
-                                   kStatusProducerTimeout, limit)) {
+                                   kStatusProducerTimeout, limit, p.wait_hint_ns)) {
               ok = false;
               break;
             }
@@ -676,7 +676,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t chunk_bytes = kBM * row_bytes;
       const int nchunks = p.bn / p.cw;
       const int nitems = nchunks * p.m_halves;
-      const uint32_t src_tile_bytes = chunk_bytes * nitems;
+      const uint32_t src_tile_bytes = p.src_chunk_bytes * nitems;
       const bool in_place = p.has_residual != 0;  // outputs overwrite the source chunk, stored from there
       uint8_t* stg_grp = stg_base + grp * (p.stg_bufs * chunk_bytes);
       int store_seq = 0;
@@ -700,11 +700,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
         bool ok = mbar_wait_bounded(smem_u32(&tfull[acc]), static_cast<uint32_t>((it >> 1) & 1),
-                                    abort_flag, status, kStatusEpilogueTimeout, limit);
+                                    abort_flag, status, kStatusEpilogueTimeout, limit,
+                                    p.wait_hint_ns);
         if (ok && p.has_residual && grp < nitems) {
           const uint32_t par = static_cast<uint32_t>(p.src_bufs == 2 ? (it >> 1) & 1 : it & 1);
           ok = mbar_wait_bounded(smem_u32(&src_full[2 * sbuf + grp]), par, abort_flag, status,
-                                 kStatusEpilogueTimeout, limit);
+                                 kStatusEpilogueTimeout, limit, p.wait_hint_ns);
         }
         if (!__all_sync(0xFFFFFFFFu, ok)) break;
         tc_fence_after();
@@ -743,7 +744,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           uint8_t* buf;
           if (in_place) {
-            buf = src_tile + q * chunk_bytes;
+            buf = src_tile + q * p.src_chunk_bytes;
           } else {
             buf = stg_grp + (p.stg_bufs == 2 ? (store_seq & 1) : 0) * chunk_bytes;
             if (leader) {
@@ -754,12 +755,19 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             named_barrier(bar_id, 128);
           }
-          if (p.cw == 64)
-            process_row_act<OutT, 64>(v, buf, static_cast<uint32_t>(row), p.beta, p.epilogue, in_place);
-          else if (p.cw == 32)
-            process_row_act<OutT, 32>(v, buf, static_cast<uint32_t>(row), p.beta, p.epilogue, in_place);
-          else
-            process_row_act<OutT, 16>(v, buf, static_cast<uint32_t>(row), p.beta, p.epilogue, in_place);
+          // Lanes past valid_rows (the junk rows of a row-window half) are
+          // never stored: they neither read nor write the buffer.
+          if (row < p.valid_rows) {
+            if (p.cw == 64)
+              process_row_act<OutT, 64>(v, buf, static_cast<uint32_t>(row), p.beta, p.epilogue,
+                                        in_place);
+            else if (p.cw == 32)
+              process_row_act<OutT, 32>(v, buf, static_cast<uint32_t>(row), p.beta, p.epilogue,
+                                        in_place);
+            else
+              process_row_act<OutT, 16>(v, buf, static_cast<uint32_t>(row), p.beta, p.epilogue,
+                                        in_place);
+          }
           fence_proxy_async_shared();
           named_barrier(bar_id, 128);
           if (leader) {
@@ -804,7 +812,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const TileInfo ti = decode_tile(p, t);
         const int acc = it & 1;
         bool ok = mbar_wait_bounded(smem_u32(&tfull[acc]), static_cast<uint32_t>((it >> 1) & 1),
-                                    abort_flag, status, kStatusEpilogueTimeout, limit);
+                                    abort_flag, status, kStatusEpilogueTimeout, limit,
+                                    p.wait_hint_ns);
         if (!__all_sync(0xFFFFFFFFu, ok)) break;
         tc_fence_after();
         const int ph = ti.phase;

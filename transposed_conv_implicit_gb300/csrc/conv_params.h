@@ -85,6 +85,8 @@ struct ConvKernelParams {  // aligned like CUtensorMap (64 B or more)
   int epi_mode;                    // 0 direct stores, 1 TMA store [M][C_out], 2 TMA store 4-D phase grid
   int cw;                          // epilogue chunk width in columns (16, 32 or 64)
   int src_bufs;                    // residual-source tile buffers (0, 1 or 2)
+  uint32_t src_chunk_bytes;        // stride of one (half, chunk) item in a source buffer
+  int valid_rows;                  // TMEM lanes per half that map to stored rows (128, or win_half_rows)
   int stg_bufs;                    // output staging buffers per epilogue group (0: in place)
 
   int Ho, Wo, Cout;
@@ -96,6 +98,7 @@ struct ConvKernelParams {  // aligned like CUtensorMap (64 B or more)
   void* out;
   unsigned int* status;
   long long timeout_cycles;        // limit of every bounded wait, in SM cycles
+  uint32_t wait_hint_ns;           // suspend hint for waits off the MMA's critical path (0: poll)
   int fault_mode;                  // test hook: 1 = CTA 0 skips its first arrive
 };
 

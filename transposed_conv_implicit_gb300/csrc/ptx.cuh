@@ -49,6 +49,20 @@ __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
 
+// try_wait with a suspend-time hint: the thread may sleep (up to hint_ns)
+// until the phase completes instead of polling.
+__device__ __forceinline__ bool mbar_try_wait_hint(uint32_t bar, uint32_t parity, uint32_t hint_ns) {
+  uint32_t done;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(done)
+      : "r"(bar), "r"(parity), "r"(hint_ns)
+      : "memory");
+  return done != 0;
+}
+
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   uint32_t done;
   asm volatile(
@@ -67,13 +81,15 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 // when another role of the CTA has already aborted.  Never traps.
 __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
                                                   volatile int* abort_flag, unsigned int* status,
-                                                  unsigned int code, long long limit_cycles) {
+                                                  unsigned int code, long long limit_cycles,
+                                                  uint32_t hint_ns = 0) {
   if (mbar_try_wait(bar, parity)) return true;
   const long long t0 = cycle_count();
   for (;;) {
 #pragma unroll 1
     for (int i = 0; i < 8; ++i)
-      if (mbar_try_wait(bar, parity)) return true;
+      if (hint_ns ? mbar_try_wait_hint(bar, parity, hint_ns) : mbar_try_wait(bar, parity))
+        return true;
     if (*abort_flag) return false;
     if (cycle_count() - t0 > limit_cycles) {
       *abort_flag = 1;
