@@ -44,7 +44,9 @@ KERNEL_SOURCES = ["transposed_conv_implicit_gb300/csrc/conv_kernel.cuh",
                   "transposed_conv_implicit_gb300/csrc/ptx.cuh",
                   "transposed_conv_implicit_gb300/csrc/conv_params.h",
                   "transposed_conv_implicit_gb300/csrc/conv_api.cu",
-                  "transposed_conv_implicit_gb300/csrc/conv_kernels.cu"]
+                  "transposed_conv_implicit_gb300/csrc/conv_kernels.cu",
+                  "transposed_conv_implicit_gb300/csrc/conv_kernels_gather.cu",
+                  "transposed_conv_implicit_gb300/csrc/conv_launch.cuh"]
 
 
 def kernel_source_hash() -> str:
@@ -209,24 +211,25 @@ def _bits(t):
 
 def _oracle_one(case, x, w, src):
     import oracle
-    st, pd = (case.stride,) * 2, (case.pad,) * 2
+    st, pd = (case.stride,) * 2, case.pads
     if case.kind == "transposed":
         return oracle.conv_transposed(x, w, out_hw=(case.Ho, case.Wo), stride=st, padding=pd,
                                       source=src, beta=case.beta, act=case.epilogue)
     return oracle.conv2d_fwd(x, w, filter_is_fcrs=case.filter_layout == "FCRS", stride=st,
-                             padding=pd, source=src, beta=case.beta, act=case.epilogue)
+                             padding=pd, dilation=case.dilations, source=src, beta=case.beta,
+                             act=case.epilogue)
 
 
 def _oracle_points(case, x, w, src, pts):
     import oracle
-    st, pd = (case.stride,) * 2, (case.pad,) * 2
+    st, pd = (case.stride,) * 2, case.pads
     if case.kind == "transposed":
         return oracle.conv_transposed_points(x, w, pts, out_hw=(case.Ho, case.Wo), stride=st,
                                              padding=pd, source=src, beta=case.beta,
                                              act=case.epilogue)
     return oracle.conv2d_fwd_points(x, w, pts, filter_is_fcrs=case.filter_layout == "FCRS",
-                                    stride=st, padding=pd, source=src, beta=case.beta,
-                                    act=case.epilogue)
+                                    stride=st, padding=pd, dilation=case.dilations, source=src,
+                                    beta=case.beta, act=case.epilogue)
 
 
 # ----------------------------------------------------------------------------- distributed
@@ -252,6 +255,16 @@ def dist_max(value: float, world: int, device) -> float:
     t = torch.tensor([value], dtype=torch.float64, device=dev)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def whole_job_value(step_ms, flops_per_step: float, world: int, device):
+    """(ms per step, whole-job TFLOP/s) from this rank's timed steps.
+
+    Every rank runs the same steps on its own replica, so the job processed
+    world x steps x flops_per_step; the time is the slowest rank's."""
+    total_ms = dist_max(float(sum(step_ms)), world, device)
+    steps = len(step_ms)
+    return total_ms / steps, flops_per_step * world * steps / (total_ms * 1e-3) / 1e12
 
 
 def dist_barrier(world):
@@ -327,7 +340,7 @@ def run_ours(args, world, rank, local):
         dev_inputs.append((x, w, src))
     pack_ev[0].record(stream)
     for case, (x, w, src) in zip(cases, dev_inputs):
-        st, pd = (case.stride,) * 2, (case.pad,) * 2
+        st, pd = (case.stride,) * 2, case.pads
         if case.kind == "transposed":
             packed.append(cg.conv_transposed_pack_filter(w, stride=st, padding=pd))
         else:
@@ -337,9 +350,11 @@ def run_ours(args, world, rank, local):
     for case, (x, w, src), pk in zip(cases, dev_inputs, packed):
         out = torch.empty(case.out_shape, dtype=synthetic.TORCH_DTYPES[case.out_dtype], device=dev)
         outs.append(out)
-        st, pd = (case.stride,) * 2, (case.pad,) * 2
+        st, pd = (case.stride,) * 2, case.pads
         kw = dict(r=case.R, s=case.S, stride=st, has_residual=case.has_residual, source=src,
                   beta=case.beta, epilogue=case.epilogue, workspace=workspace, stream=stream)
+        if case.kind != "transposed":
+            kw["dilation"] = case.dilations
         if case.kind == "transposed":
             calls.append(cg.bind_conv_transposed_packed(x, pk, out, padding=pd, **kw))
         else:
@@ -402,10 +417,7 @@ def run_ours(args, world, rank, local):
     torch.cuda.synchronize(dev)
     per_kernel_ms = [[kev[k][i].elapsed_time(kev[k][i + 1]) for k in range(kreps)]
                      for i in range(len(calls))]
-    total_ms = dist_max(sum(step_ms), world, dev)
-    ms_per_step = total_ms / args.steps
-    flops_step = sum(c.flops for c in cases)
-    value = flops_step * world * args.steps / (total_ms * 1e-3) / 1e12
+    ms_per_step, value = whole_job_value(step_ms, sum(c.flops for c in cases), world, dev)
 
     # Roofline of the dominant kernel (largest share of the step).
     mean_k = [statistics.fmean(v) for v in per_kernel_ms]
@@ -513,7 +525,7 @@ def run_e2e(args, cases, inputs, dev, stream):
         host_out.append(torch.empty(o.shape, dtype=o.dtype, pin_memory=True))
         d2h += o.numel() * o.element_size()
         w = inp["w"].to(dev)
-        st, pd = (case.stride,) * 2, (case.pad,) * 2
+        st, pd = (case.stride,) * 2, case.pads
         if case.kind == "transposed":
             packed.append(cg.conv_transposed_pack_filter(w, stride=st, padding=pd))
         else:
@@ -525,9 +537,11 @@ def run_e2e(args, cases, inputs, dev, stream):
             dx.copy_(hx, non_blocking=True)
             if hs is not None:
                 ds.copy_(hs, non_blocking=True)
-            st, pd = (case.stride,) * 2, (case.pad,) * 2
+            st, pd = (case.stride,) * 2, case.pads
             kw = dict(r=case.R, s=case.S, stride=st, has_residual=case.has_residual, source=ds,
                       beta=case.beta, epilogue=case.epilogue, workspace=ws)
+            if case.kind != "transposed":
+                kw["dilation"] = case.dilations
             if case.kind == "transposed":
                 cg.conv_transposed_packed(dx, pk, o, padding=pd, **kw)
             else:

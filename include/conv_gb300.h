@@ -74,7 +74,11 @@ const char* conv_status_string(conv_status_t status);
  * filter is transposed once to the (C_out, K = R*S*C_in) NK matrix).
  *
  * Packed layout: packed[f][k], k = (r*S + s)*C_in + c, K-major, element type
- * = dtype.  `filter` is FCRS [C_out][C_in][R][S] when filter_is_fcrs is
+ * = dtype.  For channel counts the gather loader serves (c_in * elt not a
+ * multiple of 16 bytes, or under 32) each filter row r is one run of
+ * S*C_in elements zero-padded to a multiple of 16 bytes:
+ * packed[f][r*RP + s*C_in + c], RP = ceil(S*C_in*elt / 16) * 16 / elt.
+ * `filter` is FCRS [C_out][C_in][R][S] when filter_is_fcrs is
  * nonzero, else RSCF [R][S][C_in][C_out] ("dispatch_amd_4wave_conv2d",
  * Parameters: filter_is_fcrs).  Returns CONV_ERR_WORKSPACE_TOO_SMALL when
  * packed_bytes < conv2d_packed_filter_bytes(...).
@@ -104,9 +108,12 @@ size_t conv2d_workspace_size(int r, int s, int c_in, int c_out, conv_dtype_t dty
  *          (then it must be non-NULL); beta is ignored otherwise
  *
  * Gates (CONV_ERR_NOT_SUPPORTED otherwise): in_dtype in {BF16, F16, F8E4M3};
- * out_dtype as above; stride (1,1) or (2,2); dilation (1,1); padding (0,0),
- * (1,1) or (2,2); num_groups == 1; c_in * sizeof(in_dtype) a multiple of 16
- * bytes and at least 32 bytes (the TMA im2col loader's channel rows); r, s <= 32.
+ * out_dtype as above; stride (1,1) or (2,2); dilation d_h, d_w in [1, 32];
+ * padding per axis 0 <= p_h <= d_h*(r-1), 0 <= p_w <= d_w*(s-1) (a TMA map
+ * also needs the padded corners within [-128, 127]); num_groups == 1;
+ * r, s <= 32.  Any c_in: channel rows of c_in * sizeof(in_dtype) bytes that
+ * are a multiple of 16 and at least 32 are loaded by TMA; other channel
+ * counts (e.g. c_in = 3) by the gather loader, which needs d_w == 1.
  * CONV_ERR_INVALID_VALUE: null pointers, non-positive sizes, ho/wo not equal
  * to floor((h + 2p - (r-1) - 1)/stride) + 1, has_residual with NULL source,
  * unknown epilogue.

@@ -34,7 +34,8 @@ void conv_testing_set_wait_fault(int mode, unsigned long long timeout_ns);
  * 128 x bk tile (un-swizzled, row = pixel, bk channels per row) to
  * out_tile (device, 128 * bk * sizeof(dtype) bytes).  bk is what the
  * convolution would use for this c_in and dtype; it is returned in *bk_out.
- * Shapes and gates as conv2d_fwd.  Synchronous. */
+ * Shapes and gates as conv2d_fwd; channel counts served by the gather loader
+ * (no im2col map) return CONV_ERR_NOT_SUPPORTED.  Synchronous. */
 conv_status_t conv_testing_im2col_tile(const void* input, int n, int h, int w, int c_in,
                                        conv_dtype_t dtype, int r, int s, const int stride[2],
                                        const int symmetric_padding[2], int m0, int tap_r,
@@ -46,12 +47,13 @@ conv_status_t conv_testing_im2col_tile(const void* input, int n, int h, int w, i
  * (channels per k-block), out[2] = pipeline stages, out[3] = dynamic shared
  * memory bytes, out[4] = total tiles, out[5] = grid size (CTAs), out[6] =
  * TMEM columns, out[7] = epilogue mode (0 direct stores, 1 TMA 2-D, 2 TMA
- * phase grid), out[8] = filter resident in shared memory, out[9] = residual
- * source buffers, out[10] = output staging buffers.  Host-only. */
+ * phase grid, 3 TMA row window), out[8] = filter resident in shared memory,
+ * out[9] = residual source buffers, out[10] = output staging buffers,
+ * out[11] = A loader (0 TMA im2col, 1 row window, 2 gather).  Host-only. */
 conv_status_t conv_testing_fwd_plan(int n, int h, int w, int c_in, conv_dtype_t dtype, int r,
                                     int s, int c_out, const int stride[2],
                                     const int symmetric_padding[2], int has_residual, int num_sms,
-                                    int out[11]);
+                                    int out[12]);
 
 #ifdef __cplusplus
 }

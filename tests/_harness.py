@@ -33,7 +33,7 @@ def oracle_full(case, inp):
     x = decode(inp["x"], case.dtype)
     w = decode(inp["w"], case.dtype)
     src = decode(inp["src"], case.out_dtype) if inp["src"] is not None else None
-    st, pd, dl = (case.stride,) * 2, (case.pad,) * 2, (case.dilation,) * 2
+    st, pd, dl = (case.stride,) * 2, case.pads, case.dilations
     if case.kind == "transposed":
         return oracle.conv_transposed(x, w, out_hw=(case.Ho, case.Wo), stride=st, padding=pd,
                                       dilation=dl, source=src, beta=case.beta, act=case.epilogue)
@@ -46,7 +46,7 @@ def oracle_points(case, inp, pts):
     x = decode(inp["x"], case.dtype)
     w = decode(inp["w"], case.dtype)
     src = decode(inp["src"], case.out_dtype) if inp["src"] is not None else None
-    st, pd, dl = (case.stride,) * 2, (case.pad,) * 2, (case.dilation,) * 2
+    st, pd, dl = (case.stride,) * 2, case.pads, case.dilations
     if case.kind == "transposed":
         return oracle.conv_transposed_points(x, w, pts, out_hw=(case.Ho, case.Wo), stride=st,
                                              padding=pd, dilation=dl, source=src, beta=case.beta,
@@ -81,7 +81,7 @@ def run_gpu(case, inp, *, packed=True, device="cuda:0", out=None, workspace=None
     src = inp["src"].to(device) if inp["src"] is not None else None
     if out is None:
         out = torch.empty(case.out_shape, dtype=synthetic.TORCH_DTYPES[case.out_dtype], device=device)
-    st, pd, dl = (case.stride,) * 2, (case.pad,) * 2, (case.dilation,) * 2
+    st, pd, dl = (case.stride,) * 2, case.pads, case.dilations
     kw = dict(has_residual=case.has_residual, source=src, beta=case.beta, epilogue=case.epilogue,
               workspace=workspace)
     if case.kind == "transposed":

@@ -96,16 +96,15 @@ def fwd(lib, *, inp=A, n=2, h=8, w=8, c=64, dt=BF16, flt=B, r=3, s=3, f=64, fcrs
     (dict(epi=3), INVALID),
     (dict(stride=(3, 3)), NOTSUP),
     (dict(stride=(1, 2)), NOTSUP),
-    (dict(dil=(2, 2)), NOTSUP),
-    (dict(pad=(1, 2)), NOTSUP),
+    (dict(dil=(33, 33)), NOTSUP),
+    (dict(c=20, dil=(1, 2)), NOTSUP),                          # gather loader needs dil_w = 1
+    (dict(pad=(1, 3)), NOTSUP),                               # pad beyond the filter extent - 1
     (dict(pad=(3, 3)), NOTSUP),
+    (dict(r=1, s=1, pad=(1, 1)), NOTSUP),
     (dict(groups=2), NOTSUP),
     (dict(dt=F8, odt=F8), NOTSUP),                            # fp8 must write bf16
     (dict(dt=BF16, odt=F16), NOTSUP),
     (dict(dt=7), NOTSUP),
-    (dict(c=8), NOTSUP),                                      # 16 B channel rows: below one MMA K-step
-    (dict(c=20), NOTSUP),                                     # 40 B rows: not a multiple of 16 B
-    (dict(dt=F8, c=16), NOTSUP),                              # 16 B of fp8
     (dict(r=33, s=33, h=40, w=40), NOTSUP),
     (dict(ws_bytes=1000), WS_SMALL),                          # cannot hold the packed filter
     (dict(ws_bytes=100, packed=True), WS_SMALL),
@@ -155,10 +154,11 @@ def test_pack_validation(lib):
 
 
 def _plan(lib, n, h, w, c, dt, r, f, st, pd, res=0, sms=148):
-    out = (ctypes.c_int * 11)()
+    out = (ctypes.c_int * 12)()
     assert lib.conv_testing_fwd_plan(n, h, w, c, dt, r, r, f, _lib.pair((st, st)), _lib.pair((pd, pd)),
                                      res, sms, out) == OK
-    keys = ("bn", "bk", "stages", "smem", "tiles", "grid", "tmem", "epi", "bres", "srcb", "stgb")
+    keys = ("bn", "bk", "stages", "smem", "tiles", "grid", "tmem", "epi", "bres", "srcb", "stgb",
+            "loader")
     return dict(zip(keys, list(out)))
 
 
@@ -195,3 +195,28 @@ def test_noalloc_rejects_filters_beyond_its_scratch(lib):
                                     None, 0.0, 0, None)
     assert status == WS_SMALL
     assert _lib.CONV_NOALLOC_SCRATCH_BYTES == 8 << 20
+
+
+def test_gather_loader_plans(lib):
+    """Channel rows TMA cannot address (C_in * elt not a multiple of 16 bytes,
+    or under 32) go to the gather loader: 128-byte k-blocks over runs of
+    S taps x C_in channels padded to 16 bytes."""
+    # RGB stem, 7x7 stride 2: runs of 7*3*2 = 42 -> 48 bytes, K = 7*48 = 336 B = 3 k-blocks
+    p = _plan(lib, 32, 224, 224, 3, BF16, 7, 64, 2, 2, sms=152)
+    assert (p["loader"], p["bk"], p["bn"], p["bres"]) == (2, 64, 64, 1)
+    assert p["smem"] <= 227 * 1024 and p["stages"] >= 2
+    for c, dt in [(8, BF16), (20, BF16), (1, F16), (16, F8), (5, F8), (3, F16)]:
+        q = _plan(lib, 2, 9, 9, c, dt, 3, 24, 1, 1)
+        assert q["loader"] == 2 and q["bk"] == 128 // (1 if dt == F8 else 2)
+    # TMA-addressable channel rows keep the TMA loaders.
+    assert _plan(lib, 2, 9, 9, 24, BF16, 3, 24, 2, 1)["loader"] == 0
+    assert _plan(lib, 2, 9, 9, 64, BF16, 3, 64, 1, 1)["loader"] == 1
+
+
+def test_gather_packed_filter_bytes(lib):
+    # per output channel: R runs of ceil16(S * C_in * elt) bytes
+    assert lib.conv2d_packed_filter_bytes(7, 7, 3, 64, BF16) == 64 * 7 * 48
+    assert lib.conv2d_packed_filter_bytes(3, 3, 20, 8, BF16) == 8 * 3 * 128
+    assert lib.conv2d_packed_filter_bytes(3, 3, 5, 4, F8) == 4 * 3 * 16
+    assert lib.conv2d_packed_filter_bytes(1, 1, 8, 16, BF16) == 16 * 16
+    assert lib.conv2d_workspace_size(7, 7, 3, 64, BF16) == 256 + 64 * 7 * 48

@@ -21,12 +21,13 @@ pytestmark = pytest.mark.gpu
 
 
 def _fwd(name, dt, N, Hh, W, C, F, R, st, pd, *, layout="RSCF", res=False, beta=0.0, epi="none",
-         seed=1, xd=None, wd=None, S=None):
+         seed=1, xd=None, wd=None, S=None, dil=1, pad_w=None, dil_w=None):
     S = R if S is None else S
     return ConvCase(name, "fwd", dt, N, Hh, W, C, F, R, S, st, pd, layout,
                     xd or Dist("normal", 1.0), wd or Dist("normal", 1.0 / (R * S * C)), seed=seed,
-                    has_residual=res, beta=beta, src_dist=Dist("normal", 1.0) if res else None,
-                    epilogue=epi)
+                    dilation=dil, has_residual=res, beta=beta,
+                    src_dist=Dist("normal", 1.0) if res else None, epilogue=epi, pad_w=pad_w,
+                    dilation_w=dil_w)
 
 
 def _tr(name, dt, N, Hh, W, C, F, R, st, pd, extra=0, *, res=False, beta=0.0, epi="none", seed=1,
@@ -84,6 +85,34 @@ SMALL_FWD = [
     _fwd("b_single_partial_tile", "bf16", 1, 5, 7, 64, 64, 3, 1, 1),
     _fwd("b_exact_one_tile", "bf16", 2, 8, 8, 64, 64, 3, 1, 1),
     _fwd("b_tiny_image", "bf16", 3, 2, 3, 32, 16, 3, 2, 2),
+    # Gather loader: channel rows TMA cannot address (C_in * elt % 16 != 0 or < 32).
+    _fwd("b_gather_c3_stem3x3_s2", "bf16", 2, 17, 19, 3, 32, 3, 2, 1),
+    _fwd("b_gather_c3_7x7_s2p3", "bf16", 2, 23, 21, 3, 64, 7, 2, 3, layout="FCRS"),
+    _fwd("h_gather_c5_res_silu", "f16", 1, 13, 11, 5, 40, 3, 1, 1, res=True, beta=0.5, epi="silu"),
+    _fwd("b_gather_c8_16B", "bf16", 2, 10, 10, 8, 16, 3, 1, 1),
+    _fwd("b_gather_c20_fcrs", "bf16", 2, 9, 11, 20, 48, 3, 2, 1, layout="FCRS"),
+    _fwd("e_gather_c3_5x5", "f8e4m3", 2, 12, 12, 3, 32, 5, 1, 2),
+    _fwd("e_gather_c16_res", "f8e4m3", 1, 11, 11, 16, 64, 3, 1, 1, res=True, beta=0.5),
+    _fwd("b_gather_c3_dil_h2", "bf16", 1, 15, 15, 3, 16, 3, 1, 2, dil=2, dil_w=1),
+    _fwd("b_gather_c1_1x1", "bf16", 2, 9, 9, 1, 16, 1, 1, 0),
+    _fwd("b_gather_c6_cout300", "bf16", 1, 10, 10, 6, 300, 3, 1, 1, epi="relu"),
+    _fwd("h_gather_c3_tail_rows", "f16", 3, 7, 5, 3, 24, 3, 1, 1),
+    # ... with input rows staged by bulk copies (W * C_in * elt a multiple of 16 bytes),
+    # including tiles that span two or more images.
+    _fwd("b_stage_c3_7x7_s2p3", "bf16", 3, 16, 16, 3, 64, 7, 2, 3),
+    _fwd("h_stage_c5_res", "f16", 2, 12, 8, 5, 24, 3, 1, 1, res=True, beta=0.5),
+    _fwd("e_stage_c3_s2", "f8e4m3", 2, 20, 16, 3, 32, 3, 2, 1),
+    _fwd("b_stage_c3_dil_h3", "bf16", 1, 30, 16, 3, 16, 3, 1, 3, dil=3, dil_w=1, pad_w=1),
+    _fwd("b_stage_c6_tiny_images", "bf16", 6, 4, 8, 6, 32, 3, 1, 1, epi="silu"),
+    _fwd("b_stage_c8_cout200", "bf16", 2, 14, 14, 8, 200, 3, 2, 1),
+    # Dilation (TMA im2col tap offsets) and padding per axis.
+    _fwd("b_dil2_same", "bf16", 2, 15, 14, 64, 64, 3, 1, 2, dil=2),
+    _fwd("h_dil3_s2", "f16", 1, 20, 20, 32, 48, 3, 2, 2, dil=3),
+    _fwd("b_dil_w2_only", "bf16", 1, 12, 13, 32, 32, 3, 1, 1, dil=1, dil_w=2),
+    _fwd("b_pad3_7x7_s2", "bf16", 1, 20, 20, 32, 32, 7, 2, 3),
+    _fwd("b_window_7x7_p3", "bf16", 1, 14, 14, 64, 16, 7, 1, 3, res=True, beta=1.0),
+    _fwd("b_pad_h1_w0", "bf16", 2, 10, 12, 64, 64, 3, 1, 1, pad_w=0),
+    _fwd("e_pad_h0_w2_5x5", "f8e4m3", 1, 12, 12, 64, 32, 5, 2, 0, pad_w=2),
 ]
 
 SMALL_TR = [
@@ -112,7 +141,8 @@ def test_small_case_every_element(case):
 
 
 @pytest.mark.parametrize("case", [c for c in SMALL_FWD + SMALL_TR if c.name in (
-    "b_3x3_s2p1", "b_cout17_res", "e_3x3_s1p1_res", "t_h_4x4_s2p1_relu", "t_b_3x3_s2p1_op1")],
+    "b_3x3_s2p1", "b_cout17_res", "e_3x3_s1p1_res", "t_h_4x4_s2p1_relu", "t_b_3x3_s2p1_op1",
+    "b_gather_c3_7x7_s2p3", "e_gather_c3_5x5")],
     ids=lambda c: c.name)
 def test_unpacked_entry_point_equals_packed(case):
     """conv2d_fwd / conv_transposed pack in the workspace; the result must be
@@ -138,6 +168,10 @@ INT_CASES = [
     _int_case("int_e_3x3", "fwd", "f8e4m3", 2, 10, 10, 32, 64, 3, 1, 1),
     _int_case("int_h_tr", "transposed", "f16", 2, 8, 8, 64, 32, 4, 2, 1),
     _int_case("int_e_tr", "transposed", "f8e4m3", 1, 7, 7, 32, 16, 3, 2, 1, extra=1),
+    _int_case("int_b_gather_c3", "fwd", "bf16", 2, 11, 13, 3, 16, 7, 2, 3),
+    _int_case("int_b_stage_c3", "fwd", "bf16", 2, 16, 16, 3, 16, 7, 2, 3),
+    _int_case("int_e_gather_c5", "fwd", "f8e4m3", 1, 9, 9, 5, 32, 3, 1, 1),
+    _int_case("int_h_dil2", "fwd", "f16", 1, 12, 12, 16, 16, 3, 1, 2, dil=2),
 ]
 
 

@@ -92,7 +92,10 @@ def conv2d_workspace_size(r, s, c_in, c_out, dtype: str) -> int:
 
 
 def conv2d_pack_filter(filter, *, filter_is_fcrs: bool, out=None, stream=None):
-    """Pack an FCRS/RSCF filter into the K-major [C_out][R*S*C_in] matrix (returns `out`)."""
+    """Pack an FCRS/RSCF filter into the K-major [C_out][K] matrix (returns `out`).
+
+    K = R*S*C_in, or, for channel counts the gather loader serves, R runs of
+    S*C_in padded to 16 bytes; conv2d_packed_filter_bytes gives the size."""
     import torch
     _need_dense(filter)
     if filter_is_fcrs:
@@ -100,7 +103,9 @@ def conv2d_pack_filter(filter, *, filter_is_fcrs: bool, out=None, stream=None):
     else:
         r, s, c_in, c_out = filter.shape
     if out is None:
-        out = torch.empty((c_out, r * s * c_in), dtype=filter.dtype, device=filter.device)
+        nbytes = conv2d_packed_filter_bytes(r, s, c_in, c_out, dtype_name(filter))
+        out = torch.empty((c_out, nbytes // (c_out * filter.element_size())), dtype=filter.dtype,
+                          device=filter.device)
     _check(_lib.lib().conv2d_pack_filter(_ptr(filter), r, s, c_in, c_out, int(bool(filter_is_fcrs)),
                                          _code(filter), _ptr(out), out.numel() * out.element_size(),
                                          _stream(stream, filter.device)), "conv2d_pack_filter")
@@ -145,7 +150,8 @@ def conv2d_fwd_packed(input, packed_filter, output, *, r, s, stride=(1, 1), dila
     n, h, w, c_in, ho, wo, c_out, st, dl, pd = _fwd_common(input, output, stride, dilation,
                                                              symmetric_padding, source)
     _need_dense(packed_filter)
-    if packed_filter.numel() != c_out * r * s * c_in:
+    if (packed_filter.numel() * packed_filter.element_size()
+            != conv2d_packed_filter_bytes(r, s, c_in, c_out, dtype_name(input))):
         raise ConvError(CONV_ERR_INVALID_VALUE, "packed filter size does not match")
     if workspace is None:
         workspace = new_workspace(CONV_STATUS_BYTES, input.device)

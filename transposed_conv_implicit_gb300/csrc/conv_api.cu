@@ -152,6 +152,79 @@ conv_status_t channel_block(int c_in, int elt, int* bk, uint32_t* row_bytes) {
   return CONV_OK;
 }
 
+FastDiv make_fast_div(uint32_t d) {
+  FastDiv f{};
+  f.d = d;
+  uint32_t s = 0;
+  while ((1ull << s) < d) ++s;
+  f.shift = s;
+  f.mul = static_cast<uint32_t>((((1ull << 32) * ((1ull << s) - d)) / d + 1) & 0xFFFFFFFFull);
+  return f;
+}
+
+// Forward convs whose channel rows a TMA box cannot address (C_in * elt not
+// a multiple of 16 bytes, or under 32) use the gather A loader.  Its
+// contraction layout: per filter row r one run of S taps x C_in channels
+// (S * C_in * elt bytes, contiguous in the NHWC input when dil_w = 1),
+// zero-padded to a multiple of 16 bytes; the packed filter follows it.
+bool gather_mode(int c_in, int elt) {
+  const long long cb = static_cast<long long>(c_in) * elt;
+  return cb % 16 != 0 || cb < 32;
+}
+
+uint32_t align1k(size_t v) { return static_cast<uint32_t>((v + 1023) & ~static_cast<size_t>(1023)); }
+
+// Shared memory of the gather loader beyond the barriers: one row table per
+// producer warp (16 bytes per tile row) and, when input rows are staged, two
+// staging buffers.  Decides whether rows are staged (sets g_stage, g_slots,
+// g_stage_bytes); needs m_halves.
+size_t gather_smem_bytes(ConvKernelParams& kp) {
+  if (!kp.gather) return 0;
+  const size_t tables = static_cast<size_t>(2) * kBM * kp.m_halves * 16;
+  kp.g_stage = 0;
+  kp.g_slots = 0;
+  kp.g_stage_bytes = 0;
+  if (kp.g_row_bytes % 16 == 0 && env_int("CONV_GATHER_STAGE") != -1) {
+    // Padded rows a tile of `rows` consecutive output pixels can touch: its
+    // output rows (at most (rows-1)/Wo + 2 of them) step stride_h apart, plus
+    // the filter extent, plus, at each image boundary crossed, the rest of
+    // the filter extent of the image it leaves.
+    const long long rows = static_cast<long long>(kBM) * kp.m_halves;
+    const long long out_rows = (rows - 1) / kp.Wo + 2;
+    const long long ext = static_cast<long long>(kp.g_runs - 1) * kp.dil_h + 1;
+    const long long crossings =
+        std::min(out_rows - 1, (rows - 1) / (static_cast<long long>(kp.Ho) * kp.Wo) + 1);
+    const long long slots = (out_rows - 1) * kp.step_h + ext +
+                            crossings * std::max<long long>(0, ext - kp.step_h);
+    // Zero margins: a piece may start pad_w pixels left of the row (minus the
+    // 3 bytes of 4-byte rounding) and end pad_w pixels plus a run's padding
+    // and the 20-byte read window right of it.
+    const long long pix = kp.g_row_bytes / kp.g_w;
+    const long long pad_l = ((-kp.base_w[0]) * pix + 4 + 15) / 16 * 16;
+    const long long pad_r = ((-kp.base_w[0]) * pix + 32 + 15) / 16 * 16;
+    const long long slot = pad_l + kp.g_row_bytes + pad_r;
+    const size_t buf = align1k(static_cast<size_t>(slots * slot));
+    if (2 * buf <= 96 * 1024) {
+      kp.g_stage = 1;
+      kp.g_slots = static_cast<int>(slots);
+      kp.g_slot_bytes = static_cast<int>(slot);
+      kp.g_slot_pad = static_cast<int>(pad_l);
+      kp.g_stage_bytes = static_cast<uint32_t>(buf);
+    }
+  }
+  return align1k(tables) + 2 * static_cast<size_t>(kp.g_stage_bytes);
+}
+
+long long gather_run_bytes(int s, int c_in, int elt) {
+  return ((static_cast<long long>(s) * c_in * elt + 15) / 16) * 16;
+}
+
+// Packed K (elements per output channel) of the forward filter.
+long long fwd_packed_k(int r, int s, int c_in, int elt) {
+  if (gather_mode(c_in, elt)) return r * gather_run_bytes(s, c_in, elt) / elt;
+  return static_cast<long long>(r) * s * c_in;
+}
+
 uint32_t make_idesc(conv_dtype_t in, int bn) {
   // kind::f16: A/B format 0 = fp16, 1 = bf16; kind::f8f6f4: 0 = e4m3.
   // D format (bits 4-5) 1 = fp32; both operands K-major (bits 15, 16 = 0);
@@ -262,7 +335,9 @@ void choose_tiling(Plan* pl, const long long rows[], int num_phases, int max_kbl
       const double a = static_cast<double>(kBM) * mh * kp.sw_bytes;
       const double b = static_cast<double>(bn) * kp.sw_bytes;
       const bool res = num_phases == 1 && nte == 1 && max_kblocks * b <= 96.0 * 1024;
-      const double load = (a + (res ? 0.0 : b)) / 70.0 + 40.0 * (res ? 1 : 2);
+      // The gather loader builds A with two producer warps at ~5.6 cycles per row.
+      const double load = kp.gather ? std::max(kBM * mh * 5.6, (res ? 0.0 : b) / 70.0 + 40.0)
+                                    : (a + (res ? 0.0 : b)) / 70.0 + 40.0 * (res ? 1 : 2);
       const double mma = static_cast<double>(mh) * ksteps * (63.0 * std::max(1.0, bn / 128.0) + 8.0);
       const double epi = static_cast<double>(kBM) * mh * bn * 2 / 64.0;
       // The smaller term still costs a little (issue slots, barriers): it breaks
@@ -307,9 +382,18 @@ conv_status_t check_fwd_shape(const FwdShape& f, int num_groups) {
   if (!dtype_pair_ok(f.in_dtype, f.out_dtype)) return CONV_ERR_NOT_SUPPORTED;
   if (!((f.stride_h == 1 && f.stride_w == 1) || (f.stride_h == 2 && f.stride_w == 2)))
     return CONV_ERR_NOT_SUPPORTED;
-  if (f.dil_h != 1 || f.dil_w != 1) return CONV_ERR_NOT_SUPPORTED;
-  if (f.pad_h != f.pad_w || f.pad_h < 0 || f.pad_h > 2) return CONV_ERR_NOT_SUPPORTED;
+  if (f.dil_h < 1 || f.dil_w < 1 || f.dil_h > kMaxFilterExtent || f.dil_w > kMaxFilterExtent)
+    return CONV_ERR_NOT_SUPPORTED;
+  // Padding per axis, up to the dilated filter extent minus one (beyond it
+  // whole output rows would see only padding).
+  if (f.pad_h < 0 || f.pad_w < 0 || f.pad_h > f.dil_h * (f.r - 1) || f.pad_w > f.dil_w * (f.s - 1))
+    return CONV_ERR_NOT_SUPPORTED;
   if (num_groups != 1) return CONV_ERR_NOT_SUPPORTED;
+  // The gather loader reads S adjacent pixels per filter row and indexes
+  // input pixels with 32-bit integers.
+  if (gather_mode(f.c_in, elt_bytes(f.in_dtype)) &&
+      (f.dil_w != 1 || static_cast<long long>(f.n) * f.h * f.w >= (1ll << 30)))
+    return CONV_ERR_NOT_SUPPORTED;
   if (f.r > kMaxFilterExtent || f.s > kMaxFilterExtent) return CONV_ERR_NOT_SUPPORTED;
   const long long ho = (static_cast<long long>(f.h) + 2 * f.pad_h - f.dil_h * (f.r - 1) - 1) /
                            f.stride_h + 1;
@@ -323,7 +407,6 @@ conv_status_t check_fwd_shape(const FwdShape& f, int num_groups) {
   return CONV_OK;
 }
 
-uint32_t align1k(size_t v) { return static_cast<uint32_t>((v + 1023) & ~static_cast<size_t>(1023)); }
 
 // Row-window A loader for stride-1 forward convs: when a padded output row
 // (Wo + S - 1 pixels) fits in one 128-row MMA half, the tile's input rows are
@@ -380,17 +463,53 @@ void plan_window_or_keep(const FwdShape& f, Plan* pl, int num_sms, int has_resid
   if (pl->kp.window && layout_memory_window(pl, has_residual) != CONV_OK) *pl = saved;
 }
 
+// The gather loader's k-blocks: 128-byte rows (64 bf16/f16 or 128 fp8
+// elements) over the run layout; the last block reaches past K, where the
+// builder writes zeros and the filter map zero-fills.
+conv_status_t plan_gather(const FwdShape& f, Plan* pl) {
+  ConvKernelParams& kp = pl->kp;
+  const int elt = elt_bytes(f.in_dtype);
+  const long long run_bytes = gather_run_bytes(f.s, f.c_in, elt);
+  const long long kbytes = f.r * run_bytes;
+  if (kbytes > (1ll << 24)) return CONV_ERR_NOT_SUPPORTED;
+  kp.bk = 128 / elt;
+  kp.sw_bytes = 128;
+  kp.c_blocks = static_cast<int>((kbytes + 127) / 128);
+  kp.c_tail = 0;
+  kp.c_in = f.c_in;
+  kp.gather = 1;
+  kp.g_n = f.n;
+  kp.g_h = f.h;
+  kp.g_w = f.w;
+  kp.g_c = f.c_in;
+  kp.g_elt = elt;
+  kp.g_runs = f.r;
+  kp.g_s = f.s;
+  kp.g_run_len_bytes = f.s * f.c_in * elt;
+  kp.g_run_bytes = static_cast<int>(run_bytes);
+  const long long row_bytes = static_cast<long long>(f.w) * f.c_in * elt;
+  kp.g_row_bytes = row_bytes < (1ll << 30) ? static_cast<int>(row_bytes) : 1;  // 1: never staged
+  kp.g_pr = (f.ho - 1) * f.stride_h + (f.r - 1) * f.dil_h + 1;
+  kp.g_div_run = make_fast_div(static_cast<uint32_t>(run_bytes));
+  kp.g_div_pr = make_fast_div(static_cast<uint32_t>(kp.g_pr));
+  pl->in_dtype = f.in_dtype;
+  pl->out_bf16 = (f.in_dtype != CONV_DTYPE_F16);
+  pl->kind = f.in_dtype == CONV_DTYPE_F8E4M3 ? kKindF8 : kKindF16;
+  return CONV_OK;
+}
+
 conv_status_t plan_fwd(const FwdShape& f, Plan* pl, int num_sms, int has_residual) {
   std::memset(pl, 0, sizeof(*pl));
-  conv_status_t st = plan_channels(pl, f.in_dtype, f.c_in);
+  const bool gather = gather_mode(f.c_in, elt_bytes(f.in_dtype));
+  conv_status_t st = gather ? plan_gather(f, pl) : plan_channels(pl, f.in_dtype, f.c_in);
   if (st != CONV_OK) return st;
   ConvKernelParams& kp = pl->kp;
   kp.num_phases = 1;
   kp.grid_h[0] = f.ho;
   kp.grid_w[0] = f.wo;
   kp.rows[0] = f.n * f.ho * f.wo;
-  kp.taps_h[0] = f.r;
-  kp.taps_w[0] = f.s;
+  kp.taps_h[0] = gather ? 1 : f.r;  // gather k-blocks span the whole contraction
+  kp.taps_w[0] = gather ? 1 : f.s;
   kp.base_h[0] = -f.pad_h;
   kp.base_w[0] = -f.pad_w;
   kp.out_off_h[0] = 0;
@@ -403,7 +522,7 @@ conv_status_t plan_fwd(const FwdShape& f, Plan* pl, int num_sms, int has_residua
   kp.dil_h = f.dil_h;
   kp.dil_w = f.dil_w;
   const long long rows[1] = {kp.rows[0]};
-  choose_tiling(pl, rows, 1, f.r * f.s * kp.c_blocks, f.c_out, num_sms);
+  choose_tiling(pl, rows, 1, kp.taps_h[0] * kp.taps_w[0] * kp.c_blocks, f.c_out, num_sms);
   const int tile_m = kBM * kp.m_halves;
   const int m_tiles = (kp.rows[0] + tile_m - 1) / tile_m;
   kp.tile_start[0] = 0;
@@ -414,9 +533,9 @@ conv_status_t plan_fwd(const FwdShape& f, Plan* pl, int num_sms, int has_residua
   kp.Cout = f.c_out;
   kp.vec_ok = (f.c_out * 2) % 16 == 0;
   pl->phases_packed = 1;
-  pl->kmax = f.r * f.s * f.c_in;
+  pl->kmax = static_cast<int>(fwd_packed_k(f.r, f.s, f.c_in, elt_bytes(f.in_dtype)));
   pl->packed_bytes = static_cast<size_t>(f.c_out) * pl->kmax * elt_bytes(f.in_dtype);
-  plan_window_or_keep(f, pl, num_sms, has_residual);
+  if (!gather) plan_window_or_keep(f, pl, num_sms, has_residual);
   return CONV_OK;
 }
 
@@ -441,6 +560,11 @@ conv_status_t encode_window_input(const FwdShape& f, const void* input, Plan* pl
 }
 
 conv_status_t encode_fwd_input(const FwdShape& f, const void* input, Plan* pl) {
+  if (pl->kp.gather) {  // plain loads: the kernel needs only the base and the extent
+    pl->kp.g_input = static_cast<const uint8_t*>(input);
+    pl->kp.g_input_bytes = static_cast<long long>(f.n) * f.h * f.w * f.c_in * elt_bytes(f.in_dtype);
+    return CONV_OK;
+  }
   if (pl->kp.window) return encode_window_input(f, input, pl);
   return encode_input_map(&pl->kp.map_a[0], input, f.n, f.h, f.w, f.c_in, f.in_dtype, pl->kp.bk,
                           pl->kp.sw_bytes, kBM * pl->kp.m_halves, -f.pad_w, -f.pad_h, f.pad_w - (f.s - 1) * f.dil_w,
@@ -592,6 +716,29 @@ __global__ void pack_fwd_kernel(const T* __restrict__ w, T* __restrict__ out, in
   }
 }
 
+// Gather layout: out[f][r][j], j < run_elems, holds W(r, s, c, f) for
+// j = s*C + c < S*C and zero in the run's padding.
+template <typename T>
+__global__ void pack_fwd_gather_kernel(const T* __restrict__ w, T* __restrict__ out, int R, int S,
+                                       int C, int F, int fcrs, int run_elems) {
+  const long long per_f = static_cast<long long>(R) * run_elems;
+  const long long total = per_f * F;
+  for (long long idx = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; idx < total;
+       idx += static_cast<long long>(gridDim.x) * blockDim.x) {
+    const long long f = idx / per_f;
+    const long long k = idx - f * per_f;
+    const long long r = k / run_elems;
+    const long long j = k - r * run_elems;
+    T v = T(0);
+    if (j < static_cast<long long>(S) * C) {
+      const long long s = j / C;
+      const long long c = j - s * C;
+      v = fcrs ? w[((f * C + c) * R + r) * S + s] : w[((r * S + s) * C + c) * F + f];
+    }
+    out[idx] = v;
+  }
+}
+
 struct TrPackDesc {
   int slots, kmax, sh, sw;
   int r0h[kMaxPhases], r0w[kMaxPhases], th[kMaxPhases], tw[kMaxPhases];
@@ -630,6 +777,20 @@ int pack_grid(long long total) {
 
 conv_status_t launch_pack_fwd(const void* filter, int r, int s, int c_in, int c_out, int fcrs,
                               conv_dtype_t dt, void* packed, cudaStream_t stream) {
+  const int elt = elt_bytes(dt);
+  if (gather_mode(c_in, elt)) {
+    const int run_elems = static_cast<int>(gather_run_bytes(s, c_in, elt) / elt);
+    const long long total = static_cast<long long>(r) * run_elems * c_out;
+    if (elt == 2)
+      pack_fwd_gather_kernel<uint16_t><<<pack_grid(total), 256, 0, stream>>>(
+          static_cast<const uint16_t*>(filter), static_cast<uint16_t*>(packed), r, s, c_in, c_out,
+          fcrs, run_elems);
+    else
+      pack_fwd_gather_kernel<uint8_t><<<pack_grid(total), 256, 0, stream>>>(
+          static_cast<const uint8_t*>(filter), static_cast<uint8_t*>(packed), r, s, c_in, c_out,
+          fcrs, run_elems);
+    return cudaGetLastError() == cudaSuccess ? CONV_OK : CONV_ERR_CUDA;
+  }
   const long long total = static_cast<long long>(r) * s * c_in * c_out;
   if (elt_bytes(dt) == 2)
     pack_fwd_kernel<uint16_t><<<pack_grid(total), 256, 0, stream>>>(
@@ -745,7 +906,7 @@ conv_status_t layout_memory(Plan* pl, int has_residual) {
   const size_t bres = can_res ? static_cast<size_t>(kp.taps_h[0]) * kp.taps_w[0] * kp.c_blocks * b_bytes : 0;
   const size_t src_tile = static_cast<size_t>(kBM) * kp.m_halves * kp.bn * 2;
   const size_t chunk = static_cast<size_t>(kBM) * cw * 2;
-  const size_t bar_bytes = 1024;
+  const size_t bar_bytes = 1024 + gather_smem_bytes(kp);
   struct Opt { bool res; int srcb, stgb; };
   Opt opts[12];
   int nopt = 0;
@@ -803,6 +964,8 @@ conv_status_t layout_memory(Plan* pl, int has_residual) {
   kp.off_stg = off;
   off += kEpilogueGroups * o.stgb * align1k(chunk);
   kp.off_bar = off;
+  kp.off_gtab = off + 1024;
+  kp.off_gstage = kp.off_gtab + align1k(static_cast<size_t>(2) * kBM * kp.m_halves * 16);
   off += bar_bytes;
   pl->smem_bytes = off + 1024;
   return CONV_OK;
@@ -920,7 +1083,7 @@ conv_status_t plan_memory_direct(Plan* pl) {
   ConvKernelParams& kp = pl->kp;
   const uint32_t a_bytes = kBM * kp.m_halves * kp.sw_bytes;
   const uint32_t b_bytes = static_cast<uint32_t>(kp.bn) * kp.sw_bytes;
-  const size_t bar_bytes = 1024;
+  const size_t bar_bytes = 1024 + gather_smem_bytes(kp);
   kp.epi_mode = 0;
   kp.cw = 16;
   kp.src_bufs = 0;
@@ -955,6 +1118,8 @@ conv_status_t plan_memory_direct(Plan* pl) {
   kp.off_src = off;
   kp.off_stg = off;
   kp.off_bar = off;
+  kp.off_gtab = off + 1024;
+  kp.off_gstage = kp.off_gtab + align1k(static_cast<size_t>(2) * kBM * kp.m_halves * 16);
   off += bar_bytes;
   pl->smem_bytes = off + 1024;
   return CONV_OK;
@@ -983,6 +1148,14 @@ conv_status_t finish_and_launch(Plan* pl, int n_images, const void* packed, void
     kp.wait_hint_ns = h ? static_cast<uint32_t>(std::atoi(h)) : 0u;
   }
   kp.fault_mode = g_fault_mode.load(std::memory_order_relaxed);
+  kp.div_ntiles = make_fast_div(static_cast<uint32_t>(std::max(kp.n_tiles, 1)));
+  for (int ph = 0; ph < kMaxPhases; ++ph) {
+    const uint32_t gh = static_cast<uint32_t>(std::max(kp.grid_h[ph], 1));
+    const uint32_t gw = static_cast<uint32_t>(std::max(kp.grid_w[ph], 1));
+    kp.div_ghw[ph] = make_fast_div(gh * gw);
+    kp.div_gw[ph] = make_fast_div(gw);
+  }
+  kp.div_win_rb = make_fast_div(static_cast<uint32_t>(std::max(kp.win_row_blocks, 1)));
   // Prefetching the next tile's input only pays when CTAs walk several tiles
   // that all start at the first C_out tile (one n-tile).
   kp.l2_prefetch = (kp.n_tiles == 1 && env_int("CONV_L2_PREFETCH") != -1) ? 1 : 0;
@@ -1044,10 +1217,6 @@ conv_status_t fwd_impl(const void* input, const FwdShape& f, const void* filter,
   if (st != CONV_OK) return st;
   if (!epilogue_ok(epilogue)) return CONV_ERR_INVALID_VALUE;
   st = check_fwd_shape(f, num_groups);
-  if (st != CONV_OK) return st;
-  int bk = 0;
-  uint32_t row_bytes = 0;
-  st = channel_block(f.c_in, elt_bytes(f.in_dtype), &bk, &row_bytes);
   if (st != CONV_OK) return st;
   const size_t packed_bytes = conv2d_packed_filter_bytes(f.r, f.s, f.c_in, f.c_out, f.in_dtype);
   const size_t need = CONV_STATUS_BYTES + (prepacked ? 0 : round_up_256(packed_bytes));
@@ -1162,7 +1331,8 @@ const char* conv_status_string(conv_status_t status) {
 
 size_t conv2d_packed_filter_bytes(int r, int s, int c_in, int c_out, conv_dtype_t dtype) {
   if (r <= 0 || s <= 0 || c_in <= 0 || c_out <= 0 || !known_dtype(dtype)) return 0;
-  return static_cast<size_t>(r) * s * c_in * c_out * elt_bytes(dtype);
+  const int elt = elt_bytes(dtype);
+  return static_cast<size_t>(fwd_packed_k(r, s, c_in, elt)) * c_out * elt;
 }
 
 size_t conv2d_workspace_size(int r, int s, int c_in, int c_out, conv_dtype_t dtype) {
@@ -1350,7 +1520,7 @@ void conv_testing_set_wait_fault(int mode, unsigned long long timeout_ns) {
 conv_status_t conv_testing_fwd_plan(int n, int h, int w, int c_in, conv_dtype_t dtype, int r,
                                     int s, int c_out, const int stride[2],
                                     const int symmetric_padding[2], int has_residual, int num_sms,
-                                    int out[11]) {
+                                    int out[12]) {
   if (!stride || !symmetric_padding || !out) return CONV_ERR_INVALID_VALUE;
   const int dil[2] = {1, 1};
   const conv_dtype_t out_dt = dtype == CONV_DTYPE_F8E4M3 ? CONV_DTYPE_BF16 : dtype;
@@ -1377,6 +1547,7 @@ conv_status_t conv_testing_fwd_plan(int n, int h, int w, int c_in, conv_dtype_t 
   out[8] = pl.kp.b_resident;
   out[9] = pl.kp.src_bufs;
   out[10] = pl.kp.stg_bufs;
+  out[11] = pl.kp.gather ? 2 : (pl.kp.window ? 1 : 0);
   return CONV_OK;
 }
 
@@ -1400,6 +1571,7 @@ conv_status_t conv_testing_im2col_tile(const void* input, int n, int h, int w, i
   Plan pl;
   st = plan_fwd(f, &pl, 1, 0);
   if (st != CONV_OK) return st;
+  if (pl.kp.gather) return CONV_ERR_NOT_SUPPORTED;  // no im2col map: plain loads build A
   pl.kp.m_halves = 1;  // the probe copies out one 128-row column of an im2col load
   pl.kp.window = 0;
   if (m0 < 0 || m0 >= pl.kp.rows[0] || tap_r < 0 || tap_r >= r || tap_s < 0 || tap_s >= s ||

@@ -7,9 +7,13 @@
 
 namespace convgb300 {
 
-// Launches the implicit-GEMM kernel instance for (kind, output dtype).
+// Launches the implicit-GEMM kernel instance for (kind, output dtype, loader).
 cudaError_t launch_conv_igemm(int kind, bool out_bf16, const ConvKernelParams& p, int grid,
                               size_t smem_bytes, cudaStream_t stream);
+
+// The gather-loader instances (their own translation unit).
+cudaError_t launch_conv_igemm_gather(int kind, bool out_bf16, const ConvKernelParams& p, int grid,
+                                     size_t smem_bytes, cudaStream_t stream);
 
 // One TMA im2col load into shared memory, copied out un-swizzled (test hook).
 cudaError_t launch_im2col_probe(const CUtensorMap& map, int c, int w, int h, int n, int off_w,

@@ -1,27 +1,38 @@
-// Implicit-GEMM convolution kernel for sm_103a (tcgen05 + TMA im2col).
+// Implicit-GEMM convolution kernel for sm_103a (tcgen05 + TMA).
 //
 // One kernel serves the forward convolution and every stride phase of the
 // transposed convolution.  The GEMM view ("dispatch_fused_im2col_conv2d_apple",
 // description): rows m are output pixels (n, oy, ox), columns are output
 // channels, and the contraction index is k = (r*S + s)*C_in + c.  The A operand
-// (the im2col matrix) is never materialised: each 128-pixel x (one filter tap,
-// bk channels) block is fetched straight from the NHWC input by a TMA im2col
-// load, with the hardware zero-filling pixels that fall in the padding.  The B
-// operand is the filter pre-packed once into a K-major [C_out][K] matrix; when
-// it fits, it is loaded into shared memory once per CTA and kept there.
+// (the im2col matrix) is never materialised; one of three loaders brings each
+// k-block of it into shared memory straight from the NHWC input:
+//   - TMA im2col: one 128-pixel x (one filter tap, bk channels) box per
+//     k-block, the hardware zero-filling pixels that fall in the padding;
+//   - row window (stride-1 forward convs whose padded output row fits in
+//     128 MMA rows): one tiled box of the tile's input rows with halo per
+//     channel block, read by every filter tap at a row offset;
+//   - gather (channel rows TMA cannot address, e.g. C_in = 3): the producer
+//     warps load 16-byte pieces of the input with plain loads and write them
+//     into the swizzled stage.
+// The B operand is the filter pre-packed once into a K-major [C_out][K]
+// matrix; when it fits, it is loaded into shared memory with the first tile
+// and kept there.
 //
-// Warp roles (192 threads, one persistent CTA per SM):
-//   warp 0      TMA producer: one elected lane streams A (and B unless it is
-//               resident) k-blocks into an S-stage shared-memory ring guarded
-//               by full/empty mbarriers;
-//   warp 1      TMEM owner and MMA issuer: one lane issues tcgen05.mma
-//               (M=128, N=bn) into a double-buffered fp32 TMEM accumulator;
-//   warps 2-5   epilogue: tcgen05.ld the accumulator, add beta*source, apply
-//               the activation, round once to the output dtype and store.
-//               With a TMA epilogue the residual source tile is prefetched by
-//               TMA one tile ahead into swizzled shared memory, and results are
-//               staged in swizzled shared memory and written by TMA stores
-//               (which also clip the ragged M tail and the C_out edge tile).
+// Warp roles (352 threads, one persistent CTA per SM):
+//   warps 0, 10  producers: k-block `seq` belongs to warp (seq & 1); one lane
+//                issues its TMA loads (the whole warp builds it in gather
+//                mode) into an S-stage shared-memory ring guarded by
+//                full/empty mbarriers;
+//   warp 1       TMEM owner and MMA issuer: one lane issues tcgen05.mma
+//                (M=128 per half, N=bn) into a double-buffered fp32 TMEM
+//                accumulator;
+//   warps 2-9    epilogue, two warpgroups taking alternate (half, column
+//                chunk) items: tcgen05.ld the accumulator, add beta*source,
+//                apply the activation, round once to the output dtype and
+//                store.  With a TMA epilogue the residual source is loaded by
+//                TMA ahead of use into swizzled shared memory, and results are
+//                staged there and written by TMA stores (which also clip the
+//                ragged M tail and the C_out edge tile).
 // Every wait is bounded in time; on expiry the CTA records a status bit,
 // stops, lets in-flight copies and MMAs land, frees TMEM and returns.
 #pragma once
@@ -41,6 +52,12 @@ struct TileInfo {
   int kblocks;  // k-blocks in this tile's contraction
 };
 
+// x / f.d for 0 <= x < 2^31 (see FastDiv).
+__device__ __forceinline__ int fast_div(int x, const FastDiv& f) {
+  const uint32_t u = static_cast<uint32_t>(x);
+  return static_cast<int>((static_cast<uint64_t>(__umulhi(u, f.mul)) + u) >> f.shift);
+}
+
 __device__ __forceinline__ TileInfo decode_tile(const ConvKernelParams& p, int t) {
   if (p.window) {  // one C_out tile; m0 carries the tile index
     TileInfo ti;
@@ -55,8 +72,9 @@ __device__ __forceinline__ TileInfo decode_tile(const ConvKernelParams& p, int t
   const int local = t - p.tile_start[ph];
   TileInfo ti;
   ti.phase = ph;
-  ti.n0 = (local % p.n_tiles) * p.bn;
-  ti.m0 = (local / p.n_tiles) * (kBM * p.m_halves);
+  const int mt = fast_div(local, p.div_ntiles);
+  ti.n0 = (local - mt * p.n_tiles) * p.bn;
+  ti.m0 = mt * (kBM * p.m_halves);
   ti.kblocks = p.taps_h[ph] * p.taps_w[ph] * p.c_blocks;
   return ti;
 }
@@ -64,17 +82,16 @@ __device__ __forceinline__ TileInfo decode_tile(const ConvKernelParams& p, int t
 // Image and first output row of row-window tile t.
 __device__ __forceinline__ void window_origin(const ConvKernelParams& p, int t, int& n_img,
                                               int& oy0) {
-  n_img = t / p.win_row_blocks;
+  n_img = fast_div(t, p.div_win_rb);
   oy0 = (t - n_img * p.win_row_blocks) * (p.win_rows * p.m_halves);
 }
 
 // (image, grid row, grid column) of GEMM row m in phase ph.
 __device__ __forceinline__ void grid_pos(const ConvKernelParams& p, int ph, int m, int& n_img,
                                          int& j, int& i) {
-  const int hw = p.grid_h[ph] * p.grid_w[ph];
-  n_img = m / hw;
-  const int rem = m - n_img * hw;
-  j = rem / p.grid_w[ph];
+  n_img = fast_div(m, p.div_ghw[ph]);
+  const int rem = m - n_img * static_cast<int>(p.div_ghw[ph].d);
+  j = fast_div(rem, p.div_gw[ph]);
   i = rem - j * p.grid_w[ph];
 }
 
@@ -435,7 +452,370 @@ __device__ __forceinline__ bool mma_role_window(const ConvKernelParams& p, uint3
   return ok;
 }
 
-template <int kKind, typename OutT>
+// ---------------------------------------------------------------- gather A loader
+// Builds the A operand with plain loads for inputs whose channel rows a TMA
+// box cannot address.  An A row (output pixel) of the contraction is the
+// sequence of runs r = 0 .. R-1; run r holds the input bytes under filter row
+// r and taps s = 0 .. S-1, which for dil_w = 1 are S adjacent pixels, i.e.
+// S*C_in*elt contiguous bytes of the NHWC input, zero-padded to g_run_bytes.
+// A k-block is 128 bytes of that sequence, so each of its 16-byte pieces lies
+// inside one run: it is the bytes at one input address, with the pixels left
+// or right of the image (and the run's padding) zeroed.
+
+constexpr int kGatherBatch = 8;  // rows per lane whose loads are in flight together
+
+// Mask keeping bytes [lo, hi) of a 16-byte piece (lo, hi clamped to [0, 16]).
+__device__ __forceinline__ uint4 byte_range_mask(int lo, int hi) {
+  uint32_t m[4];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const int a = min(max(lo - 4 * j, 0), 4);
+    const int b = min(max(hi - 4 * j, 0), 4);
+    const uint32_t below_b = b == 4 ? 0xFFFFFFFFu : ((1u << (8 * b)) - 1u);
+    const uint32_t below_a = a == 4 ? 0xFFFFFFFFu : ((1u << (8 * a)) - 1u);
+    m[j] = b > a ? (below_b & ~below_a) : 0u;
+  }
+  return make_uint4(m[0], m[1], m[2], m[3]);
+}
+
+__device__ __forceinline__ uint4 and4(uint4 a, uint4 b) {
+  return make_uint4(a.x & b.x, a.y & b.y, a.z & b.z, a.w & b.w);
+}
+
+// Bytes [sh, sh + 16) of the 32 bytes (w0, w1), sh in [0, 16).
+__device__ __forceinline__ uint4 shift_pair(uint4 w0, uint4 w1, int sh) {
+  const uint32_t v[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+  const int wq = sh >> 2;
+  uint32_t t[6], u[5];
+#pragma unroll
+  for (int j = 0; j < 6; ++j) t[j] = (wq & 2) ? v[j + 2] : v[j];
+#pragma unroll
+  for (int j = 0; j < 5; ++j) u[j] = (wq & 1) ? t[j + 1] : t[j];
+  const uint32_t bits = static_cast<uint32_t>(sh & 3) * 8u;
+  return make_uint4(__funnelshift_r(u[0], u[1], bits), __funnelshift_r(u[1], u[2], bits),
+                    __funnelshift_r(u[2], u[3], bits), __funnelshift_r(u[3], u[4], bits));
+}
+
+// First padded input row (see g_pr) that the tile starting at GEMM row m0
+// reads, and how many consecutive padded rows it spans.
+__device__ __forceinline__ void gather_tile_rows(const ConvKernelParams& p, int m0, int& g_first,
+                                                 int& count) {
+  const int m_last = min(m0 + kBM * p.m_halves, p.rows[0]) - 1;
+  int na, oya, nb, oyb, xa, xb;
+  grid_pos(p, 0, m0, na, oya, xa);
+  grid_pos(p, 0, m_last, nb, oyb, xb);
+  g_first = na * p.g_pr + oya * p.step_h;
+  count = nb * p.g_pr + oyb * p.step_h + (p.g_runs - 1) * p.dil_h - g_first + 1;
+}
+
+// Row table of the tile whose first GEMM row is m0, one 16-byte entry per
+// row: {row index of filter row 0 -- in the input tensor, n*H + iy0, or,
+// with staging, the staging slot --, iy0, ix0, row < M}.  Built once per
+// tile by each producer warp, so that its k-blocks need no division and
+// every row's work is independent of the others'.
+__device__ __forceinline__ void gather_row_table(const ConvKernelParams& p, int4* tab, int m0,
+                                                 int g_first, int lane) {
+  const int rows = kBM * p.m_halves;
+  const FastDiv div_hw = p.div_ghw[0], div_wo = p.div_gw[0];
+  const int Wo = p.Wo, hw = p.Ho * p.Wo, M = p.rows[0];
+  const int step_h = p.step_h, step_w = p.step_w, base_h = p.base_h[0], base_w = p.base_w[0];
+  const int staged = p.g_stage, g_pr = p.g_pr, g_h = p.g_h;
+  for (int i = lane; i < rows; i += 32) {
+    const int m = m0 + i;
+    const int n = fast_div(m, div_hw);
+    const int rem = m - n * hw;
+    const int oy = fast_div(rem, div_wo);
+    const int ox = rem - oy * Wo;
+    const int iy0 = oy * step_h + base_h;
+    const int ix0 = ox * step_w + base_w;
+    const int row = staged ? n * g_pr + oy * step_h - g_first : n * g_h + iy0;
+    tab[i] = make_int4(row, iy0, ix0, m < M ? 1 : 0);
+  }
+  __syncwarp();
+}
+
+// Zeroes the margins of every slot of both staging buffers (the bulk copies
+// only ever write the rows between them).
+__device__ __forceinline__ void gather_zero_margins(const ConvKernelParams& p, uint8_t* gstage,
+                                                    int lane) {
+  const int slots = 2 * p.g_slots;
+  const int left = p.g_slot_pad / 16;
+  const int right = (p.g_slot_bytes - p.g_slot_pad - p.g_row_bytes) / 16;
+  const int per = left + right;
+  for (int i = lane; i < slots * per; i += 32) {
+    const int j = i / per, k = i - j * per;
+    const int buf = j / p.g_slots, slot = j - buf * p.g_slots;
+    const int off = k < left ? 16 * k : p.g_slot_pad + p.g_row_bytes + 16 * (k - left);
+    *reinterpret_cast<uint4*>(gstage + buf * p.g_stage_bytes + slot * p.g_slot_bytes + off) =
+        make_uint4(0u, 0u, 0u, 0u);
+  }
+  __syncwarp();
+}
+
+// Issues the bulk copies of the input rows the tile starting at GEMM row m0
+// reads into a staging buffer (slot j = padded row g_first + j, rows in the
+// padding are not copied), completing on `bar`.  The whole warp takes part:
+// lane l copies slots l, l + 32, ...
+__device__ __forceinline__ void gather_stage_tile(const ConvKernelParams& p, int m0, uint8_t* buf,
+                                                  uint32_t bar, int lane) {
+  int g_first, count;
+  gather_tile_rows(p, m0, g_first, count);
+  count = min(count, p.g_slots);  // the host's bound makes this a no-op
+  const int pad_h = -p.base_h[0], g_pr = p.g_pr, g_n = p.g_n, g_h = p.g_h;
+  const int row_bytes = p.g_row_bytes, slot_bytes = p.g_slot_bytes, slot_pad = p.g_slot_pad;
+  const uint8_t* const input = p.g_input;
+  const FastDiv div_pr = p.g_div_pr;
+  for (int j0 = 0; j0 < count; j0 += 32) {
+    // Each pass raises the transaction count by its bytes before its copies;
+    // the phase completes after the final arrival below.
+    const int j = j0 + lane;
+    const int g = g_first + j;
+    const int n = fast_div(g, div_pr);
+    const int iy = g - n * g_pr - pad_h;
+    const bool copy = j < count && n < g_n && iy >= 0 && iy < g_h;
+    const uint32_t bytes = __reduce_add_sync(0xFFFFFFFFu, copy ? static_cast<uint32_t>(row_bytes) : 0u);
+    if (lane == 0 && bytes) mbar_expect_tx(bar, bytes);
+    __syncwarp();
+    if (copy)
+      bulk_load(smem_u32(buf + static_cast<size_t>(j) * slot_bytes + slot_pad),
+                input + (static_cast<long long>(n) * g_h + iy) * row_bytes,
+                static_cast<uint32_t>(row_bytes), bar);
+  }
+  __syncwarp();
+  if (lane == 0) mbar_arrive(bar);
+}
+
+// Fills one A stage (128 * m_halves rows x 128 bytes, 128-byte swizzle) with
+// k-block kb, from the tile's row table and either the input in global
+// memory or the tile's staged input rows (kStaged; `stage` is their
+// shared-memory address).  Lane l writes piece l % 8 of rows l / 8, l / 8 + 4, ...
+// A piece keeps only the bytes of its run that lie inside the image: bytes
+// past the run's end (its padding) are cleared by a per-lane mask, pixels
+// left or right of the image by a byte mask on the (rare) edge rows, and
+// rows in the padding or past M are zero.
+template <bool kStaged>
+__device__ __forceinline__ void gather_a_kblock(const ConvKernelParams& p, const int4* tab,
+                                                uint32_t stage, uint8_t* a_stage, int kb,
+                                                int lane) {
+  // Every parameter the loop needs, in registers (the loop's stores could
+  // otherwise make the compiler re-read them).
+  const int g_h = p.g_h, g_w = p.g_w, g_s = p.g_s, g_slots = p.g_slots;
+  const int slot_bytes = p.g_slot_bytes, slot_pad = p.g_slot_pad;
+  const uint8_t* const input = p.g_input;
+  const int q = lane & 7;
+  const int kbyte = kb * 128 + 16 * q;
+  const int u = fast_div(kbyte, p.g_div_run);  // filter row of this piece's run
+  const int jb = kbyte - u * p.g_run_bytes;
+  const bool piece_ok = u < p.g_runs && jb < p.g_run_len_bytes;
+  const uint4 run_mask = byte_range_mask(0, p.g_run_len_bytes - jb);
+  const int pix_bytes = p.g_c * p.g_elt;
+  const long long row_bytes = static_cast<long long>(g_w) * pix_bytes;
+  const int dy = u * p.dil_h;
+  const int rows = kBM * p.m_halves;
+  for (int i0 = lane >> 3; i0 < rows; i0 += 4 * kGatherBatch) {
+    long long addr[kGatherBatch];
+    bool ok[kGatherBatch], edge[kGatherBatch];
+    int e_lo[kGatherBatch], e_hi[kGatherBatch];
+#pragma unroll
+    for (int g = 0; g < kGatherBatch; ++g) {
+      const int4 row = tab[i0 + 4 * g];
+      const int iy = row.y + dy;
+      // (Staged rows: the slot also stays inside the buffer, whatever the tile.)
+      ok[g] = piece_ok && row.w != 0 && static_cast<unsigned>(iy) < static_cast<unsigned>(g_h) &&
+              (!kStaged || static_cast<unsigned>(row.x + dy) < static_cast<unsigned>(g_slots));
+      // Bytes of the run inside the image: taps s with 0 <= ix0 + s < W.
+      edge[g] = row.z < 0 || row.z + g_s > g_w;
+      e_lo[g] = max(max(0, -row.z) * pix_bytes - jb, 0);
+      e_hi[g] = min(min(g_s, g_w - row.z) * pix_bytes - jb, 16);
+      addr[g] = kStaged ? static_cast<long long>((row.x + dy) * slot_bytes + slot_pad + row.z * pix_bytes + jb)
+                        : (row.x + dy) * row_bytes + static_cast<long long>(row.z) * pix_bytes + jb;
+    }
+    if (kStaged) {
+      // Five 4-byte words from the one holding the piece's first byte; the
+      // slot's zero margins supply the pixels left or right of the image.
+      uint32_t w[kGatherBatch][5];
+#pragma unroll
+      for (int g = 0; g < kGatherBatch; ++g) {
+        const uint32_t a = stage + (static_cast<uint32_t>(addr[g]) & ~3u);
+#pragma unroll
+        for (int k = 0; k < 5; ++k) w[g][k] = ok[g] ? lds32(a + 4u * k) : 0u;
+      }
+#pragma unroll
+      for (int g = 0; g < kGatherBatch; ++g) {
+        const uint32_t bits = (static_cast<uint32_t>(addr[g]) & 3u) * 8u;
+        const uint4 v = and4(make_uint4(__funnelshift_r(w[g][0], w[g][1], bits),
+                                        __funnelshift_r(w[g][1], w[g][2], bits),
+                                        __funnelshift_r(w[g][2], w[g][3], bits),
+                                        __funnelshift_r(w[g][3], w[g][4], bits)),
+                             run_mask);
+        const uint32_t row = static_cast<uint32_t>(i0 + 4 * g);
+        *reinterpret_cast<uint4*>(a_stage + swizzled_offset(row, static_cast<uint32_t>(q), 128u)) =
+            v;
+      }
+    } else {
+      // Only aligned 16-byte words that hold a kept byte are read, so every
+      // load stays inside the input's 16-byte granules.
+      uint4 w0[kGatherBatch], w1[kGatherBatch];
+#pragma unroll
+      for (int g = 0; g < kGatherBatch; ++g) {
+        const long long f = addr[g] & ~15ll;
+        w0[g] = make_uint4(0u, 0u, 0u, 0u);
+        w1[g] = make_uint4(0u, 0u, 0u, 0u);
+        if (ok[g] && e_hi[g] > e_lo[g]) {
+          if (addr[g] + e_lo[g] < f + 16) w0[g] = __ldg(reinterpret_cast<const uint4*>(input + f));
+          if (addr[g] + e_hi[g] > f + 16)
+            w1[g] = __ldg(reinterpret_cast<const uint4*>(input + f + 16));
+        }
+      }
+#pragma unroll
+      for (int g = 0; g < kGatherBatch; ++g) {
+        uint4 v = and4(shift_pair(w0[g], w1[g], static_cast<int>(addr[g] & 15)), run_mask);
+        if (__any_sync(0xFFFFFFFFu, edge[g]) && edge[g])
+          v = and4(v, byte_range_mask(e_lo[g], e_hi[g]));
+        if (!ok[g]) v = make_uint4(0u, 0u, 0u, 0u);
+        const uint32_t row = static_cast<uint32_t>(i0 + 4 * g);
+        *reinterpret_cast<uint4*>(a_stage + swizzled_offset(row, static_cast<uint32_t>(q), 128u)) =
+            v;
+      }
+    }
+  }
+}
+
+// Producer role of the gather loader: the whole warp builds the A k-blocks
+// whose sequence number has this warp's parity; lane 0 also streams the B
+// k-block (or, on the first tile, the resident filter block) by TMA.  The
+// stage's full barrier completes with lane 0's arrival after the warp's
+// shared-memory writes are fenced for the tensor cores, plus the B bytes.
+// With row staging, warp 0's lane 0 also issues the bulk copies of the next
+// tile's input rows into the other staging buffer once both warps have
+// released it; each warp waits for a tile's rows before its first k-block
+// there and releases the buffer after its last.
+__device__ __forceinline__ void gather_producer(const ConvKernelParams& p, int role, int lane,
+                                                uint8_t* a_ring, uint8_t* b_ring, uint8_t* b_res,
+                                                int4* tab, uint8_t* gstage, uint64_t* full,
+                                                uint64_t* empty, uint64_t* gst_full,
+                                                uint64_t* gst_empty, volatile int* abort_flag,
+                                                unsigned int* status, long long limit) {
+  const int stages = p.stages;
+  const uint32_t a_bytes = kBM * p.m_halves * 128u;
+  const uint32_t b_bytes = static_cast<uint32_t>(p.bn) * 128u;
+  int stage = 0;
+  uint32_t phase = 0;
+  long long seq = 0, last_issued = -1;
+  bool ok = true, first_tile = true;
+  int staged[2] = {0, 0};  // staging uses issued per buffer (warp 0, lane 0)
+  int it = 0;
+  for (int t = blockIdx.x; t < p.total_tiles && ok; t += gridDim.x, ++it) {
+    const TileInfo ti = decode_tile(p, t);
+    const bool load_res = p.b_resident && first_tile;
+    const int sb = it & 1;
+    if (p.g_stage) {
+      if (role == 0) {
+        if (first_tile) {
+          gather_zero_margins(p, gstage, lane);
+          gather_stage_tile(p, ti.m0, gstage, smem_u32(&gst_full[0]), lane);
+          ++staged[0];
+        }
+        const int tn = t + static_cast<int>(gridDim.x);
+        if (tn < p.total_tiles) {
+          // The other buffer last held tile it-1: both warps must be done with it.
+          const int nb = sb ^ 1;
+          int w = 1;
+          if (lane == 0)
+            w = mbar_wait_bounded(smem_u32(&gst_empty[nb]),
+                                  static_cast<uint32_t>(((it + 1) >> 1) & 1) ^ 1u, abort_flag,
+                                  status, kStatusProducerTimeout, limit) ? 1 : 0;
+          if (__shfl_sync(0xFFFFFFFFu, w, 0)) {
+            gather_stage_tile(p, decode_tile(p, tn).m0, gstage + nb * p.g_stage_bytes,
+                              smem_u32(&gst_full[nb]), lane);
+            ++staged[nb];
+          } else {
+            ok = false;
+          }
+        }
+      }
+      if (!ok) break;
+      // Every warp waits for the tile's rows, even one without a k-block
+      // here, so that no warp can release a buffer use twice.
+      int w = 1;
+      if (lane == 0)
+        w = mbar_wait_bounded(smem_u32(&gst_full[sb]), static_cast<uint32_t>((it >> 1) & 1),
+                              abort_flag, status, kStatusProducerTimeout, limit) ? 1 : 0;
+      if (!__shfl_sync(0xFFFFFFFFu, w, 0)) {
+        ok = false;
+        break;
+      }
+    }
+    first_tile = false;
+    int g_first = 0, count = 0;
+    if (p.g_stage) gather_tile_rows(p, ti.m0, g_first, count);
+    const uint32_t stage_u32 = smem_u32(gstage + sb * p.g_stage_bytes);
+    bool have_table = false;
+    for (int kb = 0; kb < ti.kblocks; ++kb, ++seq) {
+      if ((seq & 1) == role) {
+        if (!have_table) {
+          gather_row_table(p, tab, ti.m0, g_first, lane);
+          have_table = true;
+        }
+        int w = 1;
+        if (lane == 0)
+          w = mbar_wait_bounded(smem_u32(&empty[stage]), phase ^ 1u, abort_flag, status,
+                                kStatusProducerTimeout, limit, p.wait_hint_ns) ? 1 : 0;
+        w = __shfl_sync(0xFFFFFFFFu, w, 0);
+        if (!w) {
+          ok = false;
+          break;
+        }
+        last_issued = seq;
+        if (!(p.fault_mode == 1 && blockIdx.x == 0 && seq == 0)) {
+          // (fault_mode 1, a test hook: CTA 0 leaves its first stage un-armed.)
+          const uint32_t fb = smem_u32(&full[stage]);
+          if (lane == 0) {
+            if (!p.b_resident) {
+              mbar_expect_tx(fb, b_bytes);
+              tma_load_3d(smem_u32(b_ring + stage * b_bytes), &p.map_b, fb, kb * p.bk, ti.n0, 0);
+            } else if (load_res) {
+              mbar_expect_tx(fb, b_bytes);
+              tma_load_3d(smem_u32(b_res + kb * b_bytes), &p.map_b, fb, kb * p.bk, 0, 0);
+            }
+          }
+          if (p.g_stage)
+            gather_a_kblock<true>(p, tab, stage_u32, a_ring + stage * a_bytes, kb, lane);
+          else
+            gather_a_kblock<false>(p, tab, 0u, a_ring + stage * a_bytes, kb, lane);
+          fence_proxy_async_shared();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(fb);
+        }
+      }
+      if (++stage == stages) {
+        stage = 0;
+        phase ^= 1u;
+      }
+    }
+    if (p.g_stage && ok) {
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&gst_empty[sb]));
+    }
+  }
+  if (!ok && lane == 0) {
+    // Let this warp's copies in flight land before exiting: B k-blocks, and
+    // (warp 0) the latest row staging of each buffer.
+    for (long long q = last_issued - stages + 1; q <= last_issued; ++q)
+      if (q >= 0 && (q & 1) == role)
+        mbar_wait_drain(smem_u32(&full[q % stages]), static_cast<uint32_t>((q / stages) & 1),
+                        limit / 8 + 1);
+    for (int b = 0; b < 2; ++b)
+      if (staged[b] > 0)
+        mbar_wait_drain(smem_u32(&gst_full[b]), static_cast<uint32_t>((staged[b] - 1) & 1),
+                        limit / 8 + 1);
+  }
+}
+
+// kGather selects the producer role: the gather loader, or the TMA loaders
+// (im2col and row window).  The two are separate instances so that neither
+// carries the other's registers.
+template <int kKind, typename OutT, bool kGather>
 __global__ void __launch_bounds__(kThreads, 1)
     conv_igemm_kernel(const __grid_constant__ ConvKernelParams p) {
   extern __shared__ uint8_t smem_raw[];
@@ -462,7 +842,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* bres_full = drain + 1;
   uint64_t* src_full = bres_full + 1;  // [buffer][group]
   uint64_t* epi_done = src_full + 4;   // every epilogue warp has finished with TMEM
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(epi_done + 1);
+  uint64_t* gst_full = epi_done + 1;   // gather row staging: [buffer]
+  uint64_t* gst_empty = gst_full + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gst_empty + 2);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   unsigned int* status = p.status;
   const long long limit = p.timeout_cycles;
@@ -481,6 +863,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(smem_u32(drain), 1);
     mbar_init(smem_u32(bres_full), 1);
     mbar_init(smem_u32(epi_done), kEpilogueWarps);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(smem_u32(&gst_full[b]), 1);
+      mbar_init(smem_u32(&gst_empty[b]), 2);  // both producer warps
+    }
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -489,7 +875,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     tmem_relinquish();
   }
   if (warp == 0 && lane == 0) {
-    for (int ph = 0; ph < p.num_phases; ++ph) tma_prefetch_desc(&p.map_a[ph]);
+    if (!kGather)
+      for (int ph = 0; ph < p.num_phases; ++ph) tma_prefetch_desc(&p.map_a[ph]);
     tma_prefetch_desc(&p.map_b);
   }
   tc_fence_before();
@@ -505,7 +892,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------ producers
     // Two producer warps walk the same k-block sequence; k-block `seq` is
     // issued by producer (seq & 1), so two TMA issue streams overlap.
-    if (lane == 0) {
+    if constexpr (kGather) {
+      const int role = warp == 0 ? 0 : 1;
+      int4* tab = reinterpret_cast<int4*>(smem + p.off_gtab) + role * kBM * p.m_halves;
+      gather_producer(p, role, lane, a_ring, b_ring, b_res, tab, smem + p.off_gstage, full, empty,
+                      gst_full, gst_empty, abort_flag, status, limit);
+    } else if (lane == 0) {
       const int role = warp == 0 ? 0 : 1;
       int stage = 0;
       uint32_t phase = 0;

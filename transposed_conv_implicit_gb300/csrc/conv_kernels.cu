@@ -1,49 +1,10 @@
-// Instances of the implicit-GEMM kernel and the im2col probe, with their launchers.
-#include <atomic>
-
-#include "conv_internal.h"
-#include "conv_kernel.cuh"
+// Instances of the implicit-GEMM kernel with the TMA loaders, and the im2col
+// probe, with their launchers.
+#include "conv_launch.cuh"
 
 namespace convgb300 {
 
 namespace {
-
-constexpr int kMaxDevices = 64;
-
-template <int kKind, typename OutT>
-cudaError_t launch_instance(const ConvKernelParams& p, int grid, size_t smem_bytes,
-                            cudaStream_t stream) {
-  // The dynamic shared-memory limit is a per-device function attribute: raise
-  // it once per device to the largest size requested so far.
-  static std::atomic<size_t> configured[kMaxDevices];
-  int dev = 0;
-  cudaError_t err = cudaGetDevice(&dev);
-  if (err != cudaSuccess) return err;
-  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
-  if (configured[dev].load(std::memory_order_relaxed) < smem_bytes) {
-    err = cudaFuncSetAttribute(conv_igemm_kernel<kKind, OutT>,
-                               cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               static_cast<int>(smem_bytes));
-    if (err != cudaSuccess) return err;
-    configured[dev].store(smem_bytes, std::memory_order_relaxed);
-  }
-  // Programmatic stream serialization: the kernel may be scheduled while the
-  // previous kernel of the stream drains; it waits (griddepcontrol.wait)
-  // before touching global memory, so stream order is preserved.
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(static_cast<unsigned>(grid));
-  cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = smem_bytes;
-  cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  err = cudaLaunchKernelEx(&cfg, conv_igemm_kernel<kKind, OutT>, p);
-  if (err != cudaSuccess) return err;
-  return cudaGetLastError();
-}
 
 __global__ void im2col_probe_kernel(const __grid_constant__ CUtensorMap map, int c, int w, int h,
                                     int n, int off_w, int off_h, uint32_t row_bytes,
@@ -85,9 +46,8 @@ __global__ void im2col_probe_kernel(const __grid_constant__ CUtensorMap map, int
 
 cudaError_t launch_conv_igemm(int kind, bool out_bf16, const ConvKernelParams& p, int grid,
                               size_t smem_bytes, cudaStream_t stream) {
-  if (kind == kKindF8) return launch_instance<kKindF8, __nv_bfloat16>(p, grid, smem_bytes, stream);
-  if (out_bf16) return launch_instance<kKindF16, __nv_bfloat16>(p, grid, smem_bytes, stream);
-  return launch_instance<kKindF16, __half>(p, grid, smem_bytes, stream);
+  if (p.gather) return launch_conv_igemm_gather(kind, out_bf16, p, grid, smem_bytes, stream);
+  return launch_family<false>(kind, out_bf16, p, grid, smem_bytes, stream);
 }
 
 cudaError_t launch_im2col_probe(const CUtensorMap& map, int c, int w, int h, int n, int off_w,

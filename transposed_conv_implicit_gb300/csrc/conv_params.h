@@ -27,6 +27,13 @@ constexpr unsigned int kStatusProducerTimeout = 1u;
 constexpr unsigned int kStatusMmaTimeout = 2u;
 constexpr unsigned int kStatusEpilogueTimeout = 4u;
 
+// Division by a fixed divisor d >= 1 as a multiply and shift, exact for
+// 0 <= x < 2^31: q = (umulhi(x, mul) + x) >> shift with shift = ceil(log2 d)
+// and mul = floor(2^32 * (2^shift - d) / d) + 1 (taken mod 2^32).
+struct FastDiv {
+  uint32_t d, mul, shift;
+};
+
 struct ConvKernelParams {  // aligned like CUtensorMap (64 B or more)
   CUtensorMap map_a[kMaxPhases];  // im2col maps over the NHWC input, one per phase
   CUtensorMap map_b;              // tiled map over the packed filter [phase][C_out][K]
@@ -63,9 +70,17 @@ struct ConvKernelParams {  // aligned like CUtensorMap (64 B or more)
   int out_step_h, out_step_w;
   int dil_h, dil_w;                // input offset per filter tap
   int b_index[kMaxPhases];         // phase slot of the packed filter read by each phase
+  // Division by the fixed divisors above, as multiply and shift (a runtime
+  // integer division costs hundreds of cycles of latency).
+  FastDiv div_ntiles;              // n_tiles
+  FastDiv div_ghw[kMaxPhases];     // grid_h * grid_w
+  FastDiv div_gw[kMaxPhases];      // grid_w
+  FastDiv div_win_rb;              // win_row_blocks
 
   // Shared-memory carve-up (byte offsets from the 1024-B aligned base).
   uint32_t off_a, off_b, off_bres, off_src, off_stg, off_bar;
+  uint32_t off_gtab;               // gather loader: per-producer-warp row tables
+  uint32_t off_gstage;             // gather loader: two input-row staging buffers
   int b_resident;                  // whole packed filter kept in shared memory (one phase, one n-tile)
   int l2_prefetch;                 // prefetch the next tile's A boxes into L2
 
@@ -82,7 +97,43 @@ struct ConvKernelParams {  // aligned like CUtensorMap (64 B or more)
   int win_R, win_S;                // filter extent
   int win_pad_h, win_pad_w;
   uint32_t win_stage_bytes;        // A stage size (box plus the rows junk MMA rows may read)
-  int epi_mode;                    // 0 direct stores, 1 TMA store [M][C_out], 2 TMA store 4-D phase grid
+
+  // Gather A loader (forward convs whose channel rows TMA cannot address:
+  // C_in * elt not a multiple of 16 bytes, or under 32).  An A row is laid
+  // out as R runs; run r holds the input bytes under filter row r and taps
+  // s = 0 .. S-1, all channels: with dil_w = 1 these are S adjacent pixels,
+  // i.e. g_run_len_bytes contiguous bytes of the NHWC input.  Each run is
+  // zero-padded to g_run_bytes (a multiple of 16) so every 16-byte piece of
+  // an A row comes from one input address.  The producer warps build A with
+  // plain loads and shared-memory stores.
+  int gather;
+  const uint8_t* g_input;
+  long long g_input_bytes;
+  int g_n, g_h, g_w, g_c;          // input shape (NHWC)
+  int g_elt;                       // bytes per element
+  int g_runs;                      // runs per A row (= R)
+  int g_s;                         // filter extent along S
+  int g_run_len_bytes;             // valid bytes of a run (S * C_in * elt)
+  int g_run_bytes;                 // padded bytes of a run
+  // Row staging (when an input row, W * C_in * elt bytes, is a multiple of 16
+  // bytes): the input rows a tile reads arrive in shared memory by bulk
+  // copies, one tile ahead, and the pieces are cut from there.  Slot j of a
+  // tile's buffer holds padded input row g_first + j, where padded row
+  // g = n * g_pr + (iy + pad_h) enumerates each image's rows oy*stride +
+  // r*dil_h; slots in the padding stay unloaded.
+  // A slot is [g_slot_pad zero bytes][the row][zero bytes], g_slot_bytes in
+  // all: reads of pixels left or right of the image see zeros.
+  int g_stage;
+  int g_slots;                     // slots per staging buffer
+  int g_slot_bytes;                // slot stride (multiple of 16)
+  int g_slot_pad;                  // zero bytes before the row (multiple of 16)
+  int g_row_bytes;                 // W * C_in * elt
+  int g_pr;                        // padded rows per image: (Ho-1)*stride_h + (R-1)*dil_h + 1
+  FastDiv g_div_run, g_div_pr;     // division by g_run_bytes and by g_pr
+  uint32_t g_stage_bytes;          // bytes per staging buffer
+
+  int epi_mode;                    // 0 direct stores, 1 TMA store [M][C_out], 2 TMA 4-D phase grid,
+                                   // 3 TMA 4-D row window
   int cw;                          // epilogue chunk width in columns (16, 32 or 64)
   int src_bufs;                    // residual-source tile buffers (0, 1 or 2)
   uint32_t src_chunk_bytes;        // stride of one (half, chunk) item in a source buffer

@@ -69,6 +69,18 @@ class ConvCase:
     src_dist: Optional[Dist] = None
     epilogue: str = "none"
     out_hw: Optional[Tuple[int, int]] = None
+    pad_w: Optional[int] = None        # padding along W when it differs from `pad` (H)
+    dilation_w: Optional[int] = None   # dilation along W when it differs from `dilation` (H)
+
+    @property
+    def pads(self) -> Tuple[int, int]:
+        """(pad_h, pad_w)."""
+        return (self.pad, self.pad if self.pad_w is None else self.pad_w)
+
+    @property
+    def dilations(self) -> Tuple[int, int]:
+        """(dil_h, dil_w)."""
+        return (self.dilation, self.dilation if self.dilation_w is None else self.dilation_w)
 
     @property
     def out_dtype(self) -> str:
@@ -84,7 +96,7 @@ class ConvCase:
     def Wo(self) -> int:
         if self.out_hw is not None:
             return self.out_hw[1]
-        return (self.W + 2 * self.pad - self.dilation * (self.S - 1) - 1) // self.stride + 1
+        return (self.W + 2 * self.pads[1] - self.dilations[1] * (self.S - 1) - 1) // self.stride + 1
 
     @property
     def filter_shape(self):
@@ -169,6 +181,9 @@ WORKLOADS = {
                           _n(1.0), _n(1.0 / (16 * 256)), seed=1005, epilogue="relu", out_hw=(64, 64)),
     "fwd5x5_f16": ConvCase("fwd5x5_f16", "fwd", "f16", 8, 128, 128, 128, 128, 5, 5, 2, 2, "RSCF",
                            _n(1.0), _n(1.0 / (25 * 128)), seed=1015),
+    # RGB stem: 3 input channels (6-byte pixels) need the gather A loader.
+    "stem_c3_bf16": ConvCase("stem_c3_bf16", "fwd", "bf16", 32, 224, 224, 3, 64, 7, 7, 2, 3, "RSCF",
+                             _n(1.0), _n(2.0 / (49 * 3)), seed=1020, epilogue="relu"),
 }
 
 # The ResNet-style block: the stride-1 residual conv and the stride-2 downsample.
