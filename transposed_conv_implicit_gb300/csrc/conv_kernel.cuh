@@ -334,13 +334,18 @@ __device__ __forceinline__ bool mma_role(const ConvKernelParams& p, uint32_t tme
   const uint32_t bn_cols = static_cast<uint32_t>(p.bn);
   const uint32_t idesc = p.idesc;
   const uint32_t full0 = smem_u32(full), empty0 = smem_u32(empty);
+  // Loop-invariant parameters in registers: the tcgen05 asm statements below
+  // clobber memory, which would otherwise make the compiler re-read them.
+  const bool b_resident = p.b_resident != 0;
+  const uint32_t acc_stride = p.acc_stride;
+  const int total_tiles = p.total_tiles;
   int stage = 0;
   uint32_t phase = 0;
   uint32_t a_lo = a_lo0;
   uint32_t bs_lo = b_lo0;  // streamed B: advances with the ring
   bool ok = true;
   int it = 0;
-  for (int t = blockIdx.x; ok && t < p.total_tiles; t += gridDim.x, ++it) {
+  for (int t = blockIdx.x; ok && t < total_tiles; t += gridDim.x, ++it) {
     const TileInfo ti = decode_tile(p, t);
     const int acc = it & 1;
     if (!mbar_wait_bounded(smem_u32(&tempty[acc]), static_cast<uint32_t>(((it >> 1) & 1) ^ 1),
@@ -353,16 +358,17 @@ __device__ __forceinline__ bool mma_role(const ConvKernelParams& p, uint32_t tme
       mbar_arrive(smem_u32(&tfull[acc]));
       continue;
     }
-    const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc) * p.acc_stride;
+    const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc) * acc_stride;
     uint32_t br_lo = b_lo0;  // resident B: restarts every tile
-    for (int kb = 0; kb < ti.kblocks; ++kb) {
+    const int kblocks = ti.kblocks;
+    for (int kb = 0; kb < kblocks; ++kb) {
       if (!mbar_wait_bounded(full0 + 8u * stage, phase, abort_flag, status, kStatusMmaTimeout,
                              limit)) {
         ok = false;
         break;
       }
       tc_fence_after();
-      issue_kblock<kKind, kSteps, kHalves>(d_tmem, desc_hi, a_lo, p.b_resident ? br_lo : bs_lo,
+      issue_kblock<kKind, kSteps, kHalves>(d_tmem, desc_hi, a_lo, b_resident ? br_lo : bs_lo,
                                            half_lo, bn_cols, idesc, kb != 0 ? 1u : 0u);
       mma_commit(empty0 + 8u * stage);
       br_lo += b_step;
@@ -406,12 +412,17 @@ __device__ __forceinline__ bool mma_role_window(const ConvKernelParams& p, uint3
   const uint32_t full0 = smem_u32(full), empty0 = smem_u32(empty);
   const int taps_s = p.win_S;
   const int taps = p.win_R * p.win_S;
+  // Loop-invariant parameters in registers (the tcgen05 asm clobbers memory).
+  const int c_blocks = p.c_blocks, total_tiles = p.total_tiles;
+  const uint32_t acc_stride = p.acc_stride;
+  const uint32_t b_tap_step = static_cast<uint32_t>(c_blocks) * b_step;  // next tap, same block
+  const uint32_t a_row_skip = static_cast<uint32_t>(p.win_pitch - taps_s) * row_lo;
   int stage = 0;
   uint32_t phase = 0;
   uint32_t a_lo = a_lo0;
   bool ok = true;
   int it = 0;
-  for (int t = blockIdx.x; ok && t < p.total_tiles; t += gridDim.x, ++it) {
+  for (int t = blockIdx.x; ok && t < total_tiles; t += gridDim.x, ++it) {
     const int acc = it & 1;
     if (!mbar_wait_bounded(smem_u32(&tempty[acc]), static_cast<uint32_t>(((it >> 1) & 1) ^ 1),
                            abort_flag, status, kStatusMmaTimeout, limit)) {
@@ -419,23 +430,26 @@ __device__ __forceinline__ bool mma_role_window(const ConvKernelParams& p, uint3
       break;
     }
     tc_fence_after();
-    const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc) * p.acc_stride;
-    for (int cb = 0; cb < p.c_blocks; ++cb) {
+    const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc) * acc_stride;
+    for (int cb = 0; cb < c_blocks; ++cb) {
       if (!mbar_wait_bounded(full0 + 8u * stage, phase, abort_flag, status, kStatusMmaTimeout,
                              limit)) {
         ok = false;
         break;
       }
       tc_fence_after();
-      int r = 0, s = 0;
+      // Tap (r, s) reads box row r*pitch + s and filter block tap*c_blocks + cb.
+      uint32_t tap_lo = a_lo;
+      uint32_t b_lo = b_lo0 + static_cast<uint32_t>(cb) * b_step;
+      int s = 0;
       for (int tap = 0; tap < taps; ++tap) {
-        const uint32_t tap_lo = a_lo + static_cast<uint32_t>(r * p.win_pitch + s) * row_lo;
-        const uint32_t b_lo = b_lo0 + static_cast<uint32_t>(tap * p.c_blocks + cb) * b_step;
         issue_kblock<kKind, kSteps, kHalves>(d_tmem, desc_hi, tap_lo, b_lo, half_lo, bn_cols,
                                              idesc, (cb | tap) != 0 ? 1u : 0u);
+        b_lo += b_tap_step;
+        tap_lo += row_lo;
         if (++s == taps_s) {
           s = 0;
-          ++r;
+          tap_lo += a_row_skip;
         }
       }
       mma_commit(empty0 + 8u * stage);
