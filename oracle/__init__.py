@@ -64,9 +64,10 @@ def _load():
             lib.oracle_activation.restype = dbl
             conv_args = [P, i64, i64, i64, i64, P, i64, i64, i64]
             geo = [i32] * 6 + [i64, i64, i32, P, dbl, i32]
-            lib.oracle_conv2d_fwd.argtypes = conv_args + [i32] + geo + [P]
+            fwd_args = [P, i64, i64, i64, i64, i64, P, i64, i64, i64]  # + groups after C
+            lib.oracle_conv2d_fwd.argtypes = fwd_args + [i32] + geo + [P]
             lib.oracle_conv2d_fwd.restype = i32
-            lib.oracle_conv2d_fwd_points.argtypes = conv_args + [i32] + geo + [P, i64, P]
+            lib.oracle_conv2d_fwd_points.argtypes = fwd_args + [i32] + geo + [P, i64, P]
             lib.oracle_conv2d_fwd_points.restype = i32
             lib.oracle_conv_transposed.argtypes = conv_args + geo + [P]
             lib.oracle_conv_transposed.restype = i32
@@ -118,16 +119,17 @@ def _res_args(source, shape):
 
 
 def conv2d_fwd(x, w, *, filter_is_fcrs, stride=(1, 1), padding=(0, 0), dilation=(1, 1),
-               source=None, beta=0.0, act="none", out_hw=None) -> np.ndarray:
-    """Forward NHWC conv over fp64 arrays. x: [N,H,W,C]; w: FCRS [F,C,R,S] or RSCF [R,S,C,F]."""
+               source=None, beta=0.0, act="none", out_hw=None, groups=1) -> np.ndarray:
+    """Forward NHWC conv over fp64 arrays. x: [N,H,W,C]; w: FCRS [F,C/G,R,S] or RSCF
+    [R,S,C/G,F] for G = ``groups`` channel groups."""
     x, w = _f64(x), _f64(w)
     N, H, W, C = x.shape
     if filter_is_fcrs:
         F, C2, R, S = w.shape
     else:
         R, S, C2, F = w.shape
-    if C2 != C:
-        raise ValueError("filter C_in mismatch")
+    if C2 * groups != C or F % groups != 0:
+        raise ValueError("filter channels do not match the input and groups")
     sh, sw = stride
     ph, pw = padding
     dh, dw = dilation
@@ -135,7 +137,8 @@ def conv2d_fwd(x, w, *, filter_is_fcrs, stride=(1, 1), padding=(0, 0), dilation=
                                                fwd_out_size(W, S, sw, pw, dw))
     y = np.empty((N, Ho, Wo, F), dtype=np.float64)
     has_res, _, src = _res_args(source, y.shape)
-    rc = _load().oracle_conv2d_fwd(_ptr(x), N, H, W, C, _ptr(w), R, S, F, int(bool(filter_is_fcrs)),
+    rc = _load().oracle_conv2d_fwd(_ptr(x), N, H, W, C, int(groups), _ptr(w), R, S, F,
+                                   int(bool(filter_is_fcrs)),
                                    sh, sw, ph, pw, dh, dw, Ho, Wo, has_res, _ptr(src), float(beta),
                                    ACT_CODES[act], _ptr(y))
     if rc != 0:
@@ -144,7 +147,7 @@ def conv2d_fwd(x, w, *, filter_is_fcrs, stride=(1, 1), padding=(0, 0), dilation=
 
 
 def conv2d_fwd_points(x, w, pts, *, filter_is_fcrs, stride=(1, 1), padding=(0, 0),
-                      dilation=(1, 1), source=None, beta=0.0, act="none", out_hw=None):
+                      dilation=(1, 1), source=None, beta=0.0, act="none", out_hw=None, groups=1):
     """Forward conv evaluated only at flat NHWC output indices ``pts``."""
     x, w = _f64(x), _f64(w)
     N, H, W, C = x.shape
@@ -160,7 +163,7 @@ def conv2d_fwd_points(x, w, pts, *, filter_is_fcrs, stride=(1, 1), padding=(0, 0
     pts = np.ascontiguousarray(pts, dtype=np.int64)
     out = np.empty(pts.shape, dtype=np.float64)
     has_res, _, src = _res_args(source, (N, Ho, Wo, F))
-    rc = _load().oracle_conv2d_fwd_points(_ptr(x), N, H, W, C, _ptr(w), R, S, F,
+    rc = _load().oracle_conv2d_fwd_points(_ptr(x), N, H, W, C, int(groups), _ptr(w), R, S, F,
                                           int(bool(filter_is_fcrs)), sh, sw, ph, pw, dh, dw, Ho, Wo,
                                           has_res, _ptr(src), float(beta), ACT_CODES[act],
                                           _ptr(pts), pts.size, _ptr(out))

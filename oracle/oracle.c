@@ -29,6 +29,9 @@
  * exact fp64 value of act(conv + beta*source) over the decoded inputs.
  *
  * Readings where the pages are silent (stated once, used throughout):
+ *  - num_groups = G splits input and output channels into G equal groups;
+ *    output group g reads input group g only, and the filter's channel
+ *    extent is C_in/G (FCRS [C_out][C_in/G][R][S], RSCF [R][S][C_in/G][C_out]);
  *  - residual before activation: y = act(conv + beta*source);
  *  - activations: none, ReLU = max(v, 0), SiLU = v / (1 + exp(-v));
  *  - output size of the forward conv: floor((H + 2p - d(R-1) - 1)/s) + 1.
@@ -105,30 +108,34 @@ double oracle_activation(double v, int act)
     return v;
 }
 
-/* Filter element W(r, s, c, f) of a forward filter stored FCRS or RSCF. */
+/* Filter element W(r, s, c, f) of a forward filter stored FCRS or RSCF, C
+ * being the filter's channel extent (C_in / groups). */
 static double fwd_filter(const double *w, int64_t R, int64_t S, int64_t C, int64_t F,
                          int fcrs, int64_t r, int64_t s, int64_t c, int64_t f)
 {
-    if (fcrs) return w[((f * C + c) * R + r) * S + s];   /* [C_out][C_in][R][S] */
-    return w[((r * S + s) * C + c) * F + f];             /* [R][S][C_in][C_out] */
+    if (fcrs) return w[((f * C + c) * R + r) * S + s];   /* [C_out][C_in/G][R][S] */
+    return w[((r * S + s) * C + c) * F + f];             /* [R][S][C_in/G][C_out] */
 }
 
 /* One forward output element: the plain correlation sum over (r, s, c), input
- * taken as zero outside [0,H) x [0,W). */
-static double fwd_point(const double *x, int64_t H, int64_t W, int64_t C,
+ * taken as zero outside [0,H) x [0,W).  With G groups, output channel f
+ * belongs to group g = f / (F/G) and sums only the input channels
+ * g*(C/G) + c, c < C/G, against filter channel c. */
+static double fwd_point(const double *x, int64_t H, int64_t W, int64_t C, int64_t G,
                         const double *w, int64_t R, int64_t S, int64_t F, int fcrs,
                         int sh, int sw, int ph, int pw, int dh, int dw,
                         int64_t n, int64_t oy, int64_t ox, int64_t f)
 {
+    const int64_t Cg = C / G, g = f / (F / G);
     double acc = 0.0;
     for (int64_t r = 0; r < R; ++r) {
         for (int64_t s = 0; s < S; ++s) {
             int64_t iy = oy * sh - ph + r * dh;
             int64_t ix = ox * sw - pw + s * dw;
             if (iy < 0 || iy >= H || ix < 0 || ix >= W) continue;
-            for (int64_t c = 0; c < C; ++c)
-                acc += x[((n * H + iy) * W + ix) * C + c] *
-                       fwd_filter(w, R, S, C, F, fcrs, r, s, c, f);
+            for (int64_t c = 0; c < Cg; ++c)
+                acc += x[((n * H + iy) * W + ix) * C + g * Cg + c] *
+                       fwd_filter(w, R, S, Cg, F, fcrs, r, s, c, f);
         }
     }
     return acc;
@@ -136,8 +143,11 @@ static double fwd_point(const double *x, int64_t H, int64_t W, int64_t C,
 
 /* Full forward convolution, direct seven-loop form.
  * y[n][oy][ox][f] = act( sum_{r,s,c} X(n, oy*sh-ph+r*dh, ox*sw-pw+s*dw, c) * W(r,s,c,f)
- *                        + (has_res ? beta * src[n][oy][ox][f] : 0) ). */
-int oracle_conv2d_fwd(const double *x, int64_t N, int64_t H, int64_t W, int64_t C,
+ *                        + (has_res ? beta * src[n][oy][ox][f] : 0) ),
+ * with G channel groups ("dispatch_amd_4wave_conv2d", Args: num_groups), read
+ * in the usual way: C and F split into G equal groups, group g of the output
+ * sees group g of the input only, and the filter's channel extent is C/G. */
+int oracle_conv2d_fwd(const double *x, int64_t N, int64_t H, int64_t W, int64_t C, int64_t G,
                       const double *w, int64_t R, int64_t S, int64_t F, int fcrs,
                       int sh, int sw, int ph, int pw, int dh, int dw,
                       int64_t Ho, int64_t Wo,
@@ -146,13 +156,14 @@ int oracle_conv2d_fwd(const double *x, int64_t N, int64_t H, int64_t W, int64_t 
 {
     if (N < 0 || H <= 0 || W <= 0 || C <= 0 || R <= 0 || S <= 0 || F <= 0) return -1;
     if (sh <= 0 || sw <= 0 || dh <= 0 || dw <= 0 || Ho < 0 || Wo < 0) return -1;
+    if (G <= 0 || C % G != 0 || F % G != 0) return -1;
     for (int64_t n = 0; n < N; ++n)
         for (int64_t oy = 0; oy < Ho; ++oy)
             for (int64_t ox = 0; ox < Wo; ++ox)
                 for (int64_t f = 0; f < F; ++f) {
                     int64_t o = ((n * Ho + oy) * Wo + ox) * F + f;
-                    double v = fwd_point(x, H, W, C, w, R, S, F, fcrs, sh, sw, ph, pw, dh, dw,
-                                         n, oy, ox, f);
+                    double v = fwd_point(x, H, W, C, G, w, R, S, F, fcrs, sh, sw, ph, pw, dh,
+                                         dw, n, oy, ox, f);
                     if (has_res) v += beta * src[o];
                     y[o] = oracle_activation(v, act);
                 }
@@ -162,12 +173,13 @@ int oracle_conv2d_fwd(const double *x, int64_t N, int64_t H, int64_t W, int64_t 
 /* The same definition evaluated only at the flat NHWC output indices `pts`
  * (each in [0, N*Ho*Wo*F)); out[i] is the value at pts[i]. */
 int oracle_conv2d_fwd_points(const double *x, int64_t N, int64_t H, int64_t W, int64_t C,
-                             const double *w, int64_t R, int64_t S, int64_t F, int fcrs,
-                             int sh, int sw, int ph, int pw, int dh, int dw,
+                             int64_t G, const double *w, int64_t R, int64_t S, int64_t F,
+                             int fcrs, int sh, int sw, int ph, int pw, int dh, int dw,
                              int64_t Ho, int64_t Wo,
                              int has_res, const double *src, double beta, int act,
                              const int64_t *pts, int64_t npts, double *out)
 {
+    if (G <= 0 || C % G != 0 || F % G != 0) return -1;
     int64_t total = N * Ho * Wo * F;
     for (int64_t i = 0; i < npts; ++i) {
         int64_t o = pts[i];
@@ -176,7 +188,8 @@ int oracle_conv2d_fwd_points(const double *x, int64_t N, int64_t H, int64_t W, i
         int64_t ox = t % Wo; t /= Wo;
         int64_t oy = t % Ho;
         int64_t n = t / Ho;
-        double v = fwd_point(x, H, W, C, w, R, S, F, fcrs, sh, sw, ph, pw, dh, dw, n, oy, ox, f);
+        double v = fwd_point(x, H, W, C, G, w, R, S, F, fcrs, sh, sw, ph, pw, dh, dw, n, oy, ox,
+                             f);
         if (has_res) v += beta * src[o];
         out[i] = oracle_activation(v, act);
     }

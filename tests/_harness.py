@@ -26,7 +26,7 @@ def decode(t: torch.Tensor, dtype: str) -> np.ndarray:
 def contraction_length(case) -> int:
     if case.kind == "transposed":
         return math.ceil(case.R / case.stride) * math.ceil(case.S / case.stride) * case.C_in
-    return case.R * case.S * case.C_in
+    return case.R * case.S * case.C_in // case.groups
 
 
 def oracle_full(case, inp):
@@ -39,7 +39,7 @@ def oracle_full(case, inp):
                                       dilation=dl, source=src, beta=case.beta, act=case.epilogue)
     return oracle.conv2d_fwd(x, w, filter_is_fcrs=case.filter_layout == "FCRS", stride=st,
                              padding=pd, dilation=dl, source=src, beta=case.beta,
-                             act=case.epilogue, out_hw=(case.Ho, case.Wo))
+                             act=case.epilogue, out_hw=(case.Ho, case.Wo), groups=case.groups)
 
 
 def oracle_points(case, inp, pts):
@@ -53,7 +53,8 @@ def oracle_points(case, inp, pts):
                                              act=case.epilogue)
     return oracle.conv2d_fwd_points(x, w, pts, filter_is_fcrs=case.filter_layout == "FCRS",
                                     stride=st, padding=pd, dilation=dl, source=src,
-                                    beta=case.beta, act=case.epilogue, out_hw=(case.Ho, case.Wo))
+                                    beta=case.beta, act=case.epilogue, out_hw=(case.Ho, case.Wo),
+                                    groups=case.groups)
 
 
 def sample_points(case, count, seed=0):

@@ -22,13 +22,13 @@ GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
 RNG = np.random.default_rng(12345)
 
 
-def _torch_fwd(x, w, filter_is_fcrs, stride, pad, dil):
-    """PyTorch's own fp64 CPU conv2d (cross-correlation, FCRS weight)."""
+def _torch_fwd(x, w, filter_is_fcrs, stride, pad, dil, groups=1):
+    """PyTorch's own fp64 CPU conv2d (cross-correlation, FCRS weight [F, C/G, R, S])."""
     xt = torch.from_numpy(x).permute(0, 3, 1, 2)
     wt = torch.from_numpy(w)
-    if not filter_is_fcrs:                       # RSCF [R,S,C,F] -> [F,C,R,S]
+    if not filter_is_fcrs:                       # RSCF [R,S,C/G,F] -> [F,C/G,R,S]
         wt = wt.permute(3, 2, 0, 1)
-    y = F.conv2d(xt, wt.contiguous(), stride=stride, padding=pad, dilation=dil)
+    y = F.conv2d(xt, wt.contiguous(), stride=stride, padding=pad, dilation=dil, groups=groups)
     return y.permute(0, 2, 3, 1).contiguous().numpy()
 
 
@@ -329,3 +329,50 @@ def test_tolerance_formula():
     np.testing.assert_allclose(tol, [2e-3 * 24 * 1.5, 0.02 + 2e-3 * 24 * 1.5])
     tol8 = oracle.tolerance(np.array([1.0]), 2880, 1.0, 1.0, "f8e4m3")
     np.testing.assert_allclose(tol8, [0.02 + 2e-3 * math.sqrt(2880)])
+
+
+# ----------------------------------------------------------------------------- channel groups
+
+GROUP_CASES = [
+    # N, H, W, C, F, G, R, S, stride, pad, dil, fcrs
+    (1, 6, 7, 4, 6, 2, 3, 3, (1, 1), (1, 1), (1, 1), True),
+    (2, 7, 6, 8, 8, 4, 3, 3, (2, 2), (1, 1), (1, 1), False),
+    (1, 8, 8, 6, 6, 6, 3, 3, (1, 1), (1, 1), (1, 1), True),      # depthwise
+    (1, 9, 8, 6, 12, 3, 5, 3, (2, 1), (2, 1), (1, 2), False),
+    (2, 5, 5, 4, 2, 2, 1, 1, (1, 1), (0, 0), (1, 1), True),      # 1x1, one output per group
+]
+
+
+@pytest.mark.parametrize("case", GROUP_CASES)
+def test_grouped_forward_matches_torch(case):
+    N, H, W, C, Fo, G, R, S, st, pd, dl, fcrs = case
+    x = RNG.standard_normal((N, H, W, C))
+    w = RNG.standard_normal((Fo, C // G, R, S) if fcrs else (R, S, C // G, Fo))
+    ours = oracle.conv2d_fwd(x, w, filter_is_fcrs=fcrs, stride=st, padding=pd, dilation=dl,
+                             groups=G)
+    ref = _torch_fwd(x, w, fcrs, st, pd, dl, groups=G)
+    assert ours.shape == ref.shape
+    np.testing.assert_allclose(ours, ref, rtol=1e-12, atol=1e-12)
+    pts = np.arange(0, ours.size, 3, dtype=np.int64)
+    got = oracle.conv2d_fwd_points(x, w, pts, filter_is_fcrs=fcrs, stride=st, padding=pd,
+                                   dilation=dl, groups=G)
+    np.testing.assert_array_equal(got, ours.reshape(-1)[pts])
+
+
+def test_grouped_forward_is_independent_convs_side_by_side():
+    """Group g of the output is the ungrouped conv of group g of the input with
+    group g of the filter, computed on integers so the comparison is exact."""
+    G, Cg, Fg = 3, 2, 4
+    x = RNG.integers(-3, 4, size=(2, 6, 5, G * Cg)).astype(np.float64)
+    w = RNG.integers(-2, 3, size=(3, 3, Cg, G * Fg)).astype(np.float64)   # RSCF
+    y = oracle.conv2d_fwd(x, w, filter_is_fcrs=False, padding=(1, 1), groups=G)
+    for g in range(G):
+        part = oracle.conv2d_fwd(x[..., g * Cg:(g + 1) * Cg], w[..., g * Fg:(g + 1) * Fg],
+                                 filter_is_fcrs=False, padding=(1, 1))
+        assert np.array_equal(y[..., g * Fg:(g + 1) * Fg], part)
+
+
+def test_grouped_forward_rejects_indivisible_channels():
+    x = np.zeros((1, 4, 4, 6))
+    with pytest.raises(ValueError):
+        oracle.conv2d_fwd(x, np.zeros((4, 3, 3, 3)), filter_is_fcrs=True, groups=4)

@@ -71,6 +71,7 @@ class ConvCase:
     out_hw: Optional[Tuple[int, int]] = None
     pad_w: Optional[int] = None        # padding along W when it differs from `pad` (H)
     dilation_w: Optional[int] = None   # dilation along W when it differs from `dilation` (H)
+    groups: int = 1                    # channel groups (forward): filter channels = C_in / groups
 
     @property
     def pads(self) -> Tuple[int, int]:
@@ -101,9 +102,9 @@ class ConvCase:
     @property
     def filter_shape(self):
         if self.filter_layout == "FCRS":
-            return (self.C_out, self.C_in, self.R, self.S)
+            return (self.C_out, self.C_in // self.groups, self.R, self.S)
         if self.filter_layout == "RSCF":
-            return (self.R, self.S, self.C_in, self.C_out)
+            return (self.R, self.S, self.C_in // self.groups, self.C_out)
         if self.filter_layout == "RSFC":
             return (self.R, self.S, self.C_out, self.C_in)
         raise ValueError(self.filter_layout)
@@ -118,14 +119,14 @@ class ConvCase:
         transposed (the scatter count, no zero insertion)."""
         if self.kind == "transposed":
             return 2 * self.N * self.H * self.W * self.C_in * self.C_out * self.R * self.S
-        return 2 * self.N * self.Ho * self.Wo * self.C_out * self.R * self.S * self.C_in
+        return 2 * self.N * self.Ho * self.Wo * self.C_out * self.R * self.S * self.C_in // self.groups
 
     @property
     def bytes(self) -> int:
         """Algorithmic bytes: input, filter and output once, plus the source once."""
         e_in, e_out = ELT_BYTES[self.dtype], ELT_BYTES[self.out_dtype]
         b = self.N * self.H * self.W * self.C_in * e_in
-        b += self.R * self.S * self.C_in * self.C_out * e_in
+        b += self.R * self.S * self.C_in // self.groups * self.C_out * e_in
         b += self.N * self.Ho * self.Wo * self.C_out * e_out
         if self.has_residual:
             b += self.N * self.Ho * self.Wo * self.C_out * e_out
