@@ -78,6 +78,8 @@ const char* conv_status_string(conv_status_t status);
  * multiple of 16 bytes, or under 32) each filter row r is one run of
  * S*C_in elements zero-padded to a multiple of 16 bytes:
  * packed[f][r*RP + s*C_in + c], RP = ceil(S*C_in*elt / 16) * 16 / elt.
+ * For a grouped conv pack with c_in = C_in / num_groups (the filter's own
+ * channel extent).
  * `filter` is FCRS [C_out][C_in][R][S] when filter_is_fcrs is
  * nonzero, else RSCF [R][S][C_in][C_out] ("dispatch_amd_4wave_conv2d",
  * Parameters: filter_is_fcrs).  Returns CONV_ERR_WORKSPACE_TOO_SMALL when
@@ -110,10 +112,17 @@ size_t conv2d_workspace_size(int r, int s, int c_in, int c_out, conv_dtype_t dty
  * Gates (CONV_ERR_NOT_SUPPORTED otherwise): in_dtype in {BF16, F16, F8E4M3};
  * out_dtype as above; stride (1,1) or (2,2); dilation d_h, d_w in [1, 32];
  * padding per axis 0 <= p_h <= d_h*(r-1), 0 <= p_w <= d_w*(s-1) (a TMA map
- * also needs the padded corners within [-128, 127]); num_groups == 1;
+ * also needs the padded corners within [-128, 127]);
  * r, s <= 32.  Any c_in: channel rows of c_in * sizeof(in_dtype) bytes that
  * are a multiple of 16 and at least 32 are loaded by TMA; other channel
  * counts (e.g. c_in = 3) by the gather loader, which needs d_w == 1.
+ * num_groups = G splits input and output channels into G equal groups
+ * (output group g reads input group g; the filter is FCRS
+ * [c_out][c_in/G][r][s] or RSCF [r][s][c_in/G][c_out]); G > 1 needs
+ * (c_in/G) * sizeof(in_dtype) to be whole TMA channel blocks (a multiple of
+ * 16 bytes, at least 32, e.g. 16+ bf16 channels per group), else
+ * CONV_ERR_NOT_SUPPORTED; channels not divisible by G are
+ * CONV_ERR_INVALID_VALUE.
  * CONV_ERR_INVALID_VALUE: null pointers, non-positive sizes, ho/wo not equal
  * to floor((h + 2p - (r-1) - 1)/stride) + 1, has_residual with NULL source,
  * unknown epilogue.

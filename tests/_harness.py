@@ -97,10 +97,10 @@ def run_gpu(case, inp, *, packed=True, device="cuda:0", out=None, workspace=None
         if packed:
             pk = cg.conv2d_pack_filter(w, filter_is_fcrs=fcrs)
             cg.conv2d_fwd_packed(x, pk, out, r=case.R, s=case.S, stride=st, dilation=dl,
-                                 symmetric_padding=pd, **kw)
+                                 symmetric_padding=pd, num_groups=case.groups, **kw)
         else:
             cg.conv2d_fwd(x, w, out, stride=st, dilation=dl, symmetric_padding=pd,
-                          filter_is_fcrs=fcrs, **kw)
+                          filter_is_fcrs=fcrs, num_groups=case.groups, **kw)
     return out
 
 

@@ -21,13 +21,13 @@ pytestmark = pytest.mark.gpu
 
 
 def _fwd(name, dt, N, Hh, W, C, F, R, st, pd, *, layout="RSCF", res=False, beta=0.0, epi="none",
-         seed=1, xd=None, wd=None, S=None, dil=1, pad_w=None, dil_w=None):
+         seed=1, xd=None, wd=None, S=None, dil=1, pad_w=None, dil_w=None, groups=1):
     S = R if S is None else S
     return ConvCase(name, "fwd", dt, N, Hh, W, C, F, R, S, st, pd, layout,
-                    xd or Dist("normal", 1.0), wd or Dist("normal", 1.0 / (R * S * C)), seed=seed,
-                    dilation=dil, has_residual=res, beta=beta,
+                    xd or Dist("normal", 1.0), wd or Dist("normal", groups / (R * S * C)),
+                    seed=seed, dilation=dil, has_residual=res, beta=beta,
                     src_dist=Dist("normal", 1.0) if res else None, epilogue=epi, pad_w=pad_w,
-                    dilation_w=dil_w)
+                    dilation_w=dil_w, groups=groups)
 
 
 def _tr(name, dt, N, Hh, W, C, F, R, st, pd, extra=0, *, res=False, beta=0.0, epi="none", seed=1,
@@ -113,6 +113,13 @@ SMALL_FWD = [
     _fwd("b_window_7x7_p3", "bf16", 1, 14, 14, 64, 16, 7, 1, 3, res=True, beta=1.0),
     _fwd("b_pad_h1_w0", "bf16", 2, 10, 12, 64, 64, 3, 1, 1, pad_w=0),
     _fwd("e_pad_h0_w2_5x5", "f8e4m3", 1, 12, 12, 64, 32, 5, 2, 0, pad_w=2),
+    # Channel groups: per-group channel offsets, filter slots and output clipping.
+    _fwd("b_groups2", "bf16", 2, 11, 10, 64, 64, 3, 1, 1, groups=2),
+    _fwd("b_groups4_fg24_res", "bf16", 1, 12, 12, 128, 96, 3, 1, 1, groups=4, res=True, beta=1.0),
+    _fwd("h_groups2_s2_fcrs", "f16", 2, 13, 13, 64, 128, 3, 2, 1, groups=2, layout="FCRS"),
+    _fwd("e_groups8", "f8e4m3", 1, 10, 10, 256, 64, 3, 1, 1, groups=8, epi="relu"),
+    _fwd("b_groups2_fg3_direct", "bf16", 1, 9, 9, 64, 6, 3, 1, 1, groups=2),
+    _fwd("b_groups32_1x1", "bf16", 2, 8, 8, 1024, 512, 1, 1, 0, groups=32, epi="silu"),
 ]
 
 SMALL_TR = [
@@ -142,7 +149,7 @@ def test_small_case_every_element(case):
 
 @pytest.mark.parametrize("case", [c for c in SMALL_FWD + SMALL_TR if c.name in (
     "b_3x3_s2p1", "b_cout17_res", "e_3x3_s1p1_res", "t_h_4x4_s2p1_relu", "t_b_3x3_s2p1_op1",
-    "b_gather_c3_7x7_s2p3", "e_gather_c3_5x5")],
+    "b_gather_c3_7x7_s2p3", "e_gather_c3_5x5", "b_groups4_fg24_res", "h_groups2_s2_fcrs")],
     ids=lambda c: c.name)
 def test_unpacked_entry_point_equals_packed(case):
     """conv2d_fwd / conv_transposed pack in the workspace; the result must be
@@ -172,6 +179,7 @@ INT_CASES = [
     _int_case("int_b_stage_c3", "fwd", "bf16", 2, 16, 16, 3, 16, 7, 2, 3),
     _int_case("int_e_gather_c5", "fwd", "f8e4m3", 1, 9, 9, 5, 32, 3, 1, 1),
     _int_case("int_h_dil2", "fwd", "f16", 1, 12, 12, 16, 16, 3, 1, 2, dil=2),
+    _int_case("int_b_groups4", "fwd", "bf16", 1, 10, 10, 64, 32, 3, 1, 1, groups=4),
 ]
 
 

@@ -130,8 +130,8 @@ def conv2d_fwd(input, filter, output, *, stride=(1, 1), dilation=(1, 1), symmetr
         f_out, f_in, r, s = filter.shape
     else:
         r, s, f_in, f_out = filter.shape
-    if f_in != c_in or f_out != c_out:
-        raise ConvError(CONV_ERR_INVALID_VALUE, "filter shape does not match input/output")
+    if f_in * int(num_groups) != c_in or f_out != c_out:
+        raise ConvError(CONV_ERR_INVALID_VALUE, "filter shape does not match input/output/groups")
     if workspace is None:
         workspace = new_workspace(conv2d_workspace_size(r, s, c_in, c_out, dtype_name(input)),
                                   input.device)
@@ -150,8 +150,9 @@ def conv2d_fwd_packed(input, packed_filter, output, *, r, s, stride=(1, 1), dila
     n, h, w, c_in, ho, wo, c_out, st, dl, pd = _fwd_common(input, output, stride, dilation,
                                                              symmetric_padding, source)
     _need_dense(packed_filter)
+    groups = max(int(num_groups), 1)
     if (packed_filter.numel() * packed_filter.element_size()
-            != conv2d_packed_filter_bytes(r, s, c_in, c_out, dtype_name(input))):
+            != conv2d_packed_filter_bytes(r, s, c_in // groups, c_out, dtype_name(input))):
         raise ConvError(CONV_ERR_INVALID_VALUE, "packed filter size does not match")
     if workspace is None:
         workspace = new_workspace(CONV_STATUS_BYTES, input.device)

@@ -372,6 +372,7 @@ void choose_tiling(Plan* pl, const long long rows[], int num_phases, int max_kbl
 struct FwdShape {
   int n, h, w, c_in, r, s, c_out, ho, wo;
   int stride_h, stride_w, pad_h, pad_w, dil_h, dil_w;
+  int groups;  // channel groups (num_groups)
   conv_dtype_t in_dtype, out_dtype;
 };
 
@@ -388,7 +389,19 @@ conv_status_t check_fwd_shape(const FwdShape& f, int num_groups) {
   // whole output rows would see only padding).
   if (f.pad_h < 0 || f.pad_w < 0 || f.pad_h > f.dil_h * (f.r - 1) || f.pad_w > f.dil_w * (f.s - 1))
     return CONV_ERR_NOT_SUPPORTED;
-  if (num_groups != 1) return CONV_ERR_NOT_SUPPORTED;
+  if (num_groups < 1 || f.c_in % num_groups != 0 || f.c_out % num_groups != 0)
+    return CONV_ERR_INVALID_VALUE;
+  if (num_groups > 1) {
+    // Grouped convs run on the TMA im2col loader: a group's input channels
+    // must be whole channel blocks of TMA rows, so that no load reaches into
+    // the next group.
+    const int cg = f.c_in / num_groups;
+    int bk = 0;
+    uint32_t rb = 0;
+    if (gather_mode(cg, elt_bytes(f.in_dtype)) ||
+        channel_block(cg, elt_bytes(f.in_dtype), &bk, &rb) != CONV_OK || cg % bk != 0)
+      return CONV_ERR_NOT_SUPPORTED;
+  }
   // The gather loader reads S adjacent pixels per filter row and indexes
   // input pixels with 32-bit integers.
   if (gather_mode(f.c_in, elt_bytes(f.in_dtype)) &&
@@ -500,10 +513,17 @@ conv_status_t plan_gather(const FwdShape& f, Plan* pl) {
 
 conv_status_t plan_fwd(const FwdShape& f, Plan* pl, int num_sms, int has_residual) {
   std::memset(pl, 0, sizeof(*pl));
-  const bool gather = gather_mode(f.c_in, elt_bytes(f.in_dtype));
-  conv_status_t st = gather ? plan_gather(f, pl) : plan_channels(pl, f.in_dtype, f.c_in);
+  const int groups = std::max(f.groups, 1);
+  const int cg = f.c_in / groups, fg = f.c_out / groups;
+  const bool gather = gather_mode(cg, elt_bytes(f.in_dtype));
+  if (gather && groups > 1) return CONV_ERR_NOT_SUPPORTED;
+  conv_status_t st = gather ? plan_gather(f, pl) : plan_channels(pl, f.in_dtype, cg);
   if (st != CONV_OK) return st;
   ConvKernelParams& kp = pl->kp;
+  if (groups > 1 && kp.c_tail != 0) return CONV_ERR_NOT_SUPPORTED;
+  kp.groups = groups;
+  kp.c_group = cg;
+  kp.f_group = fg;
   kp.num_phases = 1;
   kp.grid_h[0] = f.ho;
   kp.grid_w[0] = f.wo;
@@ -521,21 +541,23 @@ conv_status_t plan_fwd(const FwdShape& f, Plan* pl, int num_sms, int has_residua
   kp.out_step_w = 1;
   kp.dil_h = f.dil_h;
   kp.dil_w = f.dil_w;
-  const long long rows[1] = {kp.rows[0]};
-  choose_tiling(pl, rows, 1, kp.taps_h[0] * kp.taps_w[0] * kp.c_blocks, f.c_out, num_sms);
+  // (Groups repeat the tile grid: the model sees all groups' rows.)
+  const long long rows[1] = {static_cast<long long>(kp.rows[0]) * groups};
+  choose_tiling(pl, rows, 1, kp.taps_h[0] * kp.taps_w[0] * kp.c_blocks, fg, num_sms);
   const int tile_m = kBM * kp.m_halves;
   const int m_tiles = (kp.rows[0] + tile_m - 1) / tile_m;
   kp.tile_start[0] = 0;
   kp.tile_start[1] = m_tiles * kp.n_tiles;
-  kp.total_tiles = kp.tile_start[1];
+  kp.tiles_per_group = kp.tile_start[1];
+  kp.total_tiles = kp.tile_start[1] * groups;
   kp.Ho = f.ho;
   kp.Wo = f.wo;
   kp.Cout = f.c_out;
-  kp.vec_ok = (f.c_out * 2) % 16 == 0;
+  kp.vec_ok = (f.c_out * 2) % 16 == 0 && (fg * 2) % 16 == 0;
   pl->phases_packed = 1;
-  pl->kmax = static_cast<int>(fwd_packed_k(f.r, f.s, f.c_in, elt_bytes(f.in_dtype)));
+  pl->kmax = static_cast<int>(fwd_packed_k(f.r, f.s, cg, elt_bytes(f.in_dtype)));
   pl->packed_bytes = static_cast<size_t>(f.c_out) * pl->kmax * elt_bytes(f.in_dtype);
-  if (!gather) plan_window_or_keep(f, pl, num_sms, has_residual);
+  if (!gather && groups == 1) plan_window_or_keep(f, pl, num_sms, has_residual);
   return CONV_OK;
 }
 
@@ -829,15 +851,20 @@ conv_status_t launch_pack_tr(const Plan& pl, const void* filter, int r, int s, i
 // ------------------------------------------------------------------ epilogue + shared memory
 conv_status_t plan_memory_direct(Plan* pl);
 
-conv_status_t encode_out_map_2d(CUtensorMap* map, const void* base, int c_out, long long rows,
-                                conv_dtype_t out_dt, int cw) {
+// The output (or source) as [rows][groups][c_out / groups]: a store box of cw
+// channels x 1 group x 128 rows clips at the group's last channel as well as
+// at the last row (groups = 1 is the plain [rows][c_out] matrix).
+conv_status_t encode_out_map_grouped(CUtensorMap* map, const void* base, int c_out, int groups,
+                                     long long rows, conv_dtype_t out_dt, int cw) {
   const DriverFns* fns = driver_fns();
   if (!fns) return CONV_ERR_CUDA;
-  cuuint64_t dims[2] = {static_cast<cuuint64_t>(c_out), static_cast<cuuint64_t>(rows)};
-  cuuint64_t strides[1] = {static_cast<cuuint64_t>(c_out) * 2};
-  cuuint32_t box[2] = {static_cast<cuuint32_t>(cw), static_cast<cuuint32_t>(kBM)};
-  cuuint32_t estr[2] = {1, 1};
-  CUresult r = fns->tiled(map, tmap_dtype(out_dt), 2, const_cast<void*>(base), dims, strides, box,
+  const int fg = c_out / groups;
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(fg), static_cast<cuuint64_t>(groups),
+                        static_cast<cuuint64_t>(rows)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(fg) * 2, static_cast<cuuint64_t>(c_out) * 2};
+  cuuint32_t box[3] = {static_cast<cuuint32_t>(cw), 1, static_cast<cuuint32_t>(kBM)};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = fns->tiled(map, tmap_dtype(out_dt), 3, const_cast<void*>(base), dims, strides, box,
                           estr, CU_TENSOR_MAP_INTERLEAVE_NONE, tmap_swizzle(cw * 2),
                           CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? CONV_OK : CONV_ERR_CUDA;
@@ -902,7 +929,8 @@ conv_status_t layout_memory(Plan* pl, int has_residual) {
   if (kp.m_halves * (kp.bn / cw) < kEpilogueGroups && cw > 16) cw /= 2;
   const uint32_t a_bytes = kBM * kp.m_halves * kp.sw_bytes;
   const uint32_t b_bytes = static_cast<uint32_t>(kp.bn) * kp.sw_bytes;
-  const bool can_res = kp.num_phases == 1 && kp.n_tiles == 1 && !(std::getenv("CONV_FILTER_RESIDENT") && env_int("CONV_FILTER_RESIDENT") == 0);
+  const bool can_res = kp.num_phases == 1 && kp.n_tiles == 1 && kp.groups <= 1 &&
+                       !(std::getenv("CONV_FILTER_RESIDENT") && env_int("CONV_FILTER_RESIDENT") == 0);
   const size_t bres = can_res ? static_cast<size_t>(kp.taps_h[0]) * kp.taps_w[0] * kp.c_blocks * b_bytes : 0;
   const size_t src_tile = static_cast<size_t>(kBM) * kp.m_halves * kp.bn * 2;
   const size_t chunk = static_cast<size_t>(kBM) * cw * 2;
@@ -1064,9 +1092,10 @@ conv_status_t plan_memory(Plan* pl, int n_images, const void* output, const void
       return CONV_ERR_CUDA;
   } else if (kp.epi_mode == 1) {
     const long long rows = kp.rows[0];
-    if (encode_out_map_2d(&kp.map_out[0], output, kp.Cout, rows, out_dt, kp.cw) != CONV_OK ||
-        (has_residual &&
-         encode_out_map_2d(&kp.map_src[0], source, kp.Cout, rows, out_dt, kp.cw) != CONV_OK))
+    if (encode_out_map_grouped(&kp.map_out[0], output, kp.Cout, kp.groups, rows, out_dt, kp.cw) !=
+            CONV_OK ||
+        (has_residual && encode_out_map_grouped(&kp.map_src[0], source, kp.Cout, kp.groups, rows,
+                                                out_dt, kp.cw) != CONV_OK))
       return plan_memory_direct(pl);
   } else if (kp.epi_mode == 2) {
     for (int ph = 0; ph < kp.num_phases; ++ph)
@@ -1090,7 +1119,7 @@ conv_status_t plan_memory_direct(Plan* pl) {
   kp.stg_bufs = 0;
   kp.src_chunk_bytes = 0;
   kp.valid_rows = kBM;
-  const bool can_res = kp.num_phases == 1 && kp.n_tiles == 1;
+  const bool can_res = kp.num_phases == 1 && kp.n_tiles == 1 && kp.groups <= 1;
   const size_t bres = can_res ? static_cast<size_t>(kp.taps_h[0]) * kp.taps_w[0] * kp.c_blocks * b_bytes : 0;
   bool res = false;
   int stages = 0;
@@ -1130,8 +1159,19 @@ conv_status_t finish_and_launch(Plan* pl, int n_images, const void* packed, void
                                 int has_residual, const void* source, float beta,
                                 conv_epilogue_t epilogue, void* workspace, cudaStream_t stream) {
   ConvKernelParams& kp = pl->kp;
-  conv_status_t st = encode_filter_map(&kp.map_b, packed, pl->kmax, kp.Cout, pl->phases_packed,
-                                       pl->in_dtype, kp.bk, kp.bn, kp.sw_bytes);
+  if (kp.groups < 1) {  // plans without channel groups
+    kp.groups = 1;
+    kp.c_group = kp.c_in;
+    kp.f_group = kp.Cout;
+    kp.tiles_per_group = kp.total_tiles;
+  }
+  // Filter slots: the stride phases, or the channel groups ([G][C_out/G][K]).
+  conv_status_t st =
+      kp.groups > 1
+          ? encode_filter_map(&kp.map_b, packed, pl->kmax, kp.f_group, kp.groups, pl->in_dtype,
+                              kp.bk, kp.bn, kp.sw_bytes)
+          : encode_filter_map(&kp.map_b, packed, pl->kmax, kp.Cout, pl->phases_packed,
+                              pl->in_dtype, kp.bk, kp.bn, kp.sw_bytes);
   if (st != CONV_OK) return st;
   st = plan_memory(pl, n_images, output, has_residual ? source : nullptr, has_residual);
   if (st != CONV_OK) return st;
@@ -1156,6 +1196,7 @@ conv_status_t finish_and_launch(Plan* pl, int n_images, const void* packed, void
     kp.div_gw[ph] = make_fast_div(gw);
   }
   kp.div_win_rb = make_fast_div(static_cast<uint32_t>(std::max(kp.win_row_blocks, 1)));
+  kp.div_tpg = make_fast_div(static_cast<uint32_t>(std::max(kp.tiles_per_group, 1)));
   // Prefetching the next tile's input only pays when CTAs walk several tiles
   // that all start at the first C_out tile (one n-tile).
   kp.l2_prefetch = (kp.n_tiles == 1 && env_int("CONV_L2_PREFETCH") != -1) ? 1 : 0;
@@ -1191,6 +1232,7 @@ FwdShape make_fwd_shape(int n, int h, int w, int c_in, conv_dtype_t in_dtype, in
   f.stride_h = stride[0]; f.stride_w = stride[1];
   f.pad_h = pad[0]; f.pad_w = pad[1];
   f.dil_h = dilation[0]; f.dil_w = dilation[1];
+  f.groups = 1;
   f.in_dtype = in_dtype; f.out_dtype = out_dtype;
   return f;
 }
@@ -1209,16 +1251,19 @@ TrShape make_tr_shape(int n, int h, int w, int c_in, conv_dtype_t in_dtype, int 
 
 // Common body of conv2d_fwd / conv2d_fwd_packed.  `filter` is raw (packed
 // into the workspace first) unless `prepacked`.
-conv_status_t fwd_impl(const void* input, const FwdShape& f, const void* filter, int fcrs,
+conv_status_t fwd_impl(const void* input, const FwdShape& shape, const void* filter, int fcrs,
                        bool prepacked, void* output, int num_groups, int has_residual,
                        const void* source, float beta, conv_epilogue_t epilogue, void* workspace,
                        size_t workspace_bytes, cudaStream_t stream) {
   conv_status_t st = check_common_ptrs(input, filter, output, has_residual, source, workspace);
   if (st != CONV_OK) return st;
   if (!epilogue_ok(epilogue)) return CONV_ERR_INVALID_VALUE;
-  st = check_fwd_shape(f, num_groups);
+  st = check_fwd_shape(shape, num_groups);
   if (st != CONV_OK) return st;
-  const size_t packed_bytes = conv2d_packed_filter_bytes(f.r, f.s, f.c_in, f.c_out, f.in_dtype);
+  FwdShape f = shape;
+  f.groups = num_groups;
+  const int cg = f.c_in / num_groups;  // the filter's channel extent
+  const size_t packed_bytes = conv2d_packed_filter_bytes(f.r, f.s, cg, f.c_out, f.in_dtype);
   const size_t need = CONV_STATUS_BYTES + (prepacked ? 0 : round_up_256(packed_bytes));
   if (workspace_bytes < need) return CONV_ERR_WORKSPACE_TOO_SMALL;
   const int sms = device_sm_count();
@@ -1231,7 +1276,7 @@ conv_status_t fwd_impl(const void* input, const FwdShape& f, const void* filter,
   const void* packed = filter;
   if (!prepacked) {
     void* dst = static_cast<uint8_t*>(workspace) + CONV_STATUS_BYTES;
-    st = launch_pack_fwd(filter, f.r, f.s, f.c_in, f.c_out, fcrs, f.in_dtype, dst, stream);
+    st = launch_pack_fwd(filter, f.r, f.s, cg, f.c_out, fcrs, f.in_dtype, dst, stream);
     if (st != CONV_OK) return st;
     packed = dst;
   }

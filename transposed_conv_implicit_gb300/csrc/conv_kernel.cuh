@@ -47,6 +47,7 @@ namespace convgb300 {
 
 struct TileInfo {
   int phase;
+  int group;    // channel group (forward convs with num_groups > 1), else 0
   int m0;       // first row (pixel) of the tile within its phase grid
   int n0;       // first output channel
   int kblocks;  // k-blocks in this tile's contraction
@@ -62,16 +63,23 @@ __device__ __forceinline__ TileInfo decode_tile(const ConvKernelParams& p, int t
   if (p.window) {  // one C_out tile; m0 carries the tile index
     TileInfo ti;
     ti.phase = 0;
+    ti.group = 0;
     ti.n0 = 0;
     ti.m0 = t;
     ti.kblocks = p.c_blocks;
     return ti;
+  }
+  int group = 0;
+  if (p.groups > 1) {
+    group = fast_div(t, p.div_tpg);
+    t -= group * p.tiles_per_group;
   }
   int ph = 0;
   while (ph + 1 < p.num_phases && t >= p.tile_start[ph + 1]) ++ph;
   const int local = t - p.tile_start[ph];
   TileInfo ti;
   ti.phase = ph;
+  ti.group = group;
   const int mt = fast_div(local, p.div_ntiles);
   ti.n0 = (local - mt * p.n_tiles) * p.bn;
   ti.m0 = mt * (kBM * p.m_halves);
@@ -277,7 +285,7 @@ __device__ __forceinline__ void issue_source_items(const ConvKernelParams& p, co
     const int mh = ti.m0 + h * kBM;
     const uint32_t dst = smem_u32(buf + q * p.src_chunk_bytes);
     if (p.epi_mode == 1) {
-      tma_load_2d(dst, &p.map_src[ti.phase], bar, ti.n0 + c * p.cw, mh);
+      tma_load_3d(dst, &p.map_src[ti.phase], bar, ti.n0 + c * p.cw, ti.group, mh);
     } else if (p.epi_mode == 3) {
       int n_img, oy0;
       window_origin(p, ti.m0, n_img, oy0);
@@ -964,7 +972,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int w0 = p.base_w[ph] + i * p.step_w;
         const int tw = p.taps_w[ph];
         const CUtensorMap* amap = &p.map_a[ph];
-        const int bz = p.b_index[ph];
+        // Filter slot: the stride phase, or the channel group.
+        const int bz = p.groups > 1 ? ti.group : p.b_index[ph];
+        const int c_base = ti.group * p.c_group;  // first input channel of the group
         int cb = 0, uw = 0, uh = 0;
         int bk_k = 0;  // k coordinate of this k-block in the packed filter: tap*C_in + cb*bk
         const bool load_res = p.b_resident && first_tile;
@@ -982,7 +992,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           pf_h0 = p.base_h[tin.phase] + pj * p.step_h;
           pf_w0 = p.base_w[tin.phase] + pi * p.step_w;
           pf_map = &p.map_a[tin.phase];
-          if (tin.kblocks != ti.kblocks || tin.n0 != 0 || tin.m0 == ti.m0) pf_n = -1;  // skip
+          if (tin.kblocks != ti.kblocks || tin.n0 != 0 || tin.m0 == ti.m0 || tin.group != ti.group)
+            pf_n = -1;  // skip
         }
         for (int kb = 0; kb < ti.kblocks; ++kb, ++seq) {
           if ((seq & 1) == role) {
@@ -996,8 +1007,8 @@ __global__ void __launch_bounds__(kThreads, 1)
               // (fault_mode 1, a test hook: CTA 0 leaves its first stage un-armed.)
               const uint32_t fb = smem_u32(&full[stage]);
               mbar_arrive_expect_tx(fb, stage_tx + (load_res ? b_bytes : 0u));
-              tma_load_im2col_4d(smem_u32(a_ring + stage * a_bytes), amap, fb, cb * p.bk, w0, h0,
-                                 n_img, static_cast<uint16_t>(uw * p.dil_w),
+              tma_load_im2col_4d(smem_u32(a_ring + stage * a_bytes), amap, fb, c_base + cb * p.bk,
+                                 w0, h0, n_img, static_cast<uint16_t>(uw * p.dil_w),
                                  static_cast<uint16_t>(uh * p.dil_h));
               if (!p.b_resident)
                 tma_load_3d(smem_u32(b_ring + stage * b_bytes), &p.map_b, fb, bk_k, ti.n0, bz);
@@ -1005,7 +1016,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tma_load_3d(smem_u32(b_res + kb * b_bytes), &p.map_b, fb, bk_k, 0, bz);
             }
             if (pf && pf_n >= 0)
-              tma_prefetch_im2col_4d(pf_map, cb * p.bk, pf_w0, pf_h0, pf_n,
+              tma_prefetch_im2col_4d(pf_map, c_base + cb * p.bk, pf_w0, pf_h0, pf_n,
                                      static_cast<uint16_t>(uw * p.dil_w),
                                      static_cast<uint16_t>(uh * p.dil_h));
           }
@@ -1178,7 +1189,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           named_barrier(bar_id, 128);
           if (leader) {
             if (p.epi_mode == 1) {
-              tma_store_2d(&p.map_out[ti.phase], smem_u32(buf), ti.n0 + c * p.cw, mh);
+              tma_store_3d(&p.map_out[ti.phase], smem_u32(buf), ti.n0 + c * p.cw, ti.group, mh);
             } else if (p.epi_mode == 3) {
               int n_img, oy0;
               window_origin(p, ti.m0, n_img, oy0);
@@ -1233,7 +1244,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             grid_pos(p, ph, m, n_img, j, i);
             const long long oy = static_cast<long long>(p.out_step_h) * j + p.out_off_h[ph];
             const long long ox = static_cast<long long>(p.out_step_w) * i + p.out_off_w[ph];
-            out_off = ((static_cast<long long>(n_img) * p.Ho + oy) * p.Wo + ox) * p.Cout;
+            out_off = ((static_cast<long long>(n_img) * p.Ho + oy) * p.Wo + ox) * p.Cout +
+                      static_cast<long long>(ti.group) * p.f_group;
           }
           const uint32_t taddr = tmem_base + lane_field + static_cast<uint32_t>(acc) * p.acc_stride +
                                  static_cast<uint32_t>(h * p.bn);
@@ -1246,9 +1258,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
               for (int j = 0; j < 16; ++j) v[j] = 0u;
             }
+            // Columns past the group's (or the conv's) last output channel are not stored.
             const int ch = ti.n0 + c0;
-            if (valid && ch < p.Cout) {
-              const int nvalid = p.Cout - ch < 16 ? p.Cout - ch : 16;
+            if (valid && ch < p.f_group) {
+              const int nvalid = p.f_group - ch < 16 ? p.f_group - ch : 16;
               epilogue_16_direct<OutT>(p, out_off + ch, v, nvalid);
             }
           }

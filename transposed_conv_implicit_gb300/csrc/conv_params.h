@@ -70,12 +70,20 @@ struct ConvKernelParams {  // aligned like CUtensorMap (64 B or more)
   int out_step_h, out_step_w;
   int dil_h, dil_w;                // input offset per filter tap
   int b_index[kMaxPhases];         // phase slot of the packed filter read by each phase
+  // Channel groups (forward convs): output group g reads input channels
+  // [g*c_group, (g+1)*c_group) through filter slot g and writes channels
+  // [g*f_group, (g+1)*f_group).  Tiles are group-major:
+  // t = g * tiles_per_group + (the tile within the group).
+  int groups;
+  int c_group, f_group;
+  int tiles_per_group;
   // Division by the fixed divisors above, as multiply and shift (a runtime
   // integer division costs hundreds of cycles of latency).
   FastDiv div_ntiles;              // n_tiles
   FastDiv div_ghw[kMaxPhases];     // grid_h * grid_w
   FastDiv div_gw[kMaxPhases];      // grid_w
   FastDiv div_win_rb;              // win_row_blocks
+  FastDiv div_tpg;                 // tiles_per_group
 
   // Shared-memory carve-up (byte offsets from the 1024-B aligned base).
   uint32_t off_a, off_b, off_bres, off_src, off_stg, off_bar;
