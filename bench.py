@@ -46,7 +46,8 @@ KERNEL_SOURCES = ["transposed_conv_implicit_gb300/csrc/conv_kernel.cuh",
                   "transposed_conv_implicit_gb300/csrc/conv_api.cu",
                   "transposed_conv_implicit_gb300/csrc/conv_kernels.cu",
                   "transposed_conv_implicit_gb300/csrc/conv_kernels_gather.cu",
-                  "transposed_conv_implicit_gb300/csrc/conv_launch.cuh"]
+                  "transposed_conv_implicit_gb300/csrc/conv_launch.cuh",
+                  "transposed_conv_implicit_gb300/csrc/conv_direct.cu"]
 
 
 def kernel_source_hash() -> str:
@@ -91,6 +92,8 @@ def describe(cases):
         kind = "convT" if c.kind == "transposed" else "conv"
         s = "%s %s %dx%dx%dx%d -> %dx%dx%dx%d %dx%d s%d p%d" % (
             c.dtype, kind, c.N, c.H, c.W, c.C_in, c.N, c.Ho, c.Wo, c.C_out, c.R, c.S, c.stride, c.pad)
+        if c.groups > 1:
+            s += " groups=%d" % c.groups
         if c.has_residual:
             s += " +%.2g*src" % c.beta
         if c.epilogue != "none":
@@ -217,7 +220,7 @@ def _oracle_one(case, x, w, src):
                                       source=src, beta=case.beta, act=case.epilogue)
     return oracle.conv2d_fwd(x, w, filter_is_fcrs=case.filter_layout == "FCRS", stride=st,
                              padding=pd, dilation=case.dilations, source=src, beta=case.beta,
-                             act=case.epilogue)
+                             act=case.epilogue, groups=case.groups)
 
 
 def _oracle_points(case, x, w, src, pts):
@@ -229,7 +232,7 @@ def _oracle_points(case, x, w, src, pts):
                                              act=case.epilogue)
     return oracle.conv2d_fwd_points(x, w, pts, filter_is_fcrs=case.filter_layout == "FCRS",
                                     stride=st, padding=pd, dilation=case.dilations, source=src,
-                                    beta=case.beta, act=case.epilogue)
+                                    beta=case.beta, act=case.epilogue, groups=case.groups)
 
 
 # ----------------------------------------------------------------------------- distributed
@@ -355,6 +358,7 @@ def run_ours(args, world, rank, local):
                   beta=case.beta, epilogue=case.epilogue, workspace=workspace, stream=stream)
         if case.kind != "transposed":
             kw["dilation"] = case.dilations
+            kw["num_groups"] = case.groups
         if case.kind == "transposed":
             calls.append(cg.bind_conv_transposed_packed(x, pk, out, padding=pd, **kw))
         else:
@@ -542,6 +546,7 @@ def run_e2e(args, cases, inputs, dev, stream):
                       beta=case.beta, epilogue=case.epilogue, workspace=ws)
             if case.kind != "transposed":
                 kw["dilation"] = case.dilations
+                kw["num_groups"] = case.groups
             if case.kind == "transposed":
                 cg.conv_transposed_packed(dx, pk, o, padding=pd, **kw)
             else:

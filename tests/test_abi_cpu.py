@@ -101,8 +101,7 @@ def fwd(lib, *, inp=A, n=2, h=8, w=8, c=64, dt=BF16, flt=B, r=3, s=3, f=64, fcrs
     (dict(pad=(1, 3)), NOTSUP),                               # pad beyond the filter extent - 1
     (dict(pad=(3, 3)), NOTSUP),
     (dict(r=1, s=1, pad=(1, 1)), NOTSUP),
-    (dict(groups=64), NOTSUP),                                # depthwise: 2-byte channel groups
-    (dict(groups=8), NOTSUP),                                 # 16-byte channel groups
+    (dict(c=60, f=60, groups=4, r=8, s=8, h=16, w=16), NOTSUP),  # direct kernel's filter slice > 200 KB
     (dict(groups=3), INVALID),                                # 64 channels do not split in 3
     (dict(groups=0), INVALID),
     (dict(dt=F8, odt=F8), NOTSUP),                            # fp8 must write bf16

@@ -120,6 +120,17 @@ SMALL_FWD = [
     _fwd("e_groups8", "f8e4m3", 1, 10, 10, 256, 64, 3, 1, 1, groups=8, epi="relu"),
     _fwd("b_groups2_fg3_direct", "bf16", 1, 9, 9, 64, 6, 3, 1, 1, groups=2),
     _fwd("b_groups32_1x1", "bf16", 2, 8, 8, 1024, 512, 1, 1, 0, groups=32, epi="silu"),
+    # Narrow groups on the direct CUDA-core kernel: depthwise (vector path),
+    # channel multipliers, groups of 4 and 40 channels, both filter layouts.
+    _fwd("b_depthwise_3x3", "bf16", 2, 12, 12, 64, 64, 3, 1, 1, groups=64),
+    _fwd("b_depthwise_s2_res_relu", "bf16", 2, 13, 11, 128, 128, 3, 2, 1, groups=128, res=True,
+         beta=0.5, epi="relu", layout="FCRS"),
+    _fwd("h_depthwise_mult2", "f16", 1, 10, 10, 32, 64, 3, 1, 1, groups=32),
+    _fwd("b_groups16_cg4", "bf16", 2, 9, 9, 64, 64, 3, 1, 1, groups=16, layout="FCRS"),
+    _fwd("e_depthwise_5x5", "f8e4m3", 1, 12, 12, 64, 64, 5, 1, 2, groups=64, epi="silu"),
+    _fwd("b_depthwise_7x7_dil2", "bf16", 1, 20, 20, 32, 32, 7, 1, 6, groups=32, dil=2),
+    _fwd("b_groups2_cg40_flat", "bf16", 1, 9, 9, 80, 48, 3, 1, 1, groups=2),
+    _fwd("b_depthwise_c3", "bf16", 2, 9, 9, 3, 3, 3, 1, 1, groups=3),
 ]
 
 SMALL_TR = [
@@ -149,7 +160,8 @@ def test_small_case_every_element(case):
 
 @pytest.mark.parametrize("case", [c for c in SMALL_FWD + SMALL_TR if c.name in (
     "b_3x3_s2p1", "b_cout17_res", "e_3x3_s1p1_res", "t_h_4x4_s2p1_relu", "t_b_3x3_s2p1_op1",
-    "b_gather_c3_7x7_s2p3", "e_gather_c3_5x5", "b_groups4_fg24_res", "h_groups2_s2_fcrs")],
+    "b_gather_c3_7x7_s2p3", "e_gather_c3_5x5", "b_groups4_fg24_res", "h_groups2_s2_fcrs", "b_depthwise_s2_res_relu",
+    "b_groups16_cg4")],
     ids=lambda c: c.name)
 def test_unpacked_entry_point_equals_packed(case):
     """conv2d_fwd / conv_transposed pack in the workspace; the result must be
@@ -180,6 +192,7 @@ INT_CASES = [
     _int_case("int_e_gather_c5", "fwd", "f8e4m3", 1, 9, 9, 5, 32, 3, 1, 1),
     _int_case("int_h_dil2", "fwd", "f16", 1, 12, 12, 16, 16, 3, 1, 2, dil=2),
     _int_case("int_b_groups4", "fwd", "bf16", 1, 10, 10, 64, 32, 3, 1, 1, groups=4),
+    _int_case("int_h_depthwise", "fwd", "f16", 2, 9, 9, 32, 32, 3, 1, 1, groups=32),
 ]
 
 

@@ -215,6 +215,16 @@ size_t gather_smem_bytes(ConvKernelParams& kp) {
   return align1k(tables) + 2 * static_cast<size_t>(kp.g_stage_bytes);
 }
 
+// Grouped convs run on the tensor cores (TMA im2col loader) when a group's
+// input channels are whole channel blocks of TMA rows, so that no load
+// reaches into the next group; otherwise on the direct CUDA-core kernel.
+bool groups_on_tensor_cores(int c_group, int elt) {
+  int bk = 0;
+  uint32_t rb = 0;
+  return !gather_mode(c_group, elt) && channel_block(c_group, elt, &bk, &rb) == CONV_OK &&
+         c_group % bk == 0;
+}
+
 long long gather_run_bytes(int s, int c_in, int elt) {
   return ((static_cast<long long>(s) * c_in * elt + 15) / 16) * 16;
 }
@@ -391,20 +401,14 @@ conv_status_t check_fwd_shape(const FwdShape& f, int num_groups) {
     return CONV_ERR_NOT_SUPPORTED;
   if (num_groups < 1 || f.c_in % num_groups != 0 || f.c_out % num_groups != 0)
     return CONV_ERR_INVALID_VALUE;
-  if (num_groups > 1) {
-    // Grouped convs run on the TMA im2col loader: a group's input channels
-    // must be whole channel blocks of TMA rows, so that no load reaches into
-    // the next group.
-    const int cg = f.c_in / num_groups;
-    int bk = 0;
-    uint32_t rb = 0;
-    if (gather_mode(cg, elt_bytes(f.in_dtype)) ||
-        channel_block(cg, elt_bytes(f.in_dtype), &bk, &rb) != CONV_OK || cg % bk != 0)
-      return CONV_ERR_NOT_SUPPORTED;
-  }
+  // Narrow channel groups run on the direct kernel, whose filter slice must
+  // fit in shared memory.
+  if (num_groups > 1 && !groups_on_tensor_cores(f.c_in / num_groups, elt_bytes(f.in_dtype)) &&
+      direct_smem_bytes(f.r, f.s, f.c_in / num_groups) > 200 * 1024)
+    return CONV_ERR_NOT_SUPPORTED;
   // The gather loader reads S adjacent pixels per filter row and indexes
   // input pixels with 32-bit integers.
-  if (gather_mode(f.c_in, elt_bytes(f.in_dtype)) &&
+  if (num_groups == 1 && gather_mode(f.c_in, elt_bytes(f.in_dtype)) &&
       (f.dil_w != 1 || static_cast<long long>(f.n) * f.h * f.w >= (1ll << 30)))
     return CONV_ERR_NOT_SUPPORTED;
   if (f.r > kMaxFilterExtent || f.s > kMaxFilterExtent) return CONV_ERR_NOT_SUPPORTED;
@@ -1268,6 +1272,39 @@ conv_status_t fwd_impl(const void* input, const FwdShape& shape, const void* fil
   if (workspace_bytes < need) return CONV_ERR_WORKSPACE_TOO_SMALL;
   const int sms = device_sm_count();
   if (sms <= 0) return CONV_ERR_CUDA;
+  if (num_groups > 1 && !groups_on_tensor_cores(cg, elt_bytes(f.in_dtype))) {
+    const void* packed = filter;
+    if (!prepacked) {
+      void* dst = static_cast<uint8_t*>(workspace) + CONV_STATUS_BYTES;
+      st = launch_pack_fwd(filter, f.r, f.s, cg, f.c_out, fcrs, f.in_dtype, dst, stream);
+      if (st != CONV_OK) return st;
+      packed = dst;
+    }
+    const int elt = elt_bytes(f.in_dtype);
+    DirectParams dp{};
+    dp.x = input;
+    dp.w = packed;
+    dp.src = has_residual ? source : nullptr;
+    dp.y = output;
+    dp.N = f.n; dp.H = f.h; dp.W = f.w; dp.C = f.c_in; dp.Ho = f.ho; dp.Wo = f.wo;
+    dp.F = f.c_out; dp.R = f.r; dp.S = f.s;
+    dp.c_group = cg;
+    dp.f_group = f.c_out / num_groups;
+    dp.stride_h = f.stride_h; dp.stride_w = f.stride_w;
+    dp.pad_h = f.pad_h; dp.pad_w = f.pad_w;
+    dp.dil_h = f.dil_h; dp.dil_w = f.dil_w;
+    dp.w_runs = gather_mode(cg, elt) ? 1 : 0;
+    dp.run_elems = static_cast<int>(gather_run_bytes(f.s, cg, elt) / elt);
+    dp.kdim = static_cast<int>(fwd_packed_k(f.r, f.s, cg, elt));
+    dp.has_residual = has_residual ? 1 : 0;
+    dp.epilogue = static_cast<int>(epilogue);
+    dp.beta = has_residual ? beta : 0.0f;
+    dp.div_wo = make_fast_div(static_cast<uint32_t>(f.wo));
+    dp.div_ho = make_fast_div(static_cast<uint32_t>(f.ho));
+    cudaError_t e = launch_conv_direct(static_cast<int>(f.in_dtype), f.in_dtype != CONV_DTYPE_F16,
+                                       dp, sms, stream);
+    return e == cudaSuccess ? CONV_OK : CONV_ERR_CUDA;
+  }
   Plan pl;
   st = plan_fwd(f, &pl, sms, has_residual);
   if (st != CONV_OK) return st;

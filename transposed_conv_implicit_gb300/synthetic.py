@@ -185,6 +185,9 @@ WORKLOADS = {
     # RGB stem: 3 input channels (6-byte pixels) need the gather A loader.
     "stem_c3_bf16": ConvCase("stem_c3_bf16", "fwd", "bf16", 32, 224, 224, 3, 64, 7, 7, 2, 3, "RSCF",
                              _n(1.0), _n(2.0 / (49 * 3)), seed=1020, epilogue="relu"),
+    # Depthwise 3x3 (one channel per group): the direct CUDA-core kernel.
+    "dw_bf16": ConvCase("dw_bf16", "fwd", "bf16", 32, 112, 112, 64, 64, 3, 3, 1, 1, "RSCF",
+                        _n(1.0), _n(2.0 / 9), seed=1021, epilogue="relu", groups=64),
 }
 
 # The ResNet-style block: the stride-1 residual conv and the stride-2 downsample.
