@@ -49,7 +49,10 @@ conv_status_t conv_testing_im2col_tile(const void* input, int n, int h, int w, i
  * TMEM columns, out[7] = epilogue mode (0 direct stores, 1 TMA 2-D, 2 TMA
  * phase grid, 3 TMA row window), out[8] = filter resident in shared memory,
  * out[9] = residual source buffers, out[10] = output staging buffers,
- * out[11] = A loader (0 TMA im2col, 1 row window, 2 gather).  Host-only. */
+ * out[11] = A loader (0 TMA im2col, 1 row window, 2 gather, 3 row-tap).  For
+ * the row-tap kernel (few output channels: the filter taps along S and the
+ * output channels share the MMA's N) out[0] = R * g16 (MMA width), out[10] =
+ * output rows per tile.  Host-only. */
 conv_status_t conv_testing_fwd_plan(int n, int h, int w, int c_in, conv_dtype_t dtype, int r,
                                     int s, int c_out, const int stride[2],
                                     const int symmetric_padding[2], int has_residual, int num_sms,

@@ -174,13 +174,31 @@ def test_tile_plans_for_the_workloads(lib):
     assert (p["bn"], p["tiles"], p["epi"], p["bres"]) == (128, 98, 1, 0) and p["stages"] >= 4
     p = _plan(lib, 16, 64, 64, 320, F8, 3, 320, 1, 1, res=1, sms=152)    # fp8: 2 x 160 columns,
     assert (p["bn"], p["bk"], p["tiles"], p["tmem"], p["epi"]) == (160, 128, 1024, 512, 1)  # 128-ch blocks
-    p = _plan(lib, 1, 512, 512, 128, BF16, 3, 3, 1, 1, sms=152)          # C_out = 3: masked 16-wide tile
-    assert (p["bn"], p["bk"], p["tiles"], p["epi"], p["bres"]) == (16, 64, 1024, 0, 1)
+    p = _plan(lib, 1, 512, 512, 128, BF16, 3, 3, 1, 1, sms=152)          # C_out = 3: row-tap kernel,
+    assert (p["loader"], p["bn"], p["bk"], p["stgb"]) == (3, 48, 64, 9)  # N = 3 rows x 16, bands of 9
+    assert p["tiles"] == 5 * 57 and p["grid"] == 152 and p["tmem"] == 512   # 5 segments x 57 bands
     p = _plan(lib, 1, 16, 16, 16, BF16, 3, 16, 1, 1, sms=152)            # 32-byte channel rows
     assert (p["bn"], p["bk"], p["grid"]) == (16, 16, p["tiles"])
     for args in [(1, 256, 256, 512, BF16, 3, 512, 1, 1), (8, 128, 128, 128, F16, 5, 128, 2, 2)]:
         q = _plan(lib, *args, sms=152)
         assert q["smem"] <= 227 * 1024 and q["stages"] >= 3 and q["tmem"] <= 512
+
+
+def test_row_tap_gate(lib, monkeypatch):
+    """Few output channels (S * C_out <= 32), stride 1, dilation 1, 128-byte
+    channel blocks and more than one tap take the row-tap kernel; the rest,
+    or CONV_ROWTAP=-1, the implicit GEMM's masked edge tile."""
+    assert _plan(lib, 1, 40, 40, 64, BF16, 3, 10, 1, 1)["loader"] == 3      # S * C_out = 30
+    assert _plan(lib, 1, 40, 40, 128, F8, 3, 8, 1, 1)["loader"] == 3        # fp8: 128 channels
+    q = _plan(lib, 1, 40, 40, 64, BF16, 3, 8, 1, 1)                          # g16 = 32: N = 96,
+    assert (q["loader"], q["bn"]) == (3, 96) and q["stgb"] <= 4              # bands of <= 4 rows
+    assert _plan(lib, 1, 40, 40, 64, BF16, 3, 11, 1, 1)["loader"] != 3      # S * C_out = 33
+    assert _plan(lib, 1, 40, 40, 64, BF16, 3, 3, 2, 1)["loader"] != 3       # stride 2
+    assert _plan(lib, 1, 40, 40, 32, BF16, 3, 3, 1, 1)["loader"] != 3       # 64-byte channel rows
+    assert _plan(lib, 1, 40, 40, 64, BF16, 1, 3, 1, 0)["loader"] != 3       # a single tap
+    monkeypatch.setenv("CONV_ROWTAP", "-1")
+    p = _plan(lib, 1, 512, 512, 128, BF16, 3, 3, 1, 1, sms=152)              # masked 16-wide tile
+    assert (p["loader"], p["bn"], p["bk"], p["tiles"], p["epi"], p["bres"]) == (0, 16, 64, 1024, 0, 1)
 
 
 def test_binding_raises_without_library(monkeypatch, tmp_path):

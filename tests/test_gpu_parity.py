@@ -131,6 +131,19 @@ SMALL_FWD = [
     _fwd("b_depthwise_7x7_dil2", "bf16", 1, 20, 20, 32, 32, 7, 1, 6, groups=32, dil=2),
     _fwd("b_groups2_cg40_flat", "bf16", 1, 9, 9, 80, 48, 3, 1, 1, groups=2),
     _fwd("b_depthwise_c3", "bf16", 2, 9, 9, 3, 3, 3, 1, 1, groups=3),
+    # Row-tap kernel (few output channels, stride 1): two or more 126-pixel
+    # segments with a ragged last one, short last bands, g16 = 16 and 32,
+    # R = 1, 3 and 5, S = 1 and 3, padding 0..2, several channel blocks.
+    _fwd("rt_b_w150_res_silu", "bf16", 2, 13, 150, 64, 3, 3, 1, 1, res=True, beta=0.5, epi="silu"),
+    _fwd("rt_h_cout1_w20", "f16", 1, 9, 20, 128, 1, 3, 1, 1, layout="FCRS"),
+    _fwd("rt_e_cout5", "f8e4m3", 2, 10, 40, 128, 5, 3, 1, 1, epi="relu"),
+    _fwd("rt_b_cout8_g32", "bf16", 1, 11, 30, 64, 8, 3, 1, 1, res=True, beta=-1.0),
+    _fwd("rt_b_5x5_p2_cout3", "bf16", 1, 12, 140, 64, 3, 5, 1, 2, epi="relu"),
+    _fwd("rt_b_3x3_p0_cout2", "bf16", 2, 9, 12, 128, 2, 3, 1, 0),
+    _fwd("rt_h_1x3_cout4", "f16", 1, 6, 133, 64, 4, 1, 1, 0, S=3, pad_w=1),
+    _fwd("rt_b_3x1_cout10", "bf16", 1, 14, 17, 64, 10, 3, 1, 1, S=1, pad_w=0, layout="FCRS"),
+    _fwd("rt_b_cin256_cout3", "bf16", 1, 8, 8, 256, 3, 3, 1, 1),
+    _fwd("rt_e_cout10_g32", "f8e4m3", 1, 9, 27, 256, 10, 3, 1, 1, res=True, beta=0.5),
 ]
 
 SMALL_TR = [
@@ -158,10 +171,23 @@ def test_small_case_every_element(case):
     H.assert_parity(case, inp, got, ref)
 
 
+@pytest.mark.parametrize("case", [c for c in SMALL_FWD if c.name in (
+    "b_cout1", "b_cout3_head", "e_cout3", "rt_b_cout8_g32", "rt_h_1x3_cout4")],
+    ids=lambda c: c.name)
+def test_masked_edge_tile_without_row_tap(case, monkeypatch):
+    """The same small-C_out convs on the implicit GEMM's masked edge tile (the
+    row-tap kernel switched off)."""
+    monkeypatch.setenv("CONV_ROWTAP", "-1")
+    inp = synthetic.make_inputs(case)
+    out = H.run_gpu(case, inp)
+    torch.cuda.synchronize()
+    H.assert_parity(case, inp, H.decode(out.cpu(), case.out_dtype), H.oracle_full(case, inp))
+
+
 @pytest.mark.parametrize("case", [c for c in SMALL_FWD + SMALL_TR if c.name in (
     "b_3x3_s2p1", "b_cout17_res", "e_3x3_s1p1_res", "t_h_4x4_s2p1_relu", "t_b_3x3_s2p1_op1",
     "b_gather_c3_7x7_s2p3", "e_gather_c3_5x5", "b_groups4_fg24_res", "h_groups2_s2_fcrs", "b_depthwise_s2_res_relu",
-    "b_groups16_cg4")],
+    "b_groups16_cg4", "rt_b_w150_res_silu", "rt_e_cout5")],
     ids=lambda c: c.name)
 def test_unpacked_entry_point_equals_packed(case):
     """conv2d_fwd / conv_transposed pack in the workspace; the result must be
@@ -193,6 +219,8 @@ INT_CASES = [
     _int_case("int_h_dil2", "fwd", "f16", 1, 12, 12, 16, 16, 3, 1, 2, dil=2),
     _int_case("int_b_groups4", "fwd", "bf16", 1, 10, 10, 64, 32, 3, 1, 1, groups=4),
     _int_case("int_h_depthwise", "fwd", "f16", 2, 9, 9, 32, 32, 3, 1, 1, groups=32),
+    _int_case("int_b_rowtap", "fwd", "bf16", 1, 12, 140, 64, 3, 3, 1, 1),
+    _int_case("int_e_rowtap_g32", "fwd", "f8e4m3", 1, 9, 30, 128, 9, 3, 1, 1),
 ]
 
 

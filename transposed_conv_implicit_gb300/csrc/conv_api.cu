@@ -1212,6 +1212,133 @@ conv_status_t finish_and_launch(Plan* pl, int n_images, const void* packed, void
   return e == cudaSuccess ? CONV_OK : CONV_ERR_CUDA;
 }
 
+// ------------------------------------------------------------------ row-tap path
+// Forward convs with few output channels (S * C_out <= 32): the filter taps
+// along S and the output channels share the MMA's N dimension, each input row
+// segment is loaded and multiplied once, and the R filter rows accumulate into
+// R output rows in tensor memory (conv_rowtap.cu).  Gate: one channel group,
+// stride 1, dilation 1, a filter of more than one tap, 128-byte channel
+// blocks (C_in * elt a multiple of 128), R * g16 <= 256 columns and a band of
+// at least one row.  CONV_ROWTAP=-1 disables it.
+struct RowTapPlan {
+  RowTapParams rp;
+  int grid;
+  size_t smem_bytes;
+};
+
+bool plan_rowtap(const FwdShape& f, int groups, int num_sms, RowTapPlan* out) {
+  if (env_int("CONV_ROWTAP") == -1) return false;
+  if (groups != 1 || f.stride_h != 1 || f.stride_w != 1 || f.dil_h != 1 || f.dil_w != 1)
+    return false;
+  if (f.r * f.s < 2) return false;
+  const int elt = elt_bytes(f.in_dtype);
+  if ((static_cast<long long>(f.c_in) * elt) % 128 != 0) return false;
+  const int sf = f.s * f.c_out;
+  if (sf > 32) return false;
+  const int g16 = sf <= 16 ? 16 : 32;
+  if (f.r * g16 > 256) return false;
+  // Columns per accumulator buffer: g16 * (band + 2R - 2) <= 256 (two buffers).
+  const int band_max = std::min(kRowTapMaxBand, 256 / g16 - 2 * f.r + 2);
+  if (band_max < 1) return false;
+  const int seg_w = 128 - (f.s - 1);
+  const int n_seg = (f.wo + seg_w - 1) / seg_w;
+  // Band height: the fewest input-row loads on the busiest SM (each tile
+  // loads band + R - 1 rows); ties go to the taller band.
+  int best = 1;
+  long long best_cost = -1;
+  for (int b = 1; b <= band_max; ++b) {
+    const long long tiles = static_cast<long long>(f.n) * ((f.ho + b - 1) / b) * n_seg;
+    const long long waves = (tiles + num_sms - 1) / num_sms;
+    const long long cost = waves * (b + f.r - 1);
+    if (best_cost < 0 || cost <= best_cost) {
+      best_cost = cost;
+      best = b;
+    }
+  }
+  const int n_band = (f.ho + best - 1) / best;
+  const long long tiles = static_cast<long long>(f.n) * n_band * n_seg;
+  if (tiles >= (1ll << 31)) return false;
+  std::memset(out, 0, sizeof(*out));
+  RowTapParams& rp = out->rp;
+  rp.N = f.n; rp.H = f.h; rp.W = f.w; rp.Ho = f.ho; rp.Wo = f.wo;
+  rp.F = f.c_out; rp.R = f.r; rp.S = f.s;
+  rp.pad_h = f.pad_h; rp.pad_w = f.pad_w;
+  rp.c_blocks = static_cast<int>((static_cast<long long>(f.c_in) * elt) / 128);
+  rp.g16 = g16;
+  rp.band = best;
+  rp.seg_w = seg_w;
+  rp.n_seg = n_seg;
+  rp.n_band = n_band;
+  rp.total_tiles = static_cast<int>(tiles);
+  rp.idesc_all = make_idesc(f.in_dtype, f.r * g16);
+  rp.idesc_one = make_idesc(f.in_dtype, g16);
+  rp.idesc_rest = make_idesc(f.in_dtype, std::max(f.r - 1, 1) * g16);
+  rp.cols_per_buf = static_cast<uint32_t>(g16 * (best + 2 * f.r - 2));
+  rp.tmem_cols = next_pow2_cols(static_cast<int>(2 * rp.cols_per_buf));
+  // Shared memory: the A ring at 0, the resident filter, the epilogue's
+  // exchange buffers (two groups x two rows), the barriers.
+  const size_t stage_bytes = 128 * 128;
+  const size_t b_bytes = static_cast<size_t>(rp.c_blocks) * f.r * g16 * 128;
+  const size_t part_bytes = static_cast<size_t>(2 * 2) * g16 * 128 * sizeof(float);
+  const size_t fixed = 1024 + align1k(b_bytes) + align1k(part_bytes) + 1024;
+  if (fixed + 2 * stage_bytes > kSmemLimit) return false;
+  rp.stages = static_cast<int>(std::min<size_t>(kMaxStages, (kSmemLimit - fixed) / stage_bytes));
+  rp.off_b = static_cast<uint32_t>(rp.stages * stage_bytes);
+  rp.off_part = rp.off_b + align1k(b_bytes);
+  rp.off_bar = rp.off_part + align1k(part_bytes);
+  out->smem_bytes = 1024 + rp.off_bar + 1024;
+  out->grid = static_cast<int>(std::min<long long>(tiles, num_sms));
+  return true;
+}
+
+conv_status_t launch_rowtap_path(RowTapPlan* pl, const FwdShape& f, const void* input,
+                                 const void* packed, void* output, int has_residual,
+                                 const void* source, float beta, conv_epilogue_t epilogue,
+                                 void* workspace, cudaStream_t stream) {
+  const DriverFns* fns = driver_fns();
+  if (!fns) return CONV_ERR_CUDA;
+  RowTapParams& rp = pl->rp;
+  const cuuint64_t e = static_cast<cuuint64_t>(elt_bytes(f.in_dtype));
+  const cuuint32_t bk = static_cast<cuuint32_t>(128 / e);
+  {
+    cuuint64_t dims[4] = {static_cast<cuuint64_t>(f.c_in), static_cast<cuuint64_t>(f.w),
+                          static_cast<cuuint64_t>(f.h), static_cast<cuuint64_t>(f.n)};
+    cuuint64_t strides[3] = {dims[0] * e, dims[0] * dims[1] * e, dims[0] * dims[1] * dims[2] * e};
+    cuuint32_t box[4] = {bk, 128, 1, 1};
+    cuuint32_t estr[4] = {1, 1, 1, 1};
+    if (fns->tiled(&rp.map_x, tmap_dtype(f.in_dtype), 4, const_cast<void*>(input), dims, strides,
+                   box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return CONV_ERR_CUDA;
+  }
+  {
+    // The packed filter [F][(r*S + s)*C_in + c] seen as {C_in, S, R, F}.
+    cuuint64_t dims[4] = {static_cast<cuuint64_t>(f.c_in), static_cast<cuuint64_t>(f.s),
+                          static_cast<cuuint64_t>(f.r), static_cast<cuuint64_t>(f.c_out)};
+    cuuint64_t strides[3] = {dims[0] * e, dims[0] * dims[1] * e, dims[0] * dims[1] * dims[2] * e};
+    cuuint32_t box[4] = {bk, static_cast<cuuint32_t>(f.s), 1, static_cast<cuuint32_t>(f.c_out)};
+    cuuint32_t estr[4] = {1, 1, 1, 1};
+    if (fns->tiled(&rp.map_w, tmap_dtype(f.in_dtype), 4, const_cast<void*>(packed), dims,
+                   strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return CONV_ERR_CUDA;
+  }
+  rp.has_residual = has_residual ? 1 : 0;
+  rp.src = has_residual ? source : nullptr;
+  rp.beta = has_residual ? beta : 0.0f;
+  rp.epilogue = static_cast<int>(epilogue);
+  rp.out = output;
+  rp.status = static_cast<unsigned int*>(workspace);
+  const unsigned long long tmo = g_timeout_ns.load(std::memory_order_relaxed);
+  rp.timeout_cycles = ns_to_cycles(tmo ? tmo : kDefaultTimeoutNs);
+  if (rp.total_tiles == 0) return CONV_OK;
+  cudaError_t err = launch_conv_rowtap(static_cast<int>(f.in_dtype), f.in_dtype != CONV_DTYPE_F16,
+                                       rp, pl->grid, pl->smem_bytes, stream);
+  return err == cudaSuccess ? CONV_OK : CONV_ERR_CUDA;
+}
+
 bool epilogue_ok(conv_epilogue_t e) {
   return e == CONV_EPI_NONE || e == CONV_EPI_RELU || e == CONV_EPI_SILU;
 }
@@ -1304,6 +1431,18 @@ conv_status_t fwd_impl(const void* input, const FwdShape& shape, const void* fil
     cudaError_t e = launch_conv_direct(static_cast<int>(f.in_dtype), f.in_dtype != CONV_DTYPE_F16,
                                        dp, sms, stream);
     return e == cudaSuccess ? CONV_OK : CONV_ERR_CUDA;
+  }
+  RowTapPlan rt;
+  if (plan_rowtap(f, num_groups, sms, &rt)) {
+    const void* packed = filter;
+    if (!prepacked) {
+      void* dst = static_cast<uint8_t*>(workspace) + CONV_STATUS_BYTES;
+      st = launch_pack_fwd(filter, f.r, f.s, cg, f.c_out, fcrs, f.in_dtype, dst, stream);
+      if (st != CONV_OK) return st;
+      packed = dst;
+    }
+    return launch_rowtap_path(&rt, f, input, packed, output, has_residual, source, beta, epilogue,
+                              workspace, stream);
   }
   Plan pl;
   st = plan_fwd(f, &pl, sms, has_residual);
@@ -1613,6 +1752,23 @@ conv_status_t conv_testing_fwd_plan(int n, int h, int w, int c_in, conv_dtype_t 
                                     symmetric_padding);
   conv_status_t st = check_fwd_shape(f, 1);
   if (st != CONV_OK) return st;
+  RowTapPlan rt;
+  if (plan_rowtap(f, 1, num_sms, &rt)) {
+    const RowTapParams& rp = rt.rp;
+    out[0] = rp.R * rp.g16;
+    out[1] = 128 / elt_bytes(dtype);
+    out[2] = rp.stages;
+    out[3] = static_cast<int>(rt.smem_bytes);
+    out[4] = rp.total_tiles;
+    out[5] = rt.grid;
+    out[6] = static_cast<int>(rp.tmem_cols);
+    out[7] = 0;
+    out[8] = 1;
+    out[9] = 0;
+    out[10] = rp.band;
+    out[11] = 3;
+    return CONV_OK;
+  }
   Plan pl;
   st = plan_fwd(f, &pl, num_sms, has_residual);
   if (st != CONV_OK) return st;

@@ -35,6 +35,42 @@ size_t direct_smem_bytes(int r, int s, int c_group);
 cudaError_t launch_conv_direct(int in_dtype, bool out_bf16, const DirectParams& p, int num_sms,
                                cudaStream_t stream);
 
+// Row-tap kernel for forward convs with few output channels (S * C_out <= 32,
+// e.g. an RGB head): the filter taps along S and the output channels share
+// the MMA's N dimension, so each input-row segment is multiplied once by the
+// filter rows of all R taps and its products accumulate, in tensor memory,
+// into the R output rows it touches; the epilogue sums the S taps across
+// neighbouring pixels.  Stride 1, dilation 1, one channel group.
+constexpr int kRowTapMaxBand = 16;  // output rows per tile (upper bound)
+
+struct RowTapParams {  // aligned like CUtensorMap
+  CUtensorMap map_x;   // tiled {C_in, W, H, N}, box {bk, 128, 1, 1}, 128-B swizzle
+  CUtensorMap map_w;   // tiled {C_in, S, R, F} over the packed filter, box {bk, S, 1, F}
+  int N, H, W, Ho, Wo, F, R, S;
+  int pad_h, pad_w;
+  int c_blocks;        // 128-byte channel blocks of C_in (the last one zero-filled past C_in)
+  int g16;             // TMEM columns (B rows) per filter row r: S*F rounded up to 16
+  int band;            // output rows per tile
+  int seg_w;           // output columns per tile: 128 - (S - 1)
+  int n_seg, n_band, total_tiles;
+  int stages;
+  uint32_t idesc_all;  // N = R * g16
+  uint32_t idesc_one;  // N = g16
+  uint32_t idesc_rest; // N = (R - 1) * g16 (R > 1)
+  uint32_t cols_per_buf, tmem_cols;
+  uint32_t off_b, off_part, off_bar;  // shared-memory offsets (A ring at 0)
+  int has_residual, epilogue;
+  float beta;
+  const void* src;
+  void* out;
+  unsigned int* status;
+  long long timeout_cycles;
+};
+
+// Launches the row-tap kernel; in_dtype: 0 bf16, 1 f16, 2 e4m3 (bf16 out).
+cudaError_t launch_conv_rowtap(int in_dtype, bool out_bf16, const RowTapParams& p, int grid,
+                               size_t smem_bytes, cudaStream_t stream);
+
 // The gather-loader instances (their own translation unit).
 cudaError_t launch_conv_igemm_gather(int kind, bool out_bf16, const ConvKernelParams& p, int grid,
                                      size_t smem_bytes, cudaStream_t stream);
