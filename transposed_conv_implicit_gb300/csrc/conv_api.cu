@@ -1219,7 +1219,8 @@ conv_status_t finish_and_launch(Plan* pl, int n_images, const void* packed, void
 // R output rows in tensor memory (conv_rowtap.cu).  Gate: one channel group,
 // stride 1, dilation 1, a filter of more than one tap, 128-byte channel
 // blocks (C_in * elt a multiple of 128), R * g16 <= 256 columns and a band of
-// at least one row.  CONV_ROWTAP=-1 disables it.
+// at least one row.  CONV_ROWTAP=-1 disables it; CONV_ROWTAP_BAND sets the
+// band height (output rows per tile, capped by the TMEM columns).
 struct RowTapPlan {
   RowTapParams rp;
   int grid;
@@ -1255,6 +1256,8 @@ bool plan_rowtap(const FwdShape& f, int groups, int num_sms, RowTapPlan* out) {
       best = b;
     }
   }
+  const int band_env = env_int("CONV_ROWTAP_BAND");  // tuning override: output rows per tile
+  if (band_env > 0) best = std::min(band_env, band_max);
   const int n_band = (f.ho + best - 1) / best;
   const long long tiles = static_cast<long long>(f.n) * n_band * n_seg;
   if (tiles >= (1ll << 31)) return false;
