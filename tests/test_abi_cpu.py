@@ -156,11 +156,11 @@ def test_pack_validation(lib):
 
 
 def _plan(lib, n, h, w, c, dt, r, f, st, pd, res=0, sms=148):
-    out = (ctypes.c_int * 12)()
+    out = (ctypes.c_int * 13)()
     assert lib.conv_testing_fwd_plan(n, h, w, c, dt, r, r, f, _lib.pair((st, st)), _lib.pair((pd, pd)),
                                      res, sms, out) == OK
     keys = ("bn", "bk", "stages", "smem", "tiles", "grid", "tmem", "epi", "bres", "srcb", "stgb",
-            "loader")
+            "loader", "pair")
     return dict(zip(keys, list(out)))
 
 
@@ -173,7 +173,8 @@ def test_tile_plans_for_the_workloads(lib):
     p = _plan(lib, 32, 56, 56, 64, BF16, 3, 128, 2, 1, sms=152)          # downsample: 147 KB filter
     assert (p["bn"], p["tiles"], p["epi"], p["bres"]) == (128, 98, 1, 0) and p["stages"] >= 4
     p = _plan(lib, 16, 64, 64, 320, F8, 3, 320, 1, 1, res=1, sms=152)    # fp8: 2 x 160 columns,
-    assert (p["bn"], p["bk"], p["tiles"], p["tmem"], p["epi"]) == (160, 128, 1024, 512, 1)  # 128-ch blocks
+    assert (p["bn"], p["bk"], p["tmem"], p["epi"]) == (160, 128, 512, 1)  # 128-ch blocks, CTA pairs
+    assert (p["pair"], p["tiles"], p["grid"]) == (1, 512, 152)            # on 256-row tiles
     p = _plan(lib, 1, 512, 512, 128, BF16, 3, 3, 1, 1, sms=152)          # C_out = 3: row-tap kernel,
     assert (p["loader"], p["bn"], p["bk"], p["stgb"]) == (3, 48, 64, 9)  # N = 3 rows x 16, bands of 9
     assert p["tiles"] == 5 * 57 and p["grid"] == 152 and p["tmem"] == 512   # 5 segments x 57 bands
@@ -199,6 +200,27 @@ def test_row_tap_gate(lib, monkeypatch):
     monkeypatch.setenv("CONV_ROWTAP", "-1")
     p = _plan(lib, 1, 512, 512, 128, BF16, 3, 3, 1, 1, sms=152)              # masked 16-wide tile
     assert (p["loader"], p["bn"], p["bk"], p["tiles"], p["epi"], p["bres"]) == (0, 16, 64, 1024, 0, 1)
+
+
+def test_cta_pair_plans(lib, monkeypatch):
+    """CTA pairs (cta_group::2, 256-row tiles shared by two CTAs) when every
+    pair of SMs gets at least 4 tiles and bn >= 128; CONV_PAIR=1/0 force."""
+    monkeypatch.delenv("CONV_PAIR", raising=False)
+    vae = (1, 256, 256, 512, BF16, 3, 512, 1, 1)
+    p = _plan(lib, *vae, sms=152)
+    assert (p["pair"], p["bn"], p["tiles"], p["grid"], p["tmem"]) == (1, 256, 512, 152, 512)
+    f5 = (8, 128, 128, 128, 1, 5, 128, 2, 2)                     # 128 pair tiles < 4 x 76
+    assert _plan(lib, *f5, sms=152)["pair"] == 0
+    assert _plan(lib, *vae, sms=1000)["pair"] == 0              # too few tiles per pair
+    monkeypatch.setenv("CONV_PAIR", "1")
+    q = _plan(lib, *f5, sms=152)
+    assert (q["pair"], q["tiles"], q["grid"], q["tmem"]) == (1, 128, 152, 256)
+    assert _plan(lib, 3, 30, 30, 64, BF16, 3, 48, 2, 1, sms=5)["grid"] == 4  # even grid: 2 pairs
+    assert _plan(lib, 32, 56, 56, 64, BF16, 3, 64, 1, 1, res=1, sms=152)["pair"] == 0  # row window
+    assert _plan(lib, 32, 224, 224, 3, BF16, 7, 64, 2, 2, sms=152)["pair"] == 0       # gather
+    assert _plan(lib, 2, 9, 9, 64, BF16, 3, 16, 2, 1, sms=152)["pair"] == 0           # bn < 32
+    monkeypatch.setenv("CONV_PAIR", "0")
+    assert _plan(lib, *vae, sms=152)["pair"] == 0
 
 
 def test_binding_raises_without_library(monkeypatch, tmp_path):

@@ -239,6 +239,35 @@ def test_integer_inputs_bit_exact(case):
     assert mism.size == 0, mism[:5].tolist()
 
 
+PAIR_CASES = ("b_3x3_s2p1", "h_5x5_s2p2", "e_3x3_s1p1_res", "b_cout512_silu", "b_cout272",
+              "e_3x3_s2p1", "h_res_silu", "b_5x5_s2p2", "b_cout17_res", "b_cin80_partial_block",
+              "e_cin160_partial_block", "b_tiny_image", "b_1x1_s2p0", "t_h_4x4_s2p1_relu",
+              "t_b_3x3_s2p1_op1", "t_h_cout256_silu", "t_b_1x1_s2_zero_tap_phase",
+              "t_h_cin80_partial_block", "t_e_4x4_s2p1", "int_b_s2_res", "int_h_5x5", "int_h_tr",
+              "int_e_tr")
+
+
+def _pair_cases():
+    return [c for c in SMALL_FWD + SMALL_TR + INT_CASES if c.name in PAIR_CASES]
+
+
+@pytest.mark.parametrize("case", _pair_cases(), ids=lambda c: c.name)
+def test_cta_pair_every_element(case, monkeypatch):
+    """CTA pairs forced on (clusters of two CTAs, cta_group::2 MMAs over
+    256-row tiles): every element against the oracle; integer cases bit-exact."""
+    monkeypatch.setenv("CONV_PAIR", "1")
+    inp = synthetic.make_inputs(case)
+    out = H.run_gpu(case, inp)
+    torch.cuda.synchronize()
+    got = H.decode(out.cpu(), case.out_dtype)
+    ref = H.oracle_full(case, inp)
+    if case.name.startswith("int_"):
+        mism = np.argwhere(got != ref)
+        assert mism.size == 0, mism[:5].tolist()
+    else:
+        H.assert_parity(case, inp, got, ref)
+
+
 @pytest.mark.parametrize("name", list(WORKLOADS), ids=str)
 def test_full_size_workload_sampled(name):
     """Full-size workloads, sampled outputs checked against the oracle point by

@@ -19,7 +19,8 @@ CSRC = os.path.join(HERE, "csrc")
 ROOT = os.path.dirname(HERE)
 BUILD_DIR = os.path.join(HERE, "_build")
 LIB_PATH = os.path.join(HERE, "libconvgb300.so")
-SOURCES = ["conv_api.cu", "conv_kernels.cu", "conv_kernels_gather.cu", "conv_direct.cu",
+SOURCES = ["conv_api.cu", "conv_kernels.cu", "conv_kernels_gather.cu", "conv_kernels_pair.cu",
+           "conv_direct.cu",
            "conv_rowtap.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 

@@ -235,7 +235,7 @@ long long fwd_packed_k(int r, int s, int c_in, int elt) {
   return static_cast<long long>(r) * s * c_in;
 }
 
-uint32_t make_idesc(conv_dtype_t in, int bn) {
+uint32_t make_idesc(conv_dtype_t in, int bn, int m = kBM) {
   // kind::f16: A/B format 0 = fp16, 1 = bf16; kind::f8f6f4: 0 = e4m3.
   // D format (bits 4-5) 1 = fp32; both operands K-major (bits 15, 16 = 0);
   // N >> 3 in bits 17-22; M >> 4 in bits 24-28.
@@ -245,7 +245,7 @@ uint32_t make_idesc(conv_dtype_t in, int bn) {
   d |= fmt << 7;
   d |= fmt << 10;
   d |= (static_cast<uint32_t>(bn) >> 3) << 17;
-  d |= (static_cast<uint32_t>(kBM) >> 4) << 24;
+  d |= (static_cast<uint32_t>(m) >> 4) << 24;
   return d;
 }
 
@@ -377,6 +377,41 @@ void choose_tiling(Plan* pl, const long long rows[], int num_phases, int max_kbl
   kp.acc_stride = static_cast<uint32_t>(best_mh * best_bn);
   kp.tmem_cols = next_pow2_cols(2 * best_mh * best_bn);
   kp.idesc = make_idesc(pl->in_dtype, best_bn);
+}
+
+// CTA pairs (cta_group::2): a cluster of two CTAs shares each 256-row tile;
+// each CTA loads its 128 rows of A and half of the tile's bn filter rows, so
+// per SM the filter bytes written into shared memory halve (measured: the
+// VAE 3x3 512->512 conv 194.6 -> 181.3 us).  Pairs halve the number of tile
+// slots, so they pay only with many tiles: the default takes them when every
+// pair gets at least 4 tiles and bn >= 128 (the fp8 3x3 320->320 conv ran
+// equally fast either way; convs with under two waves of 256-row tiles ran
+// 12-30% slower).  For the TMA im2col loader with a streamed filter and one
+// channel group.  CONV_PAIR=1 forces pairs where they apply, 0 forbids them.
+void plan_pair(Plan* pl, int num_sms) {
+  ConvKernelParams& kp = pl->kp;
+  kp.pair = 0;
+  const int force = std::getenv("CONV_PAIR") ? env_int("CONV_PAIR") : -1;
+  if (force == 0) return;
+  if (kp.window || kp.gather || kp.groups > 1 || kp.bn < 32) return;
+  const int tile_m = 2 * kBM;
+  int tile = 0;
+  for (int ph = 0; ph < kp.num_phases; ++ph)
+    tile += ((kp.rows[ph] + tile_m - 1) / tile_m) * kp.n_tiles;
+  if (force != 1 && (kp.bn < 128 || tile < 4 * std::max(num_sms / 2, 1))) return;
+  kp.pair = 1;
+  kp.m_halves = 1;
+  tile = 0;
+  for (int ph = 0; ph < kp.num_phases; ++ph) {
+    kp.tile_start[ph] = tile;
+    tile += ((kp.rows[ph] + tile_m - 1) / tile_m) * kp.n_tiles;
+  }
+  kp.tile_start[kp.num_phases] = tile;
+  kp.total_tiles = tile;
+  kp.tiles_per_group = tile;
+  kp.acc_stride = static_cast<uint32_t>(kp.bn);
+  kp.tmem_cols = next_pow2_cols(2 * kp.bn);
+  kp.idesc = make_idesc(pl->in_dtype, kp.bn, 2 * kBM);
 }
 
 struct FwdShape {
@@ -562,6 +597,7 @@ conv_status_t plan_fwd(const FwdShape& f, Plan* pl, int num_sms, int has_residua
   pl->kmax = static_cast<int>(fwd_packed_k(f.r, f.s, cg, elt_bytes(f.in_dtype)));
   pl->packed_bytes = static_cast<size_t>(f.c_out) * pl->kmax * elt_bytes(f.in_dtype);
   if (!gather && groups == 1) plan_window_or_keep(f, pl, num_sms, has_residual);
+  plan_pair(pl, num_sms);
   return CONV_OK;
 }
 
@@ -703,6 +739,7 @@ conv_status_t plan_transposed(const TrShape& t, Plan* pl, int num_sms) {
   kp.Wo = t.wo;
   kp.Cout = t.c_out;
   kp.vec_ok = (t.c_out * 2) % 16 == 0;
+  plan_pair(pl, num_sms);
   pl->kmax = kmax;
   pl->packed_bytes = static_cast<size_t>(pl->phases_packed) * t.c_out * kmax * elt_bytes(t.in_dtype);
   return CONV_OK;
@@ -932,8 +969,9 @@ conv_status_t layout_memory(Plan* pl, int has_residual) {
   // Two epilogue warpgroups split a tile's (half, chunk) items: make at least two.
   if (kp.m_halves * (kp.bn / cw) < kEpilogueGroups && cw > 16) cw /= 2;
   const uint32_t a_bytes = kBM * kp.m_halves * kp.sw_bytes;
-  const uint32_t b_bytes = static_cast<uint32_t>(kp.bn) * kp.sw_bytes;
-  const bool can_res = kp.num_phases == 1 && kp.n_tiles == 1 && kp.groups <= 1 &&
+  // (A pair's CTA holds half of the tile's filter rows.)
+  const uint32_t b_bytes = static_cast<uint32_t>(kp.pair ? kp.bn / 2 : kp.bn) * kp.sw_bytes;
+  const bool can_res = !kp.pair && kp.num_phases == 1 && kp.n_tiles == 1 && kp.groups <= 1 &&
                        !(std::getenv("CONV_FILTER_RESIDENT") && env_int("CONV_FILTER_RESIDENT") == 0);
   const size_t bres = can_res ? static_cast<size_t>(kp.taps_h[0]) * kp.taps_w[0] * kp.c_blocks * b_bytes : 0;
   const size_t src_tile = static_cast<size_t>(kBM) * kp.m_halves * kp.bn * 2;
@@ -1115,7 +1153,7 @@ conv_status_t plan_memory(Plan* pl, int n_images, const void* output, const void
 conv_status_t plan_memory_direct(Plan* pl) {
   ConvKernelParams& kp = pl->kp;
   const uint32_t a_bytes = kBM * kp.m_halves * kp.sw_bytes;
-  const uint32_t b_bytes = static_cast<uint32_t>(kp.bn) * kp.sw_bytes;
+  const uint32_t b_bytes = static_cast<uint32_t>(kp.pair ? kp.bn / 2 : kp.bn) * kp.sw_bytes;
   const size_t bar_bytes = 1024 + gather_smem_bytes(kp);
   kp.epi_mode = 0;
   kp.cw = 16;
@@ -1123,7 +1161,7 @@ conv_status_t plan_memory_direct(Plan* pl) {
   kp.stg_bufs = 0;
   kp.src_chunk_bytes = 0;
   kp.valid_rows = kBM;
-  const bool can_res = kp.num_phases == 1 && kp.n_tiles == 1 && kp.groups <= 1;
+  const bool can_res = !kp.pair && kp.num_phases == 1 && kp.n_tiles == 1 && kp.groups <= 1;
   const size_t bres = can_res ? static_cast<size_t>(kp.taps_h[0]) * kp.taps_w[0] * kp.c_blocks * b_bytes : 0;
   bool res = false;
   int stages = 0;
@@ -1175,7 +1213,7 @@ conv_status_t finish_and_launch(Plan* pl, int n_images, const void* packed, void
           ? encode_filter_map(&kp.map_b, packed, pl->kmax, kp.f_group, kp.groups, pl->in_dtype,
                               kp.bk, kp.bn, kp.sw_bytes)
           : encode_filter_map(&kp.map_b, packed, pl->kmax, kp.Cout, pl->phases_packed,
-                              pl->in_dtype, kp.bk, kp.bn, kp.sw_bytes);
+                              pl->in_dtype, kp.bk, kp.pair ? kp.bn / 2 : kp.bn, kp.sw_bytes);
   if (st != CONV_OK) return st;
   st = plan_memory(pl, n_images, output, has_residual ? source : nullptr, has_residual);
   if (st != CONV_OK) return st;
@@ -1207,7 +1245,8 @@ conv_status_t finish_and_launch(Plan* pl, int n_images, const void* packed, void
   if (kp.total_tiles == 0) return CONV_OK;
   const int sms = device_sm_count();
   if (sms <= 0) return CONV_ERR_CUDA;
-  pl->grid = std::min(kp.total_tiles, sms);
+  // Pairs: clusters of two CTAs, one tile per cluster at a time.
+  pl->grid = kp.pair ? 2 * std::min(kp.total_tiles, sms / 2) : std::min(kp.total_tiles, sms);
   cudaError_t e = launch_conv_igemm(pl->kind, pl->out_bf16, kp, pl->grid, pl->smem_bytes, stream);
   return e == cudaSuccess ? CONV_OK : CONV_ERR_CUDA;
 }
@@ -1744,7 +1783,7 @@ void conv_testing_set_wait_fault(int mode, unsigned long long timeout_ns) {
 conv_status_t conv_testing_fwd_plan(int n, int h, int w, int c_in, conv_dtype_t dtype, int r,
                                     int s, int c_out, const int stride[2],
                                     const int symmetric_padding[2], int has_residual, int num_sms,
-                                    int out[12]) {
+                                    int out[13]) {
   if (!stride || !symmetric_padding || !out) return CONV_ERR_INVALID_VALUE;
   const int dil[2] = {1, 1};
   const conv_dtype_t out_dt = dtype == CONV_DTYPE_F8E4M3 ? CONV_DTYPE_BF16 : dtype;
@@ -1770,6 +1809,7 @@ conv_status_t conv_testing_fwd_plan(int n, int h, int w, int c_in, conv_dtype_t 
     out[9] = 0;
     out[10] = rp.band;
     out[11] = 3;
+    out[12] = 0;
     return CONV_OK;
   }
   Plan pl;
@@ -1782,13 +1822,15 @@ conv_status_t conv_testing_fwd_plan(int n, int h, int w, int c_in, conv_dtype_t 
   out[2] = pl.kp.stages;
   out[3] = static_cast<int>(pl.smem_bytes);
   out[4] = pl.kp.total_tiles;
-  out[5] = std::min(pl.kp.total_tiles, num_sms);
+  out[5] = pl.kp.pair ? 2 * std::min(pl.kp.total_tiles, num_sms / 2)
+                     : std::min(pl.kp.total_tiles, num_sms);
   out[6] = static_cast<int>(pl.kp.tmem_cols);
   out[7] = pl.kp.epi_mode;
   out[8] = pl.kp.b_resident;
   out[9] = pl.kp.src_bufs;
   out[10] = pl.kp.stg_bufs;
   out[11] = pl.kp.gather ? 2 : (pl.kp.window ? 1 : 0);
+  out[12] = pl.kp.pair;
   return CONV_OK;
 }
 

@@ -71,6 +71,10 @@ struct RowTapParams {  // aligned like CUtensorMap
 cudaError_t launch_conv_rowtap(int in_dtype, bool out_bf16, const RowTapParams& p, int grid,
                                size_t smem_bytes, cudaStream_t stream);
 
+// The CTA-pair instances (cta_group::2; their own translation unit).
+cudaError_t launch_conv_igemm_pair(int kind, bool out_bf16, const ConvKernelParams& p, int grid,
+                                   size_t smem_bytes, cudaStream_t stream);
+
 // The gather-loader instances (their own translation unit).
 cudaError_t launch_conv_igemm_gather(int kind, bool out_bf16, const ConvKernelParams& p, int grid,
                                      size_t smem_bytes, cudaStream_t stream);

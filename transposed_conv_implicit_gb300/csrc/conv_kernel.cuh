@@ -82,7 +82,7 @@ __device__ __forceinline__ TileInfo decode_tile(const ConvKernelParams& p, int t
   ti.group = group;
   const int mt = fast_div(local, p.div_ntiles);
   ti.n0 = (local - mt * p.n_tiles) * p.bn;
-  ti.m0 = mt * (kBM * p.m_halves);
+  ti.m0 = mt * ((kBM * p.m_halves) << p.pair);  // a pair's tile spans both CTAs' rows
   ti.kblocks = p.taps_h[ph] * p.taps_w[ph] * p.c_blocks;
   return ti;
 }
@@ -302,7 +302,8 @@ __device__ __forceinline__ void issue_source_items(const ConvKernelParams& p, co
 // kHalves 128-row halves of A sharing the B operand.  Descriptors are built
 // from precomputed high bits plus an address field advanced by adds only: the
 // issuing thread is latency-bound, so nothing here divides or branches.
-template <int kKind, int kSteps, int kHalves>
+// kPair: one M = 256 MMA over both CTAs of a pair (issued by rank 0).
+template <int kKind, int kSteps, int kHalves, bool kPair = false>
 __device__ __forceinline__ void issue_kblock(uint32_t d_tmem, uint64_t desc_hi, uint32_t a_lo,
                                              uint32_t b_lo, uint32_t half_lo, uint32_t bn_cols,
                                              uint32_t idesc, uint32_t first_accumulate) {
@@ -313,26 +314,35 @@ __device__ __forceinline__ void issue_kblock(uint32_t d_tmem, uint64_t desc_hi, 
 #pragma unroll
     for (int h = 0; h < kHalves; ++h) {
       const uint64_t adesc = desc_hi | static_cast<uint64_t>(a_lo + h * half_lo + 2u * kk);
-      if (kKind == kKindF16)
-        mma_f16(d_tmem + h * bn_cols, adesc, bdesc, idesc, accumulate);
-      else
-        mma_f8(d_tmem + h * bn_cols, adesc, bdesc, idesc, accumulate);
+      if (kPair) {
+        if (kKind == kKindF16)
+          mma_f16_pair(d_tmem + h * bn_cols, adesc, bdesc, idesc, accumulate);
+        else
+          mma_f8_pair(d_tmem + h * bn_cols, adesc, bdesc, idesc, accumulate);
+      } else {
+        if (kKind == kKindF16)
+          mma_f16(d_tmem + h * bn_cols, adesc, bdesc, idesc, accumulate);
+        else
+          mma_f8(d_tmem + h * bn_cols, adesc, bdesc, idesc, accumulate);
+      }
     }
   }
 }
 
-// The MMA role for one (kSteps, kHalves) specialisation.
-template <int kKind, int kSteps, int kHalves>
+// The MMA role for one (kSteps, kHalves) specialisation.  Tiles t0, t0 +
+// step, ...  kPair: rank 0 of a CTA pair issues M = 256 MMAs over both CTAs'
+// operands (each holds bn/2 rows of B) and commits to both CTAs' barriers.
+template <int kKind, int kSteps, int kHalves, bool kPair = false>
 __device__ __forceinline__ bool mma_role(const ConvKernelParams& p, uint32_t tmem_base,
                                          uint8_t* a_ring, uint8_t* b_ring, uint8_t* b_res,
                                          uint64_t* full, uint64_t* empty, uint64_t* tfull,
                                          uint64_t* tempty, uint64_t* bres_full,
                                          volatile int* abort_flag, unsigned int* status,
-                                         long long limit) {
+                                         long long limit, int t0, int step) {
   const int stages = p.stages;
   const uint32_t sw = p.sw_bytes;
   const uint32_t a_bytes = kBM * kHalves * sw;
-  const uint32_t b_bytes = static_cast<uint32_t>(p.bn) * sw;
+  const uint32_t b_bytes = static_cast<uint32_t>(kPair ? p.bn / 2 : p.bn) * sw;
   const uint64_t desc_hi = smem_desc_kmajor(0, sw);  // address field zero
   const uint32_t a_lo0 = smem_u32(a_ring) >> 4;
   const uint32_t b_lo0 = smem_u32(p.b_resident ? b_res : b_ring) >> 4;
@@ -353,17 +363,21 @@ __device__ __forceinline__ bool mma_role(const ConvKernelParams& p, uint32_t tme
   uint32_t bs_lo = b_lo0;  // streamed B: advances with the ring
   bool ok = true;
   int it = 0;
-  for (int t = blockIdx.x; ok && t < total_tiles; t += gridDim.x, ++it) {
+  for (int t = t0; ok && t < total_tiles; t += step, ++it) {
     const TileInfo ti = decode_tile(p, t);
     const int acc = it & 1;
     if (!mbar_wait_bounded(smem_u32(&tempty[acc]), static_cast<uint32_t>(((it >> 1) & 1) ^ 1),
-                           abort_flag, status, kStatusMmaTimeout, limit)) {
+                           abort_flag, status, kStatusMmaTimeout, limit, 0u, kPair)) {
       ok = false;
       break;
     }
     tc_fence_after();
     if (ti.kblocks == 0) {  // a phase with no filter taps: the epilogue writes act(0)
-      mbar_arrive(smem_u32(&tfull[acc]));
+      if (kPair) {
+        mma_commit_pair(smem_u32(&tfull[acc]));
+      } else {
+        mbar_arrive(smem_u32(&tfull[acc]));
+      }
       continue;
     }
     const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc) * acc_stride;
@@ -371,14 +385,18 @@ __device__ __forceinline__ bool mma_role(const ConvKernelParams& p, uint32_t tme
     const int kblocks = ti.kblocks;
     for (int kb = 0; kb < kblocks; ++kb) {
       if (!mbar_wait_bounded(full0 + 8u * stage, phase, abort_flag, status, kStatusMmaTimeout,
-                             limit)) {
+                             limit, 0u, kPair)) {
         ok = false;
         break;
       }
       tc_fence_after();
-      issue_kblock<kKind, kSteps, kHalves>(d_tmem, desc_hi, a_lo, b_resident ? br_lo : bs_lo,
-                                           half_lo, bn_cols, idesc, kb != 0 ? 1u : 0u);
-      mma_commit(empty0 + 8u * stage);
+      issue_kblock<kKind, kSteps, kHalves, kPair>(d_tmem, desc_hi, a_lo,
+                                                  b_resident ? br_lo : bs_lo, half_lo, bn_cols,
+                                                  idesc, kb != 0 ? 1u : 0u);
+      if (kPair)
+        mma_commit_pair(empty0 + 8u * stage);
+      else
+        mma_commit(empty0 + 8u * stage);
       br_lo += b_step;
       a_lo += a_step;
       bs_lo += b_step;
@@ -390,7 +408,10 @@ __device__ __forceinline__ bool mma_role(const ConvKernelParams& p, uint32_t tme
       }
     }
     if (!ok) break;
-    mma_commit(smem_u32(&tfull[acc]));
+    if (kPair)
+      mma_commit_pair(smem_u32(&tfull[acc]));
+    else
+      mma_commit(smem_u32(&tfull[acc]));
   }
   return ok;
 }
@@ -404,7 +425,7 @@ __device__ __forceinline__ bool mma_role_window(const ConvKernelParams& p, uint3
                                                 uint8_t* a_ring, uint8_t* b_res, uint64_t* full,
                                                 uint64_t* empty, uint64_t* tfull, uint64_t* tempty,
                                                 volatile int* abort_flag, unsigned int* status,
-                                                long long limit) {
+                                                long long limit, int t0, int step) {
   const int stages = p.stages;
   const uint32_t sw = p.sw_bytes;  // 128 in this mode
   const uint32_t b_bytes = static_cast<uint32_t>(p.bn) * sw;
@@ -430,7 +451,7 @@ __device__ __forceinline__ bool mma_role_window(const ConvKernelParams& p, uint3
   uint32_t a_lo = a_lo0;
   bool ok = true;
   int it = 0;
-  for (int t = blockIdx.x; ok && t < total_tiles; t += gridDim.x, ++it) {
+  for (int t = t0; ok && t < total_tiles; t += step, ++it) {
     const int acc = it & 1;
     if (!mbar_wait_bounded(smem_u32(&tempty[acc]), static_cast<uint32_t>(((it >> 1) & 1) ^ 1),
                            abort_flag, status, kStatusMmaTimeout, limit)) {
@@ -837,7 +858,12 @@ __device__ __forceinline__ void gather_producer(const ConvKernelParams& p, int r
 // kGather selects the producer role: the gather loader, or the TMA loaders
 // (im2col and row window).  The two are separate instances so that neither
 // carries the other's registers.
-template <int kKind, typename OutT, bool kGather>
+// kPair: the CTAs run as clusters of two.  A pair works on one tile of 256
+// rows: rank r's producers load rows [128r, 128r + 128) of A and filter rows
+// [r*bn/2, (r+1)*bn/2) of B into its own shared memory, rank 0 issues M = 256
+// MMAs over both (tcgen05 cta_group::2), and each CTA's epilogue stores its
+// 128 rows from its own TMEM.  TMA im2col loader, streamed filter only.
+template <int kKind, typename OutT, bool kGather, bool kPair = false>
 __global__ void __launch_bounds__(kThreads, 1)
     conv_igemm_kernel(const __grid_constant__ ConvKernelParams p) {
   extern __shared__ uint8_t smem_raw[];
@@ -848,7 +874,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int stages = p.stages;
   const uint32_t sw = p.sw_bytes;
   const uint32_t a_bytes = kBM * p.m_halves * sw;
-  const uint32_t b_bytes = static_cast<uint32_t>(p.bn) * sw;
+  const uint32_t b_bytes = static_cast<uint32_t>(kPair ? p.bn / 2 : p.bn) * sw;
+  // Tile walk: CTAs (or CTA pairs) take tiles tile0, tile0 + tile_step, ...
+  const uint32_t rank = kPair ? cluster_rank() : 0u;
+  const int tile0 = kPair ? static_cast<int>(cluster_id_x()) : static_cast<int>(blockIdx.x);
+  const int tile_step = kPair ? static_cast<int>(num_clusters_x()) : static_cast<int>(gridDim.x);
+  const int m_off = static_cast<int>(rank) * kBM;  // this CTA's rows within a pair's tile
 
   uint8_t* a_ring = smem + p.off_a;
   uint8_t* b_ring = smem + p.off_b;
@@ -878,7 +909,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(smem_u32(&tfull[a]), 1);
-      mbar_init(smem_u32(&tempty[a]), kEpilogueWarps);
+      mbar_init(smem_u32(&tempty[a]), kEpilogueWarps * (kPair ? 2 : 1));
       mbar_init(smem_u32(&src_full[2 * a]), 1);
       mbar_init(smem_u32(&src_full[2 * a + 1]), 1);
     }
@@ -893,8 +924,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     fence_barrier_init();
   }
   if (warp == 1) {
-    tmem_alloc(smem_u32(tmem_slot), p.tmem_cols);
-    tmem_relinquish();
+    if (kPair) {
+      tmem_alloc_pair(smem_u32(tmem_slot), p.tmem_cols);
+      tmem_relinquish_pair();
+    } else {
+      tmem_alloc(smem_u32(tmem_slot), p.tmem_cols);
+      tmem_relinquish();
+    }
   }
   if (warp == 0 && lane == 0) {
     if (!kGather)
@@ -903,6 +939,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   tc_fence_before();
   __syncthreads();
+  // Both CTAs of a pair have initialised their barriers before either
+  // signals one of the other's.
+  if (kPair) cluster_sync();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
   // Set-up above may overlap the previous kernel in the stream; every global
@@ -933,7 +972,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // first tile also brings every tap's filter block of that channel block.
         const uint32_t box_bytes = static_cast<uint32_t>(p.win_pitch * p.win_box_rows) * sw;
         const int taps = p.win_R * p.win_S;
-        for (int t = blockIdx.x; t < p.total_tiles && ok; t += gridDim.x) {
+        for (int t = tile0; t < p.total_tiles && ok; t += tile_step) {
           int n_img, oy0;
           window_origin(p, t, n_img, oy0);
           for (int cb = 0; cb < p.c_blocks; ++cb, ++seq) {
@@ -963,8 +1002,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           first_tile = false;
         }
       }
-      for (int t = blockIdx.x; !p.window && t < p.total_tiles && ok; t += gridDim.x) {
-        const TileInfo ti = decode_tile(p, t);
+      // A pair's rank 0 arms its stage barrier for both CTAs' bytes; rank 1's
+      // copies count on rank 0's barrier.
+      const uint32_t arm_tx = kPair ? 2u * stage_tx : stage_tx;
+      for (int t = tile0; !p.window && t < p.total_tiles && ok; t += tile_step) {
+        TileInfo ti = decode_tile(p, t);
+        ti.m0 += m_off;
         const int ph = ti.phase;
         int n_img, j, i;
         grid_pos(p, ph, ti.m0, n_img, j, i);
@@ -981,12 +1024,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         first_tile = false;
         // This CTA's next tile: its A boxes are prefetched into L2 alongside
         // this tile's loads, so they come from L2 rather than HBM later.
-        const int tn = t + static_cast<int>(gridDim.x);
+        const int tn = t + tile_step;
         const bool pf = p.l2_prefetch && tn < p.total_tiles;
         int pf_n = 0, pf_h0 = 0, pf_w0 = 0;
         const CUtensorMap* pf_map = amap;
         if (pf) {
-          const TileInfo tin = decode_tile(p, tn);
+          TileInfo tin = decode_tile(p, tn);
+          tin.m0 += m_off;
           int pj, pi;
           grid_pos(p, tin.phase, tin.m0, pf_n, pj, pi);
           pf_h0 = p.base_h[tin.phase] + pj * p.step_h;
@@ -998,12 +1042,30 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int kb = 0; kb < ti.kblocks; ++kb, ++seq) {
           if ((seq & 1) == role) {
             if (!mbar_wait_bounded(smem_u32(&empty[stage]), phase ^ 1u, abort_flag, status,
-                                   kStatusProducerTimeout, limit, p.wait_hint_ns)) {
+                                   kStatusProducerTimeout, limit, p.wait_hint_ns, kPair)) {
               ok = false;
               break;
             }
             last_issued = seq;
-            if (!(p.fault_mode == 1 && blockIdx.x == 0 && seq == 0)) {
+            if (kPair) {
+              const uint32_t fb = smem_u32(&full[stage]);
+              const int n_b = ti.n0 + static_cast<int>(rank) * (p.bn / 2);
+              if (rank == 0) {
+                mbar_arrive_expect_tx(fb, arm_tx);
+                tma_load_im2col_4d(smem_u32(a_ring + stage * a_bytes), amap, fb,
+                                   c_base + cb * p.bk, w0, h0, n_img,
+                                   static_cast<uint16_t>(uw * p.dil_w),
+                                   static_cast<uint16_t>(uh * p.dil_h));
+                tma_load_3d(smem_u32(b_ring + stage * b_bytes), &p.map_b, fb, bk_k, n_b, bz);
+              } else {
+                const uint32_t fb0 = map_to_rank(fb, 0);
+                tma_load_im2col_4d_pair(smem_u32(a_ring + stage * a_bytes), amap, fb0,
+                                        c_base + cb * p.bk, w0, h0, n_img,
+                                        static_cast<uint16_t>(uw * p.dil_w),
+                                        static_cast<uint16_t>(uh * p.dil_h));
+                tma_load_3d_pair(smem_u32(b_ring + stage * b_bytes), &p.map_b, fb0, bk_k, n_b, bz);
+              }
+            } else if (!(p.fault_mode == 1 && blockIdx.x == 0 && seq == 0)) {
               // (fault_mode 1, a test hook: CTA 0 leaves its first stage un-armed.)
               const uint32_t fb = smem_u32(&full[stage]);
               mbar_arrive_expect_tx(fb, stage_tx + (load_res ? b_bytes : 0u));
@@ -1035,8 +1097,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       }
-      if (!ok) {
+      if (!ok && rank == 0) {
         // Let every copy this producer still has in flight land before exiting.
+        // (A pair's rank-0 barriers count rank 1's copies too.)
         for (long long q = last_issued - stages + 1; q <= last_issued; ++q)
           if (q >= 0 && (q & 1) == role)
             mbar_wait_drain(smem_u32(&full[q % stages]), static_cast<uint32_t>((q / stages) & 1),
@@ -1046,31 +1109,35 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
+    // (In a pair only rank 0 issues.)
+    if (lane == 0 && rank == 0) {
       bool ok;
       const int ks = static_cast<int>(sw / 32);
-      if (p.window) {
+      if (!kPair && p.window) {
         ok = p.m_halves == 2
                  ? mma_role_window<kKind, 4, 2>(p, tmem_base, a_ring, b_res, full, empty, tfull,
-                                                tempty, abort_flag, status, limit)
+                                                tempty, abort_flag, status, limit, tile0, tile_step)
                  : mma_role_window<kKind, 4, 1>(p, tmem_base, a_ring, b_res, full, empty, tfull,
-                                                tempty, abort_flag, status, limit);
+                                                tempty, abort_flag, status, limit, tile0, tile_step);
         if (!ok) {
           mma_commit(smem_u32(drain));
           mbar_wait_drain(smem_u32(drain), 0, limit / 8 + 1);
         }
       } else {
 #define CONV_MMA_ROLE(KS, MH)                                                                   \
-  mma_role<kKind, KS, MH>(p, tmem_base, a_ring, b_ring, b_res, full, empty, tfull, tempty, bres_full, \
-                          abort_flag, status, limit)
-      if (p.m_halves == 2)
+  mma_role<kKind, KS, MH, kPair>(p, tmem_base, a_ring, b_ring, b_res, full, empty, tfull, tempty,  \
+                                 bres_full, abort_flag, status, limit, tile0, tile_step)
+      if (!kPair && p.m_halves == 2)
         ok = ks == 4 ? CONV_MMA_ROLE(4, 2) : (ks == 2 ? CONV_MMA_ROLE(2, 2) : CONV_MMA_ROLE(1, 2));
       else
         ok = ks == 4 ? CONV_MMA_ROLE(4, 1) : (ks == 2 ? CONV_MMA_ROLE(2, 1) : CONV_MMA_ROLE(1, 1));
 #undef CONV_MMA_ROLE
       if (!ok) {
         // Every MMA already issued must finish before TMEM is released.
-        mma_commit(smem_u32(drain));
+        if (kPair)
+          mma_commit_pair(smem_u32(drain));
+        else
+          mma_commit(smem_u32(drain));
         mbar_wait_drain(smem_u32(drain), 0, limit / 8 + 1);
       }
       }
@@ -1088,6 +1155,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     const bool leader = (warp == 2 + 4 * grp) && lane == 0;
     const uint32_t bar_id = 1 + grp;
     int it = 0;
+    // This CTA's share of tile t (a pair's rank 1 takes rows 128..255).
+    auto tile_at = [&](int t) {
+      TileInfo x = decode_tile(p, t);
+      x.m0 += m_off;
+      return x;
+    };
+    // Hands accumulator buffer `acc` back to the MMA issuer (lane 0, after
+    // tcgen05.fence::before_thread_sync and __syncwarp).
+    auto release_acc = [&](int acc) {
+      if (kPair && rank != 0)
+        mbar_arrive_remote(map_to_rank(smem_u32(&tempty[acc]), 0));
+      else
+        mbar_arrive(smem_u32(&tempty[acc]));
+    };
     if (p.epi_mode != 0) {
       const uint32_t row_bytes = static_cast<uint32_t>(p.cw) * 2;
       const uint32_t chunk_bytes = kBM * row_bytes;
@@ -1098,27 +1179,27 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint8_t* stg_grp = stg_base + grp * (p.stg_bufs * chunk_bytes);
       int store_seq = 0;
       int src_issued[2] = {0, 0};  // source loads issued per buffer (leader only)
-      if (p.has_residual && leader && static_cast<int>(blockIdx.x) < p.total_tiles) {
-        issue_source_items(p, decode_tile(p, blockIdx.x), src_base, smem_u32(&src_full[grp]), grp);
+      if (p.has_residual && leader && tile0 < p.total_tiles) {
+        issue_source_items(p, tile_at(tile0), src_base, smem_u32(&src_full[grp]), grp);
         ++src_issued[0];
       }
-      for (int t = blockIdx.x; t < p.total_tiles; t += gridDim.x, ++it) {
-        const TileInfo ti = decode_tile(p, t);
+      for (int t = tile0; t < p.total_tiles; t += tile_step, ++it) {
+        const TileInfo ti = tile_at(t);
         const int acc = it & 1;
         const int sbuf = p.src_bufs == 2 ? acc : 0;
         if (p.has_residual && leader && p.src_bufs == 2) {
-          const int tn = t + gridDim.x;
+          const int tn = t + tile_step;
           if (tn < p.total_tiles) {
             // The other buffer last held tile it-1, whose stores must have read it.
             bulk_wait_read_all();
-            issue_source_items(p, decode_tile(p, tn), src_base + (acc ^ 1) * src_tile_bytes,
+            issue_source_items(p, tile_at(tn), src_base + (acc ^ 1) * src_tile_bytes,
                                smem_u32(&src_full[2 * (acc ^ 1) + grp]), grp);
             ++src_issued[acc ^ 1];
           }
         }
         bool ok = mbar_wait_bounded(smem_u32(&tfull[acc]), static_cast<uint32_t>((it >> 1) & 1),
                                     abort_flag, status, kStatusEpilogueTimeout, limit,
-                                    p.wait_hint_ns);
+                                    p.wait_hint_ns, kPair);
         if (ok && p.has_residual && grp < nitems) {
           const uint32_t par = static_cast<uint32_t>(p.src_bufs == 2 ? (it >> 1) & 1 : it & 1);
           ok = mbar_wait_bounded(smem_u32(&src_full[2 * sbuf + grp]), par, abort_flag, status,
@@ -1131,7 +1212,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (grp >= nitems) {  // nothing for this group in this tile
           tc_fence_before();
           __syncwarp();
-          if (lane == 0) mbar_arrive(smem_u32(&tempty[acc]));
+          if (lane == 0) release_acc(acc);
         }
         for (int q = grp; q < nitems; q += kEpilogueGroups) {
           const int h = q / nchunks;
@@ -1157,7 +1238,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             // This group's last TMEM read of the tile: hand the buffer back early.
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(smem_u32(&tempty[acc]));
+            if (lane == 0) release_acc(acc);
           }
           uint8_t* buf;
           if (in_place) {
@@ -1207,10 +1288,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (p.has_residual && leader && p.src_bufs == 1) {
           // Single source buffer: fetch the next tile's source once this
           // tile's stores (which read it) are done reading.
-          const int tn = t + gridDim.x;
+          const int tn = t + tile_step;
           if (tn < p.total_tiles) {
             bulk_wait_read_all();
-            issue_source_items(p, decode_tile(p, tn), src_base, smem_u32(&src_full[grp]), grp);
+            issue_source_items(p, tile_at(tn), src_base, smem_u32(&src_full[grp]), grp);
             ++src_issued[0];
           }
         }
@@ -1225,12 +1306,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                             static_cast<uint32_t>((src_issued[b] - 1) & 1), limit / 8 + 1);
       }
     } else {
-      for (int t = blockIdx.x; t < p.total_tiles; t += gridDim.x, ++it) {
-        const TileInfo ti = decode_tile(p, t);
+      for (int t = tile0; t < p.total_tiles; t += tile_step, ++it) {
+        const TileInfo ti = tile_at(t);
         const int acc = it & 1;
         bool ok = mbar_wait_bounded(smem_u32(&tfull[acc]), static_cast<uint32_t>((it >> 1) & 1),
                                     abort_flag, status, kStatusEpilogueTimeout, limit,
-                                    p.wait_hint_ns);
+                                    p.wait_hint_ns, kPair);
         if (!__all_sync(0xFFFFFFFFu, ok)) break;
         tc_fence_after();
         const int ph = ti.phase;
@@ -1268,7 +1349,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(smem_u32(&tempty[acc]));
+        if (lane == 0) release_acc(acc);
       }
     }
   }
@@ -1279,13 +1360,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) mbar_arrive(smem_u32(epi_done));
   }
   __syncthreads();
+  // Neither CTA of a pair exits (or frees TMEM) while the other may still
+  // signal one of its barriers or read its TMEM.
+  if (kPair) cluster_sync();
   if (warp == 1) {
     // TMEM is released only once every epilogue warp has signalled that its
     // last tcgen05.ld is complete.
     if (lane == 0) mbar_wait_drain(smem_u32(epi_done), 0, limit);
     __syncwarp();
     tc_fence_after();
-    tmem_dealloc(tmem_base, p.tmem_cols);
+    if (kPair)
+      tmem_dealloc_pair(tmem_base, p.tmem_cols);
+    else
+      tmem_dealloc(tmem_base, p.tmem_cols);
   }
 }
 

@@ -47,6 +47,7 @@ __global__ void im2col_probe_kernel(const __grid_constant__ CUtensorMap map, int
 cudaError_t launch_conv_igemm(int kind, bool out_bf16, const ConvKernelParams& p, int grid,
                               size_t smem_bytes, cudaStream_t stream) {
   if (p.gather) return launch_conv_igemm_gather(kind, out_bf16, p, grid, smem_bytes, stream);
+  if (p.pair) return launch_conv_igemm_pair(kind, out_bf16, p, grid, smem_bytes, stream);
   return launch_family<false>(kind, out_bf16, p, grid, smem_bytes, stream);
 }
 

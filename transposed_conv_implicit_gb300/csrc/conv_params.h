@@ -42,6 +42,7 @@ struct ConvKernelParams {  // aligned like CUtensorMap (64 B or more)
 
   int num_phases;
   int total_tiles;
+  int pair;             // clusters of two CTAs share 256-row tiles (cta_group::2 MMAs)
   int m_halves;         // 128-row halves per tile (1 or 2): tile_m = 128 * m_halves
   int n_tiles;          // tiles along C_out
   int bn;               // tile width along C_out (multiple of 16, <= 256)
