@@ -48,7 +48,8 @@ KERNEL_SOURCES = ["transposed_conv_implicit_gb300/csrc/conv_kernel.cuh",
                   "transposed_conv_implicit_gb300/csrc/conv_kernels_gather.cu",
                   "transposed_conv_implicit_gb300/csrc/conv_launch.cuh",
                   "transposed_conv_implicit_gb300/csrc/conv_direct.cu",
-                  "transposed_conv_implicit_gb300/csrc/conv_rowtap.cu"]
+                  "transposed_conv_implicit_gb300/csrc/conv_rowtap.cu",
+                  "transposed_conv_implicit_gb300/csrc/conv_kernels_pair.cu"]
 
 
 def kernel_source_hash() -> str:

@@ -173,8 +173,8 @@ def test_tile_plans_for_the_workloads(lib):
     p = _plan(lib, 32, 56, 56, 64, BF16, 3, 128, 2, 1, sms=152)          # downsample: 147 KB filter
     assert (p["bn"], p["tiles"], p["epi"], p["bres"]) == (128, 98, 1, 0) and p["stages"] >= 4
     p = _plan(lib, 16, 64, 64, 320, F8, 3, 320, 1, 1, res=1, sms=152)    # fp8: 2 x 160 columns,
-    assert (p["bn"], p["bk"], p["tmem"], p["epi"]) == (160, 128, 512, 1)  # 128-ch blocks, CTA pairs
-    assert (p["pair"], p["tiles"], p["grid"]) == (1, 512, 152)            # on 256-row tiles
+    assert (p["bn"], p["bk"], p["tiles"], p["tmem"], p["epi"]) == (160, 128, 1024, 512, 1)  # 128-ch blocks
+    assert p["pair"] == 0
     p = _plan(lib, 1, 512, 512, 128, BF16, 3, 3, 1, 1, sms=152)          # C_out = 3: row-tap kernel,
     assert (p["loader"], p["bn"], p["bk"], p["stgb"]) == (3, 48, 64, 9)  # N = 3 rows x 16, bands of 9
     assert p["tiles"] == 5 * 57 and p["grid"] == 152 and p["tmem"] == 512   # 5 segments x 57 bands
@@ -204,7 +204,7 @@ def test_row_tap_gate(lib, monkeypatch):
 
 def test_cta_pair_plans(lib, monkeypatch):
     """CTA pairs (cta_group::2, 256-row tiles shared by two CTAs) when every
-    pair of SMs gets at least 4 tiles and bn >= 128; CONV_PAIR=1/0 force."""
+    pair of SMs gets at least 4 tiles and bn = 256; CONV_PAIR=1/0 force."""
     monkeypatch.delenv("CONV_PAIR", raising=False)
     vae = (1, 256, 256, 512, BF16, 3, 512, 1, 1)
     p = _plan(lib, *vae, sms=152)

@@ -38,7 +38,10 @@ int elt_bytes(conv_dtype_t d) { return d == CONV_DTYPE_F8E4M3 ? 1 : 2; }
 // Tuning overrides read from the environment (0 or unset = let the planner
 // choose): CONV_TILE_M (128 or 256), CONV_TILE_N (a multiple of 16, <= 256),
 // CONV_FILTER_RESIDENT (0 forbids keeping the filter in shared memory),
-// CONV_MAX_STAGES (caps the operand ring).  Read on every call.
+// CONV_MAX_STAGES (caps the operand ring), CONV_SRC_BUFS (1: one residual
+// source buffer), CONV_PAIR (1/0: force CTA pairs on/off), CONV_WINDOW and
+// CONV_ROWTAP (-1 disables those loaders), CONV_ROWTAP_BAND.  Read on every
+// call.
 int env_int(const char* name) {
   const char* v = std::getenv(name);
   return v ? std::atoi(v) : 0;
@@ -382,12 +385,14 @@ void choose_tiling(Plan* pl, const long long rows[], int num_phases, int max_kbl
 // CTA pairs (cta_group::2): a cluster of two CTAs shares each 256-row tile;
 // each CTA loads its 128 rows of A and half of the tile's bn filter rows, so
 // per SM the filter bytes written into shared memory halve (measured: the
-// VAE 3x3 512->512 conv 194.6 -> 181.3 us).  Pairs halve the number of tile
-// slots, so they pay only with many tiles: the default takes them when every
-// pair gets at least 4 tiles and bn >= 128 (the fp8 3x3 320->320 conv ran
-// equally fast either way; convs with under two waves of 256-row tiles ran
-// 12-30% slower).  For the TMA im2col loader with a streamed filter and one
-// channel group.  CONV_PAIR=1 forces pairs where they apply, 0 forbids them.
+// VAE 3x3 512->512 conv, bn = 256, 194.6 -> 181.3 us).  The gain is that
+// share of the shared-memory traffic, so the default takes pairs only for
+// filter-heavy tiles (bn = 256: B twice the A bytes per k-block; the fp8
+// 3x3 320->320 conv at bn = 160 ran no faster) and only when every pair gets
+// at least 4 tiles (pairs halve the tile slots: convs with under two waves of
+// 256-row tiles ran 12-30% slower).  For the TMA im2col loader with a
+// streamed filter and one channel group.  CONV_PAIR=1 forces pairs where
+// they apply, 0 forbids them.
 void plan_pair(Plan* pl, int num_sms) {
   ConvKernelParams& kp = pl->kp;
   kp.pair = 0;
@@ -398,7 +403,7 @@ void plan_pair(Plan* pl, int num_sms) {
   int tile = 0;
   for (int ph = 0; ph < kp.num_phases; ++ph)
     tile += ((kp.rows[ph] + tile_m - 1) / tile_m) * kp.n_tiles;
-  if (force != 1 && (kp.bn < 128 || tile < 4 * std::max(num_sms / 2, 1))) return;
+  if (force != 1 && (kp.bn < 2 * kBM || tile < 4 * std::max(num_sms / 2, 1))) return;
   kp.pair = 1;
   kp.m_halves = 1;
   tile = 0;
@@ -980,7 +985,9 @@ conv_status_t layout_memory(Plan* pl, int has_residual) {
   struct Opt { bool res; int srcb, stgb; };
   Opt opts[12];
   int nopt = 0;
-  const int srcb_max = has_residual ? 2 : 0;
+  // CONV_SRC_BUFS (1 or 2) caps the residual-source tile buffers (tuning override).
+  const int srcb_env = env_int("CONV_SRC_BUFS");
+  const int srcb_max = has_residual ? ((srcb_env == 1) ? 1 : 2) : 0;
   // With a residual the outputs are written in place into the source tile
   // buffer and stored from there: no staging buffers.
   const int stg_max = has_residual ? 0 : 2;
