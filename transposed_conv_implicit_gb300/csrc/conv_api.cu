@@ -1477,6 +1477,26 @@ conv_status_t fwd_impl(const void* input, const FwdShape& shape, const void* fil
     dp.beta = has_residual ? beta : 0.0f;
     dp.div_wo = make_fast_div(static_cast<uint32_t>(f.wo));
     dp.div_ho = make_fast_div(static_cast<uint32_t>(f.ho));
+    dp.status = static_cast<unsigned int*>(workspace);
+    const unsigned long long tmo = g_timeout_ns.load(std::memory_order_relaxed);
+    dp.timeout_cycles = ns_to_cycles(tmo ? tmo : kDefaultTimeoutNs);
+    if (direct_uses_dw_tiles(static_cast<int>(f.in_dtype), dp)) {
+      // Depthwise 3x3 tiles: {C, W, H, N} boxes of kDwRows + 2 rows x kDwCols + 2
+      // columns x 64 channels, zero outside the image.
+      const DriverFns* fns = driver_fns();
+      if (!fns) return CONV_ERR_CUDA;
+      const cuuint64_t e = static_cast<cuuint64_t>(elt);
+      cuuint64_t dims[4] = {static_cast<cuuint64_t>(f.c_in), static_cast<cuuint64_t>(f.w),
+                            static_cast<cuuint64_t>(f.h), static_cast<cuuint64_t>(f.n)};
+      cuuint64_t strides[3] = {dims[0] * e, dims[0] * dims[1] * e, dims[0] * dims[1] * dims[2] * e};
+      cuuint32_t box[4] = {64, kDwCols + 2, kDwRows + 2, 1};
+      cuuint32_t estr[4] = {1, 1, 1, 1};
+      if (fns->tiled(&dp.map_x, tmap_dtype(f.in_dtype), 4, const_cast<void*>(input), dims, strides,
+                     box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return CONV_ERR_CUDA;
+    }
     cudaError_t e = launch_conv_direct(static_cast<int>(f.in_dtype), f.in_dtype != CONV_DTYPE_F16,
                                        dp, sms, stream);
     return e == cudaSuccess ? CONV_OK : CONV_ERR_CUDA;

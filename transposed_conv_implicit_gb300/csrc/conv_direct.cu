@@ -18,6 +18,7 @@
 #include <cuda_fp8.h>
 
 #include "conv_internal.h"
+#include "ptx.cuh"
 
 namespace convgb300 {
 
@@ -194,8 +195,197 @@ __global__ void __launch_bounds__(kDirectThreads)
   }
 }
 
+long long dw_tile_count(const DirectParams& p) {
+  return static_cast<long long>(p.N) * ((p.Ho + kDwRows - 1) / kDwRows) *
+         ((p.Wo + kDwCols - 1) / kDwCols) * ((p.F + kDirectChannels - 1) / kDirectChannels);
+}
+
+bool dw_tiles_apply(const DirectParams& p) {
+  if (!(p.R == 3 && p.S == 3 && p.stride_h == 1 && p.stride_w == 1 && p.dil_h == 1 &&
+        p.dil_w == 1 && p.c_group == 1 && p.f_group == 1 && p.C % kDirectVec == 0))
+    return false;
+  return dw_tile_count(p) < (1ll << 31);
+}
+
+// 3x3 depthwise with multiplier 1, stride 1, dilation 1, 16-bit inputs, C a
+// multiple of 8.  A tile is kDwRows output rows x kDwCols output columns x 64
+// channels; its input (kDwRows + 2 rows x kDwCols + 2 columns x 64 channels,
+// zero outside the image) arrives in shared memory as one TMA box; the CTA
+// keeps the boxes of its next kDwBufs - 1 tiles in flight while it computes
+// this one.  Thread (slot, px) owns 4 channels of output column px, with their
+// nine filter taps in registers: it walks down the tile's input rows, reads
+// the three taps of each row from shared memory (converted to fp32 once) and
+// adds them into the three output rows that row touches (a rolling set of
+// fp32 accumulators); an output row is stored once its third input row is in.
+constexpr int kDwBoxRows = kDwRows + 2;
+constexpr int kDwBoxCols = kDwCols + 2;
+constexpr uint32_t kDwBoxBytes = kDwBoxRows * kDwBoxCols * kDirectChannels * 2;
+
+constexpr int kDwThreads = 512;
+constexpr int kDwBufs = 2;  // input boxes in flight per CTA (one being read)
+constexpr int kDwVec = 4;  // channels per thread
+
+// Four 16-bit inputs (8 bytes) -> four floats.
+template <typename InT>
+__device__ __forceinline__ void dw_unpack(uint2 raw, float (&f)[kDwVec]) {
+  const InT* v = reinterpret_cast<const InT*>(&raw);
+#pragma unroll
+  for (int j = 0; j < kDwVec; ++j) f[j] = load_f32<InT>(v + j);
+}
+
+template <typename OutT>
+__device__ __forceinline__ void dw_store(const DirectParams& p, const float (&acc)[kDwVec], int n,
+                                         int oy, int ox, int f0) {
+  if (ox >= p.Wo || f0 >= p.F) return;
+  const long long o = ((static_cast<long long>(n) * p.Ho + oy) * p.Wo + ox) * p.F + f0;
+  uint2 sraw = make_uint2(0u, 0u);
+  if (p.has_residual) sraw = __ldg(reinterpret_cast<const uint2*>(static_cast<const OutT*>(p.src) + o));
+  const OutT* sv = reinterpret_cast<const OutT*>(&sraw);
+  uint2 out;
+  OutT* ov = reinterpret_cast<OutT*>(&out);
+#pragma unroll
+  for (int j = 0; j < kDwVec; ++j) {
+    float v = acc[j];
+    if (p.has_residual) v = fmaf(p.beta, load_f32<OutT>(sv + j), v);
+    ov[j] = store_rn<OutT>(direct_activation(v, p.epilogue));
+  }
+  *reinterpret_cast<uint2*>(static_cast<OutT*>(p.y) + o) = out;
+}
+
+struct DwTile {
+  int cb, n, oy0, x0;
+};
+
+__device__ __forceinline__ DwTile dw_decode(const DirectParams& p, int t) {
+  const int n_xseg = (p.Wo + kDwCols - 1) / kDwCols;
+  const int n_yblk = (p.Ho + kDwRows - 1) / kDwRows;
+  const int per_cb = p.N * n_yblk * n_xseg;
+  DwTile d;
+  d.cb = t / per_cb;
+  int rest = t - d.cb * per_cb;
+  const int xs = rest % n_xseg;
+  rest /= n_xseg;
+  d.oy0 = (rest % n_yblk) * kDwRows;
+  d.n = rest / n_yblk;
+  d.x0 = xs * kDwCols;
+  return d;
+}
+
+template <typename InT, typename OutT>
+__global__ void __launch_bounds__(kDwThreads, 1)
+    conv_dw3x3_kernel(const __grid_constant__ DirectParams p, int tiles) {
+  extern __shared__ uint8_t dw_smem_raw[];
+  // [kDwBufs buffers][box], from a 128-byte aligned base (TMA destinations)
+  uint8_t* boxes = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(dw_smem_raw) + 127) & ~static_cast<uintptr_t>(127));
+  __shared__ __align__(8) uint64_t bar[kDwBufs];
+  __shared__ int abort_flag;
+  const int slot = threadIdx.x & 15;  // channels [4*slot, 4*slot+4) of the tile's 64
+  const int px = threadIdx.x >> 4;    // output column of the tile (0..31)
+  const InT* __restrict__ w = static_cast<const InT*>(p.w);
+  if (threadIdx.x == 0) {
+    for (int b = 0; b < kDwBufs; ++b) mbar_init(smem_u32(&bar[b]), 1);
+    abort_flag = 0;
+    fence_barrier_init();
+    tma_prefetch_desc(&p.map_x);
+  }
+  __syncthreads();
+  int issued[kDwBufs] = {};  // boxes issued per buffer (thread 0)
+  auto issue = [&](int t, int buf) {  // thread 0: the input box of tile t
+    const DwTile d = dw_decode(p, t);
+    const uint32_t b = smem_u32(&bar[buf]);
+    ++issued[buf];
+    fence_proxy_async_shared();  // earlier generic reads of the buffer come first
+    mbar_arrive_expect_tx(b, kDwBoxBytes);
+    tma_load_4d(smem_u32(boxes + buf * kDwBoxBytes), &p.map_x, b, d.cb * kDirectChannels,
+                d.x0 - p.pad_w, d.oy0 - p.pad_h, d.n);
+  };
+  // Tile i of this CTA (t = blockIdx.x + i * gridDim.x) uses buffer i % kDwBufs.
+  if (threadIdx.x == 0)
+    for (int j = 0; j < kDwBufs - 1; ++j) {
+      const long long tj = blockIdx.x + static_cast<long long>(j) * gridDim.x;
+      if (tj < tiles) issue(static_cast<int>(tj), j);
+    }
+  float wr[9][kDwVec];  // this thread's filter taps, in registers
+  int cb_loaded = -1;
+  int i = 0;
+  for (int t = blockIdx.x; t < tiles; t += gridDim.x, ++i) {
+    const int buf = i % kDwBufs;
+    const DwTile d = dw_decode(p, t);
+    const int f0 = d.cb * kDirectChannels + slot * kDwVec;
+    if (d.cb != cb_loaded) {
+#pragma unroll
+      for (int tap = 0; tap < 9; ++tap)
+#pragma unroll
+        for (int j = 0; j < kDwVec; ++j)
+          wr[tap][j] = f0 + j < p.F ? load_f32<InT>(w + packed_index(p, f0 + j, tap / 3, tap % 3, 0))
+                                    : 0.0f;
+      cb_loaded = d.cb;
+    }
+    // Tile i + kDwBufs - 1 goes into the buffer read in the previous
+    // iteration, which every thread has finished (the __syncthreads at its end).
+    const long long tn = t + static_cast<long long>(kDwBufs - 1) * gridDim.x;
+    if (threadIdx.x == 0 && tn < tiles) issue(static_cast<int>(tn), (i + kDwBufs - 1) % kDwBufs);
+    if (threadIdx.x == 0) {
+      if (!mbar_wait_bounded(smem_u32(&bar[buf]), static_cast<uint32_t>((i / kDwBufs) & 1), &abort_flag,
+                             p.status, kStatusProducerTimeout, p.timeout_cycles))
+        abort_flag = 1;
+    }
+    __syncthreads();  // the box is in (thread 0 saw its barrier complete)
+    if (abort_flag) break;
+    const int ox = d.x0 + px;
+    const int rows = min(kDwRows, p.Ho - d.oy0);
+    const uint8_t* col = boxes + buf * kDwBoxBytes + (px * kDirectChannels + slot * kDwVec) * 2;
+    float a0[kDwVec], a1[kDwVec], a2[kDwVec];  // output rows k, k-1, k-2
+#pragma unroll
+    for (int j = 0; j < kDwVec; ++j) a0[j] = a1[j] = a2[j] = 0.0f;
+    for (int k = 0; k < rows + 2; ++k) {
+      const uint8_t* rowp = col + k * (kDwBoxCols * kDirectChannels * 2);
+      float in[3][kDwVec];  // taps s = 0, 1, 2 of this input row
+      dw_unpack<InT>(*reinterpret_cast<const uint2*>(rowp), in[0]);
+      dw_unpack<InT>(*reinterpret_cast<const uint2*>(rowp + kDirectChannels * 2), in[1]);
+      dw_unpack<InT>(*reinterpret_cast<const uint2*>(rowp + 2 * kDirectChannels * 2), in[2]);
+      // Filter row 0 feeds output row k, row 1 row k-1, row 2 row k-2.
+#pragma unroll
+      for (int s = 0; s < 3; ++s)
+#pragma unroll
+        for (int j = 0; j < kDwVec; ++j) {
+          a0[j] = fmaf(in[s][j], wr[s][j], a0[j]);
+          a1[j] = fmaf(in[s][j], wr[3 + s][j], a1[j]);
+          a2[j] = fmaf(in[s][j], wr[6 + s][j], a2[j]);
+        }
+      if (k >= 2) dw_store<OutT>(p, a2, d.n, d.oy0 + k - 2, ox, f0);
+#pragma unroll
+      for (int j = 0; j < kDwVec; ++j) {
+        a2[j] = a1[j];
+        a1[j] = a0[j];
+        a0[j] = 0.0f;
+      }
+    }
+    __syncthreads();  // done with this buffer
+  }
+  // A box still in flight (after an abort) lands before the CTA exits.
+  if (threadIdx.x == 0 && abort_flag) {
+    for (int b = 0; b < kDwBufs; ++b)
+      if (issued[b] > 0)
+        mbar_wait_drain(smem_u32(&bar[b]), static_cast<uint32_t>((issued[b] - 1) & 1),
+                        p.timeout_cycles / 8 + 1);
+  }
+}
+
 template <typename InT, typename OutT>
 cudaError_t launch_direct(const DirectParams& p, int num_sms, cudaStream_t stream) {
+  if (sizeof(InT) == 2 && dw_tiles_apply(p)) {
+    const long long tiles = dw_tile_count(p);
+    const size_t smem = 128 + kDwBufs * kDwBoxBytes;
+    cudaError_t err = cudaFuncSetAttribute(conv_dw3x3_kernel<InT, OutT>,
+                                           cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           static_cast<int>(smem));
+    if (err != cudaSuccess) return err;
+    const unsigned grid = static_cast<unsigned>(std::min<long long>(tiles, num_sms));
+    conv_dw3x3_kernel<InT, OutT><<<grid, kDwThreads, smem, stream>>>(p, static_cast<int>(tiles));
+    return cudaGetLastError();
+  }
   const size_t smem = static_cast<size_t>(p.R) * p.S * p.c_group * kDirectChannels * sizeof(float);
   cudaError_t err = cudaFuncSetAttribute(conv_direct_kernel<InT, OutT>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -213,6 +403,10 @@ cudaError_t launch_direct(const DirectParams& p, int num_sms, cudaStream_t strea
 }
 
 }  // namespace
+
+bool direct_uses_dw_tiles(int in_dtype, const DirectParams& p) {
+  return in_dtype != 2 && dw_tiles_apply(p);
+}
 
 size_t direct_smem_bytes(int r, int s, int c_group) {
   return static_cast<size_t>(r) * s * c_group * kDirectChannels * sizeof(float);

@@ -16,6 +16,11 @@ cudaError_t launch_conv_igemm(int kind, bool out_bf16, const ConvKernelParams& p
 // k = (r*S + s)*c_group + c, or, when w_runs is set, the gather layout
 // [F][r][run_elems] with run index s*c_group + c.
 struct DirectParams {
+  // 3x3 depthwise tiles: tiled {C, W, H, N} over the input, box {64, 34, 10, 1}
+  // (encoded only for that kernel).
+  CUtensorMap map_x;
+  unsigned int* status;     // workspace status word (bounded waits)
+  long long timeout_cycles;
   const void* x;
   const void* w;
   const void* src;
@@ -30,6 +35,12 @@ struct DirectParams {
 };
 
 size_t direct_smem_bytes(int r, int s, int c_group);
+
+// True when the 3x3 depthwise tile kernel runs this conv (its input map must
+// then be encoded): 16-bit inputs, multiplier 1, stride 1, dilation 1, C % 8 == 0.
+bool direct_uses_dw_tiles(int in_dtype, const DirectParams& p);
+constexpr int kDwRows = 16;   // output rows per depthwise tile
+constexpr int kDwCols = 32;   // output columns per depthwise tile
 
 // in_dtype: 0 bf16, 1 f16, 2 e4m3 (bf16 out).
 cudaError_t launch_conv_direct(int in_dtype, bool out_bf16, const DirectParams& p, int num_sms,
