@@ -183,7 +183,7 @@ uint32_t align1k(size_t v) { return static_cast<uint32_t>((v + 1023) & ~static_c
 // g_stage_bytes); needs m_halves.
 size_t gather_smem_bytes(ConvKernelParams& kp) {
   if (!kp.gather) return 0;
-  const size_t tables = static_cast<size_t>(2) * kBM * kp.m_halves * 16;
+  const size_t tables = static_cast<size_t>(kGatherProducers) * kBM * kp.m_halves * 16;
   kp.g_stage = 0;
   kp.g_slots = 0;
   kp.g_stage_bytes = 0;
@@ -348,8 +348,8 @@ void choose_tiling(Plan* pl, const long long rows[], int num_phases, int max_kbl
       const double a = static_cast<double>(kBM) * mh * kp.sw_bytes;
       const double b = static_cast<double>(bn) * kp.sw_bytes;
       const bool res = num_phases == 1 && nte == 1 && max_kblocks * b <= 96.0 * 1024;
-      // The gather loader builds A with two producer warps at ~5.6 cycles per row.
-      const double load = kp.gather ? std::max(kBM * mh * 5.6, (res ? 0.0 : b) / 70.0 + 40.0)
+      // The gather loader builds A at ~11 cycles per row per warp, with three warps.
+      const double load = kp.gather ? std::max(kBM * mh * 3.7, (res ? 0.0 : b) / 70.0 + 40.0)
                                     : (a + (res ? 0.0 : b)) / 70.0 + 40.0 * (res ? 1 : 2);
       const double mma = static_cast<double>(mh) * ksteps * (63.0 * std::max(1.0, bn / 128.0) + 8.0);
       const double epi = static_cast<double>(kBM) * mh * bn * 2 / 64.0;
@@ -1042,7 +1042,7 @@ conv_status_t layout_memory(Plan* pl, int has_residual) {
   off += kEpilogueGroups * o.stgb * align1k(chunk);
   kp.off_bar = off;
   kp.off_gtab = off + 1024;
-  kp.off_gstage = kp.off_gtab + align1k(static_cast<size_t>(2) * kBM * kp.m_halves * 16);
+  kp.off_gstage = kp.off_gtab + align1k(static_cast<size_t>(kGatherProducers) * kBM * kp.m_halves * 16);
   off += bar_bytes;
   pl->smem_bytes = off + 1024;
   return CONV_OK;
@@ -1197,7 +1197,7 @@ conv_status_t plan_memory_direct(Plan* pl) {
   kp.off_stg = off;
   kp.off_bar = off;
   kp.off_gtab = off + 1024;
-  kp.off_gstage = kp.off_gtab + align1k(static_cast<size_t>(2) * kBM * kp.m_halves * 16);
+  kp.off_gstage = kp.off_gtab + align1k(static_cast<size_t>(kGatherProducers) * kBM * kp.m_halves * 16);
   off += bar_bytes;
   pl->smem_bytes = off + 1024;
   return CONV_OK;

@@ -747,6 +747,7 @@ __device__ __forceinline__ void gather_producer(const ConvKernelParams& p, int r
   long long seq = 0, last_issued = -1;
   bool ok = true, first_tile = true;
   int staged[2] = {0, 0};  // staging uses issued per buffer (warp 0, lane 0)
+  int sel = 0;             // seq % kGatherProducers
   int it = 0;
   for (int t = blockIdx.x; t < p.total_tiles && ok; t += gridDim.x, ++it) {
     const TileInfo ti = decode_tile(p, t);
@@ -761,7 +762,7 @@ __device__ __forceinline__ void gather_producer(const ConvKernelParams& p, int r
         }
         const int tn = t + static_cast<int>(gridDim.x);
         if (tn < p.total_tiles) {
-          // The other buffer last held tile it-1: both warps must be done with it.
+          // The other buffer last held tile it-1: every builder warp must be done with it.
           const int nb = sb ^ 1;
           int w = 1;
           if (lane == 0)
@@ -795,7 +796,9 @@ __device__ __forceinline__ void gather_producer(const ConvKernelParams& p, int r
     const uint32_t stage_u32 = smem_u32(gstage + sb * p.g_stage_bytes);
     bool have_table = false;
     for (int kb = 0; kb < ti.kblocks; ++kb, ++seq) {
-      if ((seq & 1) == role) {
+      const bool mine = sel == role;  // k-block seq belongs to warp seq % kGatherProducers
+      if (++sel == kGatherProducers) sel = 0;
+      if (mine) {
         if (!have_table) {
           gather_row_table(p, tab, ti.m0, g_first, lane);
           have_table = true;
@@ -845,7 +848,7 @@ __device__ __forceinline__ void gather_producer(const ConvKernelParams& p, int r
     // Let this warp's copies in flight land before exiting: B k-blocks, and
     // (warp 0) the latest row staging of each buffer.
     for (long long q = last_issued - stages + 1; q <= last_issued; ++q)
-      if (q >= 0 && (q & 1) == role)
+      if (q >= 0 && q % kGatherProducers == role)
         mbar_wait_drain(smem_u32(&full[q % stages]), static_cast<uint32_t>((q / stages) & 1),
                         limit / 8 + 1);
     for (int b = 0; b < 2; ++b)
@@ -918,7 +921,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(smem_u32(epi_done), kEpilogueWarps);
     for (int b = 0; b < 2; ++b) {
       mbar_init(smem_u32(&gst_full[b]), 1);
-      mbar_init(smem_u32(&gst_empty[b]), 2);  // both producer warps
+      mbar_init(smem_u32(&gst_empty[b]), kGatherProducers);  // every builder warp
     }
     *abort_flag = 0;
     fence_barrier_init();
@@ -949,16 +952,18 @@ __global__ void __launch_bounds__(kThreads, 1)
   grid_dependency_wait();
   grid_launch_dependents();
 
-  if (warp == 0 || warp == kThreads / 32 - 1) {
+  if (warp == 0 || warp >= kProducer2Warp) {
     // ------------------------------------------------------------ producers
-    // Two producer warps walk the same k-block sequence; k-block `seq` is
-    // issued by producer (seq & 1), so two TMA issue streams overlap.
+    // The producer warps walk the same k-block sequence; with the TMA loaders
+    // k-block `seq` is issued by warp 0 or 10 (seq & 1), so two TMA issue
+    // streams overlap; the gather loader's three warps (0, 10, 11) build
+    // every third k-block each.
     if constexpr (kGather) {
-      const int role = warp == 0 ? 0 : 1;
+      const int role = warp == 0 ? 0 : (warp == kProducer2Warp ? 1 : 2);
       int4* tab = reinterpret_cast<int4*>(smem + p.off_gtab) + role * kBM * p.m_halves;
       gather_producer(p, role, lane, a_ring, b_ring, b_res, tab, smem + p.off_gstage, full, empty,
                       gst_full, gst_empty, abort_flag, status, limit);
-    } else if (lane == 0) {
+    } else if (lane == 0 && warp != kProducer3Warp) {
       const int role = warp == 0 ? 0 : 1;
       int stage = 0;
       uint32_t phase = 0;

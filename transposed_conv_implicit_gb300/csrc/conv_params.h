@@ -9,7 +9,12 @@
 namespace convgb300 {
 
 constexpr int kBM = 128;             // rows (output pixels) per MMA = TMEM lanes
-constexpr int kThreads = 352;        // 2 producer warps + MMA warp + 8 epilogue warps
+// Warps: 0 producer, 1 MMA, 2-9 epilogue, 10 producer, 11 producer (the gather
+// loader only: it builds A with three warps; the TMA loaders use two).
+constexpr int kThreads = 384;
+constexpr int kProducer2Warp = 10;
+constexpr int kProducer3Warp = 11;
+constexpr int kGatherProducers = 3;
 constexpr int kEpilogueWarps = 8;    // two warpgroups; each covers the 128 TMEM lanes once
 constexpr int kEpilogueGroups = 2;
 constexpr int kMaxPhases = 4;        // stride-phase GEMMs of a stride-2 transposed conv
