@@ -355,7 +355,11 @@ void choose_tiling(Plan* pl, const long long rows[], int num_phases, int max_kbl
       const double epi = static_cast<double>(kBM) * mh * bn * 2 / 64.0;
       // The smaller term still costs a little (issue slots, barriers): it breaks
       // ties in favour of fewer, wider MMAs.
-      const double tile = max_kblocks * (std::max(load, mma) + 0.1 * std::min(load, mma)) + epi;
+      // A gather tile also pays fixed work of ~2,000 cycles: each builder
+      // warp's row table and the row-staging handshake (the RGB stem ran
+      // 77.8 us on 256-row tiles against 90.1 on 128-row ones).
+      const double tile = max_kblocks * (std::max(load, mma) + 0.1 * std::min(load, mma)) + epi +
+                          (kp.gather ? 2000.0 : 0.0);
       const double cost = waves * tile;
       if (cost < best * 0.999) {
         best = cost;
