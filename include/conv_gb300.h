@@ -118,16 +118,22 @@ size_t conv2d_workspace_size(int r, int s, int c_in, int c_out, conv_dtype_t dty
  * counts (e.g. c_in = 3) by the gather loader, which needs d_w == 1.
  * num_groups = G splits input and output channels into G equal groups
  * (output group g reads input group g; the filter is FCRS
- * [c_out][c_in/G][r][s] or RSCF [r][s][c_in/G][c_out]); G > 1 needs
- * (c_in/G) * sizeof(in_dtype) to be whole TMA channel blocks (a multiple of
- * 16 bytes, at least 32, e.g. 16+ bf16 channels per group), else
- * CONV_ERR_NOT_SUPPORTED; channels not divisible by G are
- * CONV_ERR_INVALID_VALUE.
+ * [c_out][c_in/G][r][s] or RSCF [r][s][c_in/G][c_out]).  Groups of whole TMA
+ * channel blocks ((c_in/G) * sizeof(in_dtype) a multiple of 16 bytes, at
+ * least 32) run on the tensor cores; narrower ones (depthwise, channel
+ * multipliers) on CUDA cores, which need r * s * (c_in/G) * 256 bytes of
+ * shared memory <= 200 KB (else CONV_ERR_NOT_SUPPORTED); channels not
+ * divisible by G are CONV_ERR_INVALID_VALUE.
  * CONV_ERR_INVALID_VALUE: null pointers, non-positive sizes, ho/wo not equal
  * to floor((h + 2p - (r-1) - 1)/stride) + 1, has_residual with NULL source,
  * unknown epilogue.
  * conv2d_fwd packs the filter into the workspace on every call;
  * conv2d_fwd_packed takes a filter already packed by conv2d_pack_filter.
+ * Which kernel runs is the library's choice and does not change results
+ * beyond fp32 summation order: the implicit GEMM (single CTAs, or CTA pairs
+ * sharing 256-row tiles for wide, many-tile convs), the row-tap kernel for
+ * stride-1 convs with s * c_out <= 32 (e.g. an RGB head), or the CUDA-core
+ * kernels for narrow channel groups.
  * ------------------------------------------------------------------------ */
 conv_status_t conv2d_fwd(const void* input, int n, int h, int w, int c_in, conv_dtype_t in_dtype,
                          const void* filter, int r, int s, int c_out, int filter_is_fcrs,
