@@ -27,6 +27,10 @@ CASES = [
     _fwd("im2col_s2", "bf16", 2, 13, 11, 64, 272, 3, 2, 1, layout="FCRS"),
     # per-phase maps of the transposed convolution, fp8 kind
     _tr("transposed_e4m3", "f8e4m3", 2, 8, 8, 64, 64, 4, 2, 1),
+    # the row-tap kernel (few output channels)
+    _fwd("rowtap_head", "bf16", 1, 20, 140, 128, 3, 3, 1, 1),
+    # the depthwise 3x3 tile kernel (CUDA cores, TMA boxes)
+    _fwd("depthwise_tiles", "bf16", 2, 20, 40, 64, 64, 3, 1, 1, groups=64),
 ]
 
 

@@ -1000,8 +1000,8 @@ conv_status_t layout_memory(Plan* pl, int has_residual) {
     for (int srcb = srcb_max; srcb >= (srcb_max ? 1 : 0); --srcb)
       for (int stgb = stg_max; stgb >= stg_min; --stgb) opts[nopt++] = Opt{res != 0, srcb, stgb};
   // Rank the options: at least 3 ring stages; then the cheapest k-block
-  // (a resident filter saves one TMA load per k-block); then a prefetched
-  // residual source; then deeper rings.
+  // (a resident filter saves one TMA load per k-block); then at least 5
+  // stages; then a prefetched residual source; then deeper rings.
   int best = -1, best_stages = 0;
   double best_key = 1e300;
   for (int i = 0; i < nopt; ++i) {
@@ -1016,6 +1016,10 @@ conv_status_t layout_memory(Plan* pl, int has_residual) {
     double key = load;
     if (st < 3) key += 1e6;
     if (opts[i].srcb < srcb_max) key += 50.0;
+    // Below 5 stages a deeper ring beats the second source buffer (fp8 3x3
+    // 320->320 with a residual: 4 stages and two source buffers 75.8 us,
+    // 5 stages and one 73.7 us).
+    if (st < 5) key += 60.0;
     key -= 0.01 * st;
     if (key < best_key) {
       best_key = key;
@@ -1386,6 +1390,7 @@ conv_status_t launch_rowtap_path(RowTapPlan* pl, const FwdShape& f, const void* 
   rp.status = static_cast<unsigned int*>(workspace);
   const unsigned long long tmo = g_timeout_ns.load(std::memory_order_relaxed);
   rp.timeout_cycles = ns_to_cycles(tmo ? tmo : kDefaultTimeoutNs);
+  rp.fault_mode = g_fault_mode.load(std::memory_order_relaxed);
   if (rp.total_tiles == 0) return CONV_OK;
   cudaError_t err = launch_conv_rowtap(static_cast<int>(f.in_dtype), f.in_dtype != CONV_DTYPE_F16,
                                        rp, pl->grid, pl->smem_bytes, stream);
@@ -1484,6 +1489,7 @@ conv_status_t fwd_impl(const void* input, const FwdShape& shape, const void* fil
     dp.status = static_cast<unsigned int*>(workspace);
     const unsigned long long tmo = g_timeout_ns.load(std::memory_order_relaxed);
     dp.timeout_cycles = ns_to_cycles(tmo ? tmo : kDefaultTimeoutNs);
+    dp.fault_mode = g_fault_mode.load(std::memory_order_relaxed);
     if (direct_uses_dw_tiles(static_cast<int>(f.in_dtype), dp)) {
       // Depthwise 3x3 tiles: {C, W, H, N} boxes of kDwRows + 2 rows x kDwCols + 2
       // columns x 64 channels, zero outside the image.

@@ -292,6 +292,8 @@ __global__ void __launch_bounds__(kDwThreads, 1)
   __syncthreads();
   int issued[kDwBufs] = {};  // boxes issued per buffer (thread 0)
   auto issue = [&](int t, int buf) {  // thread 0: the input box of tile t
+    // (fault_mode 1, a test hook: CTA 0 never loads its first tile.)
+    if (p.fault_mode == 1 && blockIdx.x == 0 && t == static_cast<int>(blockIdx.x)) return;
     const DwTile d = dw_decode(p, t);
     const uint32_t b = smem_u32(&bar[buf]);
     ++issued[buf];

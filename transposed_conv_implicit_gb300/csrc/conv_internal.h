@@ -21,6 +21,7 @@ struct DirectParams {
   CUtensorMap map_x;
   unsigned int* status;     // workspace status word (bounded waits)
   long long timeout_cycles;
+  int fault_mode;           // test hook: 1 = CTA 0 never loads its first depthwise tile
   const void* x;
   const void* w;
   const void* src;
@@ -76,6 +77,7 @@ struct RowTapParams {  // aligned like CUtensorMap
   void* out;
   unsigned int* status;
   long long timeout_cycles;
+  int fault_mode;      // test hook: 1 = CTA 0 leaves its first A stage un-armed
 };
 
 // Launches the row-tap kernel; in_dtype: 0 bf16, 1 f16, 2 e4m3 (bf16 out).

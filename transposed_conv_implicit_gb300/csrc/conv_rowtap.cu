@@ -204,9 +204,12 @@ __global__ void __launch_bounds__(kRtThreads, 1)
               break;
             }
             const uint32_t fb = smem_u32(&full[stage]);
-            mbar_arrive_expect_tx(fb, kRtStageBytes);
-            tma_load_4d(smem_u32(a_ring + stage * kRtStageBytes), &p.map_x, fb, cb * bk,
-                        ti.x0 - p.pad_w, iy, ti.n);
+            // (fault_mode 1, a test hook: CTA 0 leaves its first stage un-armed.)
+            if (!(p.fault_mode == 1 && blockIdx.x == 0 && issued == 0)) {
+              mbar_arrive_expect_tx(fb, kRtStageBytes);
+              tma_load_4d(smem_u32(a_ring + stage * kRtStageBytes), &p.map_x, fb, cb * bk,
+                          ti.x0 - p.pad_w, iy, ti.n);
+            }
             ++issued;
             if (++stage == stages) {
               stage = 0;
