@@ -18,14 +18,17 @@
 // matrix; when it fits, it is loaded into shared memory with the first tile
 // and kept there.
 //
-// Warp roles (352 threads, one persistent CTA per SM):
+// Warp roles (384 threads, one persistent CTA per SM, or one per SM of a
+// CTA pair):
 //   warps 0, 10  producers: k-block `seq` belongs to warp (seq & 1); one lane
-//                issues its TMA loads (the whole warp builds it in gather
-//                mode) into an S-stage shared-memory ring guarded by
-//                full/empty mbarriers;
+//                issues its TMA loads into an S-stage shared-memory ring
+//                guarded by full/empty mbarriers;
+//   warp 11      idle with the TMA loaders; in gather mode warps 0, 10 and 11
+//                each build every third k-block (k-block `seq` belongs to
+//                warp seq % 3), the whole warp writing it;
 //   warp 1       TMEM owner and MMA issuer: one lane issues tcgen05.mma
-//                (M=128 per half, N=bn) into a double-buffered fp32 TMEM
-//                accumulator;
+//                (M=128 per half, N=bn; M=256 over both CTAs of a pair, from
+//                rank 0) into a double-buffered fp32 TMEM accumulator;
 //   warps 2-9    epilogue, two warpgroups taking alternate (half, column
 //                chunk) items: tcgen05.ld the accumulator, add beta*source,
 //                apply the activation, round once to the output dtype and
@@ -724,15 +727,16 @@ __device__ __forceinline__ void gather_a_kblock(const ConvKernelParams& p, const
   }
 }
 
-// Producer role of the gather loader: the whole warp builds the A k-blocks
-// whose sequence number has this warp's parity; lane 0 also streams the B
-// k-block (or, on the first tile, the resident filter block) by TMA.  The
-// stage's full barrier completes with lane 0's arrival after the warp's
-// shared-memory writes are fenced for the tensor cores, plus the B bytes.
-// With row staging, warp 0's lane 0 also issues the bulk copies of the next
-// tile's input rows into the other staging buffer once both warps have
-// released it; each warp waits for a tile's rows before its first k-block
-// there and releases the buffer after its last.
+// Producer role of the gather loader (one of kGatherProducers warps, `role`):
+// the whole warp builds the A k-blocks whose sequence number is congruent to
+// its role; lane 0 also streams the B k-block (or, on the first tile, the
+// resident filter block) by TMA.  The stage's full barrier completes with
+// lane 0's arrival after the warp's shared-memory writes are fenced for the
+// tensor cores, plus the B bytes.  With row staging, role 0's lanes also
+// issue the bulk copies of the next tile's input rows into the other staging
+// buffer once every builder warp has released it; each warp waits for a
+// tile's rows before its first k-block there and releases the buffer after
+// its last.
 __device__ __forceinline__ void gather_producer(const ConvKernelParams& p, int role, int lane,
                                                 uint8_t* a_ring, uint8_t* b_ring, uint8_t* b_res,
                                                 int4* tab, uint8_t* gstage, uint64_t* full,
