@@ -223,6 +223,24 @@ def test_cta_pair_plans(lib, monkeypatch):
     assert _plan(lib, *vae, sms=152)["pair"] == 0
 
 
+def test_measured_planner_choices(lib, monkeypatch):
+    """Plans the measurements picked (each alternative was timed on GB300 and
+    ran slower): 256-row gather tiles for the RGB stem (77.8 vs 90.1 us on
+    128-row tiles), a 5-stage ring with one residual buffer for the fp8 conv
+    (4 stages and two buffers: 75.8 vs ~73 us), 256-row bn = 128 tiles for the
+    wave-quantised fwd5x5 (128-row: 42.0 vs 34.8 us)."""
+    for name in ("CONV_TILE_M", "CONV_TILE_N", "CONV_PAIR", "CONV_SRC_BUFS", "CONV_MAX_STAGES"):
+        monkeypatch.delenv(name, raising=False)
+    stem = _plan(lib, 32, 224, 224, 3, BF16, 7, 64, 2, 3, sms=152)
+    assert (stem["loader"], stem["tiles"], stem["tmem"]) == (2, 32 * 112 * 112 // 256, 256)
+    fp8 = _plan(lib, 16, 64, 64, 320, F8, 3, 320, 1, 1, res=1, sms=152)
+    assert (fp8["stages"], fp8["srcb"], fp8["pair"]) == (5, 1, 0)
+    f5 = _plan(lib, 8, 128, 128, 128, F16, 5, 128, 2, 2, sms=152)
+    assert (f5["bn"], f5["tiles"], f5["pair"]) == (128, 128, 0)
+    monkeypatch.setenv("CONV_SRC_BUFS", "1")   # the override still caps the buffers
+    assert _plan(lib, 16, 64, 64, 320, F8, 3, 320, 1, 1, res=1, sms=152)["srcb"] == 1
+
+
 def test_binding_raises_without_library(monkeypatch, tmp_path):
     monkeypatch.setattr(_lib, "_lib", None)
     monkeypatch.setattr(_lib, "LIB_PATH", str(tmp_path / "missing.so"))
