@@ -202,6 +202,43 @@ def test_row_tap_gate(lib, monkeypatch):
     assert (p["loader"], p["bn"], p["bk"], p["tiles"], p["epi"], p["bres"]) == (0, 16, 64, 1024, 0, 1)
 
 
+def test_row_tap_plan_invariants(lib, monkeypatch):
+    """Over many eligible shapes: the band fits the TMEM budget (two buffers
+    of g16 * (band + 2R - 2) columns within the allocation), the tile count
+    covers every output row and column segment, and shared memory fits."""
+    import random
+    monkeypatch.delenv("CONV_ROWTAP", raising=False)
+    monkeypatch.delenv("CONV_ROWTAP_BAND", raising=False)
+    rng = random.Random(7)
+    seen = 0
+    for _ in range(300):
+        r = rng.choice([1, 2, 3, 5, 7])
+        s_ = rng.choice([1, 2, 3, 5])
+        if r * s_ < 2:
+            continue
+        dt = rng.choice([BF16, F16, F8])
+        c = (128 // (1 if dt == F8 else 2)) * rng.choice([1, 2, 3])
+        f = rng.randint(1, 32 // s_)
+        n, h, w = rng.randint(1, 3), rng.randint(r, 70), rng.randint(s_, 300)
+        pd = rng.randint(0, r - 1) if r == s_ else 0
+        out = (ctypes.c_int * 13)()
+        st = lib.conv_testing_fwd_plan(n, h, w, c, dt, r, s_, f, _lib.pair((1, 1)), _lib.pair((pd, pd)),
+                                       0, 152, out)
+        assert st == OK
+        if out[11] != 3:
+            continue
+        seen += 1
+        mma_n, band, tiles, tmem, smem = out[0], out[10], out[4], out[6], out[3]
+        g16 = mma_n // r
+        assert g16 in (16, 32) and g16 >= s_ * f
+        assert 1 <= band <= 16 and 2 * g16 * (band + 2 * r - 2) <= tmem <= 512
+        ho, wo = h + 2 * pd - r + 1, w + 2 * pd - s_ + 1
+        seg = 128 - (s_ - 1)
+        assert tiles == n * -(-ho // band) * -(-wo // seg)
+        assert smem <= 227 * 1024 and out[2] >= 2
+    assert seen > 100
+
+
 def test_cta_pair_plans(lib, monkeypatch):
     """CTA pairs (cta_group::2, 256-row tiles shared by two CTAs) when every
     pair of SMs gets at least 4 tiles and bn = 256; CONV_PAIR=1/0 force."""
