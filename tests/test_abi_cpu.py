@@ -239,6 +239,44 @@ def test_row_tap_plan_invariants(lib, monkeypatch):
     assert seen > 100
 
 
+def test_cta_pair_plan_invariants(lib, monkeypatch):
+    """CTA pairs forced on over many shapes: 256-row tiles over every C_out
+    tile, an even grid of at most the SMs, accumulators of 2 x bn columns
+    within TMEM, shared memory within the limit; never with the row window
+    or the gather loader."""
+    import random
+    monkeypatch.setenv("CONV_PAIR", "1")
+    rng = random.Random(11)
+    seen = 0
+    for _ in range(300):
+        dt = rng.choice([BF16, F16, F8])
+        c = rng.choice([32, 64, 96, 128, 256, 320])
+        f = rng.choice([32, 48, 64, 128, 200, 256, 320, 512])
+        r = rng.choice([1, 3, 5])
+        st = rng.choice([1, 2])
+        pd = rng.randint(0, r - 1)
+        n, h, w = rng.randint(1, 4), rng.randint(r, 90), rng.randint(r, 90)
+        sms = rng.choice([8, 20, 152])
+        out = (ctypes.c_int * 13)()
+        if lib.conv_testing_fwd_plan(n, h, w, c, dt, r, r, f, _lib.pair((st, st)), _lib.pair((pd, pd)),
+                                     rng.randint(0, 1), sms, out) != OK:
+            continue
+        p = dict(zip(("bn", "bk", "stages", "smem", "tiles", "grid", "tmem", "epi", "bres", "srcb",
+                      "stgb", "loader", "pair"), list(out)))
+        if not p["pair"]:
+            assert p["loader"] != 0 or p["bn"] < 32 or p["loader"] == 3
+            continue
+        seen += 1
+        assert p["loader"] == 0 and p["bres"] == 0 and p["bn"] >= 32
+        ho, wo = (h + 2 * pd - r) // st + 1, (w + 2 * pd - r) // st + 1
+        nt = -(-f // p["bn"])
+        assert p["tiles"] == -(-(n * ho * wo) // 256) * nt
+        assert p["grid"] % 2 == 0 and 2 <= p["grid"] <= sms and p["grid"] <= 2 * p["tiles"]
+        assert 2 * p["bn"] <= p["tmem"] <= 512
+        assert p["smem"] <= 227 * 1024 and p["stages"] >= 2
+    assert seen > 100
+
+
 def test_cta_pair_plans(lib, monkeypatch):
     """CTA pairs (cta_group::2, 256-row tiles shared by two CTAs) when every
     pair of SMs gets at least 4 tiles and bn = 256; CONV_PAIR=1/0 force."""
