@@ -289,6 +289,43 @@ def test_residual_then_activation_order():
     np.testing.assert_allclose(y, np.maximum(plain + 0.5 * src, 0.0), rtol=1e-14, atol=1e-14)
 
 
+def test_transposed_zero_filter_gives_beta_times_source():
+    """conv_transposed_gpu, description (backward-data; the epilogue follows the
+    conv): with a zero filter the transposed conv contributes nothing, so the
+    output is exactly beta*source, for the scatter form and the point form."""
+    x = RNG.standard_normal((2, 3, 4, 3))
+    w = np.zeros((4, 4, 5, 3))                       # RSFC
+    Ho, Wo = (3 - 1) * 2 - 2 + 4 + 1, (4 - 1) * 2 - 2 + 4   # s = 2, p = 1, output padding (1, 0)
+    src = RNG.standard_normal((2, Ho, Wo, 5))
+    kw = dict(out_hw=(Ho, Wo), stride=(2, 2), padding=(1, 1), source=src, beta=-2.0)
+    y = oracle.conv_transposed(x, w, **kw)
+    assert np.array_equal(y, -2.0 * src)
+    pts = np.arange(y.size)
+    assert np.array_equal(oracle.conv_transposed_points(x, w, pts, **kw), (-2.0 * src).reshape(-1))
+
+
+@pytest.mark.parametrize("act", ["relu", "silu"])
+def test_transposed_residual_then_activation_matches_torch(act):
+    """act(conv_transpose2d(x) + beta*source) from PyTorch's fp64 conv_transpose2d,
+    at stride 2 with an output padding: the residual is added before the
+    activation, and beta scales only the source."""
+    from scipy.special import expit
+    x = RNG.standard_normal((2, 4, 3, 3))
+    w = RNG.standard_normal((4, 4, 2, 3))            # RSFC
+    Ho, Wo = (4 - 1) * 2 - 2 + 4 + 1, (3 - 1) * 2 - 2 + 4 + 1
+    src = RNG.standard_normal((2, Ho, Wo, 2))
+    beta = 0.75
+    plain = _torch_convT(x, w, (2, 2), (1, 1), (1, 1), (Ho, Wo))
+    v = plain + beta * src
+    ref = np.maximum(v, 0.0) if act == "relu" else v * expit(v)
+    kw = dict(out_hw=(Ho, Wo), stride=(2, 2), padding=(1, 1), source=src, beta=beta, act=act)
+    y = oracle.conv_transposed(x, w, **kw)
+    np.testing.assert_allclose(y, ref, rtol=1e-12, atol=1e-12)
+    pts = np.arange(y.size)
+    np.testing.assert_allclose(oracle.conv_transposed_points(x, w, pts, **kw), ref.reshape(-1),
+                               rtol=1e-12, atol=1e-12)
+
+
 def test_activations_against_library():
     from scipy.special import expit
     v = np.linspace(-30, 30, 601)
