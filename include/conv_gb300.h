@@ -213,8 +213,12 @@ conv_status_t conv_transposed_packed(const void* input, int n, int h, int w, int
  * (CONV_NOALLOC_SCRATCH_BYTES) that lives in device memory of every GPU that
  * loads the library until the process exits.  Filters whose packed size plus
  * CONV_STATUS_BYTES exceeds it return CONV_ERR_WORKSPACE_TOO_SMALL before
- * any CUDA call.  The first call on a device resolves the scratch address
- * for that device; make that first call before any stream capture.  Every
+ * any CUDA call (the packed filter spans C_in / num_groups channels, so
+ * grouped and depthwise filters are sized as conv2d_fwd sizes them; a
+ * num_groups that does not divide C_in returns CONV_ERR_INVALID_VALUE).
+ * Each call looks up the scratch address of the current device (a host-side
+ * query); the first call on a device may also load the library's device
+ * code there, so make that first call before any stream capture.  Every
  * call shares the one array: calls that overlap on the GPU (different
  * streams, or devices sharing nothing but the library) race, so serialise
  * them.  The status word is cleared at the start of each call; a bounded

@@ -332,6 +332,26 @@ def test_noalloc_rejects_filters_beyond_its_scratch(lib):
     assert _lib.CONV_NOALLOC_SCRATCH_BYTES == 8 << 20
 
 
+def test_noalloc_sizes_grouped_filters_by_channels_per_group(lib):
+    """A depthwise 3x3 filter over 1024 channels packs to 1024 x 9 x 1 values
+    (18 KB), well within the scratch; sized by the total C_in it would claim
+    ~18.9 MB and be rejected.  The output size is deliberately inconsistent so
+    that the call stops in conv2d_fwd's shape check and never launches,
+    whether or not a GPU is present (without one the scratch lookup fails
+    first with CONV_ERR_CUDA)."""
+    assert lib.conv2d_workspace_size(3, 3, 1, 1024, BF16) <= _lib.CONV_NOALLOC_SCRATCH_BYTES
+    assert lib.conv2d_workspace_size(3, 3, 1024, 1024, BF16) > _lib.CONV_NOALLOC_SCRATCH_BYTES
+    status = lib.conv2d_fwd_noalloc(A, 1, 8, 8, 1024, BF16, B, 3, 3, 1024, 0, C, 9, 8, BF16,
+                                    _lib.pair((1, 1)), _lib.pair((1, 1)), _lib.pair((1, 1)), 1024, 0,
+                                    None, 0.0, 0, None)
+    assert status in (INVALID, cg.CONV_ERR_CUDA)
+    # A group count that does not divide C_in is rejected before any CUDA call.
+    status = lib.conv2d_fwd_noalloc(A, 1, 8, 8, 1024, BF16, B, 3, 3, 1024, 0, C, 8, 8, BF16,
+                                    _lib.pair((1, 1)), _lib.pair((1, 1)), _lib.pair((1, 1)), 3, 0,
+                                    None, 0.0, 0, None)
+    assert status == INVALID
+
+
 def test_gather_loader_plans(lib):
     """Channel rows TMA cannot address (C_in * elt not a multiple of 16 bytes,
     or under 32) go to the gather loader: 128-byte k-blocks over runs of

@@ -1587,28 +1587,18 @@ namespace {
 constexpr size_t kNoAllocScratchBytes = size_t(8) << 20;  // 8 MiB
 __device__ __align__(256) uint8_t g_noalloc_scratch[kNoAllocScratchBytes];
 
-// Device address of g_noalloc_scratch per device (host code must not use the
-// symbol itself as a pointer).  Resolved once per device by the first call
-// made with that device current.
+// Device address of g_noalloc_scratch in the current device's context (host
+// code must not use the symbol itself as a pointer).  Looked up on every call:
+// the lookup is host-only and cheap, and an address cached across calls could
+// outlive the context it belongs to (after cudaDeviceReset, say).
 void* noalloc_scratch_ptr(conv_status_t* st) {
-  static std::mutex mu;
-  static void* ptrs[64] = {nullptr};
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
+  void* p = nullptr;
+  if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) {
     *st = CONV_ERR_CUDA;
     return nullptr;
   }
-  std::lock_guard<std::mutex> lock(mu);
-  if (!ptrs[dev]) {
-    void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) {
-      *st = CONV_ERR_CUDA;
-      return nullptr;
-    }
-    ptrs[dev] = p;
-  }
   *st = CONV_OK;
-  return ptrs[dev];
+  return p;
 }
 
 }  // namespace
@@ -1786,8 +1776,8 @@ conv_status_t conv_check_device_status(void* workspace, void* stream, unsigned i
 }
 
 // See include/conv_gb300.h.  Validates the size against the scratch first
-// (no CUDA call on rejection), resolves the scratch address (first call per
-// device), clears the status word, then runs the ordinary conv2d_fwd path with
+// (no CUDA call on rejection), resolves the scratch address of the current
+// device, clears the status word, then runs the ordinary conv2d_fwd path with
 // the scratch standing in for the workspace.
 conv_status_t conv2d_fwd_noalloc(const void* input, int n, int h, int w, int c_in,
                                  conv_dtype_t in_dtype, const void* filter, int r, int s, int c_out,
@@ -1798,7 +1788,9 @@ conv_status_t conv2d_fwd_noalloc(const void* input, int n, int h, int w, int c_i
                                  void* stream) {
   if (r <= 0 || s <= 0 || c_in <= 0 || c_out <= 0 || !known_dtype(in_dtype))
     return CONV_ERR_INVALID_VALUE;
-  const size_t need = conv2d_workspace_size(r, s, c_in, c_out, in_dtype);
+  if (num_groups < 1 || c_in % num_groups != 0) return CONV_ERR_INVALID_VALUE;
+  // The packed filter spans C_in / num_groups channels, as in conv2d_fwd.
+  const size_t need = conv2d_workspace_size(r, s, c_in / num_groups, c_out, in_dtype);
   if (need > kNoAllocScratchBytes) return CONV_ERR_WORKSPACE_TOO_SMALL;
   conv_status_t st = CONV_OK;
   void* scratch = noalloc_scratch_ptr(&st);
