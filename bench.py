@@ -2,21 +2,31 @@
 """Benchmark of the implicit-GEMM convolution path on GB300.
 
 One step = one pass of the workload's hot path over one batch of synthetic
-input.  The default workload is the ResNet-style bf16 block: the 3x3 stride-1
-conv 32x56x56x64 -> 64 with fused residual (beta = 1) followed by the 3x3
-stride-2 downsample 32x56x56x64 -> 32x28x28x128.  Filters are packed once
-before timing (the pack is timed separately and reported as pack_us).
+input.  The default workload, ``baseline``, is every convolution the
+benchmark configurations name, at full size, one after the other:
 
-Timing: W warm-up steps, then K steps, each preceded by an L2 flush (a write
-of max(2 x L2, 256 MiB), outside the events).  Each step is bracketed by CUDA
-events on the launch stream; its launches follow each other directly (a conv
-may set up while the previous one drains: programmatic dependent launch).  A
-barrier + synchronize bracket the region; the step time is the max over
-ranks.  Per-kernel durations for the roofline come from a second loop in
-which every launch has its own events.  One JSON line on rank 0.
+  tiny_bf16         bf16 16x16x16 -> 16, 3x3 s1 p1
+  resnet_bf16       bf16 32x56x56x64 -> 64, 3x3 s1 p1, + 1.0*source
+  resnet_down_bf16  bf16 32x56x56x64 -> 32x28x28x128, 3x3 s2 p1
+  fp8_res           e4m3 16x64x64x320 -> 320 (bf16 out), 3x3 FCRS s1 p1, + 0.5*source
+  vae_silu_bf16     bf16 1x256x256x512 -> 512, 3x3 s1 p1, SiLU
+  vae_head_bf16     bf16 1x512x512x128 -> 3, 3x3 s1 p1
+  convT_f16         f16 transposed 8x32x32x256 -> 8x64x64x128, 4x4 RSFC s2 p1, ReLU
+  fwd5x5_f16        f16 8x128x128x128 -> 8x64x64x128, 5x5 s2 p2
+
+Each conv is preceded by an L2 flush (a write of max(2 x L2, 256 MiB)) and
+bracketed by its own CUDA events on the launch stream; the flush lies
+outside the events.  The step time is the sum of the convs' event times.
+``value`` is the step's algorithmic FLOPs over the step time (whole job: all
+ranks' FLOPs over the slowest rank's time); ``per_kernel`` gives each conv's
+time, TFLOP/s, GB/s and fraction of its own roofline; ``roofline`` is the
+dominant conv's (the one with the largest share of the step).  Filters are
+packed once before timing (pack_us).  Other workloads: ``resnet_block`` (the
+3x3 residual conv then the stride-2 downsample, back to back after one flush
+per step) or any single workload name.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                  [--workload resnet_block|<one of synthetic.WORKLOADS>]
+                  [--workload baseline|resnet_block|<one of synthetic.WORKLOADS>]
 
 --impl reference times the CPU oracle (single-threaded fp64 direct loops) on
 a bounded sample of the same workload per step, on the host cores.
@@ -83,9 +93,21 @@ def load_peaks():
 
 def workload_cases(name):
     from transposed_conv_implicit_gb300 import synthetic
+    if name == "baseline":
+        return [synthetic.WORKLOADS[n] for n in synthetic.BASELINE_SET]
     if name == "resnet_block":
         return [synthetic.WORKLOADS[n] for n in synthetic.RESNET_BLOCK]
     return [synthetic.WORKLOADS[name]]
+
+
+def workload_dtype(cases) -> str:
+    dtypes = sorted(set(c.dtype for c in cases))
+    return dtypes[0] if len(dtypes) == 1 else "/".join(dtypes) + " (per conv, fp32 accumulate)"
+
+
+def flush_each_conv(name) -> bool:
+    """The baseline set times every conv on its own, after its own flush."""
+    return name == "baseline"
 
 
 def describe(cases):
@@ -165,33 +187,38 @@ class ClockSampler:
 
 
 # ----------------------------------------------------------------------------- CPU oracle timing
-def oracle_sample_seconds(cases, inputs, budget_s, min_s=0.0):
-    """Run the oracle (as it stands) over whole images of each case, image by
-    image, until `budget_s` is spent or the batch is done.  Returns
-    (flops, seconds, images)."""
-    import numpy as np
+def decode_inputs(cases, inputs):
+    """The oracle's fp64 view of each case's input, filter and source."""
     import oracle
     dec = []
     for case, inp in zip(cases, inputs):
-        x = oracle.decode(_bits(inp["x"]), case.dtype)
-        w = oracle.decode(_bits(inp["w"]), case.dtype)
-        src = oracle.decode(_bits(inp["src"]), case.out_dtype) if inp["src"] is not None else None
-        dec.append((x, w, src))
-    flops = 0
-    images = 0
+        dec.append((oracle.decode(_bits(inp["x"]), case.dtype),
+                    oracle.decode(_bits(inp["w"]), case.dtype),
+                    oracle.decode(_bits(inp["src"]), case.out_dtype) if inp["src"] is not None
+                    else None))
+    return dec
+
+
+def oracle_sample_seconds(cases, inputs, budget_s):
+    """Time the oracle (as it stands) on seeded output pixels (all channels)
+    of every conv of the workload, repeated while `budget_s` lasts.
+    Returns (flops, seconds, pixels per conv)."""
+    import numpy as np
+    dec = decode_inputs(cases, inputs)
+    rng = np.random.default_rng(4321)
     t0 = time.perf_counter()
-    N = min(c.N for c in cases)
-    # Whole images, in order; passes over the batch repeat until the budget
-    # is spent (a small batch finishes in less than the budget).
-    while time.perf_counter() - t0 < budget_s:
-        for i in range(N):
-            for case, (x, w, src) in zip(cases, dec):
-                _oracle_one(case, x[i:i + 1], w, None if src is None else src[i:i + 1])
-                flops += case.flops // case.N
-            images += 1
-            if time.perf_counter() - t0 >= budget_s:
-                break
-    return flops, time.perf_counter() - t0, images
+    oracle_points_step(cases, dec, 4, rng)
+    per_pix = max((time.perf_counter() - t0) / 4, 1e-9)
+    npix = max(1, int(budget_s / 4 / per_pix))
+    flops = 0
+    pixels = 0
+    t0 = time.perf_counter()
+    while True:
+        flops += oracle_points_step(cases, dec, npix, rng)
+        pixels += npix
+        if time.perf_counter() - t0 >= budget_s:
+            break
+    return flops, time.perf_counter() - t0, pixels
 
 
 def oracle_points_step(cases, dec, npix, rng):
@@ -212,17 +239,6 @@ def oracle_points_step(cases, dec, npix, rng):
 def _bits(t):
     from transposed_conv_implicit_gb300 import synthetic
     return synthetic.raw_bits(t)
-
-
-def _oracle_one(case, x, w, src):
-    import oracle
-    st, pd = (case.stride,) * 2, case.pads
-    if case.kind == "transposed":
-        return oracle.conv_transposed(x, w, out_hw=(case.Ho, case.Wo), stride=st, padding=pd,
-                                      source=src, beta=case.beta, act=case.epilogue)
-    return oracle.conv2d_fwd(x, w, filter_is_fcrs=case.filter_layout == "FCRS", stride=st,
-                             padding=pd, dilation=case.dilations, source=src, beta=case.beta,
-                             act=case.epilogue, groups=case.groups)
 
 
 def _oracle_points(case, x, w, src, pts):
@@ -287,10 +303,7 @@ def run_reference(args, world, rank):
     from transposed_conv_implicit_gb300 import synthetic
     cases = workload_cases(args.workload)
     inputs = [synthetic.make_inputs(c) for c in cases]
-    dec = []
-    for case, inp in zip(cases, inputs):
-        dec.append((oracle.decode(_bits(inp["x"]), case.dtype), oracle.decode(_bits(inp["w"]), case.dtype),
-                    oracle.decode(_bits(inp["src"]), case.out_dtype) if inp["src"] is not None else None))
+    dec = decode_inputs(cases, inputs)
     rng = np.random.default_rng(1234)
     # Size the per-step sample so the whole run stays within about two minutes.
     t0 = time.perf_counter()
@@ -309,8 +322,8 @@ def run_reference(args, world, rank):
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": secs / args.steps * 1e3,
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": cases[0].dtype,
-        "data": "synthetic",
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": workload_dtype(cases), "data": "synthetic",
         "config": {"workload": args.workload + ": " + describe(cases),
                    "sample": "%d output pixels x all channels per conv per step" % npix},
         "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": 1, "kind": "oracle",
@@ -323,6 +336,15 @@ def run_reference(args, world, rank):
 
 
 # ----------------------------------------------------------------------------- our arm
+def conv_bound(case, peaks):
+    """(bound, tensor peak TFLOP/s) of one conv: HBM when its arithmetic
+    intensity is below the ridge of its dtype's tensor peak, else tensor.
+    fp8 takes twice the measured bf16 peak (the nominal dense ratio)."""
+    tensor_peak = peaks["bf16_tflops"] * (2.0 if case.dtype == "f8e4m3" else 1.0)
+    ridge = tensor_peak * 1e12 / (peaks["hbm_gbs"] * 1e9)
+    return ("hbm" if case.flops / case.bytes < ridge else "tensor"), tensor_peak
+
+
 def run_ours(args, world, rank, local):
     import torch
     import transposed_conv_implicit_gb300 as cg
@@ -333,6 +355,7 @@ def run_ours(args, world, rank, local):
     cases = workload_cases(args.workload)
     inputs = [synthetic.make_inputs(c) for c in cases]
     stream = torch.cuda.current_stream(dev)
+    per_conv_flush = flush_each_conv(args.workload)
 
     # Device-resident tensors, packed filters, bound launches.
     calls, outs, packed = [], [], []
@@ -372,23 +395,39 @@ def run_ours(args, world, rank, local):
     l2 = int(getattr(props, "L2_cache_size", 128 << 20))
     flush = torch.empty(max(2 * l2, 256 << 20), dtype=torch.uint8, device=dev)
 
-    def step():
-        for call in calls:
-            call()
+    def new_events():
+        n = len(calls) if per_conv_flush else 1
+        return [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                for _ in range(n)]
 
+    def step(evs):
+        """One step.  Baseline set: each conv after its own flush, inside its own
+        events.  Otherwise: one flush, then the convs back to back inside one
+        pair of events (a conv may set up while the previous one drains:
+        programmatic dependent launch)."""
+        if per_conv_flush:
+            for call, (e0, e1) in zip(calls, evs):
+                flush.fill_(1)
+                e0.record(stream)
+                call()
+                e1.record(stream)
+        else:
+            flush.fill_(1)
+            evs[0][0].record(stream)
+            for call in calls:
+                call()
+            evs[0][1].record(stream)
+
+    warm_ev = new_events()
     for _ in range(args.warmup):
-        flush.fill_(1)
-        step()
+        step(warm_ev)
     torch.cuda.synchronize(dev)
     status, bits = cg.conv_check_device_status(workspace)
     if status != 0:
         raise RuntimeError("device status after warm-up: %s (bits %d)" % (cg.conv_status_string(status), bits))
 
-    # Timed region: K steps, each after an L2 flush (outside the events); the
-    # step's launches are back to back, so a conv may start its set-up while
-    # the previous one drains (programmatic dependent launch).
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-          for _ in range(args.steps)]
+    # Timed region: K steps, flushes outside the events.
+    ev = [new_events() for _ in range(args.steps)]
     sampler = ClockSampler(local) if rank == 0 or world > 1 else None
     if sampler:
         sampler.start()
@@ -397,10 +436,7 @@ def run_ours(args, world, rank, local):
     torch.cuda.synchronize(dev)
     wall0 = time.perf_counter()
     for k in range(args.steps):
-        flush.fill_(1)
-        ev[k][0].record(stream)
-        step()
-        ev[k][1].record(stream)
+        step(ev[k])
     torch.cuda.synchronize(dev)
     wall = time.perf_counter() - wall0
     dist_barrier(world)
@@ -408,71 +444,110 @@ def run_ours(args, world, rank, local):
     status, bits = cg.conv_check_device_status(workspace)
     if status != 0:
         raise RuntimeError("device status after timing: %s (bits %d)" % (cg.conv_status_string(status), bits))
-    step_ms = [a.elapsed_time(b) for a, b in ev]
+    step_ms = [sum(a.elapsed_time(b) for a, b in ev[k]) for k in range(args.steps)]
 
-    # Per-kernel durations (for the roofline): every launch bracketed by its
-    # own events on the launch stream, each step after an L2 flush.
-    kreps = max(10, min(args.steps, 100))
-    kev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(calls) + 1)] for _ in range(kreps)]
-    for k in range(kreps):
-        flush.fill_(1)
-        for i, call in enumerate(calls):
-            kev[k][i].record(stream)
-            call()
-        kev[k][len(calls)].record(stream)
-    torch.cuda.synchronize(dev)
-    per_kernel_ms = [[kev[k][i].elapsed_time(kev[k][i + 1]) for k in range(kreps)]
-                     for i in range(len(calls))]
+    if per_conv_flush:
+        per_kernel_ms = [[ev[k][i][0].elapsed_time(ev[k][i][1]) for k in range(args.steps)]
+                         for i in range(len(calls))]
+    else:
+        # Per-kernel durations (for the roofline): every launch bracketed by
+        # its own events on the launch stream, each step after an L2 flush.
+        kreps = max(10, min(args.steps, 100))
+        kev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(calls) + 1)]
+               for _ in range(kreps)]
+        for k in range(kreps):
+            flush.fill_(1)
+            for i, call in enumerate(calls):
+                kev[k][i].record(stream)
+                call()
+            kev[k][len(calls)].record(stream)
+        torch.cuda.synchronize(dev)
+        per_kernel_ms = [[kev[k][i].elapsed_time(kev[k][i + 1]) for k in range(kreps)]
+                         for i in range(len(calls))]
     ms_per_step, value = whole_job_value(step_ms, sum(c.flops for c in cases), world, dev)
 
-    # Roofline of the dominant kernel (largest share of the step).
+    # Host cost of one bound C-ABI call (ctypes with pre-marshalled arguments,
+    # the library's prepared-call cache lookup and the launch), and the wall
+    # time from the call to a completed synchronize.
+    host_us, sync_us = [], []
+    for call in calls:
+        ts = []
+        for rep in range(60):
+            t0 = time.perf_counter()
+            call()
+            ts.append(time.perf_counter() - t0)
+            if rep % 10 == 9:
+                torch.cuda.synchronize(dev)
+        torch.cuda.synchronize(dev)
+        host_us.append(statistics.median(ts[10:]) * 1e6)
+        ts = []
+        for rep in range(20):
+            torch.cuda.synchronize(dev)
+            t0 = time.perf_counter()
+            call()
+            torch.cuda.synchronize(dev)
+            ts.append(time.perf_counter() - t0)
+        sync_us.append(statistics.median(ts[5:]) * 1e6)
+
+    # Roofline of the dominant kernel (largest share of the step) and every
+    # conv's fraction of its own bound.
     mean_k = [statistics.fmean(v) for v in per_kernel_ms]
     dom = max(range(len(cases)), key=lambda i: mean_k[i])
-    dcase = cases[dom]
     peaks, peak_src = load_peaks()
-    ridge_flop_per_byte = peaks["bf16_tflops"] * 1e12 / (peaks["hbm_gbs"] * 1e9)
-    dt_mult = 2.0 if dcase.dtype == "f8e4m3" else 1.0
-    if dcase.flops / dcase.bytes < ridge_flop_per_byte * dt_mult:
-        achieved = dcase.bytes / (mean_k[dom] * 1e-3) / 1e9
-        roof = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s"}
-    else:
-        achieved = dcase.flops / (mean_k[dom] * 1e-3) / 1e12
-        roof = {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"] * dt_mult,
-                "unit": "TFLOP/s"}
-    roof["frac"] = roof["achieved"] / roof["peak"]
-    roof["peak_source"] = peak_src
-    roof["kernel"] = dcase.name
-    roof["traffic"] = lookup_traffic(dcase.name)
-
     per_kernel = {}
     for i, c in enumerate(cases):
         us = mean_k[i] * 1e3
-        per_kernel[c.name] = {"us": round(us, 3), "tflops": round(c.flops / (us * 1e-6) / 1e12, 2),
-                              "gbs": round(c.bytes / (us * 1e-6) / 1e9, 1),
-                              "p10_us": round(_pct(per_kernel_ms[i], 10) * 1e3, 3),
-                              "p90_us": round(_pct(per_kernel_ms[i], 90) * 1e3, 3)}
+        bound, tpeak = conv_bound(c, peaks)
+        tf = c.flops / (us * 1e-6) / 1e12
+        gbs = c.bytes / (us * 1e-6) / 1e9
+        floor_us = max(c.bytes / (peaks["hbm_gbs"] * 1e9), c.flops / (tpeak * 1e12)) * 1e6
+        per_kernel[c.name] = {
+            "us": round(us, 3), "tflops": round(tf, 2), "gbs": round(gbs, 1),
+            "bound": bound if floor_us >= 1.0 else "launch",
+            "frac": round(gbs / peaks["hbm_gbs"] if bound == "hbm" else tf / tpeak, 4),
+            "frac_hbm": round(gbs / peaks["hbm_gbs"], 4), "frac_tensor": round(tf / tpeak, 4),
+            "tensor_peak_tflops": tpeak,
+            "p10_us": round(_pct(per_kernel_ms[i], 10) * 1e3, 3),
+            "p90_us": round(_pct(per_kernel_ms[i], 90) * 1e3, 3),
+            "host_us_per_call": round(host_us[i], 2), "call_to_sync_us": round(sync_us[i], 2),
+            "traffic": lookup_traffic(c.name)}
+    dcase = cases[dom]
+    dbound, dpeak = conv_bound(dcase, peaks)
+    if dbound == "hbm":
+        roof = {"bound": "hbm", "achieved": dcase.bytes / (mean_k[dom] * 1e-3) / 1e9,
+                "peak": peaks["hbm_gbs"], "unit": "GB/s"}
+    else:
+        roof = {"bound": "tensor", "achieved": dcase.flops / (mean_k[dom] * 1e-3) / 1e12,
+                "peak": dpeak, "unit": "TFLOP/s"}
+    roof["frac"] = roof["achieved"] / roof["peak"]
+    roof["peak_source"] = peak_src
+    roof["peak_kind"] = "burst (each conv timed on its own)" if dbound == "tensor" else "copy"
+    roof["kernel"] = dcase.name
+    roof["traffic"] = lookup_traffic(dcase.name)
 
     e2e = run_e2e(args, cases, inputs, dev, stream) if not args.no_e2e else None
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        flops, secs, images = oracle_sample_seconds(cases, inputs, args.cpu_budget)
+        flops, secs, pixels = oracle_sample_seconds(cases, inputs, args.cpu_budget)
         cpu = {"value": flops / secs / 1e12, "unit": "TFLOP/s", "cores": 1, "kind": "oracle",
-               "sample": "%d whole images (batch of %d, in order, repeated while the budget "
-                         "lasts) of every conv in the workload, fp64 single-threaded direct "
-                         "loops, %.1f s" % (images, min(c.N for c in cases), secs)}
+               "sample": "%d seeded output pixels (all channels) of each of the %d convs, fp64 "
+                         "single-threaded direct loops, %.1f s" % (pixels, len(cases), secs)}
 
     if rank != 0:
         return 0
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": cases[0].dtype, "data": "synthetic",
+        "scaling": "weak", "vs_baseline": None,
+        "dtype": workload_dtype(cases),
+        "data": "synthetic",
         "config": {"workload": args.workload + ": " + describe(cases),
-                   "l2": "flushed before every step (write of %d MiB), flush outside the events"
-                         % (flush.numel() >> 20),
+                   "l2": "flushed before every %s (write of %d MiB), flush outside the events"
+                         % ("conv" if per_conv_flush else "step", flush.numel() >> 20),
+                   "step_time": "sum of the convs' own event times" if per_conv_flush
+                                else "events around the whole step",
                    "filters": "packed once before timing",
-                   "per_kernel_timing": "separate loop, each launch bracketed by events",
                    "parallelism": "replicas" if world > 1 else "single GPU",
                    "gpu": props.name, "sms": props.multi_processor_count},
         "roofline": roof,
@@ -633,7 +708,7 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=1000)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
-    ap.add_argument("--workload", default="resnet_block")
+    ap.add_argument("--workload", default="baseline")
     ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle CPU baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")

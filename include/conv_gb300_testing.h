@@ -59,6 +59,17 @@ conv_status_t conv_testing_fwd_plan(int n, int h, int w, int c_in, conv_dtype_t 
                                     const int symmetric_padding[2], int has_residual, int num_sms,
                                     int out[13]);
 
+/* Read the CONV_* tuning overrides from the environment again (the library
+ * reads them once, on first use) and invalidate every cached prepared call.
+ * For tests that change an override between calls; not to be called while
+ * other threads are inside the library. */
+void conv_testing_reload_tuning(void);
+
+/* Process-wide counts of calls that found their prepared launch in the
+ * library's cache (same entry point, arguments, device and tuning) and of
+ * calls that had to plan and encode afresh.  Either pointer may be NULL. */
+void conv_testing_cache_stats(unsigned long long* hits, unsigned long long* misses);
+
 #ifdef __cplusplus
 }
 #endif

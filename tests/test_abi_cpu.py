@@ -185,7 +185,7 @@ def test_tile_plans_for_the_workloads(lib):
         assert q["smem"] <= 227 * 1024 and q["stages"] >= 3 and q["tmem"] <= 512
 
 
-def test_row_tap_gate(lib, monkeypatch):
+def test_row_tap_gate(lib, tuning):
     """Few output channels (S * C_out <= 32), stride 1, dilation 1, 128-byte
     channel blocks and more than one tap take the row-tap kernel; the rest,
     or CONV_ROWTAP=-1, the implicit GEMM's masked edge tile."""
@@ -197,18 +197,18 @@ def test_row_tap_gate(lib, monkeypatch):
     assert _plan(lib, 1, 40, 40, 64, BF16, 3, 3, 2, 1)["loader"] != 3       # stride 2
     assert _plan(lib, 1, 40, 40, 32, BF16, 3, 3, 1, 1)["loader"] != 3       # 64-byte channel rows
     assert _plan(lib, 1, 40, 40, 64, BF16, 1, 3, 1, 0)["loader"] != 3       # a single tap
-    monkeypatch.setenv("CONV_ROWTAP", "-1")
+    tuning("CONV_ROWTAP", "-1")
     p = _plan(lib, 1, 512, 512, 128, BF16, 3, 3, 1, 1, sms=152)              # masked 16-wide tile
     assert (p["loader"], p["bn"], p["bk"], p["tiles"], p["epi"], p["bres"]) == (0, 16, 64, 1024, 0, 1)
 
 
-def test_row_tap_plan_invariants(lib, monkeypatch):
+def test_row_tap_plan_invariants(lib, tuning):
     """Over many eligible shapes: the band fits the TMEM budget (two buffers
     of g16 * (band + 2R - 2) columns within the allocation), the tile count
     covers every output row and column segment, and shared memory fits."""
     import random
-    monkeypatch.delenv("CONV_ROWTAP", raising=False)
-    monkeypatch.delenv("CONV_ROWTAP_BAND", raising=False)
+    tuning("CONV_ROWTAP", None)
+    tuning("CONV_ROWTAP_BAND", None)
     rng = random.Random(7)
     seen = 0
     for _ in range(300):
@@ -239,13 +239,13 @@ def test_row_tap_plan_invariants(lib, monkeypatch):
     assert seen > 100
 
 
-def test_cta_pair_plan_invariants(lib, monkeypatch):
+def test_cta_pair_plan_invariants(lib, tuning):
     """CTA pairs forced on over many shapes: 256-row tiles over every C_out
     tile, an even grid of at most the SMs, accumulators of 2 x bn columns
     within TMEM, shared memory within the limit; never with the row window
     or the gather loader."""
     import random
-    monkeypatch.setenv("CONV_PAIR", "1")
+    tuning("CONV_PAIR", "1")
     rng = random.Random(11)
     seen = 0
     for _ in range(300):
@@ -277,42 +277,42 @@ def test_cta_pair_plan_invariants(lib, monkeypatch):
     assert seen > 100
 
 
-def test_cta_pair_plans(lib, monkeypatch):
+def test_cta_pair_plans(lib, tuning):
     """CTA pairs (cta_group::2, 256-row tiles shared by two CTAs) when every
     pair of SMs gets at least 4 tiles and bn = 256; CONV_PAIR=1/0 force."""
-    monkeypatch.delenv("CONV_PAIR", raising=False)
+    tuning("CONV_PAIR", None)
     vae = (1, 256, 256, 512, BF16, 3, 512, 1, 1)
     p = _plan(lib, *vae, sms=152)
     assert (p["pair"], p["bn"], p["tiles"], p["grid"], p["tmem"]) == (1, 256, 512, 152, 512)
     f5 = (8, 128, 128, 128, 1, 5, 128, 2, 2)                     # 128 pair tiles < 4 x 76
     assert _plan(lib, *f5, sms=152)["pair"] == 0
     assert _plan(lib, *vae, sms=1000)["pair"] == 0              # too few tiles per pair
-    monkeypatch.setenv("CONV_PAIR", "1")
+    tuning("CONV_PAIR", "1")
     q = _plan(lib, *f5, sms=152)
     assert (q["pair"], q["tiles"], q["grid"], q["tmem"]) == (1, 128, 152, 256)
     assert _plan(lib, 3, 30, 30, 64, BF16, 3, 48, 2, 1, sms=5)["grid"] == 4  # even grid: 2 pairs
     assert _plan(lib, 32, 56, 56, 64, BF16, 3, 64, 1, 1, res=1, sms=152)["pair"] == 0  # row window
     assert _plan(lib, 32, 224, 224, 3, BF16, 7, 64, 2, 2, sms=152)["pair"] == 0       # gather
     assert _plan(lib, 2, 9, 9, 64, BF16, 3, 16, 2, 1, sms=152)["pair"] == 0           # bn < 32
-    monkeypatch.setenv("CONV_PAIR", "0")
+    tuning("CONV_PAIR", "0")
     assert _plan(lib, *vae, sms=152)["pair"] == 0
 
 
-def test_measured_planner_choices(lib, monkeypatch):
+def test_measured_planner_choices(lib, tuning):
     """Plans the measurements picked (each alternative was timed on GB300 and
     ran slower): 256-row gather tiles for the RGB stem (77.8 vs 90.1 us on
     128-row tiles), a 5-stage ring with one residual buffer for the fp8 conv
     (4 stages and two buffers: 75.8 vs ~73 us), 256-row bn = 128 tiles for the
     wave-quantised fwd5x5 (128-row: 42.0 vs 34.8 us)."""
     for name in ("CONV_TILE_M", "CONV_TILE_N", "CONV_PAIR", "CONV_SRC_BUFS", "CONV_MAX_STAGES"):
-        monkeypatch.delenv(name, raising=False)
+        tuning(name, None)
     stem = _plan(lib, 32, 224, 224, 3, BF16, 7, 64, 2, 3, sms=152)
     assert (stem["loader"], stem["tiles"], stem["tmem"]) == (2, 32 * 112 * 112 // 256, 256)
     fp8 = _plan(lib, 16, 64, 64, 320, F8, 3, 320, 1, 1, res=1, sms=152)
     assert (fp8["stages"], fp8["srcb"], fp8["pair"]) == (5, 1, 0)
     f5 = _plan(lib, 8, 128, 128, 128, F16, 5, 128, 2, 2, sms=152)
     assert (f5["bn"], f5["tiles"], f5["pair"]) == (128, 128, 0)
-    monkeypatch.setenv("CONV_SRC_BUFS", "1")   # the override still caps the buffers
+    tuning("CONV_SRC_BUFS", "1")   # the override still caps the buffers
     assert _plan(lib, 16, 64, 64, 320, F8, 3, 320, 1, 1, res=1, sms=152)["srcb"] == 1
 
 
@@ -375,3 +375,22 @@ def test_gather_packed_filter_bytes(lib):
     assert lib.conv2d_packed_filter_bytes(3, 3, 5, 4, F8) == 4 * 3 * 16
     assert lib.conv2d_packed_filter_bytes(1, 1, 8, 16, BF16) == 16 * 16
     assert lib.conv2d_workspace_size(7, 7, 3, 64, BF16) == 256 + 64 * 7 * 48
+
+
+def _cache_stats(lib):
+    hits, misses = ctypes.c_ulonglong(0), ctypes.c_ulonglong(0)
+    lib.conv_testing_cache_stats(ctypes.byref(hits), ctypes.byref(misses))
+    return hits.value, misses.value
+
+
+def test_failed_calls_are_never_cached(lib):
+    """The prepared-call cache stores only successful preparations: a call
+    rejected by validation (or unable to reach a device) misses every time."""
+    h0, m0 = _cache_stats(lib)
+    for _ in range(3):
+        status = lib.conv2d_fwd_packed(A, 1, 8, 8, 64, BF16, B, 3, 3, 64, C, 9, 8, BF16,
+                                       _lib.pair((1, 1)), _lib.pair((1, 1)), _lib.pair((1, 1)), 1, 0,
+                                       None, 0.0, 0, WS, 256, None)
+        assert status == INVALID   # Ho = 9 does not match the shape
+    h1, m1 = _cache_stats(lib)
+    assert (h1 - h0, m1 - m0) == (0, 3)

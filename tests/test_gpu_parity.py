@@ -182,10 +182,10 @@ def test_small_case_every_element(case):
 @pytest.mark.parametrize("case", [c for c in SMALL_FWD if c.name in (
     "b_cout1", "b_cout3_head", "e_cout3", "rt_b_cout8_g32", "rt_h_1x3_cout4")],
     ids=lambda c: c.name)
-def test_masked_edge_tile_without_row_tap(case, monkeypatch):
+def test_masked_edge_tile_without_row_tap(case, tuning):
     """The same small-C_out convs on the implicit GEMM's masked edge tile (the
     row-tap kernel switched off)."""
-    monkeypatch.setenv("CONV_ROWTAP", "-1")
+    tuning("CONV_ROWTAP", "-1")
     inp = synthetic.make_inputs(case)
     out = H.run_gpu(case, inp)
     torch.cuda.synchronize()
@@ -261,10 +261,10 @@ def _pair_cases():
 
 
 @pytest.mark.parametrize("case", _pair_cases(), ids=lambda c: c.name)
-def test_cta_pair_every_element(case, monkeypatch):
+def test_cta_pair_every_element(case, tuning):
     """CTA pairs forced on (clusters of two CTAs, cta_group::2 MMAs over
     256-row tiles): every element against the oracle; integer cases bit-exact."""
-    monkeypatch.setenv("CONV_PAIR", "1")
+    tuning("CONV_PAIR", "1")
     inp = synthetic.make_inputs(case)
     out = H.run_gpu(case, inp)
     torch.cuda.synchronize()

@@ -37,7 +37,8 @@ EXPORTS = (
     "conv_transposed_packed_filter_bytes", "conv_transposed_workspace_size",
     "conv_transposed_pack_filter", "conv_transposed", "conv_transposed_packed",
     "conv_check_device_status", "conv_testing_set_wait_fault", "conv_testing_im2col_tile",
-    "conv_testing_fwd_plan", "conv2d_fwd_noalloc",
+    "conv_testing_fwd_plan", "conv2d_fwd_noalloc", "conv_testing_reload_tuning",
+    "conv_testing_cache_stats",
 )
 
 
@@ -83,6 +84,10 @@ def _declare(lib):
     lib.conv_testing_im2col_tile.restype = I
     lib.conv_testing_fwd_plan.argtypes = [I, I, I, I, I, I, I, I, IP, IP, I, I, IP]
     lib.conv_testing_fwd_plan.restype = I
+    lib.conv_testing_reload_tuning.argtypes = []
+    lib.conv_testing_reload_tuning.restype = None
+    lib.conv_testing_cache_stats.argtypes = [ctypes.POINTER(U64), ctypes.POINTER(U64)]
+    lib.conv_testing_cache_stats.restype = None
     return lib
 
 

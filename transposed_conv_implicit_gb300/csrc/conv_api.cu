@@ -39,12 +39,57 @@ int elt_bytes(conv_dtype_t d) { return d == CONV_DTYPE_F8E4M3 ? 1 : 2; }
 // choose): CONV_TILE_M (128 or 256), CONV_TILE_N (a multiple of 16, <= 256),
 // CONV_FILTER_RESIDENT (0 forbids keeping the filter in shared memory),
 // CONV_MAX_STAGES (caps the operand ring), CONV_SRC_BUFS (1: one residual
-// source buffer), CONV_PAIR (1/0: force CTA pairs on/off), CONV_WINDOW and
-// CONV_ROWTAP (-1 disables those loaders), CONV_ROWTAP_BAND.  Read on every
-// call.
+// source buffer), CONV_PAIR (1/0: force CTA pairs on/off), CONV_WINDOW,
+// CONV_ROWTAP, CONV_GATHER_STAGE and CONV_L2_PREFETCH (-1 disables that
+// loader or feature), CONV_ROWTAP_BAND, CONV_WAIT_HINT_NS.  Read once per
+// process, on first use; conv_testing_reload_tuning() reads them again.
+struct Tuning {
+  int tile_m, tile_n, max_stages, src_bufs, window, rowtap, rowtap_band, gather_stage, l2_prefetch;
+  int filter_resident;  // -1 when unset
+  int pair;             // -1 when unset
+  uint32_t wait_hint_ns;
+};
+
 int env_int(const char* name) {
   const char* v = std::getenv(name);
   return v ? std::atoi(v) : 0;
+}
+
+int env_int_or(const char* name, int unset) {
+  const char* v = std::getenv(name);
+  return v ? std::atoi(v) : unset;
+}
+
+Tuning read_tuning() {
+  Tuning t{};
+  t.tile_m = env_int("CONV_TILE_M");
+  t.tile_n = env_int("CONV_TILE_N");
+  t.max_stages = env_int("CONV_MAX_STAGES");
+  t.src_bufs = env_int("CONV_SRC_BUFS");
+  t.window = env_int("CONV_WINDOW");
+  t.rowtap = env_int("CONV_ROWTAP");
+  t.rowtap_band = env_int("CONV_ROWTAP_BAND");
+  t.gather_stage = env_int("CONV_GATHER_STAGE");
+  t.l2_prefetch = env_int("CONV_L2_PREFETCH");
+  t.filter_resident = env_int_or("CONV_FILTER_RESIDENT", -1);
+  t.pair = env_int_or("CONV_PAIR", -1);
+  t.wait_hint_ns = static_cast<uint32_t>(env_int("CONV_WAIT_HINT_NS"));
+  return t;
+}
+
+std::mutex g_tuning_mu;
+Tuning g_tuning_value;
+std::atomic<unsigned> g_tuning_gen{0};  // 0: not read yet; bumped by every (re)load
+
+const Tuning& tuning() {
+  if (g_tuning_gen.load(std::memory_order_acquire) == 0) {
+    std::lock_guard<std::mutex> lock(g_tuning_mu);
+    if (g_tuning_gen.load(std::memory_order_relaxed) == 0) {
+      g_tuning_value = read_tuning();
+      g_tuning_gen.store(1, std::memory_order_release);
+    }
+  }
+  return g_tuning_value;
 }
 
 bool known_dtype(conv_dtype_t d) {
@@ -187,7 +232,7 @@ size_t gather_smem_bytes(ConvKernelParams& kp) {
   kp.g_stage = 0;
   kp.g_slots = 0;
   kp.g_stage_bytes = 0;
-  if (kp.g_row_bytes % 16 == 0 && env_int("CONV_GATHER_STAGE") != -1) {
+  if (kp.g_row_bytes % 16 == 0 && tuning().gather_stage != -1) {
     // Padded rows a tile of `rows` consecutive output pixels can touch: its
     // output rows (at most (rows-1)/Wo + 2 of them) step stride_h apart, plus
     // the filter extent, plus, at each image boundary crossed, the rest of
@@ -369,8 +414,8 @@ void choose_tiling(Plan* pl, const long long rows[], int num_phases, int max_kbl
       }
     }
   }
-  const int force_m = env_int("CONV_TILE_M");
-  const int force_n = env_int("CONV_TILE_N");
+  const int force_m = tuning().tile_m;
+  const int force_n = tuning().tile_n;
   if (force_n >= 16 && force_n <= 256 && force_n % 16 == 0) {
     best_bn = force_n;
     best_nt = (c_out + force_n - 1) / force_n;
@@ -400,7 +445,7 @@ void choose_tiling(Plan* pl, const long long rows[], int num_phases, int max_kbl
 void plan_pair(Plan* pl, int num_sms) {
   ConvKernelParams& kp = pl->kp;
   kp.pair = 0;
-  const int force = std::getenv("CONV_PAIR") ? env_int("CONV_PAIR") : -1;
+  const int force = tuning().pair;
   if (force == 0) return;
   if (kp.window || kp.gather || kp.groups > 1 || kp.bn < 32) return;
   const int tile_m = 2 * kBM;
@@ -479,7 +524,7 @@ conv_status_t layout_memory_window(Plan* pl, int has_residual);
 void plan_window(const FwdShape& f, Plan* pl, int num_sms, int has_residual) {
   ConvKernelParams& kp = pl->kp;
   kp.window = 0;
-  if (env_int("CONV_WINDOW") == -1) return;
+  if (tuning().window == -1) return;
   if (f.stride_h != 1 || f.stride_w != 1 || f.dil_h != 1 || f.dil_w != 1) return;
   if (kp.sw_bytes != 128 || !kp.vec_ok) return;
   const int pitch = f.wo + f.s - 1;
@@ -981,7 +1026,7 @@ conv_status_t layout_memory(Plan* pl, int has_residual) {
   // (A pair's CTA holds half of the tile's filter rows.)
   const uint32_t b_bytes = static_cast<uint32_t>(kp.pair ? kp.bn / 2 : kp.bn) * kp.sw_bytes;
   const bool can_res = !kp.pair && kp.num_phases == 1 && kp.n_tiles == 1 && kp.groups <= 1 &&
-                       !(std::getenv("CONV_FILTER_RESIDENT") && env_int("CONV_FILTER_RESIDENT") == 0);
+                       tuning().filter_resident != 0;
   const size_t bres = can_res ? static_cast<size_t>(kp.taps_h[0]) * kp.taps_w[0] * kp.c_blocks * b_bytes : 0;
   const size_t src_tile = static_cast<size_t>(kBM) * kp.m_halves * kp.bn * 2;
   const size_t chunk = static_cast<size_t>(kBM) * cw * 2;
@@ -990,7 +1035,7 @@ conv_status_t layout_memory(Plan* pl, int has_residual) {
   Opt opts[12];
   int nopt = 0;
   // CONV_SRC_BUFS (1 or 2) caps the residual-source tile buffers (tuning override).
-  const int srcb_env = env_int("CONV_SRC_BUFS");
+  const int srcb_env = tuning().src_bufs;
   const int srcb_max = has_residual ? ((srcb_env == 1) ? 1 : 2) : 0;
   // With a residual the outputs are written in place into the source tile
   // buffer and stored from there: no staging buffers.
@@ -1011,7 +1056,7 @@ conv_status_t layout_memory(Plan* pl, int has_residual) {
     const size_t stage = a_bytes + (opts[i].res ? 0 : b_bytes);
     if (used + 2 * stage > kSmemLimit) continue;
     int st = static_cast<int>(std::min<size_t>(kMaxStages, (kSmemLimit - used) / stage));
-    if (env_int("CONV_MAX_STAGES") >= 2) st = std::min(st, env_int("CONV_MAX_STAGES"));
+    if (tuning().max_stages >= 2) st = std::min(st, tuning().max_stages);
     const double load = (a_bytes + (opts[i].res ? 0.0 : b_bytes)) / 70.0 + 40.0 * (opts[i].res ? 1 : 2);
     double key = load;
     if (st < 3) key += 1e6;
@@ -1082,7 +1127,7 @@ conv_status_t layout_memory_window(Plan* pl, int has_residual) {
                           kEpilogueGroups * stgb * align1k(chunk);
       if (used + 2 * stage > kSmemLimit) continue;
       int st = static_cast<int>(std::min<size_t>(kMaxStages, (kSmemLimit - used) / stage));
-      if (env_int("CONV_MAX_STAGES") >= 2) st = std::min(st, env_int("CONV_MAX_STAGES"));
+      if (tuning().max_stages >= 2) st = std::min(st, tuning().max_stages);
       if (st > best_st) {
         best_st = st;
         best_srcb = srcb;
@@ -1212,9 +1257,12 @@ conv_status_t plan_memory_direct(Plan* pl) {
 }
 
 // ------------------------------------------------------------------ launch
-conv_status_t finish_and_launch(Plan* pl, int n_images, const void* packed, void* output,
-                                int has_residual, const void* source, float beta,
-                                conv_epilogue_t epilogue, void* workspace, cudaStream_t stream) {
+// Completes the kernel parameters of an implicit-GEMM plan: the filter and
+// epilogue tensor maps, the shared-memory layout, the epilogue arguments and
+// the grid.  No launch: the result may be cached and launched many times.
+conv_status_t finish_plan(Plan* pl, int n_images, const void* packed, void* output,
+                          int has_residual, const void* source, float beta,
+                          conv_epilogue_t epilogue, void* workspace) {
   ConvKernelParams& kp = pl->kp;
   if (kp.groups < 1) {  // plans without channel groups
     kp.groups = 1;
@@ -1240,10 +1288,7 @@ conv_status_t finish_and_launch(Plan* pl, int n_images, const void* packed, void
   kp.status = static_cast<unsigned int*>(workspace);
   const unsigned long long tmo = g_timeout_ns.load(std::memory_order_relaxed);
   kp.timeout_cycles = ns_to_cycles(tmo ? tmo : kDefaultTimeoutNs);
-  {
-    const char* h = std::getenv("CONV_WAIT_HINT_NS");
-    kp.wait_hint_ns = h ? static_cast<uint32_t>(std::atoi(h)) : 0u;
-  }
+  kp.wait_hint_ns = tuning().wait_hint_ns;
   kp.fault_mode = g_fault_mode.load(std::memory_order_relaxed);
   kp.div_ntiles = make_fast_div(static_cast<uint32_t>(std::max(kp.n_tiles, 1)));
   for (int ph = 0; ph < kMaxPhases; ++ph) {
@@ -1256,13 +1301,17 @@ conv_status_t finish_and_launch(Plan* pl, int n_images, const void* packed, void
   kp.div_tpg = make_fast_div(static_cast<uint32_t>(std::max(kp.tiles_per_group, 1)));
   // Prefetching the next tile's input only pays when CTAs walk several tiles
   // that all start at the first C_out tile (one n-tile).
-  kp.l2_prefetch = (kp.n_tiles == 1 && env_int("CONV_L2_PREFETCH") != -1) ? 1 : 0;
-  if (kp.total_tiles == 0) return CONV_OK;
+  kp.l2_prefetch = (kp.n_tiles == 1 && tuning().l2_prefetch != -1) ? 1 : 0;
   const int sms = device_sm_count();
   if (sms <= 0) return CONV_ERR_CUDA;
   // Pairs: clusters of two CTAs, one tile per cluster at a time.
   pl->grid = kp.pair ? 2 * std::min(kp.total_tiles, sms / 2) : std::min(kp.total_tiles, sms);
-  cudaError_t e = launch_conv_igemm(pl->kind, pl->out_bf16, kp, pl->grid, pl->smem_bytes, stream);
+  return CONV_OK;
+}
+
+conv_status_t launch_plan(const Plan& pl, cudaStream_t stream) {
+  if (pl.kp.total_tiles == 0) return CONV_OK;
+  cudaError_t e = launch_conv_igemm(pl.kind, pl.out_bf16, pl.kp, pl.grid, pl.smem_bytes, stream);
   return e == cudaSuccess ? CONV_OK : CONV_ERR_CUDA;
 }
 
@@ -1279,10 +1328,11 @@ struct RowTapPlan {
   RowTapParams rp;
   int grid;
   size_t smem_bytes;
+  int in_dtype;
 };
 
 bool plan_rowtap(const FwdShape& f, int groups, int num_sms, RowTapPlan* out) {
-  if (env_int("CONV_ROWTAP") == -1) return false;
+  if (tuning().rowtap == -1) return false;
   if (groups != 1 || f.stride_h != 1 || f.stride_w != 1 || f.dil_h != 1 || f.dil_w != 1)
     return false;
   if (f.r * f.s < 2) return false;
@@ -1310,7 +1360,7 @@ bool plan_rowtap(const FwdShape& f, int groups, int num_sms, RowTapPlan* out) {
       best = b;
     }
   }
-  const int band_env = env_int("CONV_ROWTAP_BAND");  // tuning override: output rows per tile
+  const int band_env = tuning().rowtap_band;  // tuning override: output rows per tile
   if (band_env > 0) best = std::min(band_env, band_max);
   const int n_band = (f.ho + best - 1) / best;
   const long long tiles = static_cast<long long>(f.n) * n_band * n_seg;
@@ -1348,10 +1398,11 @@ bool plan_rowtap(const FwdShape& f, int groups, int num_sms, RowTapPlan* out) {
   return true;
 }
 
-conv_status_t launch_rowtap_path(RowTapPlan* pl, const FwdShape& f, const void* input,
-                                 const void* packed, void* output, int has_residual,
-                                 const void* source, float beta, conv_epilogue_t epilogue,
-                                 void* workspace, cudaStream_t stream) {
+// Encodes the row-tap kernel's maps and fills its epilogue arguments (no launch).
+conv_status_t finish_rowtap(RowTapPlan* pl, const FwdShape& f, const void* input,
+                            const void* packed, void* output, int has_residual,
+                            const void* source, float beta, conv_epilogue_t epilogue,
+                            void* workspace) {
   const DriverFns* fns = driver_fns();
   if (!fns) return CONV_ERR_CUDA;
   RowTapParams& rp = pl->rp;
@@ -1391,9 +1442,14 @@ conv_status_t launch_rowtap_path(RowTapPlan* pl, const FwdShape& f, const void* 
   const unsigned long long tmo = g_timeout_ns.load(std::memory_order_relaxed);
   rp.timeout_cycles = ns_to_cycles(tmo ? tmo : kDefaultTimeoutNs);
   rp.fault_mode = g_fault_mode.load(std::memory_order_relaxed);
-  if (rp.total_tiles == 0) return CONV_OK;
-  cudaError_t err = launch_conv_rowtap(static_cast<int>(f.in_dtype), f.in_dtype != CONV_DTYPE_F16,
-                                       rp, pl->grid, pl->smem_bytes, stream);
+  pl->in_dtype = static_cast<int>(f.in_dtype);
+  return CONV_OK;
+}
+
+conv_status_t launch_rowtap(const RowTapPlan& pl, cudaStream_t stream) {
+  if (pl.rp.total_tiles == 0) return CONV_OK;
+  cudaError_t err = launch_conv_rowtap(pl.in_dtype, pl.in_dtype != CONV_DTYPE_F16, pl.rp, pl.grid,
+                                       pl.smem_bytes, stream);
   return err == cudaSuccess ? CONV_OK : CONV_ERR_CUDA;
 }
 
@@ -1438,12 +1494,56 @@ TrShape make_tr_shape(int n, int h, int w, int c_in, conv_dtype_t in_dtype, int 
   return t;
 }
 
-// Common body of conv2d_fwd / conv2d_fwd_packed.  `filter` is raw (packed
-// into the workspace first) unless `prepacked`.
-conv_status_t fwd_impl(const void* input, const FwdShape& shape, const void* filter, int fcrs,
-                       bool prepacked, void* output, int num_groups, int has_residual,
-                       const void* source, float beta, conv_epilogue_t epilogue, void* workspace,
-                       size_t workspace_bytes, cudaStream_t stream) {
+// A call made ready to launch: which kernel runs it, its complete parameters
+// (tensor maps encoded, shared memory laid out, grid chosen) and, for the
+// entry points that take a raw filter, the packing launch that precedes it.
+enum { kPathIgemm = 0, kPathRowTap = 1, kPathDirect = 2 };
+
+struct PackStep {
+  int kind;                 // 0 none, 1 forward filter, 2 transposed filter
+  const void* filter;
+  void* dst;
+  int r, s, c_in, c_out, fcrs;
+  conv_dtype_t dtype;
+};
+
+struct Prepared {
+  int path;
+  PackStep pack;
+  Plan pl;          // kPathIgemm (also carries the transposed packing description)
+  RowTapPlan rt;    // kPathRowTap
+  DirectParams dp;  // kPathDirect
+  int direct_in_dtype;
+  int sms;
+};
+
+conv_status_t run_pack(const Prepared& pr, cudaStream_t stream) {
+  const PackStep& k = pr.pack;
+  if (k.kind == 1)
+    return launch_pack_fwd(k.filter, k.r, k.s, k.c_in, k.c_out, k.fcrs, k.dtype, k.dst, stream);
+  if (k.kind == 2)
+    return launch_pack_tr(pr.pl, k.filter, k.r, k.s, k.c_in, k.c_out, k.dtype, k.dst, stream);
+  return CONV_OK;
+}
+
+conv_status_t launch_prepared(const Prepared& pr, cudaStream_t stream) {
+  conv_status_t st = run_pack(pr, stream);
+  if (st != CONV_OK) return st;
+  if (pr.path == kPathRowTap) return launch_rowtap(pr.rt, stream);
+  if (pr.path == kPathDirect) {
+    cudaError_t e = launch_conv_direct(pr.direct_in_dtype, pr.direct_in_dtype != CONV_DTYPE_F16,
+                                       pr.dp, pr.sms, stream);
+    return e == cudaSuccess ? CONV_OK : CONV_ERR_CUDA;
+  }
+  return launch_plan(pr.pl, stream);
+}
+
+// Prepares conv2d_fwd / conv2d_fwd_packed.  `filter` is raw (packed into the
+// workspace first) unless `prepacked`.
+conv_status_t prepare_fwd(const void* input, const FwdShape& shape, const void* filter, int fcrs,
+                          bool prepacked, void* output, int num_groups, int has_residual,
+                          const void* source, float beta, conv_epilogue_t epilogue,
+                          void* workspace, size_t workspace_bytes, Prepared* pr) {
   conv_status_t st = check_common_ptrs(input, filter, output, has_residual, source, workspace);
   if (st != CONV_OK) return st;
   if (!epilogue_ok(epilogue)) return CONV_ERR_INVALID_VALUE;
@@ -1457,16 +1557,18 @@ conv_status_t fwd_impl(const void* input, const FwdShape& shape, const void* fil
   if (workspace_bytes < need) return CONV_ERR_WORKSPACE_TOO_SMALL;
   const int sms = device_sm_count();
   if (sms <= 0) return CONV_ERR_CUDA;
+  pr->sms = sms;
+  const void* packed = filter;
+  pr->pack.kind = 0;
+  if (!prepacked) {
+    void* dst = static_cast<uint8_t*>(workspace) + CONV_STATUS_BYTES;
+    pr->pack = PackStep{1, filter, dst, f.r, f.s, cg, f.c_out, fcrs, f.in_dtype};
+    packed = dst;
+  }
   if (num_groups > 1 && !groups_on_tensor_cores(cg, elt_bytes(f.in_dtype))) {
-    const void* packed = filter;
-    if (!prepacked) {
-      void* dst = static_cast<uint8_t*>(workspace) + CONV_STATUS_BYTES;
-      st = launch_pack_fwd(filter, f.r, f.s, cg, f.c_out, fcrs, f.in_dtype, dst, stream);
-      if (st != CONV_OK) return st;
-      packed = dst;
-    }
     const int elt = elt_bytes(f.in_dtype);
-    DirectParams dp{};
+    DirectParams& dp = pr->dp;
+    dp = DirectParams{};
     dp.x = input;
     dp.w = packed;
     dp.src = has_residual ? source : nullptr;
@@ -1507,42 +1609,28 @@ conv_status_t fwd_impl(const void* input, const FwdShape& shape, const void* fil
                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
         return CONV_ERR_CUDA;
     }
-    cudaError_t e = launch_conv_direct(static_cast<int>(f.in_dtype), f.in_dtype != CONV_DTYPE_F16,
-                                       dp, sms, stream);
-    return e == cudaSuccess ? CONV_OK : CONV_ERR_CUDA;
+    pr->path = kPathDirect;
+    pr->direct_in_dtype = static_cast<int>(f.in_dtype);
+    return CONV_OK;
   }
-  RowTapPlan rt;
-  if (plan_rowtap(f, num_groups, sms, &rt)) {
-    const void* packed = filter;
-    if (!prepacked) {
-      void* dst = static_cast<uint8_t*>(workspace) + CONV_STATUS_BYTES;
-      st = launch_pack_fwd(filter, f.r, f.s, cg, f.c_out, fcrs, f.in_dtype, dst, stream);
-      if (st != CONV_OK) return st;
-      packed = dst;
-    }
-    return launch_rowtap_path(&rt, f, input, packed, output, has_residual, source, beta, epilogue,
-                              workspace, stream);
+  if (plan_rowtap(f, num_groups, sms, &pr->rt)) {
+    pr->path = kPathRowTap;
+    return finish_rowtap(&pr->rt, f, input, packed, output, has_residual, source, beta, epilogue,
+                         workspace);
   }
-  Plan pl;
+  Plan& pl = pr->pl;
   st = plan_fwd(f, &pl, sms, has_residual);
   if (st != CONV_OK) return st;
   st = encode_fwd_input(f, input, &pl);
   if (st != CONV_OK) return st;
-  const void* packed = filter;
-  if (!prepacked) {
-    void* dst = static_cast<uint8_t*>(workspace) + CONV_STATUS_BYTES;
-    st = launch_pack_fwd(filter, f.r, f.s, cg, f.c_out, fcrs, f.in_dtype, dst, stream);
-    if (st != CONV_OK) return st;
-    packed = dst;
-  }
-  return finish_and_launch(&pl, f.n, packed, output, has_residual, source, beta, epilogue,
-                           workspace, stream);
+  pr->path = kPathIgemm;
+  return finish_plan(&pl, f.n, packed, output, has_residual, source, beta, epilogue, workspace);
 }
 
-conv_status_t tr_impl(const void* input, const TrShape& t, const void* filter, bool prepacked,
-                      void* output, int has_residual, const void* source, float beta,
-                      conv_epilogue_t epilogue, void* workspace, size_t workspace_bytes,
-                      cudaStream_t stream) {
+conv_status_t prepare_tr(const void* input, const TrShape& t, const void* filter, bool prepacked,
+                         void* output, int has_residual, const void* source, float beta,
+                         conv_epilogue_t epilogue, void* workspace, size_t workspace_bytes,
+                         Prepared* pr) {
   conv_status_t st = check_common_ptrs(input, filter, output, has_residual, source, workspace);
   if (st != CONV_OK) return st;
   if (!epilogue_ok(epilogue)) return CONV_ERR_INVALID_VALUE;
@@ -1560,20 +1648,117 @@ conv_status_t tr_impl(const void* input, const TrShape& t, const void* filter, b
   if (workspace_bytes < need) return CONV_ERR_WORKSPACE_TOO_SMALL;
   const int sms = device_sm_count();
   if (sms <= 0) return CONV_ERR_CUDA;
-  Plan pl;
+  pr->sms = sms;
+  Plan& pl = pr->pl;
   st = plan_transposed(t, &pl, sms);
   if (st != CONV_OK) return st;
   st = encode_tr_inputs(t, input, &pl);
   if (st != CONV_OK) return st;
   const void* packed = filter;
+  pr->pack.kind = 0;
   if (!prepacked) {
     void* dst = static_cast<uint8_t*>(workspace) + CONV_STATUS_BYTES;
-    st = launch_pack_tr(pl, filter, t.r, t.s, t.c_in, t.c_out, t.in_dtype, dst, stream);
-    if (st != CONV_OK) return st;
+    pr->pack = PackStep{2, filter, dst, t.r, t.s, t.c_in, t.c_out, 0, t.in_dtype};
     packed = dst;
   }
-  return finish_and_launch(&pl, t.n, packed, output, has_residual, source, beta, epilogue,
-                           workspace, stream);
+  pr->path = kPathIgemm;
+  return finish_plan(&pl, t.n, packed, output, has_residual, source, beta, epilogue, workspace);
+}
+
+// ------------------------------------------------------------------ prepared-call cache
+// Planning and tensor-map encoding cost microseconds of host time per call;
+// a call repeated with the same arguments (pointers included: a tensor map
+// holds the address) reuses the prepared launch.  The key holds every
+// argument plus the device, the tuning generation and the test hooks, so an
+// entry is valid exactly when a fresh preparation would produce it.
+struct CallKey {
+  int entry;  // 0 conv2d_fwd, 1 conv2d_fwd_packed, 2 conv_transposed, 3 conv_transposed_packed
+  int device;
+  unsigned tuning_gen;
+  int fault_mode;
+  unsigned long long timeout_ns;
+  const void* ptrs[5];  // input, filter, output, source, workspace
+  size_t workspace_bytes;
+  int dims[20];
+  uint32_t beta_bits;
+};
+
+constexpr int kCacheEntries = 32;
+struct CacheSlot {
+  bool valid;
+  CallKey key;
+  Prepared prep;
+};
+
+std::mutex g_cache_mu;
+CacheSlot g_cache[kCacheEntries];
+int g_cache_next = 0;
+std::atomic<unsigned long long> g_cache_hits{0}, g_cache_misses{0};
+
+CallKey make_key(int entry, const void* input, const void* filter, const void* output,
+                 const void* source, const void* workspace, size_t workspace_bytes, int n, int h,
+                 int w, int c_in, conv_dtype_t in_dtype, int r, int s, int c_out, int fcrs, int ho,
+                 int wo, conv_dtype_t out_dtype, const int stride[2], const int dilation[2],
+                 const int pad[2], int num_groups, int has_residual, float beta,
+                 conv_epilogue_t epilogue) {
+  CallKey k;
+  std::memset(&k, 0, sizeof(k));  // padding bytes take part in the comparison
+  k.entry = entry;
+  if (cudaGetDevice(&k.device) != cudaSuccess) k.device = -1;
+  k.tuning_gen = g_tuning_gen.load(std::memory_order_acquire);
+  k.fault_mode = g_fault_mode.load(std::memory_order_relaxed);
+  k.timeout_ns = g_timeout_ns.load(std::memory_order_relaxed);
+  k.ptrs[0] = input;
+  k.ptrs[1] = filter;
+  k.ptrs[2] = output;
+  k.ptrs[3] = has_residual ? source : nullptr;
+  k.ptrs[4] = workspace;
+  k.workspace_bytes = workspace_bytes;
+  const int d[20] = {n, h, w, c_in, static_cast<int>(in_dtype), r, s, c_out, fcrs, ho, wo,
+                     static_cast<int>(out_dtype), stride[0], stride[1], dilation[0], dilation[1],
+                     pad[0], pad[1], num_groups, has_residual ? 1 : 0};
+  std::memcpy(k.dims, d, sizeof(d));
+  const float b = has_residual ? beta : 0.0f;
+  std::memcpy(&k.beta_bits, &b, sizeof(b));
+  k.dims[19] |= static_cast<int>(epilogue) << 8;
+  return k;
+}
+
+bool cache_lookup(const CallKey& key, Prepared* out) {
+  std::lock_guard<std::mutex> lock(g_cache_mu);
+  for (int i = 0; i < kCacheEntries; ++i) {
+    if (g_cache[i].valid && std::memcmp(&g_cache[i].key, &key, sizeof(key)) == 0) {
+      *out = g_cache[i].prep;
+      g_cache_hits.fetch_add(1, std::memory_order_relaxed);
+      return true;
+    }
+  }
+  g_cache_misses.fetch_add(1, std::memory_order_relaxed);
+  return false;
+}
+
+void cache_store(const CallKey& key, const Prepared& prep) {
+  std::lock_guard<std::mutex> lock(g_cache_mu);
+  CacheSlot& slot = g_cache[g_cache_next];
+  g_cache_next = (g_cache_next + 1) % kCacheEntries;
+  slot.key = key;
+  slot.prep = prep;
+  slot.valid = true;
+}
+
+// Looks the call up, prepares it on a miss (caching only successful
+// preparations), and launches it.
+template <typename PrepareFn>
+conv_status_t cached_call(const CallKey& key, PrepareFn prepare, cudaStream_t stream) {
+  // Large (several KB): keep it off the stack of callers with small stacks.
+  thread_local Prepared pr;
+  if (!cache_lookup(key, &pr)) {
+    std::memset(&pr, 0, sizeof(pr));
+    conv_status_t st = prepare(&pr);
+    if (st != CONV_OK) return st;
+    if (key.device >= 0) cache_store(key, pr);
+  }
+  return launch_prepared(pr, stream);
 }
 
 }  // namespace
@@ -1652,9 +1837,15 @@ conv_status_t conv2d_fwd(const void* input, int n, int h, int w, int c_in, conv_
   if (!stride || !dilation || !symmetric_padding) return CONV_ERR_INVALID_VALUE;
   const FwdShape f = make_fwd_shape(n, h, w, c_in, in_dtype, r, s, c_out, ho, wo, out_dtype,
                                     stride, dilation, symmetric_padding);
-  return fwd_impl(input, f, filter, filter_is_fcrs ? 1 : 0, false, output, num_groups,
-                  has_residual, source, beta, epilogue, workspace, workspace_bytes,
-                  static_cast<cudaStream_t>(stream));
+  const int fcrs = filter_is_fcrs ? 1 : 0;
+  const CallKey key = make_key(0, input, filter, output, source, workspace, workspace_bytes, n, h,
+                               w, c_in, in_dtype, r, s, c_out, fcrs, ho, wo, out_dtype, stride,
+                               dilation, symmetric_padding, num_groups, has_residual, beta,
+                               epilogue);
+  return cached_call(key, [&](Prepared* pr) {
+    return prepare_fwd(input, f, filter, fcrs, false, output, num_groups, has_residual, source,
+                       beta, epilogue, workspace, workspace_bytes, pr);
+  }, static_cast<cudaStream_t>(stream));
 }
 
 conv_status_t conv2d_fwd_packed(const void* input, int n, int h, int w, int c_in,
@@ -1667,8 +1858,14 @@ conv_status_t conv2d_fwd_packed(const void* input, int n, int h, int w, int c_in
   if (!stride || !dilation || !symmetric_padding) return CONV_ERR_INVALID_VALUE;
   const FwdShape f = make_fwd_shape(n, h, w, c_in, in_dtype, r, s, c_out, ho, wo, out_dtype,
                                     stride, dilation, symmetric_padding);
-  return fwd_impl(input, f, packed_filter, 0, true, output, num_groups, has_residual, source, beta,
-                  epilogue, workspace, workspace_bytes, static_cast<cudaStream_t>(stream));
+  const CallKey key = make_key(1, input, packed_filter, output, source, workspace, workspace_bytes,
+                               n, h, w, c_in, in_dtype, r, s, c_out, 0, ho, wo, out_dtype, stride,
+                               dilation, symmetric_padding, num_groups, has_residual, beta,
+                               epilogue);
+  return cached_call(key, [&](Prepared* pr) {
+    return prepare_fwd(input, f, packed_filter, 0, true, output, num_groups, has_residual, source,
+                       beta, epilogue, workspace, workspace_bytes, pr);
+  }, static_cast<cudaStream_t>(stream));
 }
 
 size_t conv_transposed_packed_filter_bytes(int r, int s, int c_in, int c_out, const int stride[2],
@@ -1743,8 +1940,13 @@ conv_status_t conv_transposed(const void* input, int n, int h, int w, int c_in,
   if (!stride || !dilation || !padding) return CONV_ERR_INVALID_VALUE;
   const TrShape t = make_tr_shape(n, h, w, c_in, in_dtype, r, s, c_out, ho, wo, out_dtype, stride,
                                   dilation, padding);
-  return tr_impl(input, t, filter_rsfc, false, output, has_residual, source, beta, epilogue,
-                 workspace, workspace_bytes, static_cast<cudaStream_t>(stream));
+  const CallKey key = make_key(2, input, filter_rsfc, output, source, workspace, workspace_bytes,
+                               n, h, w, c_in, in_dtype, r, s, c_out, 0, ho, wo, out_dtype, stride,
+                               dilation, padding, 1, has_residual, beta, epilogue);
+  return cached_call(key, [&](Prepared* pr) {
+    return prepare_tr(input, t, filter_rsfc, false, output, has_residual, source, beta, epilogue,
+                      workspace, workspace_bytes, pr);
+  }, static_cast<cudaStream_t>(stream));
 }
 
 conv_status_t conv_transposed_packed(const void* input, int n, int h, int w, int c_in,
@@ -1757,8 +1959,13 @@ conv_status_t conv_transposed_packed(const void* input, int n, int h, int w, int
   if (!stride || !dilation || !padding) return CONV_ERR_INVALID_VALUE;
   const TrShape t = make_tr_shape(n, h, w, c_in, in_dtype, r, s, c_out, ho, wo, out_dtype, stride,
                                   dilation, padding);
-  return tr_impl(input, t, packed_filter, true, output, has_residual, source, beta, epilogue,
-                 workspace, workspace_bytes, static_cast<cudaStream_t>(stream));
+  const CallKey key = make_key(3, input, packed_filter, output, source, workspace, workspace_bytes,
+                               n, h, w, c_in, in_dtype, r, s, c_out, 0, ho, wo, out_dtype, stride,
+                               dilation, padding, 1, has_residual, beta, epilogue);
+  return cached_call(key, [&](Prepared* pr) {
+    return prepare_tr(input, t, packed_filter, true, output, has_residual, source, beta, epilogue,
+                      workspace, workspace_bytes, pr);
+  }, static_cast<cudaStream_t>(stream));
 }
 
 conv_status_t conv_check_device_status(void* workspace, void* stream, unsigned int* detail) {
@@ -1807,6 +2014,18 @@ conv_status_t conv2d_fwd_noalloc(const void* input, int n, int h, int w, int c_i
 void conv_testing_set_wait_fault(int mode, unsigned long long timeout_ns) {
   g_fault_mode.store(mode, std::memory_order_relaxed);
   g_timeout_ns.store(timeout_ns, std::memory_order_relaxed);
+}
+
+void conv_testing_reload_tuning(void) {
+  std::lock_guard<std::mutex> lock(g_tuning_mu);
+  g_tuning_value = read_tuning();
+  const unsigned gen = g_tuning_gen.load(std::memory_order_relaxed);
+  g_tuning_gen.store(gen + 1 == 0 ? 1 : gen + 1, std::memory_order_release);
+}
+
+void conv_testing_cache_stats(unsigned long long* hits, unsigned long long* misses) {
+  if (hits) *hits = g_cache_hits.load(std::memory_order_relaxed);
+  if (misses) *misses = g_cache_misses.load(std::memory_order_relaxed);
 }
 
 conv_status_t conv_testing_fwd_plan(int n, int h, int w, int c_in, conv_dtype_t dtype, int r,

@@ -192,3 +192,7 @@ WORKLOADS = {
 
 # The ResNet-style block: the stride-1 residual conv and the stride-2 downsample.
 RESNET_BLOCK = ("resnet_bf16", "resnet_down_bf16")
+
+# Every convolution of the benchmark configurations, in their order.
+BASELINE_SET = ("tiny_bf16", "resnet_bf16", "resnet_down_bf16", "fp8_res", "vae_silu_bf16",
+                "vae_head_bf16", "convT_f16", "fwd5x5_f16")
