@@ -1,6 +1,7 @@
 """The kernels' bounded-wait failure path, exercised without faulting the GPU.
 
-The test hook makes CTA 0's producer leave its first pipeline stage un-armed,
+The test hook makes CTA 0's producer leave its first pipeline stage un-armed
+(for CTA pairs: both CTAs of the first pair leave it un-armed and unloaded),
 so the MMA warp's wait on that stage can only end by running out of time (a
 few milliseconds here).  The kernel must then record the timeout in the
 workspace status word, stop its other roles, let its copies in flight land,
@@ -8,6 +9,8 @@ release its tensor memory and return; the host reads CONV_ERR_DEVICE_TIMEOUT
 from conv_check_device_status.  A normal launch afterwards, in the same
 context, must still produce the right answer.
 """
+import ctypes
+
 import pytest
 import torch
 
@@ -34,8 +37,38 @@ CASES = [
 ]
 
 
+# Cases run again on CTA pairs (clusters of two CTAs sharing 256-row tiles):
+# there rank 1's epilogue and producers time out in turn once rank 0's MMA
+# warp stops, and both CTAs meet at the exit cluster barrier.
+PAIR_CASES = [
+    _fwd("pair_e4m3_s2", "f8e4m3", 2, 13, 13, 64, 64, 3, 2, 1),
+    _fwd("pair_cout512_silu", "bf16", 1, 12, 12, 64, 512, 3, 1, 1, epi="silu"),
+    # direct-store epilogue with a residual source
+    _fwd("pair_cout17_res", "bf16", 2, 10, 10, 32, 17, 3, 1, 1, res=True, beta=0.5),
+    _tr("pair_transposed_relu", "f16", 2, 9, 8, 64, 64, 4, 2, 1, epi="relu"),
+]
+
+
 @pytest.mark.parametrize("case", CASES, ids=lambda c: c.name)
 def test_timeout_is_reported_and_context_survives(case):
+    _timeout_then_normal(case)
+
+
+@pytest.mark.parametrize("case", PAIR_CASES, ids=lambda c: c.name)
+def test_cta_pair_timeout_is_reported_and_context_survives(case, tuning):
+    tuning("CONV_PAIR", "1")
+    if case.kind == "fwd":   # the planner must put it on CTA pairs on this device
+        plan = (ctypes.c_int * 13)()
+        sms = torch.cuda.get_device_properties(0).multi_processor_count
+        st = _lib.lib().conv_testing_fwd_plan(
+            case.N, case.H, case.W, case.C_in, _lib.DTYPE_CODES[case.dtype], case.R, case.S,
+            case.C_out, _lib.pair((case.stride,) * 2), _lib.pair(case.pads), int(case.has_residual),
+            sms, plan)
+        assert st == 0 and plan[12] == 1, list(plan)
+    _timeout_then_normal(case)
+
+
+def _timeout_then_normal(case):
     inp = synthetic.make_inputs(case)
     ws = cg.new_workspace(cg.CONV_STATUS_BYTES, "cuda:0")
     lib = _lib.lib()

@@ -1705,6 +1705,7 @@ CallKey make_key(int entry, const void* input, const void* filter, const void* o
   std::memset(&k, 0, sizeof(k));  // padding bytes take part in the comparison
   k.entry = entry;
   if (cudaGetDevice(&k.device) != cudaSuccess) k.device = -1;
+  tuning();  // loads the overrides on first use, so the generation below is final
   k.tuning_gen = g_tuning_gen.load(std::memory_order_acquire);
   k.fault_mode = g_fault_mode.load(std::memory_order_relaxed);
   k.timeout_ns = g_timeout_ns.load(std::memory_order_relaxed);
