@@ -14,9 +14,15 @@ benchmark configurations name, at full size, one after the other:
   convT_f16         f16 transposed 8x32x32x256 -> 8x64x64x128, 4x4 RSFC s2 p1, ReLU
   fwd5x5_f16        f16 8x128x128x128 -> 8x64x64x128, 5x5 s2 p2
 
-Each conv is preceded by an L2 flush (a write of max(2 x L2, 256 MiB)) and
-bracketed by its own CUDA events on the launch stream; the flush lies
-outside the events.  The step time is the sum of the convs' event times.
+Each conv runs as a stream of back-to-back launches over rotating copies of
+all its tensors (input, packed filter, source, output) that together exceed
+3 x L2, so that every launch reads its operands from HBM (inputs larger than
+L2 in place of a flush); the stream is bracketed by CUDA events on the launch
+stream and the per-launch time is its event time over the launches.  The
+tiny conv, too small for that, is timed alone after an L2 flush (a write of
+max(2 x L2, 256 MiB)) outside its events.  The step time is the sum of the
+convs' per-launch times; ``per_kernel`` also reports each conv alone after a
+flush (``us_isolated``: that includes the launch latency a stream hides).
 ``value`` is the step's algorithmic FLOPs over the step time (whole job: all
 ranks' FLOPs over the slowest rank's time); ``per_kernel`` gives each conv's
 time, TFLOP/s, GB/s and fraction of its own roofline; ``roofline`` is the
@@ -375,19 +381,20 @@ def run_ours(args, world, rank, local):
             packed.append(cg.conv2d_pack_filter(w, filter_is_fcrs=case.filter_layout == "FCRS"))
     pack_ev[1].record(stream)
     workspace = cg.new_workspace(cg.CONV_STATUS_BYTES, dev)
-    for case, (x, w, src), pk in zip(cases, dev_inputs, packed):
-        out = torch.empty(case.out_shape, dtype=synthetic.TORCH_DTYPES[case.out_dtype], device=dev)
-        outs.append(out)
+
+    def bind(case, x, pk, src, out):
         st, pd = (case.stride,) * 2, case.pads
         kw = dict(r=case.R, s=case.S, stride=st, has_residual=case.has_residual, source=src,
                   beta=case.beta, epilogue=case.epilogue, workspace=workspace, stream=stream)
-        if case.kind != "transposed":
-            kw["dilation"] = case.dilations
-            kw["num_groups"] = case.groups
         if case.kind == "transposed":
-            calls.append(cg.bind_conv_transposed_packed(x, pk, out, padding=pd, **kw))
-        else:
-            calls.append(cg.bind_conv2d_fwd_packed(x, pk, out, symmetric_padding=pd, **kw))
+            return cg.bind_conv_transposed_packed(x, pk, out, padding=pd, **kw)
+        return cg.bind_conv2d_fwd_packed(x, pk, out, symmetric_padding=pd, dilation=case.dilations,
+                                         num_groups=case.groups, **kw)
+
+    for case, (x, w, src), pk in zip(cases, dev_inputs, packed):
+        out = torch.empty(case.out_shape, dtype=synthetic.TORCH_DTYPES[case.out_dtype], device=dev)
+        outs.append(out)
+        calls.append(bind(case, x, pk, src, out))
     torch.cuda.synchronize(dev)
     pack_us = pack_ev[0].elapsed_time(pack_ev[1]) * 1e3
 
@@ -395,28 +402,63 @@ def run_ours(args, world, rank, local):
     l2 = int(getattr(props, "L2_cache_size", 128 << 20))
     flush = torch.empty(max(2 * l2, 256 << 20), dtype=torch.uint8, device=dev)
 
+    # Baseline set: each conv runs as a stream of back-to-back launches over
+    # rotating copies of all its tensors (input, packed filter, source,
+    # output) that together exceed 3 x L2, so every launch reads its operands
+    # from HBM; the per-launch time is the stream's event time over the
+    # launches.  A conv too small for that within 64 copies is timed alone
+    # after an L2 flush instead.
+    rotate_sets = []
+    if per_conv_flush:
+        for i, case in enumerate(cases):
+            x, w, src = dev_inputs[i]
+            per_copy = case.bytes
+            ncopy = max(1, math.ceil(3 * l2 / per_copy))
+            if ncopy > 64:
+                rotate_sets.append(None)
+                continue
+            group = [calls[i]]
+            for _ in range(ncopy - 1):
+                o = torch.empty_like(outs[i])
+                group.append(bind(case, x.clone(), packed[i].clone(),
+                                  src.clone() if src is not None else None, o))
+            rotate_sets.append(group)
+        torch.cuda.synchronize(dev)
+
     def new_events():
         n = len(calls) if per_conv_flush else 1
         return [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
                 for _ in range(n)]
 
     def step(evs):
-        """One step.  Baseline set: each conv after its own flush, inside its own
-        events.  Otherwise: one flush, then the convs back to back inside one
-        pair of events (a conv may set up while the previous one drains:
-        programmatic dependent launch)."""
+        """One step.  Baseline set: each conv's stream of launches (or its one
+        launch after a flush) inside its own events.  Otherwise: one flush,
+        then the convs back to back inside one pair of events (a conv may set
+        up while the previous one drains: programmatic dependent launch)."""
         if per_conv_flush:
-            for call, (e0, e1) in zip(calls, evs):
-                flush.fill_(1)
-                e0.record(stream)
-                call()
-                e1.record(stream)
+            for i, (e0, e1) in enumerate(evs):
+                group = rotate_sets[i]
+                if group is None:
+                    flush.fill_(1)
+                    e0.record(stream)
+                    calls[i]()
+                    e1.record(stream)
+                else:
+                    e0.record(stream)
+                    for call in group:
+                        call()
+                    e1.record(stream)
         else:
             flush.fill_(1)
             evs[0][0].record(stream)
             for call in calls:
                 call()
             evs[0][1].record(stream)
+
+    def launches_of(i):
+        if per_conv_flush and rotate_sets[i] is not None:
+            return len(rotate_sets[i])
+        return 1
 
     warm_ev = new_events()
     for _ in range(args.warmup):
@@ -444,12 +486,29 @@ def run_ours(args, world, rank, local):
     status, bits = cg.conv_check_device_status(workspace)
     if status != 0:
         raise RuntimeError("device status after timing: %s (bits %d)" % (cg.conv_status_string(status), bits))
-    step_ms = [sum(a.elapsed_time(b) for a, b in ev[k]) for k in range(args.steps)]
 
+    isolated_ms = None
     if per_conv_flush:
-        per_kernel_ms = [[ev[k][i][0].elapsed_time(ev[k][i][1]) for k in range(args.steps)]
-                         for i in range(len(calls))]
+        # Per-launch time of conv i in step k; a step's time is their sum.
+        per_kernel_ms = [[ev[k][i][0].elapsed_time(ev[k][i][1]) / launches_of(i)
+                          for k in range(args.steps)] for i in range(len(calls))]
+        step_ms = [sum(per_kernel_ms[i][k] for i in range(len(calls))) for k in range(args.steps)]
+        # For reference: every conv alone between events right after a flush
+        # (this includes the launch latency a stream of launches hides).
+        reps = 20
+        iev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                for _ in calls] for _ in range(reps)]
+        for k in range(reps):
+            for i, call in enumerate(calls):
+                flush.fill_(1)
+                iev[k][i][0].record(stream)
+                call()
+                iev[k][i][1].record(stream)
+        torch.cuda.synchronize(dev)
+        isolated_ms = [statistics.median(iev[k][i][0].elapsed_time(iev[k][i][1]) for k in range(reps))
+                       for i in range(len(calls))]
     else:
+        step_ms = [sum(a.elapsed_time(b) for a, b in ev[k]) for k in range(args.steps)]
         # Per-kernel durations (for the roofline): every launch bracketed by
         # its own events on the launch stream, each step after an L2 flush.
         kreps = max(10, min(args.steps, 100))
@@ -511,6 +570,13 @@ def run_ours(args, world, rank, local):
             "p90_us": round(_pct(per_kernel_ms[i], 90) * 1e3, 3),
             "host_us_per_call": round(host_us[i], 2), "call_to_sync_us": round(sync_us[i], 2),
             "traffic": lookup_traffic(c.name)}
+        if per_conv_flush:
+            n = launches_of(i)
+            per_kernel[c.name]["timing"] = (
+                "stream of %d back-to-back launches over rotating copies (%d MB in all)"
+                % (n, n * c.bytes >> 20) if rotate_sets[i] is not None
+                else "one launch between events after an L2 flush")
+            per_kernel[c.name]["us_isolated"] = round(isolated_ms[i] * 1e3, 3)
     dcase = cases[dom]
     dbound, dpeak = conv_bound(dcase, peaks)
     if dbound == "hbm":
@@ -543,9 +609,13 @@ def run_ours(args, world, rank, local):
         "dtype": workload_dtype(cases),
         "data": "synthetic",
         "config": {"workload": args.workload + ": " + describe(cases),
-                   "l2": "flushed before every %s (write of %d MiB), flush outside the events"
-                         % ("conv" if per_conv_flush else "step", flush.numel() >> 20),
-                   "step_time": "sum of the convs' own event times" if per_conv_flush
+                   "l2": ("inputs larger than L2: each conv streams over rotating copies of "
+                          "its tensors totalling >= 3 x L2 (%d MiB); a conv too small for that "
+                          "runs after a flush (write of %d MiB) outside its events"
+                          % (3 * l2 >> 20, flush.numel() >> 20)) if per_conv_flush else
+                         "flushed before every step (write of %d MiB), flush outside the events"
+                         % (flush.numel() >> 20),
+                   "step_time": "sum over the convs of their per-launch event time" if per_conv_flush
                                 else "events around the whole step",
                    "filters": "packed once before timing",
                    "parallelism": "replicas" if world > 1 else "single GPU",
@@ -553,7 +623,7 @@ def run_ours(args, world, rank, local):
         "roofline": roof,
         "cpu_baseline": cpu,
         "e2e": e2e,
-        "gpu_launches": len(calls) * args.steps,
+        "gpu_launches": sum(launches_of(i) for i in range(len(calls))) * args.steps,
         "step_us_p10_p90": [round(_pct(step_ms, 10) * 1e3, 2), round(_pct(step_ms, 90) * 1e3, 2)],
         "clocks": clocks,
         "pack_us": round(pack_us, 2),

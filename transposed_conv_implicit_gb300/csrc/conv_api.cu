@@ -17,6 +17,7 @@
 #include <cstdlib>
 #include <cstring>
 #include <mutex>
+#include <new>
 
 #include "../../include/conv_gb300.h"
 #include "../../include/conv_gb300_testing.h"
@@ -1683,7 +1684,11 @@ struct CallKey {
   uint32_t beta_bits;
 };
 
-constexpr int kCacheEntries = 32;
+// Open addressing: a key's home slot is its hash modulo the table size and
+// it may sit in any of the kProbe slots from there; a store into a full
+// window replaces the slot after the one replaced last.
+constexpr int kCacheEntries = 1024;
+constexpr int kProbe = 8;
 struct CacheSlot {
   bool valid;
   CallKey key;
@@ -1691,9 +1696,20 @@ struct CacheSlot {
 };
 
 std::mutex g_cache_mu;
-CacheSlot g_cache[kCacheEntries];
-int g_cache_next = 0;
+CacheSlot* g_cache = nullptr;  // kCacheEntries slots, allocated on first use
+int g_cache_victim = 0;
 std::atomic<unsigned long long> g_cache_hits{0}, g_cache_misses{0};
+
+uint64_t key_hash(const CallKey& key) {
+  // FNV-1a over the key's bytes (padding included: keys are zero-filled).
+  const unsigned char* b = reinterpret_cast<const unsigned char*>(&key);
+  uint64_t h = 1469598103934665603ull;
+  for (size_t i = 0; i < sizeof(key); ++i) {
+    h ^= b[i];
+    h *= 1099511628211ull;
+  }
+  return h;
+}
 
 CallKey make_key(int entry, const void* input, const void* filter, const void* output,
                  const void* source, const void* workspace, size_t workspace_bytes, int n, int h,
@@ -1726,12 +1742,16 @@ CallKey make_key(int entry, const void* input, const void* filter, const void* o
 }
 
 bool cache_lookup(const CallKey& key, Prepared* out) {
+  const size_t home = key_hash(key) % kCacheEntries;
   std::lock_guard<std::mutex> lock(g_cache_mu);
-  for (int i = 0; i < kCacheEntries; ++i) {
-    if (g_cache[i].valid && std::memcmp(&g_cache[i].key, &key, sizeof(key)) == 0) {
-      *out = g_cache[i].prep;
-      g_cache_hits.fetch_add(1, std::memory_order_relaxed);
-      return true;
+  if (g_cache) {
+    for (int i = 0; i < kProbe; ++i) {
+      const CacheSlot& slot = g_cache[(home + i) % kCacheEntries];
+      if (slot.valid && std::memcmp(&slot.key, &key, sizeof(key)) == 0) {
+        *out = slot.prep;
+        g_cache_hits.fetch_add(1, std::memory_order_relaxed);
+        return true;
+      }
     }
   }
   g_cache_misses.fetch_add(1, std::memory_order_relaxed);
@@ -1739,9 +1759,21 @@ bool cache_lookup(const CallKey& key, Prepared* out) {
 }
 
 void cache_store(const CallKey& key, const Prepared& prep) {
+  const size_t home = key_hash(key) % kCacheEntries;
   std::lock_guard<std::mutex> lock(g_cache_mu);
-  CacheSlot& slot = g_cache[g_cache_next];
-  g_cache_next = (g_cache_next + 1) % kCacheEntries;
+  if (!g_cache) {
+    g_cache = new (std::nothrow) CacheSlot[kCacheEntries];
+    if (!g_cache) return;  // no cache: every call prepares afresh
+    for (int i = 0; i < kCacheEntries; ++i) g_cache[i].valid = false;
+  }
+  int pick = -1;
+  for (int i = 0; i < kProbe && pick < 0; ++i)
+    if (!g_cache[(home + i) % kCacheEntries].valid) pick = i;
+  if (pick < 0) {
+    pick = g_cache_victim;
+    g_cache_victim = (g_cache_victim + 1) % kProbe;
+  }
+  CacheSlot& slot = g_cache[(home + pick) % kCacheEntries];
   slot.key = key;
   slot.prep = prep;
   slot.valid = true;
