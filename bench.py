@@ -380,7 +380,9 @@ def run_ours(args, world, rank, local):
         else:
             packed.append(cg.conv2d_pack_filter(w, filter_is_fcrs=case.filter_layout == "FCRS"))
     pack_ev[1].record(stream)
-    workspace = cg.new_workspace(cg.CONV_STATUS_BYTES, dev)
+    # A workspace with room for stream-K partials (the planner then uses that
+    # schedule where it expects a gain).
+    workspace = cg.new_workspace(cg.CONV_STATUS_BYTES + cg.conv_streamk_workspace_size(), dev)
 
     def bind(case, x, pk, src, out):
         st, pd = (case.stride,) * 2, case.pads
@@ -692,7 +694,7 @@ def run_e2e(args, cases, inputs, dev, stream):
             packed.append(cg.conv_transposed_pack_filter(w, stride=st, padding=pd))
         else:
             packed.append(cg.conv2d_pack_filter(w, filter_is_fcrs=case.filter_layout == "FCRS"))
-    ws = cg.new_workspace(cg.CONV_STATUS_BYTES, dev)
+    ws = cg.new_workspace(cg.CONV_STATUS_BYTES + cg.conv_streamk_workspace_size(), dev)
     n_in = n_out = 1
     s_ins = [torch.cuda.Stream(dev) for _ in range(n_in)]
     s_outs = [torch.cuda.Stream(dev) for _ in range(n_out)]

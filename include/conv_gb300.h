@@ -95,6 +95,20 @@ conv_status_t conv2d_pack_filter(const void* filter, int r, int s, int c_in, int
  * filter.  conv2d_fwd_packed needs only CONV_STATUS_BYTES. */
 size_t conv2d_workspace_size(int r, int s, int c_in, int c_out, conv_dtype_t dtype);
 
+/* Extra workspace that enables the stream-K schedule on the current device:
+ * for convolutions whose output tiles fill less than one wave of the GPU's
+ * SMs, every SM takes an equal share of the (tile, k-block) iterations, and
+ * a tile split between CTAs is summed through fp32 partial tiles kept in the
+ * workspace (one slot of up to 128 KB per SM, plus flags).  A workspace of
+ * at least (conv2d_workspace_size or CONV_STATUS_BYTES for the packed entry
+ * points, or conv_transposed_workspace_size) + this many bytes lets every
+ * forward and transposed call use it where the planner expects a gain; a
+ * smaller workspace only disables it.  Launches that use stream-K keep
+ * their partials and flags in the workspace: launches that may overlap on
+ * the GPU need separate workspaces.  Returns 0 when no device is current.
+ * No counterpart on the pages: a schedule of the implicit GEMM's tiles. */
+size_t conv_streamk_workspace_size(void);
+
 /* ------------------------------------------------------------------------
  * Forward convolution ("dispatch_amd_4wave_conv2d", signature and Args):
  *   y[n][oy][ox][f] = act( sum_{r,s,c} x[n][oy*st - p + r][ox*st - p + s][c] * W(r,s,c,f)
@@ -207,8 +221,10 @@ conv_status_t conv_transposed_packed(const void* input, int n, int h, int w, int
  * allocation, or a real-time loop whose policy forbids cudaMalloc after
  * start-up -- and so cannot provide conv2d_fwd's workspace.
  *
- * Arguments, gates and results are those of conv2d_fwd (raw FCRS/RSCF filter;
- * the caller still passes input, filter, output and source).  The packed
+ * Arguments, gates and results are those of conv2d_fwd called with a
+ * workspace of exactly conv2d_workspace_size bytes (raw FCRS/RSCF filter; the
+ * caller still passes input, filter, output and source): the same plan, so
+ * the same output bits.  The packed
  * filter and the status word go to a library-owned scratch array of 8 MiB
  * (CONV_NOALLOC_SCRATCH_BYTES) that lives in device memory of every GPU that
  * loads the library until the process exits.  Filters whose packed size plus

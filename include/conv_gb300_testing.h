@@ -21,7 +21,11 @@ extern "C" {
  * a way that only exercises its bounded waits:
  *   mode 0: normal operation (the default);
  *   mode 1: CTA 0's producer skips the arrive of its first k-block, so the
- *           MMA warp's wait on it can only end by running out of time.
+ *           MMA warp's wait on it can only end by running out of time (for
+ *           CTA pairs: both CTAs of the first pair leave their first stage
+ *           un-armed and unloaded);
+ *   mode 2: stream-K launches never publish their partial tiles, so the CTAs
+ *           that finish split tiles wait for them until the limit runs out.
  * timeout_ns sets the per-wait limit of subsequent launches (0 = default,
  * one second).  The kernel then records CONV_ERR_DEVICE_TIMEOUT in the
  * workspace status word, releases its tensor memory and returns; nothing
@@ -43,7 +47,8 @@ conv_status_t conv_testing_im2col_tile(const void* input, int n, int h, int w, i
                                        void* status_workspace, void* stream);
 
 /* The tile and shared-memory configuration the dispatcher picks for a
- * forward convolution: out[0] = bn (tile width along C_out), out[1] = bk
+ * forward convolution through conv2d_fwd_packed with a workspace of
+ * workspace_bytes: out[0] = bn (tile width along C_out), out[1] = bk
  * (channels per k-block), out[2] = pipeline stages, out[3] = dynamic shared
  * memory bytes, out[4] = total tiles, out[5] = grid size (CTAs), out[6] =
  * TMEM columns, out[7] = epilogue mode (0 direct stores, 1 TMA 2-D, 2 TMA
@@ -53,11 +58,12 @@ conv_status_t conv_testing_im2col_tile(const void* input, int n, int h, int w, i
  * the row-tap kernel (few output channels: the filter taps along S and the
  * output channels share the MMA's N) out[0] = R * g16 (MMA width), out[10] =
  * output rows per tile.  out[12] = 1 when CTA pairs (clusters of two CTAs
- * sharing 256-row tiles through cta_group::2 MMAs) run the conv.  Host-only. */
+ * sharing 256-row tiles through cta_group::2 MMAs) run the conv.  out[13] = 1
+ * when the stream-K schedule runs it.  Host-only. */
 conv_status_t conv_testing_fwd_plan(int n, int h, int w, int c_in, conv_dtype_t dtype, int r,
                                     int s, int c_out, const int stride[2],
                                     const int symmetric_padding[2], int has_residual, int num_sms,
-                                    int out[13]);
+                                    size_t workspace_bytes, int out[14]);
 
 /* Read the CONV_* tuning overrides from the environment again (the library
  * reads them once, on first use) and invalidate every cached prepared call.

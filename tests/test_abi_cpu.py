@@ -155,12 +155,12 @@ def test_pack_validation(lib):
                                            F16, D, 1 << 20, None) == NOTSUP
 
 
-def _plan(lib, n, h, w, c, dt, r, f, st, pd, res=0, sms=148):
-    out = (ctypes.c_int * 13)()
+def _plan(lib, n, h, w, c, dt, r, f, st, pd, res=0, sms=148, ws=256):
+    out = (ctypes.c_int * 14)()
     assert lib.conv_testing_fwd_plan(n, h, w, c, dt, r, r, f, _lib.pair((st, st)), _lib.pair((pd, pd)),
-                                     res, sms, out) == OK
+                                     res, sms, ws, out) == OK
     keys = ("bn", "bk", "stages", "smem", "tiles", "grid", "tmem", "epi", "bres", "srcb", "stgb",
-            "loader", "pair")
+            "loader", "pair", "streamk")
     return dict(zip(keys, list(out)))
 
 
@@ -221,9 +221,9 @@ def test_row_tap_plan_invariants(lib, tuning):
         f = rng.randint(1, 32 // s_)
         n, h, w = rng.randint(1, 3), rng.randint(r, 70), rng.randint(s_, 300)
         pd = rng.randint(0, r - 1) if r == s_ else 0
-        out = (ctypes.c_int * 13)()
+        out = (ctypes.c_int * 14)()
         st = lib.conv_testing_fwd_plan(n, h, w, c, dt, r, s_, f, _lib.pair((1, 1)), _lib.pair((pd, pd)),
-                                       0, 152, out)
+                                       0, 152, 256, out)
         assert st == OK
         if out[11] != 3:
             continue
@@ -257,9 +257,9 @@ def test_cta_pair_plan_invariants(lib, tuning):
         pd = rng.randint(0, r - 1)
         n, h, w = rng.randint(1, 4), rng.randint(r, 90), rng.randint(r, 90)
         sms = rng.choice([8, 20, 152])
-        out = (ctypes.c_int * 13)()
+        out = (ctypes.c_int * 14)()
         if lib.conv_testing_fwd_plan(n, h, w, c, dt, r, r, f, _lib.pair((st, st)), _lib.pair((pd, pd)),
-                                     rng.randint(0, 1), sms, out) != OK:
+                                     rng.randint(0, 1), sms, 256, out) != OK:
             continue
         p = dict(zip(("bn", "bk", "stages", "smem", "tiles", "grid", "tmem", "epi", "bres", "srcb",
                       "stgb", "loader", "pair"), list(out)))
@@ -394,3 +394,36 @@ def test_failed_calls_are_never_cached(lib):
         assert status == INVALID   # Ho = 9 does not match the shape
     h1, m1 = _cache_stats(lib)
     assert (h1 - h0, m1 - m0) == (0, 3)
+
+
+SK_WS = 256 + 152 * 8 * 4 + 152 * 128 * 1024 + 4096   # status + stream-K room for 152 SMs
+
+
+def test_streamk_planner(lib, tuning):
+    """Stream-K (every SM an equal share of the (tile, k-block) iterations,
+    split tiles summed through fp32 partial slots) is chosen by its cost model
+    only where few tiles carry a long contraction; it needs the workspace
+    room; CONV_STREAMK=1 forces it where it applies (never with the row
+    window, the gather loader or CTA pairs) and 0 forbids it."""
+    tuning("CONV_STREAMK", None)
+    tuning("CONV_PAIR", None)
+    # Few tiles, long contraction: 2 x 8 x 8 x 1024 -> 256, 3x3 s2 (32 rows, K = 9216).
+    deep = (2, 8, 8, 1024, BF16, 3, 256, 2, 1)
+    p = _plan(lib, *deep, sms=152, ws=SK_WS)
+    assert p["streamk"] == 1 and p["grid"] == 152 and p["bres"] == 0
+    assert _plan(lib, *deep, sms=152, ws=256)["streamk"] == 0          # no workspace room
+    # The benchmark convs keep whole tiles (the fix-up outweighs the balance).
+    for conv in [(32, 56, 56, 64, BF16, 3, 128, 2, 1), (8, 128, 128, 128, F16, 5, 128, 2, 2),
+                 (1, 16, 16, 16, BF16, 3, 16, 1, 1), (16, 64, 64, 320, F8, 3, 320, 1, 1),
+                 (1, 256, 256, 512, BF16, 3, 512, 1, 1)]:
+        assert _plan(lib, *conv, sms=152, ws=SK_WS)["streamk"] == 0, conv
+    tuning("CONV_STREAMK", "1")
+    q = _plan(lib, 8, 128, 128, 128, F16, 5, 128, 2, 2, sms=152, ws=SK_WS)
+    assert (q["streamk"], q["grid"], q["tiles"]) == (1, 152, 128)
+    assert _plan(lib, 32, 56, 56, 64, BF16, 3, 64, 1, 1, sms=152, ws=SK_WS)["streamk"] == 0  # window
+    assert _plan(lib, 32, 224, 224, 3, BF16, 7, 64, 2, 3, sms=152, ws=SK_WS)["streamk"] == 0  # gather
+    tuning("CONV_PAIR", "1")
+    assert _plan(lib, 8, 128, 128, 128, F16, 5, 128, 2, 2, sms=152, ws=SK_WS)["streamk"] == 0  # pairs
+    tuning("CONV_PAIR", None)
+    tuning("CONV_STREAMK", "0")
+    assert _plan(lib, *deep, sms=152, ws=SK_WS)["streamk"] == 0

@@ -277,13 +277,90 @@ def test_cta_pair_every_element(case, tuning):
         H.assert_parity(case, inp, got, ref)
 
 
+# Stream-K forced on (CONV_STREAMK=1, a workspace with room for its partial
+# tiles).  On these small convs most SMs hold one or two k-blocks of the
+# iteration sequence, so every tile is split between several CTAs: the
+# finisher adds many partials.  Ragged M tails, several C_out tiles, the
+# direct-store epilogue (C_out 3 and 17), a residual source, partial channel
+# blocks, fp8, and transposed convs whose phases have equal or unequal K.
+STREAMK_CASES = (
+    "b_3x3_s2p1", "b_5x5_s2p2", "b_5x5_s1p2_res", "b_3x3_s1p0", "b_1x1_s2p0", "b_cout17_res",
+    "b_cout272", "b_cout512_silu", "b_cin48_64B", "h_5x5_s2p2", "h_cout3", "e_3x3_s1p1_res",
+    "e_3x3_s2p1", "e_5x5_p2_relu", "b_cin80_partial_block", "e_cin160_partial_block",
+    "b_window_cout256", "b_tiny_image", "b_pad3_7x7_s2", "t_h_4x4_s2p1_relu", "t_b_3x3_s2p1_op1",
+    "t_b_3x3_s2p1_op0", "t_h_5x5_s2p2_res", "t_b_2x2_s2p0", "t_e_4x4_s2p1", "t_h_cout3",
+    "t_h_cout256_silu", "t_h_cin80_partial_block", "int_b_3x3", "int_b_s2_res", "int_h_5x5",
+    "int_e_3x3", "int_h_tr", "int_e_tr")
+
+
+def _streamk_cases():
+    return [c for c in SMALL_FWD + SMALL_TR + INT_CASES if c.name in STREAMK_CASES]
+
+
+def streamk_workspace(device="cuda"):
+    import transposed_conv_implicit_gb300 as cg
+    return cg.new_workspace(cg.CONV_STATUS_BYTES + cg.conv_streamk_workspace_size(), device)
+
+
+def plan_of(case, workspace_bytes):
+    """The dispatcher's plan for a forward case through conv2d_fwd_packed on this device."""
+    import ctypes
+    from transposed_conv_implicit_gb300 import _lib
+    out = (ctypes.c_int * 14)()
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    st = _lib.lib().conv_testing_fwd_plan(
+        case.N, case.H, case.W, case.C_in, _lib.DTYPE_CODES[case.dtype], case.R, case.S, case.C_out,
+        _lib.pair((case.stride,) * 2), _lib.pair(case.pads), int(case.has_residual), sms,
+        workspace_bytes, out)
+    assert st == 0
+    return list(out)
+
+
+@pytest.mark.parametrize("case", _streamk_cases(), ids=lambda c: c.name)
+def test_streamk_every_element(case, tuning):
+    """Stream-K forced on: every element against the oracle, integer cases
+    bit-exact, and a clean status word."""
+    import transposed_conv_implicit_gb300 as cg
+    tuning("CONV_STREAMK", "1")
+    ws = streamk_workspace()
+    if case.kind == "fwd":
+        assert plan_of(case, ws.numel())[13] == 1
+    inp = synthetic.make_inputs(case)
+    out = H.run_gpu(case, inp, workspace=ws)
+    status, bits = cg.conv_check_device_status(ws)
+    assert status == 0 and bits == 0
+    got = H.decode(out.cpu(), case.out_dtype)
+    ref = H.oracle_full(case, inp)
+    if case.name.startswith("int_"):
+        mism = np.argwhere(got != ref)
+        assert mism.size == 0, mism[:5].tolist()
+    else:
+        H.assert_parity(case, inp, got, ref)
+
+
+def test_streamk_chosen_for_a_deep_contraction():
+    """The planner's own choice (no override): 32 output rows over a
+    contraction of 9216 leave most SMs idle with whole tiles, so stream-K
+    spreads the k-blocks over all of them; every element against the oracle."""
+    import transposed_conv_implicit_gb300 as cg
+    case = _fwd("b_deepk_s2", "bf16", 2, 8, 8, 1024, 256, 3, 2, 1, res=True, beta=-1.0, epi="relu")
+    ws = streamk_workspace()
+    assert plan_of(case, ws.numel())[13] == 1
+    inp = synthetic.make_inputs(case)
+    out = H.run_gpu(case, inp, workspace=ws)
+    status, bits = cg.conv_check_device_status(ws)
+    assert status == 0 and bits == 0
+    H.assert_parity(case, inp, H.decode(out.cpu(), "bf16"), H.oracle_full(case, inp))
+
+
 @pytest.mark.parametrize("name", list(WORKLOADS), ids=str)
 def test_full_size_workload_sampled(name):
-    """Full-size workloads, sampled outputs checked against the oracle point by
-    point; every output must be finite."""
+    """Full-size workloads in the launch configuration the benchmark times
+    (packed filter, a workspace with stream-K room), sampled outputs checked
+    against the oracle point by point; every output must be finite."""
     case = WORKLOADS[name]
     inp = synthetic.make_inputs(case)
-    out = H.run_gpu(case, inp).cpu()
+    out = H.run_gpu(case, inp, workspace=streamk_workspace()).cpu()
     flat = H.decode(out, case.out_dtype).reshape(-1)
     assert np.isfinite(flat).all()
     pts = H.sample_points(case, 3000, seed=11)

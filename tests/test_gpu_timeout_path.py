@@ -16,7 +16,7 @@ import torch
 
 import transposed_conv_implicit_gb300 as cg
 from tests import _harness as H
-from tests.test_gpu_parity import _fwd, _tr
+from tests.test_gpu_parity import _fwd, _tr, streamk_workspace
 from transposed_conv_implicit_gb300 import _lib, synthetic
 
 pytestmark = pytest.mark.gpu
@@ -49,39 +49,60 @@ PAIR_CASES = [
 ]
 
 
+# Stream-K forced on with the partials never published (fault mode 2): the
+# CTAs that finish split tiles wait for them until the limit runs out.  The
+# launch after it must be right again: its flags carry a new launch value, so
+# the stale partial slots and flags of the failed launch are never taken.
+STREAMK_CASES = [
+    _fwd("sk_s2_res", "bf16", 2, 13, 11, 64, 96, 3, 2, 1, res=True, beta=0.5),
+    _tr("sk_transposed", "f16", 2, 8, 8, 64, 64, 4, 2, 1),
+]
+
+
 @pytest.mark.parametrize("case", CASES, ids=lambda c: c.name)
 def test_timeout_is_reported_and_context_survives(case):
     _timeout_then_normal(case)
+
+
+@pytest.mark.parametrize("case", STREAMK_CASES, ids=lambda c: c.name)
+def test_streamk_partial_timeout_is_reported_and_context_survives(case, tuning):
+    tuning("CONV_STREAMK", "1")
+    ws = streamk_workspace("cuda:0")
+    _timeout_then_normal(case, mode=2, ws=ws)
 
 
 @pytest.mark.parametrize("case", PAIR_CASES, ids=lambda c: c.name)
 def test_cta_pair_timeout_is_reported_and_context_survives(case, tuning):
     tuning("CONV_PAIR", "1")
     if case.kind == "fwd":   # the planner must put it on CTA pairs on this device
-        plan = (ctypes.c_int * 13)()
+        plan = (ctypes.c_int * 14)()
         sms = torch.cuda.get_device_properties(0).multi_processor_count
         st = _lib.lib().conv_testing_fwd_plan(
             case.N, case.H, case.W, case.C_in, _lib.DTYPE_CODES[case.dtype], case.R, case.S,
             case.C_out, _lib.pair((case.stride,) * 2), _lib.pair(case.pads), int(case.has_residual),
-            sms, plan)
+            sms, 256, plan)
         assert st == 0 and plan[12] == 1, list(plan)
     _timeout_then_normal(case)
 
 
-def _timeout_then_normal(case):
+def _timeout_then_normal(case, mode=1, ws=None):
     inp = synthetic.make_inputs(case)
-    ws = cg.new_workspace(cg.CONV_STATUS_BYTES, "cuda:0")
+    if ws is None:
+        ws = cg.new_workspace(cg.CONV_STATUS_BYTES, "cuda:0")
     lib = _lib.lib()
     try:
-        lib.conv_testing_set_wait_fault(1, TIMEOUT_NS)
+        lib.conv_testing_set_wait_fault(mode, TIMEOUT_NS)
         H.run_gpu(case, inp, workspace=ws)
         status, bits = cg.conv_check_device_status(ws)
     finally:
         lib.conv_testing_set_wait_fault(0, 0)
     assert status == cg.CONV_ERR_DEVICE_TIMEOUT, cg.conv_status_string(status)
-    # Which role's wait ran out first (MMA = 2, epilogue = 4, producer = 1)
-    # depends on timing; at least one did, and nothing else was recorded.
-    assert bits != 0 and bits & ~7 == 0, bits
+    # Which role's wait ran out first (MMA = 2, epilogue = 4, producer = 1,
+    # a stream-K partial = 8) depends on timing; at least one did, and
+    # nothing else was recorded.  Fault mode 2 always leaves the partial's.
+    assert bits != 0 and bits & ~15 == 0, bits
+    if mode == 2:
+        assert bits & 8, bits
 
     # The status was cleared by the check; a normal launch is right again.
     out = H.run_gpu(case, inp, workspace=ws)

@@ -22,7 +22,8 @@ from ._lib import (CONV_ERR_CUDA, CONV_ERR_DEVICE_TIMEOUT, CONV_ERR_INVALID_VALU
 
 __all__ = [
     "conv2d_fwd", "conv2d_fwd_packed", "conv2d_pack_filter", "conv2d_packed_filter_bytes",
-    "conv2d_workspace_size", "conv_transposed", "conv_transposed_packed",
+    "conv2d_workspace_size", "conv_streamk_workspace_size", "conv_transposed",
+    "conv_transposed_packed",
     "conv_transposed_pack_filter", "conv_transposed_packed_filter_bytes",
     "conv_transposed_workspace_size", "conv_check_device_status", "conv_status_string",
     "ConvError", "ExtensionMissing", "new_workspace", "dtype_name", "library_path",
@@ -89,6 +90,11 @@ def conv2d_packed_filter_bytes(r, s, c_in, c_out, dtype: str) -> int:
 
 def conv2d_workspace_size(r, s, c_in, c_out, dtype: str) -> int:
     return _lib.lib().conv2d_workspace_size(r, s, c_in, c_out, _lib.DTYPE_CODES[dtype])
+
+
+def conv_streamk_workspace_size() -> int:
+    """Extra workspace bytes that enable the stream-K schedule on the current device."""
+    return _lib.lib().conv_streamk_workspace_size()
 
 
 def conv2d_pack_filter(filter, *, filter_is_fcrs: bool, out=None, stream=None):

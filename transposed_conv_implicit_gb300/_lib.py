@@ -38,7 +38,7 @@ EXPORTS = (
     "conv_transposed_pack_filter", "conv_transposed", "conv_transposed_packed",
     "conv_check_device_status", "conv_testing_set_wait_fault", "conv_testing_im2col_tile",
     "conv_testing_fwd_plan", "conv2d_fwd_noalloc", "conv_testing_reload_tuning",
-    "conv_testing_cache_stats",
+    "conv_testing_cache_stats", "conv_streamk_workspace_size",
 )
 
 
@@ -55,6 +55,8 @@ def _declare(lib):
     lib.conv2d_packed_filter_bytes.restype = Z
     lib.conv2d_workspace_size.argtypes = [I, I, I, I, I]
     lib.conv2d_workspace_size.restype = Z
+    lib.conv_streamk_workspace_size.argtypes = []
+    lib.conv_streamk_workspace_size.restype = Z
     lib.conv2d_pack_filter.argtypes = [P, I, I, I, I, I, I, P, Z, P]
     lib.conv2d_pack_filter.restype = I
     fwd_tail = [IP, IP, IP, I, I, P, F, I, P, Z, P]
@@ -82,7 +84,7 @@ def _declare(lib):
     lib.conv_testing_set_wait_fault.restype = None
     lib.conv_testing_im2col_tile.argtypes = [P, I, I, I, I, I, I, I, IP, IP, I, I, I, I, P, IP, P, P]
     lib.conv_testing_im2col_tile.restype = I
-    lib.conv_testing_fwd_plan.argtypes = [I, I, I, I, I, I, I, I, IP, IP, I, I, IP]
+    lib.conv_testing_fwd_plan.argtypes = [I, I, I, I, I, I, I, I, IP, IP, I, I, Z, IP]
     lib.conv_testing_fwd_plan.restype = I
     lib.conv_testing_reload_tuning.argtypes = []
     lib.conv_testing_reload_tuning.restype = None

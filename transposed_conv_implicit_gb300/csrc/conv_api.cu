@@ -42,12 +42,14 @@ int elt_bytes(conv_dtype_t d) { return d == CONV_DTYPE_F8E4M3 ? 1 : 2; }
 // CONV_MAX_STAGES (caps the operand ring), CONV_SRC_BUFS (1: one residual
 // source buffer), CONV_PAIR (1/0: force CTA pairs on/off), CONV_WINDOW,
 // CONV_ROWTAP, CONV_GATHER_STAGE and CONV_L2_PREFETCH (-1 disables that
-// loader or feature), CONV_ROWTAP_BAND, CONV_WAIT_HINT_NS.  Read once per
-// process, on first use; conv_testing_reload_tuning() reads them again.
+// loader or feature), CONV_ROWTAP_BAND, CONV_STREAMK (1/0: force the
+// stream-K schedule on where it applies / off), CONV_WAIT_HINT_NS.  Read once
+// per process, on first use; conv_testing_reload_tuning() reads them again.
 struct Tuning {
   int tile_m, tile_n, max_stages, src_bufs, window, rowtap, rowtap_band, gather_stage, l2_prefetch;
   int filter_resident;  // -1 when unset
   int pair;             // -1 when unset
+  int streamk;          // -1 when unset
   uint32_t wait_hint_ns;
 };
 
@@ -74,6 +76,7 @@ Tuning read_tuning() {
   t.l2_prefetch = env_int("CONV_L2_PREFETCH");
   t.filter_resident = env_int_or("CONV_FILTER_RESIDENT", -1);
   t.pair = env_int_or("CONV_PAIR", -1);
+  t.streamk = env_int_or("CONV_STREAMK", -1);
   t.wait_hint_ns = static_cast<uint32_t>(env_int("CONV_WAIT_HINT_NS"));
   return t;
 }
@@ -179,6 +182,7 @@ struct Plan {
   // packing description of the transposed filter, per phase slot
   int r0h[kMaxPhases], r0w[kMaxPhases], th[kMaxPhases], tw[kMaxPhases];
   int sh, sw;
+  size_t sk_offset;    // stream-K flags and partial slots: this far into the workspace
 };
 
 // Channels per k-block: rows of 128, 64 or 32 bytes (the swizzle span).  The
@@ -469,6 +473,74 @@ void plan_pair(Plan* pl, int num_sms) {
   kp.idesc = make_idesc(pl->in_dtype, kp.bn, 2 * kBM);
 }
 
+// Stream-K schedule: when the tiles fill less than one wave of CTAs, the
+// sequence of (tile, k-block) iterations is cut into one equal share per SM
+// (work items end at tile boundaries); a tile split between CTAs is summed
+// through fp32 partial slots in the workspace.  Cost model, in k-block
+// times: the tile-per-CTA schedule's k-blocks per tile against the even share
+// plus the fix-up.  Measured on this part, writing a 128 KB partial tile and
+// reading it back take ~8 us of a CTA's critical path, against ~0.47 us for
+// a 48 KB k-block: the fix-up is charged as 8x the partial tile's bytes in
+// k-block loads, so stream-K pays for few tiles with a long contraction
+// (small images with many channels), not for the benchmark convs.
+// Needs `room` workspace bytes (streamk_bytes); TMA im2col loader, streamed
+// filter, no CTA pairs, one channel group, every phase with filter taps.
+// CONV_STREAMK=1 forces it where it applies, 0 forbids it.
+size_t sk_slot_bytes(const ConvKernelParams& kp) {
+  return static_cast<size_t>(kBM) * kp.m_halves * kp.bn * sizeof(float);
+}
+
+size_t sk_flag_bytes(int ctas) {
+  return (static_cast<size_t>(ctas) * kEpilogueWarps * sizeof(unsigned int) + 255) & ~size_t(255);
+}
+
+size_t streamk_bytes(const ConvKernelParams& kp, int ctas) {
+  return sk_flag_bytes(ctas) + static_cast<size_t>(ctas) * sk_slot_bytes(kp);
+}
+
+void plan_streamk(Plan* pl, int num_sms, size_t room) {
+  ConvKernelParams& kp = pl->kp;
+  kp.streamk = 0;
+  const int force = tuning().streamk;
+  if (force == 0 || num_sms < 2) return;
+  if (kp.pair || kp.window || kp.gather || kp.groups > 1) return;
+  long long iters = 0;
+  int kpt_max = 0;
+  for (int ph = 0; ph < kp.num_phases; ++ph) {
+    const int kpt = kp.taps_h[ph] * kp.taps_w[ph] * kp.c_blocks;
+    if (kpt <= 0) return;
+    kpt_max = std::max(kpt_max, kpt);
+    iters += static_cast<long long>(kp.tile_start[ph + 1] - kp.tile_start[ph]) * kpt;
+  }
+  if (iters <= 0 || iters >= (1ll << 31)) return;
+  if (room < streamk_bytes(kp, num_sms)) return;
+  if (force != 1) {
+    if (kp.total_tiles >= num_sms) return;  // a full wave or more: whole tiles
+    const long long share = (iters + num_sms - 1) / num_sms;
+    const double kblock_bytes = static_cast<double>(kBM * kp.m_halves + kp.bn) * kp.sw_bytes;
+    const double fixup = 8.0 * static_cast<double>(sk_slot_bytes(kp)) / kblock_bytes;
+    if (kpt_max < 4 || static_cast<double>(share) + fixup > 0.85 * kpt_max) return;
+  }
+  kp.streamk = 1;
+  kp.sk_iters = iters;
+  long long it = 0;
+  for (int ph = 0; ph < kMaxPhases; ++ph) {
+    kp.sk_iter_start[ph] = it;
+    if (ph < kp.num_phases) {
+      const int kpt = kp.taps_h[ph] * kp.taps_w[ph] * kp.c_blocks;
+      kp.sk_kpt[ph] = kpt;
+      kp.sk_div_kpt[ph] = make_fast_div(static_cast<uint32_t>(kpt));
+      it += static_cast<long long>(kp.tile_start[ph + 1] - kp.tile_start[ph]) * kpt;
+    } else {
+      kp.sk_kpt[ph] = 1;
+      kp.sk_div_kpt[ph] = make_fast_div(1u);
+    }
+  }
+  kp.sk_iter_start[kMaxPhases] = it;
+  kp.sk_slot_floats = static_cast<uint32_t>(sk_slot_bytes(kp) / sizeof(float));
+  kp.l2_prefetch = 0;
+}
+
 struct FwdShape {
   int n, h, w, c_in, r, s, c_out, ho, wo;
   int stride_h, stride_w, pad_h, pad_w, dil_h, dil_w;
@@ -532,7 +604,7 @@ void plan_window(const FwdShape& f, Plan* pl, int num_sms, int has_residual) {
   if (pitch > kBM || f.c_out > 256) return;
   const int bn = ((f.c_out + 15) / 16) * 16;
   const size_t bres = static_cast<size_t>(f.r) * f.s * kp.c_blocks * bn * kp.sw_bytes;
-  if (bres > 120 * 1024) return;
+  if (bres > 120 * 1024 || f.r * f.s * kp.c_blocks > kMaxWindowBlocks) return;
   const int mh = bn <= 128 ? 2 : 1;
   const int rows = kBM / pitch;
   const int rows_tile = mh * rows;
@@ -605,7 +677,8 @@ conv_status_t plan_gather(const FwdShape& f, Plan* pl) {
   return CONV_OK;
 }
 
-conv_status_t plan_fwd(const FwdShape& f, Plan* pl, int num_sms, int has_residual) {
+conv_status_t plan_fwd(const FwdShape& f, Plan* pl, int num_sms, int has_residual,
+                       size_t sk_room = 0) {
   std::memset(pl, 0, sizeof(*pl));
   const int groups = std::max(f.groups, 1);
   const int cg = f.c_in / groups, fg = f.c_out / groups;
@@ -653,6 +726,7 @@ conv_status_t plan_fwd(const FwdShape& f, Plan* pl, int num_sms, int has_residua
   pl->packed_bytes = static_cast<size_t>(f.c_out) * pl->kmax * elt_bytes(f.in_dtype);
   if (!gather && groups == 1) plan_window_or_keep(f, pl, num_sms, has_residual);
   plan_pair(pl, num_sms);
+  plan_streamk(pl, num_sms, sk_room);
   return CONV_OK;
 }
 
@@ -732,7 +806,7 @@ conv_status_t check_tr_shape(const TrShape& t) {
   return CONV_OK;
 }
 
-conv_status_t plan_transposed(const TrShape& t, Plan* pl, int num_sms) {
+conv_status_t plan_transposed(const TrShape& t, Plan* pl, int num_sms, size_t sk_room = 0) {
   std::memset(pl, 0, sizeof(*pl));
   conv_status_t st = plan_channels(pl, t.in_dtype, t.c_in);
   if (st != CONV_OK) return st;
@@ -795,6 +869,7 @@ conv_status_t plan_transposed(const TrShape& t, Plan* pl, int num_sms) {
   kp.Cout = t.c_out;
   kp.vec_ok = (t.c_out * 2) % 16 == 0;
   plan_pair(pl, num_sms);
+  plan_streamk(pl, num_sms, sk_room);
   pl->kmax = kmax;
   pl->packed_bytes = static_cast<size_t>(pl->phases_packed) * t.c_out * kmax * elt_bytes(t.in_dtype);
   return CONV_OK;
@@ -1026,8 +1101,8 @@ conv_status_t layout_memory(Plan* pl, int has_residual) {
   const uint32_t a_bytes = kBM * kp.m_halves * kp.sw_bytes;
   // (A pair's CTA holds half of the tile's filter rows.)
   const uint32_t b_bytes = static_cast<uint32_t>(kp.pair ? kp.bn / 2 : kp.bn) * kp.sw_bytes;
-  const bool can_res = !kp.pair && kp.num_phases == 1 && kp.n_tiles == 1 && kp.groups <= 1 &&
-                       tuning().filter_resident != 0;
+  const bool can_res = !kp.pair && !kp.streamk && kp.num_phases == 1 && kp.n_tiles == 1 &&
+                       kp.groups <= 1 && tuning().filter_resident != 0;
   const size_t bres = can_res ? static_cast<size_t>(kp.taps_h[0]) * kp.taps_w[0] * kp.c_blocks * b_bytes : 0;
   const size_t src_tile = static_cast<size_t>(kBM) * kp.m_halves * kp.bn * 2;
   const size_t chunk = static_cast<size_t>(kBM) * cw * 2;
@@ -1222,7 +1297,8 @@ conv_status_t plan_memory_direct(Plan* pl) {
   kp.stg_bufs = 0;
   kp.src_chunk_bytes = 0;
   kp.valid_rows = kBM;
-  const bool can_res = !kp.pair && kp.num_phases == 1 && kp.n_tiles == 1 && kp.groups <= 1;
+  const bool can_res = !kp.pair && !kp.streamk && kp.num_phases == 1 && kp.n_tiles == 1 &&
+                       kp.groups <= 1;
   const size_t bres = can_res ? static_cast<size_t>(kp.taps_h[0]) * kp.taps_w[0] * kp.c_blocks * b_bytes : 0;
   bool res = false;
   int stages = 0;
@@ -1302,11 +1378,18 @@ conv_status_t finish_plan(Plan* pl, int n_images, const void* packed, void* outp
   kp.div_tpg = make_fast_div(static_cast<uint32_t>(std::max(kp.tiles_per_group, 1)));
   // Prefetching the next tile's input only pays when CTAs walk several tiles
   // that all start at the first C_out tile (one n-tile).
-  kp.l2_prefetch = (kp.n_tiles == 1 && tuning().l2_prefetch != -1) ? 1 : 0;
+  kp.l2_prefetch = (kp.n_tiles == 1 && !kp.streamk && tuning().l2_prefetch != -1) ? 1 : 0;
   const int sms = device_sm_count();
   if (sms <= 0) return CONV_ERR_CUDA;
-  // Pairs: clusters of two CTAs, one tile per cluster at a time.
-  pl->grid = kp.pair ? 2 * std::min(kp.total_tiles, sms / 2) : std::min(kp.total_tiles, sms);
+  // Pairs: clusters of two CTAs, one tile per cluster at a time.  Stream-K:
+  // one CTA per SM, each with its share of the iterations.
+  pl->grid = kp.pair ? 2 * std::min(kp.total_tiles, sms / 2)
+                     : (kp.streamk ? sms : std::min(kp.total_tiles, sms));
+  if (kp.streamk) {
+    uint8_t* base = static_cast<uint8_t*>(workspace) + pl->sk_offset;
+    kp.sk_flags = reinterpret_cast<unsigned int*>(base);
+    kp.sk_partials = reinterpret_cast<float*>(base + sk_flag_bytes(pl->grid));
+  }
   return CONV_OK;
 }
 
@@ -1527,9 +1610,23 @@ conv_status_t run_pack(const Prepared& pr, cudaStream_t stream) {
   return CONV_OK;
 }
 
-conv_status_t launch_prepared(const Prepared& pr, cudaStream_t stream) {
+// Stream-K flags hold the value of the launch that raised them: every launch
+// takes a new value (never 0, the value of a fresh workspace), so flags left
+// by an earlier launch -- finished or stopped by a timeout -- never match.
+std::atomic<uint32_t> g_sk_epoch{0};
+
+uint32_t next_sk_epoch() {
+  uint32_t e;
+  do {
+    e = g_sk_epoch.fetch_add(1, std::memory_order_relaxed) + 1;
+  } while (e == 0);
+  return e;
+}
+
+conv_status_t launch_prepared(Prepared& pr, cudaStream_t stream) {
   conv_status_t st = run_pack(pr, stream);
   if (st != CONV_OK) return st;
+  if (pr.path == kPathIgemm && pr.pl.kp.streamk) pr.pl.kp.sk_epoch = next_sk_epoch();
   if (pr.path == kPathRowTap) return launch_rowtap(pr.rt, stream);
   if (pr.path == kPathDirect) {
     cudaError_t e = launch_conv_direct(pr.direct_in_dtype, pr.direct_in_dtype != CONV_DTYPE_F16,
@@ -1620,8 +1717,11 @@ conv_status_t prepare_fwd(const void* input, const FwdShape& shape, const void* 
                          workspace);
   }
   Plan& pl = pr->pl;
-  st = plan_fwd(f, &pl, sms, has_residual);
+  const size_t sk_offset = need;
+  st = plan_fwd(f, &pl, sms, has_residual,
+                workspace_bytes > sk_offset ? workspace_bytes - sk_offset : 0);
   if (st != CONV_OK) return st;
+  pl.sk_offset = sk_offset;
   st = encode_fwd_input(f, input, &pl);
   if (st != CONV_OK) return st;
   pr->path = kPathIgemm;
@@ -1651,8 +1751,10 @@ conv_status_t prepare_tr(const void* input, const TrShape& t, const void* filter
   if (sms <= 0) return CONV_ERR_CUDA;
   pr->sms = sms;
   Plan& pl = pr->pl;
-  st = plan_transposed(t, &pl, sms);
+  const size_t sk_offset = need;
+  st = plan_transposed(t, &pl, sms, workspace_bytes > sk_offset ? workspace_bytes - sk_offset : 0);
   if (st != CONV_OK) return st;
+  pl.sk_offset = sk_offset;
   st = encode_tr_inputs(t, input, &pl);
   if (st != CONV_OK) return st;
   const void* packed = filter;
@@ -1847,6 +1949,13 @@ size_t conv2d_workspace_size(int r, int s, int c_in, int c_out, conv_dtype_t dty
   return CONV_STATUS_BYTES + round_up_256(conv2d_packed_filter_bytes(r, s, c_in, c_out, dtype));
 }
 
+size_t conv_streamk_workspace_size(void) {
+  const int sms = device_sm_count();
+  if (sms <= 0) return 0;
+  // The largest tile: 128 x 256 or 256 x 128 fp32 accumulators.
+  return sk_flag_bytes(sms) + static_cast<size_t>(sms) * (size_t(kBM) * 256 * sizeof(float));
+}
+
 conv_status_t conv2d_pack_filter(const void* filter, int r, int s, int c_in, int c_out,
                                  int filter_is_fcrs, conv_dtype_t dtype, void* packed,
                                  size_t packed_bytes, void* stream) {
@@ -2038,9 +2147,12 @@ conv_status_t conv2d_fwd_noalloc(const void* input, int n, int h, int w, int c_i
   if (cudaMemsetAsync(scratch, 0, CONV_STATUS_BYTES, static_cast<cudaStream_t>(stream)) !=
       cudaSuccess)
     return CONV_ERR_CUDA;
+  // The scratch stands in for a workspace of exactly conv2d_fwd's minimum
+  // size, so the plan (and every result bit) is that of conv2d_fwd with such
+  // a workspace.
   return conv2d_fwd(input, n, h, w, c_in, in_dtype, filter, r, s, c_out, filter_is_fcrs, output,
                     ho, wo, out_dtype, stride, dilation, symmetric_padding, num_groups,
-                    has_residual, source, beta, epilogue, scratch, kNoAllocScratchBytes, stream);
+                    has_residual, source, beta, epilogue, scratch, need, stream);
 }
 
 // ------------------------------------------------------------------- testing hooks
@@ -2064,7 +2176,7 @@ void conv_testing_cache_stats(unsigned long long* hits, unsigned long long* miss
 conv_status_t conv_testing_fwd_plan(int n, int h, int w, int c_in, conv_dtype_t dtype, int r,
                                     int s, int c_out, const int stride[2],
                                     const int symmetric_padding[2], int has_residual, int num_sms,
-                                    int out[13]) {
+                                    size_t workspace_bytes, int out[14]) {
   if (!stride || !symmetric_padding || !out) return CONV_ERR_INVALID_VALUE;
   const int dil[2] = {1, 1};
   const conv_dtype_t out_dt = dtype == CONV_DTYPE_F8E4M3 ? CONV_DTYPE_BF16 : dtype;
@@ -2091,10 +2203,12 @@ conv_status_t conv_testing_fwd_plan(int n, int h, int w, int c_in, conv_dtype_t 
     out[10] = rp.band;
     out[11] = 3;
     out[12] = 0;
+    out[13] = 0;
     return CONV_OK;
   }
   Plan pl;
-  st = plan_fwd(f, &pl, num_sms, has_residual);
+  st = plan_fwd(f, &pl, num_sms, has_residual,
+                workspace_bytes > CONV_STATUS_BYTES ? workspace_bytes - CONV_STATUS_BYTES : 0);
   if (st != CONV_OK) return st;
   st = layout_memory(&pl, has_residual);
   if (st != CONV_OK) return st;
@@ -2104,7 +2218,7 @@ conv_status_t conv_testing_fwd_plan(int n, int h, int w, int c_in, conv_dtype_t 
   out[3] = static_cast<int>(pl.smem_bytes);
   out[4] = pl.kp.total_tiles;
   out[5] = pl.kp.pair ? 2 * std::min(pl.kp.total_tiles, num_sms / 2)
-                     : std::min(pl.kp.total_tiles, num_sms);
+                     : (pl.kp.streamk ? num_sms : std::min(pl.kp.total_tiles, num_sms));
   out[6] = static_cast<int>(pl.kp.tmem_cols);
   out[7] = pl.kp.epi_mode;
   out[8] = pl.kp.b_resident;
@@ -2112,6 +2226,7 @@ conv_status_t conv_testing_fwd_plan(int n, int h, int w, int c_in, conv_dtype_t 
   out[10] = pl.kp.stg_bufs;
   out[11] = pl.kp.gather ? 2 : (pl.kp.window ? 1 : 0);
   out[12] = pl.kp.pair;
+  out[13] = pl.kp.streamk;
   return CONV_OK;
 }
 

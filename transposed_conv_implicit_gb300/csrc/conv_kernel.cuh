@@ -90,6 +90,194 @@ __device__ __forceinline__ TileInfo decode_tile(const ConvKernelParams& p, int t
   return ti;
 }
 
+// ---------------------------------------------------------------- work items
+// A CTA's (or CTA pair's) work: whole tiles cta, cta + nctas, ...
+// (data-parallel), or, with stream-K, its equal share of the iteration
+// sequence (tile by tile, k-block by k-block), cut at tile boundaries.
+struct Work {
+  TileInfo ti;
+  int tile;
+  int kb0, kb1;  // k-blocks [kb0, kb1) of the tile
+};
+
+struct WorkWalk {
+  long long pos, end;  // stream-K iteration range
+  int t, step;         // data-parallel tile walk
+};
+
+__device__ __forceinline__ long long sk_share_begin(const ConvKernelParams& p, int cta, int nctas) {
+  return p.sk_iters * cta / nctas;
+}
+
+// The CTA whose share holds iteration `pos`: the last c with share_begin(c) <= pos.
+__device__ __forceinline__ int sk_owner(const ConvKernelParams& p, long long pos, int nctas) {
+  return static_cast<int>(((pos + 1) * nctas - 1) / p.sk_iters);
+}
+
+__device__ __forceinline__ WorkWalk work_begin(const ConvKernelParams& p, int cta, int nctas) {
+  WorkWalk w;
+  w.t = cta;
+  w.step = nctas;
+  w.pos = p.streamk ? sk_share_begin(p, cta, nctas) : 0;
+  w.end = p.streamk ? sk_share_begin(p, cta + 1, nctas) : 0;
+  return w;
+}
+
+// First iteration of tile `tile` (stream-K).
+__device__ __forceinline__ long long sk_tile_iter(const ConvKernelParams& p, int tile, int phase) {
+  return p.sk_iter_start[phase] +
+         static_cast<long long>(tile - p.tile_start[phase]) * p.sk_kpt[phase];
+}
+
+__device__ __forceinline__ bool work_next(const ConvKernelParams& p, WorkWalk& w, Work& out) {
+  if (p.streamk) {
+    if (w.pos >= w.end) return false;
+    int ph = 0;
+    while (ph + 1 < p.num_phases && w.pos >= p.sk_iter_start[ph + 1]) ++ph;
+    const int local = static_cast<int>(w.pos - p.sk_iter_start[ph]);
+    const int tl = fast_div(local, p.sk_div_kpt[ph]);
+    out.tile = p.tile_start[ph] + tl;
+    out.ti = decode_tile(p, out.tile);
+    out.kb0 = local - tl * p.sk_kpt[ph];
+    const long long room = w.end - w.pos;
+    out.kb1 = room < out.ti.kblocks - out.kb0 ? out.kb0 + static_cast<int>(room) : out.ti.kblocks;
+    w.pos += out.kb1 - out.kb0;
+    return true;
+  }
+  if (w.t >= p.total_tiles) return false;
+  out.tile = w.t;
+  out.ti = decode_tile(p, w.t);
+  out.kb0 = 0;
+  out.kb1 = out.ti.kblocks;
+  w.t += w.step;
+  return true;
+}
+
+// The role of a work item in its tile's epilogue.
+constexpr int kSkWhole = 0;    // the whole tile: the ordinary epilogue
+constexpr int kSkPartial = 1;  // starts inside the tile: accumulators go to the partial slot
+constexpr int kSkFinish = 2;   // the tile's first k-blocks, others follow: add their partials
+
+__device__ __forceinline__ int work_role(const Work& w) {
+  if (w.kb0 != 0) return kSkPartial;
+  return w.kb1 < w.ti.kblocks ? kSkFinish : kSkWhole;
+}
+
+// Partial slot layout: [16-column group][quarter k of the group][128 rows][4
+// floats], so each 16-byte store or load instruction of a warp (32 rows, one
+// (group, k)) touches 512 consecutive bytes: whole sectors and lines.
+__device__ __forceinline__ float4* sk_slot_at(const ConvKernelParams& p, int cta, int group, int k,
+                                              int row) {
+  return reinterpret_cast<float4*>(p.sk_partials + static_cast<size_t>(cta) * p.sk_slot_floats) +
+         (static_cast<size_t>(group) * 4 + k) * kBM + row;
+}
+
+// Contributor: 16 accumulator columns of one row into the slot.
+__device__ __forceinline__ void sk_store16(const ConvKernelParams& p, int cta, int group, int row,
+                                           const uint32_t* v) {
+#pragma unroll
+  for (int k = 0; k < 4; ++k)
+    *sk_slot_at(p, cta, group, k, row) =
+        make_float4(__uint_as_float(v[4 * k]), __uint_as_float(v[4 * k + 1]),
+                    __uint_as_float(v[4 * k + 2]), __uint_as_float(v[4 * k + 3]));
+}
+
+// Finisher: waits (bounded) until every CTA holding later k-blocks of the
+// work item's tile has raised the flag of epilogue warp `ew` for this launch.
+// Returns false on timeout (status bit and abort flag raised) or abort.
+__device__ __forceinline__ bool sk_wait_partials(const ConvKernelParams& p, const Work& w, int ew,
+                                                 int nctas, volatile int* abort_flag,
+                                                 long long limit) {
+  const long long first = sk_tile_iter(p, w.tile, w.ti.phase);
+  const long long end = first + w.ti.kblocks;
+  const long long t0 = cycle_count();
+  for (long long pos = first + w.kb1; pos < end;) {
+    const int c = sk_owner(p, pos, nctas);
+    const unsigned int* flag = p.sk_flags + static_cast<size_t>(c) * kEpilogueWarps + ew;
+    while (ld_acquire_gpu(flag) != p.sk_epoch) {
+      if (*abort_flag) return false;
+      if (cycle_count() - t0 > limit) {
+        *abort_flag = 1;
+        atomicOr(p.status, kStatusStreamKTimeout);
+        return false;
+      }
+    }
+    pos = sk_share_begin(p, c + 1, nctas);
+  }
+  return true;
+}
+
+// Finisher: sets v to the sum of every later contributor's partial of the
+// 16-column groups [g0, g0 + ngroups) (ngroups <= kGroups) of row `row`
+// (v[16 * k + j] is column j of group g0 + k, as float bits).  The first
+// contributor's loads land straight in v, all in flight together; further
+// contributors (rare: tiles split three ways or more) add group by group.
+template <int kGroups>
+__device__ __forceinline__ void sk_sum_partials(const ConvKernelParams& p, const Work& w, int g0,
+                                                int ngroups, int row, int nctas,
+                                                uint32_t (&v)[16 * kGroups]) {
+  const long long first = sk_tile_iter(p, w.tile, w.ti.phase);
+  const long long end = first + w.ti.kblocks;
+  long long pos = first + w.kb1;
+  int c = sk_owner(p, pos, nctas);
+#pragma unroll
+  for (int k = 0; k < kGroups; ++k)
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const float4 a = k < ngroups ? __ldcg(sk_slot_at(p, c, g0 + k, j, row))
+                                   : make_float4(0.f, 0.f, 0.f, 0.f);
+      v[16 * k + 4 * j] = __float_as_uint(a.x);
+      v[16 * k + 4 * j + 1] = __float_as_uint(a.y);
+      v[16 * k + 4 * j + 2] = __float_as_uint(a.z);
+      v[16 * k + 4 * j + 3] = __float_as_uint(a.w);
+    }
+  for (pos = sk_share_begin(p, c + 1, nctas); pos < end; pos = sk_share_begin(p, c + 1, nctas)) {
+    c = sk_owner(p, pos, nctas);
+#pragma unroll
+    for (int k = 0; k < kGroups; ++k) {
+      if (k < ngroups) {
+        float4 a[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) a[j] = __ldcg(sk_slot_at(p, c, g0 + k, j, row));
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const int e = 16 * k + 4 * j;
+          v[e] = __float_as_uint(__uint_as_float(v[e]) + a[j].x);
+          v[e + 1] = __float_as_uint(__uint_as_float(v[e + 1]) + a[j].y);
+          v[e + 2] = __float_as_uint(__uint_as_float(v[e + 2]) + a[j].z);
+          v[e + 3] = __float_as_uint(__uint_as_float(v[e + 3]) + a[j].w);
+        }
+      }
+    }
+  }
+}
+
+// v[16 * k + j] += TMEM column 16 * k + j (from taddr), k < ngroups: 16 columns
+// per load, so only 16 more registers are live.
+template <int kGroups>
+__device__ __forceinline__ void tmem_add_groups(uint32_t taddr, int ngroups,
+                                                uint32_t (&v)[16 * kGroups]) {
+#pragma unroll
+  for (int k = 0; k < kGroups; ++k) {
+    if (k < ngroups) {
+      uint32_t t[16];
+      tmem_ld_32x32b_x16(taddr + static_cast<uint32_t>(16 * k), t);
+      tmem_wait_ld_regs(t);
+#pragma unroll
+      for (int j = 0; j < 16; ++j)
+        v[16 * k + j] = __float_as_uint(__uint_as_float(v[16 * k + j]) + __uint_as_float(t[j]));
+    }
+  }
+}
+
+// Contributor: after the warp's partial stores, publish them (flag = epoch).
+__device__ __forceinline__ void sk_publish(const ConvKernelParams& p, int cta, int ew, int lane) {
+  __threadfence();
+  __syncwarp();
+  if (lane == 0 && p.fault_mode != 2)  // (fault_mode 2, a test hook: never publish)
+    st_release_gpu(p.sk_flags + static_cast<size_t>(cta) * kEpilogueWarps + ew, p.sk_epoch);
+}
+
 // Image and first output row of row-window tile t.
 __device__ __forceinline__ void window_origin(const ConvKernelParams& p, int t, int& n_img,
                                               int& oy0) {
@@ -366,8 +554,11 @@ __device__ __forceinline__ bool mma_role(const ConvKernelParams& p, uint32_t tme
   uint32_t bs_lo = b_lo0;  // streamed B: advances with the ring
   bool ok = true;
   int it = 0;
-  for (int t = t0; ok && t < total_tiles; t += step, ++it) {
-    const TileInfo ti = decode_tile(p, t);
+  (void)total_tiles;
+  WorkWalk walk = work_begin(p, t0, step);
+  Work wk;
+  for (; ok && work_next(p, walk, wk); ++it) {
+    const TileInfo& ti = wk.ti;
     const int acc = it & 1;
     if (!mbar_wait_bounded(smem_u32(&tempty[acc]), static_cast<uint32_t>(((it >> 1) & 1) ^ 1),
                            abort_flag, status, kStatusMmaTimeout, limit, 0u, kPair)) {
@@ -384,8 +575,9 @@ __device__ __forceinline__ bool mma_role(const ConvKernelParams& p, uint32_t tme
       continue;
     }
     const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc) * acc_stride;
-    uint32_t br_lo = b_lo0;  // resident B: restarts every tile
-    const int kblocks = ti.kblocks;
+    // Resident B: block kb of the tile sits at index kb.
+    uint32_t br_lo = b_lo0 + static_cast<uint32_t>(wk.kb0) * b_step;
+    const int kblocks = wk.kb1 - wk.kb0;
     for (int kb = 0; kb < kblocks; ++kb) {
       if (!mbar_wait_bounded(full0 + 8u * stage, phase, abort_flag, status, kStatusMmaTimeout,
                              limit, 0u, kPair)) {
@@ -423,12 +615,16 @@ __device__ __forceinline__ bool mma_role(const ConvKernelParams& p, uint32_t tme
 // the tile's input rows with halo; tap (r, s) of half h starts at box row
 // h*win_half_rows + r*win_pitch + s.  The filter is resident: block
 // (tap, cb) of the packed filter sits at index tap*c_blocks + cb.
+// On the CTA's first tile each filter block (tap, cb) has its own barrier
+// (wbar[tap * c_blocks + cb]), so the MMAs of tap 0 start as soon as the
+// input box and that one block have landed.
 template <int kKind, int kSteps, int kHalves>
 __device__ __forceinline__ bool mma_role_window(const ConvKernelParams& p, uint32_t tmem_base,
                                                 uint8_t* a_ring, uint8_t* b_res, uint64_t* full,
                                                 uint64_t* empty, uint64_t* tfull, uint64_t* tempty,
-                                                volatile int* abort_flag, unsigned int* status,
-                                                long long limit, int t0, int step) {
+                                                uint64_t* wbar, volatile int* abort_flag,
+                                                unsigned int* status, long long limit, int t0,
+                                                int step) {
   const int stages = p.stages;
   const uint32_t sw = p.sw_bytes;  // 128 in this mode
   const uint32_t b_bytes = static_cast<uint32_t>(p.bn) * sw;
@@ -475,6 +671,14 @@ __device__ __forceinline__ bool mma_role_window(const ConvKernelParams& p, uint3
       uint32_t b_lo = b_lo0 + static_cast<uint32_t>(cb) * b_step;
       int s = 0;
       for (int tap = 0; tap < taps; ++tap) {
+        if (it == 0) {
+          if (!mbar_wait_bounded(smem_u32(&wbar[tap * c_blocks + cb]), 0u, abort_flag, status,
+                                 kStatusMmaTimeout, limit)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+        }
         issue_kblock<kKind, kSteps, kHalves>(d_tmem, desc_hi, tap_lo, b_lo, half_lo, bn_cols,
                                              idesc, (cb | tap) != 0 ? 1u : 0u);
         b_lo += b_tap_step;
@@ -484,6 +688,7 @@ __device__ __forceinline__ bool mma_role_window(const ConvKernelParams& p, uint3
           tap_lo += a_row_skip;
         }
       }
+      if (!ok) break;
       mma_commit(empty0 + 8u * stage);
       a_lo += a_step;
       if (++stage == stages) {
@@ -906,6 +1111,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* gst_empty = gst_full + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gst_empty + 2);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  // Row-window loader: one barrier per resident filter block, for the first
+  // tile (at most kMaxWindowBlocks, from byte 512 of the barrier region).
+  uint64_t* wbar = bars + 64;
   unsigned int* status = p.status;
   const long long limit = p.timeout_cycles;
 
@@ -927,6 +1135,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(smem_u32(&gst_full[b]), 1);
       mbar_init(smem_u32(&gst_empty[b]), kGatherProducers);  // every builder warp
     }
+    if (p.window)
+      for (int i = 0; i < p.win_R * p.win_S * p.c_blocks; ++i) mbar_init(smem_u32(&wbar[i]), 1);
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -976,6 +1186,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = true;
       const uint32_t stage_tx = a_bytes + (p.b_resident ? 0u : b_bytes);
       bool first_tile = true;  // a resident filter is loaded k-block by k-block with it
+      unsigned long long win_blocks_issued = 0;  // channel blocks whose filter blocks are in flight
       if (p.window) {
         // One tiled box of input rows (with halo) per channel block; the
         // first tile also brings every tap's filter block of that channel block.
@@ -994,13 +1205,20 @@ __global__ void __launch_bounds__(kThreads, 1)
               last_issued = seq;
               if (!(p.fault_mode == 1 && blockIdx.x == 0 && seq == 0)) {
                 const uint32_t fb = smem_u32(&full[stage]);
-                mbar_arrive_expect_tx(fb, box_bytes + (first_tile ? b_bytes * taps : 0u));
+                mbar_arrive_expect_tx(fb, box_bytes);
                 tma_load_4d(smem_u32(a_ring + stage * p.win_stage_bytes), &p.map_a[0], fb,
                             cb * p.bk, -p.win_pad_w, oy0 - p.win_pad_h, n_img);
-                if (first_tile)
-                  for (int tap = 0; tap < taps; ++tap)
-                    tma_load_3d(smem_u32(b_res + (tap * p.c_blocks + cb) * b_bytes), &p.map_b, fb,
+                if (first_tile) {
+                  // Each filter block on its own barrier, in the MMA's order.
+                  for (int tap = 0; tap < taps; ++tap) {
+                    const int blk = tap * p.c_blocks + cb;
+                    const uint32_t wb = smem_u32(&wbar[blk]);
+                    mbar_arrive_expect_tx(wb, b_bytes);
+                    tma_load_3d(smem_u32(b_res + blk * b_bytes), &p.map_b, wb,
                                 tap * p.c_in + cb * p.bk, 0, 0);
+                  }
+                  win_blocks_issued |= 1ull << cb;
+                }
               }
             }
             if (++stage == stages) {
@@ -1014,8 +1232,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       // A pair's rank 0 arms its stage barrier for both CTAs' bytes; rank 1's
       // copies count on rank 0's barrier.
       const uint32_t arm_tx = kPair ? 2u * stage_tx : stage_tx;
-      for (int t = tile0; !p.window && t < p.total_tiles && ok; t += tile_step) {
-        TileInfo ti = decode_tile(p, t);
+      WorkWalk walk = work_begin(p, tile0, tile_step);
+      Work wk;
+      while (!p.window && ok && work_next(p, walk, wk)) {
+        const int t = wk.tile;
+        TileInfo ti = wk.ti;
         ti.m0 += m_off;
         const int ph = ti.phase;
         int n_img, j, i;
@@ -1027,8 +1248,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         // Filter slot: the stride phase, or the channel group.
         const int bz = p.groups > 1 ? ti.group : p.b_index[ph];
         const int c_base = ti.group * p.c_group;  // first input channel of the group
+        // The work item's first k-block: channel block cb of tap (uh, uw).
         int cb = 0, uw = 0, uh = 0;
         int bk_k = 0;  // k coordinate of this k-block in the packed filter: tap*C_in + cb*bk
+        if (wk.kb0 != 0) {
+          const int tap = wk.kb0 / p.c_blocks;
+          cb = wk.kb0 - tap * p.c_blocks;
+          uh = tap / tw;
+          uw = tap - uh * tw;
+          bk_k = tap * p.c_in + cb * p.bk;
+        }
         const bool load_res = p.b_resident && first_tile;
         first_tile = false;
         // This CTA's next tile: its A boxes are prefetched into L2 alongside
@@ -1048,7 +1277,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (tin.kblocks != ti.kblocks || tin.n0 != 0 || tin.m0 == ti.m0 || tin.group != ti.group)
             pf_n = -1;  // skip
         }
-        for (int kb = 0; kb < ti.kblocks; ++kb, ++seq) {
+        for (int kb = wk.kb0; kb < wk.kb1; ++kb, ++seq) {
           if ((seq & 1) == role) {
             if (!mbar_wait_bounded(smem_u32(&empty[stage]), phase ^ 1u, abort_flag, status,
                                    kStatusProducerTimeout, limit, p.wait_hint_ns, kPair)) {
@@ -1116,6 +1345,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (q >= 0 && (q & 1) == role)
             mbar_wait_drain(smem_u32(&full[q % stages]), static_cast<uint32_t>((q / stages) & 1),
                             limit / 8 + 1);
+        if (p.window)
+          for (int cb = 0; cb < p.c_blocks; ++cb)
+            if (win_blocks_issued >> cb & 1ull)
+              for (int tap = 0; tap < p.win_R * p.win_S; ++tap)
+                mbar_wait_drain(smem_u32(&wbar[tap * p.c_blocks + cb]), 0u, limit / 8 + 1);
       }
     }
     __syncwarp();
@@ -1128,9 +1362,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!kPair && p.window) {
         ok = p.m_halves == 2
                  ? mma_role_window<kKind, 4, 2>(p, tmem_base, a_ring, b_res, full, empty, tfull,
-                                                tempty, abort_flag, status, limit, tile0, tile_step)
+                                                tempty, wbar, abort_flag, status, limit, tile0,
+                                                tile_step)
                  : mma_role_window<kKind, 4, 1>(p, tmem_base, a_ring, b_res, full, empty, tfull,
-                                                tempty, abort_flag, status, limit, tile0, tile_step);
+                                                tempty, wbar, abort_flag, status, limit, tile0,
+                                                tile_step);
         if (!ok) {
           mma_commit(smem_u32(drain));
           mbar_wait_drain(smem_u32(drain), 0, limit / 8 + 1);
@@ -1167,12 +1403,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const bool leader = (warp == 2 + 4 * grp) && lane == 0;
     const uint32_t bar_id = 1 + grp;
     int it = 0;
-    // This CTA's share of tile t (a pair's rank 1 takes rows 128..255).
-    auto tile_at = [&](int t) {
-      TileInfo x = decode_tile(p, t);
-      x.m0 += m_off;
-      return x;
-    };
+    // (A pair's rank 1 takes rows 128..255 of each tile: m_off.)
     // Hands accumulator buffer `acc` back to the MMA issuer (lane 0, after
     // tcgen05.fence::before_thread_sync and __syncwarp).
     auto release_acc = [&](int acc) {
@@ -1181,6 +1412,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       else
         mbar_arrive(smem_u32(&tempty[acc]));
     };
+    const int ew = warp - 2;  // epilogue warp index: its stream-K flag
     if (p.epi_mode != 0) {
       const uint32_t row_bytes = static_cast<uint32_t>(p.cw) * 2;
       const uint32_t chunk_bytes = kBM * row_bytes;
@@ -1191,20 +1423,30 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint8_t* stg_grp = stg_base + grp * (p.stg_bufs * chunk_bytes);
       int store_seq = 0;
       int src_issued[2] = {0, 0};  // source loads issued per buffer (leader only)
-      if (p.has_residual && leader && tile0 < p.total_tiles) {
-        issue_source_items(p, tile_at(tile0), src_base, smem_u32(&src_full[grp]), grp);
+      // Work items in order; the source prefetch peeks at the next one.
+      WorkWalk walk = work_begin(p, tile0, tile_step);
+      Work cur{};
+      bool have = work_next(p, walk, cur);
+      if (p.has_residual && leader && have) {
+        TileInfo t0i = cur.ti;
+        t0i.m0 += m_off;
+        issue_source_items(p, t0i, src_base, smem_u32(&src_full[grp]), grp);
         ++src_issued[0];
       }
-      for (int t = tile0; t < p.total_tiles; t += tile_step, ++it) {
-        const TileInfo ti = tile_at(t);
+      for (; have; ++it, have = work_next(p, walk, cur)) {
+        TileInfo ti = cur.ti;
+        ti.m0 += m_off;
+        const int role = p.streamk ? work_role(cur) : kSkWhole;
         const int acc = it & 1;
         const int sbuf = p.src_bufs == 2 ? acc : 0;
         if (p.has_residual && leader && p.src_bufs == 2) {
-          const int tn = t + tile_step;
-          if (tn < p.total_tiles) {
-            // The other buffer last held tile it-1, whose stores must have read it.
+          WorkWalk ahead = walk;
+          Work nx;
+          if (work_next(p, ahead, nx)) {
+            nx.ti.m0 += m_off;
+            // The other buffer last held item it-1, whose stores must have read it.
             bulk_wait_read_all();
-            issue_source_items(p, tile_at(tn), src_base + (acc ^ 1) * src_tile_bytes,
+            issue_source_items(p, nx.ti, src_base + (acc ^ 1) * src_tile_bytes,
                                smem_u32(&src_full[2 * (acc ^ 1) + grp]), grp);
             ++src_issued[acc ^ 1];
           }
@@ -1217,6 +1459,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           ok = mbar_wait_bounded(smem_u32(&src_full[2 * sbuf + grp]), par, abort_flag, status,
                                  kStatusEpilogueTimeout, limit, p.wait_hint_ns);
         }
+        if (ok && role == kSkFinish)
+          ok = sk_wait_partials(p, cur, ew, tile_step, abort_flag, limit);
         if (!__all_sync(0xFFFFFFFFu, ok)) break;
         tc_fence_after();
         uint8_t* src_tile = src_base + sbuf * src_tile_bytes;
@@ -1231,7 +1475,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int c = q - h * nchunks;
           const int mh = ti.m0 + h * kBM;
           uint32_t v[64];
-          if (ti.kblocks > 0) {
+          // 16-column groups of this chunk within the tile's partial slot.
+          const int g0 = h * (p.bn / 16) + c * (p.cw / 16);
+          if (role == kSkFinish) {
+            // The later k-blocks' partials first, then this CTA's accumulators.
+            sk_sum_partials<4>(p, cur, g0, p.cw / 16, row, tile_step, v);
+            tmem_add_groups<4>(tacc + static_cast<uint32_t>(h * p.bn + c * p.cw), p.cw / 16, v);
+          } else if (ti.kblocks > 0) {
             const uint32_t taddr = tacc + static_cast<uint32_t>(h * p.bn + c * p.cw);
 #pragma unroll
             for (int k = 0; k < 4; ++k)
@@ -1251,6 +1501,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_before();
             __syncwarp();
             if (lane == 0) release_acc(acc);
+          }
+          if (role == kSkPartial) {
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+              if (k < p.cw / 16)
+                sk_store16(p, static_cast<int>(blockIdx.x), g0 + k, row, &v[k * 16]);
+            continue;  // no output from a partial
           }
           uint8_t* buf;
           if (in_place) {
@@ -1297,13 +1554,16 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           ++store_seq;
         }
+        if (role == kSkPartial) sk_publish(p, static_cast<int>(blockIdx.x), ew, lane);
         if (p.has_residual && leader && p.src_bufs == 1) {
-          // Single source buffer: fetch the next tile's source once this
-          // tile's stores (which read it) are done reading.
-          const int tn = t + tile_step;
-          if (tn < p.total_tiles) {
+          WorkWalk ahead = walk;
+          Work nx;
+          if (work_next(p, ahead, nx)) {
+            nx.ti.m0 += m_off;
+            // Single source buffer: fetch the next item's source once this
+            // item's stores (which read it) are done reading.
             bulk_wait_read_all();
-            issue_source_items(p, tile_at(tn), src_base, smem_u32(&src_full[grp]), grp);
+            issue_source_items(p, nx.ti, src_base, smem_u32(&src_full[grp]), grp);
             ++src_issued[0];
           }
         }
@@ -1318,12 +1578,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                             static_cast<uint32_t>((src_issued[b] - 1) & 1), limit / 8 + 1);
       }
     } else {
-      for (int t = tile0; t < p.total_tiles; t += tile_step, ++it) {
-        const TileInfo ti = tile_at(t);
+      WorkWalk walk = work_begin(p, tile0, tile_step);
+      Work wk;
+      for (; work_next(p, walk, wk); ++it) {
+        TileInfo ti = wk.ti;
+        ti.m0 += m_off;
+        const int role = p.streamk ? work_role(wk) : kSkWhole;
         const int acc = it & 1;
         bool ok = mbar_wait_bounded(smem_u32(&tfull[acc]), static_cast<uint32_t>((it >> 1) & 1),
                                     abort_flag, status, kStatusEpilogueTimeout, limit,
                                     p.wait_hint_ns, kPair);
+        if (ok && role == kSkFinish)
+          ok = sk_wait_partials(p, wk, ew, tile_step, abort_flag, limit);
         if (!__all_sync(0xFFFFFFFFu, ok)) break;
         tc_fence_after();
         const int ph = ti.phase;
@@ -1344,12 +1610,20 @@ __global__ void __launch_bounds__(kThreads, 1)
                                  static_cast<uint32_t>(h * p.bn);
           for (int c0 = grp * 16; c0 < p.bn; c0 += 16 * kEpilogueGroups) {
             uint32_t v[16];
-            if (ti.kblocks > 0) {
+            const int g = h * (p.bn / 16) + c0 / 16;  // 16-column group within the tile
+            if (role == kSkFinish) {
+              sk_sum_partials<1>(p, wk, g, 1, row, tile_step, v);
+              tmem_add_groups<1>(taddr + static_cast<uint32_t>(c0), 1, v);
+            } else if (ti.kblocks > 0) {
               tmem_ld_32x32b_x16(taddr + static_cast<uint32_t>(c0), v);
               tmem_wait_ld_regs(v);
             } else {
 #pragma unroll
               for (int j = 0; j < 16; ++j) v[j] = 0u;
+            }
+            if (role == kSkPartial) {
+              sk_store16(p, static_cast<int>(blockIdx.x), g, row, v);
+              continue;
             }
             // Columns past the group's (or the conv's) last output channel are not stored.
             const int ch = ti.n0 + c0;
@@ -1362,6 +1636,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_before();
         __syncwarp();
         if (lane == 0) release_acc(acc);
+        if (role == kSkPartial) sk_publish(p, static_cast<int>(blockIdx.x), ew, lane);
       }
     }
   }

@@ -19,6 +19,7 @@ constexpr int kEpilogueWarps = 8;    // two warpgroups; each covers the 128 TMEM
 constexpr int kEpilogueGroups = 2;
 constexpr int kMaxPhases = 4;        // stride-phase GEMMs of a stride-2 transposed conv
 constexpr int kMaxStages = 12;
+constexpr int kMaxWindowBlocks = 60;  // resident filter blocks of the row-window loader
 
 constexpr int kKindF16 = 0;          // tcgen05.mma kind::f16 (bf16 or fp16 operands)
 constexpr int kKindF8 = 1;           // tcgen05.mma kind::f8f6f4 (fp8 e4m3 operands)
@@ -31,6 +32,7 @@ constexpr int kEpiSilu = 2;
 constexpr unsigned int kStatusProducerTimeout = 1u;
 constexpr unsigned int kStatusMmaTimeout = 2u;
 constexpr unsigned int kStatusEpilogueTimeout = 4u;
+constexpr unsigned int kStatusStreamKTimeout = 8u;  // a stream-K partial never arrived
 
 // Division by a fixed divisor d >= 1 as a multiply and shift, exact for
 // 0 <= x < 2^31: q = (umulhi(x, mul) + x) >> shift with shift = ceil(log2 d)
@@ -146,6 +148,23 @@ struct ConvKernelParams {  // aligned like CUtensorMap (64 B or more)
   FastDiv g_div_run, g_div_pr;     // division by g_run_bytes and by g_pr
   uint32_t g_stage_bytes;          // bytes per staging buffer
 
+  // Stream-K (convs whose tiles fill less than one wave of CTAs): the
+  // sequence of (tile, k-block) iterations, tile by tile, is cut into equal
+  // contiguous shares, one per CTA, and each share into work items at tile
+  // boundaries.  A CTA whose share starts inside a tile writes that item's
+  // fp32 accumulators to its partial slot and raises its epilogue warps'
+  // flags to sk_epoch; the CTA holding the tile's first k-block adds every
+  // such partial and runs the epilogue.
+  int streamk;
+  long long sk_iters;                    // iterations in all (< 2^31)
+  long long sk_iter_start[kMaxPhases + 1];  // first iteration of each phase
+  int sk_kpt[kMaxPhases];                // k-blocks per tile of each phase (> 0)
+  FastDiv sk_div_kpt[kMaxPhases];
+  uint32_t sk_epoch;                     // this launch's flag value (never 0)
+  unsigned int* sk_flags;                // [CTA][epilogue warp]
+  float* sk_partials;                    // [CTA][m_halves * bn / 16][128 rows][16]
+  uint32_t sk_slot_floats;               // floats per CTA slot
+
   int epi_mode;                    // 0 direct stores, 1 TMA store [M][C_out], 2 TMA 4-D phase grid,
                                    // 3 TMA 4-D row window
   int cw;                          // epilogue chunk width in columns (16, 32 or 64)
@@ -164,7 +183,8 @@ struct ConvKernelParams {  // aligned like CUtensorMap (64 B or more)
   unsigned int* status;
   long long timeout_cycles;        // limit of every bounded wait, in SM cycles
   uint32_t wait_hint_ns;           // suspend hint for waits off the MMA's critical path (0: poll)
-  int fault_mode;                  // test hook: 1 = CTA 0 skips its first arrive
+  int fault_mode;                  // test hook: 1 = CTA 0 skips its first arrive;
+                                   // 2 = stream-K partials never raise their flags
 };
 
 }  // namespace convgb300

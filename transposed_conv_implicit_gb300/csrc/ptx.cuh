@@ -131,6 +131,20 @@ __device__ __forceinline__ bool mbar_wait_drain(uint32_t bar, uint32_t parity, l
   }
 }
 
+// ---------------------------------------------------------------- global flags
+// 32-bit flag store with release semantics at GPU scope: every write this
+// thread made (or observed through a barrier) before it is visible to a
+// thread whose acquire load sees the value.
+__device__ __forceinline__ void st_release_gpu(unsigned int* addr, unsigned int v) {
+  asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(addr), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ unsigned int ld_acquire_gpu(const unsigned int* addr) {
+  unsigned int v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(addr) : "memory");
+  return v;
+}
+
 // ---------------------------------------------------------------- TMA
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
