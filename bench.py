@@ -65,7 +65,9 @@ KERNEL_SOURCES = ["transposed_conv_implicit_gb300/csrc/conv_kernel.cuh",
                   "transposed_conv_implicit_gb300/csrc/conv_launch.cuh",
                   "transposed_conv_implicit_gb300/csrc/conv_direct.cu",
                   "transposed_conv_implicit_gb300/csrc/conv_rowtap.cu",
-                  "transposed_conv_implicit_gb300/csrc/conv_kernels_pair.cu"]
+                  "transposed_conv_implicit_gb300/csrc/conv_kernels_pair.cu",
+                  "transposed_conv_implicit_gb300/csrc/conv_kernels_sk.cu",
+                  "transposed_conv_implicit_gb300/csrc/segment_copy.cuh"]
 
 
 def kernel_source_hash() -> str:

@@ -1,7 +1,8 @@
 """Builds libconvgb300.so in-tree with nvcc for sm_103a.
 
-Three translation units compile in parallel (host dispatcher + packing
-kernels, the implicit-GEMM kernel instances) and link into one shared library
+The translation units compile in parallel (host dispatcher + packing
+kernels, the implicit-GEMM kernel instances by loader and schedule, the
+row-tap and direct kernels) and link into one shared library
 next to this file.  The library links the shared CUDA runtime, so a process
 that already loaded PyTorch's runtime reuses it; the driver's tensor-map
 encoders are fetched at run time, so no libcuda link is needed.
@@ -20,8 +21,7 @@ ROOT = os.path.dirname(HERE)
 BUILD_DIR = os.path.join(HERE, "_build")
 LIB_PATH = os.path.join(HERE, "libconvgb300.so")
 SOURCES = ["conv_api.cu", "conv_kernels.cu", "conv_kernels_gather.cu", "conv_kernels_pair.cu",
-           "conv_direct.cu",
-           "conv_rowtap.cu"]
+           "conv_kernels_sk.cu", "conv_direct.cu", "conv_rowtap.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -604,7 +604,7 @@ void plan_window(const FwdShape& f, Plan* pl, int num_sms, int has_residual) {
   if (pitch > kBM || f.c_out > 256) return;
   const int bn = ((f.c_out + 15) / 16) * 16;
   const size_t bres = static_cast<size_t>(f.r) * f.s * kp.c_blocks * bn * kp.sw_bytes;
-  if (bres > 120 * 1024 || f.r * f.s * kp.c_blocks > kMaxWindowBlocks) return;
+  if (bres > 120 * 1024) return;
   const int mh = bn <= 128 ? 2 : 1;
   const int rows = kBM / pitch;
   const int rows_tile = mh * rows;
@@ -1300,17 +1300,23 @@ conv_status_t plan_memory_direct(Plan* pl) {
   const bool can_res = !kp.pair && !kp.streamk && kp.num_phases == 1 && kp.n_tiles == 1 &&
                        kp.groups <= 1;
   const size_t bres = can_res ? static_cast<size_t>(kp.taps_h[0]) * kp.taps_w[0] * kp.c_blocks * b_bytes : 0;
+  // Few output channels with contiguous rows: staged 16-byte stores.
+  kp.seg_store = (!kp.vec_ok && kp.num_phases == 1 && kp.out_step_h == 1 && kp.out_step_w == 1 &&
+                  kp.groups <= 1 && kp.n_tiles == 1 && kp.bn == 16 && kp.Cout <= 16 && !kp.pair)
+                     ? 1 : 0;
+  kp.seg_slot_bytes = static_cast<uint32_t>((32 * 16 * 2 + 16 + 15) & ~15);
+  const size_t seg_bytes = kp.seg_store ? align1k(static_cast<size_t>(4) * 2 * kp.seg_slot_bytes) : 0;
   bool res = false;
   int stages = 0;
   if (can_res) {
-    const size_t used = 1024 + bar_bytes + align1k(bres);
+    const size_t used = 1024 + bar_bytes + align1k(bres) + seg_bytes;
     if (used + 4 * static_cast<size_t>(a_bytes) <= kSmemLimit) {
       res = true;
       stages = static_cast<int>(std::min<size_t>(kMaxStages, (kSmemLimit - used) / a_bytes));
     }
   }
   if (!res) {
-    const size_t used = 1024 + bar_bytes;
+    const size_t used = 1024 + bar_bytes + seg_bytes;
     stages = static_cast<int>(std::min<size_t>(kMaxStages, (kSmemLimit - used) / (a_bytes + b_bytes)));
     if (stages < 2) return CONV_ERR_NOT_SUPPORTED;
   }
@@ -1323,6 +1329,8 @@ conv_status_t plan_memory_direct(Plan* pl) {
   if (!res) off += align1k(static_cast<size_t>(stages) * b_bytes);
   kp.off_bres = off;
   if (res) off += align1k(bres);
+  kp.off_seg = off;
+  off += static_cast<uint32_t>(seg_bytes);
   kp.off_src = off;
   kp.off_stg = off;
   kp.off_bar = off;
@@ -1471,12 +1479,17 @@ bool plan_rowtap(const FwdShape& f, int groups, int num_sms, RowTapPlan* out) {
   const size_t stage_bytes = 128 * 128;
   const size_t b_bytes = static_cast<size_t>(rp.c_blocks) * f.r * g16 * 128;
   const size_t part_bytes = static_cast<size_t>(2 * 2) * g16 * 128 * sizeof(float);
-  const size_t fixed = 1024 + align1k(b_bytes) + align1k(part_bytes) + 1024;
+  // Row-segment stages of the epilogue: output and source, per group.
+  const int seg_stage = static_cast<int>((static_cast<size_t>(128) * f.c_out * 2 + 16 + 15) & ~size_t(15));
+  const size_t seg_bytes = static_cast<size_t>(4) * seg_stage;
+  const size_t fixed = 1024 + align1k(b_bytes) + align1k(part_bytes) + align1k(seg_bytes) + 1024;
   if (fixed + 2 * stage_bytes > kSmemLimit) return false;
   rp.stages = static_cast<int>(std::min<size_t>(kMaxStages, (kSmemLimit - fixed) / stage_bytes));
   rp.off_b = static_cast<uint32_t>(rp.stages * stage_bytes);
   rp.off_part = rp.off_b + align1k(b_bytes);
-  rp.off_bar = rp.off_part + align1k(part_bytes);
+  rp.off_stage = rp.off_part + align1k(part_bytes);
+  rp.stage_bytes = seg_stage;
+  rp.off_bar = rp.off_stage + align1k(seg_bytes);
   out->smem_bytes = 1024 + rp.off_bar + 1024;
   out->grid = static_cast<int>(std::min<long long>(tiles, num_sms));
   return true;

@@ -71,6 +71,8 @@ struct RowTapParams {  // aligned like CUtensorMap
   uint32_t idesc_rest; // N = (R - 1) * g16 (R > 1)
   uint32_t cols_per_buf, tmem_cols;
   uint32_t off_b, off_part, off_bar;  // shared-memory offsets (A ring at 0)
+  uint32_t off_stage;  // output and source row-segment stages, two epilogue groups each
+  int stage_bytes;     // bytes per segment stage: 128 * F * elt + 16, rounded to 16
   int has_residual, epilogue;
   float beta;
   const void* src;
@@ -87,6 +89,10 @@ cudaError_t launch_conv_rowtap(int in_dtype, bool out_bf16, const RowTapParams& 
 // The CTA-pair instances (cta_group::2; their own translation unit).
 cudaError_t launch_conv_igemm_pair(int kind, bool out_bf16, const ConvKernelParams& p, int grid,
                                    size_t smem_bytes, cudaStream_t stream);
+
+// The stream-K instances (TMA loaders, single CTAs; their own translation unit).
+cudaError_t launch_conv_igemm_streamk(int kind, bool out_bf16, const ConvKernelParams& p, int grid,
+                                      size_t smem_bytes, cudaStream_t stream);
 
 // The gather-loader instances (their own translation unit).
 cudaError_t launch_conv_igemm_gather(int kind, bool out_bf16, const ConvKernelParams& p, int grid,

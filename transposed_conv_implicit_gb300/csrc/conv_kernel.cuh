@@ -45,6 +45,7 @@
 
 #include "conv_params.h"
 #include "ptx.cuh"
+#include "segment_copy.cuh"
 
 namespace convgb300 {
 
@@ -114,12 +115,15 @@ __device__ __forceinline__ int sk_owner(const ConvKernelParams& p, long long pos
   return static_cast<int>(((pos + 1) * nctas - 1) / p.sk_iters);
 }
 
+// kStreamK: the kernel instance runs the stream-K schedule (a separate
+// instance, so that the whole-tile instances carry none of its code).
+template <bool kStreamK>
 __device__ __forceinline__ WorkWalk work_begin(const ConvKernelParams& p, int cta, int nctas) {
   WorkWalk w;
   w.t = cta;
   w.step = nctas;
-  w.pos = p.streamk ? sk_share_begin(p, cta, nctas) : 0;
-  w.end = p.streamk ? sk_share_begin(p, cta + 1, nctas) : 0;
+  w.pos = kStreamK ? sk_share_begin(p, cta, nctas) : 0;
+  w.end = kStreamK ? sk_share_begin(p, cta + 1, nctas) : 0;
   return w;
 }
 
@@ -129,8 +133,9 @@ __device__ __forceinline__ long long sk_tile_iter(const ConvKernelParams& p, int
          static_cast<long long>(tile - p.tile_start[phase]) * p.sk_kpt[phase];
 }
 
+template <bool kStreamK>
 __device__ __forceinline__ bool work_next(const ConvKernelParams& p, WorkWalk& w, Work& out) {
-  if (p.streamk) {
+  if constexpr (kStreamK) {
     if (w.pos >= w.end) return false;
     int ph = 0;
     while (ph + 1 < p.num_phases && w.pos >= p.sk_iter_start[ph + 1]) ++ph;
@@ -455,6 +460,46 @@ __device__ __forceinline__ void epilogue_16_direct(const ConvKernelParams& p, lo
   }
 }
 
+// Direct epilogue of few output channels through a shared-memory stage
+// (seg_store): the warp's 32 rows, from GEMM row mw0, are one contiguous run
+// of nrows * C_out outputs; each lane computes its row's C_out values from
+// acc (+ beta * source, read through the source stage), the warp then writes
+// the run with 16-byte words.  `st` holds the output stage, then the source
+// stage.
+template <typename OutT>
+__device__ __forceinline__ void epilogue_seg_warp(const ConvKernelParams& p, int mw0, int lane,
+                                                  const uint32_t (&acc)[16], uint8_t* st) {
+  const int nrows = min(32, p.rows[0] - mw0);
+  if (nrows <= 0) return;
+  const int cout = p.Cout;
+  const long long first = static_cast<long long>(mw0) * cout;
+  uint8_t* gout = reinterpret_cast<uint8_t*>(static_cast<OutT*>(p.out) + first);
+  const int phase16 = static_cast<int>(reinterpret_cast<uintptr_t>(gout) & 15u);
+  const int bytes = nrows * cout * static_cast<int>(sizeof(OutT));
+  uint8_t* st_src = st + p.seg_slot_bytes;
+  if (p.has_residual) {
+    copy_segment16<true>(
+        reinterpret_cast<const uint8_t*>(static_cast<const OutT*>(p.src) + first), st_src,
+        phase16, bytes, lane, 32);
+    __syncwarp();
+  }
+  if (lane < nrows) {
+    const OutT* sv = reinterpret_cast<const OutT*>(st_src + phase16) + lane * cout;
+    OutT* ov = reinterpret_cast<OutT*>(st + phase16) + lane * cout;
+#pragma unroll
+    for (int c = 0; c < 16; ++c) {
+      if (c < cout) {
+        float f = __uint_as_float(acc[c]);
+        if (p.has_residual) f = fmaf(p.beta, to_f32<OutT>(sv[c]), f);
+        ov[c] = from_f32<OutT>(activation(f, p.epilogue));
+      }
+    }
+  }
+  __syncwarp();
+  copy_segment16<false>(gout, st, phase16, bytes, lane, 32);
+  __syncwarp();  // the stage is free again
+}
+
 // Issues the TMA loads of the residual-source chunks that epilogue group
 // `grp` owns in one tile: work item q = h * nchunks + c (128-row half h,
 // column chunk c) belongs to group q % 2.  The buffer is laid out
@@ -523,7 +568,7 @@ __device__ __forceinline__ void issue_kblock(uint32_t d_tmem, uint64_t desc_hi, 
 // The MMA role for one (kSteps, kHalves) specialisation.  Tiles t0, t0 +
 // step, ...  kPair: rank 0 of a CTA pair issues M = 256 MMAs over both CTAs'
 // operands (each holds bn/2 rows of B) and commits to both CTAs' barriers.
-template <int kKind, int kSteps, int kHalves, bool kPair = false>
+template <int kKind, int kSteps, int kHalves, bool kPair = false, bool kStreamK = false>
 __device__ __forceinline__ bool mma_role(const ConvKernelParams& p, uint32_t tmem_base,
                                          uint8_t* a_ring, uint8_t* b_ring, uint8_t* b_res,
                                          uint64_t* full, uint64_t* empty, uint64_t* tfull,
@@ -555,9 +600,9 @@ __device__ __forceinline__ bool mma_role(const ConvKernelParams& p, uint32_t tme
   bool ok = true;
   int it = 0;
   (void)total_tiles;
-  WorkWalk walk = work_begin(p, t0, step);
+  WorkWalk walk = work_begin<kStreamK>(p, t0, step);
   Work wk;
-  for (; ok && work_next(p, walk, wk); ++it) {
+  for (; ok && work_next<kStreamK>(p, walk, wk); ++it) {
     const TileInfo& ti = wk.ti;
     const int acc = it & 1;
     if (!mbar_wait_bounded(smem_u32(&tempty[acc]), static_cast<uint32_t>(((it >> 1) & 1) ^ 1),
@@ -615,16 +660,12 @@ __device__ __forceinline__ bool mma_role(const ConvKernelParams& p, uint32_t tme
 // the tile's input rows with halo; tap (r, s) of half h starts at box row
 // h*win_half_rows + r*win_pitch + s.  The filter is resident: block
 // (tap, cb) of the packed filter sits at index tap*c_blocks + cb.
-// On the CTA's first tile each filter block (tap, cb) has its own barrier
-// (wbar[tap * c_blocks + cb]), so the MMAs of tap 0 start as soon as the
-// input box and that one block have landed.
 template <int kKind, int kSteps, int kHalves>
 __device__ __forceinline__ bool mma_role_window(const ConvKernelParams& p, uint32_t tmem_base,
                                                 uint8_t* a_ring, uint8_t* b_res, uint64_t* full,
                                                 uint64_t* empty, uint64_t* tfull, uint64_t* tempty,
-                                                uint64_t* wbar, volatile int* abort_flag,
-                                                unsigned int* status, long long limit, int t0,
-                                                int step) {
+                                                volatile int* abort_flag, unsigned int* status,
+                                                long long limit, int t0, int step) {
   const int stages = p.stages;
   const uint32_t sw = p.sw_bytes;  // 128 in this mode
   const uint32_t b_bytes = static_cast<uint32_t>(p.bn) * sw;
@@ -671,14 +712,6 @@ __device__ __forceinline__ bool mma_role_window(const ConvKernelParams& p, uint3
       uint32_t b_lo = b_lo0 + static_cast<uint32_t>(cb) * b_step;
       int s = 0;
       for (int tap = 0; tap < taps; ++tap) {
-        if (it == 0) {
-          if (!mbar_wait_bounded(smem_u32(&wbar[tap * c_blocks + cb]), 0u, abort_flag, status,
-                                 kStatusMmaTimeout, limit)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-        }
         issue_kblock<kKind, kSteps, kHalves>(d_tmem, desc_hi, tap_lo, b_lo, half_lo, bn_cols,
                                              idesc, (cb | tap) != 0 ? 1u : 0u);
         b_lo += b_tap_step;
@@ -688,7 +721,6 @@ __device__ __forceinline__ bool mma_role_window(const ConvKernelParams& p, uint3
           tap_lo += a_row_skip;
         }
       }
-      if (!ok) break;
       mma_commit(empty0 + 8u * stage);
       a_lo += a_step;
       if (++stage == stages) {
@@ -1075,7 +1107,7 @@ __device__ __forceinline__ void gather_producer(const ConvKernelParams& p, int r
 // [r*bn/2, (r+1)*bn/2) of B into its own shared memory, rank 0 issues M = 256
 // MMAs over both (tcgen05 cta_group::2), and each CTA's epilogue stores its
 // 128 rows from its own TMEM.  TMA im2col loader, streamed filter only.
-template <int kKind, typename OutT, bool kGather, bool kPair = false>
+template <int kKind, typename OutT, bool kGather, bool kPair = false, bool kStreamK = false>
 __global__ void __launch_bounds__(kThreads, 1)
     conv_igemm_kernel(const __grid_constant__ ConvKernelParams p) {
   extern __shared__ uint8_t smem_raw[];
@@ -1111,9 +1143,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* gst_empty = gst_full + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gst_empty + 2);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
-  // Row-window loader: one barrier per resident filter block, for the first
-  // tile (at most kMaxWindowBlocks, from byte 512 of the barrier region).
-  uint64_t* wbar = bars + 64;
   unsigned int* status = p.status;
   const long long limit = p.timeout_cycles;
 
@@ -1135,8 +1164,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(smem_u32(&gst_full[b]), 1);
       mbar_init(smem_u32(&gst_empty[b]), kGatherProducers);  // every builder warp
     }
-    if (p.window)
-      for (int i = 0; i < p.win_R * p.win_S * p.c_blocks; ++i) mbar_init(smem_u32(&wbar[i]), 1);
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -1186,7 +1213,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = true;
       const uint32_t stage_tx = a_bytes + (p.b_resident ? 0u : b_bytes);
       bool first_tile = true;  // a resident filter is loaded k-block by k-block with it
-      unsigned long long win_blocks_issued = 0;  // channel blocks whose filter blocks are in flight
       if (p.window) {
         // One tiled box of input rows (with halo) per channel block; the
         // first tile also brings every tap's filter block of that channel block.
@@ -1205,20 +1231,17 @@ __global__ void __launch_bounds__(kThreads, 1)
               last_issued = seq;
               if (!(p.fault_mode == 1 && blockIdx.x == 0 && seq == 0)) {
                 const uint32_t fb = smem_u32(&full[stage]);
-                mbar_arrive_expect_tx(fb, box_bytes);
+                // The first tile also brings every tap's filter block of this
+                // channel block, on the same barrier.  (Each block on its own
+                // barrier, so that tap 0's MMAs could start earlier, measured
+                // slower: the ResNet 3x3 conv ran 19.0 against 16.7 us.)
+                mbar_arrive_expect_tx(fb, box_bytes + (first_tile ? b_bytes * taps : 0u));
                 tma_load_4d(smem_u32(a_ring + stage * p.win_stage_bytes), &p.map_a[0], fb,
                             cb * p.bk, -p.win_pad_w, oy0 - p.win_pad_h, n_img);
-                if (first_tile) {
-                  // Each filter block on its own barrier, in the MMA's order.
-                  for (int tap = 0; tap < taps; ++tap) {
-                    const int blk = tap * p.c_blocks + cb;
-                    const uint32_t wb = smem_u32(&wbar[blk]);
-                    mbar_arrive_expect_tx(wb, b_bytes);
-                    tma_load_3d(smem_u32(b_res + blk * b_bytes), &p.map_b, wb,
+                if (first_tile)
+                  for (int tap = 0; tap < taps; ++tap)
+                    tma_load_3d(smem_u32(b_res + (tap * p.c_blocks + cb) * b_bytes), &p.map_b, fb,
                                 tap * p.c_in + cb * p.bk, 0, 0);
-                  }
-                  win_blocks_issued |= 1ull << cb;
-                }
               }
             }
             if (++stage == stages) {
@@ -1232,9 +1255,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       // A pair's rank 0 arms its stage barrier for both CTAs' bytes; rank 1's
       // copies count on rank 0's barrier.
       const uint32_t arm_tx = kPair ? 2u * stage_tx : stage_tx;
-      WorkWalk walk = work_begin(p, tile0, tile_step);
+      WorkWalk walk = work_begin<kStreamK>(p, tile0, tile_step);
       Work wk;
-      while (!p.window && ok && work_next(p, walk, wk)) {
+      while (!p.window && ok && work_next<kStreamK>(p, walk, wk)) {
         const int t = wk.tile;
         TileInfo ti = wk.ti;
         ti.m0 += m_off;
@@ -1251,7 +1274,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // The work item's first k-block: channel block cb of tap (uh, uw).
         int cb = 0, uw = 0, uh = 0;
         int bk_k = 0;  // k coordinate of this k-block in the packed filter: tap*C_in + cb*bk
-        if (wk.kb0 != 0) {
+        if (kStreamK && wk.kb0 != 0) {
           const int tap = wk.kb0 / p.c_blocks;
           cb = wk.kb0 - tap * p.c_blocks;
           uh = tap / tw;
@@ -1345,11 +1368,6 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (q >= 0 && (q & 1) == role)
             mbar_wait_drain(smem_u32(&full[q % stages]), static_cast<uint32_t>((q / stages) & 1),
                             limit / 8 + 1);
-        if (p.window)
-          for (int cb = 0; cb < p.c_blocks; ++cb)
-            if (win_blocks_issued >> cb & 1ull)
-              for (int tap = 0; tap < p.win_R * p.win_S; ++tap)
-                mbar_wait_drain(smem_u32(&wbar[tap * p.c_blocks + cb]), 0u, limit / 8 + 1);
       }
     }
     __syncwarp();
@@ -1362,18 +1380,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!kPair && p.window) {
         ok = p.m_halves == 2
                  ? mma_role_window<kKind, 4, 2>(p, tmem_base, a_ring, b_res, full, empty, tfull,
-                                                tempty, wbar, abort_flag, status, limit, tile0,
-                                                tile_step)
+                                                tempty, abort_flag, status, limit, tile0, tile_step)
                  : mma_role_window<kKind, 4, 1>(p, tmem_base, a_ring, b_res, full, empty, tfull,
-                                                tempty, wbar, abort_flag, status, limit, tile0,
-                                                tile_step);
+                                                tempty, abort_flag, status, limit, tile0, tile_step);
         if (!ok) {
           mma_commit(smem_u32(drain));
           mbar_wait_drain(smem_u32(drain), 0, limit / 8 + 1);
         }
       } else {
 #define CONV_MMA_ROLE(KS, MH)                                                                   \
-  mma_role<kKind, KS, MH, kPair>(p, tmem_base, a_ring, b_ring, b_res, full, empty, tfull, tempty,  \
+  mma_role<kKind, KS, MH, kPair, kStreamK>(p, tmem_base, a_ring, b_ring, b_res, full, empty,       \
+                                           tfull, tempty,                                         \
                                  bres_full, abort_flag, status, limit, tile0, tile_step)
       if (!kPair && p.m_halves == 2)
         ok = ks == 4 ? CONV_MMA_ROLE(4, 2) : (ks == 2 ? CONV_MMA_ROLE(2, 2) : CONV_MMA_ROLE(1, 2));
@@ -1424,25 +1441,25 @@ __global__ void __launch_bounds__(kThreads, 1)
       int store_seq = 0;
       int src_issued[2] = {0, 0};  // source loads issued per buffer (leader only)
       // Work items in order; the source prefetch peeks at the next one.
-      WorkWalk walk = work_begin(p, tile0, tile_step);
+      WorkWalk walk = work_begin<kStreamK>(p, tile0, tile_step);
       Work cur{};
-      bool have = work_next(p, walk, cur);
+      bool have = work_next<kStreamK>(p, walk, cur);
       if (p.has_residual && leader && have) {
         TileInfo t0i = cur.ti;
         t0i.m0 += m_off;
         issue_source_items(p, t0i, src_base, smem_u32(&src_full[grp]), grp);
         ++src_issued[0];
       }
-      for (; have; ++it, have = work_next(p, walk, cur)) {
+      for (; have; ++it, have = work_next<kStreamK>(p, walk, cur)) {
         TileInfo ti = cur.ti;
         ti.m0 += m_off;
-        const int role = p.streamk ? work_role(cur) : kSkWhole;
+        const int role = kStreamK ? work_role(cur) : kSkWhole;
         const int acc = it & 1;
         const int sbuf = p.src_bufs == 2 ? acc : 0;
         if (p.has_residual && leader && p.src_bufs == 2) {
           WorkWalk ahead = walk;
           Work nx;
-          if (work_next(p, ahead, nx)) {
+          if (work_next<kStreamK>(p, ahead, nx)) {
             nx.ti.m0 += m_off;
             // The other buffer last held item it-1, whose stores must have read it.
             bulk_wait_read_all();
@@ -1558,7 +1575,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (p.has_residual && leader && p.src_bufs == 1) {
           WorkWalk ahead = walk;
           Work nx;
-          if (work_next(p, ahead, nx)) {
+          if (work_next<kStreamK>(p, ahead, nx)) {
             nx.ti.m0 += m_off;
             // Single source buffer: fetch the next item's source once this
             // item's stores (which read it) are done reading.
@@ -1578,12 +1595,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                             static_cast<uint32_t>((src_issued[b] - 1) & 1), limit / 8 + 1);
       }
     } else {
-      WorkWalk walk = work_begin(p, tile0, tile_step);
+      WorkWalk walk = work_begin<kStreamK>(p, tile0, tile_step);
       Work wk;
-      for (; work_next(p, walk, wk); ++it) {
+      for (; work_next<kStreamK>(p, walk, wk); ++it) {
         TileInfo ti = wk.ti;
         ti.m0 += m_off;
-        const int role = p.streamk ? work_role(wk) : kSkWhole;
+        const int role = kStreamK ? work_role(wk) : kSkWhole;
         const int acc = it & 1;
         bool ok = mbar_wait_bounded(smem_u32(&tfull[acc]), static_cast<uint32_t>((it >> 1) & 1),
                                     abort_flag, status, kStatusEpilogueTimeout, limit,
@@ -1623,6 +1640,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             if (role == kSkPartial) {
               sk_store16(p, static_cast<int>(blockIdx.x), g, row, v);
+              continue;
+            }
+            if (p.seg_store) {  // (one 16-column chunk: group 0's warps only)
+              epilogue_seg_warp<OutT>(p, ti.m0 + h * kBM + quarter * 32, lane, v,
+                                      smem + p.off_seg + quarter * 2 * p.seg_slot_bytes);
               continue;
             }
             // Columns past the group's (or the conv's) last output channel are not stored.

@@ -48,6 +48,7 @@ cudaError_t launch_conv_igemm(int kind, bool out_bf16, const ConvKernelParams& p
                               size_t smem_bytes, cudaStream_t stream) {
   if (p.gather) return launch_conv_igemm_gather(kind, out_bf16, p, grid, smem_bytes, stream);
   if (p.pair) return launch_conv_igemm_pair(kind, out_bf16, p, grid, smem_bytes, stream);
+  if (p.streamk) return launch_conv_igemm_streamk(kind, out_bf16, p, grid, smem_bytes, stream);
   return launch_family<false>(kind, out_bf16, p, grid, smem_bytes, stream);
 }
 

@@ -11,7 +11,7 @@ namespace convgb300 {
 
 constexpr int kMaxDevices = 64;
 
-template <int kKind, typename OutT, bool kGather, bool kPair = false>
+template <int kKind, typename OutT, bool kGather, bool kPair = false, bool kStreamK = false>
 cudaError_t launch_instance(const ConvKernelParams& p, int grid, size_t smem_bytes,
                             cudaStream_t stream) {
   // The dynamic shared-memory limit is a per-device function attribute: raise
@@ -22,7 +22,7 @@ cudaError_t launch_instance(const ConvKernelParams& p, int grid, size_t smem_byt
   if (err != cudaSuccess) return err;
   if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
   if (configured[dev].load(std::memory_order_relaxed) < smem_bytes) {
-    err = cudaFuncSetAttribute(conv_igemm_kernel<kKind, OutT, kGather, kPair>,
+    err = cudaFuncSetAttribute(conv_igemm_kernel<kKind, OutT, kGather, kPair, kStreamK>,
                                cudaFuncAttributeMaxDynamicSharedMemorySize,
                                static_cast<int>(smem_bytes));
     if (err != cudaSuccess) return err;
@@ -48,19 +48,21 @@ cudaError_t launch_instance(const ConvKernelParams& p, int grid, size_t smem_byt
     attr[1].val.clusterDim.z = 1;
     cfg.numAttrs = 2;
   }
-  err = cudaLaunchKernelEx(&cfg, conv_igemm_kernel<kKind, OutT, kGather, kPair>, p);
+  err = cudaLaunchKernelEx(&cfg, conv_igemm_kernel<kKind, OutT, kGather, kPair, kStreamK>, p);
   if (err != cudaSuccess) return err;
   return cudaGetLastError();
 }
 
-template <bool kGather, bool kPair = false>
+template <bool kGather, bool kPair = false, bool kStreamK = false>
 cudaError_t launch_family(int kind, bool out_bf16, const ConvKernelParams& p, int grid,
                           size_t smem_bytes, cudaStream_t stream) {
   if (kind == kKindF8)
-    return launch_instance<kKindF8, __nv_bfloat16, kGather, kPair>(p, grid, smem_bytes, stream);
+    return launch_instance<kKindF8, __nv_bfloat16, kGather, kPair, kStreamK>(p, grid, smem_bytes,
+                                                                            stream);
   if (out_bf16)
-    return launch_instance<kKindF16, __nv_bfloat16, kGather, kPair>(p, grid, smem_bytes, stream);
-  return launch_instance<kKindF16, __half, kGather, kPair>(p, grid, smem_bytes, stream);
+    return launch_instance<kKindF16, __nv_bfloat16, kGather, kPair, kStreamK>(p, grid, smem_bytes,
+                                                                             stream);
+  return launch_instance<kKindF16, __half, kGather, kPair, kStreamK>(p, grid, smem_bytes, stream);
 }
 
 }  // namespace convgb300

@@ -19,7 +19,6 @@ constexpr int kEpilogueWarps = 8;    // two warpgroups; each covers the 128 TMEM
 constexpr int kEpilogueGroups = 2;
 constexpr int kMaxPhases = 4;        // stride-phase GEMMs of a stride-2 transposed conv
 constexpr int kMaxStages = 12;
-constexpr int kMaxWindowBlocks = 60;  // resident filter blocks of the row-window loader
 
 constexpr int kKindF16 = 0;          // tcgen05.mma kind::f16 (bf16 or fp16 operands)
 constexpr int kKindF8 = 1;           // tcgen05.mma kind::f8f6f4 (fp8 e4m3 operands)
@@ -175,6 +174,14 @@ struct ConvKernelParams {  // aligned like CUtensorMap (64 B or more)
 
   int Ho, Wo, Cout;
   int vec_ok;                      // C_out * 2 bytes is a multiple of 16: 16-B stores
+  // Direct epilogue of few output channels (C_out <= 16, not a multiple of
+  // 8; one phase, one group, rows contiguous in the output): each epilogue
+  // warp assembles its 32 rows' outputs in a shared-memory stage and writes
+  // them as 16-byte words (seg_slot_bytes per stage; an output and a source
+  // stage per warp of the first epilogue group, from off_seg).
+  int seg_store;
+  uint32_t off_seg;
+  uint32_t seg_slot_bytes;
   int has_residual;
   int epilogue;
   float beta;

@@ -32,6 +32,7 @@
 
 #include "conv_internal.h"
 #include "ptx.cuh"
+#include "segment_copy.cuh"
 
 namespace convgb300 {
 
@@ -40,17 +41,6 @@ namespace {
 constexpr int kRtWarps = 10;  // producer, MMA, 8 epilogue warps (two groups of 4)
 constexpr int kRtThreads = 32 * kRtWarps;
 constexpr uint32_t kRtStageBytes = 128 * 128;  // 128 pixels x 128-byte channel block
-
-template <typename OutT>
-__device__ __forceinline__ float rt_load(const OutT* p);
-template <>
-__device__ __forceinline__ float rt_load<__nv_bfloat16>(const __nv_bfloat16* p) {
-  return __bfloat162float(*p);
-}
-template <>
-__device__ __forceinline__ float rt_load<__half>(const __half* p) {
-  return __half2float(*p);
-}
 
 template <typename OutT>
 __device__ __forceinline__ OutT rt_round(float v);
@@ -68,6 +58,9 @@ __device__ __forceinline__ float rt_activation(float v, int act) {
   if (act == kEpiSilu) return v / (1.0f + __expf(-v));
   return v;
 }
+
+__device__ __forceinline__ float rt_to_float(__nv_bfloat16 v) { return __bfloat162float(v); }
+__device__ __forceinline__ float rt_to_float(__half v) { return __half2float(v); }
 
 struct RtTile {
   int n, oy0, x0, rows;
@@ -124,6 +117,8 @@ __global__ void __launch_bounds__(kRtThreads, 1)
   uint8_t* a_ring = smem;
   uint8_t* b_res = smem + p.off_b;
   float* part = reinterpret_cast<float*>(smem + p.off_part);
+  uint8_t* ostage = smem + p.off_stage;                   // [group] output row segment
+  uint8_t* sstage = ostage + 2 * p.stage_bytes;           // [group] residual source segment
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + p.off_bar);
   uint64_t* full = bars;
   uint64_t* empty = bars + stages;
@@ -354,18 +349,40 @@ __global__ void __launch_bounds__(kRtThreads, 1)
           ok = false;
           break;
         }
-        const int ox = ti.x0 + j;
-        if (j < p.seg_w && ox < p.Wo) {
-          const long long o =
-              ((static_cast<long long>(ti.n) * p.Ho + ti.oy0 + q) * p.Wo + ox) * p.F;
+        // The row segment's outputs are contiguous in the NHWC output
+        // (npx pixels x F channels).  They are assembled in shared memory at
+        // the same 16-byte phase as their global address, so that the copy
+        // out (and the residual source's copy in) moves aligned 16-byte words;
+        // only the few bytes before the first and after the last 16-byte
+        // boundary move as single elements.
+        const int npx = min(p.seg_w, p.Wo - ti.x0);
+        const long long o0 =
+            ((static_cast<long long>(ti.n) * p.Ho + ti.oy0 + q) * p.Wo + ti.x0) * p.F;
+        const int nel = npx * p.F;
+        const uintptr_t gbeg = reinterpret_cast<uintptr_t>(y + o0);
+        const int phase16 = static_cast<int>(gbeg & 15u);  // bytes before the first boundary's 16-byte word
+        uint8_t* ost = ostage + grp * p.stage_bytes;
+        if (p.has_residual) {
+          // Source segment in, same layout (into the group's source stage).
+          uint8_t* sst = sstage + grp * p.stage_bytes;
+          copy_segment16<true>(reinterpret_cast<const uint8_t*>(src + o0), sst, phase16,
+                                nel * static_cast<int>(sizeof(OutT)), j, 128);
+          named_barrier(bar_id, 128);
+        }
+        if (j < npx) {
+          const OutT* sv = reinterpret_cast<const OutT*>(sstage + grp * p.stage_bytes + phase16);
+          OutT* ov = reinterpret_cast<OutT*>(ost + phase16);
           for (int f = 0; f < p.F; ++f) {
             float a = 0.0f;
             const float* pf = pb + f * p.S * 128 + j;
             for (int s = 0; s < p.S; ++s) a += pf[s * 128 + s];
-            if (p.has_residual) a = fmaf(p.beta, rt_load<OutT>(src + o + f), a);
-            y[o + f] = rt_round<OutT>(rt_activation(a, p.epilogue));
+            if (p.has_residual) a = fmaf(p.beta, rt_to_float(sv[j * p.F + f]), a);
+            ov[j * p.F + f] = rt_round<OutT>(rt_activation(a, p.epilogue));
           }
         }
+        named_barrier(bar_id, 128);
+        copy_segment16<false>(reinterpret_cast<uint8_t*>(y + o0), ost, phase16,
+                               nel * static_cast<int>(sizeof(OutT)), j, 128);
       }
       if (!ok) break;
       tc_fence_before();
