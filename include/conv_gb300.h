@@ -168,35 +168,57 @@ conv_status_t conv2d_fwd_packed(const void* input, int n, int h, int w, int c_in
 /* ------------------------------------------------------------------------
  * Transposed convolution ("conv_transposed_gpu", description and Args): the
  * backward-data pass of the forward convolution, written as the scatter
- *   Y[n][iy*st - p + r][ix*st - p + s][f] += x[n][iy][ix][c] * w[r][s][f][c]
+ *   Y[n][iy*st_h - p_h + r*d_h][ix*st_w - p_w + s*d_w][f] += x[n][iy][ix][c] * w[r][s][f][c]
  * over the RSFC filter w [R][S][C_out][C_in] (F = output channels, C = input
  * channels; the same memory as the RSCF filter of the forward convolution
  * whose backward-data this is), then y = act(Y + beta*source).
  * It is computed as stride_h*stride_w dense implicit GEMMs, one per output
- * phase (oy mod stride, ox mod stride), with no zero insertion.
+ * phase (oy mod stride_h, ox mod stride_w), with no zero insertion: the taps
+ * r of phase a are those with r*d = a + p (mod stride) (with g = gcd(d,
+ * stride), every stride/g-th tap, or none), read at input dilation d/g.
+ * Phases are launched four at a time (a stride of 3 or 4 takes several
+ * launches of the same kernel; they write disjoint output pixels).
  *
  *  input  [n][h][w][c_in]; output [n][ho][wo][c_out]
- *  ho - ((h-1)*stride - 2*pad + (r-1) + 1) must lie in [0, stride) (the
- *  extra rows play the role of an output padding), likewise wo.
- * Gates: dtypes as conv2d_fwd; stride (1,1) or (2,2); dilation (1,1);
- * 0 <= pad < r (and < s); c_in * sizeof(in_dtype) a multiple of 16 bytes and
- * at least 32 bytes; r, s <= 32.
+ *  ho - ((h-1)*stride_h - 2*p_h + d_h*(r-1) + 1) must lie in [0, stride_h)
+ *  (the extra rows play the role of an output padding), likewise wo.
+ * Gates: dtypes as conv2d_fwd; stride_h, stride_w >= 1 with
+ * stride_h*stride_w <= 16 (per-axis strides may differ); dilation 1..32 per
+ * axis; 0 <= p <= d*(r-1) per axis; c_in * sizeof(in_dtype) a multiple of 16
+ * bytes and at least 32 bytes; r, s <= 32.
  * conv_transposed packs the filter into the workspace on every call;
- * conv_transposed_packed takes the result of conv_transposed_pack_filter.
+ * conv_transposed_packed takes the result of conv_transposed_pack_filter
+ * (dilation 1) or conv_transposed_pack_filter_dilated, which must have been
+ * called with the same stride, dilation and padding.
  * Packed layout: [stride_h*stride_w phases][c_out][K_max], phase (a, b) at
  * index a*stride_w + b, with k = (u*T_w + v)*c_in + c over the phase's taps.
+ * The _dilated sizes and packing take the dilation; the others assume (1, 1).
  * ------------------------------------------------------------------------ */
 size_t conv_transposed_packed_filter_bytes(int r, int s, int c_in, int c_out,
                                            const int stride[2], const int padding[2],
                                            conv_dtype_t dtype);
 
+size_t conv_transposed_packed_filter_bytes_dilated(int r, int s, int c_in, int c_out,
+                                                   const int stride[2], const int dilation[2],
+                                                   const int padding[2], conv_dtype_t dtype);
+
 size_t conv_transposed_workspace_size(int r, int s, int c_in, int c_out, const int stride[2],
                                       const int padding[2], conv_dtype_t dtype);
+
+size_t conv_transposed_workspace_size_dilated(int r, int s, int c_in, int c_out,
+                                              const int stride[2], const int dilation[2],
+                                              const int padding[2], conv_dtype_t dtype);
 
 conv_status_t conv_transposed_pack_filter(const void* filter_rsfc, int r, int s, int c_in,
                                           int c_out, const int stride[2], const int padding[2],
                                           conv_dtype_t dtype, void* packed, size_t packed_bytes,
                                           void* stream);
+
+conv_status_t conv_transposed_pack_filter_dilated(const void* filter_rsfc, int r, int s, int c_in,
+                                                  int c_out, const int stride[2],
+                                                  const int dilation[2], const int padding[2],
+                                                  conv_dtype_t dtype, void* packed,
+                                                  size_t packed_bytes, void* stream);
 
 conv_status_t conv_transposed(const void* input, int n, int h, int w, int c_in,
                               conv_dtype_t in_dtype, const void* filter_rsfc, int r, int s,

@@ -23,9 +23,18 @@ def decode(t: torch.Tensor, dtype: str) -> np.ndarray:
     return oracle.decode(synthetic.raw_bits(t), dtype)
 
 
+def _max_taps(extent, stride, dilation, pad):
+    """Most filter taps r in [0, extent) that reach one output index of a
+    transposed conv: o = i*stride - pad + r*dilation for some input i, i.e.
+    r*dilation = o + pad (mod stride), maximised over the output phase o."""
+    return max(sum(1 for r in range(extent) if (r * dilation - a - pad) % stride == 0)
+               for a in range(stride))
+
+
 def contraction_length(case) -> int:
     if case.kind == "transposed":
-        return math.ceil(case.R / case.stride) * math.ceil(case.S / case.stride) * case.C_in
+        (sh, sw), (dh, dw), (ph, pw) = case.strides, case.dilations, case.pads
+        return max(1, _max_taps(case.R, sh, dh, ph) * _max_taps(case.S, sw, dw, pw)) * case.C_in
     return case.R * case.S * case.C_in // case.groups
 
 
@@ -33,7 +42,7 @@ def oracle_full(case, inp):
     x = decode(inp["x"], case.dtype)
     w = decode(inp["w"], case.dtype)
     src = decode(inp["src"], case.out_dtype) if inp["src"] is not None else None
-    st, pd, dl = (case.stride,) * 2, case.pads, case.dilations
+    st, pd, dl = case.strides, case.pads, case.dilations
     if case.kind == "transposed":
         return oracle.conv_transposed(x, w, out_hw=(case.Ho, case.Wo), stride=st, padding=pd,
                                       dilation=dl, source=src, beta=case.beta, act=case.epilogue)
@@ -46,7 +55,7 @@ def oracle_points(case, inp, pts):
     x = decode(inp["x"], case.dtype)
     w = decode(inp["w"], case.dtype)
     src = decode(inp["src"], case.out_dtype) if inp["src"] is not None else None
-    st, pd, dl = (case.stride,) * 2, case.pads, case.dilations
+    st, pd, dl = case.strides, case.pads, case.dilations
     if case.kind == "transposed":
         return oracle.conv_transposed_points(x, w, pts, out_hw=(case.Ho, case.Wo), stride=st,
                                              padding=pd, dilation=dl, source=src, beta=case.beta,
@@ -82,12 +91,12 @@ def run_gpu(case, inp, *, packed=True, device="cuda:0", out=None, workspace=None
     src = inp["src"].to(device) if inp["src"] is not None else None
     if out is None:
         out = torch.empty(case.out_shape, dtype=synthetic.TORCH_DTYPES[case.out_dtype], device=device)
-    st, pd, dl = (case.stride,) * 2, case.pads, case.dilations
+    st, pd, dl = case.strides, case.pads, case.dilations
     kw = dict(has_residual=case.has_residual, source=src, beta=case.beta, epilogue=case.epilogue,
               workspace=workspace)
     if case.kind == "transposed":
         if packed:
-            pk = cg.conv_transposed_pack_filter(w, stride=st, padding=pd)
+            pk = cg.conv_transposed_pack_filter(w, stride=st, padding=pd, dilation=dl)
             cg.conv_transposed_packed(x, pk, out, r=case.R, s=case.S, stride=st, dilation=dl,
                                       padding=pd, **kw)
         else:

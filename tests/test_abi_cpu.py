@@ -119,9 +119,9 @@ def tr(lib, *, n=2, h=8, w=8, c=64, dt=F16, r=4, s=4, f=32, ho=None, wo=None, st
        dil=(1, 1), pad=(1, 1), res=0, src=None, epi=0, ws_bytes=1 << 22, odt=None):
     odt = (BF16 if dt == F8 else dt) if odt is None else odt
     if ho is None:
-        ho = (h - 1) * stride[0] - 2 * pad[0] + r
+        ho = (h - 1) * stride[0] - 2 * pad[0] + dil[0] * (r - 1) + 1
     if wo is None:
-        wo = (w - 1) * stride[1] - 2 * pad[1] + s
+        wo = (w - 1) * stride[1] - 2 * pad[1] + dil[1] * (s - 1) + 1
     src = ctypes.c_void_p(0) if src is None else src
     return lib.conv_transposed(A, n, h, w, c, dt, B, r, s, f, C, ho, wo, odt, _lib.pair(stride),
                                _lib.pair(dil), _lib.pair(pad), res, src, 0.0, epi, WS, ws_bytes,
@@ -131,10 +131,16 @@ def tr(lib, *, n=2, h=8, w=8, c=64, dt=F16, r=4, s=4, f=32, ho=None, wo=None, st
 @pytest.mark.parametrize("kw,want", [
     (dict(ho=13), INVALID),                   # below (h-1)s - 2p + r
     (dict(ho=18), INVALID),                   # output padding must be < stride
-    (dict(dil=(2, 2)), NOTSUP),
-    (dict(pad=(4, 4)), NOTSUP),               # pad >= r
-    (dict(stride=(2, 1)), NOTSUP),
-    (dict(stride=(3, 3)), NOTSUP),
+    # Accepted shapes stop at the (deliberately too small) workspace, past every shape gate.
+    (dict(dil=(2, 2), ws_bytes=512), WS_SMALL),
+    (dict(stride=(2, 1), ws_bytes=512), WS_SMALL),   # per-axis strides
+    (dict(stride=(3, 3), ws_bytes=512), WS_SMALL),   # 9 phases: three launches
+    (dict(stride=(4, 4), pad=(0, 0), ws_bytes=512), WS_SMALL),
+    (dict(dil=(33, 1)), NOTSUP),
+    (dict(pad=(4, 4)), NOTSUP),               # pad > dil*(r-1)
+    (dict(dil=(2, 2), pad=(7, 7)), NOTSUP),
+    (dict(stride=(5, 4)), NOTSUP),            # 20 phases
+    (dict(stride=(0, 2)), NOTSUP),
     (dict(c=8), NOTSUP),
     (dict(dt=F8, odt=F16), NOTSUP),
     (dict(res=1), INVALID),
@@ -144,6 +150,22 @@ def test_transposed_validation(lib, kw, want):
     assert tr(lib, **kw) == want
 
 
+def test_transposed_packed_sizes_with_dilation_and_stride(lib):
+    """Packed layout [stride_h*stride_w phases][c_out][K_max]: with stride 2 and
+    dilation 2 one output phase per axis gets every tap and the other none
+    (K_max = 4*4*64); stride 4 with a 4x4 filter gives 16 phases of one tap."""
+    nb = lambda r, s, c, f, st, dl, pd, dt: lib.conv_transposed_packed_filter_bytes_dilated(
+        r, s, c, f, _lib.pair(st), _lib.pair(dl), _lib.pair(pd), dt)
+    assert nb(4, 4, 64, 32, (2, 2), (2, 2), (1, 1), F16) == 4 * 32 * (16 * 64) * 2
+    assert nb(4, 4, 64, 32, (4, 4), (1, 1), (0, 0), F16) == 16 * 32 * 64 * 2
+    assert nb(3, 3, 64, 16, (3, 3), (2, 2), (2, 2), F8) == 9 * 16 * 64 * 1   # gcd(2, 3) = 1: one tap each
+    assert nb(4, 4, 64, 32, (2, 2), (1, 1), (1, 1), F16) == \
+        lib.conv_transposed_packed_filter_bytes(4, 4, 64, 32, _lib.pair((2, 2)), _lib.pair((1, 1)), F16)
+    assert nb(4, 4, 64, 32, (5, 4), (1, 1), (1, 1), F16) == 0                 # 20 phases
+    assert lib.conv_transposed_workspace_size_dilated(
+        4, 4, 64, 32, _lib.pair((2, 2)), _lib.pair((2, 2)), _lib.pair((1, 1)), F16) == 256 + 4 * 32 * 1024 * 2
+
+
 def test_pack_validation(lib):
     assert lib.conv2d_pack_filter(B, 3, 3, 64, 64, 0, BF16, D, 100, None) == WS_SMALL
     assert lib.conv2d_pack_filter(None, 3, 3, 64, 64, 0, BF16, D, 1 << 20, None) == INVALID
@@ -151,8 +173,14 @@ def test_pack_validation(lib):
                                   None) == MISALIGNED
     assert lib.conv_transposed_pack_filter(B, 4, 4, 64, 32, _lib.pair((2, 2)), _lib.pair((1, 1)),
                                            F16, D, 64, None) == WS_SMALL
-    assert lib.conv_transposed_pack_filter(B, 4, 4, 64, 32, _lib.pair((3, 3)), _lib.pair((1, 1)),
-                                           F16, D, 1 << 20, None) == NOTSUP
+    assert lib.conv_transposed_pack_filter(B, 4, 4, 64, 32, _lib.pair((5, 4)), _lib.pair((1, 1)),
+                                           F16, D, 1 << 20, None) == NOTSUP   # 20 phases
+    assert lib.conv_transposed_pack_filter_dilated(
+        B, 4, 4, 64, 32, _lib.pair((2, 2)), _lib.pair((2, 2)), _lib.pair((7, 1)), F16, D, 1 << 20,
+        None) == NOTSUP                                                        # pad > dil*(r-1)
+    assert lib.conv_transposed_pack_filter_dilated(
+        B, 4, 4, 64, 32, _lib.pair((3, 3)), _lib.pair((2, 2)), _lib.pair((1, 1)), F16, D, 64,
+        None) == WS_SMALL                                                      # accepted shape
 
 
 def _plan(lib, n, h, w, c, dt, r, f, st, pd, res=0, sms=148, ws=256):

@@ -31,13 +31,14 @@ def _fwd(name, dt, N, Hh, W, C, F, R, st, pd, *, layout="RSCF", res=False, beta=
 
 
 def _tr(name, dt, N, Hh, W, C, F, R, st, pd, extra=0, *, res=False, beta=0.0, epi="none", seed=1,
-        xd=None, wd=None):
-    Ho = (Hh - 1) * st - 2 * pd + R + extra
-    Wo = (W - 1) * st - 2 * pd + R + extra
+        xd=None, wd=None, dil=1, st_w=None, extra_w=None):
+    sw = st if st_w is None else st_w
+    Ho = (Hh - 1) * st - 2 * pd + dil * (R - 1) + 1 + extra
+    Wo = (W - 1) * sw - 2 * pd + dil * (R - 1) + 1 + (extra if extra_w is None else extra_w)
     return ConvCase(name, "transposed", dt, N, Hh, W, C, F, R, R, st, pd, "RSFC",
                     xd or Dist("normal", 1.0), wd or Dist("normal", 1.0 / (R * R * C)), seed=seed,
                     has_residual=res, beta=beta, src_dist=Dist("normal", 1.0) if res else None,
-                    epilogue=epi, out_hw=(Ho, Wo))
+                    epilogue=epi, out_hw=(Ho, Wo), dilation=dil, stride_w=st_w)
 
 
 # Several M tiles with a ragged tail (N*Ho*Wo not a multiple of 128), edge
@@ -166,6 +167,17 @@ SMALL_TR = [
     _tr("t_h_cout3", "f16", 1, 10, 10, 64, 3, 4, 2, 1),
     _tr("t_h_cout256_silu", "f16", 1, 6, 6, 64, 256, 4, 2, 1, epi="silu"),
     _tr("t_h_cin80_partial_block", "f16", 1, 7, 7, 80, 32, 4, 2, 1),
+    # Dilation and general strides: with dilation 2 at stride 2 half the
+    # output phases have no taps; strides 3 and 4 have 9 and 16 phases (three
+    # and four launches of four phases); stride 3 with dilation 2 (gcd 1);
+    # per-axis strides; C_out 17 on the direct epilogue; fp8 with a residual.
+    _tr("t_h_4x4_s2p1_d2", "f16", 2, 7, 6, 64, 32, 4, 2, 1, dil=2, epi="relu"),
+    _tr("t_b_3x3_s3p1", "bf16", 2, 6, 5, 64, 48, 3, 3, 1, extra=2),
+    _tr("t_b_4x4_s4p0", "bf16", 1, 5, 6, 32, 64, 4, 4, 0, extra=1),
+    _tr("t_h_3x3_s3p2_d2", "f16", 1, 6, 6, 64, 32, 3, 3, 2, dil=2, extra=1),
+    _tr("t_b_3x3_s12", "bf16", 2, 7, 6, 64, 32, 3, 1, 1, st_w=2, extra=0, extra_w=1),
+    _tr("t_h_cout17_s3", "f16", 1, 5, 7, 64, 17, 3, 3, 0, extra=1),
+    _tr("t_e_5x5_s2p3_d2_res", "f8e4m3", 1, 6, 6, 64, 64, 5, 2, 3, dil=2, res=True, beta=0.5),
 ]
 
 
@@ -221,6 +233,7 @@ INT_CASES = [
     _int_case("int_e_3x3", "fwd", "f8e4m3", 2, 10, 10, 32, 64, 3, 1, 1),
     _int_case("int_h_tr", "transposed", "f16", 2, 8, 8, 64, 32, 4, 2, 1),
     _int_case("int_e_tr", "transposed", "f8e4m3", 1, 7, 7, 32, 16, 3, 2, 1, extra=1),
+    _int_case("int_b_tr_s3_d2", "transposed", "bf16", 1, 5, 6, 32, 16, 3, 3, 2, extra=1, dil=2),
     _int_case("int_b_gather_c3", "fwd", "bf16", 2, 11, 13, 3, 16, 7, 2, 3),
     _int_case("int_b_stage_c3", "fwd", "bf16", 2, 16, 16, 3, 16, 7, 2, 3),
     _int_case("int_e_gather_c5", "fwd", "f8e4m3", 1, 9, 9, 5, 32, 3, 1, 1),

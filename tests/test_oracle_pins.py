@@ -150,6 +150,13 @@ TR_CASES = [
     (1, 3, 3, 4, 3, 5, 5, (2, 2), (2, 2), (1, 1), (1, 0)),
     (2, 4, 3, 1, 2, 2, 3, (2, 1), (0, 1), (1, 1), (0, 0)),
     (1, 4, 4, 2, 2, 3, 3, (1, 1), (0, 0), (2, 2), (0, 0)),
+    # stride 2 with dilation 2 (taps reach only every other output phase)
+    (2, 4, 5, 2, 3, 4, 4, (2, 2), (1, 1), (2, 2), (0, 1)),
+    # strides 3 and 4, dilation 2 with stride 3, per-axis stride and dilation
+    (1, 3, 4, 2, 2, 3, 3, (3, 3), (1, 1), (1, 1), (2, 0)),
+    (1, 3, 3, 3, 2, 4, 4, (4, 4), (0, 0), (1, 1), (0, 3)),
+    (2, 3, 3, 2, 2, 3, 3, (3, 3), (2, 2), (2, 2), (1, 1)),
+    (1, 4, 3, 2, 3, 3, 2, (1, 2), (1, 0), (3, 1), (0, 1)),
 ]
 
 

@@ -171,32 +171,40 @@ def conv2d_fwd_packed(input, packed_filter, output, *, r, s, stride=(1, 1), dila
     return output
 
 
-def conv_transposed_packed_filter_bytes(r, s, c_in, c_out, stride, padding, dtype: str) -> int:
-    return _lib.lib().conv_transposed_packed_filter_bytes(r, s, c_in, c_out, _lib.pair(stride),
-                                                          _lib.pair(padding), _lib.DTYPE_CODES[dtype])
+def conv_transposed_packed_filter_bytes(r, s, c_in, c_out, stride, padding, dtype: str,
+                                        dilation=(1, 1)) -> int:
+    return _lib.lib().conv_transposed_packed_filter_bytes_dilated(
+        r, s, c_in, c_out, _lib.pair(stride), _lib.pair(dilation), _lib.pair(padding),
+        _lib.DTYPE_CODES[dtype])
 
 
-def conv_transposed_workspace_size(r, s, c_in, c_out, stride, padding, dtype: str) -> int:
-    return _lib.lib().conv_transposed_workspace_size(r, s, c_in, c_out, _lib.pair(stride),
-                                                     _lib.pair(padding), _lib.DTYPE_CODES[dtype])
+def conv_transposed_workspace_size(r, s, c_in, c_out, stride, padding, dtype: str,
+                                   dilation=(1, 1)) -> int:
+    return _lib.lib().conv_transposed_workspace_size_dilated(
+        r, s, c_in, c_out, _lib.pair(stride), _lib.pair(dilation), _lib.pair(padding),
+        _lib.DTYPE_CODES[dtype])
 
 
-def conv_transposed_pack_filter(filter_rsfc, *, stride, padding, out=None, stream=None):
-    """Pack an RSFC filter into per-phase K-major matrices (returns `out`, uint8 bytes)."""
+def conv_transposed_pack_filter(filter_rsfc, *, stride, padding, dilation=(1, 1), out=None,
+                                stream=None):
+    """Pack an RSFC filter into per-phase K-major matrices (returns `out`).
+
+    The packing depends on stride, dilation and padding: conv_transposed_packed
+    must be called with the same three."""
     import torch
     _need_dense(filter_rsfc)
     r, s, c_out, c_in = filter_rsfc.shape
     dt = dtype_name(filter_rsfc)
-    nbytes = conv_transposed_packed_filter_bytes(r, s, c_in, c_out, stride, padding, dt)
+    nbytes = conv_transposed_packed_filter_bytes(r, s, c_in, c_out, stride, padding, dt, dilation)
     if nbytes == 0:
         raise ConvError(CONV_ERR_NOT_SUPPORTED, "conv_transposed_pack_filter")
     if out is None:
         out = torch.empty(nbytes // filter_rsfc.element_size(), dtype=filter_rsfc.dtype,
                           device=filter_rsfc.device)
-    _check(_lib.lib().conv_transposed_pack_filter(
-        _ptr(filter_rsfc), r, s, c_in, c_out, _lib.pair(stride), _lib.pair(padding), _code(filter_rsfc),
-        _ptr(out), out.numel() * out.element_size(), _stream(stream, filter_rsfc.device)),
-        "conv_transposed_pack_filter")
+    _check(_lib.lib().conv_transposed_pack_filter_dilated(
+        _ptr(filter_rsfc), r, s, c_in, c_out, _lib.pair(stride), _lib.pair(dilation),
+        _lib.pair(padding), _code(filter_rsfc), _ptr(out), out.numel() * out.element_size(),
+        _stream(stream, filter_rsfc.device)), "conv_transposed_pack_filter")
     return out
 
 
@@ -212,7 +220,8 @@ def conv_transposed(input, filter_rsfc, output, *, stride=(1, 1), dilation=(1, 1
         raise ConvError(CONV_ERR_INVALID_VALUE, "filter shape does not match input/output")
     if workspace is None:
         workspace = new_workspace(conv_transposed_workspace_size(r, s, c_in, c_out, stride, padding,
-                                                                 dtype_name(input)), input.device)
+                                                                 dtype_name(input), dilation),
+                                  input.device)
     _check(_lib.lib().conv_transposed(
         _ptr(input), n, h, w, c_in, _code(input), _ptr(filter_rsfc), r, s, c_out, _ptr(output), ho, wo,
         _code(output), st, dl, pd, int(bool(has_residual)), _ptr(source), float(beta),

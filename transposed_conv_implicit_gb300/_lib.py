@@ -39,6 +39,8 @@ EXPORTS = (
     "conv_check_device_status", "conv_testing_set_wait_fault", "conv_testing_im2col_tile",
     "conv_testing_fwd_plan", "conv2d_fwd_noalloc", "conv_testing_reload_tuning",
     "conv_testing_cache_stats", "conv_streamk_workspace_size",
+    "conv_transposed_packed_filter_bytes_dilated", "conv_transposed_workspace_size_dilated",
+    "conv_transposed_pack_filter_dilated",
 )
 
 
@@ -70,6 +72,12 @@ def _declare(lib):
     lib.conv_transposed_workspace_size.restype = Z
     lib.conv_transposed_pack_filter.argtypes = [P, I, I, I, I, IP, IP, I, P, Z, P]
     lib.conv_transposed_pack_filter.restype = I
+    lib.conv_transposed_packed_filter_bytes_dilated.argtypes = [I, I, I, I, IP, IP, IP, I]
+    lib.conv_transposed_packed_filter_bytes_dilated.restype = Z
+    lib.conv_transposed_workspace_size_dilated.argtypes = [I, I, I, I, IP, IP, IP, I]
+    lib.conv_transposed_workspace_size_dilated.restype = Z
+    lib.conv_transposed_pack_filter_dilated.argtypes = [P, I, I, I, I, IP, IP, IP, I, P, Z, P]
+    lib.conv_transposed_pack_filter_dilated.restype = I
     tr_tail = [IP, IP, IP, I, P, F, I, P, Z, P]
     lib.conv_transposed.argtypes = [P, I, I, I, I, I, P, I, I, I, P, I, I, I] + tr_tail
     lib.conv_transposed.restype = I

@@ -16,6 +16,7 @@
 #include <cstdint>
 #include <cstdlib>
 #include <cstring>
+#include <memory>
 #include <mutex>
 #include <new>
 
@@ -179,9 +180,6 @@ struct Plan {
   size_t packed_bytes;
   int grid;
   size_t smem_bytes;
-  // packing description of the transposed filter, per phase slot
-  int r0h[kMaxPhases], r0w[kMaxPhases], th[kMaxPhases], tw[kMaxPhases];
-  int sh, sw;
   size_t sk_offset;    // stream-K flags and partial slots: this far into the workspace
 };
 
@@ -762,22 +760,88 @@ conv_status_t encode_fwd_input(const FwdShape& f, const void* input, Plan* pl) {
                           f.pad_h - (f.r - 1) * f.dil_h, f.stride_w, f.stride_h);
 }
 
-// Stride-phase decomposition of the transposed conv along one axis.
-// Output index o = st*j + a receives input i = j + L + u through filter tap
-// r(u) = r0 + st*(T-1-u), u in [0, T), where r0 = (a + pad) mod st,
-// T = #{r in [0,R) : r = r0 mod st}, q = (a + pad - r0)/st, L = q - T + 1.
+// Stride-phase decomposition of the transposed conv along one axis, with
+// stride st and dilation dil ("conv_transposed_gpu", Args: stride, dilation).
+// Input i, tap r lands on output o = st*i - pad + r*dil.  Output index
+// o = st*j + a (phase a) therefore receives tap r only when
+// r*dil = a + pad (mod st): with g = gcd(dil, st) these taps are
+// r0, r0 + st/g, r0 + 2*st/g, ... (none when g does not divide a + pad), and
+// tap r reads input i = j + (a + pad - r*dil)/st.  Listing the T taps in
+// reverse, u = T-1-k for r = r0 + k*st/g, the input row is j + L + u*dil/g
+// with L = (a + pad - r_last*dil)/st: each phase is a stride-1 correlation
+// with T taps at dilation dil/g, over the input shifted by L.
 struct AxisPhase {
   int r0, taps, lower, grid;
+  int rstep;  // st / g: filter index between consecutive taps of a phase
+  int dil;    // dil / g: input index between consecutive taps
 };
 
-AxisPhase axis_phase(int a, int st, int pad, int R, int out_extent) {
-  AxisPhase ph;
-  ph.r0 = (a + pad) % st;
-  ph.taps = R > ph.r0 ? (R - ph.r0 + st - 1) / st : 0;
-  const int q = (a + pad - ph.r0) / st;
-  ph.lower = q - ph.taps + 1;
+int gcd_int(int a, int b) {
+  while (b) {
+    const int t = a % b;
+    a = b;
+    b = t;
+  }
+  return a;
+}
+
+AxisPhase axis_phase(int a, int st, int pad, int R, int out_extent, int dil) {
+  AxisPhase ph{};
+  const int g = gcd_int(dil, st);
+  ph.rstep = st / g;
+  ph.dil = dil / g;
+  ph.r0 = -1;
+  for (int r = 0; r < std::min(R, ph.rstep) && ph.r0 < 0; ++r)
+    if (((r * dil - a - pad) % st + st) % st == 0) ph.r0 = r;
+  ph.taps = ph.r0 < 0 ? 0 : (R - ph.r0 + ph.rstep - 1) / ph.rstep;
+  if (ph.taps > 0) {
+    const int r_last = ph.r0 + (ph.taps - 1) * ph.rstep;
+    ph.lower = (a + pad - r_last * dil) / st;  // exact: a + pad - r*dil is a multiple of st
+  } else {
+    ph.r0 = 0;
+    ph.lower = 0;
+  }
   ph.grid = out_extent > a ? (out_extent - a + st - 1) / st : 0;
   return ph;
+}
+
+// The packed transposed filter: one [C_out][kmax] K-major matrix per phase
+// slot (slot = a * stride_w + b), phase (a, b) holding its taps in the order
+// the kernel walks them.  Depends on filter extent, stride, dilation and
+// padding only.
+constexpr int kMaxTrSlots = 16;  // stride_h * stride_w phases at most
+constexpr int kMaxTrLaunches = kMaxTrSlots / kMaxPhases;
+
+struct TrPacking {
+  int slots, kmax, sh, sw, rsh, rsw;
+  int r0h[kMaxTrSlots], r0w[kMaxTrSlots], th[kMaxTrSlots], tw[kMaxTrSlots];
+};
+
+bool tr_packing(int r, int s, int c_in, const int stride[2], const int dilation[2],
+                const int padding[2], TrPacking* pk) {
+  std::memset(pk, 0, sizeof(*pk));
+  if (stride[0] < 1 || stride[1] < 1 || stride[0] * stride[1] > kMaxTrSlots) return false;
+  if (dilation[0] < 1 || dilation[1] < 1 || padding[0] < 0 || padding[1] < 0) return false;
+  pk->slots = stride[0] * stride[1];
+  pk->sh = stride[0];
+  pk->sw = stride[1];
+  int kmax = 0;
+  for (int a = 0; a < stride[0]; ++a) {
+    const AxisPhase ya = axis_phase(a, stride[0], padding[0], r, stride[0], dilation[0]);
+    pk->rsh = ya.rstep;
+    for (int b = 0; b < stride[1]; ++b) {
+      const AxisPhase xb = axis_phase(b, stride[1], padding[1], s, stride[1], dilation[1]);
+      pk->rsw = xb.rstep;
+      const int slot = a * stride[1] + b;
+      pk->r0h[slot] = ya.r0;
+      pk->r0w[slot] = xb.r0;
+      pk->th[slot] = ya.taps;
+      pk->tw[slot] = xb.taps;
+      kmax = std::max(kmax, ya.taps * xb.taps * c_in);
+    }
+  }
+  pk->kmax = kmax ? kmax : c_in;  // keep the filter map well-formed
+  return true;
 }
 
 struct TrShape {
@@ -786,19 +850,26 @@ struct TrShape {
   conv_dtype_t in_dtype, out_dtype;
 };
 
+// Gates of the transposed conv: strides up to kMaxTrSlots phases in all,
+// dilation 1..32, 0 <= pad <= dil*(R-1), and the output size
+// (h-1)*stride - 2*pad + dil*(R-1) + 1 plus an output padding in [0, stride).
 conv_status_t check_tr_shape(const TrShape& t) {
   if (t.n <= 0 || t.h <= 0 || t.w <= 0 || t.c_in <= 0 || t.r <= 0 || t.s <= 0 || t.c_out <= 0 ||
       t.ho <= 0 || t.wo <= 0)
     return CONV_ERR_INVALID_VALUE;
   if (!known_dtype(t.in_dtype) || !known_dtype(t.out_dtype)) return CONV_ERR_NOT_SUPPORTED;
   if (!dtype_pair_ok(t.in_dtype, t.out_dtype)) return CONV_ERR_NOT_SUPPORTED;
-  if (!((t.stride_h == 1 && t.stride_w == 1) || (t.stride_h == 2 && t.stride_w == 2)))
+  if (t.stride_h < 1 || t.stride_w < 1 || t.stride_h * t.stride_w > kMaxTrSlots)
     return CONV_ERR_NOT_SUPPORTED;
-  if (t.dil_h != 1 || t.dil_w != 1) return CONV_ERR_NOT_SUPPORTED;
+  if (t.dil_h < 1 || t.dil_w < 1 || t.dil_h > kMaxFilterExtent || t.dil_w > kMaxFilterExtent)
+    return CONV_ERR_NOT_SUPPORTED;
   if (t.r > kMaxFilterExtent || t.s > kMaxFilterExtent) return CONV_ERR_NOT_SUPPORTED;
-  if (t.pad_h < 0 || t.pad_w < 0 || t.pad_h >= t.r || t.pad_w >= t.s) return CONV_ERR_NOT_SUPPORTED;
-  const long long base_h = static_cast<long long>(t.h - 1) * t.stride_h - 2 * t.pad_h + (t.r - 1) + 1;
-  const long long base_w = static_cast<long long>(t.w - 1) * t.stride_w - 2 * t.pad_w + (t.s - 1) + 1;
+  if (t.pad_h < 0 || t.pad_w < 0 || t.pad_h > t.dil_h * (t.r - 1) || t.pad_w > t.dil_w * (t.s - 1))
+    return CONV_ERR_NOT_SUPPORTED;
+  const long long base_h =
+      static_cast<long long>(t.h - 1) * t.stride_h - 2 * t.pad_h + t.dil_h * (t.r - 1) + 1;
+  const long long base_w =
+      static_cast<long long>(t.w - 1) * t.stride_w - 2 * t.pad_w + t.dil_w * (t.s - 1) + 1;
   if (t.ho - base_h < 0 || t.ho - base_h >= t.stride_h) return CONV_ERR_INVALID_VALUE;
   if (t.wo - base_w < 0 || t.wo - base_w >= t.stride_w) return CONV_ERR_INVALID_VALUE;
   const long long rows = static_cast<long long>(t.n) * t.ho * t.wo;
@@ -806,72 +877,79 @@ conv_status_t check_tr_shape(const TrShape& t) {
   return CONV_OK;
 }
 
-conv_status_t plan_transposed(const TrShape& t, Plan* pl, int num_sms, size_t sk_room = 0) {
+// The phase slots of a transposed conv that have output pixels, in slot order.
+int tr_active_slots(const TrShape& t, int out[kMaxTrSlots]) {
+  int n = 0;
+  for (int a = 0; a < t.stride_h; ++a) {
+    const AxisPhase ya = axis_phase(a, t.stride_h, t.pad_h, t.r, t.ho, t.dil_h);
+    for (int b = 0; b < t.stride_w; ++b) {
+      const AxisPhase xb = axis_phase(b, t.stride_w, t.pad_w, t.s, t.wo, t.dil_w);
+      if (ya.grid > 0 && xb.grid > 0) out[n++] = a * t.stride_w + b;
+    }
+  }
+  return n;
+}
+
+// Plans one launch over the phase slots slots[0 .. nslots) (at most
+// kMaxPhases): each is a dense stride-1 implicit GEMM over the input.
+conv_status_t plan_transposed(const TrShape& t, const TrPacking& pk, const int* slots, int nslots,
+                              Plan* pl, int num_sms, size_t sk_room = 0) {
   std::memset(pl, 0, sizeof(*pl));
+  if (nslots < 1 || nslots > kMaxPhases) return CONV_ERR_INVALID_VALUE;
   conv_status_t st = plan_channels(pl, t.in_dtype, t.c_in);
   if (st != CONV_OK) return st;
   ConvKernelParams& kp = pl->kp;
-  pl->sh = t.stride_h;
-  pl->sw = t.stride_w;
-  pl->phases_packed = t.stride_h * t.stride_w;
-  int kmax = 0;
-  int active = 0;
-  for (int a = 0; a < t.stride_h; ++a) {
-    const AxisPhase ya = axis_phase(a, t.stride_h, t.pad_h, t.r, t.ho);
-    for (int b = 0; b < t.stride_w; ++b) {
-      const AxisPhase xb = axis_phase(b, t.stride_w, t.pad_w, t.s, t.wo);
-      const int slot = a * t.stride_w + b;
-      pl->r0h[slot] = ya.r0;
-      pl->r0w[slot] = xb.r0;
-      pl->th[slot] = ya.taps;
-      pl->tw[slot] = xb.taps;
-      kmax = std::max(kmax, ya.taps * xb.taps * t.c_in);
-      if (ya.grid == 0 || xb.grid == 0) continue;
-      kp.grid_h[active] = ya.grid;
-      kp.grid_w[active] = xb.grid;
-      kp.rows[active] = t.n * ya.grid * xb.grid;
-      // A phase without taps still runs (kblocks = 0): it writes act(0 + beta*source).
-      kp.taps_h[active] = ya.taps;
-      kp.taps_w[active] = xb.taps;
-      kp.base_h[active] = ya.lower;
-      kp.base_w[active] = xb.lower;
-      kp.out_off_h[active] = a;
-      kp.out_off_w[active] = b;
-      kp.b_index[active] = slot;
-      ++active;
-    }
+  pl->phases_packed = pk.slots;
+  int dil_h = 1, dil_w = 1;
+  for (int ph = 0; ph < nslots; ++ph) {
+    const int slot = slots[ph];
+    const int a = slot / t.stride_w, b = slot - (slot / t.stride_w) * t.stride_w;
+    const AxisPhase ya = axis_phase(a, t.stride_h, t.pad_h, t.r, t.ho, t.dil_h);
+    const AxisPhase xb = axis_phase(b, t.stride_w, t.pad_w, t.s, t.wo, t.dil_w);
+    dil_h = ya.dil;
+    dil_w = xb.dil;
+    kp.grid_h[ph] = ya.grid;
+    kp.grid_w[ph] = xb.grid;
+    kp.rows[ph] = t.n * ya.grid * xb.grid;
+    // A phase without taps still runs (kblocks = 0): it writes act(0 + beta*source).
+    kp.taps_h[ph] = ya.taps;
+    kp.taps_w[ph] = xb.taps;
+    kp.base_h[ph] = ya.lower;
+    kp.base_w[ph] = xb.lower;
+    kp.out_off_h[ph] = a;
+    kp.out_off_w[ph] = b;
+    kp.b_index[ph] = slot;
   }
   long long rows[kMaxPhases];
   int max_kb = 0;
-  for (int ph = 0; ph < active; ++ph) {
+  for (int ph = 0; ph < nslots; ++ph) {
     rows[ph] = kp.rows[ph];
     max_kb = std::max(max_kb, kp.taps_h[ph] * kp.taps_w[ph] * kp.c_blocks);
   }
-  kp.num_phases = active;
-  choose_tiling(pl, rows, active, max_kb, t.c_out, num_sms);
+  kp.num_phases = nslots;
+  choose_tiling(pl, rows, nslots, max_kb, t.c_out, num_sms);
   const int tile_m = kBM * kp.m_halves;
   int tile = 0;
-  for (int ph = 0; ph < active; ++ph) {
+  for (int ph = 0; ph < nslots; ++ph) {
     kp.tile_start[ph] = tile;
     tile += ((kp.rows[ph] + tile_m - 1) / tile_m) * kp.n_tiles;
   }
-  if (kmax == 0) kmax = t.c_in;  // keep the filter map well-formed
-  kp.tile_start[active] = tile;
+  kp.tile_start[nslots] = tile;
   kp.total_tiles = tile;
   kp.step_h = 1;
   kp.step_w = 1;
   kp.out_step_h = t.stride_h;
   kp.out_step_w = t.stride_w;
-  kp.dil_h = 1;
-  kp.dil_w = 1;
+  kp.dil_h = dil_h;  // the same for every phase of an axis
+  kp.dil_w = dil_w;
   kp.Ho = t.ho;
   kp.Wo = t.wo;
   kp.Cout = t.c_out;
   kp.vec_ok = (t.c_out * 2) % 16 == 0;
   plan_pair(pl, num_sms);
   plan_streamk(pl, num_sms, sk_room);
-  pl->kmax = kmax;
-  pl->packed_bytes = static_cast<size_t>(pl->phases_packed) * t.c_out * kmax * elt_bytes(t.in_dtype);
+  pl->kmax = pk.kmax;
+  pl->packed_bytes = static_cast<size_t>(pk.slots) * t.c_out * pk.kmax * elt_bytes(t.in_dtype);
   return CONV_OK;
 }
 
@@ -932,14 +1010,9 @@ __global__ void pack_fwd_gather_kernel(const T* __restrict__ w, T* __restrict__ 
   }
 }
 
-struct TrPackDesc {
-  int slots, kmax, sh, sw;
-  int r0h[kMaxPhases], r0w[kMaxPhases], th[kMaxPhases], tw[kMaxPhases];
-};
-
 template <typename T>
 __global__ void pack_transposed_kernel(const T* __restrict__ w, T* __restrict__ out, int R, int S,
-                                       int C, int F, TrPackDesc d) {
+                                       int C, int F, TrPacking d) {
   const long long per_slot = static_cast<long long>(F) * d.kmax;
   const long long total = per_slot * d.slots;
   for (long long idx = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; idx < total;
@@ -953,10 +1026,11 @@ __global__ void pack_transposed_kernel(const T* __restrict__ w, T* __restrict__ 
     const int th = d.th[slot], tw = d.tw[slot];
     T v = T(0);
     if (tap < static_cast<long long>(th) * tw) {
+      // Tap (uh, uw) of the phase: filter index r0 + rstep*(T-1-u) per axis.
       const int uh = static_cast<int>(tap / tw);
       const int uw = static_cast<int>(tap - static_cast<long long>(uh) * tw);
-      const long long r = d.r0h[slot] + static_cast<long long>(d.sh) * (th - 1 - uh);
-      const long long s = d.r0w[slot] + static_cast<long long>(d.sw) * (tw - 1 - uw);
+      const long long r = d.r0h[slot] + static_cast<long long>(d.rsh) * (th - 1 - uh);
+      const long long s = d.r0w[slot] + static_cast<long long>(d.rsw) * (tw - 1 - uw);
       v = w[((r * S + s) * F + f) * C + c];  // RSFC [R][S][F][C]
     }
     out[idx] = v;
@@ -996,19 +1070,8 @@ conv_status_t launch_pack_fwd(const void* filter, int r, int s, int c_in, int c_
   return cudaGetLastError() == cudaSuccess ? CONV_OK : CONV_ERR_CUDA;
 }
 
-conv_status_t launch_pack_tr(const Plan& pl, const void* filter, int r, int s, int c_in,
+conv_status_t launch_pack_tr(const TrPacking& d, const void* filter, int r, int s, int c_in,
                              int c_out, conv_dtype_t dt, void* packed, cudaStream_t stream) {
-  TrPackDesc d{};
-  d.slots = pl.phases_packed;
-  d.kmax = pl.kmax;
-  d.sh = pl.sh;
-  d.sw = pl.sw;
-  for (int i = 0; i < kMaxPhases; ++i) {
-    d.r0h[i] = pl.r0h[i];
-    d.r0w[i] = pl.r0w[i];
-    d.th[i] = pl.th[i];
-    d.tw[i] = pl.tw[i];
-  }
   const long long total = static_cast<long long>(d.slots) * c_out * d.kmax;
   if (elt_bytes(dt) == 2)
     pack_transposed_kernel<uint16_t><<<pack_grid(total), 256, 0, stream>>>(
@@ -1607,7 +1670,12 @@ struct PackStep {
 struct Prepared {
   int path;
   PackStep pack;
-  Plan pl;          // kPathIgemm (also carries the transposed packing description)
+  TrPacking trp;    // transposed convs: the packed filter's layout (for the pack step)
+  // kPathIgemm: the launches, in order (one, or for a transposed conv with
+  // more than kMaxPhases phase slots, one per group of kMaxPhases slots; the
+  // groups write disjoint output pixels).
+  int n_plans;
+  Plan pl[kMaxTrLaunches];
   RowTapPlan rt;    // kPathRowTap
   DirectParams dp;  // kPathDirect
   int direct_in_dtype;
@@ -1619,7 +1687,7 @@ conv_status_t run_pack(const Prepared& pr, cudaStream_t stream) {
   if (k.kind == 1)
     return launch_pack_fwd(k.filter, k.r, k.s, k.c_in, k.c_out, k.fcrs, k.dtype, k.dst, stream);
   if (k.kind == 2)
-    return launch_pack_tr(pr.pl, k.filter, k.r, k.s, k.c_in, k.c_out, k.dtype, k.dst, stream);
+    return launch_pack_tr(pr.trp, k.filter, k.r, k.s, k.c_in, k.c_out, k.dtype, k.dst, stream);
   return CONV_OK;
 }
 
@@ -1636,17 +1704,29 @@ uint32_t next_sk_epoch() {
   return e;
 }
 
-conv_status_t launch_prepared(Prepared& pr, cudaStream_t stream) {
+conv_status_t launch_prepared(const Prepared& pr, cudaStream_t stream) {
   conv_status_t st = run_pack(pr, stream);
   if (st != CONV_OK) return st;
-  if (pr.path == kPathIgemm && pr.pl.kp.streamk) pr.pl.kp.sk_epoch = next_sk_epoch();
   if (pr.path == kPathRowTap) return launch_rowtap(pr.rt, stream);
   if (pr.path == kPathDirect) {
     cudaError_t e = launch_conv_direct(pr.direct_in_dtype, pr.direct_in_dtype != CONV_DTYPE_F16,
                                        pr.dp, pr.sms, stream);
     return e == cudaSuccess ? CONV_OK : CONV_ERR_CUDA;
   }
-  return launch_plan(pr.pl, stream);
+  for (int i = 0; i < pr.n_plans; ++i) {
+    if (pr.pl[i].kp.streamk) {
+      // The prepared plan is shared and immutable: the launch's flag value
+      // goes into a copy.
+      thread_local Plan sk_plan;
+      sk_plan = pr.pl[i];
+      sk_plan.kp.sk_epoch = next_sk_epoch();
+      st = launch_plan(sk_plan, stream);
+    } else {
+      st = launch_plan(pr.pl[i], stream);
+    }
+    if (st != CONV_OK) return st;
+  }
+  return CONV_OK;
 }
 
 // Prepares conv2d_fwd / conv2d_fwd_packed.  `filter` is raw (packed into the
@@ -1729,7 +1809,8 @@ conv_status_t prepare_fwd(const void* input, const FwdShape& shape, const void* 
     return finish_rowtap(&pr->rt, f, input, packed, output, has_residual, source, beta, epilogue,
                          workspace);
   }
-  Plan& pl = pr->pl;
+  Plan& pl = pr->pl[0];
+  pr->n_plans = 1;
   const size_t sk_offset = need;
   st = plan_fwd(f, &pl, sms, has_residual,
                 workspace_bytes > sk_offset ? workspace_bytes - sk_offset : 0);
@@ -1755,21 +1836,16 @@ conv_status_t prepare_tr(const void* input, const TrShape& t, const void* filter
   st = channel_block(t.c_in, elt_bytes(t.in_dtype), &bk, &row_bytes);
   if (st != CONV_OK) return st;
   const int st_hw[2] = {t.stride_h, t.stride_w};
+  const int dil_hw[2] = {t.dil_h, t.dil_w};
   const int pad_hw[2] = {t.pad_h, t.pad_w};
+  if (!tr_packing(t.r, t.s, t.c_in, st_hw, dil_hw, pad_hw, &pr->trp)) return CONV_ERR_NOT_SUPPORTED;
   const size_t packed_bytes =
-      conv_transposed_packed_filter_bytes(t.r, t.s, t.c_in, t.c_out, st_hw, pad_hw, t.in_dtype);
+      static_cast<size_t>(pr->trp.slots) * t.c_out * pr->trp.kmax * elt_bytes(t.in_dtype);
   const size_t need = CONV_STATUS_BYTES + (prepacked ? 0 : round_up_256(packed_bytes));
   if (workspace_bytes < need) return CONV_ERR_WORKSPACE_TOO_SMALL;
   const int sms = device_sm_count();
   if (sms <= 0) return CONV_ERR_CUDA;
   pr->sms = sms;
-  Plan& pl = pr->pl;
-  const size_t sk_offset = need;
-  st = plan_transposed(t, &pl, sms, workspace_bytes > sk_offset ? workspace_bytes - sk_offset : 0);
-  if (st != CONV_OK) return st;
-  pl.sk_offset = sk_offset;
-  st = encode_tr_inputs(t, input, &pl);
-  if (st != CONV_OK) return st;
   const void* packed = filter;
   pr->pack.kind = 0;
   if (!prepacked) {
@@ -1778,7 +1854,24 @@ conv_status_t prepare_tr(const void* input, const TrShape& t, const void* filter
     packed = dst;
   }
   pr->path = kPathIgemm;
-  return finish_plan(&pl, t.n, packed, output, has_residual, source, beta, epilogue, workspace);
+  // Phase slots with output pixels, kMaxPhases per launch.
+  int slots[kMaxTrSlots];
+  const int nslots = tr_active_slots(t, slots);
+  pr->n_plans = (nslots + kMaxPhases - 1) / kMaxPhases;
+  const size_t sk_offset = need;
+  for (int i = 0; i < pr->n_plans; ++i) {
+    Plan& pl = pr->pl[i];
+    st = plan_transposed(t, pr->trp, slots + i * kMaxPhases,
+                         std::min(kMaxPhases, nslots - i * kMaxPhases), &pl, sms,
+                         workspace_bytes > sk_offset ? workspace_bytes - sk_offset : 0);
+    if (st != CONV_OK) return st;
+    pl.sk_offset = sk_offset;
+    st = encode_tr_inputs(t, input, &pl);
+    if (st != CONV_OK) return st;
+    st = finish_plan(&pl, t.n, packed, output, has_residual, source, beta, epilogue, workspace);
+    if (st != CONV_OK) return st;
+  }
+  return CONV_OK;
 }
 
 // ------------------------------------------------------------------ prepared-call cache
@@ -1807,7 +1900,7 @@ constexpr int kProbe = 8;
 struct CacheSlot {
   bool valid;
   CallKey key;
-  Prepared prep;
+  std::shared_ptr<const Prepared> prep;  // immutable once stored
 };
 
 std::mutex g_cache_mu;
@@ -1856,24 +1949,23 @@ CallKey make_key(int entry, const void* input, const void* filter, const void* o
   return k;
 }
 
-bool cache_lookup(const CallKey& key, Prepared* out) {
+std::shared_ptr<const Prepared> cache_lookup(const CallKey& key) {
   const size_t home = key_hash(key) % kCacheEntries;
   std::lock_guard<std::mutex> lock(g_cache_mu);
   if (g_cache) {
     for (int i = 0; i < kProbe; ++i) {
       const CacheSlot& slot = g_cache[(home + i) % kCacheEntries];
       if (slot.valid && std::memcmp(&slot.key, &key, sizeof(key)) == 0) {
-        *out = slot.prep;
         g_cache_hits.fetch_add(1, std::memory_order_relaxed);
-        return true;
+        return slot.prep;
       }
     }
   }
   g_cache_misses.fetch_add(1, std::memory_order_relaxed);
-  return false;
+  return nullptr;
 }
 
-void cache_store(const CallKey& key, const Prepared& prep) {
+void cache_store(const CallKey& key, const std::shared_ptr<const Prepared>& prep) {
   const size_t home = key_hash(key) % kCacheEntries;
   std::lock_guard<std::mutex> lock(g_cache_mu);
   if (!g_cache) {
@@ -1898,15 +1990,17 @@ void cache_store(const CallKey& key, const Prepared& prep) {
 // preparations), and launches it.
 template <typename PrepareFn>
 conv_status_t cached_call(const CallKey& key, PrepareFn prepare, cudaStream_t stream) {
-  // Large (several KB): keep it off the stack of callers with small stacks.
-  thread_local Prepared pr;
-  if (!cache_lookup(key, &pr)) {
-    std::memset(&pr, 0, sizeof(pr));
-    conv_status_t st = prepare(&pr);
+  std::shared_ptr<const Prepared> pr = cache_lookup(key);
+  if (!pr) {
+    // Large (several plans): on the heap, zero-initialised.
+    std::shared_ptr<Prepared> fresh(new (std::nothrow) Prepared());
+    if (!fresh) return CONV_ERR_INVALID_VALUE;
+    conv_status_t st = prepare(fresh.get());
     if (st != CONV_OK) return st;
-    if (key.device >= 0) cache_store(key, pr);
+    if (key.device >= 0) cache_store(key, fresh);
+    pr = fresh;
   }
-  return launch_prepared(pr, stream);
+  return launch_prepared(*pr, stream);
 }
 
 }  // namespace
@@ -2023,66 +2117,68 @@ conv_status_t conv2d_fwd_packed(const void* input, int n, int h, int w, int c_in
   }, static_cast<cudaStream_t>(stream));
 }
 
+size_t conv_transposed_packed_filter_bytes_dilated(int r, int s, int c_in, int c_out,
+                                                   const int stride[2], const int dilation[2],
+                                                   const int padding[2], conv_dtype_t dtype) {
+  if (!stride || !dilation || !padding || r <= 0 || s <= 0 || c_in <= 0 || c_out <= 0 ||
+      !known_dtype(dtype))
+    return 0;
+  TrPacking pk;
+  if (!tr_packing(r, s, c_in, stride, dilation, padding, &pk)) return 0;
+  return static_cast<size_t>(pk.slots) * c_out * pk.kmax * elt_bytes(dtype);
+}
+
 size_t conv_transposed_packed_filter_bytes(int r, int s, int c_in, int c_out, const int stride[2],
                                            const int padding[2], conv_dtype_t dtype) {
-  if (!stride || !padding || r <= 0 || s <= 0 || c_in <= 0 || c_out <= 0 || !known_dtype(dtype))
-    return 0;
-  if (stride[0] <= 0 || stride[1] <= 0 || stride[0] > 2 || stride[1] > 2) return 0;
-  if (padding[0] < 0 || padding[1] < 0) return 0;
-  int kmax = 0;
-  for (int a = 0; a < stride[0]; ++a) {
-    const int ta = axis_phase(a, stride[0], padding[0], r, stride[0]).taps;
-    for (int b = 0; b < stride[1]; ++b) {
-      const int tb = axis_phase(b, stride[1], padding[1], s, stride[1]).taps;
-      kmax = std::max(kmax, ta * tb * c_in);
-    }
-  }
-  if (kmax == 0) kmax = c_in;
-  return static_cast<size_t>(stride[0]) * stride[1] * c_out * kmax * elt_bytes(dtype);
+  const int dil[2] = {1, 1};
+  return conv_transposed_packed_filter_bytes_dilated(r, s, c_in, c_out, stride, dil, padding, dtype);
+}
+
+size_t conv_transposed_workspace_size_dilated(int r, int s, int c_in, int c_out,
+                                              const int stride[2], const int dilation[2],
+                                              const int padding[2], conv_dtype_t dtype) {
+  return CONV_STATUS_BYTES + round_up_256(conv_transposed_packed_filter_bytes_dilated(
+                                 r, s, c_in, c_out, stride, dilation, padding, dtype));
 }
 
 size_t conv_transposed_workspace_size(int r, int s, int c_in, int c_out, const int stride[2],
                                       const int padding[2], conv_dtype_t dtype) {
-  return CONV_STATUS_BYTES +
-         round_up_256(conv_transposed_packed_filter_bytes(r, s, c_in, c_out, stride, padding, dtype));
+  const int dil[2] = {1, 1};
+  return conv_transposed_workspace_size_dilated(r, s, c_in, c_out, stride, dil, padding, dtype);
+}
+
+conv_status_t conv_transposed_pack_filter_dilated(const void* filter_rsfc, int r, int s, int c_in,
+                                                  int c_out, const int stride[2],
+                                                  const int dilation[2], const int padding[2],
+                                                  conv_dtype_t dtype, void* packed,
+                                                  size_t packed_bytes, void* stream) {
+  if (!filter_rsfc || !packed || !stride || !dilation || !padding) return CONV_ERR_INVALID_VALUE;
+  if (r <= 0 || s <= 0 || c_in <= 0 || c_out <= 0) return CONV_ERR_INVALID_VALUE;
+  if (!known_dtype(dtype)) return CONV_ERR_NOT_SUPPORTED;
+  if (stride[0] < 1 || stride[1] < 1 || stride[0] * stride[1] > kMaxTrSlots)
+    return CONV_ERR_NOT_SUPPORTED;
+  if (dilation[0] < 1 || dilation[1] < 1 || dilation[0] > kMaxFilterExtent ||
+      dilation[1] > kMaxFilterExtent)
+    return CONV_ERR_NOT_SUPPORTED;
+  if (padding[0] < 0 || padding[1] < 0 || padding[0] > dilation[0] * (r - 1) ||
+      padding[1] > dilation[1] * (s - 1))
+    return CONV_ERR_NOT_SUPPORTED;
+  if (!aligned16(filter_rsfc) || !aligned16(packed)) return CONV_ERR_MISALIGNED;
+  TrPacking pk;
+  if (!tr_packing(r, s, c_in, stride, dilation, padding, &pk)) return CONV_ERR_NOT_SUPPORTED;
+  if (packed_bytes < static_cast<size_t>(pk.slots) * c_out * pk.kmax * elt_bytes(dtype))
+    return CONV_ERR_WORKSPACE_TOO_SMALL;
+  return launch_pack_tr(pk, filter_rsfc, r, s, c_in, c_out, dtype, packed,
+                        static_cast<cudaStream_t>(stream));
 }
 
 conv_status_t conv_transposed_pack_filter(const void* filter_rsfc, int r, int s, int c_in,
                                           int c_out, const int stride[2], const int padding[2],
                                           conv_dtype_t dtype, void* packed, size_t packed_bytes,
                                           void* stream) {
-  if (!filter_rsfc || !packed || !stride || !padding) return CONV_ERR_INVALID_VALUE;
-  if (r <= 0 || s <= 0 || c_in <= 0 || c_out <= 0) return CONV_ERR_INVALID_VALUE;
-  if (!known_dtype(dtype)) return CONV_ERR_NOT_SUPPORTED;
-  if (!((stride[0] == 1 && stride[1] == 1) || (stride[0] == 2 && stride[1] == 2)))
-    return CONV_ERR_NOT_SUPPORTED;
-  if (padding[0] < 0 || padding[1] < 0 || padding[0] >= r || padding[1] >= s)
-    return CONV_ERR_NOT_SUPPORTED;
-  if (!aligned16(filter_rsfc) || !aligned16(packed)) return CONV_ERR_MISALIGNED;
-  const size_t need = conv_transposed_packed_filter_bytes(r, s, c_in, c_out, stride, padding, dtype);
-  if (packed_bytes < need) return CONV_ERR_WORKSPACE_TOO_SMALL;
-  // The phase taps depend only on stride, padding and filter extent.
-  Plan pl;
-  std::memset(&pl, 0, sizeof(pl));
-  pl.sh = stride[0];
-  pl.sw = stride[1];
-  pl.phases_packed = stride[0] * stride[1];
-  int kmax = 0;
-  for (int a = 0; a < stride[0]; ++a) {
-    const AxisPhase ya = axis_phase(a, stride[0], padding[0], r, stride[0]);
-    for (int b = 0; b < stride[1]; ++b) {
-      const AxisPhase xb = axis_phase(b, stride[1], padding[1], s, stride[1]);
-      const int slot = a * stride[1] + b;
-      pl.r0h[slot] = ya.r0;
-      pl.r0w[slot] = xb.r0;
-      pl.th[slot] = ya.taps;
-      pl.tw[slot] = xb.taps;
-      kmax = std::max(kmax, ya.taps * xb.taps * c_in);
-    }
-  }
-  pl.kmax = kmax ? kmax : c_in;
-  return launch_pack_tr(pl, filter_rsfc, r, s, c_in, c_out, dtype, packed,
-                        static_cast<cudaStream_t>(stream));
+  const int dil[2] = {1, 1};
+  return conv_transposed_pack_filter_dilated(filter_rsfc, r, s, c_in, c_out, stride, dil, padding,
+                                             dtype, packed, packed_bytes, stream);
 }
 
 conv_status_t conv_transposed(const void* input, int n, int h, int w, int c_in,

@@ -72,6 +72,12 @@ class ConvCase:
     pad_w: Optional[int] = None        # padding along W when it differs from `pad` (H)
     dilation_w: Optional[int] = None   # dilation along W when it differs from `dilation` (H)
     groups: int = 1                    # channel groups (forward): filter channels = C_in / groups
+    stride_w: Optional[int] = None     # stride along W when it differs from `stride` (H; transposed)
+
+    @property
+    def strides(self) -> Tuple[int, int]:
+        """(stride_h, stride_w)."""
+        return (self.stride, self.stride if self.stride_w is None else self.stride_w)
 
     @property
     def pads(self) -> Tuple[int, int]:
