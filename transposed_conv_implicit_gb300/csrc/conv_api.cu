@@ -44,13 +44,15 @@ int elt_bytes(conv_dtype_t d) { return d == CONV_DTYPE_F8E4M3 ? 1 : 2; }
 // source buffer), CONV_PAIR (1/0: force CTA pairs on/off), CONV_WINDOW,
 // CONV_ROWTAP, CONV_GATHER_STAGE and CONV_L2_PREFETCH (-1 disables that
 // loader or feature), CONV_ROWTAP_BAND, CONV_STREAMK (1/0: force the
-// stream-K schedule on where it applies / off), CONV_WAIT_HINT_NS.  Read once
+// stream-K schedule on where it applies / off), CONV_MMA_SPLIT (0: one MMA
+// issuer for both 128-row halves), CONV_WAIT_HINT_NS.  Read once
 // per process, on first use; conv_testing_reload_tuning() reads them again.
 struct Tuning {
   int tile_m, tile_n, max_stages, src_bufs, window, rowtap, rowtap_band, gather_stage, l2_prefetch;
   int filter_resident;  // -1 when unset
   int pair;             // -1 when unset
   int streamk;          // -1 when unset
+  int mma_split;        // 0 disables the second MMA issuer
   uint32_t wait_hint_ns;
 };
 
@@ -78,6 +80,7 @@ Tuning read_tuning() {
   t.filter_resident = env_int_or("CONV_FILTER_RESIDENT", -1);
   t.pair = env_int_or("CONV_PAIR", -1);
   t.streamk = env_int_or("CONV_STREAMK", -1);
+  t.mma_split = env_int_or("CONV_MMA_SPLIT", 1);
   t.wait_hint_ns = static_cast<uint32_t>(env_int("CONV_WAIT_HINT_NS"));
   return t;
 }
@@ -1438,6 +1441,9 @@ conv_status_t finish_plan(Plan* pl, int n_images, const void* packed, void* outp
   kp.timeout_cycles = ns_to_cycles(tmo ? tmo : kDefaultTimeoutNs);
   kp.wait_hint_ns = tuning().wait_hint_ns;
   kp.fault_mode = g_fault_mode.load(std::memory_order_relaxed);
+  // Two MMA issuers, one per 128-row half, where there are two halves and
+  // warp 11 is free (TMA loaders, single CTAs).  CONV_MMA_SPLIT=0 disables.
+  kp.mma_split = (kp.m_halves == 2 && !kp.gather && !kp.pair && tuning().mma_split != 0) ? 1 : 0;
   kp.div_ntiles = make_fast_div(static_cast<uint32_t>(std::max(kp.n_tiles, 1)));
   for (int ph = 0; ph < kMaxPhases; ++ph) {
     const uint32_t gh = static_cast<uint32_t>(std::max(kp.grid_h[ph], 1));

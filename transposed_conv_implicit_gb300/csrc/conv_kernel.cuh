@@ -568,19 +568,23 @@ __device__ __forceinline__ void issue_kblock(uint32_t d_tmem, uint64_t desc_hi, 
 // The MMA role for one (kSteps, kHalves) specialisation.  Tiles t0, t0 +
 // step, ...  kPair: rank 0 of a CTA pair issues M = 256 MMAs over both CTAs'
 // operands (each holds bn/2 rows of B) and commits to both CTAs' barriers.
+// `half`: with two issuing warps (mma_split) each issues the MMAs of one
+// 128-row half (kHalves = 1), into that half's accumulator columns; -1: this
+// warp issues every half.
 template <int kKind, int kSteps, int kHalves, bool kPair = false, bool kStreamK = false>
 __device__ __forceinline__ bool mma_role(const ConvKernelParams& p, uint32_t tmem_base,
                                          uint8_t* a_ring, uint8_t* b_ring, uint8_t* b_res,
                                          uint64_t* full, uint64_t* empty, uint64_t* tfull,
-                                         uint64_t* tempty, uint64_t* bres_full,
-                                         volatile int* abort_flag, unsigned int* status,
-                                         long long limit, int t0, int step) {
+                                         uint64_t* tempty, int half, volatile int* abort_flag,
+                                         unsigned int* status, long long limit, int t0,
+                                         int step) {
   const int stages = p.stages;
   const uint32_t sw = p.sw_bytes;
-  const uint32_t a_bytes = kBM * kHalves * sw;
+  const uint32_t a_bytes = kBM * p.m_halves * sw;  // stage stride: every half of A
   const uint32_t b_bytes = static_cast<uint32_t>(kPair ? p.bn / 2 : p.bn) * sw;
   const uint64_t desc_hi = smem_desc_kmajor(0, sw);  // address field zero
-  const uint32_t a_lo0 = smem_u32(a_ring) >> 4;
+  const uint32_t h0 = half < 0 ? 0u : static_cast<uint32_t>(half);
+  const uint32_t a_lo0 = (smem_u32(a_ring) >> 4) + h0 * ((kBM * sw) >> 4);
   const uint32_t b_lo0 = smem_u32(p.b_resident ? b_res : b_ring) >> 4;
   const uint32_t a_step = a_bytes >> 4;
   const uint32_t b_step = b_bytes >> 4;
@@ -619,7 +623,8 @@ __device__ __forceinline__ bool mma_role(const ConvKernelParams& p, uint32_t tme
       }
       continue;
     }
-    const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc) * acc_stride;
+    const uint32_t d_tmem =
+        tmem_base + static_cast<uint32_t>(acc) * acc_stride + h0 * bn_cols;
     // Resident B: block kb of the tile sits at index kb.
     uint32_t br_lo = b_lo0 + static_cast<uint32_t>(wk.kb0) * b_step;
     const int kblocks = wk.kb1 - wk.kb0;
@@ -664,18 +669,20 @@ template <int kKind, int kSteps, int kHalves>
 __device__ __forceinline__ bool mma_role_window(const ConvKernelParams& p, uint32_t tmem_base,
                                                 uint8_t* a_ring, uint8_t* b_res, uint64_t* full,
                                                 uint64_t* empty, uint64_t* tfull, uint64_t* tempty,
-                                                volatile int* abort_flag, unsigned int* status,
-                                                long long limit, int t0, int step) {
+                                                int half, volatile int* abort_flag,
+                                                unsigned int* status, long long limit, int t0,
+                                                int step) {
   const int stages = p.stages;
   const uint32_t sw = p.sw_bytes;  // 128 in this mode
   const uint32_t b_bytes = static_cast<uint32_t>(p.bn) * sw;
   const uint64_t desc_hi = smem_desc_kmajor(0, sw);
-  const uint32_t a_lo0 = smem_u32(a_ring) >> 4;
+  const uint32_t row_lo = sw >> 4;  // one box row in descriptor address units
+  const uint32_t half_lo = static_cast<uint32_t>(p.win_half_rows) * row_lo;
+  const uint32_t h0 = half < 0 ? 0u : static_cast<uint32_t>(half);
+  const uint32_t a_lo0 = (smem_u32(a_ring) >> 4) + h0 * half_lo;
   const uint32_t b_lo0 = smem_u32(b_res) >> 4;
   const uint32_t a_step = p.win_stage_bytes >> 4;
   const uint32_t b_step = b_bytes >> 4;
-  const uint32_t row_lo = sw >> 4;  // one box row in descriptor address units
-  const uint32_t half_lo = static_cast<uint32_t>(p.win_half_rows) * row_lo;
   const uint32_t bn_cols = static_cast<uint32_t>(p.bn);
   const uint32_t idesc = p.idesc;
   const uint32_t full0 = smem_u32(full), empty0 = smem_u32(empty);
@@ -699,7 +706,7 @@ __device__ __forceinline__ bool mma_role_window(const ConvKernelParams& p, uint3
       break;
     }
     tc_fence_after();
-    const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc) * acc_stride;
+    const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc) * acc_stride + h0 * bn_cols;
     for (int cb = 0; cb < c_blocks; ++cb) {
       if (!mbar_wait_bounded(full0 + 8u * stage, phase, abort_flag, status, kStatusMmaTimeout,
                              limit)) {
@@ -1141,23 +1148,27 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* epi_done = src_full + 4;   // every epilogue warp has finished with TMEM
   uint64_t* gst_full = epi_done + 1;   // gather row staging: [buffer]
   uint64_t* gst_empty = gst_full + 2;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gst_empty + 2);
+  uint64_t* drain2 = gst_empty + 2;    // the second MMA issuer's drain
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain2 + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   unsigned int* status = p.status;
   const long long limit = p.timeout_cycles;
 
   if (threadIdx.x == 0) {
+    // Stage-empty and accumulator-full phases take one commit per MMA issuer.
+    const uint32_t issuers = p.mma_split ? 2u : 1u;
     for (int s = 0; s < stages; ++s) {
       mbar_init(smem_u32(&full[s]), 1);
-      mbar_init(smem_u32(&empty[s]), 1);
+      mbar_init(smem_u32(&empty[s]), issuers);
     }
     for (int a = 0; a < 2; ++a) {
-      mbar_init(smem_u32(&tfull[a]), 1);
+      mbar_init(smem_u32(&tfull[a]), issuers);
       mbar_init(smem_u32(&tempty[a]), kEpilogueWarps * (kPair ? 2 : 1));
       mbar_init(smem_u32(&src_full[2 * a]), 1);
       mbar_init(smem_u32(&src_full[2 * a + 1]), 1);
     }
     mbar_init(smem_u32(drain), 1);
+    mbar_init(smem_u32(drain2), 1);
     mbar_init(smem_u32(bres_full), 1);
     mbar_init(smem_u32(epi_done), kEpilogueWarps);
     for (int b = 0; b < 2; ++b) {
@@ -1193,7 +1204,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   grid_dependency_wait();
   grid_launch_dependents();
 
-  if (warp == 0 || warp >= kProducer2Warp) {
+  const bool split_issuer = !kGather && !kPair && p.mma_split;  // warp 11 issues MMAs
+  if (warp == 0 || warp == kProducer2Warp || (warp == kProducer3Warp && !split_issuer)) {
     // ------------------------------------------------------------ producers
     // The producer warps walk the same k-block sequence; with the TMA loaders
     // k-block `seq` is issued by warp 0 or 10 (seq & 1), so two TMA issue
@@ -1371,28 +1383,36 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
     __syncwarp();
-  } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
-    // (In a pair only rank 0 issues.)
+  } else if (warp == 1 || warp == kProducer3Warp) {
+    // ------------------------------------------------------------ MMA issuers
+    // Warp 1 issues; with mma_split (two 128-row halves, no gather loader,
+    // no pair) warp 11 issues the second half's MMAs beside it: one thread
+    // cannot issue MMAs of N <= 128 as fast as the tensor core runs them
+    // (measured: 183 cycles per MMA with a barrier wait and commit per 4,
+    // 65 with two issuing warps).  (In a pair only rank 0 issues.)
     if (lane == 0 && rank == 0) {
       bool ok;
       const int ks = static_cast<int>(sw / 32);
+      const int half = p.mma_split ? (warp == 1 ? 0 : 1) : -1;
+      uint64_t* my_drain = warp == 1 ? drain : drain2;
       if (!kPair && p.window) {
-        ok = p.m_halves == 2
+        ok = (p.m_halves == 2 && half < 0)
                  ? mma_role_window<kKind, 4, 2>(p, tmem_base, a_ring, b_res, full, empty, tfull,
-                                                tempty, abort_flag, status, limit, tile0, tile_step)
+                                                tempty, half, abort_flag, status, limit, tile0,
+                                                tile_step)
                  : mma_role_window<kKind, 4, 1>(p, tmem_base, a_ring, b_res, full, empty, tfull,
-                                                tempty, abort_flag, status, limit, tile0, tile_step);
+                                                tempty, half, abort_flag, status, limit, tile0,
+                                                tile_step);
         if (!ok) {
-          mma_commit(smem_u32(drain));
-          mbar_wait_drain(smem_u32(drain), 0, limit / 8 + 1);
+          mma_commit(smem_u32(my_drain));
+          mbar_wait_drain(smem_u32(my_drain), 0, limit / 8 + 1);
         }
       } else {
 #define CONV_MMA_ROLE(KS, MH)                                                                   \
   mma_role<kKind, KS, MH, kPair, kStreamK>(p, tmem_base, a_ring, b_ring, b_res, full, empty,       \
-                                           tfull, tempty,                                         \
-                                 bres_full, abort_flag, status, limit, tile0, tile_step)
-      if (!kPair && p.m_halves == 2)
+                                           tfull, tempty, half, abort_flag, status, limit, tile0,  \
+                                           tile_step)
+      if (!kPair && p.m_halves == 2 && half < 0)
         ok = ks == 4 ? CONV_MMA_ROLE(4, 2) : (ks == 2 ? CONV_MMA_ROLE(2, 2) : CONV_MMA_ROLE(1, 2));
       else
         ok = ks == 4 ? CONV_MMA_ROLE(4, 1) : (ks == 2 ? CONV_MMA_ROLE(2, 1) : CONV_MMA_ROLE(1, 1));
@@ -1400,10 +1420,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!ok) {
         // Every MMA already issued must finish before TMEM is released.
         if (kPair)
-          mma_commit_pair(smem_u32(drain));
+          mma_commit_pair(smem_u32(my_drain));
         else
-          mma_commit(smem_u32(drain));
-        mbar_wait_drain(smem_u32(drain), 0, limit / 8 + 1);
+          mma_commit(smem_u32(my_drain));
+        mbar_wait_drain(smem_u32(my_drain), 0, limit / 8 + 1);
       }
       }
     }

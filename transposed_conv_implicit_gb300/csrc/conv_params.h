@@ -10,7 +10,8 @@ namespace convgb300 {
 
 constexpr int kBM = 128;             // rows (output pixels) per MMA = TMEM lanes
 // Warps: 0 producer, 1 MMA, 2-9 epilogue, 10 producer, 11 producer (the gather
-// loader only: it builds A with three warps; the TMA loaders use two).
+// loader: it builds A with three warps) or, with the TMA loaders and two
+// 128-row halves per tile, the second MMA issuer.
 constexpr int kThreads = 384;
 constexpr int kProducer2Warp = 10;
 constexpr int kProducer3Warp = 11;
@@ -49,6 +50,7 @@ struct ConvKernelParams {  // aligned like CUtensorMap (64 B or more)
   int num_phases;
   int total_tiles;
   int pair;             // clusters of two CTAs share 256-row tiles (cta_group::2 MMAs)
+  int mma_split;        // two MMA-issuing warps, one per 128-row half (m_halves = 2)
   int m_halves;         // 128-row halves per tile (1 or 2): tile_m = 128 * m_halves
   int n_tiles;          // tiles along C_out
   int bn;               // tile width along C_out (multiple of 16, <= 256)
