@@ -20,15 +20,19 @@
 //
 // Warp roles (384 threads, one persistent CTA per SM, or one per SM of a
 // CTA pair):
-//   warps 0, 10  producers: k-block `seq` belongs to warp (seq & 1); one lane
-//                issues its TMA loads into an S-stage shared-memory ring
-//                guarded by full/empty mbarriers;
-//   warp 11      idle with the TMA loaders; in gather mode warps 0, 10 and 11
-//                each build every third k-block (k-block `seq` belongs to
-//                warp seq % 3), the whole warp writing it;
-//   warp 1       TMEM owner and MMA issuer: one lane issues tcgen05.mma
+//   warps 0, 10  producers: k-block `seq` belongs to producer seq % nprod;
+//   (and 11)     the whole warp walks the k-blocks and one lane issues its
+//                TMA loads into an S-stage shared-memory ring guarded by
+//                full/empty mbarriers.  Warp 11 is the third TMA producer
+//                unless it issues MMAs (below); in gather mode warps 0, 10
+//                and 11 each build every third k-block, the whole warp
+//                writing it;
+//   warp 1       TMEM owner and MMA issuer: the converged warp walks the
+//                k-blocks and one elected lane issues each tcgen05.mma
 //                (M=128 per half, N=bn; M=256 over both CTAs of a pair, from
-//                rank 0) into a double-buffered fp32 TMEM accumulator;
+//                rank 0) into a double-buffered fp32 TMEM accumulator; with
+//                two 128-row halves and the TMA loaders warp 11 issues the
+//                second half's MMAs;
 //   warps 2-9    epilogue, two warpgroups taking alternate (half, column
 //                chunk) items: tcgen05.ld the accumulator, add beta*source,
 //                apply the activation, round once to the output dtype and
@@ -537,7 +541,8 @@ __device__ __forceinline__ void issue_source_items(const ConvKernelParams& p, co
 // Issues the MMAs of one k-block: kSteps K-steps of 32 bytes per operand row,
 // kHalves 128-row halves of A sharing the B operand.  Descriptors are built
 // from precomputed high bits plus an address field advanced by adds only: the
-// issuing thread is latency-bound, so nothing here divides or branches.
+// issuing warp is latency-bound, so nothing here divides or branches.  Every
+// lane of the (converged) MMA warp runs this; one lane issues each MMA.
 // kPair: one M = 256 MMA over both CTAs of a pair (issued by rank 0).
 template <int kKind, int kSteps, int kHalves, bool kPair = false>
 __device__ __forceinline__ void issue_kblock(uint32_t d_tmem, uint64_t desc_hi, uint32_t a_lo,
@@ -552,14 +557,14 @@ __device__ __forceinline__ void issue_kblock(uint32_t d_tmem, uint64_t desc_hi, 
       const uint64_t adesc = desc_hi | static_cast<uint64_t>(a_lo + h * half_lo + 2u * kk);
       if (kPair) {
         if (kKind == kKindF16)
-          mma_f16_pair(d_tmem + h * bn_cols, adesc, bdesc, idesc, accumulate);
+          mma_f16_pair_warp(d_tmem + h * bn_cols, adesc, bdesc, idesc, accumulate);
         else
-          mma_f8_pair(d_tmem + h * bn_cols, adesc, bdesc, idesc, accumulate);
+          mma_f8_pair_warp(d_tmem + h * bn_cols, adesc, bdesc, idesc, accumulate);
       } else {
         if (kKind == kKindF16)
-          mma_f16(d_tmem + h * bn_cols, adesc, bdesc, idesc, accumulate);
+          mma_f16_warp(d_tmem + h * bn_cols, adesc, bdesc, idesc, accumulate);
         else
-          mma_f8(d_tmem + h * bn_cols, adesc, bdesc, idesc, accumulate);
+          mma_f8_warp(d_tmem + h * bn_cols, adesc, bdesc, idesc, accumulate);
       }
     }
   }
@@ -602,6 +607,7 @@ __device__ __forceinline__ bool mma_role(const ConvKernelParams& p, uint32_t tme
   uint32_t a_lo = a_lo0;
   uint32_t bs_lo = b_lo0;  // streamed B: advances with the ring
   bool ok = true;
+  bool ahead_ready = false;  // the look-ahead test found the current stage landed
   int it = 0;
   (void)total_tiles;
   WorkWalk walk = work_begin<kStreamK>(p, t0, step);
@@ -609,18 +615,21 @@ __device__ __forceinline__ bool mma_role(const ConvKernelParams& p, uint32_t tme
   for (; ok && work_next<kStreamK>(p, walk, wk); ++it) {
     const TileInfo& ti = wk.ti;
     const int acc = it & 1;
-    if (!mbar_wait_bounded(smem_u32(&tempty[acc]), static_cast<uint32_t>(((it >> 1) & 1) ^ 1),
-                           abort_flag, status, kStatusMmaTimeout, limit, 0u, kPair)) {
+    if (!__all_sync(0xFFFFFFFFu,
+                    mbar_wait_bounded(smem_u32(&tempty[acc]),
+                                      static_cast<uint32_t>(((it >> 1) & 1) ^ 1), abort_flag,
+                                      status, kStatusMmaTimeout, limit, 0u, kPair))) {
       ok = false;
       break;
     }
     tc_fence_after();
     if (ti.kblocks == 0) {  // a phase with no filter taps: the epilogue writes act(0)
       if (kPair) {
-        mma_commit_pair(smem_u32(&tfull[acc]));
-      } else {
+        mma_commit_pair_warp(smem_u32(&tfull[acc]));
+      } else if ((threadIdx.x & 31) == 0) {
         mbar_arrive(smem_u32(&tfull[acc]));
       }
+      __syncwarp();
       continue;
     }
     const uint32_t d_tmem =
@@ -629,19 +638,30 @@ __device__ __forceinline__ bool mma_role(const ConvKernelParams& p, uint32_t tme
     uint32_t br_lo = b_lo0 + static_cast<uint32_t>(wk.kb0) * b_step;
     const int kblocks = wk.kb1 - wk.kb0;
     for (int kb = 0; kb < kblocks; ++kb) {
-      if (!mbar_wait_bounded(full0 + 8u * stage, phase, abort_flag, status, kStatusMmaTimeout,
-                             limit, 0u, kPair)) {
+      if (!ahead_ready &&
+          !__all_sync(0xFFFFFFFFu, mbar_wait_bounded(full0 + 8u * stage, phase, abort_flag,
+                                                     status, kStatusMmaTimeout, limit, 0u,
+                                                     kPair))) {
         ok = false;
         break;
       }
       tc_fence_after();
+      // Test the next stage now: the test's latency overlaps this k-block's
+      // issue, and a stage already landed then needs no blocking wait.
+      {
+        const bool wrap = stage + 1 == stages;
+        const uint32_t nbar = full0 + (wrap ? 0u : 8u * (stage + 1));
+        const uint32_t nphase = wrap ? phase ^ 1u : phase;
+        ahead_ready = kPair ? mbar_test_wait_cluster(nbar, nphase) : mbar_test_wait(nbar, nphase);
+      }
       issue_kblock<kKind, kSteps, kHalves, kPair>(d_tmem, desc_hi, a_lo,
                                                   b_resident ? br_lo : bs_lo, half_lo, bn_cols,
                                                   idesc, kb != 0 ? 1u : 0u);
       if (kPair)
-        mma_commit_pair(empty0 + 8u * stage);
+        mma_commit_pair_warp(empty0 + 8u * stage);
       else
-        mma_commit(empty0 + 8u * stage);
+        mma_commit_warp(empty0 + 8u * stage);
+      ahead_ready = __all_sync(0xFFFFFFFFu, ahead_ready);
       br_lo += b_step;
       a_lo += a_step;
       bs_lo += b_step;
@@ -654,9 +674,9 @@ __device__ __forceinline__ bool mma_role(const ConvKernelParams& p, uint32_t tme
     }
     if (!ok) break;
     if (kPair)
-      mma_commit_pair(smem_u32(&tfull[acc]));
+      mma_commit_pair_warp(smem_u32(&tfull[acc]));
     else
-      mma_commit(smem_u32(&tfull[acc]));
+      mma_commit_warp(smem_u32(&tfull[acc]));
   }
   return ok;
 }
@@ -700,16 +720,18 @@ __device__ __forceinline__ bool mma_role_window(const ConvKernelParams& p, uint3
   int it = 0;
   for (int t = t0; ok && t < total_tiles; t += step, ++it) {
     const int acc = it & 1;
-    if (!mbar_wait_bounded(smem_u32(&tempty[acc]), static_cast<uint32_t>(((it >> 1) & 1) ^ 1),
-                           abort_flag, status, kStatusMmaTimeout, limit)) {
+    if (!__all_sync(0xFFFFFFFFu,
+                    mbar_wait_bounded(smem_u32(&tempty[acc]),
+                                      static_cast<uint32_t>(((it >> 1) & 1) ^ 1), abort_flag,
+                                      status, kStatusMmaTimeout, limit))) {
       ok = false;
       break;
     }
     tc_fence_after();
     const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc) * acc_stride + h0 * bn_cols;
     for (int cb = 0; cb < c_blocks; ++cb) {
-      if (!mbar_wait_bounded(full0 + 8u * stage, phase, abort_flag, status, kStatusMmaTimeout,
-                             limit)) {
+      if (!__all_sync(0xFFFFFFFFu, mbar_wait_bounded(full0 + 8u * stage, phase, abort_flag,
+                                                     status, kStatusMmaTimeout, limit))) {
         ok = false;
         break;
       }
@@ -728,7 +750,7 @@ __device__ __forceinline__ bool mma_role_window(const ConvKernelParams& p, uint3
           tap_lo += a_row_skip;
         }
       }
-      mma_commit(empty0 + 8u * stage);
+      mma_commit_warp(empty0 + 8u * stage);
       a_lo += a_step;
       if (++stage == stages) {
         stage = 0;
@@ -737,7 +759,7 @@ __device__ __forceinline__ bool mma_role_window(const ConvKernelParams& p, uint3
       }
     }
     if (!ok) break;
-    mma_commit(smem_u32(&tfull[acc]));
+    mma_commit_warp(smem_u32(&tfull[acc]));
   }
   return ok;
 }
@@ -1208,16 +1230,23 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 0 || warp == kProducer2Warp || (warp == kProducer3Warp && !split_issuer)) {
     // ------------------------------------------------------------ producers
     // The producer warps walk the same k-block sequence; with the TMA loaders
-    // k-block `seq` is issued by warp 0 or 10 (seq & 1), so two TMA issue
-    // streams overlap; the gather loader's three warps (0, 10, 11) build
-    // every third k-block each.
+    // k-block `seq` is issued by producer seq % nprod, so two or three TMA
+    // issue streams overlap; the gather loader's three warps (0, 10, 11)
+    // build every third k-block each.
     if constexpr (kGather) {
       const int role = warp == 0 ? 0 : (warp == kProducer2Warp ? 1 : 2);
       int4* tab = reinterpret_cast<int4*>(smem + p.off_gtab) + role * kBM * p.m_halves;
       gather_producer(p, role, lane, a_ring, b_ring, b_res, tab, smem + p.off_gstage, full, empty,
                       gst_full, gst_empty, abort_flag, status, limit);
-    } else if (lane == 0 && warp != kProducer3Warp) {
-      const int role = warp == 0 ? 0 : 1;
+    } else {
+      // The whole warp walks the k-blocks (operands stay warp-uniform); lane 0
+      // issues the copies.  K-block `seq` belongs to producer seq % nprod:
+      // warps 0 and 10, and warp 11 too when it issues no MMAs (one TMA
+      // issue stream cannot keep up with a converged MMA warp).
+      const uint32_t lead = lane == 0 ? 1u : 0u;
+      const int nprod = split_issuer ? 2 : 3;
+      const int role = warp == 0 ? 0 : (warp == kProducer2Warp ? 1 : 2);
+      int rr = 0;  // seq % nprod
       int stage = 0;
       uint32_t phase = 0;
       long long seq = 0;
@@ -1234,9 +1263,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           int n_img, oy0;
           window_origin(p, t, n_img, oy0);
           for (int cb = 0; cb < p.c_blocks; ++cb, ++seq) {
-            if ((seq & 1) == role) {
-              if (!mbar_wait_bounded(smem_u32(&empty[stage]), phase ^ 1u, abort_flag, status,
-                                     kStatusProducerTimeout, limit, p.wait_hint_ns)) {
+            if (rr == role) {
+              if (!__all_sync(0xFFFFFFFFu,
+                              mbar_wait_bounded(smem_u32(&empty[stage]), phase ^ 1u, abort_flag,
+                                                status, kStatusProducerTimeout, limit,
+                                                p.wait_hint_ns))) {
                 ok = false;
                 break;
               }
@@ -1247,15 +1278,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // channel block, on the same barrier.  (Each block on its own
                 // barrier, so that tap 0's MMAs could start earlier, measured
                 // slower: the ResNet 3x3 conv ran 19.0 against 16.7 us.)
-                mbar_arrive_expect_tx(fb, box_bytes + (first_tile ? b_bytes * taps : 0u));
-                tma_load_4d(smem_u32(a_ring + stage * p.win_stage_bytes), &p.map_a[0], fb,
-                            cb * p.bk, -p.win_pad_w, oy0 - p.win_pad_h, n_img);
+                mbar_arrive_expect_tx_if(lead, fb, box_bytes + (first_tile ? b_bytes * taps : 0u));
+                tma_load_4d_if(lead, smem_u32(a_ring + stage * p.win_stage_bytes), &p.map_a[0], fb,
+                               cb * p.bk, -p.win_pad_w, oy0 - p.win_pad_h, n_img);
                 if (first_tile)
                   for (int tap = 0; tap < taps; ++tap)
-                    tma_load_3d(smem_u32(b_res + (tap * p.c_blocks + cb) * b_bytes), &p.map_b, fb,
-                                tap * p.c_in + cb * p.bk, 0, 0);
+                    tma_load_3d_if(lead, smem_u32(b_res + (tap * p.c_blocks + cb) * b_bytes),
+                                   &p.map_b, fb, tap * p.c_in + cb * p.bk, 0, 0);
               }
             }
+            if (++rr == nprod) rr = 0;
             if (++stage == stages) {
               stage = 0;
               phase ^= 1u;
@@ -1313,9 +1345,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             pf_n = -1;  // skip
         }
         for (int kb = wk.kb0; kb < wk.kb1; ++kb, ++seq) {
-          if ((seq & 1) == role) {
-            if (!mbar_wait_bounded(smem_u32(&empty[stage]), phase ^ 1u, abort_flag, status,
-                                   kStatusProducerTimeout, limit, p.wait_hint_ns, kPair)) {
+          if (rr == role) {
+            if (!__all_sync(0xFFFFFFFFu,
+                            mbar_wait_bounded(smem_u32(&empty[stage]), phase ^ 1u, abort_flag,
+                                              status, kStatusProducerTimeout, limit,
+                                              p.wait_hint_ns, kPair))) {
               ok = false;
               break;
             }
@@ -1327,37 +1361,42 @@ __global__ void __launch_bounds__(kThreads, 1)
               const uint32_t fb = smem_u32(&full[stage]);
               const int n_b = ti.n0 + static_cast<int>(rank) * (p.bn / 2);
               if (rank == 0) {
-                mbar_arrive_expect_tx(fb, arm_tx);
-                tma_load_im2col_4d(smem_u32(a_ring + stage * a_bytes), amap, fb,
-                                   c_base + cb * p.bk, w0, h0, n_img,
-                                   static_cast<uint16_t>(uw * p.dil_w),
-                                   static_cast<uint16_t>(uh * p.dil_h));
-                tma_load_3d(smem_u32(b_ring + stage * b_bytes), &p.map_b, fb, bk_k, n_b, bz);
+                mbar_arrive_expect_tx_if(lead, fb, arm_tx);
+                tma_load_im2col_4d_if(lead, smem_u32(a_ring + stage * a_bytes), amap, fb,
+                                      c_base + cb * p.bk, w0, h0, n_img,
+                                      static_cast<uint16_t>(uw * p.dil_w),
+                                      static_cast<uint16_t>(uh * p.dil_h));
+                tma_load_3d_if(lead, smem_u32(b_ring + stage * b_bytes), &p.map_b, fb, bk_k, n_b,
+                               bz);
               } else {
                 const uint32_t fb0 = map_to_rank(fb, 0);
-                tma_load_im2col_4d_pair(smem_u32(a_ring + stage * a_bytes), amap, fb0,
-                                        c_base + cb * p.bk, w0, h0, n_img,
-                                        static_cast<uint16_t>(uw * p.dil_w),
-                                        static_cast<uint16_t>(uh * p.dil_h));
-                tma_load_3d_pair(smem_u32(b_ring + stage * b_bytes), &p.map_b, fb0, bk_k, n_b, bz);
+                tma_load_im2col_4d_pair_if(lead, smem_u32(a_ring + stage * a_bytes), amap, fb0,
+                                           c_base + cb * p.bk, w0, h0, n_img,
+                                           static_cast<uint16_t>(uw * p.dil_w),
+                                           static_cast<uint16_t>(uh * p.dil_h));
+                tma_load_3d_pair_if(lead, smem_u32(b_ring + stage * b_bytes), &p.map_b, fb0, bk_k,
+                                    n_b, bz);
               }
             } else if (!(p.fault_mode == 1 && blockIdx.x == 0 && seq == 0)) {
               // (fault_mode 1, a test hook: CTA 0 leaves its first stage un-armed.)
               const uint32_t fb = smem_u32(&full[stage]);
-              mbar_arrive_expect_tx(fb, stage_tx + (load_res ? b_bytes : 0u));
-              tma_load_im2col_4d(smem_u32(a_ring + stage * a_bytes), amap, fb, c_base + cb * p.bk,
-                                 w0, h0, n_img, static_cast<uint16_t>(uw * p.dil_w),
-                                 static_cast<uint16_t>(uh * p.dil_h));
+              mbar_arrive_expect_tx_if(lead, fb, stage_tx + (load_res ? b_bytes : 0u));
+              tma_load_im2col_4d_if(lead, smem_u32(a_ring + stage * a_bytes), amap, fb,
+                                    c_base + cb * p.bk, w0, h0, n_img,
+                                    static_cast<uint16_t>(uw * p.dil_w),
+                                    static_cast<uint16_t>(uh * p.dil_h));
               if (!p.b_resident)
-                tma_load_3d(smem_u32(b_ring + stage * b_bytes), &p.map_b, fb, bk_k, ti.n0, bz);
+                tma_load_3d_if(lead, smem_u32(b_ring + stage * b_bytes), &p.map_b, fb, bk_k, ti.n0,
+                               bz);
               else if (load_res)
-                tma_load_3d(smem_u32(b_res + kb * b_bytes), &p.map_b, fb, bk_k, 0, bz);
+                tma_load_3d_if(lead, smem_u32(b_res + kb * b_bytes), &p.map_b, fb, bk_k, 0, bz);
             }
             if (pf && pf_n >= 0)
-              tma_prefetch_im2col_4d(pf_map, c_base + cb * p.bk, pf_w0, pf_h0, pf_n,
-                                     static_cast<uint16_t>(uw * p.dil_w),
-                                     static_cast<uint16_t>(uh * p.dil_h));
+              tma_prefetch_im2col_4d_if(lead, pf_map, c_base + cb * p.bk, pf_w0, pf_h0, pf_n,
+                                        static_cast<uint16_t>(uw * p.dil_w),
+                                        static_cast<uint16_t>(uh * p.dil_h));
           }
+          if (++rr == nprod) rr = 0;
           if (++stage == stages) {
             stage = 0;
             phase ^= 1u;
@@ -1377,7 +1416,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // Let every copy this producer still has in flight land before exiting.
         // (A pair's rank-0 barriers count rank 1's copies too.)
         for (long long q = last_issued - stages + 1; q <= last_issued; ++q)
-          if (q >= 0 && (q & 1) == role)
+          if (q >= 0 && static_cast<int>(q % nprod) == role)
             mbar_wait_drain(smem_u32(&full[q % stages]), static_cast<uint32_t>((q / stages) & 1),
                             limit / 8 + 1);
       }
@@ -1386,11 +1425,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == 1 || warp == kProducer3Warp) {
     // ------------------------------------------------------------ MMA issuers
     // Warp 1 issues; with mma_split (two 128-row halves, no gather loader,
-    // no pair) warp 11 issues the second half's MMAs beside it: one thread
-    // cannot issue MMAs of N <= 128 as fast as the tensor core runs them
-    // (measured: 183 cycles per MMA with a barrier wait and commit per 4,
-    // 65 with two issuing warps).  (In a pair only rank 0 issues.)
-    if (lane == 0 && rank == 0) {
+    // no pair) warp 11 issues the second half's MMAs beside it.  Each issuer
+    // is a converged warp with one elected lane per MMA: a lone lane of a
+    // diverged warp issued one MMA every ~100 cycles (187 with a barrier
+    // wait and commit per 4), a converged warp keeps the tensor core busy
+    // (64 cycles per N = 128 MMA), but its per-k-block wait and commit still
+    // cost ~90 cycles, which the second warp hides for N <= 128.  (In a pair
+    // only rank 0 issues.)
+    if (rank == 0) {  // the whole warp: one elected lane issues each MMA
       bool ok;
       const int ks = static_cast<int>(sw / 32);
       const int half = p.mma_split ? (warp == 1 ? 0 : 1) : -1;
@@ -1404,7 +1446,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                                 tempty, half, abort_flag, status, limit, tile0,
                                                 tile_step);
         if (!ok) {
-          mma_commit(smem_u32(my_drain));
+          mma_commit_warp(smem_u32(my_drain));
           mbar_wait_drain(smem_u32(my_drain), 0, limit / 8 + 1);
         }
       } else {
@@ -1420,9 +1462,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!ok) {
         // Every MMA already issued must finish before TMEM is released.
         if (kPair)
-          mma_commit_pair(smem_u32(my_drain));
+          mma_commit_pair_warp(smem_u32(my_drain));
         else
-          mma_commit(smem_u32(my_drain));
+          mma_commit_warp(smem_u32(my_drain));
         mbar_wait_drain(smem_u32(my_drain), 0, limit / 8 + 1);
       }
       }
