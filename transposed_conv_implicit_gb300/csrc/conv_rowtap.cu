@@ -78,13 +78,14 @@ __device__ __forceinline__ RtTile rt_decode(const RowTapParams& p, int t) {
   return ti;
 }
 
+// Issued from the converged MMA warp: one elected lane issues.
 template <int kKind>
 __device__ __forceinline__ void rt_mma(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc,
                                        uint32_t accumulate) {
   if (kKind == kKindF16)
-    mma_f16(d, a, b, idesc, accumulate);
+    mma_f16_warp(d, a, b, idesc, accumulate);
   else
-    mma_f8(d, a, b, idesc, accumulate);
+    mma_f8_warp(d, a, b, idesc, accumulate);
 }
 
 // bar.sync over `count` threads that also ANDs a predicate across them, so
@@ -175,15 +176,17 @@ __global__ void __launch_bounds__(kRtThreads, 1)
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
-    if (lane == 0) {
+    // The whole warp walks the loads (warp-uniform operands); lane 0 issues.
+    {
+      const uint32_t lead = lane == 0 ? 1u : 0u;
       bool ok = true;
       const uint32_t b_blk = static_cast<uint32_t>(brows) * 128u;
-      mbar_arrive_expect_tx(smem_u32(bres_full),
-                            static_cast<uint32_t>(p.c_blocks * p.R * sf) * 128u);
+      mbar_arrive_expect_tx_if(lead, smem_u32(bres_full),
+                               static_cast<uint32_t>(p.c_blocks * p.R * sf) * 128u);
       for (int cb = 0; cb < p.c_blocks; ++cb)
         for (int r = 0; r < p.R; ++r)
-          tma_load_4d(smem_u32(b_res + cb * b_blk + r * p.g16 * 128), &p.map_w,
-                      smem_u32(bres_full), cb * bk, 0, r, 0);
+          tma_load_4d_if(lead, smem_u32(b_res + cb * b_blk + r * p.g16 * 128), &p.map_w,
+                         smem_u32(bres_full), cb * bk, 0, r, 0);
       int stage = 0;
       uint32_t phase = 0;
       long long issued = 0;
@@ -193,17 +196,18 @@ __global__ void __launch_bounds__(kRtThreads, 1)
         for (int k = 0; ok && k < kin; ++k) {
           const int iy = ti.oy0 - p.pad_h + k;  // rows outside the image arrive as zeros
           for (int cb = 0; cb < p.c_blocks; ++cb) {
-            if (!mbar_wait_bounded(smem_u32(&empty[stage]), phase ^ 1u, abort_flag, status,
-                                   kStatusProducerTimeout, limit)) {
+            if (!__all_sync(0xFFFFFFFFu,
+                            mbar_wait_bounded(smem_u32(&empty[stage]), phase ^ 1u, abort_flag,
+                                              status, kStatusProducerTimeout, limit))) {
               ok = false;
               break;
             }
             const uint32_t fb = smem_u32(&full[stage]);
             // (fault_mode 1, a test hook: CTA 0 leaves its first stage un-armed.)
             if (!(p.fault_mode == 1 && blockIdx.x == 0 && issued == 0)) {
-              mbar_arrive_expect_tx(fb, kRtStageBytes);
-              tma_load_4d(smem_u32(a_ring + stage * kRtStageBytes), &p.map_x, fb, cb * bk,
-                          ti.x0 - p.pad_w, iy, ti.n);
+              mbar_arrive_expect_tx_if(lead, fb, kRtStageBytes);
+              tma_load_4d_if(lead, smem_u32(a_ring + stage * kRtStageBytes), &p.map_x, fb,
+                             cb * bk, ti.x0 - p.pad_w, iy, ti.n);
             }
             ++issued;
             if (++stage == stages) {
@@ -225,9 +229,10 @@ __global__ void __launch_bounds__(kRtThreads, 1)
     __syncwarp();
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
-      bool ok = mbar_wait_bounded(smem_u32(bres_full), 0, abort_flag, status, kStatusMmaTimeout,
-                                  limit);
+    // The converged warp walks the MMAs; one elected lane issues each.
+    {
+      bool ok = __all_sync(0xFFFFFFFFu, mbar_wait_bounded(smem_u32(bres_full), 0, abort_flag,
+                                                          status, kStatusMmaTimeout, limit));
       tc_fence_after();
       const uint64_t desc_hi = smem_desc_kmajor(0, 128);
       const uint32_t a_lo0 = smem_u32(a_ring) >> 4;
@@ -245,8 +250,10 @@ __global__ void __launch_bounds__(kRtThreads, 1)
       for (int t = blockIdx.x; ok && t < total_tiles; t += gridDim.x, ++it) {
         const RtTile ti = rt_decode(p, t);
         const int buf = it & 1;
-        if (!mbar_wait_bounded(smem_u32(&tempty[buf]), static_cast<uint32_t>(((it >> 1) & 1) ^ 1),
-                               abort_flag, status, kStatusMmaTimeout, limit)) {
+        if (!__all_sync(0xFFFFFFFFu,
+                        mbar_wait_bounded(smem_u32(&tempty[buf]),
+                                          static_cast<uint32_t>(((it >> 1) & 1) ^ 1), abort_flag,
+                                          status, kStatusMmaTimeout, limit))) {
           ok = false;
           break;
         }
@@ -257,8 +264,9 @@ __global__ void __launch_bounds__(kRtThreads, 1)
           // Output row k's column; the MMA's R groups cover rows k .. k-R+1.
           const uint32_t d = base + g16 * static_cast<uint32_t>(kin - 1 - k);
           for (int cb = 0; cb < c_blocks; ++cb) {
-            if (!mbar_wait_bounded(smem_u32(&full[stage]), phase, abort_flag, status,
-                                   kStatusMmaTimeout, limit)) {
+            if (!__all_sync(0xFFFFFFFFu, mbar_wait_bounded(smem_u32(&full[stage]), phase,
+                                                           abort_flag, status, kStatusMmaTimeout,
+                                                           limit))) {
               ok = false;
               break;
             }
@@ -278,22 +286,23 @@ __global__ void __launch_bounds__(kRtThreads, 1)
                 rt_mma<kKind>(d, a, b, idesc_all, 1u);
               }
             }
-            mma_commit(smem_u32(&empty[stage]));
+            mma_commit_warp(smem_u32(&empty[stage]));
             if (++stage == stages) {
               stage = 0;
               phase ^= 1u;
             }
           }
-          if (ok && k >= R - 1) mma_commit(smem_u32(&rowfull[buf * kRowTapMaxBand + k - (R - 1)]));
+          if (ok && k >= R - 1)
+            mma_commit_warp(smem_u32(&rowfull[buf * kRowTapMaxBand + k - (R - 1)]));
         }
         // A short band (the image's last) still completes every row barrier
         // of the buffer once, so that their phases stay in step with its uses.
         for (int q = ti.rows; ok && q < band; ++q)
-          mma_commit(smem_u32(&rowfull[buf * kRowTapMaxBand + q]));
+          mma_commit_warp(smem_u32(&rowfull[buf * kRowTapMaxBand + q]));
       }
       if (!ok) {
         // Every MMA already issued must finish before TMEM is released.
-        mma_commit(smem_u32(drain));
+        mma_commit_warp(smem_u32(drain));
         mbar_wait_drain(smem_u32(drain), 0, limit / 8 + 1);
       }
     }
