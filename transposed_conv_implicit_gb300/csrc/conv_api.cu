@@ -440,14 +440,14 @@ void choose_tiling(Plan* pl, const long long rows[], int num_phases, int max_kbl
 // CTA pairs (cta_group::2): a cluster of two CTAs shares each 256-row tile;
 // each CTA loads its 128 rows of A and half of the tile's bn filter rows, so
 // per SM the filter bytes written into shared memory halve (measured: the
-// VAE 3x3 512->512 conv, bn = 256, 194.6 -> 181.3 us).  The gain is that
-// share of the shared-memory traffic, so the default takes pairs only for
-// filter-heavy tiles (bn = 256: B twice the A bytes per k-block; the fp8
-// 3x3 320->320 conv at bn = 160 ran no faster) and only when every pair gets
-// at least 4 tiles (pairs halve the tile slots: convs with under two waves of
-// 256-row tiles ran 12-30% slower).  For the TMA im2col loader with a
-// streamed filter and one channel group.  CONV_PAIR=1 forces pairs where
-// they apply, 0 forbids them.
+// VAE 3x3 512->512 conv, bn = 256, 194.6 -> 181.3 us; the fp8 3x3 320->320
+// conv, bn = 160, 64.5 -> 61.7 us).  The gain is that share of the
+// shared-memory traffic, so the default takes pairs only for filter-heavy
+// tiles (bn > 128: B more than the A bytes per k-block; 256-row tiles of
+// bn = 128 ran 12-30% slower as pairs) and only when every pair gets at
+// least 4 tiles (pairs halve the tile slots).  For the TMA im2col loader
+// with a streamed filter and one channel group.  CONV_PAIR=1 forces pairs
+// where they apply, 0 forbids them.
 void plan_pair(Plan* pl, int num_sms) {
   ConvKernelParams& kp = pl->kp;
   kp.pair = 0;
@@ -458,7 +458,7 @@ void plan_pair(Plan* pl, int num_sms) {
   int tile = 0;
   for (int ph = 0; ph < kp.num_phases; ++ph)
     tile += ((kp.rows[ph] + tile_m - 1) / tile_m) * kp.n_tiles;
-  if (force != 1 && (kp.bn < 2 * kBM || tile < 4 * std::max(num_sms / 2, 1))) return;
+  if (force != 1 && (kp.bn <= kBM || tile < 4 * std::max(num_sms / 2, 1))) return;
   kp.pair = 1;
   kp.m_halves = 1;
   tile = 0;
