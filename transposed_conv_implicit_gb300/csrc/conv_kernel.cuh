@@ -1502,6 +1502,27 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint8_t* stg_grp = stg_base + grp * (p.stg_bufs * chunk_bytes);
       int store_seq = 0;
       int src_issued[2] = {0, 0};  // source loads issued per buffer (leader only)
+      if (!in_place) {
+        // While the first tile's MMAs run, pass zeros through this
+        // epilogue's row code into the (still unused) staging buffer: its
+        // instructions are then cached when the first accumulator lands.  A
+        // conv of one tile per CTA otherwise fetches them cold at its end.
+        uint32_t zeros[64];
+#pragma unroll
+        for (int k = 0; k < 64; ++k) zeros[k] = 0u;
+        if (row < p.valid_rows) {
+          if (p.cw == 64)
+            process_row_act<OutT, 64>(zeros, stg_grp, static_cast<uint32_t>(row), p.beta,
+                                      p.epilogue, false);
+          else if (p.cw == 32)
+            process_row_act<OutT, 32>(zeros, stg_grp, static_cast<uint32_t>(row), p.beta,
+                                      p.epilogue, false);
+          else
+            process_row_act<OutT, 16>(zeros, stg_grp, static_cast<uint32_t>(row), p.beta,
+                                      p.epilogue, false);
+        }
+        named_barrier(bar_id, 128);
+      }
       // Work items in order; the source prefetch peeks at the next one.
       WorkWalk walk = work_begin<kStreamK>(p, tile0, tile_step);
       Work cur{};
