@@ -607,7 +607,6 @@ __device__ __forceinline__ bool mma_role(const ConvKernelParams& p, uint32_t tme
   uint32_t a_lo = a_lo0;
   uint32_t bs_lo = b_lo0;  // streamed B: advances with the ring
   bool ok = true;
-  bool ahead_ready = false;  // the look-ahead test found the current stage landed
   int it = 0;
   (void)total_tiles;
   WorkWalk walk = work_begin<kStreamK>(p, t0, step);
@@ -638,22 +637,13 @@ __device__ __forceinline__ bool mma_role(const ConvKernelParams& p, uint32_t tme
     uint32_t br_lo = b_lo0 + static_cast<uint32_t>(wk.kb0) * b_step;
     const int kblocks = wk.kb1 - wk.kb0;
     for (int kb = 0; kb < kblocks; ++kb) {
-      if (!ahead_ready &&
-          !__all_sync(0xFFFFFFFFu, mbar_wait_bounded(full0 + 8u * stage, phase, abort_flag,
+      if (!__all_sync(0xFFFFFFFFu, mbar_wait_bounded(full0 + 8u * stage, phase, abort_flag,
                                                      status, kStatusMmaTimeout, limit, 0u,
                                                      kPair))) {
         ok = false;
         break;
       }
       tc_fence_after();
-      // Test the next stage now: the test's latency overlaps this k-block's
-      // issue, and a stage already landed then needs no blocking wait.
-      {
-        const bool wrap = stage + 1 == stages;
-        const uint32_t nbar = full0 + (wrap ? 0u : 8u * (stage + 1));
-        const uint32_t nphase = wrap ? phase ^ 1u : phase;
-        ahead_ready = kPair ? mbar_test_wait_cluster(nbar, nphase) : mbar_test_wait(nbar, nphase);
-      }
       issue_kblock<kKind, kSteps, kHalves, kPair>(d_tmem, desc_hi, a_lo,
                                                   b_resident ? br_lo : bs_lo, half_lo, bn_cols,
                                                   idesc, kb != 0 ? 1u : 0u);
@@ -661,7 +651,6 @@ __device__ __forceinline__ bool mma_role(const ConvKernelParams& p, uint32_t tme
         mma_commit_pair_warp(empty0 + 8u * stage);
       else
         mma_commit_warp(empty0 + 8u * stage);
-      ahead_ready = __all_sync(0xFFFFFFFFu, ahead_ready);
       br_lo += b_step;
       a_lo += a_step;
       bs_lo += b_step;

@@ -96,35 +96,6 @@ __device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t par
   return done != 0;
 }
 
-// Non-blocking test of a phase: returns at once whether it has completed
-// (with the acquire of a completed wait when it has).  The MMA issuer tests
-// the next ring stage this way before issuing the current stage's MMAs, so
-// the test's latency overlaps the issue instead of preceding it.
-__device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
-  uint32_t done;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(done)
-      : "r"(bar), "r"(parity)
-      : "memory");
-  return done != 0;
-}
-
-// Same with cluster-scope acquire (phases completed by the peer of a pair).
-__device__ __forceinline__ bool mbar_test_wait_cluster(uint32_t bar, uint32_t parity) {
-  uint32_t done;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.test_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(done)
-      : "r"(bar), "r"(parity)
-      : "memory");
-  return done != 0;
-}
-
 // Wait for the phase with the given parity to complete, for at most
 // `limit_cycles` SM cycles.  Returns false (and raises the CTA's abort flag
 // and the device status bit `code`) when the limit runs out, or false at once
