@@ -1210,12 +1210,16 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (kPair) cluster_sync();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
-  // Set-up above may overlap the previous kernel in the stream; every global
-  // memory access below comes after that kernel has completed.
-  grid_dependency_wait();
+  // Set-up above may overlap the previous kernel in the stream.  Every role
+  // waits for that kernel to complete before its first global memory access
+  // or bounded wait; a TMA producer waits only right before its first copy,
+  // so walking to it (parameters only, no memory) overlaps that kernel too.
   grid_launch_dependents();
 
   const bool split_issuer = !kGather && !kPair && p.mma_split;  // warp 11 issues MMAs
+  const bool tma_producer =
+      !kGather && (warp == 0 || warp == kProducer2Warp || (warp == kProducer3Warp && !split_issuer));
+  if (!tma_producer) grid_dependency_wait();
   if (warp == 0 || warp == kProducer2Warp || (warp == kProducer3Warp && !split_issuer)) {
     // ------------------------------------------------------------ producers
     // The producer warps walk the same k-block sequence; with the TMA loaders
@@ -1236,6 +1240,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int nprod = split_issuer ? 2 : 3;
       const int role = warp == 0 ? 0 : (warp == kProducer2Warp ? 1 : 2);
       int rr = 0;  // seq % nprod
+      bool dep_done = false;  // grid_dependency_wait() passed
       int stage = 0;
       uint32_t phase = 0;
       long long seq = 0;
@@ -1259,6 +1264,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                                                 p.wait_hint_ns))) {
                 ok = false;
                 break;
+              }
+              if (!dep_done) {
+                grid_dependency_wait();
+                dep_done = true;
               }
               last_issued = seq;
               if (!(p.fault_mode == 1 && blockIdx.x == 0 && seq == 0)) {
@@ -1341,6 +1350,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                                               p.wait_hint_ns, kPair))) {
               ok = false;
               break;
+            }
+            if (!dep_done) {
+              grid_dependency_wait();
+              dep_done = true;
             }
             last_issued = seq;
             if (kPair && p.fault_mode == 1 && tile0 == 0 && seq == 0) {
