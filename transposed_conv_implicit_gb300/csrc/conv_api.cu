@@ -53,6 +53,7 @@ struct Tuning {
   int pair;             // -1 when unset
   int streamk;          // -1 when unset
   int mma_split;        // 0 disables the second MMA issuer
+  int rowtap_blocks;    // row-tap A stage: 1 = one channel block, 0 = the planner's choice
   uint32_t wait_hint_ns;
 };
 
@@ -81,6 +82,7 @@ Tuning read_tuning() {
   t.pair = env_int_or("CONV_PAIR", -1);
   t.streamk = env_int_or("CONV_STREAMK", -1);
   t.mma_split = env_int_or("CONV_MMA_SPLIT", 1);
+  t.rowtap_blocks = env_int("CONV_ROWTAP_BLOCKS");
   t.wait_hint_ns = static_cast<uint32_t>(env_int("CONV_WAIT_HINT_NS"));
   return t;
 }
@@ -1544,14 +1546,21 @@ bool plan_rowtap(const FwdShape& f, int groups, int num_sms, RowTapPlan* out) {
   rp.cols_per_buf = static_cast<uint32_t>(g16 * (best + 2 * f.r - 2));
   rp.tmem_cols = next_pow2_cols(static_cast<int>(2 * rp.cols_per_buf));
   // Shared memory: the A ring at 0, the resident filter, the epilogue's
-  // exchange buffers (two groups x two rows), the barriers.
-  const size_t stage_bytes = 128 * 128;
+  // exchange buffers (two groups x two rows), the barriers.  An A stage holds
+  // every channel block of one input row segment when four such stages fit
+  // (one wait and one commit per input row instead of per block: the RGB
+  // head's MMA warp spent ~560 cycles per 16 KB stage), else one block.
+  const size_t blk_bytes = 128 * 128;
   const size_t b_bytes = static_cast<size_t>(rp.c_blocks) * f.r * g16 * 128;
   const size_t part_bytes = static_cast<size_t>(2 * 2) * g16 * 128 * sizeof(float);
   // Row-segment stages of the epilogue: output and source, per group.
   const int seg_stage = static_cast<int>((static_cast<size_t>(128) * f.c_out * 2 + 16 + 15) & ~size_t(15));
   const size_t seg_bytes = static_cast<size_t>(4) * seg_stage;
   const size_t fixed = 1024 + align1k(b_bytes) + align1k(part_bytes) + align1k(seg_bytes) + 1024;
+  int blocks = rp.c_blocks;
+  if (tuning().rowtap_blocks == 1 || fixed + 4 * blocks * blk_bytes > kSmemLimit) blocks = 1;
+  const size_t stage_bytes = blocks * blk_bytes;
+  rp.blocks_per_stage = blocks;
   if (fixed + 2 * stage_bytes > kSmemLimit) return false;
   rp.stages = static_cast<int>(std::min<size_t>(kMaxStages, (kSmemLimit - fixed) / stage_bytes));
   rp.off_b = static_cast<uint32_t>(rp.stages * stage_bytes);

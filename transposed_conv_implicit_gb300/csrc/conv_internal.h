@@ -66,6 +66,7 @@ struct RowTapParams {  // aligned like CUtensorMap
   int seg_w;           // output columns per tile: 128 - (S - 1)
   int n_seg, n_band, total_tiles;
   int stages;
+  int blocks_per_stage;  // channel blocks of one input row segment per A stage (1 or c_blocks)
   uint32_t idesc_all;  // N = R * g16
   uint32_t idesc_one;  // N = g16
   uint32_t idesc_rest; // N = (R - 1) * g16 (R > 1)

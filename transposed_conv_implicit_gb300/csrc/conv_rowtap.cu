@@ -190,12 +190,14 @@ __global__ void __launch_bounds__(kRtThreads, 1)
       int stage = 0;
       uint32_t phase = 0;
       long long issued = 0;
+      const int bps = p.blocks_per_stage;
+      const uint32_t stage_bytes = static_cast<uint32_t>(bps) * kRtStageBytes;
       for (int t = blockIdx.x; ok && t < p.total_tiles; t += gridDim.x) {
         const RtTile ti = rt_decode(p, t);
         const int kin = ti.rows + p.R - 1;
         for (int k = 0; ok && k < kin; ++k) {
           const int iy = ti.oy0 - p.pad_h + k;  // rows outside the image arrive as zeros
-          for (int cb = 0; cb < p.c_blocks; ++cb) {
+          for (int cb0 = 0; cb0 < p.c_blocks; cb0 += bps) {
             if (!__all_sync(0xFFFFFFFFu,
                             mbar_wait_bounded(smem_u32(&empty[stage]), phase ^ 1u, abort_flag,
                                               status, kStatusProducerTimeout, limit))) {
@@ -205,9 +207,10 @@ __global__ void __launch_bounds__(kRtThreads, 1)
             const uint32_t fb = smem_u32(&full[stage]);
             // (fault_mode 1, a test hook: CTA 0 leaves its first stage un-armed.)
             if (!(p.fault_mode == 1 && blockIdx.x == 0 && issued == 0)) {
-              mbar_arrive_expect_tx_if(lead, fb, kRtStageBytes);
-              tma_load_4d_if(lead, smem_u32(a_ring + stage * kRtStageBytes), &p.map_x, fb,
-                             cb * bk, ti.x0 - p.pad_w, iy, ti.n);
+              mbar_arrive_expect_tx_if(lead, fb, stage_bytes);
+              for (int i = 0; i < bps; ++i)
+                tma_load_4d_if(lead, smem_u32(a_ring + stage * stage_bytes + i * kRtStageBytes),
+                               &p.map_x, fb, (cb0 + i) * bk, ti.x0 - p.pad_w, iy, ti.n);
             }
             ++issued;
             if (++stage == stages) {
@@ -243,6 +246,8 @@ __global__ void __launch_bounds__(kRtThreads, 1)
       const uint32_t idesc_all = p.idesc_all, idesc_one = p.idesc_one, idesc_rest = p.idesc_rest;
       const bool multi_row = p.R > 1;
       const int R = p.R, c_blocks = p.c_blocks, total_tiles = p.total_tiles, band = p.band;
+      const int bps = p.blocks_per_stage;
+      const uint32_t stage_lo = (static_cast<uint32_t>(bps) * kRtStageBytes) >> 4;
       const uint32_t cols_per_buf = p.cols_per_buf;
       int stage = 0;
       uint32_t phase = 0;
@@ -263,7 +268,7 @@ __global__ void __launch_bounds__(kRtThreads, 1)
         for (int k = 0; ok && k < kin; ++k) {
           // Output row k's column; the MMA's R groups cover rows k .. k-R+1.
           const uint32_t d = base + g16 * static_cast<uint32_t>(kin - 1 - k);
-          for (int cb = 0; cb < c_blocks; ++cb) {
+          for (int cb0 = 0; cb0 < c_blocks; cb0 += bps) {
             if (!__all_sync(0xFFFFFFFFu, mbar_wait_bounded(smem_u32(&full[stage]), phase,
                                                            abort_flag, status, kStatusMmaTimeout,
                                                            limit))) {
@@ -271,19 +276,23 @@ __global__ void __launch_bounds__(kRtThreads, 1)
               break;
             }
             tc_fence_after();
-            const uint32_t a_lo = a_lo0 + static_cast<uint32_t>(stage) * (kRtStageBytes >> 4);
-            const uint32_t b_lo = b_lo0 + static_cast<uint32_t>(cb) * b_blk;
+            for (int i = 0; i < bps; ++i) {
+              const int cb = cb0 + i;
+              const uint32_t a_lo = a_lo0 + static_cast<uint32_t>(stage) * stage_lo +
+                                    static_cast<uint32_t>(i) * (kRtStageBytes >> 4);
+              const uint32_t b_lo = b_lo0 + static_cast<uint32_t>(cb) * b_blk;
 #pragma unroll
-            for (int kk = 0; kk < 4; ++kk) {
-              const uint64_t a = desc_hi | static_cast<uint64_t>(a_lo + 2u * kk);
-              const uint64_t b = desc_hi | static_cast<uint64_t>(b_lo + 2u * kk);
-              if (kk == 0 && cb == 0) {
-                rt_mma<kKind>(d, a, b, idesc_one, 0u);  // output row k: first product
-                if (multi_row)
-                  rt_mma<kKind>(d + g16, a, desc_hi | static_cast<uint64_t>(b_lo + g_lo),
-                                idesc_rest, 1u);
-              } else {
-                rt_mma<kKind>(d, a, b, idesc_all, 1u);
+              for (int kk = 0; kk < 4; ++kk) {
+                const uint64_t a = desc_hi | static_cast<uint64_t>(a_lo + 2u * kk);
+                const uint64_t b = desc_hi | static_cast<uint64_t>(b_lo + 2u * kk);
+                if (kk == 0 && cb == 0) {
+                  rt_mma<kKind>(d, a, b, idesc_one, 0u);  // output row k: first product
+                  if (multi_row)
+                    rt_mma<kKind>(d + g16, a, desc_hi | static_cast<uint64_t>(b_lo + g_lo),
+                                  idesc_rest, 1u);
+                } else {
+                  rt_mma<kKind>(d, a, b, idesc_all, 1u);
+                }
               }
             }
             mma_commit_warp(smem_u32(&empty[stage]));
