@@ -56,8 +56,9 @@ conv_status_t conv_testing_im2col_tile(const void* input, int n, int h, int w, i
  * out[9] = residual source buffers, out[10] = output staging buffers,
  * out[11] = A loader (0 TMA im2col, 1 row window, 2 gather, 3 row-tap).  For
  * the row-tap kernel (few output channels: the filter taps along S and the
- * output channels share the MMA's N) out[0] = R * g16 (MMA width), out[10] =
- * output rows per tile.  out[12] = 1 when CTA pairs (clusters of two CTAs
+ * output channels share the MMA's N) out[0] = R * g16 (MMA width), out[9] =
+ * 128-byte channel blocks per A stage (all of an input row segment's, or
+ * one), out[10] = output rows per tile.  out[12] = 1 when CTA pairs (clusters of two CTAs
  * sharing 256-row tiles through cta_group::2 MMAs) run the conv.  out[13] = 1
  * when the stream-K schedule runs it.  Host-only. */
 conv_status_t conv_testing_fwd_plan(int n, int h, int w, int c_in, conv_dtype_t dtype, int r,

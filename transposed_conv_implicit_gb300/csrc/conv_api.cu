@@ -2323,7 +2323,7 @@ conv_status_t conv_testing_fwd_plan(int n, int h, int w, int c_in, conv_dtype_t 
     out[6] = static_cast<int>(rp.tmem_cols);
     out[7] = 0;
     out[8] = 1;
-    out[9] = 0;
+    out[9] = rp.blocks_per_stage;
     out[10] = rp.band;
     out[11] = 3;
     out[12] = 0;
