@@ -1219,7 +1219,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   const bool split_issuer = !kGather && !kPair && p.mma_split;  // warp 11 issues MMAs
   const bool tma_producer =
       !kGather && (warp == 0 || warp == kProducer2Warp || (warp == kProducer3Warp && !split_issuer));
-  const bool staged_epilogue = warp >= 2 && warp < 2 + kEpilogueWarps && p.epi_mode != 0;
+  // (Not with the gather loader: its builder warps ran the RGB stem 78 -> 85
+  // us when the epilogue warps waited after their zero pass.)
+  const bool staged_epilogue =
+      !kGather && warp >= 2 && warp < 2 + kEpilogueWarps && p.epi_mode != 0;
   if (!tma_producer && !staged_epilogue) grid_dependency_wait();
   if (warp == 0 || warp == kProducer2Warp || (warp == kProducer3Warp && !split_issuer)) {
     // ------------------------------------------------------------ producers
@@ -1526,7 +1529,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         named_barrier(bar_id, 128);
       }
-      grid_dependency_wait();  // (the pass above touched shared memory only)
+      if (!kGather) grid_dependency_wait();  // (the pass above touched shared memory only)
       // Work items in order; the source prefetch peeks at the next one.
       WorkWalk walk = work_begin<kStreamK>(p, tile0, tile_step);
       Work cur{};
