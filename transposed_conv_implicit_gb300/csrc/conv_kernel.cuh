@@ -1675,7 +1675,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       }
-      if (leader) bulk_wait_all();
+      // Before the CTA exits, its stores must have read their shared-memory
+      // sources; their global writes complete with the grid (a dependent
+      // kernel's griddepcontrol.wait sees them).
+      if (leader) bulk_wait_read_all();
       // On abort, source loads issued for tiles never processed must land
       // before the CTA exits: wait for the latest phase of each buffer.
       if (leader && p.has_residual && *abort_flag && grp < nitems) {
