@@ -290,6 +290,32 @@ def test_cta_pair_every_element(case, tuning):
         H.assert_parity(case, inp, got, ref)
 
 
+# One MMA warp for both 128-row halves of a 256-row tile (CONV_MMA_SPLIT=0):
+# the converged warp issues the two halves' MMAs of every K-step itself,
+# instead of warps 1 and 11 taking one half each.
+SPLIT_OFF_CASES = ("b_3x3_s2p1", "h_5x5_s2p2", "b_cout17_res", "int_b_3x3", "int_h_5x5",
+                   "int_b_s2_res", "t_h_4x4_s2p1_relu", "t_h_5x5_s2p2_res")
+
+
+def _split_off_cases():
+    return [c for c in SMALL_FWD + SMALL_TR + INT_CASES if c.name in SPLIT_OFF_CASES]
+
+
+@pytest.mark.parametrize("case", _split_off_cases(), ids=lambda c: c.name)
+def test_single_mma_warp_for_both_halves(case, tuning):
+    tuning("CONV_MMA_SPLIT", "0")
+    inp = synthetic.make_inputs(case)
+    out = H.run_gpu(case, inp)
+    torch.cuda.synchronize()
+    got = H.decode(out.cpu(), case.out_dtype)
+    ref = H.oracle_full(case, inp)
+    if case.name.startswith("int_"):
+        mism = np.argwhere(got != ref)
+        assert mism.size == 0, mism[:5].tolist()
+    else:
+        H.assert_parity(case, inp, got, ref)
+
+
 # Stream-K forced on (CONV_STREAMK=1, a workspace with room for its partial
 # tiles).  On these small convs most SMs hold one or two k-blocks of the
 # iteration sequence, so every tile is split between several CTAs: the
