@@ -338,15 +338,15 @@ def test_measured_planner_choices(lib, tuning):
     """Plans the measurements picked (each alternative was timed on GB300 and
     ran slower): 256-row gather tiles for the RGB stem (77.8 vs 90.1 us on
     128-row tiles), CTA pairs for the fp8 conv's 160-column tiles (64.5 vs
-    61.7 us; each CTA's 26 KB stages leave room for 5 stages and two residual
-    buffers), 256-row bn = 128 tiles for the wave-quantised fwd5x5 (128-row:
-    30.5 vs 27.0 us; CTA pairs 31.2)."""
+    61.7 us) with a 7-stage ring and one residual buffer (5 stages and two
+    buffers: 60.8 vs 59.3 us), 256-row bn = 128 tiles for the wave-quantised
+    fwd5x5 (128-row: 30.5 vs 27.0 us; CTA pairs 31.2)."""
     for name in ("CONV_TILE_M", "CONV_TILE_N", "CONV_PAIR", "CONV_SRC_BUFS", "CONV_MAX_STAGES"):
         tuning(name, None)
     stem = _plan(lib, 32, 224, 224, 3, BF16, 7, 64, 2, 3, sms=152)
     assert (stem["loader"], stem["tiles"], stem["tmem"]) == (2, 32 * 112 * 112 // 256, 256)
     fp8 = _plan(lib, 16, 64, 64, 320, F8, 3, 320, 1, 1, res=1, sms=152)
-    assert (fp8["stages"], fp8["srcb"], fp8["pair"]) == (5, 2, 1)
+    assert (fp8["stages"], fp8["srcb"], fp8["pair"]) == (7, 1, 1)
     f5 = _plan(lib, 8, 128, 128, 128, F16, 5, 128, 2, 2, sms=152)
     assert (f5["bn"], f5["tiles"], f5["pair"]) == (128, 128, 0)
     tuning("CONV_SRC_BUFS", "1")   # the override still caps the buffers

@@ -1205,10 +1205,11 @@ conv_status_t layout_memory(Plan* pl, int has_residual) {
     double key = load;
     if (st < 3) key += 1e6;
     if (opts[i].srcb < srcb_max) key += 50.0;
-    // Below 5 stages a deeper ring beats the second source buffer (fp8 3x3
-    // 320->320 with a residual: 4 stages and two source buffers 75.8 us,
-    // 5 stages and one 73.7 us).
-    if (st < 5) key += 60.0;
+    // Below 6 stages a deeper ring beats the second source buffer (fp8 3x3
+    // 320->320 with a residual: 4 stages and two source buffers 75.8 us
+    // against 5 stages and one 73.7 us; on CTA pairs 5 stages and two
+    // buffers 60.8 us against 7 stages and one 59.3 us).
+    if (st < 6) key += 60.0;
     key -= 0.01 * st;
     if (key < best_key) {
       best_key = key;
