@@ -294,7 +294,9 @@ def test_cta_pair_every_element(case, tuning):
 # the converged warp issues the two halves' MMAs of every K-step itself,
 # instead of warps 1 and 11 taking one half each.
 SPLIT_OFF_CASES = ("b_3x3_s2p1", "h_5x5_s2p2", "b_cout17_res", "int_b_3x3", "int_h_5x5",
-                   "int_b_s2_res", "t_h_4x4_s2p1_relu", "t_h_5x5_s2p2_res")
+                   "int_b_s2_res", "t_h_4x4_s2p1_relu", "t_h_5x5_s2p2_res",
+                   # the row-window loader's MMA role, both halves from one warp
+                   "b_res_relu", "b_window_rowblocks_res", "h_res_silu")
 
 
 def _split_off_cases():
