@@ -20,9 +20,13 @@ all its tensors (input, packed filter, source, output) that together exceed
 L2 in place of a flush); the stream is bracketed by CUDA events on the launch
 stream and the per-launch time is its event time over the launches.  The
 tiny conv, too small for that, is timed alone after an L2 flush (a write of
-max(2 x L2, 256 MiB)) outside its events.  The step time is the sum of the
-convs' per-launch times; ``per_kernel`` also reports each conv alone after a
-flush (``us_isolated``: that includes the launch latency a stream hides).
+max(2 x L2, 256 MiB)) outside its events.  Each conv's events follow one
+untimed launch of the same conv (of its stream's last copy; for the tiny
+conv, before the flush), so its code is warm while its operands come from
+HBM.  The step time is the sum of the convs' per-launch times; ``per_kernel``
+also reports each conv alone after a flush, right after a different conv
+(``us_isolated``: that includes the launch latency a stream hides and the
+kernel's code fetched cold).
 ``value`` is the step's algorithmic FLOPs over the step time (whole job: all
 ranks' FLOPs over the slowest rank's time); ``per_kernel`` gives each conv's
 time, TFLOP/s, GB/s and fraction of its own roofline; ``roofline`` is the
@@ -440,14 +444,20 @@ def run_ours(args, world, rank, local):
         then the convs back to back inside one pair of events (a conv may set
         up while the previous one drains: programmatic dependent launch)."""
         if per_conv_flush:
+            # Each conv's events follow one untimed launch of the same conv,
+            # so its kernel's code is warm (after another kernel, and with L2
+            # flushed, that code would be fetched from HBM: up to ~8 us on
+            # the tiny conv); its operands still come from HBM.
             for i, (e0, e1) in enumerate(evs):
                 group = rotate_sets[i]
                 if group is None:
+                    calls[i]()
                     flush.fill_(1)
                     e0.record(stream)
                     calls[i]()
                     e1.record(stream)
                 else:
+                    group[-1]()
                     e0.record(stream)
                     for call in group:
                         call()
@@ -615,7 +625,9 @@ def run_ours(args, world, rank, local):
         "config": {"workload": args.workload + ": " + describe(cases),
                    "l2": ("inputs larger than L2: each conv streams over rotating copies of "
                           "its tensors totalling >= 3 x L2 (%d MiB); a conv too small for that "
-                          "runs after a flush (write of %d MiB) outside its events"
+                          "runs after a flush (write of %d MiB) outside its events; each "
+                          "conv's events follow one untimed launch of the same conv (its code "
+                          "warm, its operands not)"
                           % (3 * l2 >> 20, flush.numel() >> 20)) if per_conv_flush else
                          "flushed before every step (write of %d MiB), flush outside the events"
                          % (flush.numel() >> 20),
@@ -627,7 +639,8 @@ def run_ours(args, world, rank, local):
         "roofline": roof,
         "cpu_baseline": cpu,
         "e2e": e2e,
-        "gpu_launches": sum(launches_of(i) for i in range(len(calls))) * args.steps,
+        "gpu_launches": sum(launches_of(i) + (1 if per_conv_flush else 0)
+                            for i in range(len(calls))) * args.steps,
         "step_us_p10_p90": [round(_pct(step_ms, 10) * 1e3, 2), round(_pct(step_ms, 90) * 1e3, 2)],
         "clocks": clocks,
         "pack_us": round(pack_us, 2),
