@@ -1799,8 +1799,9 @@ conv_status_t prepare_fwd(const void* input, const FwdShape& shape, const void* 
     const unsigned long long tmo = g_timeout_ns.load(std::memory_order_relaxed);
     dp.timeout_cycles = ns_to_cycles(tmo ? tmo : kDefaultTimeoutNs);
     dp.fault_mode = g_fault_mode.load(std::memory_order_relaxed);
+    dp.dw_cols = dw_tile_cols(f.wo);
     if (direct_uses_dw_tiles(static_cast<int>(f.in_dtype), dp)) {
-      // Depthwise 3x3 tiles: {C, W, H, N} boxes of kDwRows + 2 rows x kDwCols + 2
+      // Depthwise 3x3 tiles: {C, W, H, N} boxes of kDwRows + 2 rows x dw_cols + 2
       // columns x 64 channels, zero outside the image.
       const DriverFns* fns = driver_fns();
       if (!fns) return CONV_ERR_CUDA;
@@ -1808,7 +1809,7 @@ conv_status_t prepare_fwd(const void* input, const FwdShape& shape, const void* 
       cuuint64_t dims[4] = {static_cast<cuuint64_t>(f.c_in), static_cast<cuuint64_t>(f.w),
                             static_cast<cuuint64_t>(f.h), static_cast<cuuint64_t>(f.n)};
       cuuint64_t strides[3] = {dims[0] * e, dims[0] * dims[1] * e, dims[0] * dims[1] * dims[2] * e};
-      cuuint32_t box[4] = {64, kDwCols + 2, kDwRows + 2, 1};
+      cuuint32_t box[4] = {64, static_cast<cuuint32_t>(dp.dw_cols + 2), kDwRows + 2, 1};
       cuuint32_t estr[4] = {1, 1, 1, 1};
       if (fns->tiled(&dp.map_x, tmap_dtype(f.in_dtype), 4, const_cast<void*>(input), dims, strides,
                      box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,

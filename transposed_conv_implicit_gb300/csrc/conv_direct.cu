@@ -197,59 +197,95 @@ __global__ void __launch_bounds__(kDirectThreads)
 
 long long dw_tile_count(const DirectParams& p) {
   return static_cast<long long>(p.N) * ((p.Ho + kDwRows - 1) / kDwRows) *
-         ((p.Wo + kDwCols - 1) / kDwCols) * ((p.F + kDirectChannels - 1) / kDirectChannels);
+         ((p.Wo + p.dw_cols - 1) / p.dw_cols) * ((p.F + kDirectChannels - 1) / kDirectChannels);
 }
 
 bool dw_tiles_apply(const DirectParams& p) {
   if (!(p.R == 3 && p.S == 3 && p.stride_h == 1 && p.stride_w == 1 && p.dil_h == 1 &&
         p.dil_w == 1 && p.c_group == 1 && p.f_group == 1 && p.C % kDirectVec == 0))
     return false;
+  if (p.dw_cols != 28 && p.dw_cols != 32) return false;
   return dw_tile_count(p) < (1ll << 31);
 }
 
 // 3x3 depthwise with multiplier 1, stride 1, dilation 1, 16-bit inputs, C a
-// multiple of 8.  A tile is kDwRows output rows x kDwCols output columns x 64
-// channels; its input (kDwRows + 2 rows x kDwCols + 2 columns x 64 channels,
-// zero outside the image) arrives in shared memory as one TMA box; the CTA
-// keeps the boxes of its next kDwBufs - 1 tiles in flight while it computes
-// this one.  Thread (slot, px) owns 4 channels of output column px, with their
-// nine filter taps in registers: it walks down the tile's input rows, reads
-// the three taps of each row from shared memory (converted to fp32 once) and
-// adds them into the three output rows that row touches (a rolling set of
-// fp32 accumulators); an output row is stored once its third input row is in.
+// multiple of 8.  A tile is kDwRows output rows x kCols output columns x 64
+// channels (kCols = 28 or 32, dw_tile_cols); its input (kDwRows + 2 rows x
+// kCols + 2 columns x 64 channels, zero outside the image) arrives in shared
+// memory as one TMA box; the CTA keeps the box of its next tile in flight
+// while it computes this one.  Thread (slot, pair, half)
+// owns 4 channels of output columns 2*pair and 2*pair + 1 in output rows
+// [8*half, 8*half + 8) of the tile, with the nine filter taps in registers as
+// two channel pairs: it walks down its ten input rows, converts the four
+// input columns of each row to fp32 once and adds them, two channels per
+// packed fp32 FMA, into the three output rows that row touches; an output row
+// is stored once its third input row is in.  Every output is the same fp32
+// chain of nine FMAs in filter order (r, s) as in the plain direct kernel.
 constexpr int kDwBoxRows = kDwRows + 2;
-constexpr int kDwBoxCols = kDwCols + 2;
-constexpr uint32_t kDwBoxBytes = kDwBoxRows * kDwBoxCols * kDirectChannels * 2;
+constexpr int kDwHalfRows = kDwRows / 2;  // output rows per thread
+constexpr int kDwVec = 4;                 // channels per thread
+constexpr int kDwPixBytes = kDirectChannels * 2;  // one box pixel: 64 16-bit channels
 
-constexpr int kDwThreads = 512;
-constexpr int kDwBufs = 2;  // input boxes in flight per CTA (one being read)
-constexpr int kDwVec = 4;  // channels per thread
+template <int kCols>
+constexpr uint32_t dw_box_bytes() {
+  return static_cast<uint32_t>(kDwBoxRows * (kCols + 2) * kDwPixBytes);
+}
+// Input boxes per CTA: one being read, one in flight.  (Three boxes of 28
+// columns fit as well, and ran the 32x112x112x64 conv 35.8 us against 34.4.)
+template <int kCols>
+constexpr int dw_bufs() {
+  return 2;
+}
 
-// Four 16-bit inputs (8 bytes) -> four floats.
+// Four 16-bit inputs (8 bytes) -> channels 0-1 and 2-3 as float pairs.
 template <typename InT>
-__device__ __forceinline__ void dw_unpack(uint2 raw, float (&f)[kDwVec]) {
-  const InT* v = reinterpret_cast<const InT*>(&raw);
-#pragma unroll
-  for (int j = 0; j < kDwVec; ++j) f[j] = load_f32<InT>(v + j);
+__device__ __forceinline__ void dw_unpack2(uint2 raw, float2& lo, float2& hi);
+template <>
+__device__ __forceinline__ void dw_unpack2<__nv_bfloat16>(uint2 raw, float2& lo, float2& hi) {
+  // A bfloat16 is the high half of the float with the same value.
+  lo = make_float2(__uint_as_float(raw.x << 16), __uint_as_float(raw.x & 0xFFFF0000u));
+  hi = make_float2(__uint_as_float(raw.y << 16), __uint_as_float(raw.y & 0xFFFF0000u));
+}
+template <>
+__device__ __forceinline__ void dw_unpack2<__half>(uint2 raw, float2& lo, float2& hi) {
+  lo = __half22float2(*reinterpret_cast<const __half2*>(&raw.x));
+  hi = __half22float2(*reinterpret_cast<const __half2*>(&raw.y));
+}
+
+// Four outputs (channel pairs lo, hi) at y: + beta * source (when src is
+// given), the activation, one round-to-nearest-even each, 8 bytes.
+template <int kAct>
+__device__ __forceinline__ float dw_act(float v) {
+  if (kAct == kEpiRelu) return fmaxf(v, 0.0f);
+  if (kAct == kEpiSilu) return v / (1.0f + __expf(-v));
+  return v;
 }
 
 template <typename OutT>
-__device__ __forceinline__ void dw_store(const DirectParams& p, const float (&acc)[kDwVec], int n,
-                                         int oy, int ox, int f0) {
-  if (ox >= p.Wo || f0 >= p.F) return;
-  const long long o = ((static_cast<long long>(n) * p.Ho + oy) * p.Wo + ox) * p.F + f0;
-  uint2 sraw = make_uint2(0u, 0u);
-  if (p.has_residual) sraw = __ldg(reinterpret_cast<const uint2*>(static_cast<const OutT*>(p.src) + o));
-  const OutT* sv = reinterpret_cast<const OutT*>(&sraw);
-  uint2 out;
-  OutT* ov = reinterpret_cast<OutT*>(&out);
+__device__ __forceinline__ uint32_t dw_pack2(float a, float b);
+template <>
+__device__ __forceinline__ uint32_t dw_pack2<__nv_bfloat16>(float a, float b) {
+  const __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
+  return *reinterpret_cast<const uint32_t*>(&v);
+}
+template <>
+__device__ __forceinline__ uint32_t dw_pack2<__half>(float a, float b) {
+  const __half2 v = __floats2half2_rn(a, b);
+  return *reinterpret_cast<const uint32_t*>(&v);
+}
+
+template <typename OutT, int kAct>
+__device__ __forceinline__ void dw_store2(float2 lo, float2 hi, OutT* y, const OutT* src,
+                                          float beta) {
+  float v[kDwVec] = {lo.x, lo.y, hi.x, hi.y};
+  if (src) {
+    const uint2 sraw = __ldg(reinterpret_cast<const uint2*>(src));
+    const OutT* sv = reinterpret_cast<const OutT*>(&sraw);
 #pragma unroll
-  for (int j = 0; j < kDwVec; ++j) {
-    float v = acc[j];
-    if (p.has_residual) v = fmaf(p.beta, load_f32<OutT>(sv + j), v);
-    ov[j] = store_rn<OutT>(direct_activation(v, p.epilogue));
+    for (int j = 0; j < kDwVec; ++j) v[j] = fmaf(beta, load_f32<OutT>(sv + j), v[j]);
   }
-  *reinterpret_cast<uint2*>(static_cast<OutT*>(p.y) + o) = out;
+  *reinterpret_cast<uint2*>(y) = make_uint2(dw_pack2<OutT>(dw_act<kAct>(v[0]), dw_act<kAct>(v[1])),
+                                            dw_pack2<OutT>(dw_act<kAct>(v[2]), dw_act<kAct>(v[3])));
 }
 
 struct DwTile {
@@ -257,7 +293,7 @@ struct DwTile {
 };
 
 __device__ __forceinline__ DwTile dw_decode(const DirectParams& p, int t) {
-  const int n_xseg = (p.Wo + kDwCols - 1) / kDwCols;
+  const int n_xseg = (p.Wo + p.dw_cols - 1) / p.dw_cols;
   const int n_yblk = (p.Ho + kDwRows - 1) / kDwRows;
   const int per_cb = p.N * n_yblk * n_xseg;
   DwTile d;
@@ -267,13 +303,18 @@ __device__ __forceinline__ DwTile dw_decode(const DirectParams& p, int t) {
   rest /= n_xseg;
   d.oy0 = (rest % n_yblk) * kDwRows;
   d.n = rest / n_yblk;
-  d.x0 = xs * kDwCols;
+  d.x0 = xs * p.dw_cols;
   return d;
 }
 
-template <typename InT, typename OutT>
-__global__ void __launch_bounds__(kDwThreads, 1)
+template <typename InT, typename OutT, int kCols, int kAct>
+__global__ void __launch_bounds__(16 * kCols, 1)
     conv_dw3x3_kernel(const __grid_constant__ DirectParams p, int tiles) {
+  constexpr uint32_t kBoxBytes = dw_box_bytes<kCols>();
+  constexpr int kDwBufs = dw_bufs<kCols>();
+  static_assert(kDwBufs >= 2, "two input boxes must fit");
+  constexpr int kPairs = kCols / 2;
+  constexpr int kRowBytes = (kCols + 2) * kDwPixBytes;
   extern __shared__ uint8_t dw_smem_raw[];
   // [kDwBufs buffers][box], from a 128-byte aligned base (TMA destinations)
   uint8_t* boxes = reinterpret_cast<uint8_t*>(
@@ -281,7 +322,8 @@ __global__ void __launch_bounds__(kDwThreads, 1)
   __shared__ __align__(8) uint64_t bar[kDwBufs];
   __shared__ int abort_flag;
   const int slot = threadIdx.x & 15;  // channels [4*slot, 4*slot+4) of the tile's 64
-  const int px = threadIdx.x >> 4;    // output column of the tile (0..31)
+  const int pair = (threadIdx.x >> 4) % kPairs;  // output columns 2*pair, 2*pair + 1
+  const int half = (threadIdx.x >> 4) / kPairs;  // output rows [8*half, 8*half + 8)
   const InT* __restrict__ w = static_cast<const InT*>(p.w);
   if (threadIdx.x == 0) {
     for (int b = 0; b < kDwBufs; ++b) mbar_init(smem_u32(&bar[b]), 1);
@@ -298,8 +340,8 @@ __global__ void __launch_bounds__(kDwThreads, 1)
     const uint32_t b = smem_u32(&bar[buf]);
     ++issued[buf];
     fence_proxy_async_shared();  // earlier generic reads of the buffer come first
-    mbar_arrive_expect_tx(b, kDwBoxBytes);
-    tma_load_4d(smem_u32(boxes + buf * kDwBoxBytes), &p.map_x, b, d.cb * kDirectChannels,
+    mbar_arrive_expect_tx(b, kBoxBytes);
+    tma_load_4d(smem_u32(boxes + buf * kBoxBytes), &p.map_x, b, d.cb * kDirectChannels,
                 d.x0 - p.pad_w, d.oy0 - p.pad_h, d.n);
   };
   // Tile i of this CTA (t = blockIdx.x + i * gridDim.x) uses buffer i % kDwBufs.
@@ -308,7 +350,7 @@ __global__ void __launch_bounds__(kDwThreads, 1)
       const long long tj = blockIdx.x + static_cast<long long>(j) * gridDim.x;
       if (tj < tiles) issue(static_cast<int>(tj), j);
     }
-  float wr[9][kDwVec];  // this thread's filter taps, in registers
+  float2 wl[9], wh[9];  // this thread's filter taps r*3 + s: channels 0-1 and 2-3
   int cb_loaded = -1;
   int i = 0;
   for (int t = blockIdx.x; t < tiles; t += gridDim.x, ++i) {
@@ -316,12 +358,18 @@ __global__ void __launch_bounds__(kDwThreads, 1)
     const DwTile d = dw_decode(p, t);
     const int f0 = d.cb * kDirectChannels + slot * kDwVec;
     if (d.cb != cb_loaded) {
+      float wv[9][kDwVec];
 #pragma unroll
       for (int tap = 0; tap < 9; ++tap)
 #pragma unroll
         for (int j = 0; j < kDwVec; ++j)
-          wr[tap][j] = f0 + j < p.F ? load_f32<InT>(w + packed_index(p, f0 + j, tap / 3, tap % 3, 0))
+          wv[tap][j] = f0 + j < p.F ? load_f32<InT>(w + packed_index(p, f0 + j, tap / 3, tap % 3, 0))
                                     : 0.0f;
+#pragma unroll
+      for (int tap = 0; tap < 9; ++tap) {
+        wl[tap] = make_float2(wv[tap][0], wv[tap][1]);
+        wh[tap] = make_float2(wv[tap][2], wv[tap][3]);
+      }
       cb_loaded = d.cb;
     }
     // Tile i + kDwBufs - 1 goes into the buffer read in the previous
@@ -335,33 +383,55 @@ __global__ void __launch_bounds__(kDwThreads, 1)
     }
     __syncthreads();  // the box is in (thread 0 saw its barrier complete)
     if (abort_flag) break;
-    const int ox = d.x0 + px;
-    const int rows = min(kDwRows, p.Ho - d.oy0);
-    const uint8_t* col = boxes + buf * kDwBoxBytes + (px * kDirectChannels + slot * kDwVec) * 2;
-    float a0[kDwVec], a1[kDwVec], a2[kDwVec];  // output rows k, k-1, k-2
+    const int oy_first = d.oy0 + kDwHalfRows * half;  // this thread's first output row
+    const int ox0 = d.x0 + 2 * pair;
+    const bool store_ok[2] = {ox0 < p.Wo && f0 < p.F, ox0 + 1 < p.Wo && f0 < p.F};
+    const long long o_row0 =
+        ((static_cast<long long>(d.n) * p.Ho + oy_first) * p.Wo + ox0) * p.F + f0;
+    const long long o_row_step = static_cast<long long>(p.Wo) * p.F;
+    // Box row kDwHalfRows*half + k, columns 2*pair .. 2*pair + 3, this thread's channels.
+    const uint8_t* src_rows =
+        boxes + buf * kBoxBytes + (kDwHalfRows * half) * kRowBytes + (2 * pair) * kDwPixBytes + slot * 8;
+    float2 acc[3][2][2];  // [output row % 3][column q][channel pair]
+    OutT* yrow = static_cast<OutT*>(p.y) + o_row0;  // this thread's output row o = 0
+    const OutT* srow = p.has_residual ? static_cast<const OutT*>(p.src) + o_row0 : nullptr;
 #pragma unroll
-    for (int j = 0; j < kDwVec; ++j) a0[j] = a1[j] = a2[j] = 0.0f;
-    for (int k = 0; k < rows + 2; ++k) {
-      const uint8_t* rowp = col + k * (kDwBoxCols * kDirectChannels * 2);
-      float in[3][kDwVec];  // taps s = 0, 1, 2 of this input row
-      dw_unpack<InT>(*reinterpret_cast<const uint2*>(rowp), in[0]);
-      dw_unpack<InT>(*reinterpret_cast<const uint2*>(rowp + kDirectChannels * 2), in[1]);
-      dw_unpack<InT>(*reinterpret_cast<const uint2*>(rowp + 2 * kDirectChannels * 2), in[2]);
-      // Filter row 0 feeds output row k, row 1 row k-1, row 2 row k-2.
+    for (int k = 0; k < kDwHalfRows + 2; ++k) {
+      float2 in[4][2];  // input columns 2*pair + c, channel pairs
 #pragma unroll
-      for (int s = 0; s < 3; ++s)
+      for (int c = 0; c < 4; ++c)
+        dw_unpack2<InT>(*reinterpret_cast<const uint2*>(src_rows + k * kRowBytes + c * kDwPixBytes),
+                        in[c][0], in[c][1]);
+      // Filter row r takes this input row into output row k - r (of this
+      // thread's 8); an output row starts at its r = 0 input row.
 #pragma unroll
-        for (int j = 0; j < kDwVec; ++j) {
-          a0[j] = fmaf(in[s][j], wr[s][j], a0[j]);
-          a1[j] = fmaf(in[s][j], wr[3 + s][j], a1[j]);
-          a2[j] = fmaf(in[s][j], wr[6 + s][j], a2[j]);
+      for (int r = 0; r < 3; ++r) {
+        const int o = k - r;
+        if (o < 0 || o >= kDwHalfRows) continue;
+        float2(&a)[2][2] = acc[o % 3];
+        if (r == 0) {
+#pragma unroll
+          for (int q = 0; q < 2; ++q) a[q][0] = a[q][1] = make_float2(0.0f, 0.0f);
         }
-      if (k >= 2) dw_store<OutT>(p, a2, d.n, d.oy0 + k - 2, ox, f0);
 #pragma unroll
-      for (int j = 0; j < kDwVec; ++j) {
-        a2[j] = a1[j];
-        a1[j] = a0[j];
-        a0[j] = 0.0f;
+        for (int s = 0; s < 3; ++s)
+#pragma unroll
+          for (int q = 0; q < 2; ++q) {
+            a[q][0] = __ffma2_rn(in[q + s][0], wl[r * 3 + s], a[q][0]);
+            a[q][1] = __ffma2_rn(in[q + s][1], wh[r * 3 + s], a[q][1]);
+          }
+      }
+      const int o = k - 2;  // complete after this input row
+      if (o >= 0) {
+        if (oy_first + o < p.Ho) {
+#pragma unroll
+          for (int q = 0; q < 2; ++q)
+            if (store_ok[q])
+              dw_store2<OutT, kAct>(acc[o % 3][q][0], acc[o % 3][q][1], yrow + q * p.F,
+                                    srow ? srow + q * p.F : nullptr, p.beta);
+        }
+        yrow += o_row_step;
+        if (srow) srow += o_row_step;
       }
     }
     __syncthreads();  // done with this buffer
@@ -375,18 +445,33 @@ __global__ void __launch_bounds__(kDwThreads, 1)
   }
 }
 
+template <typename InT, typename OutT, int kCols, int kAct>
+cudaError_t launch_dw_tiles_act(const DirectParams& p, int num_sms, cudaStream_t stream) {
+  const long long tiles = dw_tile_count(p);
+  const size_t smem = 128 + dw_bufs<kCols>() * dw_box_bytes<kCols>();
+  cudaError_t err = cudaFuncSetAttribute(conv_dw3x3_kernel<InT, OutT, kCols, kAct>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(smem));
+  if (err != cudaSuccess) return err;
+  const unsigned grid = static_cast<unsigned>(std::min<long long>(tiles, num_sms));
+  conv_dw3x3_kernel<InT, OutT, kCols, kAct>
+      <<<grid, 16 * kCols, smem, stream>>>(p, static_cast<int>(tiles));
+  return cudaGetLastError();
+}
+
+template <typename InT, typename OutT, int kCols>
+cudaError_t launch_dw_tiles(const DirectParams& p, int num_sms, cudaStream_t stream) {
+  if (p.epilogue == kEpiRelu) return launch_dw_tiles_act<InT, OutT, kCols, kEpiRelu>(p, num_sms, stream);
+  if (p.epilogue == kEpiSilu) return launch_dw_tiles_act<InT, OutT, kCols, kEpiSilu>(p, num_sms, stream);
+  return launch_dw_tiles_act<InT, OutT, kCols, kEpiNone>(p, num_sms, stream);
+}
+
 template <typename InT, typename OutT>
 cudaError_t launch_direct(const DirectParams& p, int num_sms, cudaStream_t stream) {
-  if (sizeof(InT) == 2 && dw_tiles_apply(p)) {
-    const long long tiles = dw_tile_count(p);
-    const size_t smem = 128 + kDwBufs * kDwBoxBytes;
-    cudaError_t err = cudaFuncSetAttribute(conv_dw3x3_kernel<InT, OutT>,
-                                           cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                           static_cast<int>(smem));
-    if (err != cudaSuccess) return err;
-    const unsigned grid = static_cast<unsigned>(std::min<long long>(tiles, num_sms));
-    conv_dw3x3_kernel<InT, OutT><<<grid, kDwThreads, smem, stream>>>(p, static_cast<int>(tiles));
-    return cudaGetLastError();
+  if constexpr (sizeof(InT) == 2) {
+    if (dw_tiles_apply(p))
+      return p.dw_cols == 28 ? launch_dw_tiles<InT, OutT, 28>(p, num_sms, stream)
+                             : launch_dw_tiles<InT, OutT, 32>(p, num_sms, stream);
   }
   const size_t smem = static_cast<size_t>(p.R) * p.S * p.c_group * kDirectChannels * sizeof(float);
   cudaError_t err = cudaFuncSetAttribute(conv_direct_kernel<InT, OutT>,
@@ -405,6 +490,12 @@ cudaError_t launch_direct(const DirectParams& p, int num_sms, cudaStream_t strea
 }
 
 }  // namespace
+
+int dw_tile_cols(int wo) {
+  const int waste28 = (wo + 27) / 28 * 28 - wo;
+  const int waste32 = (wo + 31) / 32 * 32 - wo;
+  return waste28 < waste32 ? 28 : 32;
+}
 
 bool direct_uses_dw_tiles(int in_dtype, const DirectParams& p) {
   return in_dtype != 2 && dw_tiles_apply(p);

@@ -16,8 +16,8 @@ cudaError_t launch_conv_igemm(int kind, bool out_bf16, const ConvKernelParams& p
 // k = (r*S + s)*c_group + c, or, when w_runs is set, the gather layout
 // [F][r][run_elems] with run index s*c_group + c.
 struct DirectParams {
-  // 3x3 depthwise tiles: tiled {C, W, H, N} over the input, box {64, 34, 10, 1}
-  // (encoded only for that kernel).
+  // 3x3 depthwise tiles: tiled {C, W, H, N} over the input, box {64, dw_cols +
+  // 2, kDwRows + 2, 1} (encoded only for that kernel).
   CUtensorMap map_x;
   unsigned int* status;     // workspace status word (bounded waits)
   long long timeout_cycles;
@@ -33,6 +33,7 @@ struct DirectParams {
   int has_residual, epilogue;
   float beta;
   FastDiv div_wo, div_ho;  // pixel index -> (n, oy, ox)
+  int dw_cols;             // output columns per depthwise tile (dw_tile_cols)
 };
 
 size_t direct_smem_bytes(int r, int s, int c_group);
@@ -41,7 +42,9 @@ size_t direct_smem_bytes(int r, int s, int c_group);
 // then be encoded): 16-bit inputs, multiplier 1, stride 1, dilation 1, C % 8 == 0.
 bool direct_uses_dw_tiles(int in_dtype, const DirectParams& p);
 constexpr int kDwRows = 16;   // output rows per depthwise tile
-constexpr int kDwCols = 32;   // output columns per depthwise tile
+// Output columns per depthwise tile: 28 or 32, whichever leaves fewer unused
+// columns in the last tile of a row (32 on a tie).
+int dw_tile_cols(int wo);
 
 // in_dtype: 0 bf16, 1 f16, 2 e4m3 (bf16 out).
 cudaError_t launch_conv_direct(int in_dtype, bool out_bf16, const DirectParams& p, int num_sms,
