@@ -212,8 +212,9 @@ bool dw_tiles_apply(const DirectParams& p) {
 // multiple of 8.  A tile is kDwRows output rows x kCols output columns x 64
 // channels (kCols = 28 or 32, dw_tile_cols); its input (kDwRows + 2 rows x
 // kCols + 2 columns x 64 channels, zero outside the image) arrives in shared
-// memory as one TMA box; the CTA keeps the box of its next tile in flight
-// while it computes this one.  Thread (slot, pair, half)
+// memory as one TMA box, loaded by the CTA's last warp into a ring of two
+// buffers (full and empty barriers per buffer: a compute warp waits for the
+// box and releases it when done, so the warps run free of each other).  Thread (slot, pair, half)
 // owns 4 channels of output columns 2*pair and 2*pair + 1 in output rows
 // [8*half, 8*half + 8) of the tile, with the nine filter taps in registers as
 // two channel pairs: it walks down its ten input rows, converts the four
@@ -308,48 +309,68 @@ __device__ __forceinline__ DwTile dw_decode(const DirectParams& p, int t) {
 }
 
 template <typename InT, typename OutT, int kCols, int kAct>
-__global__ void __launch_bounds__(16 * kCols, 1)
+__global__ void __launch_bounds__(16 * kCols + 32, 1)
     conv_dw3x3_kernel(const __grid_constant__ DirectParams p, int tiles) {
   constexpr uint32_t kBoxBytes = dw_box_bytes<kCols>();
   constexpr int kDwBufs = dw_bufs<kCols>();
   static_assert(kDwBufs >= 2, "two input boxes must fit");
   constexpr int kPairs = kCols / 2;
   constexpr int kRowBytes = (kCols + 2) * kDwPixBytes;
+  constexpr int kComputeWarps = 16 * kCols / 32;  // the last warp loads the boxes
   extern __shared__ uint8_t dw_smem_raw[];
   // [kDwBufs buffers][box], from a 128-byte aligned base (TMA destinations)
   uint8_t* boxes = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(dw_smem_raw) + 127) & ~static_cast<uintptr_t>(127));
-  __shared__ __align__(8) uint64_t bar[kDwBufs];
+  __shared__ __align__(8) uint64_t full[kDwBufs];   // box landed
+  __shared__ __align__(8) uint64_t empty[kDwBufs];  // every compute warp is done with it
   __shared__ int abort_flag;
-  const int slot = threadIdx.x & 15;  // channels [4*slot, 4*slot+4) of the tile's 64
-  const int pair = (threadIdx.x >> 4) % kPairs;  // output columns 2*pair, 2*pair + 1
-  const int half = (threadIdx.x >> 4) / kPairs;  // output rows [8*half, 8*half + 8)
-  const InT* __restrict__ w = static_cast<const InT*>(p.w);
+  const int warp = static_cast<int>(threadIdx.x >> 5);
+  const int lane = static_cast<int>(threadIdx.x & 31);
   if (threadIdx.x == 0) {
-    for (int b = 0; b < kDwBufs; ++b) mbar_init(smem_u32(&bar[b]), 1);
+    for (int b = 0; b < kDwBufs; ++b) {
+      mbar_init(smem_u32(&full[b]), 1);
+      mbar_init(smem_u32(&empty[b]), kComputeWarps);
+    }
     abort_flag = 0;
     fence_barrier_init();
     tma_prefetch_desc(&p.map_x);
   }
   __syncthreads();
-  int issued[kDwBufs] = {};  // boxes issued per buffer (thread 0)
-  auto issue = [&](int t, int buf) {  // thread 0: the input box of tile t
-    // (fault_mode 1, a test hook: CTA 0 never loads its first tile.)
-    if (p.fault_mode == 1 && blockIdx.x == 0 && t == static_cast<int>(blockIdx.x)) return;
-    const DwTile d = dw_decode(p, t);
-    const uint32_t b = smem_u32(&bar[buf]);
-    ++issued[buf];
-    fence_proxy_async_shared();  // earlier generic reads of the buffer come first
-    mbar_arrive_expect_tx(b, kBoxBytes);
-    tma_load_4d(smem_u32(boxes + buf * kBoxBytes), &p.map_x, b, d.cb * kDirectChannels,
-                d.x0 - p.pad_w, d.oy0 - p.pad_h, d.n);
-  };
-  // Tile i of this CTA (t = blockIdx.x + i * gridDim.x) uses buffer i % kDwBufs.
-  if (threadIdx.x == 0)
-    for (int j = 0; j < kDwBufs - 1; ++j) {
-      const long long tj = blockIdx.x + static_cast<long long>(j) * gridDim.x;
-      if (tj < tiles) issue(static_cast<int>(tj), j);
+  if (warp == kComputeWarps) {
+    // Loader: tile i of this CTA (t = blockIdx.x + i * gridDim.x) goes into
+    // buffer i % kDwBufs once the compute warps have released its previous tile.
+    if (lane == 0) {
+      int issued[kDwBufs] = {};
+      int i = 0;
+      for (int t = blockIdx.x; t < tiles; t += gridDim.x, ++i) {
+        const int buf = i % kDwBufs;
+        if (i >= kDwBufs &&
+            !mbar_wait_bounded(smem_u32(&empty[buf]), static_cast<uint32_t>((i / kDwBufs - 1) & 1),
+                               &abort_flag, p.status, kStatusProducerTimeout, p.timeout_cycles))
+          break;
+        // (fault_mode 1, a test hook: CTA 0 never loads its first tile.)
+        if (p.fault_mode == 1 && blockIdx.x == 0 && i == 0) continue;
+        const DwTile d = dw_decode(p, t);
+        const uint32_t b = smem_u32(&full[buf]);
+        ++issued[buf];
+        fence_proxy_async_shared();  // the compute warps' reads of the buffer come first
+        mbar_arrive_expect_tx(b, kBoxBytes);
+        tma_load_4d(smem_u32(boxes + buf * kBoxBytes), &p.map_x, b, d.cb * kDirectChannels,
+                    d.x0 - p.pad_w, d.oy0 - p.pad_h, d.n);
+      }
+      // After an abort, the boxes still in flight land before the CTA exits.
+      if (abort_flag)
+        for (int b = 0; b < kDwBufs; ++b)
+          if (issued[b] > 0)
+            mbar_wait_drain(smem_u32(&full[b]), static_cast<uint32_t>((issued[b] - 1) & 1),
+                            p.timeout_cycles / 8 + 1);
     }
+    return;
+  }
+  const int slot = threadIdx.x & 15;  // channels [4*slot, 4*slot+4) of the tile's 64
+  const int pair = (threadIdx.x >> 4) % kPairs;  // output columns 2*pair, 2*pair + 1
+  const int half = (threadIdx.x >> 4) / kPairs;  // output rows [8*half, 8*half + 8)
+  const InT* __restrict__ w = static_cast<const InT*>(p.w);
   float2 wl[9], wh[9];  // this thread's filter taps r*3 + s: channels 0-1 and 2-3
   int cb_loaded = -1;
   int i = 0;
@@ -372,17 +393,11 @@ __global__ void __launch_bounds__(16 * kCols, 1)
       }
       cb_loaded = d.cb;
     }
-    // Tile i + kDwBufs - 1 goes into the buffer read in the previous
-    // iteration, which every thread has finished (the __syncthreads at its end).
-    const long long tn = t + static_cast<long long>(kDwBufs - 1) * gridDim.x;
-    if (threadIdx.x == 0 && tn < tiles) issue(static_cast<int>(tn), (i + kDwBufs - 1) % kDwBufs);
-    if (threadIdx.x == 0) {
-      if (!mbar_wait_bounded(smem_u32(&bar[buf]), static_cast<uint32_t>((i / kDwBufs) & 1), &abort_flag,
-                             p.status, kStatusProducerTimeout, p.timeout_cycles))
-        abort_flag = 1;
-    }
-    __syncthreads();  // the box is in (thread 0 saw its barrier complete)
-    if (abort_flag) break;
+    if (!__all_sync(0xFFFFFFFFu, mbar_wait_bounded(smem_u32(&full[buf]),
+                                                   static_cast<uint32_t>((i / kDwBufs) & 1),
+                                                   &abort_flag, p.status, kStatusProducerTimeout,
+                                                   p.timeout_cycles)))
+      break;
     const int oy_first = d.oy0 + kDwHalfRows * half;  // this thread's first output row
     const int ox0 = d.x0 + 2 * pair;
     const bool store_ok[2] = {ox0 < p.Wo && f0 < p.F, ox0 + 1 < p.Wo && f0 < p.F};
@@ -434,14 +449,8 @@ __global__ void __launch_bounds__(16 * kCols, 1)
         if (srow) srow += o_row_step;
       }
     }
-    __syncthreads();  // done with this buffer
-  }
-  // A box still in flight (after an abort) lands before the CTA exits.
-  if (threadIdx.x == 0 && abort_flag) {
-    for (int b = 0; b < kDwBufs; ++b)
-      if (issued[b] > 0)
-        mbar_wait_drain(smem_u32(&bar[b]), static_cast<uint32_t>((issued[b] - 1) & 1),
-                        p.timeout_cycles / 8 + 1);
+    __syncwarp();  // every lane of this warp is done with the buffer
+    if (lane == 0) mbar_arrive(smem_u32(&empty[buf]));
   }
 }
 
@@ -455,7 +464,7 @@ cudaError_t launch_dw_tiles_act(const DirectParams& p, int num_sms, cudaStream_t
   if (err != cudaSuccess) return err;
   const unsigned grid = static_cast<unsigned>(std::min<long long>(tiles, num_sms));
   conv_dw3x3_kernel<InT, OutT, kCols, kAct>
-      <<<grid, 16 * kCols, smem, stream>>>(p, static_cast<int>(tiles));
+      <<<grid, 16 * kCols + 32, smem, stream>>>(p, static_cast<int>(tiles));
   return cudaGetLastError();
 }
 
