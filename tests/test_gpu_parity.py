@@ -132,14 +132,19 @@ SMALL_FWD = [
     _fwd("b_depthwise_7x7_dil2", "bf16", 1, 20, 20, 32, 32, 7, 1, 6, groups=32, dil=2),
     _fwd("b_groups2_cg40_flat", "bf16", 1, 9, 9, 80, 48, 3, 1, 1, groups=2),
     _fwd("b_depthwise_c3", "bf16", 2, 9, 9, 3, 3, 3, 1, 1, groups=3),
-    # 3x3 depthwise, stride 1, on the column-walking kernel: ragged 32-column
-    # segments and 8-row bands, several channel blocks (one partial), padding
-    # 0/1/2, residual, both 16-bit types.
+    # 3x3 depthwise, stride 1, on the tile kernel: ragged 28-column tiles and
+    # 8-row halves, several channel blocks (one partial), padding 0/1/2,
+    # residual, both 16-bit types.
     _fwd("b_dw3x3_w70_res", "bf16", 3, 19, 70, 64, 64, 3, 1, 1, groups=64, res=True, beta=0.5,
          epi="relu"),
     _fwd("h_dw3x3_c72_p0", "f16", 1, 13, 35, 72, 72, 3, 1, 0, groups=72, layout="FCRS"),
     _fwd("b_dw3x3_c200_p2_silu", "bf16", 2, 6, 33, 200, 200, 3, 1, 2, groups=200, epi="silu"),
     _fwd("b_dw3x3_tall_narrow", "bf16", 1, 41, 3, 16, 16, 3, 1, 1, groups=16),
+    # Widths whose tiles are 32 columns (64 and 96: no column left over)
+    # rather than 28 (every case above).
+    _fwd("b_dw3x3_w64_res", "bf16", 2, 18, 64, 64, 64, 3, 1, 1, groups=64, res=True, beta=0.5,
+         epi="relu"),
+    _fwd("h_dw3x3_w96_c136_silu", "f16", 1, 9, 96, 136, 136, 3, 1, 1, groups=136, epi="silu"),
     # Row-tap kernel (few output channels, stride 1): two or more 126-pixel
     # segments with a ragged last one, short last bands, g16 = 16 and 32,
     # R = 1, 3 and 5, S = 1 and 3, padding 0..2, several channel blocks.
@@ -242,6 +247,7 @@ INT_CASES = [
     _int_case("int_h_depthwise", "fwd", "f16", 2, 9, 9, 32, 32, 3, 1, 1, groups=32),
     _int_case("int_b_rowtap", "fwd", "bf16", 1, 12, 140, 64, 3, 3, 1, 1),
     _int_case("int_b_dw3x3_w40", "fwd", "bf16", 2, 17, 40, 128, 128, 3, 1, 1, groups=128),
+    _int_case("int_h_dw3x3_w64", "fwd", "f16", 1, 20, 64, 64, 64, 3, 1, 1, groups=64),
     _int_case("int_e_rowtap_g32", "fwd", "f8e4m3", 1, 9, 30, 128, 9, 3, 1, 1),
 ]
 
