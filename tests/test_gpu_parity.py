@@ -415,6 +415,24 @@ def test_full_size_workload_sampled(name):
     H.assert_parity(case, inp, flat[pts], ref, "sampled")
 
 
+def test_window_one_half_tiles_several_per_cta():
+    """The ResNet-50 bottleneck expansion (1x1, 64 -> 256 channels, + residual,
+    ReLU) on 56x56 images: row-window tiles of one 128-row half (C_out > 128),
+    more tiles than CTAs, so each CTA's epilogue walks several tiles; sampled
+    outputs against the oracle."""
+    case = _fwd("b_1x1_expand_res", "bf16", 8, 56, 56, 64, 256, 1, 1, 0, res=True, beta=1.0,
+                epi="relu", seed=21)
+    plan = plan_of(case, streamk_workspace().numel())
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    assert plan[11] == 1 and plan[0] == 256 and plan[4] > sms  # row window, N = 256, > 1 wave
+    inp = synthetic.make_inputs(case)
+    out = H.run_gpu(case, inp, workspace=streamk_workspace()).cpu()
+    flat = H.decode(out, case.out_dtype).reshape(-1)
+    assert np.isfinite(flat).all()
+    pts = H.sample_points(case, 3000, seed=12)
+    H.assert_parity(case, inp, flat[pts], H.oracle_points(case, inp, pts), "sampled")
+
+
 def test_tiny_workload_every_element():
     case = WORKLOADS["tiny_bf16"]
     inp = synthetic.make_inputs(case)
