@@ -12,6 +12,7 @@
 // the input rows they share stay in L1.  The kernel is memory-bound: every
 // input element is read from HBM about once and every output written once.
 #include <algorithm>
+#include <atomic>
 
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -454,13 +455,27 @@ __global__ void __launch_bounds__(16 * kCols + 32, 1)
   }
 }
 
+// The dynamic shared-memory limit is a per-device function attribute: raise
+// it once per device (slots in `configured`) to the largest size requested.
+template <typename Kernel>
+cudaError_t raise_smem_limit(Kernel kernel, std::atomic<size_t> (&configured)[64], size_t smem) {
+  int dev = 0;
+  cudaError_t err = cudaGetDevice(&dev);
+  if (err != cudaSuccess) return err;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  if (configured[dev].load(std::memory_order_relaxed) >= smem) return cudaSuccess;
+  err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(smem));
+  if (err == cudaSuccess) configured[dev].store(smem, std::memory_order_relaxed);
+  return err;
+}
+
 template <typename InT, typename OutT, int kCols, int kAct>
 cudaError_t launch_dw_tiles_act(const DirectParams& p, int num_sms, cudaStream_t stream) {
+  static std::atomic<size_t> configured[64];
   const long long tiles = dw_tile_count(p);
   const size_t smem = 128 + dw_bufs<kCols>() * dw_box_bytes<kCols>();
-  cudaError_t err = cudaFuncSetAttribute(conv_dw3x3_kernel<InT, OutT, kCols, kAct>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(smem));
+  cudaError_t err = raise_smem_limit(conv_dw3x3_kernel<InT, OutT, kCols, kAct>, configured, smem);
   if (err != cudaSuccess) return err;
   const unsigned grid = static_cast<unsigned>(std::min<long long>(tiles, num_sms));
   conv_dw3x3_kernel<InT, OutT, kCols, kAct>
@@ -482,10 +497,9 @@ cudaError_t launch_direct(const DirectParams& p, int num_sms, cudaStream_t strea
       return p.dw_cols == 28 ? launch_dw_tiles<InT, OutT, 28>(p, num_sms, stream)
                              : launch_dw_tiles<InT, OutT, 32>(p, num_sms, stream);
   }
+  static std::atomic<size_t> configured[64];
   const size_t smem = static_cast<size_t>(p.R) * p.S * p.c_group * kDirectChannels * sizeof(float);
-  cudaError_t err = cudaFuncSetAttribute(conv_direct_kernel<InT, OutT>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(smem));
+  cudaError_t err = raise_smem_limit(conv_direct_kernel<InT, OutT>, configured, smem);
   if (err != cudaSuccess) return err;
   const long long pixels = static_cast<long long>(p.N) * p.Ho * p.Wo;
   const int pix_per_cta = kDirectThreads / (kDirectChannels / kDirectVec);
