@@ -19,11 +19,12 @@ all its tensors (input, packed filter, source, output) that together exceed
 3 x L2, so that every launch reads its operands from HBM (inputs larger than
 L2 in place of a flush); the stream is bracketed by CUDA events on the launch
 stream and the per-launch time is its event time over the launches.  The
-tiny conv, too small for that, is timed alone after an L2 flush (a write of
-max(2 x L2, 256 MiB)) outside its events.  Each conv's events follow one
-untimed launch of the same conv (of its stream's last copy; for the tiny
-conv, before the flush), so its code is warm while its operands come from
-HBM.  The step time is the sum of the convs' per-launch times; ``per_kernel``
+tiny conv, too small for that within 64 copies, streams over 64 copies right
+after an L2 flush (a write of max(2 x L2, 256 MiB), outside its events): no
+launch's operands have been touched since the flush.  Each conv's events
+follow one untimed launch of the same conv (of its stream's last copy,
+before the flush for the tiny conv), so its code is warm while its operands
+come from HBM.  The step time is the sum of the convs' per-launch times; ``per_kernel``
 also reports each conv alone after a flush, right after a different conv
 (``us_isolated``: that includes the launch latency a stream hides and the
 kernel's code fetched cold).
@@ -414,17 +415,17 @@ def run_ours(args, world, rank, local):
     # rotating copies of all its tensors (input, packed filter, source,
     # output) that together exceed 3 x L2, so every launch reads its operands
     # from HBM; the per-launch time is the stream's event time over the
-    # launches.  A conv too small for that within 64 copies is timed alone
-    # after an L2 flush instead.
-    rotate_sets = []
+    # launches.  A conv too small for that within 64 copies streams over 64
+    # copies right after an L2 flush: each launch still reads operands that
+    # nothing has touched since the flush.
+    rotate_sets, flush_first = [], []
     if per_conv_flush:
         for i, case in enumerate(cases):
             x, w, src = dev_inputs[i]
             per_copy = case.bytes
             ncopy = max(1, math.ceil(3 * l2 / per_copy))
-            if ncopy > 64:
-                rotate_sets.append(None)
-                continue
+            flush_first.append(ncopy > 64)
+            ncopy = min(ncopy, 64)
             group = [calls[i]]
             for _ in range(ncopy - 1):
                 o = torch.empty_like(outs[i])
@@ -450,18 +451,13 @@ def run_ours(args, world, rank, local):
             # the tiny conv); its operands still come from HBM.
             for i, (e0, e1) in enumerate(evs):
                 group = rotate_sets[i]
-                if group is None:
-                    calls[i]()
+                group[-1]()
+                if flush_first[i]:
                     flush.fill_(1)
-                    e0.record(stream)
-                    calls[i]()
-                    e1.record(stream)
-                else:
-                    group[-1]()
-                    e0.record(stream)
-                    for call in group:
-                        call()
-                    e1.record(stream)
+                e0.record(stream)
+                for call in group:
+                    call()
+                e1.record(stream)
         else:
             flush.fill_(1)
             evs[0][0].record(stream)
@@ -470,9 +466,7 @@ def run_ours(args, world, rank, local):
             evs[0][1].record(stream)
 
     def launches_of(i):
-        if per_conv_flush and rotate_sets[i] is not None:
-            return len(rotate_sets[i])
-        return 1
+        return len(rotate_sets[i]) if per_conv_flush else 1
 
     warm_ev = new_events()
     for _ in range(args.warmup):
@@ -587,9 +581,8 @@ def run_ours(args, world, rank, local):
         if per_conv_flush:
             n = launches_of(i)
             per_kernel[c.name]["timing"] = (
-                "stream of %d back-to-back launches over rotating copies (%d MB in all)"
-                % (n, n * c.bytes >> 20) if rotate_sets[i] is not None
-                else "one launch between events after an L2 flush")
+                "stream of %d back-to-back launches over rotating copies (%d MB in all%s)"
+                % (n, n * c.bytes >> 20, ", after an L2 flush" if flush_first[i] else ""))
             per_kernel[c.name]["us_isolated"] = round(isolated_ms[i] * 1e3, 3)
     dcase = cases[dom]
     dbound, dpeak = conv_bound(dcase, peaks)
@@ -625,7 +618,8 @@ def run_ours(args, world, rank, local):
         "config": {"workload": args.workload + ": " + describe(cases),
                    "l2": ("inputs larger than L2: each conv streams over rotating copies of "
                           "its tensors totalling >= 3 x L2 (%d MiB); a conv too small for that "
-                          "runs after a flush (write of %d MiB) outside its events; each "
+                          "within 64 copies streams over 64 copies after a flush (write of %d "
+                          "MiB) outside its events; each "
                           "conv's events follow one untimed launch of the same conv (its code "
                           "warm, its operands not)"
                           % (3 * l2 >> 20, flush.numel() >> 20)) if per_conv_flush else
