@@ -1506,28 +1506,41 @@ bool plan_rowtap(const FwdShape& f, int groups, int num_sms, RowTapPlan* out) {
   if (sf > 32) return false;
   const int g16 = sf <= 16 ? 16 : 32;
   if (f.r * g16 > 256) return false;
-  // Columns per accumulator buffer: g16 * (band + 2R - 2) <= 256 (two buffers).
-  const int band_max = std::min(kRowTapMaxBand, 256 / g16 - 2 * f.r + 2);
-  if (band_max < 1) return false;
+  // Columns per accumulator buffer: g16 * (band + 2R - 2).  Two buffers
+  // (<= 256 columns each) let a CTA's next tile start while its epilogue
+  // drains; when every CTA has one tile, one buffer of up to 512 columns
+  // allows taller bands.
+  const int band_max2 = std::min(kRowTapMaxBand, 256 / g16 - 2 * f.r + 2);
+  const int band_max1 = std::min(kRowTapMaxBand, 512 / g16 - 2 * f.r + 2);
+  if (band_max1 < 1) return false;
   const int seg_w = 128 - (f.s - 1);
   const int n_seg = (f.wo + seg_w - 1) / seg_w;
+  auto tiles_of = [&](int b) {
+    return static_cast<long long>(f.n) * ((f.ho + b - 1) / b) * n_seg;
+  };
+  auto fits = [&](int b) { return b <= band_max2 || tiles_of(b) <= num_sms; };
   // Band height: the fewest input-row loads on the busiest SM (each tile
   // loads band + R - 1 rows); ties go to the taller band.
-  int best = 1;
+  int best = 0;
   long long best_cost = -1;
-  for (int b = 1; b <= band_max; ++b) {
-    const long long tiles = static_cast<long long>(f.n) * ((f.ho + b - 1) / b) * n_seg;
-    const long long waves = (tiles + num_sms - 1) / num_sms;
+  for (int b = 1; b <= band_max1; ++b) {
+    if (!fits(b)) continue;
+    const long long waves = (tiles_of(b) + num_sms - 1) / num_sms;
     const long long cost = waves * (b + f.r - 1);
     if (best_cost < 0 || cost <= best_cost) {
       best_cost = cost;
       best = b;
     }
   }
+  if (best == 0) return false;
   const int band_env = tuning().rowtap_band;  // tuning override: output rows per tile
-  if (band_env > 0) best = std::min(band_env, band_max);
+  if (band_env > 0) {
+    best = std::min(band_env, band_max1);
+    while (best > 1 && !fits(best)) --best;
+  }
   const int n_band = (f.ho + best - 1) / best;
   const long long tiles = static_cast<long long>(f.n) * n_band * n_seg;
+  const bool one_buffer = best > band_max2;  // (then every CTA has one tile)
   if (tiles >= (1ll << 31)) return false;
   std::memset(out, 0, sizeof(*out));
   RowTapParams& rp = out->rp;
@@ -1545,7 +1558,7 @@ bool plan_rowtap(const FwdShape& f, int groups, int num_sms, RowTapPlan* out) {
   rp.idesc_one = make_idesc(f.in_dtype, g16);
   rp.idesc_rest = make_idesc(f.in_dtype, std::max(f.r - 1, 1) * g16);
   rp.cols_per_buf = static_cast<uint32_t>(g16 * (best + 2 * f.r - 2));
-  rp.tmem_cols = next_pow2_cols(static_cast<int>(2 * rp.cols_per_buf));
+  rp.tmem_cols = next_pow2_cols(static_cast<int>((one_buffer ? 1 : 2) * rp.cols_per_buf));
   // Shared memory: the A ring at 0, the resident filter, the epilogue's
   // exchange buffers (two groups x two rows), the barriers.  An A stage holds
   // every channel block of one input row segment when four such stages fit

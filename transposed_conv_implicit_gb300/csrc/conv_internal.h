@@ -56,7 +56,7 @@ cudaError_t launch_conv_direct(int in_dtype, bool out_bf16, const DirectParams& 
 // filter rows of all R taps and its products accumulate, in tensor memory,
 // into the R output rows it touches; the epilogue sums the S taps across
 // neighbouring pixels.  Stride 1, dilation 1, one channel group.
-constexpr int kRowTapMaxBand = 16;  // output rows per tile (upper bound)
+constexpr int kRowTapMaxBand = 24;  // output rows per tile (upper bound)
 
 struct RowTapParams {  // aligned like CUtensorMap
   CUtensorMap map_x;   // tiled {C_in, W, H, N}, box {bk, 128, 1, 1}, 128-B swizzle
