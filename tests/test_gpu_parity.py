@@ -433,6 +433,23 @@ def test_window_one_half_tiles_several_per_cta():
     H.assert_parity(case, inp, flat[pts], H.oracle_points(case, inp, pts), "sampled")
 
 
+def test_rgb_head_two_accumulator_buffers(tuning):
+    """The full-size RGB head with 9-row bands: 285 tiles, so CTAs walk two
+    tiles on two TMEM accumulator buffers (the default, 18-row bands in one
+    wave, keeps one); sampled outputs against the oracle."""
+    tuning("CONV_ROWTAP_BAND", "9")
+    case = WORKLOADS["vae_head_bf16"]
+    plan = plan_of(case, streamk_workspace().numel())
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    assert plan[11] == 3 and plan[10] == 9 and plan[4] > sms
+    inp = synthetic.make_inputs(case)
+    out = H.run_gpu(case, inp, workspace=streamk_workspace()).cpu()
+    flat = H.decode(out, case.out_dtype).reshape(-1)
+    assert np.isfinite(flat).all()
+    pts = H.sample_points(case, 3000, seed=13)
+    H.assert_parity(case, inp, flat[pts], H.oracle_points(case, inp, pts), "sampled")
+
+
 def test_tiny_workload_every_element():
     case = WORKLOADS["tiny_bf16"]
     inp = synthetic.make_inputs(case)
